@@ -1,0 +1,105 @@
+"""A second, deliberately different CPU reference used only to pin the oracle.
+
+It shares nothing with ``oracle/``:
+
+* monomials come from ``itertools.combinations_with_replacement`` with a
+  1/m! coefficient computed from the multiset's size;
+* per-token gradients come from torch autograd on the scalar loss
+  ||M_W(x_i) - v_i||^2 (no hand-written chain rule);
+* Newton-Schulz is evaluated through its closed form: for X/(||X||_F + eps) =
+  U diag(s) V^T, k quintic steps give U diag(f^k(s)) V^T with
+  f(s) = a s + b s^3 + c s^5 (every step maps singular values through f and
+  keeps the singular vectors);
+* everything is a plain per-token loop over python lists.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+import torch
+
+QUINTIC = (3.4445, -4.7750, 2.0315)
+EPS = 1e-7
+
+
+def monomials(x, p):
+    x = [float(t) for t in x]
+    if p == 1:
+        return np.array(x)
+    out = []
+    for m in range(p + 1):
+        for combo in itertools.combinations_with_replacement(range(len(x)), m):
+            val = 1.0 / math.factorial(m)
+            for i in combo:
+                val *= x[i]
+            out.append(val)
+    return np.array(out)
+
+
+def ns_closed_form(G, k):
+    G = np.asarray(G, np.float64)
+    X = G / (np.linalg.norm(G) + EPS)
+    U, s, Vt = np.linalg.svd(X, full_matrices=False)
+    a, b, c = QUINTIC
+    for _ in range(k):
+        s = a * s + b * s ** 3 + c * s ** 5
+    return (U * s) @ Vt
+
+
+def _mem(Wt, x, depth):
+    if depth == 1:
+        return x @ Wt[0]
+    z = x @ Wt[0]
+    return x + torch.nn.functional.silu(z) @ Wt[1]
+
+
+def autograd_grad(W, x, v, depth):
+    Wt = [torch.tensor(m, dtype=torch.float64, requires_grad=True) for m in W]
+    xt = torch.tensor(x, dtype=torch.float64)
+    vt = torch.tensor(v, dtype=torch.float64)
+    loss = ((_mem(Wt, xt, depth) - vt) ** 2).sum()
+    gs = torch.autograd.grad(loss, Wt)
+    return [g.numpy() for g in gs]
+
+
+def apply_mem(W, x, depth):
+    with torch.no_grad():
+        Wt = [torch.tensor(m, dtype=torch.float64) for m in W]
+        return _mem(Wt, torch.tensor(x, dtype=torch.float64), depth).numpy()
+
+
+def forward(depth, C, c, p, ns_iters, k, q, v, theta, eta, alpha, gamma, W0, S0,
+            P=None, prev=None):
+    """prev = (keys, values, gammas) of tokens preceding the call, oldest first."""
+    T = len(k)
+    gamma = np.ones(T) if gamma is None else gamma
+    pk, pv, pg = ([], [], []) if prev is None else prev
+    keys = list(pk) + list(k)
+    vals = list(pv) + list(v)
+    gams = list(pg) + list(gamma)
+    n_prev = len(pk)
+
+    def feat(vec):
+        f = monomials(vec, p)
+        return f if P is None else f @ np.asarray(P, np.float64)
+
+    W = [np.array(m, np.float64) for m in W0]
+    S = [np.array(m, np.float64) for m in S0]
+    W_bar = None
+    y = []
+    for t in range(T):
+        if t % C == 0:
+            W_bar = [m.copy() for m in W]
+        g = [np.zeros_like(m) for m in W]
+        for i in range(t - c + 1, t + 1):
+            if i < -n_prev:
+                continue
+            gi = autograd_grad(W_bar, feat(keys[i + n_prev]), np.asarray(vals[i + n_prev]), depth)
+            g = [a + gams[i + n_prev] * b for a, b in zip(g, gi)]
+        S = [eta[t] * Sm - theta[t] * gm for Sm, gm in zip(S, g)]
+        U = [ns_closed_form(Sm, ns_iters) for Sm in S] if ns_iters else S
+        W = [(1.0 - alpha[t]) * Wm + Um for Wm, Um in zip(W, U)]
+        y.append(apply_mem(W, feat(q[t]), depth))
+    return np.array(y), W, S

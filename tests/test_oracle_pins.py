@@ -1,0 +1,360 @@
+"""Pins of the fp64 oracle against facts the pages and the mathematics fix.
+
+Each test names the passage it follows.  None of them re-types the oracle's
+own formulas: they use hand-worked values, finite differences, autograd,
+closed forms, invariants, or the independent per-token reference in
+``tests/bruteforce.py``.
+"""
+import dataclasses
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import bruteforce as bf
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@dataclasses.dataclass
+class Cfg:
+    depth: int = 1
+    C: int = 4
+    c: int = 1
+    p: int = 1
+    ns_iters: int = 0
+
+
+def _rand_case(rng, depth, d_k, d_v, hidden, T, p=1, proj=0, gamma=True, scale_w=0.3):
+    k = rng.standard_normal((T, d_k))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    q = rng.standard_normal((T, d_k))
+    q /= np.linalg.norm(q, axis=1, keepdims=True)
+    v = rng.standard_normal((T, d_v))
+    theta = 0.1 / (1 + np.exp(-rng.standard_normal(T)))
+    eta = 1 / (1 + np.exp(-rng.normal(1, 1, T)))
+    alpha = 1 / (1 + np.exp(-rng.normal(-3, 1, T)))
+    g = 1 / (1 + np.exp(-rng.standard_normal(T))) if gamma else None
+    F = d_k if p == 1 else math.comb(d_k + 2, 2)
+    P = rng.standard_normal((F, proj)) / np.sqrt(F) if proj else None
+    Fm = proj if proj else F
+    if depth == 1:
+        shapes = [(Fm, d_v)]
+    else:
+        shapes = [(Fm, hidden), (hidden, d_v)]
+    W0 = [scale_w * rng.standard_normal(s) for s in shapes]
+    S0 = [0.1 * rng.standard_normal(s) for s in shapes]
+    return dict(k=k, q=q, v=v, theta=theta, eta=eta, alpha=alpha, gamma=g, W0=W0, S0=S0, P=P)
+
+
+def _run_oracle(cfg, case, cache=None):
+    kw = {}
+    if cache is not None:
+        kw = dict(cache_k=cache[0], cache_v=cache[1], cache_g=cache[2])
+    return oracle.forward_unit(cfg, case["k"], case["q"], case["v"], case["theta"], case["eta"],
+                               case["alpha"], case["gamma"], case["W0"], case["S0"], case["P"], **kw)
+
+
+# ------------------------------------------------------------ feature map
+def test_poly_golden_worked_example():
+    """atlas-torch README, "Atlas Extensions": Polynomial Features."""
+    lines = [ln for ln in open(os.path.join(GOLDEN, "poly_features_d3.txt")) if not ln.startswith("#")]
+    x = np.array([float(t) for t in lines[0].split(":")[1].split()])
+    want = np.array([float(t) for t in lines[1].split(":")[1].split()])
+    got = oracle.poly_features(x[None], 2)[0]
+    np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("d", [1, 3, 7])
+def test_poly_matches_itertools_enumeration(d):
+    """Exact monomial expansion with 1/m! (atlas-torch README, Polynomial Features)."""
+    x = np.random.default_rng(d).standard_normal(d)
+    np.testing.assert_allclose(oracle.poly_features(x[None], 2)[0], bf.monomials(x, 2), rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("d,width", [(32, 561), (64, 2145), (5, 21)])
+def test_poly_width(d, width):
+    """1 + d + d(d+1)/2 monomials; 561 for 32-dim keys (ATLAS summary, Section 3.1)."""
+    assert oracle.poly_features(np.zeros((1, d)), 2).shape[1] == width == math.comb(d + 2, 2)
+
+
+def test_poly_kernel_identity():
+    """phi(x).phi(y) = 1 + x.y + ((x.y)^2 + sum x_i^2 y_i^2)/8 for the 1/m! map."""
+    rng = np.random.default_rng(7)
+    for d in (4, 32):
+        x, y = rng.standard_normal((2, d))
+        lhs = oracle.poly_features(x[None], 2)[0] @ oracle.poly_features(y[None], 2)[0]
+        xy = x @ y
+        rhs = 1 + xy + (xy ** 2 + np.sum(x ** 2 * y ** 2)) / 8
+        assert abs(lhs - rhs) < 1e-12 * max(1, abs(rhs))
+
+
+def test_projection_is_applied_after_expansion():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((2, 4))
+    P = rng.standard_normal((15, 3))
+    want = np.stack([bf.monomials(r, 2) @ P for r in x])
+    np.testing.assert_allclose(oracle.features(x, 2, P), want, rtol=1e-13, atol=1e-13)
+
+
+# -------------------------------------------------------------- gradients
+def _fd_grad(W, x, v, depth, h=1e-6):
+    out = []
+    for m in range(len(W)):
+        g = np.zeros_like(W[m])
+        for idx in itertools.product(*[range(s) for s in W[m].shape]):
+            Wp = [w.copy() for w in W]
+            Wm = [w.copy() for w in W]
+            Wp[m][idx] += h
+            Wm[m][idx] -= h
+            lp = np.sum((oracle.memory_apply(Wp, x[None], depth)[0] - v) ** 2)
+            lm = np.sum((oracle.memory_apply(Wm, x[None], depth)[0] - v) ** 2)
+            g[idx] = (lp - lm) / (2 * h)
+        out.append(g)
+    return out
+
+
+@pytest.mark.parametrize("depth", [1, 2])
+def test_gradient_matches_finite_differences(depth):
+    """Gradient of Eq. 12 (titans-pytorch-mlx README) by central differences."""
+    rng = np.random.default_rng(depth)
+    d, h = 3, 4
+    x, v = rng.standard_normal(d), rng.standard_normal(d)
+    W = [rng.standard_normal((d, d))] if depth == 1 else [rng.standard_normal((d, h)), rng.standard_normal((h, d))]
+    got = oracle.token_gradients(W, x[None], v[None], depth)
+    want = _fd_grad(W, x, v, depth)
+    for g, w in zip(got, want):
+        np.testing.assert_allclose(g[0], w, rtol=1e-7, atol=1e-8)
+
+
+@pytest.mark.parametrize("depth", [1, 2])
+def test_gradient_matches_autograd(depth):
+    rng = np.random.default_rng(10 + depth)
+    d, h, n = 5, 7, 6
+    X, V = rng.standard_normal((n, d)), rng.standard_normal((n, d))
+    W = [rng.standard_normal((d, d))] if depth == 1 else [rng.standard_normal((d, h)), rng.standard_normal((h, d))]
+    got = oracle.token_gradients(W, X, V, depth)
+    for i in range(n):
+        want = bf.autograd_grad(W, X[i], V[i], depth)
+        for g, w in zip(got, want):
+            np.testing.assert_allclose(g[i], w, rtol=1e-12, atol=1e-12)
+
+
+def test_linear_gradient_is_delta_rule_outer_product():
+    """Linear memory: the gradient is (prediction error) x (key), scaled by 2
+    (atlas-torch README, "How the memory works"), checked by differences of
+    the loss along rank-1 probes."""
+    rng = np.random.default_rng(5)
+    d_k, d_v = 4, 3
+    x, v, W = rng.standard_normal(d_k), rng.standard_normal(d_v), rng.standard_normal((d_k, d_v))
+    g = oracle.token_gradients([W], x[None], v[None], 1)[0][0]
+    assert np.linalg.matrix_rank(g, tol=1e-10) == 1
+    # the column space is the key, the row space the prediction error
+    err = x @ W - v
+    np.testing.assert_allclose(np.abs(g @ err) / np.linalg.norm(g @ err), np.abs(x) / np.linalg.norm(x), atol=1e-12)
+
+
+# -------------------------------------------------------- whole recurrence
+def _golden_scalar():
+    rows, cases = [], {}
+    for ln in open(os.path.join(GOLDEN, "titans_scalar_1d.txt")):
+        if ln.startswith("#") or not ln.strip():
+            continue
+        if ln.startswith("tok"):
+            rows.append([float(t) for t in ln.split(":")[1].split()])
+        elif ln.startswith("case"):
+            head, vals = ln.split(":")
+            _, name, what = head.split()
+            cases.setdefault(name, {})[what] = np.array([float(t) for t in vals.split()])
+    return np.array(rows), cases
+
+
+@pytest.mark.parametrize("name,C,c,use_gamma", [("C1c1", 1, 1, False), ("C2c1", 2, 1, False), ("C2c2", 2, 2, True)])
+def test_hand_worked_scalar_memory(name, C, c, use_gamma):
+    """Values worked by hand from Eq. 12-14 (titans-pytorch-mlx README)."""
+    rows, cases = _golden_scalar()
+    k, v, q, theta, eta, alpha, gamma = rows.T
+    y, W, S, _ = oracle.forward_unit(Cfg(depth=1, C=C, c=c), k[:, None], q[:, None], v[:, None], theta, eta,
+                                     alpha, gamma if use_gamma else None, [np.array([[0.5]])], [np.zeros((1, 1))])
+    np.testing.assert_allclose(y[:, 0], cases[name]["y"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(W[0].ravel(), cases[name]["W"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(S[0].ravel(), cases[name]["S"], rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("depth", [1, 2])
+def test_C1_is_the_sequential_titans_rule(depth):
+    """C = 1: every token sees the weights left by the token before, i.e. the
+    sequential update of Eq. 13-14 (titans-pytorch-mlx README)."""
+    rng = np.random.default_rng(20 + depth)
+    case = _rand_case(rng, depth, 4, 4, 6, T=9)
+    y, W, S, _ = _run_oracle(Cfg(depth=depth, C=1, c=1), case)
+    yb, Wb, Sb = bf.forward(depth, 1, 1, 1, 0, case["k"], case["q"], case["v"], case["theta"], case["eta"],
+                            case["alpha"], case["gamma"], case["W0"], case["S0"])
+    np.testing.assert_allclose(y, yb, rtol=1e-11, atol=1e-12)
+    for a, b in zip(W + S, Wb + Sb):
+        np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-12)
+
+
+def test_window_of_one_is_the_single_token_update():
+    """c = 1 recovers the single-association update (ATLAS summary, Section 3.2):
+    with a window of one, token t's surprise is gamma_t times its own gradient
+    only, which we check against the per-token reference at C = 4."""
+    rng = np.random.default_rng(31)
+    case = _rand_case(rng, 2, 3, 3, 5, T=10)
+    y, W, S, _ = _run_oracle(Cfg(depth=2, C=4, c=1), case)
+    yb, Wb, Sb = bf.forward(2, 4, 1, 1, 0, case["k"], case["q"], case["v"], case["theta"], case["eta"],
+                            case["alpha"], case["gamma"], case["W0"], case["S0"])
+    np.testing.assert_allclose(y, yb, rtol=1e-11, atol=1e-12)
+    for a, b in zip(W + S, Wb + Sb):
+        np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("ns", [0, 5])
+def test_alpha_one_wipes_the_state(ns):
+    """alpha_t = 1 forgets everything: W_t = U_t (Eq. 13)."""
+    rng = np.random.default_rng(40 + ns)
+    case = _rand_case(rng, 2, 4, 4, 6, T=5)
+    case["alpha"] = np.ones(5)
+    y, W, S, _ = _run_oracle(Cfg(depth=2, C=2, c=2, ns_iters=ns), case)
+    for Wm, Sm in zip(W, S):
+        want = bf.ns_closed_form(Sm, ns) if ns else Sm
+        np.testing.assert_allclose(Wm, want, rtol=1e-11, atol=1e-12)
+
+
+def test_closed_form_without_momentum_or_decay():
+    """eta = alpha = 0, one chunk, no Newton-Schulz, linear memory:
+    W_T = W0 - sum_t theta_t 2 x_t^T (x_t W0 - v_t)."""
+    rng = np.random.default_rng(50)
+    T = 12
+    case = _rand_case(rng, 1, 5, 3, 0, T=T, gamma=False)
+    case["eta"], case["alpha"] = np.zeros(T), np.zeros(T)
+    y, W, S, _ = _run_oracle(Cfg(depth=1, C=T, c=1), case)
+    X, V, W0 = case["k"], case["v"], case["W0"][0]
+    closed = W0 - np.einsum("t,ti,tj->ij", 2 * case["theta"], X, X @ W0 - V)
+    np.testing.assert_allclose(W[0], closed, rtol=1e-12, atol=1e-13)
+    # and the read-out uses the post-update weights of each token
+    partial = W0 - np.cumsum(np.einsum("t,ti,tj->tij", 2 * case["theta"], X, X @ W0 - V), axis=0)
+    np.testing.assert_allclose(y, np.einsum("ti,tij->tj", case["q"], partial), rtol=1e-12, atol=1e-13)
+
+
+def test_window_perturbation_reaches_exactly_the_next_c_tokens():
+    """The Omega window of token t covers tokens t-c+1..t (atlas-torch README,
+    "Bug Fixes": Omega window slide).  With eta = 0 and alpha = 1 the read-out
+    of token t depends on the surprise g_t alone, so perturbing v_j must move
+    y_t for t in [j, j+c-1] and nowhere else (one chunk, weights frozen)."""
+    rng = np.random.default_rng(60)
+    T, c = 16, 4
+    case = _rand_case(rng, 1, 4, 3, 0, T=T)
+    case["eta"], case["alpha"] = np.zeros(T), np.ones(T)
+    cfg = Cfg(depth=1, C=T, c=c)
+    y0 = _run_oracle(cfg, case)[0]
+    for j in (0, 5, 13):
+        pert = dict(case, v=case["v"].copy())
+        pert["v"][j] += 1.0
+        moved = np.abs(_run_oracle(cfg, pert)[0] - y0).max(axis=1) > 1e-12
+        assert list(np.nonzero(moved)[0]) == list(range(j, min(T, j + c)))
+
+
+# ------------------------------------------------------------ Newton-Schulz
+def test_ns_matches_svd_closed_form():
+    """Each quintic step maps singular values through f and keeps the singular
+    vectors; compare with the SVD form for wide, tall and square inputs."""
+    rng = np.random.default_rng(70)
+    for shape in [(6, 11), (11, 6), (7, 7)]:
+        G = rng.standard_normal(shape) * 3.0
+        for k in (1, 3, 5):
+            np.testing.assert_allclose(oracle.newton_schulz(G, k), bf.ns_closed_form(G, k), rtol=1e-10, atol=1e-12)
+
+
+def test_ns_invariances_and_rank_one():
+    rng = np.random.default_rng(71)
+    G = rng.standard_normal((8, 20))
+    # positive scale invariance (up to eps) and odd symmetry
+    np.testing.assert_allclose(oracle.newton_schulz(7.0 * G, 5), oracle.newton_schulz(G, 5), rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(oracle.newton_schulz(-G, 5), -oracle.newton_schulz(G, 5), rtol=0, atol=1e-14)
+    assert np.all(oracle.newton_schulz(np.zeros((3, 5)), 5) == 0)
+    # rank one: singular value s = |G|/(|G| + eps) goes through f five times
+    u, v = rng.standard_normal(8), rng.standard_normal(20)
+    R1 = np.outer(u, v)
+    s = np.linalg.norm(R1) / (np.linalg.norm(R1) + 1e-7)
+    for _ in range(5):
+        s = 3.4445 * s - 4.7750 * s ** 3 + 2.0315 * s ** 5
+    out = oracle.newton_schulz(R1, 5)
+    assert abs(np.linalg.svd(out, compute_uv=False)[0] - s) < 1e-12
+    assert abs(s - 0.69644) < 5e-5
+    assert np.linalg.matrix_rank(out, tol=1e-9) == 1
+
+
+def test_ns_output_is_near_orthogonal():
+    """Momentum is made approximately semi-orthogonal (ATLAS summary, Section 5):
+    normalised singular values >= 0.05 land in [0.68, 1.13] after 5 steps."""
+    rng = np.random.default_rng(72)
+    U, _ = np.linalg.qr(rng.standard_normal((16, 16)))
+    V, _ = np.linalg.qr(rng.standard_normal((40, 16)))
+    s = np.linspace(0.05, 0.4, 16)
+    s = s / np.linalg.norm(s)        # Frobenius norm 1, smallest value > 0.05
+    assert s.min() >= 0.05
+    G = (U * s) @ V.T
+    out_s = np.linalg.svd(oracle.newton_schulz(G, 5), compute_uv=False)
+    assert out_s.min() > 0.68 - 1e-9 and out_s.max() < 1.13 + 1e-9
+
+
+# ---------------------------------------------------- continuation, general
+@pytest.mark.parametrize("depth,c,ns", [(1, 3, 0), (2, 4, 0), (2, 3, 3)])
+def test_split_continuation(depth, c, ns):
+    """Chunked inference with carried state equals the whole-sequence forward
+    (atlas-torch README, "Status and scope", limitation 5)."""
+    rng = np.random.default_rng(80 + depth + c)
+    T, T1, C = 24, 8, 4
+    case = _rand_case(rng, depth, 4, 4, 6, T=T)
+    cfg = Cfg(depth=depth, C=C, c=c, ns_iters=ns)
+    y, W, S, _ = _run_oracle(cfg, case)
+    first = {k: (v[:T1] if isinstance(v, np.ndarray) and v.shape[:1] == (T,) else v) for k, v in case.items()}
+    y1, W1, S1, cache = _run_oracle(cfg, first)
+    second = {k: (v[T1:] if isinstance(v, np.ndarray) and v.shape[:1] == (T,) else v) for k, v in case.items()}
+    second["W0"], second["S0"] = W1, S1
+    y2, W2, S2, _ = _run_oracle(cfg, second, cache=cache)
+    np.testing.assert_allclose(np.concatenate([y1, y2]), y, rtol=1e-12, atol=1e-12)
+    for a, b in zip(W2 + S2, W + S):
+        np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+BRUTE_CASES = [
+    # depth, C, c, p, proj, ns, d_k, d_v, hidden, T
+    (1, 4, 1, 1, 0, 0, 4, 3, 0, 10),
+    (2, 4, 1, 1, 0, 0, 4, 4, 6, 10),
+    (1, 4, 3, 2, 0, 0, 3, 2, 0, 11),      # Omega + polynomial features
+    (1, 3, 5, 2, 0, 0, 2, 2, 0, 9),       # window longer than a chunk
+    (2, 4, 3, 1, 0, 5, 4, 4, 6, 10),      # Omega + Muon
+    (2, 4, 3, 2, 4, 5, 3, 4, 5, 9),       # polynomial + projection + Muon
+]
+
+
+@pytest.mark.parametrize("case_def", BRUTE_CASES)
+def test_oracle_matches_independent_bruteforce(case_def):
+    depth, C, c, p, proj, ns, d_k, d_v, hidden, T = case_def
+    rng = np.random.default_rng(hash(case_def) % 2 ** 32)
+    case = _rand_case(rng, depth, d_k, d_v, hidden, T, p=p, proj=proj)
+    cfg = Cfg(depth=depth, C=C, c=c, p=p, ns_iters=ns)
+    y, W, S, _ = _run_oracle(cfg, case)
+    yb, Wb, Sb = bf.forward(depth, C, c, p, ns, case["k"], case["q"], case["v"], case["theta"], case["eta"],
+                            case["alpha"], case["gamma"], case["W0"], case["S0"], case["P"])
+    np.testing.assert_allclose(y, yb, rtol=1e-10, atol=1e-11)
+    for a, b in zip(W + S, Wb + Sb):
+        np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-11)
+
+
+def test_bruteforce_with_window_cache():
+    """Windows reach back into tokens handed over from a previous call."""
+    rng = np.random.default_rng(90)
+    case = _rand_case(rng, 2, 3, 3, 4, T=8)
+    prev = _rand_case(rng, 2, 3, 3, 4, T=2)
+    cache = (prev["k"], prev["v"], prev["gamma"])
+    cfg = Cfg(depth=2, C=4, c=3)
+    y, W, S, _ = _run_oracle(cfg, case, cache=cache)
+    yb, Wb, Sb = bf.forward(2, 4, 3, 1, 0, case["k"], case["q"], case["v"], case["theta"], case["eta"],
+                            case["alpha"], case["gamma"], case["W0"], case["S0"], prev=cache)
+    np.testing.assert_allclose(y, yb, rtol=1e-11, atol=1e-12)
