@@ -1,0 +1,90 @@
+// Shared device/host definitions of the memory-layer kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/atlas_mem.h"
+
+namespace atlas {
+
+// Muon quintic Newton-Schulz coefficients and the Frobenius-normalisation eps
+// (atlas-torch README, "Atlas Extensions": Muon / Newton-Schulz).
+constexpr float kNsA = 3.4445f;
+constexpr float kNsB = -4.7750f;
+constexpr float kNsC = 2.0315f;
+constexpr float kNsEps = 1e-7f;
+
+// Problem geometry shared by every kernel of one forward call.
+struct Geom {
+  int depth, d_k, d_v, hidden, C, c, p, proj_dim, ns_iters, qkv_dtype;
+  int F;          // memory input width (d_k, poly width, or proj_dim)
+  int poly;       // width of the monomial expansion (d_k when p == 1)
+  int units;      // B * H
+  int T;          // tokens of this call
+  int n_prev;     // cached tokens in front of this call (win_len)
+  int L;          // key rows per unit = n_prev + T
+  int Kw;         // max window rows of one chunk = C + c - 1
+  int rows[2], cols[2], nmat;
+};
+
+// Per-chunk indices: the chunk covers tokens [s, e) of the call; its Omega
+// windows reach back to token lo (>= -n_prev), i.e. key rows lo + n_prev ...
+struct Chunk {
+  int s, e, lo, nw;  // nw = e - lo window rows
+};
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+
+__device__ __forceinline__ float load_in(const void* p, size_t i, int dtype) {
+  return dtype == ATLAS_BF16 ? bf16_to_f32(((const uint16_t*)p)[i]) : ((const float*)p)[i];
+}
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.f / (1.f + __expf(-z)); }
+__device__ __forceinline__ float siluf_(float z) { return z * sigmoidf_(z); }
+__device__ __forceinline__ float dsiluf_(float z) {
+  float s = sigmoidf_(z);
+  return s * (1.f + z * (1.f - s));
+}
+
+// Workspace pointers of one forward call (all fp32, device).
+struct Work {
+  float* X;       // [units][L][F]     key features (cache rows first)
+  float* V;       // [units][L][d_v]   values
+  float* G;       // [units][L]        Omega weights
+  float* R;       // [units][T][F]     query features
+  float* Wst[2][2];  // [buffer][matrix] state W, ping-pong by chunk parity
+  float* Sst[2][2];  // [buffer][matrix] state S
+  // per-chunk factors of the window rows (Kw rows max)
+  float* Zpre;    // depth 2: [units][Kw][hidden] pre-activation z_i
+  float* Aact;    // depth 2: [units][Kw][hidden] a_i = SiLU(z_i)
+  float* DZ;      // depth 2: [units][Kw][hidden] dz_i (gamma folded in)
+  float* DY;      // [units][Kw][d_v] dy_i = 2 gamma_i (yhat_i - v_i)
+  float* Cs;      // [units][C][Kw]  momentum coefficient of row i in S_t
+  float* Cw;      // [units][C][Kw]  coefficient of row i in W_t
+  float* Ap;      // [units][C]  prod eta (s..t)
+  float* Bp;      // [units][C]  prod (1 - alpha) (s..t)
+  float* Dp;      // [units][C]  coefficient of S_bar in W_t
+  float* Ubuf;    // NS path: [units][C][sum_m rows*cols] U_t then W_t (X orientation)
+  int* status;    // device status word
+};
+
+// Pointers of one call that the generic kernels read (device).
+struct GenericIO {
+  const void *q, *k, *v, *P, *win_k, *win_v;
+  const float *theta, *eta, *alpha, *gamma, *win_gamma;
+  float* y;
+};
+
+// generic fp32 path (k_generic.cu)
+cudaError_t generic_prepare(const Geom& g, const Work& w, const GenericIO& io, cudaStream_t st);
+cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const GenericIO& io, int buf,
+                          cudaStream_t st);
+cudaError_t generic_cache_out(const Geom& g, const GenericIO& io, float* tmp, void* k_out, void* v_out,
+                              float* g_out, cudaStream_t st);
+size_t generic_smem_grad(const Geom& g);
+size_t generic_smem_readout(const Geom& g);
+size_t generic_smem_ns(const Geom& g, int m);
+
+}  // namespace atlas

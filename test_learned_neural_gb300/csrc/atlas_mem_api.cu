@@ -1,0 +1,383 @@
+// Host side of the C ABI: config validation, workspace, launch sequence.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <string>
+
+#include "atlas_common.cuh"
+
+
+using namespace atlas;
+
+struct atlas_mem_handle {
+  atlas_mem_config cfg;
+  Geom base;              // sizes that do not depend on the call
+  void* ws = nullptr;     // device workspace
+  size_t ws_bytes = 0;
+  void* stage = nullptr;  // device staging for atlas_mem_forward_host
+  size_t stage_bytes = 0;
+  int* status = nullptr;  // device status word (inside ws)
+  cudaStream_t last_stream = nullptr;
+  bool launched = false;
+  std::string err;
+};
+
+// message of the last atlas_mem_create failure on this thread (no handle yet)
+static thread_local std::string g_create_err;
+
+static int fail(atlas_mem_handle* h, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (h) h->err = buf;
+  return code;
+}
+
+static constexpr size_t kSmemLimit = 227 * 1024;
+
+static long long choose2(long long n) { return n * (n - 1) / 2; }
+
+static int derive_geom(const atlas_mem_config& c, Geom* g, char* why, size_t why_n, bool* unsupported) {
+  *unsupported = false;
+  memset(g, 0, sizeof *g);
+#define BAD(...)                            \
+  do {                                      \
+    snprintf(why, why_n, __VA_ARGS__);      \
+    return 0;                               \
+  } while (0)
+  if (c.depth != 1 && c.depth != 2) BAD("depth must be 1 or 2 (got %d)", c.depth);
+  if (c.d_k < 1 || c.d_v < 1) BAD("d_k and d_v must be >= 1");
+  if (c.depth == 2 && c.hidden < 1) BAD("depth 2 needs hidden >= 1");
+  if (c.C < 1) BAD("chunk size C must be >= 1");
+  if (c.c < 1) BAD("Omega window c must be >= 1");
+  if (c.p != 1 && c.p != 2) BAD("polynomial degree p must be 1 or 2 (got %d)", c.p);
+  if (c.proj_dim < 0) BAD("proj_dim must be >= 0");
+  if (c.ns_iters < 0) BAD("ns_iters must be >= 0");
+  if (c.qkv_dtype != ATLAS_F32 && c.qkv_dtype != ATLAS_BF16) BAD("qkv_dtype must be ATLAS_F32 or ATLAS_BF16");
+  long long poly = c.p == 1 ? c.d_k : 1 + c.d_k + choose2(c.d_k + 1);
+  long long F = c.proj_dim ? c.proj_dim : poly;
+  if (c.depth == 2 && F != c.d_v) BAD("depth 2 (residual memory) needs feature width %lld == d_v %d", F, c.d_v);
+  g->depth = c.depth; g->d_k = c.d_k; g->d_v = c.d_v; g->hidden = c.depth == 2 ? c.hidden : 0;
+  g->C = c.C; g->c = c.c; g->p = c.p; g->proj_dim = c.proj_dim; g->ns_iters = c.ns_iters;
+  g->qkv_dtype = c.qkv_dtype;
+  g->Kw = c.C + c.c - 1;
+  if (c.depth == 1) {
+    g->nmat = 1; g->rows[0] = (int)F; g->cols[0] = c.d_v;
+  } else {
+    g->nmat = 2; g->rows[0] = (int)F; g->cols[0] = c.hidden; g->rows[1] = c.hidden; g->cols[1] = c.d_v;
+  }
+  // limits of the kernels (valid configs beyond them are UNSUPPORTED)
+  *unsupported = true;
+  if (poly > 16384 || F > 8192 || c.d_v > 8192 || c.hidden > 8192) BAD("widths beyond 8192 features are not supported");
+  if (g->Kw > 1024) BAD("C + c - 1 = %d > 1024 window rows per chunk is not supported", g->Kw);
+  g->poly = (int)poly;
+  g->F = (int)F;
+  if (generic_smem_grad(*g) > kSmemLimit || generic_smem_readout(*g) > kSmemLimit)
+    BAD("memory widths too large for the on-chip working set");
+  if ((size_t)(c.d_k + (c.proj_dim ? poly : 0)) * 4 > kSmemLimit) BAD("feature map too wide");
+  if (c.ns_iters > 0)
+    for (int m = 0; m < g->nmat; ++m) {
+      int rX = g->rows[m] < g->cols[m] ? g->rows[m] : g->cols[m];
+      if (rX > 128) BAD("Newton-Schulz on matrices whose short side exceeds 128 is not supported");
+    }
+  *unsupported = false;
+#undef BAD
+  return 1;
+}
+
+// ------------------------------------------------------------ workspace map
+struct Layout {
+  size_t off[32];
+  size_t total;
+};
+
+static size_t al(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Sizes (in floats) of every workspace array, in Work order.
+static Layout layout(const Geom& g, int units, int T) {
+  Layout L{};
+  const size_t U = units, Lr = (size_t)(g.c - 1) + T, Kw = g.Kw, h = g.hidden;
+  size_t mat = 0;
+  for (int m = 0; m < g.nmat; ++m) mat += (size_t)g.rows[m] * g.cols[m];
+  size_t sizes[] = {
+      U * Lr * g.F,                        // X
+      U * Lr * g.d_v,                      // V
+      U * Lr,                              // G
+      U * (size_t)T * g.F,                 // R
+      U * (size_t)g.rows[0] * g.cols[0],   // W buf0 m0
+      U * (size_t)g.rows[1] * g.cols[1],   // W buf0 m1
+      U * (size_t)g.rows[0] * g.cols[0],   // W buf1 m0
+      U * (size_t)g.rows[1] * g.cols[1],   // W buf1 m1
+      U * (size_t)g.rows[0] * g.cols[0],   // S buf0 m0
+      U * (size_t)g.rows[1] * g.cols[1],   // S buf0 m1
+      U * (size_t)g.rows[0] * g.cols[0],   // S buf1 m0
+      U * (size_t)g.rows[1] * g.cols[1],   // S buf1 m1
+      U * Kw * h,                          // Zpre
+      U * Kw * h,                          // Aact
+      U * Kw * h,                          // DZ
+      U * Kw * g.d_v,                      // DY
+      U * g.C * Kw,                        // Cs
+      U * g.C * Kw,                        // Cw
+      U * g.C, U * g.C, U * g.C,           // Ap Bp Dp
+      g.ns_iters ? U * g.C * mat : 0,      // Ubuf
+      U * (size_t)(g.c > 1 ? g.c - 1 : 0) * (g.d_k + g.d_v + 1),  // cache temp
+      64,                                  // status
+  };
+  const int n = sizeof sizes / sizeof sizes[0];
+  size_t o = 0;
+  for (int i = 0; i < n; ++i) {
+    L.off[i] = o;
+    o += al(sizes[i] * sizeof(float));
+  }
+  L.total = o;
+  return L;
+}
+
+static Work work_from(const Geom& g, void* base, const Layout& L, float** cache_tmp) {
+  char* b = (char*)base;
+  auto F = [&](int i) { return (float*)(b + L.off[i]); };
+  Work w;
+  w.X = F(0); w.V = F(1); w.G = F(2); w.R = F(3);
+  w.Wst[0][0] = F(4); w.Wst[0][1] = F(5); w.Wst[1][0] = F(6); w.Wst[1][1] = F(7);
+  w.Sst[0][0] = F(8); w.Sst[0][1] = F(9); w.Sst[1][0] = F(10); w.Sst[1][1] = F(11);
+  w.Zpre = F(12); w.Aact = F(13); w.DZ = F(14); w.DY = F(15);
+  w.Cs = F(16); w.Cw = F(17); w.Ap = F(18); w.Bp = F(19); w.Dp = F(20);
+  w.Ubuf = F(21);
+  *cache_tmp = F(22);
+  w.status = (int*)F(23);
+  return w;
+}
+
+// ------------------------------------------------------------------- API
+extern "C" int atlas_mem_create(const atlas_mem_config* cfg, atlas_mem_handle** out) {
+  if (!out || !cfg) {
+    g_create_err = "cfg and out must be non-NULL";
+    if (out) *out = nullptr;
+    return ATLAS_ERR_INVALID_ARG;
+  }
+  *out = nullptr;
+  Geom g;
+  char why[256];
+  bool unsup = false;
+  if (!derive_geom(*cfg, &g, why, sizeof why, &unsup)) {
+    g_create_err = why;
+    return unsup ? ATLAS_ERR_UNSUPPORTED : ATLAS_ERR_INVALID_ARG;
+  }
+  atlas_mem_handle* h = new atlas_mem_handle();
+  h->cfg = *cfg;
+  h->base = g;
+  *out = h;
+  return ATLAS_OK;
+}
+
+extern "C" void atlas_mem_destroy(atlas_mem_handle* h) {
+  if (!h) return;
+  if (h->ws) cudaFree(h->ws);
+  if (h->stage) cudaFree(h->stage);
+  delete h;
+}
+
+extern "C" const char* atlas_mem_last_error(const atlas_mem_handle* h) {
+  return h ? h->err.c_str() : g_create_err.c_str();
+}
+
+extern "C" size_t atlas_mem_workspace_bytes(const atlas_mem_handle* h, int B, int H, int T) {
+  if (!h || B <= 0 || H <= 0 || T <= 0) return 0;
+  return layout(h->base, B * H, T).total;
+}
+
+static int check_io(atlas_mem_handle* h, const atlas_mem_io* io) {
+  if (!io) return fail(h, ATLAS_ERR_INVALID_ARG, "io is NULL");
+  const Geom& g = h->base;
+  if (io->B <= 0 || io->H <= 0 || io->T <= 0) return fail(h, ATLAS_ERR_INVALID_ARG, "B, H, T must be > 0");
+  if ((long long)io->B * io->H > (1 << 20)) return fail(h, ATLAS_ERR_UNSUPPORTED, "more than 2^20 units");
+  if (io->T % g.C != 0) return fail(h, ATLAS_ERR_UNSUPPORTED, "T = %d is not a multiple of C = %d", io->T, g.C);
+  if (!io->q || !io->k || !io->v || !io->theta || !io->eta || !io->alpha || !io->y)
+    return fail(h, ATLAS_ERR_INVALID_ARG, "q, k, v, theta, eta, alpha and y must be non-NULL");
+  for (int m = 0; m < g.nmat; ++m)
+    if (!io->W0[m] || !io->S0[m] || !io->W_out[m] || !io->S_out[m])
+      return fail(h, ATLAS_ERR_INVALID_ARG, "W0/S0/W_out/S_out[%d] must be non-NULL", m);
+  if (g.proj_dim && !io->P) return fail(h, ATLAS_ERR_INVALID_ARG, "proj_dim > 0 needs P");
+  if (io->win_len < 0 || io->win_len > g.c - 1)
+    return fail(h, ATLAS_ERR_INVALID_ARG, "win_len = %d outside [0, c-1 = %d]", io->win_len, g.c - 1);
+  if (io->win_len > 0 && (!io->win_k || !io->win_v))
+    return fail(h, ATLAS_ERR_INVALID_ARG, "win_len > 0 needs win_k and win_v");
+  return ATLAS_OK;
+}
+
+#define CUDA_TRY(call)                                                                          \
+  do {                                                                                          \
+    cudaError_t e_ = (call);                                                                    \
+    if (e_ != cudaSuccess) return fail(h, ATLAS_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+static int ensure_workspace(atlas_mem_handle* h, size_t bytes) {
+  if (h->ws_bytes >= bytes) return ATLAS_OK;
+  const char* inj = getenv("ATLAS_INJECT_ALLOC_FAILURE");
+  if (inj && inj[0] == '1') return fail(h, ATLAS_ERR_OOM, "workspace allocation of %zu bytes failed (injected)", bytes);
+  if (h->ws) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(h, ATLAS_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
+    cudaFree(h->ws);
+    h->ws = nullptr;
+    h->ws_bytes = 0;
+  }
+  cudaError_t e = cudaMalloc(&h->ws, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    h->ws = nullptr;
+    return fail(h, ATLAS_ERR_OOM, "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
+  }
+  e = cudaMemset(h->ws, 0, bytes);
+  if (e != cudaSuccess) return fail(h, ATLAS_ERR_CUDA, "cudaMemset: %s", cudaGetErrorString(e));
+  h->ws_bytes = bytes;
+  return ATLAS_OK;
+}
+
+extern "C" int atlas_mem_forward(atlas_mem_handle* h, const atlas_mem_io* io, void* stream) {
+  if (!h) return ATLAS_ERR_INVALID_ARG;
+  int rc = check_io(h, io);
+  if (rc) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  Geom g = h->base;
+  g.units = io->B * io->H;
+  g.T = io->T;
+  g.n_prev = io->win_len;
+  g.L = g.n_prev + g.T;
+  const Layout L = layout(g, g.units, g.T);
+  rc = ensure_workspace(h, L.total);
+  if (rc) return rc;
+  float* cache_tmp = nullptr;
+  Work w = work_from(g, h->ws, L, &cache_tmp);
+  h->status = w.status;
+  for (int m = 0; m < g.nmat; ++m) {
+    const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
+    CUDA_TRY(cudaMemcpyAsync(w.Wst[0][m], io->W0[m], bytes, cudaMemcpyDeviceToDevice, st));
+    CUDA_TRY(cudaMemcpyAsync(w.Sst[0][m], io->S0[m], bytes, cudaMemcpyDeviceToDevice, st));
+  }
+  GenericIO gio{io->q, io->k, io->v, io->P, io->win_len ? io->win_k : nullptr, io->win_len ? io->win_v : nullptr,
+                io->theta, io->eta, io->alpha, io->gamma, io->win_len ? io->win_gamma : nullptr, io->y};
+  CUDA_TRY(generic_prepare(g, w, gio, st));
+  int buf = 0;
+  for (int s = 0; s < g.T; s += g.C) {
+    Chunk ch;
+    ch.s = s;
+    ch.e = s + g.C;
+    ch.lo = s - g.c + 1;
+    if (ch.lo < -g.n_prev) ch.lo = -g.n_prev;
+    ch.nw = ch.e - ch.lo;
+    CUDA_TRY(generic_chunk(g, ch, w, gio, buf, st));
+    buf ^= 1;
+  }
+  for (int m = 0; m < g.nmat; ++m) {
+    const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
+    CUDA_TRY(cudaMemcpyAsync(io->W_out[m], w.Wst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
+    CUDA_TRY(cudaMemcpyAsync(io->S_out[m], w.Sst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
+  }
+  if (g.c > 1 && (io->win_k_out || io->win_v_out || io->win_gamma_out))
+    CUDA_TRY(generic_cache_out(g, gio, cache_tmp, io->win_k_out, io->win_v_out, io->win_gamma_out, st));
+  h->last_stream = st;
+  h->launched = true;
+  return ATLAS_OK;
+}
+
+extern "C" int atlas_mem_status(atlas_mem_handle* h) {
+  if (!h) return ATLAS_ERR_INVALID_ARG;
+  if (!h->launched || !h->status) return ATLAS_OK;
+  CUDA_TRY(cudaStreamSynchronize(h->last_stream));
+  int s = 0;
+  CUDA_TRY(cudaMemcpy(&s, h->status, sizeof s, cudaMemcpyDeviceToHost));
+  if (s != 0) {
+    CUDA_TRY(cudaMemset(h->status, 0, sizeof s));
+    return fail(h, ATLAS_ERR_TIMEOUT, "a device-side wait gave up (status %d)", s);
+  }
+  return ATLAS_OK;
+}
+
+extern "C" int atlas_mem_forward_host(atlas_mem_handle* h, const atlas_mem_io* io, void* stream) {
+  if (!h) return ATLAS_ERR_INVALID_ARG;
+  int rc = check_io(h, io);
+  if (rc) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  const Geom& g = h->base;
+  const size_t U = (size_t)io->B * io->H, T = io->T;
+  const size_t es = g.qkv_dtype == ATLAS_BF16 ? 2 : 4;
+  const size_t ncache = (size_t)(g.c > 1 ? g.c - 1 : 0);
+  // staged arrays: {host pointer, bytes, is_output}
+  struct Item { const void* src; void* dst_host; size_t bytes; };
+  Item items[24];
+  int n = 0;
+  auto in = [&](const void* p, size_t bytes) { items[n++] = Item{p, nullptr, p ? bytes : 0}; };
+  auto out = [&](void* p, size_t bytes) { items[n++] = Item{nullptr, p, p ? bytes : 0}; };
+  in(io->q, U * T * g.d_k * es);
+  in(io->k, U * T * g.d_k * es);
+  in(io->v, U * T * g.d_v * es);
+  in(io->theta, U * T * 4);
+  in(io->eta, U * T * 4);
+  in(io->alpha, U * T * 4);
+  in(io->gamma, U * T * 4);
+  in(io->P, (size_t)g.poly * g.proj_dim * es);
+  for (int m = 0; m < 2; ++m) in(m < g.nmat ? io->W0[m] : nullptr, U * g.rows[m] * g.cols[m] * 4);
+  for (int m = 0; m < 2; ++m) in(m < g.nmat ? io->S0[m] : nullptr, U * g.rows[m] * g.cols[m] * 4);
+  in(io->win_len ? io->win_k : nullptr, U * ncache * g.d_k * es);
+  in(io->win_len ? io->win_v : nullptr, U * ncache * g.d_v * es);
+  in(io->win_len ? io->win_gamma : nullptr, U * ncache * 4);
+  out(io->y, U * T * g.d_v * 4);
+  for (int m = 0; m < 2; ++m) out(m < g.nmat ? io->W_out[m] : nullptr, U * g.rows[m] * g.cols[m] * 4);
+  for (int m = 0; m < 2; ++m) out(m < g.nmat ? io->S_out[m] : nullptr, U * g.rows[m] * g.cols[m] * 4);
+  out(g.c > 1 ? io->win_k_out : nullptr, U * ncache * g.d_k * es);
+  out(g.c > 1 ? io->win_v_out : nullptr, U * ncache * g.d_v * es);
+  out(g.c > 1 ? io->win_gamma_out : nullptr, U * ncache * 4);
+  size_t off[24], total = 0;
+  for (int i = 0; i < n; ++i) {
+    off[i] = total;
+    total += al(items[i].bytes);
+  }
+  if (h->stage_bytes < total) {
+    if (h->stage) {
+      CUDA_TRY(cudaDeviceSynchronize());
+      cudaFree(h->stage);
+      h->stage = nullptr;
+      h->stage_bytes = 0;
+    }
+    cudaError_t e = cudaMalloc(&h->stage, total);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(h, ATLAS_ERR_OOM, "staging cudaMalloc(%zu): %s", total, cudaGetErrorString(e));
+    }
+    h->stage_bytes = total;
+  }
+  char* base = (char*)h->stage;
+  void* dptr[24];
+  for (int i = 0; i < n; ++i) {
+    dptr[i] = items[i].bytes ? base + off[i] : nullptr;
+    if (items[i].src && items[i].bytes)
+      CUDA_TRY(cudaMemcpyAsync(dptr[i], items[i].src, items[i].bytes, cudaMemcpyHostToDevice, st));
+  }
+  atlas_mem_io d = *io;
+  int i = 0;
+  d.q = dptr[i++]; d.k = dptr[i++]; d.v = dptr[i++];
+  d.theta = (const float*)dptr[i++]; d.eta = (const float*)dptr[i++]; d.alpha = (const float*)dptr[i++];
+  d.gamma = (const float*)dptr[i++];
+  d.P = dptr[i++];
+  for (int m = 0; m < 2; ++m) d.W0[m] = (const float*)dptr[i++];
+  for (int m = 0; m < 2; ++m) d.S0[m] = (const float*)dptr[i++];
+  d.win_k = dptr[i++]; d.win_v = dptr[i++]; d.win_gamma = (const float*)dptr[i++];
+  const int first_out = i;
+  d.y = (float*)dptr[i++];
+  for (int m = 0; m < 2; ++m) d.W_out[m] = (float*)dptr[i++];
+  for (int m = 0; m < 2; ++m) d.S_out[m] = (float*)dptr[i++];
+  d.win_k_out = dptr[i++]; d.win_v_out = dptr[i++]; d.win_gamma_out = (float*)dptr[i++];
+  rc = atlas_mem_forward(h, &d, stream);
+  if (rc) return rc;
+  for (int j = first_out; j < n; ++j)
+    if (items[j].dst_host && items[j].bytes)
+      CUDA_TRY(cudaMemcpyAsync(items[j].dst_host, dptr[j], items[j].bytes, cudaMemcpyDeviceToHost, st));
+  CUDA_TRY(cudaStreamSynchronize(st));
+  return atlas_mem_status(h);
+}

@@ -1,0 +1,590 @@
+// Generic fp32 SIMT kernels of the chunked memory forward.
+//
+// These cover every configuration the API accepts (any depth, widths, chunk,
+// window, feature map and Newton-Schulz count within the limits checked on
+// the host) in plain fp32 arithmetic.  The per-chunk work is split into small
+// kernels launched in order on one stream:
+//
+//   grad     gradient factors of the window rows at the chunk-start weights
+//   coef     gate scans: coefficients of every window row in S_t and W_t
+//   dual_*   (no Newton-Schulz) read-out and chunk-end state in dual form
+//   ns_*     (Newton-Schulz) per-token momentum, orthogonalisation, decay
+//            scan and read-out
+//
+// Notation (row vectors): window row i is key token lo+i of the chunk;
+// x_i its features, a_i = SiLU(z_i), z_i = x_i W1bar; dy_i = 2 gamma_i
+// (M_Wbar(x_i) - v_i); dz_i = (dy_i W2bar^T) * SiLU'(z_i).  Then
+//   S_t = A_t Sbar - sum_i Cs[t,i] G_i,   W_t = B_t Wbar + D_t Sbar - sum_i Cw[t,i] G_i
+// with G_i the per-token gradient outer products (x_i^T dy_i at depth 1;
+// x_i^T dz_i and a_i^T dy_i at depth 2), A_t = prod eta, B_t = prod (1-alpha),
+// Cs[t,i] = eta_t Cs[t-1,i] + theta_t [i in window(t)], Cw[t,i] = (1-alpha_t)
+// Cw[t-1,i] + Cs[t,i], D_t = (1-alpha_t) D_{t-1} + A_t: the Titans recurrences
+// (titans-pytorch-mlx README, Eq. 13-14) unrolled over one chunk whose
+// gradients are all taken at the chunk-start weights (ATLAS summary, 3.3).
+#include "atlas_common.cuh"
+
+namespace atlas {
+
+// ------------------------------------------------------------------ features
+// phi(x): identity, or [1, x_i, x_i x_j / 2 (i <= j, lexicographic)], then
+// optionally times P (atlas-torch README, "Atlas Extensions": Polynomial
+// Features).  One block per token row.
+__device__ __forceinline__ float poly_feature(const float* x, int d, int f) {
+  if (f == 0) return 1.f;
+  if (f <= d) return x[f - 1];
+  int q = f - 1 - d, i = 0;
+  while (q >= d - i) { q -= d - i; ++i; }
+  return 0.5f * x[i] * x[i + q];
+}
+
+__global__ void k_features(Geom g, const void* src, const void* cache, int rows_per_unit,
+                           int from_cache, const void* P, float* out) {
+  extern __shared__ float sm[];
+  float* x = sm;             // d_k
+  float* phi = sm + g.d_k;   // poly (only when projecting)
+  const int u = blockIdx.y, row = blockIdx.x;
+  const int d = g.d_k;
+  // where does this row come from: the window cache or the call's tokens
+  for (int k = threadIdx.x; k < d; k += blockDim.x) {
+    float val;
+    if (from_cache && row < g.n_prev) {
+      size_t slot = (size_t)(g.c - 1 - g.n_prev + row);
+      val = load_in(cache, ((size_t)u * (g.c - 1) + slot) * d + k, g.qkv_dtype);
+    } else {
+      int t = row - (from_cache ? g.n_prev : 0);
+      val = load_in(src, ((size_t)u * g.T + t) * d + k, g.qkv_dtype);
+    }
+    x[k] = val;
+  }
+  __syncthreads();
+  float* o = out + ((size_t)u * rows_per_unit + row) * g.F;
+  if (g.proj_dim == 0) {
+    for (int f = threadIdx.x; f < g.F; f += blockDim.x) o[f] = g.p == 1 ? x[f] : poly_feature(x, d, f);
+    return;
+  }
+  for (int f = threadIdx.x; f < g.poly; f += blockDim.x) phi[f] = g.p == 1 ? x[f] : poly_feature(x, d, f);
+  __syncthreads();
+  for (int j = threadIdx.x; j < g.proj_dim; j += blockDim.x) {
+    float acc = 0.f;
+    for (int f = 0; f < g.poly; ++f) acc += phi[f] * load_in(P, (size_t)f * g.proj_dim + j, g.qkv_dtype);
+    o[j] = acc;
+  }
+}
+
+// values and Omega weights of every key row (cache rows first)
+__global__ void k_values(Geom g, const void* v, const void* win_v, const float* gamma,
+                         const float* win_gamma, float* V, float* G) {
+  const int u = blockIdx.y, row = blockIdx.x;
+  const bool cached = row < g.n_prev;
+  const size_t slot = (size_t)(g.c - 1 - g.n_prev + row);
+  const int t = row - g.n_prev;
+  for (int k = threadIdx.x; k < g.d_v; k += blockDim.x) {
+    float val = cached ? load_in(win_v, ((size_t)u * (g.c - 1) + slot) * g.d_v + k, g.qkv_dtype)
+                       : load_in(v, ((size_t)u * g.T + t) * g.d_v + k, g.qkv_dtype);
+    V[((size_t)u * g.L + row) * g.d_v + k] = val;
+  }
+  if (threadIdx.x == 0) {
+    float gm = 1.f;
+    if (cached) { if (win_gamma) gm = win_gamma[(size_t)u * (g.c - 1) + slot]; }
+    else if (gamma) gm = gamma[(size_t)u * g.T + t];
+    G[(size_t)u * g.L + row] = gm;
+  }
+}
+
+// --------------------------------------------------------------------- grad
+// One block per (window row, unit).  Gradient factors at Wbar.
+__global__ void k_grad(Geom g, Chunk ch, Work w, int buf) {
+  extern __shared__ float sm[];
+  const int u = blockIdx.y, i = blockIdx.x;
+  const size_t key_row = (size_t)(ch.lo + g.n_prev + i);
+  const float* x = w.X + ((size_t)u * g.L + key_row) * g.F;
+  const float* v = w.V + ((size_t)u * g.L + key_row) * g.d_v;
+  const float gam = w.G[(size_t)u * g.L + key_row];
+  float* xs = sm;                 // F
+  float* dys = sm + g.F;          // d_v
+  for (int f = threadIdx.x; f < g.F; f += blockDim.x) xs[f] = x[f];
+  __syncthreads();
+  const size_t rowKw = (size_t)u * g.Kw + i;
+  if (g.depth == 1) {
+    const float* W = w.Wst[buf][0] + (size_t)u * g.F * g.d_v;
+    for (int k = threadIdx.x; k < g.d_v; k += blockDim.x) {
+      float acc = 0.f;
+      for (int f = 0; f < g.F; ++f) acc += xs[f] * W[(size_t)f * g.d_v + k];
+      w.DY[rowKw * g.d_v + k] = 2.f * gam * (acc - v[k]);
+    }
+    return;
+  }
+  const int h = g.hidden;
+  float* zs = dys + g.d_v;        // h
+  float* as = zs + h;             // h
+  const float* W1 = w.Wst[buf][0] + (size_t)u * g.F * h;
+  const float* W2 = w.Wst[buf][1] + (size_t)u * h * g.d_v;
+  for (int j = threadIdx.x; j < h; j += blockDim.x) {
+    float acc = 0.f;
+    for (int f = 0; f < g.F; ++f) acc += xs[f] * W1[(size_t)f * h + j];
+    zs[j] = acc;
+    as[j] = siluf_(acc);
+    w.Zpre[rowKw * h + j] = acc;
+    w.Aact[rowKw * h + j] = as[j];
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < g.d_v; k += blockDim.x) {
+    float acc = xs[k];  // residual (F == d_v)
+    for (int j = 0; j < h; ++j) acc += as[j] * W2[(size_t)j * g.d_v + k];
+    float dy = 2.f * gam * (acc - v[k]);
+    dys[k] = dy;
+    w.DY[rowKw * g.d_v + k] = dy;
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < h; j += blockDim.x) {
+    float acc = 0.f;
+    for (int k = 0; k < g.d_v; ++k) acc += dys[k] * W2[(size_t)j * g.d_v + k];
+    w.DZ[rowKw * h + j] = acc * dsiluf_(zs[j]);
+  }
+}
+
+// --------------------------------------------------------------------- coef
+// One block per unit, one thread per window row (plus thread 0 for the
+// per-token products).  Sequential over the tokens of the chunk.
+__global__ void k_coef(Geom g, Chunk ch, const float* theta, const float* eta, const float* alpha, Work w) {
+  const int u = blockIdx.x;
+  const int i = threadIdx.x;
+  const int ti = ch.lo + i;  // token index of window row i (may be < 0: cached)
+  float cs = 0.f, cw = 0.f, Ap = 1.f, Bp = 1.f, Dp = 0.f;
+  for (int t = ch.s; t < ch.e; ++t) {
+    const float th = theta[(size_t)u * g.T + t];
+    const float et = eta[(size_t)u * g.T + t];
+    const float be = 1.f - alpha[(size_t)u * g.T + t];
+    const int r = t - ch.s;
+    if (i < ch.nw) {
+      const bool in_win = ti <= t && t <= ti + g.c - 1;
+      cs = et * cs + (in_win ? th : 0.f);
+      cw = be * cw + cs;
+      w.Cs[((size_t)u * g.C + r) * g.Kw + i] = cs;
+      w.Cw[((size_t)u * g.C + r) * g.Kw + i] = cw;
+    }
+    if (i == 0) {
+      Ap *= et;
+      Bp *= be;
+      Dp = be * Dp + Ap;
+      w.Ap[(size_t)u * g.C + r] = Ap;
+      w.Bp[(size_t)u * g.C + r] = Bp;
+      w.Dp[(size_t)u * g.C + r] = Dp;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- dual form
+// Read-out without Newton-Schulz.  One block per (token of chunk, unit).
+__global__ void k_dual_readout(Geom g, Chunk ch, Work w, int buf, float* y) {
+  extern __shared__ float sm[];
+  const int u = blockIdx.y, r = blockIdx.x, t = ch.s + r;
+  float* rs = sm;                  // F
+  float* gm = rs + g.F;            // nw  (r . x_i, later aq . a_i)
+  float* cw = gm + g.Kw;           // nw
+  const float* rq = w.R + ((size_t)u * g.T + t) * g.F;
+  for (int f = threadIdx.x; f < g.F; f += blockDim.x) rs[f] = rq[f];
+  for (int i = threadIdx.x; i < ch.nw; i += blockDim.x) cw[i] = w.Cw[((size_t)u * g.C + r) * g.Kw + i];
+  __syncthreads();
+  const float Bt = w.Bp[(size_t)u * g.C + r], Dt = w.Dp[(size_t)u * g.C + r];
+  const float* Xw = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * g.F;
+  for (int i = threadIdx.x; i < ch.nw; i += blockDim.x) {
+    float acc = 0.f;
+    for (int f = 0; f < g.F; ++f) acc += rs[f] * Xw[(size_t)i * g.F + f];
+    gm[i] = acc * cw[i];
+  }
+  __syncthreads();
+  float* yo = y + ((size_t)u * g.T + t) * g.d_v;
+  if (g.depth == 1) {
+    const float* W = w.Wst[buf][0] + (size_t)u * g.F * g.d_v;
+    const float* S = w.Sst[buf][0] + (size_t)u * g.F * g.d_v;
+    for (int k = threadIdx.x; k < g.d_v; k += blockDim.x) {
+      float a = 0.f, b = 0.f, c = 0.f;
+      for (int f = 0; f < g.F; ++f) {
+        a += rs[f] * W[(size_t)f * g.d_v + k];
+        b += rs[f] * S[(size_t)f * g.d_v + k];
+      }
+      for (int i = 0; i < ch.nw; ++i) c += gm[i] * w.DY[((size_t)u * g.Kw + i) * g.d_v + k];
+      yo[k] = Bt * a + Dt * b - c;
+    }
+    return;
+  }
+  const int h = g.hidden;
+  float* aq = cw + g.Kw;          // h
+  const float* W1 = w.Wst[buf][0] + (size_t)u * g.F * h;
+  const float* S1 = w.Sst[buf][0] + (size_t)u * g.F * h;
+  for (int j = threadIdx.x; j < h; j += blockDim.x) {
+    float a = 0.f, b = 0.f, c = 0.f;
+    for (int f = 0; f < g.F; ++f) {
+      a += rs[f] * W1[(size_t)f * h + j];
+      b += rs[f] * S1[(size_t)f * h + j];
+    }
+    for (int i = 0; i < ch.nw; ++i) c += gm[i] * w.DZ[((size_t)u * g.Kw + i) * h + j];
+    aq[j] = siluf_(Bt * a + Dt * b - c);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < ch.nw; i += blockDim.x) {
+    float acc = 0.f;
+    for (int j = 0; j < h; ++j) acc += aq[j] * w.Aact[((size_t)u * g.Kw + i) * h + j];
+    gm[i] = acc * cw[i];
+  }
+  __syncthreads();
+  const float* W2 = w.Wst[buf][1] + (size_t)u * h * g.d_v;
+  const float* S2 = w.Sst[buf][1] + (size_t)u * h * g.d_v;
+  for (int k = threadIdx.x; k < g.d_v; k += blockDim.x) {
+    float a = 0.f, b = 0.f, c = 0.f;
+    for (int j = 0; j < h; ++j) {
+      a += aq[j] * W2[(size_t)j * g.d_v + k];
+      b += aq[j] * S2[(size_t)j * g.d_v + k];
+    }
+    for (int i = 0; i < ch.nw; ++i) c += gm[i] * w.DY[((size_t)u * g.Kw + i) * g.d_v + k];
+    yo[k] = rs[k] + Bt * a + Dt * b - c;
+  }
+}
+
+// left/right factors of window row i for matrix m
+__device__ __forceinline__ const float* left_factor(const Geom& g, const Chunk& ch, const Work& w, int u, int m) {
+  if (g.depth == 2 && m == 1) return w.Aact + (size_t)u * g.Kw * g.hidden;
+  return w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * g.F;
+}
+__device__ __forceinline__ const float* right_factor(const Geom& g, const Work& w, int u, int m) {
+  if (g.depth == 2 && m == 0) return w.DZ + (size_t)u * g.Kw * g.hidden;
+  return w.DY + (size_t)u * g.Kw * g.d_v;
+}
+
+// Chunk-end state without Newton-Schulz; one thread per matrix element.
+__global__ void k_dual_state(Geom g, Chunk ch, Work w, int m, int buf) {
+  const int u = blockIdx.y;
+  const int rows = g.rows[m], cols = g.cols[m];
+  const size_t n = (size_t)rows * cols;
+  const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= n) return;
+  const int a = (int)(e / cols), b = (int)(e % cols);
+  const float* Lf = left_factor(g, ch, w, u, m);
+  const float* Rf = right_factor(g, w, u, m);
+  const int r = ch.e - 1 - ch.s;
+  const float* cs = w.Cs + ((size_t)u * g.C + r) * g.Kw;
+  const float* cwv = w.Cw + ((size_t)u * g.C + r) * g.Kw;
+  float accs = 0.f, accw = 0.f;
+  for (int i = 0; i < ch.nw; ++i) {
+    const float prod = Lf[(size_t)i * rows + a] * Rf[(size_t)i * cols + b];
+    accs += cs[i] * prod;
+    accw += cwv[i] * prod;
+  }
+  const float Ae = w.Ap[(size_t)u * g.C + r], Be = w.Bp[(size_t)u * g.C + r], De = w.Dp[(size_t)u * g.C + r];
+  const size_t o = (size_t)u * n + e;
+  const float Sb = w.Sst[buf][m][o], Wb = w.Wst[buf][m][o];
+  w.Sst[buf ^ 1][m][o] = Ae * Sb - accs;
+  w.Wst[buf ^ 1][m][o] = Be * Wb + De * Sb - accw;
+}
+
+// ------------------------------------------------------------ Newton-Schulz
+// Block-wide 64x64 output tile of C = A * B with operand strides, 256 threads,
+// each a 4x4 micro-tile; K streamed through shared memory in steps of 16.
+struct TileOp {
+  const float* p;
+  long is, ks;  // element (i, k) at p[i * is + k * ks]
+};
+
+__device__ void tile_gemm(TileOp A, TileOp Bt, int M, int N, int K, int i0, int j0, float acc[4][4],
+                          float* As, float* Bs) {
+  // As[16][64] holds A(i0.., k0..), Bs[16][64] holds B(k0.., j0..), Bt(j, k) = B(k, j)
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  for (int a = 0; a < 4; ++a)
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int l = threadIdx.x; l < 16 * 64; l += blockDim.x) {
+      const int kk = l / 64, ii = l % 64;
+      const int gi = i0 + ii, gk = k0 + kk, gj = j0 + ii;
+      As[kk * 64 + ii] = (gi < M && gk < K) ? A.p[gi * A.is + gk * A.ks] : 0.f;
+      Bs[kk * 64 + ii] = (gj < N && gk < K) ? Bt.p[gj * Bt.is + gk * Bt.ks] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) av[a] = As[kk * 64 + ty * 4 + a];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) bv[b] = Bs[kk * 64 + tx * 4 + b];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] += av[a] * bv[b];
+    }
+    __syncthreads();
+  }
+}
+
+// One block per (token, matrix, unit): form S_t, orthogonalise, store U_t in
+// the token's slot of Ubuf (X orientation: the short side first).
+// Shared memory: Am[rX*rX] + Bm[rX*rX] + 2 tiles of 16x64.
+__global__ void __launch_bounds__(256) k_ns_simt(Geom g, Chunk ch, Work w, int buf, int m, size_t slot_stride,
+                                                  size_t slot_off) {
+  extern __shared__ float sm[];
+  const int u = blockIdx.y, r = blockIdx.x, t = ch.s + r;
+  const int rows = g.rows[m], cols = g.cols[m];
+  const bool tall = rows > cols;
+  const int rX = tall ? cols : rows, cX = tall ? rows : cols;
+  float* Am = sm;
+  float* Bm = sm + rX * rX;
+  float* As = Bm + rX * rX;
+  float* Bs = As + 16 * 64;
+  __shared__ float red[32];
+  float* X = w.Ubuf + ((size_t)u * g.C + r) * slot_stride + slot_off;
+  const size_t n = (size_t)rows * cols;
+  const float* Lf = left_factor(g, ch, w, u, m);
+  const float* Rf = right_factor(g, w, u, m);
+  const float* cs = w.Cs + ((size_t)u * g.C + r) * g.Kw;
+  const float At = w.Ap[(size_t)u * g.C + r];
+  const float* Sb = w.Sst[buf][m] + (size_t)u * n;
+  const bool last = (t == ch.e - 1);
+  float ss = 0.f;
+  for (size_t e = threadIdx.x; e < n; e += blockDim.x) {
+    const int a = (int)(e / cols), b = (int)(e % cols);
+    float acc = 0.f;
+    for (int i = 0; i < ch.nw; ++i) acc += cs[i] * Lf[(size_t)i * rows + a] * Rf[(size_t)i * cols + b];
+    const float val = At * Sb[e] - acc;
+    if (last) w.Sst[buf ^ 1][m][(size_t)u * n + e] = val;
+    X[tall ? (size_t)b * cX + a : e] = val;
+    ss += val * val;
+  }
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int k = 0; k < (int)(blockDim.x / 32); ++k) tot += red[k];
+    red[0] = 1.f / (sqrtf(tot) + kNsEps);
+  }
+  __syncthreads();
+  const float scale = red[0];
+  for (size_t e = threadIdx.x; e < n; e += blockDim.x) X[e] *= scale;
+  __syncthreads();
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  for (int it = 0; it < g.ns_iters; ++it) {
+    // A = X X^T
+    for (int i0 = 0; i0 < rX; i0 += 64)
+      for (int j0 = 0; j0 < rX; j0 += 64) {
+        float acc[4][4];
+        tile_gemm(TileOp{X, cX, 1}, TileOp{X, cX, 1}, rX, rX, cX, i0, j0, acc, As, Bs);
+        for (int a = 0; a < 4; ++a)
+          for (int b = 0; b < 4; ++b) {
+            const int i = i0 + ty * 4 + a, j = j0 + tx * 4 + b;
+            if (i < rX && j < rX) Am[i * rX + j] = acc[a][b];
+          }
+      }
+    __syncthreads();
+    // B = a I + b A + c A A
+    for (int i0 = 0; i0 < rX; i0 += 64)
+      for (int j0 = 0; j0 < rX; j0 += 64) {
+        float acc[4][4];
+        tile_gemm(TileOp{Am, rX, 1}, TileOp{Am, 1, rX}, rX, rX, rX, i0, j0, acc, As, Bs);
+        for (int a = 0; a < 4; ++a)
+          for (int b = 0; b < 4; ++b) {
+            const int i = i0 + ty * 4 + a, j = j0 + tx * 4 + b;
+            if (i < rX && j < rX) Bm[i * rX + j] = kNsB * Am[i * rX + j] + kNsC * acc[a][b] + (i == j ? kNsA : 0.f);
+          }
+      }
+    __syncthreads();
+    // X <- B X, one column block at a time (a column block only reads itself)
+    for (int j0 = 0; j0 < cX; j0 += 64) {
+      float keep[2][4][4];
+      for (int ib = 0; ib < (rX + 63) / 64; ++ib) {
+        float acc[4][4];
+        tile_gemm(TileOp{Bm, rX, 1}, TileOp{X, 1, cX}, rX, cX, rX, ib * 64, j0, acc, As, Bs);
+        // rX <= 128 (checked on the host): at most two row blocks
+        for (int a = 0; a < 4; ++a)
+          for (int b = 0; b < 4; ++b) keep[ib & 1][a][b] = acc[a][b];
+      }
+      __syncthreads();
+      for (int ib = 0; ib < (rX + 63) / 64; ++ib)
+        for (int a = 0; a < 4; ++a)
+          for (int b = 0; b < 4; ++b) {
+            const int i = ib * 64 + ty * 4 + a, j = j0 + tx * 4 + b;
+            if (i < rX && j < cX) X[(size_t)i * cX + j] = keep[ib & 1][a][b];
+          }
+      __syncthreads();
+    }
+  }
+}
+
+// Decay scan over the chunk, in place: slot t holds U_t on entry and W_t on
+// exit (W_{s-1} = Wbar).  One thread per matrix element (X orientation).
+__global__ void k_ns_wscan(Geom g, Chunk ch, Work w, int buf, int m, size_t slot_stride, size_t slot_off,
+                           const float* alpha) {
+  const int u = blockIdx.y;
+  const int rows = g.rows[m], cols = g.cols[m];
+  const bool tall = rows > cols;
+  const size_t n = (size_t)rows * cols;
+  const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= n) return;
+  const int a = (int)(e / cols), b = (int)(e % cols);
+  const size_t xe = tall ? (size_t)b * rows + a : e;
+  float W = w.Wst[buf][m][(size_t)u * n + e];
+  for (int t = ch.s; t < ch.e; ++t) {
+    float* slot = w.Ubuf + ((size_t)u * g.C + (t - ch.s)) * slot_stride + slot_off;
+    W = (1.f - alpha[(size_t)u * g.T + t]) * W + slot[xe];
+    slot[xe] = W;
+  }
+  w.Wst[buf ^ 1][m][(size_t)u * n + e] = W;
+}
+
+// Read-out from the materialised per-token weights W_t (Newton-Schulz path).
+__global__ void k_ns_readout(Geom g, Chunk ch, Work w, size_t slot_stride, float* y) {
+  extern __shared__ float sm[];
+  const int u = blockIdx.y, r = blockIdx.x, t = ch.s + r;
+  float* rs = sm;
+  const float* rq = w.R + ((size_t)u * g.T + t) * g.F;
+  for (int f = threadIdx.x; f < g.F; f += blockDim.x) rs[f] = rq[f];
+  __syncthreads();
+  const float* slot = w.Ubuf + ((size_t)u * g.C + r) * slot_stride;
+  float* yo = y + ((size_t)u * g.T + t) * g.d_v;
+  if (g.depth == 1) {
+    const bool tall = g.F > g.d_v;
+    for (int k = threadIdx.x; k < g.d_v; k += blockDim.x) {
+      float acc = 0.f;
+      for (int f = 0; f < g.F; ++f) acc += rs[f] * slot[tall ? (size_t)k * g.F + f : (size_t)f * g.d_v + k];
+      yo[k] = acc;
+    }
+    return;
+  }
+  const int h = g.hidden;
+  float* aq = rs + g.F;
+  const bool tall1 = g.F > h;
+  for (int j = threadIdx.x; j < h; j += blockDim.x) {
+    float acc = 0.f;
+    for (int f = 0; f < g.F; ++f) acc += rs[f] * slot[tall1 ? (size_t)j * g.F + f : (size_t)f * h + j];
+    aq[j] = siluf_(acc);
+  }
+  __syncthreads();
+  const float* W2 = slot + (size_t)g.F * h;
+  const bool tall2 = h > g.d_v;
+  for (int k = threadIdx.x; k < g.d_v; k += blockDim.x) {
+    float acc = rs[k];
+    for (int j = 0; j < h; ++j) acc += aq[j] * W2[tall2 ? (size_t)k * h + j : (size_t)j * g.d_v + k];
+    yo[k] = acc;
+  }
+}
+
+// Outgoing window cache: gather the last c-1 raw tokens into a temporary.
+__global__ void k_cache_gather(Geom g, const void* k, const void* v, const float* gamma, const void* win_k,
+                               const void* win_v, const float* win_gamma, float* tmp) {
+  const int u = blockIdx.y, slot = blockIdx.x;  // slot in [0, c-1)
+  const int total = g.n_prev + g.T;
+  const int j = total - (g.c - 1) + slot;       // key row; < 0 means empty
+  const int width = g.d_k + g.d_v + 1;
+  float* o = tmp + ((size_t)u * (g.c - 1) + slot) * width;
+  if (j < 0) return;
+  const bool cached = j < g.n_prev;
+  const size_t cs = (size_t)u * (g.c - 1) + (g.c - 1 - g.n_prev + j);
+  const size_t ts = (size_t)u * g.T + (j - g.n_prev);
+  for (int e = threadIdx.x; e < width; e += blockDim.x) {
+    float val;
+    if (e < g.d_k) val = cached ? load_in(win_k, cs * g.d_k + e, g.qkv_dtype) : load_in(k, ts * g.d_k + e, g.qkv_dtype);
+    else if (e < g.d_k + g.d_v) {
+      const int f = e - g.d_k;
+      val = cached ? load_in(win_v, cs * g.d_v + f, g.qkv_dtype) : load_in(v, ts * g.d_v + f, g.qkv_dtype);
+    } else {
+      val = cached ? (win_gamma ? win_gamma[cs] : 1.f) : (gamma ? gamma[ts] : 1.f);
+    }
+    o[e] = val;
+  }
+}
+
+__device__ __forceinline__ void store_out(void* p, size_t i, float val, int dtype) {
+  if (dtype == ATLAS_BF16) {
+    // the gathered values are exact copies of bf16 inputs: truncation is exact
+    ((uint16_t*)p)[i] = (uint16_t)(__float_as_uint(val) >> 16);
+  } else {
+    ((float*)p)[i] = val;
+  }
+}
+
+__global__ void k_cache_scatter(Geom g, const float* tmp, void* k_out, void* v_out, float* g_out) {
+  const int u = blockIdx.y, slot = blockIdx.x;
+  const int total = g.n_prev + g.T;
+  const int j = total - (g.c - 1) + slot;
+  if (j < 0) return;
+  const int width = g.d_k + g.d_v + 1;
+  const float* s = tmp + ((size_t)u * (g.c - 1) + slot) * width;
+  const size_t cs = (size_t)u * (g.c - 1) + slot;
+  for (int e = threadIdx.x; e < width; e += blockDim.x) {
+    if (e < g.d_k) { if (k_out) store_out(k_out, cs * g.d_k + e, s[e], g.qkv_dtype); }
+    else if (e < g.d_k + g.d_v) { if (v_out) store_out(v_out, cs * g.d_v + (e - g.d_k), s[e], g.qkv_dtype); }
+    else if (g_out) g_out[cs] = s[e];
+  }
+}
+
+// ------------------------------------------------------------------ driver
+static inline unsigned cdiv(size_t a, size_t b) { return (unsigned)((a + b - 1) / b); }
+
+cudaError_t generic_prepare(const Geom& g, const Work& w, const GenericIO& io, cudaStream_t st) {
+  const size_t sm_feat = (size_t)(g.d_k + (g.proj_dim ? g.poly : 0)) * sizeof(float);
+  if (sm_feat > 48 * 1024) cudaFuncSetAttribute(k_features, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_feat);
+  k_features<<<dim3(g.L, g.units), 128, sm_feat, st>>>(g, io.k, io.win_k, g.L, 1, io.P, w.X);
+  k_features<<<dim3(g.T, g.units), 128, sm_feat, st>>>(g, io.q, nullptr, g.T, 0, io.P, w.R);
+  k_values<<<dim3(g.L, g.units), 128, 0, st>>>(g, io.v, io.win_v, io.gamma, io.win_gamma, w.V, w.G);
+  return cudaGetLastError();
+}
+
+// Shared-memory bytes each generic kernel needs (checked against the device
+// limit on the host before launching).
+size_t generic_smem_grad(const Geom& g) {
+  return (size_t)(g.F + g.d_v + (g.depth == 2 ? 2 * g.hidden : 0)) * sizeof(float);
+}
+size_t generic_smem_readout(const Geom& g) {
+  return (size_t)(g.F + 2 * g.Kw + (g.depth == 2 ? g.hidden : 0)) * sizeof(float);
+}
+size_t generic_smem_ns(const Geom& g, int m) {
+  const int rX = g.rows[m] < g.cols[m] ? g.rows[m] : g.cols[m];
+  return (size_t)(2 * rX * rX + 2 * 16 * 64) * sizeof(float);
+}
+
+cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const GenericIO& io, int buf,
+                          cudaStream_t st) {
+  const size_t sg = generic_smem_grad(g), sr = generic_smem_readout(g);
+  cudaFuncSetAttribute(k_grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg);
+  k_grad<<<dim3(ch.nw, g.units), 256, sg, st>>>(g, ch, w, buf);
+  const int coef_threads = ((ch.nw + 31) / 32) * 32;
+  k_coef<<<g.units, coef_threads, 0, st>>>(g, ch, io.theta, io.eta, io.alpha, w);
+  if (g.ns_iters == 0) {
+    cudaFuncSetAttribute(k_dual_readout, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sr);
+    k_dual_readout<<<dim3(ch.e - ch.s, g.units), 256, sr, st>>>(g, ch, w, buf, io.y);
+    for (int m = 0; m < g.nmat; ++m) {
+      const size_t n = (size_t)g.rows[m] * g.cols[m];
+      k_dual_state<<<dim3(cdiv(n, 256), g.units), 256, 0, st>>>(g, ch, w, m, buf);
+    }
+    return cudaGetLastError();
+  }
+  size_t slot_stride = 0;
+  for (int m = 0; m < g.nmat; ++m) slot_stride += (size_t)g.rows[m] * g.cols[m];
+  size_t off = 0;
+  for (int m = 0; m < g.nmat; ++m) {
+    const size_t sn = generic_smem_ns(g, m);
+    cudaFuncSetAttribute(k_ns_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sn);
+    k_ns_simt<<<dim3(ch.e - ch.s, g.units), 256, sn, st>>>(g, ch, w, buf, m, slot_stride, off);
+    off += (size_t)g.rows[m] * g.cols[m];
+  }
+  off = 0;
+  for (int m = 0; m < g.nmat; ++m) {
+    const size_t n = (size_t)g.rows[m] * g.cols[m];
+    k_ns_wscan<<<dim3(cdiv(n, 256), g.units), 256, 0, st>>>(g, ch, w, buf, m, slot_stride, off, io.alpha);
+    off += n;
+  }
+  const size_t srd = (size_t)(g.F + (g.depth == 2 ? g.hidden : 0)) * sizeof(float);
+  cudaFuncSetAttribute(k_ns_readout, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)srd);
+  k_ns_readout<<<dim3(ch.e - ch.s, g.units), 256, srd, st>>>(g, ch, w, slot_stride, io.y);
+  return cudaGetLastError();
+}
+
+cudaError_t generic_cache_out(const Geom& g, const GenericIO& io, float* tmp, void* k_out, void* v_out,
+                              float* g_out, cudaStream_t st) {
+  if (g.c <= 1) return cudaSuccess;
+  k_cache_gather<<<dim3(g.c - 1, g.units), 128, 0, st>>>(g, io.k, io.v, io.gamma, io.win_k, io.win_v, io.win_gamma,
+                                                         tmp);
+  k_cache_scatter<<<dim3(g.c - 1, g.units), 128, 0, st>>>(g, tmp, k_out, v_out, g_out);
+  return cudaGetLastError();
+}
+
+}  // namespace atlas

@@ -1,0 +1,94 @@
+"""CUDA library vs the fp64 oracle on the same seeded inputs, element by
+element, at sizes the oracle finishes in seconds (several chunks each)."""
+import numpy as np
+import pytest
+
+import oracle
+from harness import WORKLOADS, make_inputs
+from tests.gpu_common import TOL, compare, flat_units, maxrel, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    "linear_f32": dict(),                         # full size: 1 unit x 256 tokens
+    "titans_mlp": dict(B=1, H=2, T=256),
+    "atlas_poly_c4": dict(B=1, H=2, T=256),
+    "atlas_poly_c16": dict(B=1, H=2, T=256),
+    "atlas_muon": dict(B=1, H=1, T=128),
+    "atlas_long": dict(B=1, H=2, T=192),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_parity(gpu_lib, name):
+    w = WORKLOADS[name].scaled(**SMALL[name]) if SMALL[name] else WORKLOADS[name]
+    errs = compare(w)
+    tol = TOL[w.qkv_dtype]
+    print(name, {k: f"{v:.2e}" for k, v in errs.items()})
+    assert errs["y"] <= tol
+    for k, v in errs.items():
+        if k.startswith("W"):
+            assert v <= tol, (k, v)
+        if k.startswith("S"):
+            assert v <= 5 * tol, (k, v)
+
+
+@pytest.mark.parametrize("name", ["titans_mlp", "atlas_poly_c16", "atlas_long"])
+def test_split_continuation_matches_whole(gpu_lib, name):
+    """Two calls with carried W, S and window cache equal one call."""
+    import torch
+    from test_learned_neural_gb300.runner import Memory, tensors_from_numpy
+    w = WORKLOADS[name].scaled(B=1, H=2, T=256)
+    inp = make_inputs(w)
+    whole = run_gpu(w, inp)
+    mem = Memory(w)
+    t = tensors_from_numpy(inp)
+    T1 = 128
+    first = {k: (v[:, :, :T1].contiguous() if k in ("q", "k", "v", "theta", "eta", "alpha", "gamma")
+                 and v is not None else v) for k, v in t.items()}
+    o1 = mem.forward(first)
+    second = {k: (v[:, :, T1:].contiguous() if k in ("q", "k", "v", "theta", "eta", "alpha", "gamma")
+                  and v is not None else v) for k, v in t.items()}
+    second["W0"], second["S0"] = o1["W"], o1["S"]
+    win = None
+    if w.c > 1:
+        win = (w.c - 1, o1["win_k"], o1["win_v"], o1["win_gamma"])
+    o2 = mem.forward(second, win=win)
+    torch.cuda.synchronize()
+    y = np.concatenate([o1["y"].cpu().numpy(), o2["y"].cpu().numpy()], axis=2)
+    assert maxrel(y, whole["y"]) < 1e-5
+    for m in range(len(o2["W"])):
+        assert maxrel(o2["W"][m].cpu().numpy(), whole["W"][m]) < 1e-5
+    mem.close()
+
+
+def test_host_buffers_match_device_buffers(gpu_lib):
+    w = WORKLOADS["titans_mlp"].scaled(B=1, H=2, T=128)
+    inp = make_inputs(w)
+    d = run_gpu(w, inp)
+    h = run_gpu(w, inp, host=True)
+    np.testing.assert_array_equal(d["y"], h["y"])
+    for m in range(2):
+        np.testing.assert_array_equal(d["W"][m], h["W"][m])
+
+
+def test_window_cache_out_holds_the_last_tokens(gpu_lib):
+    w = WORKLOADS["atlas_poly_c4"].scaled(B=1, H=2, T=128)
+    inp = make_inputs(w)
+    g = run_gpu(w, inp)
+    k = flat_units(inp["k"])[:, -(w.c - 1):]
+    got = g["win_k"].view(-1, w.c - 1, w.d_k).view(dtype=__import__("torch").int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(got, k)
+    np.testing.assert_array_equal(g["win_gamma"].numpy().reshape(-1, w.c - 1), flat_units(inp["gamma"])[:, -(w.c - 1):])
+
+
+def test_alpha_one_wipes_state_on_gpu(gpu_lib):
+    """alpha = 1: the final W equals the final (orthogonalised) momentum."""
+    w = WORKLOADS["atlas_long"].scaled(B=1, H=1, T=64)
+    inp = make_inputs(w)
+    inp["alpha"] = np.ones_like(inp["alpha"])
+    g = run_gpu(w, inp)
+    S = g["S"]
+    for m in range(2):
+        U = oracle.newton_schulz(flat_units(S[m])[0], w.ns_iters)
+        assert maxrel(flat_units(g["W"][m])[0], U) < 2e-3
