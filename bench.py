@@ -1,0 +1,373 @@
+"""Throughput of the Titans/ATLAS memory-layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+A step is one forward of the whole memory layer (every chunk of every unit)
+over one batch of synthetic inputs that already sit in HBM.  The default
+workload is the Titans MLP memory (B=4, H=8, T=4096, d=64, hidden 256, C=64).
+One JSON line goes to stdout on rank 0.
+
+Under torchrun (N > 1) every rank runs its own batch of the same shape on its
+own GPU (the (batch, head) units are independent: no collective on the data
+path); the timed region is bracketed by barriers and the slowest rank's time
+is reported.  ``--impl reference`` times the fp64 CPU oracle on a bounded
+sample of the same workload on the host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from harness import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "memory-layer tokens/s (B*H*T/s) on 1 GB300"
+
+
+# --------------------------------------------------------------- accounting
+def flops_per_chunk(w) -> float:
+    """Algorithmic FLOPs of one chunk of one unit: the dual form without
+    Newton-Schulz, or the per-token orthogonalisation path with it."""
+    C, Kw = w.C, w.C + w.c - 1
+    F, dv, h = w.feat_dim, w.d_v, w.hidden
+    feat = 0.0
+    if w.proj_dim:
+        feat = 2.0 * w.poly_dim * w.proj_dim * (C + C)     # keys and queries of the chunk
+    if w.ns_iters == 0:
+        if w.depth == 1:
+            fwd = 2.0 * Kw * F * dv
+            read = 2.0 * C * 2 * F * dv + 2.0 * C * Kw * F + 2.0 * C * Kw * dv
+            state = 2 * 2.0 * F * dv * Kw
+        else:
+            fwd = 3 * 2.0 * Kw * F * h
+            read = (2.0 * C * 2 * F * h + 2.0 * C * Kw * F + 2.0 * C * Kw * h
+                    + 2.0 * C * 2 * h * dv + 2.0 * C * Kw * h + 2.0 * C * Kw * dv)
+            state = 2 * 2 * 2.0 * F * h * Kw
+        return feat + fwd + read + state
+    # Newton-Schulz: per token and matrix, S_t from the window factors, k
+    # quintic steps on the short side, decay scan and read-out.
+    mats = [(F, dv)] if w.depth == 1 else [(F, h), (h, dv)]
+    fwd = 2.0 * Kw * F * dv if w.depth == 1 else 3 * 2.0 * Kw * F * h
+    per_tok = 0.0
+    for (r, c) in mats:
+        m, n = min(r, c), max(r, c)
+        per_tok += 2.0 * m * n * Kw                                   # S_t
+        per_tok += w.ns_iters * (2.0 * m * m * n * 2 + 2.0 * m ** 3)  # NS
+        per_tok += 2.0 * m * n * 2                                    # scan + read-out
+    return feat + fwd + C * per_tok
+
+
+def bytes_per_step(w) -> float:
+    es = 2 if w.qkv_dtype == "bf16" else 4
+    per_tok = es * (2 * w.d_k + w.d_v) + 4 * 3 + (4 if w.use_gamma else 0) + 4 * w.d_v
+    state = sum(r * c for r, c in w.matrix_shapes()) * 4 * 4   # W0, S0 in; W, S out
+    return w.tokens * per_tok + w.units * state
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "test_learned_neural_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of the GPU's clocks and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,pci.bus_id")
+
+    def __init__(self, bus_id=None):
+        self.bus_id = (bus_id or "").lower()
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = self.rows
+        if self.bus_id:
+            mine = [r for r in rows if r[8].lower().endswith(self.bus_id[-7:])]
+            rows = mine or rows
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ------------------------------------------------------------- CPU oracle
+_ORACLE_INPUTS = {}
+
+
+def _oracle_job(args):
+    """Worker: oracle forward of one sample; returns its compute seconds
+    (input generation is cached per process and not timed)."""
+    name, units, T = args
+    import oracle
+    w = WORKLOADS[name]
+    if name not in _ORACLE_INPUTS:
+        _ORACLE_INPUTS[name] = make_inputs(w)
+    t0 = time.perf_counter()
+    oracle.forward(w, _ORACLE_INPUTS[name], units=units, T=T)
+    return time.perf_counter() - t0
+
+
+def oracle_sample(w):
+    """Bounded sample of the workload for the CPU oracle: (units, tokens)."""
+    if w.ns_iters:
+        return list(range(min(2, w.units))), 2 * w.C
+    return list(range(min(8, w.units))), min(w.T, 4096)
+
+
+def time_oracle(name, reps=1):
+    """Time the oracle on its sample, one spawned process per unit (one BLAS
+    thread each, all in parallel).  A rep takes as long as its slowest unit.
+    Returns (tokens/s, cores used, description, per-rep seconds)."""
+    import multiprocessing as mp
+    w = WORKLOADS[name]
+    units, T = oracle_sample(w)
+    cores = min(len(units), os.cpu_count() or 1)
+    env_keep = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in env_keep:
+        os.environ[k] = "1"
+    ctx = mp.get_context("spawn")
+    times = []
+    try:
+        with ctx.Pool(cores) as pool:
+            pool.map(_oracle_job, [(name, [u], w.C) for u in units])      # inputs + imports, untimed
+            for _ in range(reps):
+                per_unit = pool.map(_oracle_job, [(name, [u], T) for u in units])
+                waves = -(-len(units) // cores)
+                times.append(max(per_unit) * waves)
+    finally:
+        for k, v in env_keep.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    tokens = len(units) * T
+    desc = f"{len(units)} units x first {T} tokens of {w.name} (fp64 numpy, one process per unit, {cores} cores)"
+    return tokens / statistics.median(times), cores, desc, times
+
+
+# -------------------------------------------------------------- reference
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = WORKLOADS[args.workload]
+    # warm-up: time_oracle runs one untimed pass per worker before the timed reps
+    tps, cores, desc, times = time_oracle(args.workload, reps=args.steps)
+    units, T = oracle_sample(w)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, harness recipe)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "sample": desc},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------- ours
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import test_learned_neural_gb300 as tln
+    from test_learned_neural_gb300.runner import Memory, tensors_from_numpy
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w0 = WORKLOADS[args.workload]
+    w = w0.scaled(seed=w0.seed + 1000 * rank) if rank else w0
+    inp = make_inputs(w)
+    t = tensors_from_numpy(inp, device=dev)
+    mem = Memory(w)
+    out = mem.alloc_outputs(w.B, w.H, w.T, dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)   # > L2 (129 MB)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        mem.forward(t, out=out)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    mem.status()
+    launches = tln.atlas_mem_last_launches(mem.h)
+
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        pass
+    clocks = ClockSampler(f"{bus:02x}:00" if isinstance(bus, int) else None)
+    clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()                    # evict L2 between timed steps
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    mem.status()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_s = sum(step_ms) / 1e3
+    if world > 1:
+        tt = torch.tensor([total_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_s = float(tt.item())
+    tokens = w.tokens * args.steps * world
+    value = tokens / total_s
+
+    # end to end through the host-buffer entry point (pinned host memory)
+    e2e = None
+    if not args.no_e2e:
+        th = tensors_from_numpy(inp, device="cpu", pin=True)
+        oh = mem.alloc_outputs(w.B, w.H, w.T, "cpu")
+        for key, val in list(oh.items()):
+            oh[key] = [x.pin_memory() for x in val] if isinstance(val, list) else val.pin_memory()
+        h2d = sum(x.numel() * x.element_size() for k, x in th.items() if k not in ("W0", "S0") and x is not None)
+        h2d += sum(x.numel() * x.element_size() for x in th["W0"] + th["S0"])
+        d2h = oh["y"].numel() * 4 + sum(x.numel() * 4 for x in oh["W"] + oh["S"])
+        mem.forward(th, out=oh, host=True)
+        reps = max(3, min(args.steps, 10))
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            mem.forward(th, out=oh, host=True)
+        e2e_s = (time.perf_counter() - t0) / reps
+        if world > 1:
+            tt = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_s = float(tt.item())
+        e2e = {"value": w.tokens * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, src = measured_peaks()
+    fl = flops_per_chunk(w) * (w.T // w.C) * w.units
+    step_s = statistics.mean(step_ms) / 1e3
+    achieved = fl / step_s / 1e12
+    peak = peaks.get("bf16_tflops", 1900.0)
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        rec = json.load(open(tpath)).get(w.name)
+        if rec and rec.get("source_digest") == source_digest():
+            traffic = rec.get("dram_bytes_per_step")
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded, harness recipe), inputs resident in HBM",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "depth": w.depth, "d": w.d_v,
+                   "hidden": w.hidden, "C": w.C, "c": w.c, "p": w.p, "ns_iters": w.ns_iters,
+                   "l2": "flushed between timed steps (256 MB write)", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": f"bf16_tflops ({src})",
+                     "kernel": "whole forward (all launches of one step)",
+                     "algorithmic_flops_per_step": fl, "algorithmic_bytes_per_step": bytes_per_step(w)},
+        "gpu_launches": launches * args.steps,
+        "e2e": e2e,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        tps, cores, desc, _ = time_oracle(w.name, reps=1)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="titans_mlp", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -125,6 +125,10 @@ int atlas_mem_status(atlas_mem_handle* h);
 /* Device workspace, in bytes, that a forward of this size uses. */
 size_t atlas_mem_workspace_bytes(const atlas_mem_handle* h, int B, int H, int T);
 
+/* Number of CUDA kernels the last atlas_mem_forward on this handle launched
+ * (copies excluded). */
+int atlas_mem_last_launches(const atlas_mem_handle* h);
+
 /* Message of the last failure on this handle ("" if none).  With h == NULL:
  * the message of the calling thread's last failed atlas_mem_create. */
 const char* atlas_mem_last_error(const atlas_mem_handle* h);

@@ -19,7 +19,7 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "OOM"
 
 # exported symbols, as declared in include/atlas_mem.h
 EXPORTS = ("atlas_mem_create", "atlas_mem_forward", "atlas_mem_forward_host", "atlas_mem_status",
-           "atlas_mem_workspace_bytes", "atlas_mem_last_error", "atlas_mem_destroy")
+           "atlas_mem_workspace_bytes", "atlas_mem_last_launches", "atlas_mem_last_error", "atlas_mem_destroy")
 
 
 class atlas_mem_config(ctypes.Structure):
@@ -72,6 +72,8 @@ def load(path: str = LIB_PATH):
     lib.atlas_mem_status.restype = ctypes.c_int
     lib.atlas_mem_workspace_bytes.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int]
     lib.atlas_mem_workspace_bytes.restype = ctypes.c_size_t
+    lib.atlas_mem_last_launches.argtypes = [ctypes.c_void_p]
+    lib.atlas_mem_last_launches.restype = ctypes.c_int
     lib.atlas_mem_last_error.argtypes = [ctypes.c_void_p]
     lib.atlas_mem_last_error.restype = ctypes.c_char_p
     lib.atlas_mem_destroy.argtypes = [ctypes.c_void_p]
@@ -110,6 +112,10 @@ def atlas_mem_status(h) -> int:
 
 def atlas_mem_workspace_bytes(h, B, H, T) -> int:
     return load().atlas_mem_workspace_bytes(h, B, H, T)
+
+
+def atlas_mem_last_launches(h) -> int:
+    return load().atlas_mem_last_launches(h)
 
 
 def atlas_mem_last_error(h) -> str:

@@ -78,11 +78,11 @@ struct GenericIO {
 };
 
 // generic fp32 path (k_generic.cu)
-cudaError_t generic_prepare(const Geom& g, const Work& w, const GenericIO& io, cudaStream_t st);
+cudaError_t generic_prepare(const Geom& g, const Work& w, const GenericIO& io, cudaStream_t st, int* nl);
 cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const GenericIO& io, int buf,
-                          cudaStream_t st);
+                          cudaStream_t st, int* nl);
 cudaError_t generic_cache_out(const Geom& g, const GenericIO& io, float* tmp, void* k_out, void* v_out,
-                              float* g_out, cudaStream_t st);
+                              float* g_out, cudaStream_t st, int* nl);
 size_t generic_smem_grad(const Geom& g);
 size_t generic_smem_readout(const Geom& g);
 size_t generic_smem_ns(const Geom& g, int m);

@@ -22,6 +22,7 @@ struct atlas_mem_handle {
   int* status = nullptr;  // device status word (inside ws)
   cudaStream_t last_stream = nullptr;
   bool launched = false;
+  int launches = 0;       // kernel launches of the last forward
   std::string err;
 };
 
@@ -182,6 +183,8 @@ extern "C" void atlas_mem_destroy(atlas_mem_handle* h) {
   delete h;
 }
 
+extern "C" int atlas_mem_last_launches(const atlas_mem_handle* h) { return h ? h->launches : 0; }
+
 extern "C" const char* atlas_mem_last_error(const atlas_mem_handle* h) {
   return h ? h->err.c_str() : g_create_err.c_str();
 }
@@ -262,7 +265,8 @@ extern "C" int atlas_mem_forward(atlas_mem_handle* h, const atlas_mem_io* io, vo
   }
   GenericIO gio{io->q, io->k, io->v, io->P, io->win_len ? io->win_k : nullptr, io->win_len ? io->win_v : nullptr,
                 io->theta, io->eta, io->alpha, io->gamma, io->win_len ? io->win_gamma : nullptr, io->y};
-  CUDA_TRY(generic_prepare(g, w, gio, st));
+  int nl = 0;
+  CUDA_TRY(generic_prepare(g, w, gio, st, &nl));
   int buf = 0;
   for (int s = 0; s < g.T; s += g.C) {
     Chunk ch;
@@ -271,7 +275,7 @@ extern "C" int atlas_mem_forward(atlas_mem_handle* h, const atlas_mem_io* io, vo
     ch.lo = s - g.c + 1;
     if (ch.lo < -g.n_prev) ch.lo = -g.n_prev;
     ch.nw = ch.e - ch.lo;
-    CUDA_TRY(generic_chunk(g, ch, w, gio, buf, st));
+    CUDA_TRY(generic_chunk(g, ch, w, gio, buf, st, &nl));
     buf ^= 1;
   }
   for (int m = 0; m < g.nmat; ++m) {
@@ -280,7 +284,8 @@ extern "C" int atlas_mem_forward(atlas_mem_handle* h, const atlas_mem_io* io, vo
     CUDA_TRY(cudaMemcpyAsync(io->S_out[m], w.Sst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
   }
   if (g.c > 1 && (io->win_k_out || io->win_v_out || io->win_gamma_out))
-    CUDA_TRY(generic_cache_out(g, gio, cache_tmp, io->win_k_out, io->win_v_out, io->win_gamma_out, st));
+    CUDA_TRY(generic_cache_out(g, gio, cache_tmp, io->win_k_out, io->win_v_out, io->win_gamma_out, st, &nl));
+  h->launches = nl;
   h->last_stream = st;
   h->launched = true;
   return ATLAS_OK;

@@ -519,7 +519,8 @@ __global__ void k_cache_scatter(Geom g, const float* tmp, void* k_out, void* v_o
 // ------------------------------------------------------------------ driver
 static inline unsigned cdiv(size_t a, size_t b) { return (unsigned)((a + b - 1) / b); }
 
-cudaError_t generic_prepare(const Geom& g, const Work& w, const GenericIO& io, cudaStream_t st) {
+cudaError_t generic_prepare(const Geom& g, const Work& w, const GenericIO& io, cudaStream_t st, int* nl) {
+  *nl += 3;
   const size_t sm_feat = (size_t)(g.d_k + (g.proj_dim ? g.poly : 0)) * sizeof(float);
   if (sm_feat > 48 * 1024) cudaFuncSetAttribute(k_features, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_feat);
   k_features<<<dim3(g.L, g.units), 128, sm_feat, st>>>(g, io.k, io.win_k, g.L, 1, io.P, w.X);
@@ -542,7 +543,8 @@ size_t generic_smem_ns(const Geom& g, int m) {
 }
 
 cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const GenericIO& io, int buf,
-                          cudaStream_t st) {
+                          cudaStream_t st, int* nl) {
+  *nl += g.ns_iters == 0 ? 3 + g.nmat : 3 + 2 * g.nmat;
   const size_t sg = generic_smem_grad(g), sr = generic_smem_readout(g);
   cudaFuncSetAttribute(k_grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg);
   k_grad<<<dim3(ch.nw, g.units), 256, sg, st>>>(g, ch, w, buf);
@@ -579,8 +581,9 @@ cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const G
 }
 
 cudaError_t generic_cache_out(const Geom& g, const GenericIO& io, float* tmp, void* k_out, void* v_out,
-                              float* g_out, cudaStream_t st) {
+                              float* g_out, cudaStream_t st, int* nl) {
   if (g.c <= 1) return cudaSuccess;
+  *nl += 2;
   k_cache_gather<<<dim3(g.c - 1, g.units), 128, 0, st>>>(g, io.k, io.v, io.gamma, io.win_k, io.win_v, io.win_gamma,
                                                          tmp);
   k_cache_scatter<<<dim3(g.c - 1, g.units), 128, 0, st>>>(g, tmp, k_out, v_out, g_out);
