@@ -118,6 +118,35 @@ int atlas_mem_forward(atlas_mem_handle* h, const atlas_mem_io* io, void* stream)
  * cache back and synchronises `stream` before returning. */
 int atlas_mem_forward_host(atlas_mem_handle* h, const atlas_mem_io* io, void* stream);
 
+/* Size of the fixed device scratch of atlas_mem_forward_noalloc: 16 MiB. */
+#define ATLAS_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
+
+/* atlas_mem_forward for callers that must not allocate device memory.
+ *
+ * No counterpart in the pages: this is a deployment variant.  Some hosts
+ * cannot let a library call cudaMalloc: a framework whose pool allocator owns
+ * the device memory (a raw cudaMalloc would fail or fragment its pool), or a
+ * serving loop that forbids allocation after start-up because cudaMalloc may
+ * synchronise the device and stall other streams.  This entry point runs the
+ * same forward as atlas_mem_forward (same arguments, device pointers, same
+ * results) but takes its working memory from a fixed array of
+ * ATLAS_NOALLOC_SCRATCH_BYTES that lives in the library's device image, and
+ * calls no cudaMalloc, cudaFree or allocating library routine.  The caller
+ * still passes every input and output buffer.
+ *
+ * - Calls whose working set exceeds the array (atlas_mem_workspace_bytes(h,
+ *   B, H, T) > ATLAS_NOALLOC_SCRATCH_BYTES) return ATLAS_ERR_UNSUPPORTED with
+ *   a message giving both sizes; nothing is launched.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ * - Every call, from every handle, shares the one array per device and finds
+ *   the previous call's contents there (the status word is cleared on each
+ *   call).  Calls whose work overlaps on the GPU race on it: serialise them
+ *   (one stream, or events between streams).
+ * - Every GPU that loads the library holds the array until the process exits. */
+int atlas_mem_forward_noalloc(atlas_mem_handle* h, const atlas_mem_io* io, void* stream);
+
 /* Wait for the last forward on this handle and return its device status
  * (ATLAS_OK or ATLAS_ERR_TIMEOUT).  Clears the status word. */
 int atlas_mem_status(atlas_mem_handle* h);

@@ -18,7 +18,8 @@ ATLAS_F32, ATLAS_BF16 = 0, 1
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "OOM", 5: "TIMEOUT"}
 
 # exported symbols, as declared in include/atlas_mem.h
-EXPORTS = ("atlas_mem_create", "atlas_mem_forward", "atlas_mem_forward_host", "atlas_mem_status",
+EXPORTS = ("atlas_mem_create", "atlas_mem_forward", "atlas_mem_forward_host", "atlas_mem_forward_noalloc",
+           "atlas_mem_status",
            "atlas_mem_workspace_bytes", "atlas_mem_last_launches", "atlas_mem_last_error", "atlas_mem_destroy")
 
 
@@ -64,7 +65,7 @@ def load(path: str = LIB_PATH):
     lib = ctypes.CDLL(path)
     lib.atlas_mem_create.argtypes = [ctypes.POINTER(atlas_mem_config), ctypes.POINTER(ctypes.c_void_p)]
     lib.atlas_mem_create.restype = ctypes.c_int
-    for name in ("atlas_mem_forward", "atlas_mem_forward_host"):
+    for name in ("atlas_mem_forward", "atlas_mem_forward_host", "atlas_mem_forward_noalloc"):
         fn = getattr(lib, name)
         fn.argtypes = [ctypes.c_void_p, ctypes.POINTER(atlas_mem_io), ctypes.c_void_p]
         fn.restype = ctypes.c_int
@@ -102,6 +103,14 @@ def atlas_mem_forward(h, io: atlas_mem_io, stream: int = 0):
 def atlas_mem_forward_host(h, io: atlas_mem_io, stream: int = 0):
     lib = load()
     rc = lib.atlas_mem_forward_host(h, ctypes.byref(io), ctypes.c_void_p(stream))
+    if rc:
+        raise AtlasError(rc, lib.atlas_mem_last_error(h).decode())
+
+
+def atlas_mem_forward_noalloc(h, io: atlas_mem_io, stream: int = 0):
+    """atlas_mem_forward without any device allocation (fixed scratch)."""
+    lib = load()
+    rc = lib.atlas_mem_forward_noalloc(h, ctypes.byref(io), ctypes.c_void_p(stream))
     if rc:
         raise AtlasError(rc, lib.atlas_mem_last_error(h).decode())
 

@@ -5,6 +5,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
 #include <string>
 
 #include "atlas_common.cuh"
@@ -385,4 +386,90 @@ extern "C" int atlas_mem_forward_host(atlas_mem_handle* h, const atlas_mem_io* i
       CUDA_TRY(cudaMemcpyAsync(items[j].dst_host, dptr[j], items[j].bytes, cudaMemcpyDeviceToHost, st));
   CUDA_TRY(cudaStreamSynchronize(st));
   return atlas_mem_status(h);
+}
+
+// -------------------------------------------------- no-allocation variant
+// Scratch for atlas_mem_forward_noalloc: a fixed device array, so that the
+// entry point never allocates.  Every GPU that loads this library holds it
+// until the process exits.  In host code this name is only a stand-in: the
+// kernels get the device address from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ATLAS_NOALLOC_SCRATCH_BYTES];
+
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_ptr[256];  // device address of the scratch, per device ordinal
+
+// Once per device, with that device current: look up the array's device
+// address.  Runs inside the first atlas_mem_forward_noalloc call on a device.
+static int noalloc_scratch(atlas_mem_handle* h, void** out) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 256) return fail(h, ATLAS_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(h, ATLAS_ERR_CUDA, "cudaGetSymbolAddress(fixed scratch) on device %d: %s", dev,
+                  cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return ATLAS_OK;
+}
+
+extern "C" int atlas_mem_forward_noalloc(atlas_mem_handle* h, const atlas_mem_io* io, void* stream) {
+  if (!h) return ATLAS_ERR_INVALID_ARG;
+  int rc = check_io(h, io);
+  if (rc) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  Geom g = h->base;
+  g.units = io->B * io->H;
+  g.T = io->T;
+  g.n_prev = io->win_len;
+  g.L = g.n_prev + g.T;
+  const Layout L = layout(g, g.units, g.T);
+  if (L.total > (size_t)ATLAS_NOALLOC_SCRATCH_BYTES)
+    return fail(h, ATLAS_ERR_UNSUPPORTED,
+                "this call needs %zu bytes of scratch but atlas_mem_forward_noalloc has a fixed %zu bytes; "
+                "use fewer units or tokens per call, or atlas_mem_forward",
+                L.total, (size_t)ATLAS_NOALLOC_SCRATCH_BYTES);
+  void* base = nullptr;
+  rc = noalloc_scratch(h, &base);
+  if (rc) return rc;
+  float* cache_tmp = nullptr;
+  Work w = work_from(g, base, L, &cache_tmp);
+  // the scratch keeps the previous call's contents: the status word must start at 0
+  CUDA_TRY(cudaMemsetAsync(w.status, 0, sizeof(int), st));
+  h->status = w.status;
+  for (int m = 0; m < g.nmat; ++m) {
+    const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
+    CUDA_TRY(cudaMemcpyAsync(w.Wst[0][m], io->W0[m], bytes, cudaMemcpyDeviceToDevice, st));
+    CUDA_TRY(cudaMemcpyAsync(w.Sst[0][m], io->S0[m], bytes, cudaMemcpyDeviceToDevice, st));
+  }
+  GenericIO gio{io->q, io->k, io->v, io->P, io->win_len ? io->win_k : nullptr, io->win_len ? io->win_v : nullptr,
+                io->theta, io->eta, io->alpha, io->gamma, io->win_len ? io->win_gamma : nullptr, io->y};
+  int nl = 0;
+  CUDA_TRY(generic_prepare(g, w, gio, st, &nl));
+  int buf = 0;
+  for (int s = 0; s < g.T; s += g.C) {
+    Chunk ch;
+    ch.s = s;
+    ch.e = s + g.C;
+    ch.lo = s - g.c + 1;
+    if (ch.lo < -g.n_prev) ch.lo = -g.n_prev;
+    ch.nw = ch.e - ch.lo;
+    CUDA_TRY(generic_chunk(g, ch, w, gio, buf, st, &nl));
+    buf ^= 1;
+  }
+  for (int m = 0; m < g.nmat; ++m) {
+    const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
+    CUDA_TRY(cudaMemcpyAsync(io->W_out[m], w.Wst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
+    CUDA_TRY(cudaMemcpyAsync(io->S_out[m], w.Sst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
+  }
+  if (g.c > 1 && (io->win_k_out || io->win_v_out || io->win_gamma_out))
+    CUDA_TRY(generic_cache_out(g, gio, cache_tmp, io->win_k_out, io->win_v_out, io->win_gamma_out, st, &nl));
+  h->launches = nl;
+  h->last_stream = st;
+  h->launched = true;
+  return ATLAS_OK;
 }
