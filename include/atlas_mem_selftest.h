@@ -1,0 +1,27 @@
+/*
+ * atlas_mem_selftest.h -- self-test of the library's tensor-core building
+ * blocks.  No counterpart in the pages: it exists so that tests can check,
+ * on the GPU, the shared-memory operand layout, the tcgen05.mma instruction
+ * descriptor and the TMEM accumulator layout that every tensor-core kernel
+ * of the library relies on.
+ */
+#ifndef ATLAS_MEM_SELFTEST_H
+#define ATLAS_MEM_SELFTEST_H
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* D = A * B^T with one CTA: M in {64, 128}, 16 <= N <= 256, 16 <= K <= 128
+ * (multiples of 16).  A: device [M][K] 16-bit (bf16 if bf16 != 0 else fp16);
+ * B: device [N][K] (b_mn_major == 0) or [K][N] (b_mn_major != 0).
+ * raw_out: device [128][N] fp32, the raw accumulator of all 128 TMEM lanes.
+ * status: device int, set to 1 if the kernel's bounded wait gave up.
+ * Asynchronous on `stream`; returns ATLAS_OK (0), ATLAS_ERR_INVALID_ARG (1)
+ * or ATLAS_ERR_CUDA (3). */
+int atlas_mem_selftest_mma(int M, int N, int K, int b_mn_major, int bf16, const void* A, const void* B,
+                           float* raw_out, int* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,72 @@
+// Self-test of the tensor-core building blocks (tc.cuh): one tcgen05.mma
+// chain D = A * B^T from shared-memory operands in the core-matrix layout,
+// dumped raw from all 128 TMEM lanes so that a test can check the
+// accumulator layout for M = 64 and M = 128 against a plain matmul.
+#include "atlas_common.cuh"
+#include "tc.cuh"
+
+namespace atlas {
+
+__global__ void __launch_bounds__(128) k_selftest_mma(int M, int N, int K, int b_mn, int bf16, const uint16_t* A,
+                                                      const uint16_t* B, float* raw, int* status) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tbase;
+  uint8_t* As = sm;
+  uint8_t* Bs = sm + (size_t)M * K * 2;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (warp == 0) tc::tmem_alloc(&tbase, 256);
+  if (threadIdx.x == 0) tc::mbar_init(&bar, 1);
+  const int rgsK = (K / 8) * 128, rgsN = (N / 8) * 128;
+  for (int e = threadIdx.x; e < M * K; e += blockDim.x)
+    *(uint16_t*)(As + tc::core_offset(e / K, e % K, rgsK)) = A[e];
+  for (int e = threadIdx.x; e < N * K; e += blockDim.x) {
+    if (b_mn) *(uint16_t*)(Bs + tc::core_offset(e / N, e % N, rgsN)) = B[e];   // B stored [K][N]
+    else *(uint16_t*)(Bs + tc::core_offset(e / K, e % K, rgsK)) = B[e];        // B stored [N][K]
+  }
+  tc::fence_smem_to_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t d = tbase;
+  if (threadIdx.x == 0) {
+    const uint32_t idesc = tc::idesc_f16(M, N, bf16, 0, b_mn);
+    for (int ks = 0; ks < K / 16; ++ks) {
+      const uint64_t ad = tc::sdesc(tc::smem_u32(As) + ks * 256, 128, rgsK);
+      const uint64_t bd = b_mn ? tc::sdesc(tc::smem_u32(Bs) + ks * 2 * rgsN, rgsN, 128)
+                               : tc::sdesc(tc::smem_u32(Bs) + ks * 256, 128, rgsK);
+      tc::mma_f16(d, ad, bd, idesc, ks > 0);
+    }
+    tc::mma_commit(&bar);
+  }
+  const bool ok = tc::mbar_wait(&bar, 0, 1ll << 30);
+  tc::fence_after_sync();
+  if (!ok) {
+    if (threadIdx.x == 0) atomicExch(status, 1);
+  } else {
+    for (int c = 0; c < N; c += 16) {
+      float v[16];
+      tc::tmem_ld16(d + ((uint32_t)(32 * warp) << 16) + c, v);
+      tc::tmem_ld_wait();
+      for (int i = 0; i < 16; ++i) raw[(size_t)(32 * warp + lane) * N + c + i] = v[i];
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tbase, 256);
+}
+
+}  // namespace atlas
+
+extern "C" int atlas_mem_selftest_mma(int M, int N, int K, int b_mn_major, int bf16, const void* A, const void* B,
+                                      float* raw_out, int* status, void* stream) {
+  using namespace atlas;
+  if (!(M == 64 || M == 128) || N < 16 || N > 256 || N % 16 || K < 16 || K > 128 || K % 16 || !A || !B ||
+      !raw_out || !status)
+    return ATLAS_ERR_INVALID_ARG;
+  const int smem = 200 * 1024;  // generous: any descriptor misreading stays inside
+  cudaFuncSetAttribute(k_selftest_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  k_selftest_mma<<<1, 128, smem, (cudaStream_t)stream>>>(M, N, K, b_mn_major, bf16, (const uint16_t*)A,
+                                                         (const uint16_t*)B, raw_out, status);
+  return cudaGetLastError() == cudaSuccess ? ATLAS_OK : ATLAS_ERR_CUDA;
+}

@@ -1,0 +1,151 @@
+// Blackwell (sm_103a) tensor-core building blocks: TMEM allocation, shared
+// memory matrix descriptors, tcgen05.mma (kind::f16, fp32 accumulate),
+// commit to an mbarrier, bounded mbarrier waits and TMEM loads.
+//
+// Operand tiles in shared memory use the canonical no-swizzle layout made of
+// 8x8 "core matrices" (8 rows of 16 bytes, 128 contiguous bytes).  Element
+// (r, k) of an R x K tile of 16-bit values sits at byte
+//     (r / 8) * row_group_stride + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2
+// with row_group_stride = (K / 8) * 128.  The same bytes serve as a K-major
+// operand (rows = M or N, columns = K) or, read the other way, as an
+// MN-major operand (rows = K, columns = N).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint32_t core_offset(int r, int k, int row_group_stride) {
+  return (uint32_t)((r >> 3) * row_group_stride + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
+
+// ---------------------------------------------------------------- TMEM
+// Executed by one full warp.  Writes the TMEM base address to *dst.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// generic-proxy shared-memory writes -> visible to the tensor core (async proxy)
+__device__ __forceinline__ void fence_smem_to_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------- descriptors
+// Shared-memory matrix descriptor, no swizzle.  lbo: byte stride between
+// core matrices along K; sbo: byte stride between core matrices along M/N.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
+  return d;                // base offset 0, relative LBO, no swizzle
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16 with fp32 accumulation.
+// bf16 = 1: A and B are bf16, else fp16.  *_mn: operand is MN-major.
+__host__ __device__ __forceinline__ uint32_t idesc_f16(int M, int N, int bf16, int a_mn, int b_mn) {
+  uint32_t d = 0;
+  d |= 1u << 4;                          // D = f32
+  d |= (uint32_t)(bf16 ? 1 : 0) << 7;    // A type
+  d |= (uint32_t)(bf16 ? 1 : 0) << 10;   // B type
+  d |= (uint32_t)(a_mn ? 1 : 0) << 15;   // A major-ness
+  d |= (uint32_t)(b_mn ? 1 : 0) << 16;   // B major-ness
+  d |= (uint32_t)(N >> 3) << 17;
+  d |= (uint32_t)(M >> 4) << 24;
+  return d;
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one instruction (K = 16), issued by one thread.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on *bar once every previously issued MMA of this thread completes.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// ------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of *bar to complete; gives up after max_cycles and
+// returns false (the caller records the timeout and unwinds).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long max_cycles) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > max_cycles) return false;
+  }
+  return true;
+}
+
+// ----------------------------------------------------------- TMEM loads
+// 32 lanes x 16 consecutive 32-bit columns: thread (lane) gets 16 values of
+// its TMEM lane.  taddr = base + ((32 * (warp % 4)) << 16) + column.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------ bf16 split
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): the pair carries 16
+// significant bits, and hi*hi' + hi*lo' + lo*hi' reproduces a product to
+// about 2^-16 relative (the dropped lo*lo' term is ~2^-18).
+__device__ __forceinline__ uint16_t f2bf(float x) {
+  uint32_t u = __float_as_uint(x);
+  u += 0x7FFFu + ((u >> 16) & 1u);  // round to nearest even (finite inputs)
+  return (uint16_t)(u >> 16);
+}
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+__device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) {
+  hi = f2bf(x);
+  lo = f2bf(x - bf2f(hi));
+}
+
+}  // namespace tc

@@ -1,0 +1,53 @@
+"""GPU self-test of the tcgen05 building blocks: shared-memory descriptors
+(K-major and MN-major operands), the kind::f16 instruction descriptor (bf16
+and fp16) and the TMEM accumulator layout for M = 64 and M = 128, against a
+float64 matmul of the same 16-bit values."""
+import ctypes
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+
+def _lanes_m64():
+    """Accumulator rows of an M = 64 MMA by TMEM lane: 16 rows in each of the
+    four 32-lane sub-partitions."""
+    return [32 * (r // 16) + r % 16 for r in range(64)]
+
+
+@pytest.mark.parametrize("M,N,K,b_mn,bf16", [
+    (128, 128, 64, 0, 1), (128, 256, 64, 1, 1), (128, 64, 128, 0, 0), (128, 128, 32, 1, 0),
+    (64, 64, 64, 0, 1), (64, 256, 64, 1, 1), (64, 128, 128, 1, 0),
+])
+def test_mma_layouts(gpu_lib, M, N, K, b_mn, bf16):
+    import torch
+    lib = gpu_lib.load()
+    lib.atlas_mem_selftest_mma.argtypes = [ctypes.c_int] * 5 + [ctypes.c_void_p] * 5
+    lib.atlas_mem_selftest_mma.restype = ctypes.c_int
+    g = torch.Generator().manual_seed(M * 1000 + N + K)
+    dt = torch.bfloat16 if bf16 else torch.float16
+    A = torch.randn(M, K, generator=g).to(dt)
+    Bm = torch.randn(N, K, generator=g).to(dt)
+    ref = A.double() @ Bm.double().T
+    Bdev = (Bm.T.contiguous() if b_mn else Bm).cuda()
+    Adev = A.cuda()
+    raw = torch.full((128, N), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = lib.atlas_mem_selftest_mma(M, N, K, b_mn, bf16, Adev.data_ptr(), Bdev.data_ptr(), raw.data_ptr(),
+                                    st.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert st.item() == 0, "bounded wait gave up"
+    raw = raw.double().cpu()
+    lanes = list(range(128)) if M == 128 else _lanes_m64()
+    got = raw[lanes]
+    err = (got - ref).abs().max().item() / ref.abs().max().item()
+    if err > 1e-6:
+        # report where the rows landed to help read the layout
+        hits = {}
+        for r in range(M):
+            d = (raw - ref[r]).abs().max(dim=1).values
+            hits[r] = int(d.argmin())
+        print("row -> lane", hits)
+    assert err < 1e-6, err
