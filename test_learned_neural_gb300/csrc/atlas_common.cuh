@@ -86,5 +86,11 @@ cudaError_t generic_cache_out(const Geom& g, const GenericIO& io, float* tmp, vo
 size_t generic_smem_grad(const Geom& g);
 size_t generic_smem_readout(const Geom& g);
 size_t generic_smem_ns(const Geom& g, int m);
+int num_sms();
+
+// tensor-core Newton-Schulz (k_ns_tc.cu)
+bool ns_tc_supported(const Geom& g);
+cudaError_t ns_tc_launch(const Geom& g, const Chunk& ch, const Work& w, int buf, size_t slot_stride, int num_sms,
+                         cudaStream_t st);
 
 }  // namespace atlas

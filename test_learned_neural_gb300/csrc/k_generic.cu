@@ -519,6 +519,25 @@ __global__ void k_cache_scatter(Geom g, const float* tmp, void* k_out, void* v_o
 // ------------------------------------------------------------------ driver
 static inline unsigned cdiv(size_t a, size_t b) { return (unsigned)((a + b - 1) / b); }
 
+#define CUDA_CHECK_RET(x)            \
+  do {                               \
+    cudaError_t e_ = (x);            \
+    if (e_ != cudaSuccess) return e_; \
+  } while (0)
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
 cudaError_t generic_prepare(const Geom& g, const Work& w, const GenericIO& io, cudaStream_t st, int* nl) {
   *nl += 3;
   const size_t sm_feat = (size_t)(g.d_k + (g.proj_dim ? g.poly : 0)) * sizeof(float);
@@ -562,6 +581,10 @@ cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const G
   size_t slot_stride = 0;
   for (int m = 0; m < g.nmat; ++m) slot_stride += (size_t)g.rows[m] * g.cols[m];
   size_t off = 0;
+  if (ns_tc_supported(g)) {
+    CUDA_CHECK_RET(ns_tc_launch(g, ch, w, buf, slot_stride, num_sms(), st));
+    *nl -= g.nmat - 1;   // one tensor-core launch covers every matrix
+  } else
   for (int m = 0; m < g.nmat; ++m) {
     const size_t sn = generic_smem_ns(g, m);
     cudaFuncSetAttribute(k_ns_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sn);
