@@ -12,14 +12,15 @@ extern "C" {
 #endif
 
 /* D = A * B^T with one CTA: M in {64, 128}, 16 <= N <= 256, 16 <= K <= 128
- * (multiples of 16).  A: device [M][K] 16-bit (bf16 if bf16 != 0 else fp16);
+ * (multiples of 16).  A: device 16-bit (bf16 if bf16 != 0 else fp16), [M][K]
+ * (a_mn_major == 0, K-major operand) or [K][M] (a_mn_major != 0, MN-major);
  * B: device [N][K] (b_mn_major == 0) or [K][N] (b_mn_major != 0).
  * raw_out: device [128][N] fp32, the raw accumulator of all 128 TMEM lanes.
  * status: device int, set to 1 if the kernel's bounded wait gave up.
  * Asynchronous on `stream`; returns ATLAS_OK (0), ATLAS_ERR_INVALID_ARG (1)
  * or ATLAS_ERR_CUDA (3). */
-int atlas_mem_selftest_mma(int M, int N, int K, int b_mn_major, int bf16, const void* A, const void* B,
-                           float* raw_out, int* status, void* stream);
+int atlas_mem_selftest_mma(int M, int N, int K, int a_mn_major, int b_mn_major, int bf16, const void* A,
+                           const void* B, float* raw_out, int* status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -88,6 +88,13 @@ size_t generic_smem_readout(const Geom& g);
 size_t generic_smem_ns(const Geom& g, int m);
 int num_sms();
 
+// fused tensor-core MLP memory without Newton-Schulz (k_mlp_tc.cu)
+bool mlp_tc_supported(const Geom& g);
+cudaError_t mlp_tc_launch(const Geom& g, const void* q, const void* k, const void* v, const float* theta,
+                          const float* eta, const float* alpha, const float* gamma, const float* const* W0,
+                          const float* const* S0, float* y, float* const* W_out, float* const* S_out, int* status,
+                          cudaStream_t st);
+
 // tensor-core Newton-Schulz (k_ns_tc.cu)
 bool ns_tc_supported(const Geom& g);
 cudaError_t ns_tc_launch(const Geom& g, const Chunk& ch, const Work& w, int buf, size_t slot_stride, int num_sms,

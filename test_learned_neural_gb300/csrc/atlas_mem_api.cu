@@ -259,6 +259,15 @@ extern "C" int atlas_mem_forward(atlas_mem_handle* h, const atlas_mem_io* io, vo
   float* cache_tmp = nullptr;
   Work w = work_from(g, h->ws, L, &cache_tmp);
   h->status = w.status;
+  if (mlp_tc_supported(g)) {
+    // fused tensor-core kernel: state in/out and read-out in one launch
+    CUDA_TRY(mlp_tc_launch(g, io->q, io->k, io->v, io->theta, io->eta, io->alpha, io->gamma, io->W0, io->S0, io->y,
+                           io->W_out, io->S_out, w.status, st));
+    h->launches = 1;
+    h->last_stream = st;
+    h->launched = true;
+    return ATLAS_OK;
+  }
   for (int m = 0; m < g.nmat; ++m) {
     const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
     CUDA_TRY(cudaMemcpyAsync(w.Wst[0][m], io->W0[m], bytes, cudaMemcpyDeviceToDevice, st));

@@ -1,0 +1,528 @@
+// Fused chunked forward of the residual SiLU MLP memory without
+// Newton-Schulz, on the tensor cores: memory width d = 64, hidden 256,
+// chunks of C = 64 tokens, Omega window c = 1 (the Titans memory of
+// titans-pytorch-mlx README, Eq. 12-14, with gradients taken at the chunk
+// start, ATLAS summary Section 3.3, and post-update read-out, atlas-torch
+// README "Known deviations from the paper's MAC").
+//
+// One cluster of 4 CTAs per (batch, head) unit; CTA q owns the hidden slice
+// [64q, 64q + 64): W1[:, slice] (d x 64), W2[slice, :] (64 x d) and the same
+// slices of S.  The kernel is persistent over the unit's chunks, so the fp32
+// state never leaves shared memory.  Per chunk, with row-vector tokens
+// (X keys, R queries, V values; Kw = C window rows since c = 1):
+//
+//   Z  = X W1q                      A = SiLU(Z)
+//   Yp = A W2q      -> summed over the 4 slices (DSMEM) -> dy = 2 gamma (X + sum - V)
+//   dz = (dy W2q^T) * SiLU'(Z)
+//   G1 = R X^T,  M1 = -Cw (.) G1
+//   Zq = B_t (R W1q) + D_t (R S1q) + M1 dz          Aq = SiLU(Zq)
+//   G2 = Aq A^T, M2 = -Cw (.) G2
+//   Yq = B_t (Aq W2q) + D_t (Aq S2q) + M2 dy  -> summed over slices (DSMEM)
+//   y  = R + sum_q Yq
+//   S1q <- A_e S1q - X^T diag(cs_e) dz,  W1q <- B_e W1q + D_e S1q - X^T diag(cw_e) dz
+//   S2q <- A_e S2q - A^T diag(cs_e) dy,  W2q <- B_e W2q + D_e S2q - A^T diag(cw_e) dy
+//
+// Cs, Cw, A_t, B_t, D_t are the momentum/decay coefficients of the chunk
+// (scans over eta and 1 - alpha, see k_generic.cu).  Every product is one
+// tcgen05.mma chain (M = 64, fp16 operands, fp32 accumulation in TMEM); the
+// operands live in shared memory in the core-matrix layout of tc.cuh, each
+// written once and read K-major or MN-major as the product needs.
+#include <cuda_fp16.h>
+
+#include "atlas_common.cuh"
+#include "tc.cuh"
+
+namespace atlas {
+namespace {
+
+constexpr int D = 64, HQ = 64, CS = 4, TOK = 64, NT = 256;
+constexpr int TILE = 64 * 64 * 2;       // fp16 64x64 operand tile
+constexpr int RGS = 1024;               // row-group stride of a 64-column tile
+constexpr int RGS2 = 2048;              // of a 128-column tile
+constexpr int F32T = 64 * 64 * 4;       // fp32 64x64 tile (swizzled rows)
+constexpr long long kWait = 1ll << 31;
+
+// shared-memory map (bytes)
+constexpr int W1F = 0, S1F = W1F + F32T, W2F = S1F + F32T, S2F = W2F + F32T;
+constexpr int OW1 = S2F + F32T, OS1 = OW1 + TILE, OW2 = OS1 + TILE, OS2 = OW2 + TILE;
+constexpr int OX = OS2 + TILE, OA = OX + TILE, ODY = OA + TILE, ODZ = ODY + TILE;
+constexpr int UNI = ODZ + TILE;                                   // phase-local operands
+constexpr int OR_ = UNI, OM1 = UNI + TILE, OAQ = UNI + 2 * TILE, OM2 = UNI + 3 * TILE;
+constexpr int ODZS = UNI, ODYS = UNI + 2 * TILE;                  // [cs.dz | cw.dz], [cs.dy | cw.dy]
+constexpr int OSP = UNI + 4 * TILE;                               // fp16 SiLU'(Z)
+constexpr int CWM = OSP + TILE;                                   // fp32 Cw[t][i]
+constexpr int RED = CWM + F32T;                                   // 2 fp32 tiles shared over the cluster
+constexpr int VEC = RED + 2 * F32T;                               // gate vectors
+constexpr int SMEM_BYTES = VEC + 12 * 64 * 4;
+
+// vectors inside VEC
+constexpr int V_TH = 0, V_ET = 64, V_BE = 128, V_GA = 192, V_AP = 256, V_BP = 320, V_DP = 384, V_CS = 448,
+              V_CW = 512;
+
+// TMEM columns
+constexpr uint32_t C_Z = 0, C_YP = 64, C_G1 = 128, C_P1 = 192, C_P2 = 256, C_P3 = 320, C_Q1 = 384, C_Q2 = 448;
+constexpr uint32_t C_G2 = 64, C_Q3 = 128, C_ST1 = 192, C_ST2 = 320;
+
+__device__ __forceinline__ int swz(int r, int c) { return r * 64 + (c ^ ((r & 7) << 2)); }
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t cta) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(cta));
+  return r;
+}
+__device__ __forceinline__ float4 ld_cluster4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void st_h8(uint8_t* tile, int rgs, int row, int col, const float* v) {
+  __half2 h[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4*>(tile + tc::core_offset(row, col, rgs)) = *reinterpret_cast<uint4*>(h);
+}
+__device__ __forceinline__ void ld_h8(const uint8_t* tile, int rgs, int row, int col, float* v) {
+  const uint4 u = *reinterpret_cast<const uint4*>(tile + tc::core_offset(row, col, rgs));
+  const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+
+// 64 x N (x K) product, fp16 operands, issued by one thread.
+__device__ __forceinline__ void mma64(uint32_t d, const uint8_t* a, int a_mn, int a_rgs, const uint8_t* b, int b_mn,
+                                      int b_rgs, int N, int K, bool accumulate) {
+  const uint32_t idesc = tc::idesc_f16(64, N, 0, a_mn, b_mn);
+  for (int ks = 0; ks < K / 16; ++ks) {
+    const uint64_t ad = a_mn ? tc::sdesc(tc::smem_u32(a) + ks * 2 * a_rgs, a_rgs, 128)
+                             : tc::sdesc(tc::smem_u32(a) + ks * 256, 128, a_rgs);
+    const uint64_t bd = b_mn ? tc::sdesc(tc::smem_u32(b) + ks * 2 * b_rgs, b_rgs, 128)
+                             : tc::sdesc(tc::smem_u32(b) + ks * 256, 128, b_rgs);
+    tc::mma_f16(d, ad, bd, idesc, (ks > 0 || accumulate) ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ void sync_smem_for_mma() {
+  tc::fence_smem_to_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+}
+
+__device__ __forceinline__ float ld_in(const void* p, size_t i, int dt) {
+  return dt == ATLAS_BF16 ? __uint_as_float(((uint32_t)((const uint16_t*)p)[i]) << 16) : ((const float*)p)[i];
+}
+
+struct Ctx {
+  uint64_t* bar;
+  uint32_t phase;
+  bool ok;
+};
+
+// commit the MMAs issued so far by thread 0 and wait for them (bounded)
+__device__ __forceinline__ void commit_wait(Ctx& c) {
+  if (threadIdx.x == 0 && c.ok) tc::mma_commit(c.bar);
+  bool good = true;
+  if (c.ok) good = tc::mbar_wait(c.bar, c.phase, kWait);
+  c.phase ^= 1;
+  const int failed = __syncthreads_or(!good);
+  if (failed) c.ok = false;
+  tc::fence_after_sync();
+}
+
+}  // namespace
+
+__global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
+    k_mlp_dual_tc(int T, int dt, const void* __restrict__ q, const void* __restrict__ k, const void* __restrict__ v,
+                  const float* __restrict__ theta, const float* __restrict__ eta, const float* __restrict__ alpha,
+                  const float* __restrict__ gamma, const float* W0a, const float* W0b, const float* S0a,
+                  const float* S0b, float* __restrict__ y, float* Woa, float* Wob, float* Soa, float* Sob,
+                  int* status) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tbase;
+  float* vec = reinterpret_cast<float*>(sm + VEC);
+  float* w1f = reinterpret_cast<float*>(sm + W1F);
+  float* s1f = reinterpret_cast<float*>(sm + S1F);
+  float* w2f = reinterpret_cast<float*>(sm + W2F);
+  float* s2f = reinterpret_cast<float*>(sm + S2F);
+  float* cwm = reinterpret_cast<float*>(sm + CWM);
+
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int sp = warp & 3, half = warp >> 2;
+  const bool act = lane < 16;                 // M = 64: rows live in lanes 0-15 of each sub-partition
+  const int row = 16 * sp + lane;             // accumulator row of this thread
+  const int c0 = 32 * half;                   // its 32 columns
+  const uint32_t lb = (uint32_t)(32 * sp) << 16;
+  const uint32_t qr = cluster_rank();
+  const int u = blockIdx.x / CS;
+  const int H = 4 * HQ;                       // hidden width
+
+  if (warp == 0) tc::tmem_alloc(&tbase, 512);
+  if (tid == 0) tc::mbar_init(&bar, 1);
+
+  // ---- state slices in: W1[:, 64q:64q+64] (d x 64), W2[64q:64q+64, :] (64 x d)
+  for (int e = tid; e < 64 * 64; e += NT) {
+    const int r = e / 64, c = e % 64;
+    const size_t i1 = ((size_t)u * D + r) * H + 64 * qr + c;
+    const size_t i2 = ((size_t)u * H + 64 * qr + r) * D + c;
+    w1f[swz(r, c)] = W0a[i1];
+    s1f[swz(r, c)] = S0a[i1];
+    w2f[swz(r, c)] = W0b[i2];
+    s2f[swz(r, c)] = S0b[i2];
+  }
+  __syncthreads();
+  for (int e = tid; e < 64 * 8; e += NT) {
+    const int r = e / 8, cc = (e % 8) * 8;
+    float a[8], b[8], c[8], d[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      a[i] = w1f[swz(r, cc + i)];
+      b[i] = s1f[swz(r, cc + i)];
+      c[i] = w2f[swz(r, cc + i)];
+      d[i] = s2f[swz(r, cc + i)];
+    }
+    st_h8(sm + OW1, RGS, r, cc, a);
+    st_h8(sm + OS1, RGS, r, cc, b);
+    st_h8(sm + OW2, RGS, r, cc, c);
+    st_h8(sm + OS2, RGS, r, cc, d);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  Ctx cx{&bar, 0u, true};
+  const uint32_t tb = tbase;
+  const uint32_t red_local = tc::smem_u32(sm + RED);
+
+  for (int s = 0; s < T; s += TOK) {
+    // ---------------------------------------------------------------- L
+    for (int e = tid; e < 64 * 8; e += NT) {
+      const int r = e / 8, cc = (e % 8) * 8;
+      float xk[8], xq[8];
+      const size_t base = ((size_t)u * T + s + r) * D + cc;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        xk[i] = ld_in(k, base + i, dt);
+        xq[i] = ld_in(q, base + i, dt);
+      }
+      st_h8(sm + OX, RGS, r, cc, xk);
+      st_h8(sm + OR_, RGS, r, cc, xq);
+    }
+    if (tid < 64) {
+      const size_t gi = (size_t)u * T + s + tid;
+      vec[V_TH + tid] = theta[gi];
+      vec[V_ET + tid] = eta[gi];
+      vec[V_BE + tid] = 1.f - alpha[gi];
+      vec[V_GA + tid] = gamma ? gamma[gi] : 1.f;
+    }
+    __syncthreads();
+    if (tid < 64) {  // column i = tid of Cs / Cw (window of token t is {t})
+      const int i = tid;
+      float cs = 0.f, cw = 0.f;
+      for (int t = 0; t < TOK; ++t) {
+        cs = vec[V_ET + t] * cs + (t == i ? vec[V_TH + t] : 0.f);
+        cw = vec[V_BE + t] * cw + cs;
+        cwm[swz(t, i)] = cw;
+      }
+      vec[V_CS + i] = cs;
+      vec[V_CW + i] = cw;
+    } else if (tid == 64) {
+      float Ap = 1.f, Bp = 1.f, Dp = 0.f;
+      for (int t = 0; t < TOK; ++t) {
+        Ap *= vec[V_ET + t];
+        Bp *= vec[V_BE + t];
+        Dp = vec[V_BE + t] * Dp + Ap;
+        vec[V_AP + t] = Ap;
+        vec[V_BP + t] = Bp;
+        vec[V_DP + t] = Dp;
+      }
+    }
+    sync_smem_for_mma();
+    // ---------------------------------------------------------------- 1: Z, G1
+    if (tid == 0 && cx.ok) {
+      mma64(tb + C_Z, sm + OX, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
+      mma64(tb + C_G1, sm + OR_, 0, RGS, sm + OX, 0, RGS, 64, 64, false);
+    }
+    commit_wait(cx);
+    for (int cc = 0; cc < 32; cc += 16) {
+      float z[16], g[16];
+      tc::tmem_ld16(tb + lb + C_Z + c0 + cc, z);
+      tc::tmem_ld16(tb + lb + C_G1 + c0 + cc, g);
+      tc::tmem_ld_wait();
+      if (act) {
+        float a[16], spv[16], m1[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float sg = 1.f / (1.f + __expf(-z[i]));
+          a[i] = z[i] * sg;
+          spv[i] = sg * (1.f + z[i] * (1.f - sg));
+          m1[i] = -cwm[swz(row, c0 + cc + i)] * g[i];
+        }
+        st_h8(sm + OA, RGS, row, c0 + cc, a);
+        st_h8(sm + OA, RGS, row, c0 + cc + 8, a + 8);
+        st_h8(sm + OSP, RGS, row, c0 + cc, spv);
+        st_h8(sm + OSP, RGS, row, c0 + cc + 8, spv + 8);
+        st_h8(sm + OM1, RGS, row, c0 + cc, m1);
+        st_h8(sm + OM1, RGS, row, c0 + cc + 8, m1 + 8);
+      }
+    }
+    sync_smem_for_mma();
+    // ---------------------------------------------------------------- 2: Yp = A W2q
+    if (tid == 0 && cx.ok) mma64(tb + C_YP, sm + OA, 0, RGS, sm + OW2, 1, RGS, 64, 64, false);
+    commit_wait(cx);
+    // cluster-shared buffers: RED holds this slice's Yp, RED + F32T its Yq.
+    // Yp(n+1) is written after the second cluster barrier of chunk n, when
+    // every peer has read Yp(n); Yq(n+1) after the first barrier of chunk
+    // n+1, when every peer has read Yq(n).
+    float* redb = reinterpret_cast<float*>(sm + RED);
+    for (int cc = 0; cc < 32; cc += 16) {
+      float yp[16];
+      tc::tmem_ld16(tb + lb + C_YP + c0 + cc, yp);
+      tc::tmem_ld_wait();
+      if (act)
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          *reinterpret_cast<float4*>(redb + swz(row, c0 + cc + i)) = make_float4(yp[i], yp[i + 1], yp[i + 2], yp[i + 3]);
+    }
+    cluster_sync();
+    // dy = 2 gamma (X + sum_q Yp_q - V): every CTA forms all of it
+    for (int e = tid; e < 64 * 16; e += NT) {
+      const int r = e / 16, cc = (e % 16) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int p = 0; p < CS; ++p) {
+        const uint32_t addr = mapa(red_local + (uint32_t)(swz(r, cc) * 4), p);
+        const float4 t4 = ld_cluster4(addr);
+        acc.x += t4.x; acc.y += t4.y; acc.z += t4.z; acc.w += t4.w;
+      }
+      const size_t gb = ((size_t)u * T + s + r) * D + cc;
+      const float g2 = 2.f * vec[V_GA + r];
+      const float dy[4] = {g2 * (ld_in(k, gb, dt) + acc.x - ld_in(v, gb, dt)),
+                           g2 * (ld_in(k, gb + 1, dt) + acc.y - ld_in(v, gb + 1, dt)),
+                           g2 * (ld_in(k, gb + 2, dt) + acc.z - ld_in(v, gb + 2, dt)),
+                           g2 * (ld_in(k, gb + 3, dt) + acc.w - ld_in(v, gb + 3, dt))};
+      __half2 h0 = __floats2half2_rn(dy[0], dy[1]), h1 = __floats2half2_rn(dy[2], dy[3]);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&h0);
+      pk.y = *reinterpret_cast<uint32_t*>(&h1);
+      *reinterpret_cast<uint2*>(sm + ODY + tc::core_offset(r, cc, RGS)) = pk;
+    }
+    sync_smem_for_mma();
+    // ---------------------------------------------------------------- 3: dz' = dy W2q^T
+    if (tid == 0 && cx.ok) mma64(tb + C_Z, sm + ODY, 0, RGS, sm + OW2, 0, RGS, 64, 64, false);
+    commit_wait(cx);
+    for (int cc = 0; cc < 32; cc += 16) {
+      float t[16];
+      tc::tmem_ld16(tb + lb + C_Z + c0 + cc, t);
+      tc::tmem_ld_wait();
+      if (act) {
+        float spv[16];
+        ld_h8(sm + OSP, RGS, row, c0 + cc, spv);
+        ld_h8(sm + OSP, RGS, row, c0 + cc + 8, spv + 8);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) t[i] *= spv[i];
+        st_h8(sm + ODZ, RGS, row, c0 + cc, t);
+        st_h8(sm + ODZ, RGS, row, c0 + cc + 8, t + 8);
+      }
+    }
+    sync_smem_for_mma();
+    // ---------------------------------------------------------------- 4: Zq parts
+    if (tid == 0 && cx.ok) {
+      mma64(tb + C_P1, sm + OR_, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
+      mma64(tb + C_P2, sm + OR_, 0, RGS, sm + OS1, 1, RGS, 64, 64, false);
+      mma64(tb + C_P3, sm + OM1, 0, RGS, sm + ODZ, 1, RGS, 64, 64, false);
+    }
+    commit_wait(cx);
+    {
+      const float Bt = vec[V_BP + row], Dt = vec[V_DP + row];
+      for (int cc = 0; cc < 32; cc += 16) {
+        float p1[16], p2[16], p3[16];
+        tc::tmem_ld16(tb + lb + C_P1 + c0 + cc, p1);
+        tc::tmem_ld16(tb + lb + C_P2 + c0 + cc, p2);
+        tc::tmem_ld16(tb + lb + C_P3 + c0 + cc, p3);
+        tc::tmem_ld_wait();
+        if (act) {
+          float aq[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float zq = Bt * p1[i] + Dt * p2[i] + p3[i];
+            aq[i] = zq / (1.f + __expf(-zq));
+          }
+          st_h8(sm + OAQ, RGS, row, c0 + cc, aq);
+          st_h8(sm + OAQ, RGS, row, c0 + cc + 8, aq + 8);
+        }
+      }
+    }
+    sync_smem_for_mma();
+    // ---------------------------------------------------------------- 5: G2, Aq W2q, Aq S2q
+    if (tid == 0 && cx.ok) {
+      mma64(tb + C_G2, sm + OAQ, 0, RGS, sm + OA, 0, RGS, 64, 64, false);
+      mma64(tb + C_Q1, sm + OAQ, 0, RGS, sm + OW2, 1, RGS, 64, 64, false);
+      mma64(tb + C_Q2, sm + OAQ, 0, RGS, sm + OS2, 1, RGS, 64, 64, false);
+    }
+    commit_wait(cx);
+    for (int cc = 0; cc < 32; cc += 16) {
+      float g[16];
+      tc::tmem_ld16(tb + lb + C_G2 + c0 + cc, g);
+      tc::tmem_ld_wait();
+      if (act) {
+        float m2[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m2[i] = -cwm[swz(row, c0 + cc + i)] * g[i];
+        st_h8(sm + OM2, RGS, row, c0 + cc, m2);
+        st_h8(sm + OM2, RGS, row, c0 + cc + 8, m2 + 8);
+      }
+    }
+    sync_smem_for_mma();
+    // ---------------------------------------------------------------- 6: Q3 = M2 dy, Yq
+    if (tid == 0 && cx.ok) mma64(tb + C_Q3, sm + OM2, 0, RGS, sm + ODY, 1, RGS, 64, 64, false);
+    commit_wait(cx);
+    float* redy = reinterpret_cast<float*>(sm + RED + F32T);
+    {
+      const float Bt = vec[V_BP + row], Dt = vec[V_DP + row];
+      for (int cc = 0; cc < 32; cc += 16) {
+        float q1[16], q2[16], q3[16];
+        tc::tmem_ld16(tb + lb + C_Q1 + c0 + cc, q1);
+        tc::tmem_ld16(tb + lb + C_Q2 + c0 + cc, q2);
+        tc::tmem_ld16(tb + lb + C_Q3 + c0 + cc, q3);
+        tc::tmem_ld_wait();
+        if (act)
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            float4 o;
+            o.x = Bt * q1[i] + Dt * q2[i] + q3[i];
+            o.y = Bt * q1[i + 1] + Dt * q2[i + 1] + q3[i + 1];
+            o.z = Bt * q1[i + 2] + Dt * q2[i + 2] + q3[i + 2];
+            o.w = Bt * q1[i + 3] + Dt * q2[i + 3] + q3[i + 3];
+            *reinterpret_cast<float4*>(redy + swz(row, c0 + cc + i)) = o;
+          }
+      }
+    }
+    // state-update operands (the read-out operands are dead): diag(cs|cw) dz, dy
+    for (int e = tid; e < 64 * 8; e += NT) {
+      const int r = e / 8, cc = (e % 8) * 8;
+      const float csr = vec[V_CS + r], cwr = vec[V_CW + r];
+      float dz[8], dy[8], t0[8], t1[8];
+      ld_h8(sm + ODZ, RGS, r, cc, dz);
+      ld_h8(sm + ODY, RGS, r, cc, dy);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { t0[i] = csr * dz[i]; t1[i] = cwr * dz[i]; }
+      st_h8(sm + ODZS, RGS2, r, cc, t0);
+      st_h8(sm + ODZS, RGS2, r, 64 + cc, t1);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { t0[i] = csr * dy[i]; t1[i] = cwr * dy[i]; }
+      st_h8(sm + ODYS, RGS2, r, cc, t0);
+      st_h8(sm + ODYS, RGS2, r, 64 + cc, t1);
+    }
+    cluster_sync();
+    // y rows [16q, 16q + 16): R + sum of the four slices' Yq
+    for (int e = tid; e < 16 * 16; e += NT) {
+      const int r = 16 * (int)qr + e / 16, cc = (e % 16) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int p = 0; p < CS; ++p) {
+        const uint32_t addr = mapa(red_local + (uint32_t)(F32T + swz(r, cc) * 4), p);
+        const float4 t4 = ld_cluster4(addr);
+        acc.x += t4.x; acc.y += t4.y; acc.z += t4.z; acc.w += t4.w;
+      }
+      const size_t gb = ((size_t)u * T + s + r) * D + cc;
+      float4 o;
+      o.x = ld_in(q, gb, dt) + acc.x;
+      o.y = ld_in(q, gb + 1, dt) + acc.y;
+      o.z = ld_in(q, gb + 2, dt) + acc.z;
+      o.w = ld_in(q, gb + 3, dt) + acc.w;
+      *reinterpret_cast<float4*>(y + gb) = o;
+    }
+    sync_smem_for_mma();
+    // ---------------------------------------------------------------- 7: state corrections
+    if (tid == 0 && cx.ok) {
+      mma64(tb + C_ST1, sm + OX, 1, RGS, sm + ODZS, 1, RGS2, 128, 64, false);   // X^T [cs dz | cw dz]
+      mma64(tb + C_ST2, sm + OA, 1, RGS, sm + ODYS, 1, RGS2, 128, 64, false);   // A^T [cs dy | cw dy]
+    }
+    commit_wait(cx);
+    {
+      const float Ae = vec[V_AP + 63], Be = vec[V_BP + 63], De = vec[V_DP + 63];
+      for (int mtx = 0; mtx < 2; ++mtx) {
+        float* wf = mtx ? w2f : w1f;
+        float* sf = mtx ? s2f : s1f;
+        uint8_t* ow = sm + (mtx ? OW2 : OW1);
+        uint8_t* os = sm + (mtx ? OS2 : OS1);
+        const uint32_t cb = mtx ? C_ST2 : C_ST1;
+        for (int cc = 0; cc < 32; cc += 16) {
+          float scr[16], wcr[16];
+          tc::tmem_ld16(tb + lb + cb + c0 + cc, scr);
+          tc::tmem_ld16(tb + lb + cb + 64 + c0 + cc, wcr);
+          tc::tmem_ld_wait();
+          if (act) {
+            float wn[16], sn[16];
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+              const float4 so = *reinterpret_cast<const float4*>(sf + swz(row, c0 + cc + i));
+              const float4 wo = *reinterpret_cast<const float4*>(wf + swz(row, c0 + cc + i));
+              const float sov[4] = {so.x, so.y, so.z, so.w}, wov[4] = {wo.x, wo.y, wo.z, wo.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                sn[i + j] = Ae * sov[j] - scr[i + j];
+                wn[i + j] = Be * wov[j] + De * sov[j] - wcr[i + j];
+              }
+              *reinterpret_cast<float4*>(sf + swz(row, c0 + cc + i)) = make_float4(sn[i], sn[i + 1], sn[i + 2], sn[i + 3]);
+              *reinterpret_cast<float4*>(wf + swz(row, c0 + cc + i)) = make_float4(wn[i], wn[i + 1], wn[i + 2], wn[i + 3]);
+            }
+            st_h8(ow, RGS, row, c0 + cc, wn);
+            st_h8(ow, RGS, row, c0 + cc + 8, wn + 8);
+            st_h8(os, RGS, row, c0 + cc, sn);
+            st_h8(os, RGS, row, c0 + cc + 8, sn + 8);
+          }
+        }
+      }
+    }
+    sync_smem_for_mma();
+  }
+
+  // ---- state slices out
+  for (int e = tid; e < 64 * 64; e += NT) {
+    const int r = e / 64, c = e % 64;
+    const size_t i1 = ((size_t)u * D + r) * H + 64 * qr + c;
+    const size_t i2 = ((size_t)u * H + 64 * qr + r) * D + c;
+    Woa[i1] = w1f[swz(r, c)];
+    Soa[i1] = s1f[swz(r, c)];
+    Wob[i2] = w2f[swz(r, c)];
+    Sob[i2] = s2f[swz(r, c)];
+  }
+  if (!cx.ok && tid == 0) atomicExch(status, ATLAS_ERR_TIMEOUT);
+  tc::fence_before_sync();
+  __syncthreads();
+  cluster_sync();   // no CTA leaves while a peer may still read its shared memory
+  if (warp == 0) tc::tmem_dealloc(tbase, 512);
+}
+
+bool mlp_tc_supported(const Geom& g) {
+  return g.depth == 2 && g.ns_iters == 0 && g.c == 1 && g.p == 1 && g.proj_dim == 0 && g.d_k == D &&
+         g.d_v == D && g.hidden == 4 * HQ && g.C == TOK && g.n_prev == 0 && g.T % TOK == 0;
+}
+
+cudaError_t mlp_tc_launch(const Geom& g, const void* q, const void* k, const void* v, const float* theta,
+                          const float* eta, const float* alpha, const float* gamma, const float* const* W0,
+                          const float* const* S0, float* y, float* const* W_out, float* const* S_out, int* status,
+                          cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(k_mlp_dual_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  k_mlp_dual_tc<<<g.units * CS, NT, SMEM_BYTES, st>>>(g.T, g.qkv_dtype, q, k, v, theta, eta, alpha, gamma, W0[0],
+                                                      W0[1], S0[0], S0[1], y, W_out[0], W_out[1], S_out[0],
+                                                      S_out[1], status);
+  return cudaGetLastError();
+}
+
+}  // namespace atlas

@@ -7,8 +7,8 @@
 
 namespace atlas {
 
-__global__ void __launch_bounds__(128) k_selftest_mma(int M, int N, int K, int b_mn, int bf16, const uint16_t* A,
-                                                      const uint16_t* B, float* raw, int* status) {
+__global__ void __launch_bounds__(128) k_selftest_mma(int M, int N, int K, int a_mn, int b_mn, int bf16,
+                                                      const uint16_t* A, const uint16_t* B, float* raw, int* status) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ uint64_t bar;
   __shared__ uint32_t tbase;
@@ -17,9 +17,11 @@ __global__ void __launch_bounds__(128) k_selftest_mma(int M, int N, int K, int b
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (warp == 0) tc::tmem_alloc(&tbase, 256);
   if (threadIdx.x == 0) tc::mbar_init(&bar, 1);
-  const int rgsK = (K / 8) * 128, rgsN = (N / 8) * 128;
-  for (int e = threadIdx.x; e < M * K; e += blockDim.x)
-    *(uint16_t*)(As + tc::core_offset(e / K, e % K, rgsK)) = A[e];
+  const int rgsK = (K / 8) * 128, rgsN = (N / 8) * 128, rgsM = (M / 8) * 128;
+  for (int e = threadIdx.x; e < M * K; e += blockDim.x) {
+    if (a_mn) *(uint16_t*)(As + tc::core_offset(e / M, e % M, rgsM)) = A[e];   // A stored [K][M]
+    else *(uint16_t*)(As + tc::core_offset(e / K, e % K, rgsK)) = A[e];        // A stored [M][K]
+  }
   for (int e = threadIdx.x; e < N * K; e += blockDim.x) {
     if (b_mn) *(uint16_t*)(Bs + tc::core_offset(e / N, e % N, rgsN)) = B[e];   // B stored [K][N]
     else *(uint16_t*)(Bs + tc::core_offset(e / K, e % K, rgsK)) = B[e];        // B stored [N][K]
@@ -30,9 +32,10 @@ __global__ void __launch_bounds__(128) k_selftest_mma(int M, int N, int K, int b
   tc::fence_after_sync();
   const uint32_t d = tbase;
   if (threadIdx.x == 0) {
-    const uint32_t idesc = tc::idesc_f16(M, N, bf16, 0, b_mn);
+    const uint32_t idesc = tc::idesc_f16(M, N, bf16, a_mn, b_mn);
     for (int ks = 0; ks < K / 16; ++ks) {
-      const uint64_t ad = tc::sdesc(tc::smem_u32(As) + ks * 256, 128, rgsK);
+      const uint64_t ad = a_mn ? tc::sdesc(tc::smem_u32(As) + ks * 2 * rgsM, rgsM, 128)
+                               : tc::sdesc(tc::smem_u32(As) + ks * 256, 128, rgsK);
       const uint64_t bd = b_mn ? tc::sdesc(tc::smem_u32(Bs) + ks * 2 * rgsN, rgsN, 128)
                                : tc::sdesc(tc::smem_u32(Bs) + ks * 256, 128, rgsK);
       tc::mma_f16(d, ad, bd, idesc, ks > 0);
@@ -58,15 +61,15 @@ __global__ void __launch_bounds__(128) k_selftest_mma(int M, int N, int K, int b
 
 }  // namespace atlas
 
-extern "C" int atlas_mem_selftest_mma(int M, int N, int K, int b_mn_major, int bf16, const void* A, const void* B,
-                                      float* raw_out, int* status, void* stream) {
+extern "C" int atlas_mem_selftest_mma(int M, int N, int K, int a_mn_major, int b_mn_major, int bf16, const void* A,
+                                      const void* B, float* raw_out, int* status, void* stream) {
   using namespace atlas;
   if (!(M == 64 || M == 128) || N < 16 || N > 256 || N % 16 || K < 16 || K > 128 || K % 16 || !A || !B ||
       !raw_out || !status)
     return ATLAS_ERR_INVALID_ARG;
   const int smem = 200 * 1024;  // generous: any descriptor misreading stays inside
   cudaFuncSetAttribute(k_selftest_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  k_selftest_mma<<<1, 128, smem, (cudaStream_t)stream>>>(M, N, K, b_mn_major, bf16, (const uint16_t*)A,
+  k_selftest_mma<<<1, 128, smem, (cudaStream_t)stream>>>(M, N, K, a_mn_major, b_mn_major, bf16, (const uint16_t*)A,
                                                          (const uint16_t*)B, raw_out, status);
   return cudaGetLastError() == cudaSuccess ? ATLAS_OK : ATLAS_ERR_CUDA;
 }

@@ -16,14 +16,15 @@ def _lanes_m64():
     return [32 * (r // 16) + r % 16 for r in range(64)]
 
 
-@pytest.mark.parametrize("M,N,K,b_mn,bf16", [
-    (128, 128, 64, 0, 1), (128, 256, 64, 1, 1), (128, 64, 128, 0, 0), (128, 128, 32, 1, 0),
-    (64, 64, 64, 0, 1), (64, 256, 64, 1, 1), (64, 128, 128, 1, 0),
+@pytest.mark.parametrize("M,N,K,a_mn,b_mn,bf16", [
+    (128, 128, 64, 0, 0, 1), (128, 256, 64, 0, 1, 1), (128, 64, 128, 0, 0, 0), (128, 128, 32, 0, 1, 0),
+    (64, 64, 64, 0, 0, 1), (64, 256, 64, 0, 1, 1), (64, 128, 128, 0, 1, 0),
+    (64, 64, 64, 1, 1, 0), (64, 128, 64, 1, 1, 0), (128, 64, 64, 1, 0, 1),
 ])
-def test_mma_layouts(gpu_lib, M, N, K, b_mn, bf16):
+def test_mma_layouts(gpu_lib, M, N, K, a_mn, b_mn, bf16):
     import torch
     lib = gpu_lib.load()
-    lib.atlas_mem_selftest_mma.argtypes = [ctypes.c_int] * 5 + [ctypes.c_void_p] * 5
+    lib.atlas_mem_selftest_mma.argtypes = [ctypes.c_int] * 6 + [ctypes.c_void_p] * 5
     lib.atlas_mem_selftest_mma.restype = ctypes.c_int
     g = torch.Generator().manual_seed(M * 1000 + N + K)
     dt = torch.bfloat16 if bf16 else torch.float16
@@ -31,10 +32,10 @@ def test_mma_layouts(gpu_lib, M, N, K, b_mn, bf16):
     Bm = torch.randn(N, K, generator=g).to(dt)
     ref = A.double() @ Bm.double().T
     Bdev = (Bm.T.contiguous() if b_mn else Bm).cuda()
-    Adev = A.cuda()
+    Adev = (A.T.contiguous() if a_mn else A).cuda()
     raw = torch.full((128, N), float("nan"), device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rc = lib.atlas_mem_selftest_mma(M, N, K, b_mn, bf16, Adev.data_ptr(), Bdev.data_ptr(), raw.data_ptr(),
+    rc = lib.atlas_mem_selftest_mma(M, N, K, a_mn, b_mn, bf16, Adev.data_ptr(), Bdev.data_ptr(), raw.data_ptr(),
                                     st.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert rc == 0
     torch.cuda.synchronize()
