@@ -22,6 +22,15 @@ extern "C" {
 int atlas_mem_selftest_mma(int M, int N, int K, int a_mn_major, int b_mn_major, int bf16, const void* A,
                            const void* B, float* raw_out, int* status, void* stream);
 
+/* Layout check of the 16x32bx2 TMEM load used on M = 64 accumulators.
+ * Runs D = A * B^T (M = 64, A: device bf16 [64][K], B: device bf16 [N][K],
+ * 64 <= N <= 256, 16 <= K <= 128, multiples of 16) and has every warp w of 4
+ * load columns [col, col + 32) of its 32-lane sub-partition with that shape.
+ * raw_out: device fp32 [128][16]: row w * 32 + t = the 16 registers of
+ * thread t of warp w.  status: device int, 1 if the bounded wait gave up. */
+int atlas_mem_selftest_ld16x2(int N, int K, const void* A, const void* B, float* raw_out, int col, int* status,
+                              void* stream);
+
 #ifdef __cplusplus
 }
 #endif

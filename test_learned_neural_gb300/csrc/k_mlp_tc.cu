@@ -127,6 +127,59 @@ __device__ __forceinline__ float ld_in(const void* p, size_t i, int dt) {
   return dt == ATLAS_BF16 ? __uint_as_float(((uint32_t)((const uint16_t*)p)[i]) << 16) : ((const float*)p)[i];
 }
 
+// Raw inputs of one chunk held in registers: thread tid covers row
+// r = tid % 64 of the k, q, v tiles, column groups g and g + 4 (g = tid / 64),
+// 8 bf16 (or 8 fp32 as two float4) values each; threads 0-63 hold token
+// tid's gates.  Loaded one chunk ahead so global latency hides behind work.
+struct Prefetch {
+  uint4 k[2][2], q[2][2], v[2][2];   // [group][0: values 0-3 | 1: values 4-7] (fp32) or [group][0] (bf16)
+  float th, et, al, ga;
+};
+
+__device__ __forceinline__ void prefetch_chunk(Prefetch& p, int dt, const void* q, const void* k, const void* v,
+                                               const float* theta, const float* eta, const float* alpha,
+                                               const float* gamma, int u, int T, int s) {
+  const int tid = threadIdx.x, r = tid % 64, g = tid / 64;
+  if (s >= T) return;
+  for (int j = 0; j < 2; ++j) {
+    const size_t base = ((size_t)u * T + s + r) * 64 + (g + 4 * j) * 8;
+    if (dt == ATLAS_BF16) {
+      p.k[j][0] = __ldg(reinterpret_cast<const uint4*>((const uint16_t*)k + base));
+      p.q[j][0] = __ldg(reinterpret_cast<const uint4*>((const uint16_t*)q + base));
+      p.v[j][0] = __ldg(reinterpret_cast<const uint4*>((const uint16_t*)v + base));
+    } else {
+      p.k[j][0] = __ldg(reinterpret_cast<const uint4*>((const float*)k + base));
+      p.k[j][1] = __ldg(reinterpret_cast<const uint4*>((const float*)k + base + 4));
+      p.q[j][0] = __ldg(reinterpret_cast<const uint4*>((const float*)q + base));
+      p.q[j][1] = __ldg(reinterpret_cast<const uint4*>((const float*)q + base + 4));
+      p.v[j][0] = __ldg(reinterpret_cast<const uint4*>((const float*)v + base));
+      p.v[j][1] = __ldg(reinterpret_cast<const uint4*>((const float*)v + base + 4));
+    }
+  }
+  if (tid < 64) {
+    const size_t gi = (size_t)u * T + s + tid;
+    p.th = __ldg(theta + gi);
+    p.et = __ldg(eta + gi);
+    p.al = __ldg(alpha + gi);
+    p.ga = gamma ? __ldg(gamma + gi) : 1.f;
+  }
+}
+
+__device__ __forceinline__ void unpack8(const uint4* w, int dt, float* o) {
+  if (dt == ATLAS_BF16) {
+    const uint32_t a[4] = {w[0].x, w[0].y, w[0].z, w[0].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(a[i] << 16);
+      o[2 * i + 1] = __uint_as_float(a[i] & 0xFFFF0000u);
+    }
+  } else {
+    const uint4 x = w[0], y = w[1];
+    o[0] = __uint_as_float(x.x); o[1] = __uint_as_float(x.y); o[2] = __uint_as_float(x.z); o[3] = __uint_as_float(x.w);
+    o[4] = __uint_as_float(y.x); o[5] = __uint_as_float(y.y); o[6] = __uint_as_float(y.z); o[7] = __uint_as_float(y.w);
+  }
+}
+
 struct Ctx {
   uint64_t* bar;
   uint32_t phase;
@@ -164,10 +217,12 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int sp = warp & 3, half = warp >> 2;
-  const bool act = lane < 16;                 // M = 64: rows live in lanes 0-15 of each sub-partition
-  const int row = 16 * sp + lane;             // accumulator row of this thread
-  const int c0 = 32 * half;                   // its 32 columns
-  const uint32_t lb = (uint32_t)(32 * sp) << 16;
+  // M = 64 accumulators keep rows 16 sp .. 16 sp + 15 in lanes 0-15 of
+  // sub-partition sp; the 16x32bx2 load gives thread `lane` row
+  // 16 sp + lane % 16 and 16 columns starting at cb (all 32 lanes busy).
+  const int row = 16 * sp + (lane & 15);
+  const int cb = 32 * half + 16 * (lane >> 4);
+  const uint32_t lb = ((uint32_t)(32 * sp) << 16) + 32 * half;
   const uint32_t qr = cluster_rank();
   const int u = blockIdx.x / CS;
   const int H = 4 * HQ;                       // hidden width
@@ -187,7 +242,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   }
   __syncthreads();
   for (int e = tid; e < 64 * 8; e += NT) {
-    const int r = e / 8, cc = (e % 8) * 8;
+    const int r = e % 64, cc = (e / 64) * 8;
     float a[8], b[8], c[8], d[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -206,33 +261,35 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   tc::fence_after_sync();
   Ctx cx{&bar, 0u, true};
   const uint32_t tb = tbase;
+  Prefetch pf;
+  prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, 0);
   const uint32_t red_local = tc::smem_u32(sm + RED);
 
   for (int s = 0; s < T; s += TOK) {
     // ---------------------------------------------------------------- L
-    for (int e = tid; e < 64 * 8; e += NT) {
-      const int r = e / 8, cc = (e % 8) * 8;
-      float xk[8], xq[8];
-      const size_t base = ((size_t)u * T + s + r) * D + cc;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        xk[i] = ld_in(k, base + i, dt);
-        xq[i] = ld_in(q, base + i, dt);
+    {
+      const int r = tid % 64, g = tid / 64;
+      for (int j = 0; j < 2; ++j) {
+        float xk[8], xq[8];
+        unpack8(pf.k[j], dt, xk);
+        unpack8(pf.q[j], dt, xq);
+        st_h8(sm + OX, RGS, r, (g + 4 * j) * 8, xk);
+        st_h8(sm + OR_, RGS, r, (g + 4 * j) * 8, xq);
       }
-      st_h8(sm + OX, RGS, r, cc, xk);
-      st_h8(sm + OR_, RGS, r, cc, xq);
+      if (tid < 64) {
+        vec[V_TH + tid] = pf.th;
+        vec[V_ET + tid] = pf.et;
+        vec[V_BE + tid] = 1.f - pf.al;
+        vec[V_GA + tid] = pf.ga;
+      }
     }
-    if (tid < 64) {
-      const size_t gi = (size_t)u * T + s + tid;
-      vec[V_TH + tid] = theta[gi];
-      vec[V_ET + tid] = eta[gi];
-      vec[V_BE + tid] = 1.f - alpha[gi];
-      vec[V_GA + tid] = gamma ? gamma[gi] : 1.f;
-    }
+    const Prefetch cur = pf;   // this chunk's k, v stay in registers for dy
+    prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, s + TOK);
     __syncthreads();
     if (tid < 64) {  // column i = tid of Cs / Cw (window of token t is {t})
       const int i = tid;
       float cs = 0.f, cw = 0.f;
+#pragma unroll
       for (int t = 0; t < TOK; ++t) {
         cs = vec[V_ET + t] * cs + (t == i ? vec[V_TH + t] : 0.f);
         cw = vec[V_BE + t] * cw + cs;
@@ -242,6 +299,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       vec[V_CW + i] = cw;
     } else if (tid == 64) {
       float Ap = 1.f, Bp = 1.f, Dp = 0.f;
+#pragma unroll
       for (int t = 0; t < TOK; ++t) {
         Ap *= vec[V_ET + t];
         Bp *= vec[V_BE + t];
@@ -256,29 +314,29 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     if (tid == 0 && cx.ok) {
       mma64(tb + C_Z, sm + OX, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
       mma64(tb + C_G1, sm + OR_, 0, RGS, sm + OX, 0, RGS, 64, 64, false);
+      mma64(tb + C_P1, sm + OR_, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
+      mma64(tb + C_P2, sm + OR_, 0, RGS, sm + OS1, 1, RGS, 64, 64, false);
     }
     commit_wait(cx);
-    for (int cc = 0; cc < 32; cc += 16) {
+    {
       float z[16], g[16];
-      tc::tmem_ld16(tb + lb + C_Z + c0 + cc, z);
-      tc::tmem_ld16(tb + lb + C_G1 + c0 + cc, g);
+      tc::tmem_ld16_x2(tb + lb + C_Z, z);
+      tc::tmem_ld16_x2(tb + lb + C_G1, g);
       tc::tmem_ld_wait();
-      if (act) {
-        float a[16], spv[16], m1[16];
+      float a[16], spv[16], m1[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float sg = 1.f / (1.f + __expf(-z[i]));
-          a[i] = z[i] * sg;
-          spv[i] = sg * (1.f + z[i] * (1.f - sg));
-          m1[i] = -cwm[swz(row, c0 + cc + i)] * g[i];
-        }
-        st_h8(sm + OA, RGS, row, c0 + cc, a);
-        st_h8(sm + OA, RGS, row, c0 + cc + 8, a + 8);
-        st_h8(sm + OSP, RGS, row, c0 + cc, spv);
-        st_h8(sm + OSP, RGS, row, c0 + cc + 8, spv + 8);
-        st_h8(sm + OM1, RGS, row, c0 + cc, m1);
-        st_h8(sm + OM1, RGS, row, c0 + cc + 8, m1 + 8);
+      for (int i = 0; i < 16; ++i) {
+        const float sg = __frcp_rn(1.f + __expf(-z[i]));
+        a[i] = z[i] * sg;
+        spv[i] = sg * (1.f + z[i] * (1.f - sg));
+        m1[i] = -cwm[swz(row, cb + i)] * g[i];
       }
+      st_h8(sm + OA, RGS, row, cb, a);
+      st_h8(sm + OA, RGS, row, cb + 8, a + 8);
+      st_h8(sm + OSP, RGS, row, cb, spv);
+      st_h8(sm + OSP, RGS, row, cb + 8, spv + 8);
+      st_h8(sm + OM1, RGS, row, cb, m1);
+      st_h8(sm + OM1, RGS, row, cb + 8, m1 + 8);
     }
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 2: Yp = A W2q
@@ -289,82 +347,74 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     // every peer has read Yp(n); Yq(n+1) after the first barrier of chunk
     // n+1, when every peer has read Yq(n).
     float* redb = reinterpret_cast<float*>(sm + RED);
-    for (int cc = 0; cc < 32; cc += 16) {
+    {
       float yp[16];
-      tc::tmem_ld16(tb + lb + C_YP + c0 + cc, yp);
+      tc::tmem_ld16_x2(tb + lb + C_YP, yp);
       tc::tmem_ld_wait();
-      if (act)
 #pragma unroll
-        for (int i = 0; i < 16; i += 4)
-          *reinterpret_cast<float4*>(redb + swz(row, c0 + cc + i)) = make_float4(yp[i], yp[i + 1], yp[i + 2], yp[i + 3]);
+      for (int i = 0; i < 16; i += 4)
+        *reinterpret_cast<float4*>(redb + swz(row, cb + i)) = make_float4(yp[i], yp[i + 1], yp[i + 2], yp[i + 3]);
     }
     cluster_sync();
     // dy = 2 gamma (X + sum_q Yp_q - V): every CTA forms all of it
-    for (int e = tid; e < 64 * 16; e += NT) {
-      const int r = e / 16, cc = (e % 16) * 4;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int p = 0; p < CS; ++p) {
-        const uint32_t addr = mapa(red_local + (uint32_t)(swz(r, cc) * 4), p);
-        const float4 t4 = ld_cluster4(addr);
-        acc.x += t4.x; acc.y += t4.y; acc.z += t4.z; acc.w += t4.w;
-      }
-      const size_t gb = ((size_t)u * T + s + r) * D + cc;
+    {
+      const int r = tid % 64, g = tid / 64;
       const float g2 = 2.f * vec[V_GA + r];
-      const float dy[4] = {g2 * (ld_in(k, gb, dt) + acc.x - ld_in(v, gb, dt)),
-                           g2 * (ld_in(k, gb + 1, dt) + acc.y - ld_in(v, gb + 1, dt)),
-                           g2 * (ld_in(k, gb + 2, dt) + acc.z - ld_in(v, gb + 2, dt)),
-                           g2 * (ld_in(k, gb + 3, dt) + acc.w - ld_in(v, gb + 3, dt))};
-      __half2 h0 = __floats2half2_rn(dy[0], dy[1]), h1 = __floats2half2_rn(dy[2], dy[3]);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&h0);
-      pk.y = *reinterpret_cast<uint32_t*>(&h1);
-      *reinterpret_cast<uint2*>(sm + ODY + tc::core_offset(r, cc, RGS)) = pk;
+      for (int j = 0; j < 2; ++j) {
+        const int cc = (g + 4 * j) * 8;
+        float acc[8], xk[8], vv[8], dy[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+        for (int p = 0; p < CS; ++p)
+#pragma unroll
+          for (int h4 = 0; h4 < 2; ++h4) {
+            const float4 t4 = ld_cluster4(mapa(red_local + (uint32_t)(swz(r, cc + 4 * h4) * 4), p));
+            acc[4 * h4] += t4.x; acc[4 * h4 + 1] += t4.y; acc[4 * h4 + 2] += t4.z; acc[4 * h4 + 3] += t4.w;
+          }
+        unpack8(cur.k[j], dt, xk);
+        unpack8(cur.v[j], dt, vv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dy[i] = g2 * (xk[i] + acc[i] - vv[i]);
+        st_h8(sm + ODY, RGS, r, cc, dy);
+      }
     }
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 3: dz' = dy W2q^T
     if (tid == 0 && cx.ok) mma64(tb + C_Z, sm + ODY, 0, RGS, sm + OW2, 0, RGS, 64, 64, false);
     commit_wait(cx);
-    for (int cc = 0; cc < 32; cc += 16) {
-      float t[16];
-      tc::tmem_ld16(tb + lb + C_Z + c0 + cc, t);
+    {
+      float t[16], spv[16];
+      tc::tmem_ld16_x2(tb + lb + C_Z, t);
+      ld_h8(sm + OSP, RGS, row, cb, spv);
+      ld_h8(sm + OSP, RGS, row, cb + 8, spv + 8);
       tc::tmem_ld_wait();
-      if (act) {
-        float spv[16];
-        ld_h8(sm + OSP, RGS, row, c0 + cc, spv);
-        ld_h8(sm + OSP, RGS, row, c0 + cc + 8, spv + 8);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) t[i] *= spv[i];
-        st_h8(sm + ODZ, RGS, row, c0 + cc, t);
-        st_h8(sm + ODZ, RGS, row, c0 + cc + 8, t + 8);
-      }
+      for (int i = 0; i < 16; ++i) t[i] *= spv[i];
+      st_h8(sm + ODZ, RGS, row, cb, t);
+      st_h8(sm + ODZ, RGS, row, cb + 8, t + 8);
     }
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 4: Zq parts
     if (tid == 0 && cx.ok) {
-      mma64(tb + C_P1, sm + OR_, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
-      mma64(tb + C_P2, sm + OR_, 0, RGS, sm + OS1, 1, RGS, 64, 64, false);
       mma64(tb + C_P3, sm + OM1, 0, RGS, sm + ODZ, 1, RGS, 64, 64, false);
     }
     commit_wait(cx);
     {
       const float Bt = vec[V_BP + row], Dt = vec[V_DP + row];
-      for (int cc = 0; cc < 32; cc += 16) {
-        float p1[16], p2[16], p3[16];
-        tc::tmem_ld16(tb + lb + C_P1 + c0 + cc, p1);
-        tc::tmem_ld16(tb + lb + C_P2 + c0 + cc, p2);
-        tc::tmem_ld16(tb + lb + C_P3 + c0 + cc, p3);
-        tc::tmem_ld_wait();
-        if (act) {
-          float aq[16];
+      float p1[16], p2[16], p3[16];
+      tc::tmem_ld16_x2(tb + lb + C_P1, p1);
+      tc::tmem_ld16_x2(tb + lb + C_P2, p2);
+      tc::tmem_ld16_x2(tb + lb + C_P3, p3);
+      tc::tmem_ld_wait();
+      float aq[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float zq = Bt * p1[i] + Dt * p2[i] + p3[i];
-            aq[i] = zq / (1.f + __expf(-zq));
-          }
-          st_h8(sm + OAQ, RGS, row, c0 + cc, aq);
-          st_h8(sm + OAQ, RGS, row, c0 + cc + 8, aq + 8);
-        }
+      for (int i = 0; i < 16; ++i) {
+        const float zq = Bt * p1[i] + Dt * p2[i] + p3[i];
+        aq[i] = zq * __frcp_rn(1.f + __expf(-zq));
       }
+      st_h8(sm + OAQ, RGS, row, cb, aq);
+      st_h8(sm + OAQ, RGS, row, cb + 8, aq + 8);
     }
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 5: G2, Aq W2q, Aq S2q
@@ -374,17 +424,14 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       mma64(tb + C_Q2, sm + OAQ, 0, RGS, sm + OS2, 1, RGS, 64, 64, false);
     }
     commit_wait(cx);
-    for (int cc = 0; cc < 32; cc += 16) {
-      float g[16];
-      tc::tmem_ld16(tb + lb + C_G2 + c0 + cc, g);
+    {
+      float g[16], m2[16];
+      tc::tmem_ld16_x2(tb + lb + C_G2, g);
       tc::tmem_ld_wait();
-      if (act) {
-        float m2[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) m2[i] = -cwm[swz(row, c0 + cc + i)] * g[i];
-        st_h8(sm + OM2, RGS, row, c0 + cc, m2);
-        st_h8(sm + OM2, RGS, row, c0 + cc + 8, m2 + 8);
-      }
+      for (int i = 0; i < 16; ++i) m2[i] = -cwm[swz(row, cb + i)] * g[i];
+      st_h8(sm + OM2, RGS, row, cb, m2);
+      st_h8(sm + OM2, RGS, row, cb + 8, m2 + 8);
     }
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 6: Q3 = M2 dy, Yq
@@ -393,27 +440,24 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     float* redy = reinterpret_cast<float*>(sm + RED + F32T);
     {
       const float Bt = vec[V_BP + row], Dt = vec[V_DP + row];
-      for (int cc = 0; cc < 32; cc += 16) {
-        float q1[16], q2[16], q3[16];
-        tc::tmem_ld16(tb + lb + C_Q1 + c0 + cc, q1);
-        tc::tmem_ld16(tb + lb + C_Q2 + c0 + cc, q2);
-        tc::tmem_ld16(tb + lb + C_Q3 + c0 + cc, q3);
-        tc::tmem_ld_wait();
-        if (act)
+      float q1[16], q2[16], q3[16];
+      tc::tmem_ld16_x2(tb + lb + C_Q1, q1);
+      tc::tmem_ld16_x2(tb + lb + C_Q2, q2);
+      tc::tmem_ld16_x2(tb + lb + C_Q3, q3);
+      tc::tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            float4 o;
-            o.x = Bt * q1[i] + Dt * q2[i] + q3[i];
-            o.y = Bt * q1[i + 1] + Dt * q2[i + 1] + q3[i + 1];
-            o.z = Bt * q1[i + 2] + Dt * q2[i + 2] + q3[i + 2];
-            o.w = Bt * q1[i + 3] + Dt * q2[i + 3] + q3[i + 3];
-            *reinterpret_cast<float4*>(redy + swz(row, c0 + cc + i)) = o;
-          }
+      for (int i = 0; i < 16; i += 4) {
+        float4 o;
+        o.x = Bt * q1[i] + Dt * q2[i] + q3[i];
+        o.y = Bt * q1[i + 1] + Dt * q2[i + 1] + q3[i + 1];
+        o.z = Bt * q1[i + 2] + Dt * q2[i + 2] + q3[i + 2];
+        o.w = Bt * q1[i + 3] + Dt * q2[i + 3] + q3[i + 3];
+        *reinterpret_cast<float4*>(redy + swz(row, cb + i)) = o;
       }
     }
     // state-update operands (the read-out operands are dead): diag(cs|cw) dz, dy
     for (int e = tid; e < 64 * 8; e += NT) {
-      const int r = e / 8, cc = (e % 8) * 8;
+      const int r = e % 64, cc = (e / 64) * 8;
       const float csr = vec[V_CS + r], cwr = vec[V_CW + r];
       float dz[8], dy[8], t0[8], t1[8];
       ld_h8(sm + ODZ, RGS, r, cc, dz);
@@ -459,32 +503,30 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
         float* sf = mtx ? s2f : s1f;
         uint8_t* ow = sm + (mtx ? OW2 : OW1);
         uint8_t* os = sm + (mtx ? OS2 : OS1);
-        const uint32_t cb = mtx ? C_ST2 : C_ST1;
-        for (int cc = 0; cc < 32; cc += 16) {
+        const uint32_t cb_t = mtx ? C_ST2 : C_ST1;
+        {
           float scr[16], wcr[16];
-          tc::tmem_ld16(tb + lb + cb + c0 + cc, scr);
-          tc::tmem_ld16(tb + lb + cb + 64 + c0 + cc, wcr);
+          tc::tmem_ld16_x2(tb + lb + cb_t, scr);
+          tc::tmem_ld16_x2(tb + lb + cb_t + 64, wcr);
           tc::tmem_ld_wait();
-          if (act) {
-            float wn[16], sn[16];
+          float wn[16], sn[16];
 #pragma unroll
-            for (int i = 0; i < 16; i += 4) {
-              const float4 so = *reinterpret_cast<const float4*>(sf + swz(row, c0 + cc + i));
-              const float4 wo = *reinterpret_cast<const float4*>(wf + swz(row, c0 + cc + i));
-              const float sov[4] = {so.x, so.y, so.z, so.w}, wov[4] = {wo.x, wo.y, wo.z, wo.w};
+          for (int i = 0; i < 16; i += 4) {
+            const float4 so = *reinterpret_cast<const float4*>(sf + swz(row, cb + i));
+            const float4 wo = *reinterpret_cast<const float4*>(wf + swz(row, cb + i));
+            const float sov[4] = {so.x, so.y, so.z, so.w}, wov[4] = {wo.x, wo.y, wo.z, wo.w};
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                sn[i + j] = Ae * sov[j] - scr[i + j];
-                wn[i + j] = Be * wov[j] + De * sov[j] - wcr[i + j];
-              }
-              *reinterpret_cast<float4*>(sf + swz(row, c0 + cc + i)) = make_float4(sn[i], sn[i + 1], sn[i + 2], sn[i + 3]);
-              *reinterpret_cast<float4*>(wf + swz(row, c0 + cc + i)) = make_float4(wn[i], wn[i + 1], wn[i + 2], wn[i + 3]);
+            for (int j = 0; j < 4; ++j) {
+              sn[i + j] = Ae * sov[j] - scr[i + j];
+              wn[i + j] = Be * wov[j] + De * sov[j] - wcr[i + j];
             }
-            st_h8(ow, RGS, row, c0 + cc, wn);
-            st_h8(ow, RGS, row, c0 + cc + 8, wn + 8);
-            st_h8(os, RGS, row, c0 + cc, sn);
-            st_h8(os, RGS, row, c0 + cc + 8, sn + 8);
+            *reinterpret_cast<float4*>(sf + swz(row, cb + i)) = make_float4(sn[i], sn[i + 1], sn[i + 2], sn[i + 3]);
+            *reinterpret_cast<float4*>(wf + swz(row, cb + i)) = make_float4(wn[i], wn[i + 1], wn[i + 2], wn[i + 3]);
           }
+          st_h8(ow, RGS, row, cb, wn);
+          st_h8(ow, RGS, row, cb + 8, wn + 8);
+          st_h8(os, RGS, row, cb, sn);
+          st_h8(os, RGS, row, cb + 8, sn + 8);
         }
       }
     }

@@ -19,6 +19,8 @@
 // Shared-memory operands use the no-swizzle core-matrix layout of tc.cuh.
 // X lives in one layout that is read as a K-major operand by X X^T and as an
 // MN-major operand by B' X.
+#include <cuda_bf16.h>
+
 #include "atlas_common.cuh"
 #include "tc.cuh"
 
@@ -27,7 +29,7 @@ namespace atlas {
 namespace {
 
 constexpr int R = 64;     // short side of X
-constexpr int NT = 128;   // threads per CTA (4 warps = 4 TMEM sub-partitions)
+constexpr int NT = 256;   // threads per CTA: two warps per TMEM sub-partition
 constexpr long long kWaitCycles = 1ll << 31;
 
 struct NsSmem {
@@ -50,17 +52,17 @@ __host__ __device__ inline NsSmem ns_smem_layout(int n, int Kp) {
 }
 
 __device__ inline void store_split16(uint8_t* hi, uint8_t* lo, uint32_t off, const float* v) {
-  // 8 consecutive values of one row -> one 16-byte chunk in each array
-  uint16_t h[8], l[8];
+  // 8 consecutive values of one row -> one 16-byte chunk in each array;
+  // hi = bf16(x) and lo = bf16(x - hi), two values per conversion
+  __nv_bfloat162 h[4], l[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) tc::split_bf16(v[i], h[i], l[i]);
-  uint4 H, L;
-  H.x = h[0] | ((uint32_t)h[1] << 16); H.y = h[2] | ((uint32_t)h[3] << 16);
-  H.z = h[4] | ((uint32_t)h[5] << 16); H.w = h[6] | ((uint32_t)h[7] << 16);
-  L.x = l[0] | ((uint32_t)l[1] << 16); L.y = l[2] | ((uint32_t)l[3] << 16);
-  L.z = l[4] | ((uint32_t)l[5] << 16); L.w = l[6] | ((uint32_t)l[7] << 16);
-  *reinterpret_cast<uint4*>(hi + off) = H;
-  *reinterpret_cast<uint4*>(lo + off) = L;
+  for (int i = 0; i < 4; ++i) {
+    h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    const float2 hf = __bfloat1622float2(h[i]);
+    l[i] = __floats2bfloat162_rn(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
+  }
+  *reinterpret_cast<uint4*>(hi + off) = *reinterpret_cast<const uint4*>(h);
+  *reinterpret_cast<uint4*>(lo + off) = *reinterpret_cast<const uint4*>(l);
 }
 
 // D (+)= A * B^T over K, split-bf16: hi*hi + hi*lo + lo*hi.
@@ -111,9 +113,15 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
   uint8_t* opr = sm + L.opr;
   float* stg = reinterpret_cast<float*>(sm + L.stg);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const bool row_ok = lane < 16;                 // M = 64: 16 rows per sub-partition
-  const int row = 16 * warp + lane;              // row of X held by this thread
-  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+  // M = 64 accumulators: rows 16 sp .. 16 sp + 15 sit in lanes 0-15 of
+  // sub-partition sp.  With the 16x32bx2 load a warp reads 16 rows x 32
+  // columns at once: thread `lane` gets row 16 sp + lane % 16 and columns
+  // c + 16 (lane / 16) + [0, 16).  The two warps of a sub-partition take
+  // alternate 32-column blocks (half = warp / 4).
+  const int sp = warp & 3, half = warp >> 2;
+  const int row = 16 * sp + (lane & 15);
+  const int csub = 16 * (lane >> 4);
+  const uint32_t lane_base = (uint32_t)(32 * sp) << 16;
   const int stg_ld = n + 4;
 
   if (warp == 0) tc::tmem_alloc(&tbase, 512);
@@ -191,9 +199,16 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
     for (int e = threadIdx.x; e < Kp * (n / 8); e += NT) {
       const int i = e / (n / 8), b0 = (e % (n / 8)) * 8;
       float v[8];
-      const float c = i < ch.nw ? cs[i] : 0.f;
+      if (i < ch.nw) {
+        const float c = cs[i];
+        const float4 r0 = *reinterpret_cast<const float4*>(Rf + (size_t)i * rstride + b0);
+        const float4 r1 = *reinterpret_cast<const float4*>(Rf + (size_t)i * rstride + b0 + 4);
+        v[0] = c * r0.x; v[1] = c * r0.y; v[2] = c * r0.z; v[3] = c * r0.w;
+        v[4] = c * r1.x; v[5] = c * r1.y; v[6] = c * r1.z; v[7] = c * r1.w;
+      } else {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) v[q] = i < ch.nw ? c * Rf[(size_t)i * rstride + b0 + q] : 0.f;
+        for (int q = 0; q < 8; ++q) v[q] = 0.f;
+      }
       // diag(cs) Rx is the MN-major B operand: k = window row i, n = long index b
       store_split16(rx_hi, rx_lo, tc::core_offset(i, b0, rgsN), v);
     }
@@ -219,18 +234,16 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
     if (!(ok = wait_all(&bar, phase))) break;
     // (d) S = A_t Sbar - D, in place in the staging; sum of squares
     float ss = 0.f;
-    for (int c0 = 0; c0 < n; c0 += 16) {
+    for (int c32 = 32 * half; c32 < n; c32 += 64) {
       float d[16];
-      tc::tmem_ld16(tX + lane_base + c0, d);
+      tc::tmem_ld16_x2(tX + lane_base + c32, d);
       tc::tmem_ld_wait();
-      if (row_ok) {
-        float* srow = stg + row * stg_ld + c0;
+      float* srow = stg + row * stg_ld + c32 + csub;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float s = At * srow[q] - d[q];
-          srow[q] = s;
-          ss += s * s;
-        }
+      for (int q = 0; q < 16; ++q) {
+        const float s = At * srow[q] - d[q];
+        srow[q] = s;
+        ss += s * s;
       }
     }
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -238,7 +251,9 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const float tot = red[0] + red[1] + red[2] + red[3];
+    float tot = 0.f;
+#pragma unroll
+    for (int k2 = 0; k2 < NT / 32; ++k2) tot += red[k2];
     const float scale = 1.f / (sqrtf(tot) + kNsEps);
     if (t == ch.e - 1) {   // chunk-end momentum, original orientation
       float* So = w.Sst[buf ^ 1][m] + (size_t)u * nel;
@@ -248,14 +263,14 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
       }
     }
     // X_0 = S * scale -> split bf16 (opr region is free: the factor MMA is done)
-    if (row_ok) {
-      for (int c0 = 0; c0 < n; c0 += 8) {
+    for (int c32 = 32 * half; c32 < n; c32 += 64)
+      for (int h8 = 0; h8 < 16; h8 += 8) {
         float v[8];
+        const int c = c32 + csub + h8;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = stg[row * stg_ld + c0 + q] * scale;
-        store_split16(x_hi, x_lo, tc::core_offset(row, c0, rgsN), v);
+        for (int q = 0; q < 8; ++q) v[q] = stg[row * stg_ld + c + q] * scale;
+        store_split16(x_hi, x_lo, tc::core_offset(row, c, rgsN), v);
       }
-    }
     sync_for_mma();
 
     float* slot = w.Ubuf + ((size_t)u * g.C + r) * slot_stride;
@@ -267,14 +282,13 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
         tc::mma_commit(&bar);
       }
       if (!(ok = wait_all(&bar, phase))) break;
-      for (int c0 = 0; c0 < R; c0 += 16) {
+      {
         float v[16];
-        tc::tmem_ld16(tA + lane_base + c0, v);
+        const int c = 32 * half + csub;
+        tc::tmem_ld16_x2(tA + lane_base + 32 * half, v);
         tc::tmem_ld_wait();
-        if (row_ok) {
-          store_split16(a_hi, a_lo, tc::core_offset(row, c0, rgsR), v);
-          store_split16(a_hi, a_lo, tc::core_offset(row, c0 + 8, rgsR), v + 8);
-        }
+        store_split16(a_hi, a_lo, tc::core_offset(row, c, rgsR), v);
+        store_split16(a_hi, a_lo, tc::core_offset(row, c + 8, rgsR), v + 8);
       }
       sync_for_mma();
       // A^2 (A symmetric: its rows serve as the K-major B operand)
@@ -283,18 +297,16 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
         tc::mma_commit(&bar);
       }
       if (!(ok = wait_all(&bar, phase))) break;
-      for (int c0 = 0; c0 < R; c0 += 16) {
-        float va[16], v2[16];
-        tc::tmem_ld16(tA + lane_base + c0, va);
-        tc::tmem_ld16(tA2 + lane_base + c0, v2);
+      {
+        float va[16], v2[16], bp[16];
+        const int c = 32 * half + csub;
+        tc::tmem_ld16_x2(tA + lane_base + 32 * half, va);
+        tc::tmem_ld16_x2(tA2 + lane_base + 32 * half, v2);
         tc::tmem_ld_wait();
-        if (row_ok) {
-          float bp[16];
 #pragma unroll
-          for (int q = 0; q < 16; ++q) bp[q] = kNsB * va[q] + kNsC * v2[q] + (row == c0 + q ? kNsA : 0.f);
-          store_split16(a_hi, a_lo, tc::core_offset(row, c0, rgsR), bp);
-          store_split16(a_hi, a_lo, tc::core_offset(row, c0 + 8, rgsR), bp + 8);
-        }
+        for (int q = 0; q < 16; ++q) bp[q] = kNsB * va[q] + kNsC * v2[q] + (row == c + q ? kNsA : 0.f);
+        store_split16(a_hi, a_lo, tc::core_offset(row, c, rgsR), bp);
+        store_split16(a_hi, a_lo, tc::core_offset(row, c + 8, rgsR), bp + 8);
       }
       sync_for_mma();
       // X = B' X  (M = 64, N = n, K = 64; X read as MN-major)
@@ -304,19 +316,18 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
       }
       if (!(ok = wait_all(&bar, phase))) break;
       const bool last = (it == g.ns_iters - 1);
-      for (int c0 = 0; c0 < n; c0 += 16) {
+      for (int c32 = 32 * half; c32 < n; c32 += 64) {
         float v[16];
-        tc::tmem_ld16(tX + lane_base + c0, v);
+        const int c = c32 + csub;
+        tc::tmem_ld16_x2(tX + lane_base + c32, v);
         tc::tmem_ld_wait();
-        if (row_ok) {
-          if (last) {
-            float4* o = reinterpret_cast<float4*>(slot + (size_t)row * n + c0);
+        if (last) {
+          float4* o = reinterpret_cast<float4*>(slot + (size_t)row * n + c);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-          } else {
-            store_split16(x_hi, x_lo, tc::core_offset(row, c0, rgsN), v);
-            store_split16(x_hi, x_lo, tc::core_offset(row, c0 + 8, rgsN), v + 8);
-          }
+          for (int q = 0; q < 4; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+          store_split16(x_hi, x_lo, tc::core_offset(row, c, rgsN), v);
+          store_split16(x_hi, x_lo, tc::core_offset(row, c + 8, rgsN), v + 8);
         }
       }
       sync_for_mma();

@@ -61,6 +61,62 @@ __global__ void __launch_bounds__(128) k_selftest_mma(int M, int N, int K, int a
 
 }  // namespace atlas
 
+// Dump of the 16x32bx2 TMEM load after an M = 64 MMA: raw[(warp * 32 + t) * 16 + j]
+// holds register j of thread t of warp `warp` when the warp loads columns
+// [c, c + 32) of its sub-partition with a half-warp split of 16 columns.
+__global__ void __launch_bounds__(128) k_selftest_ld16x2(int N, int K, const uint16_t* A, const uint16_t* B,
+                                                         float* raw, int col, int* status) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tbase;
+  const int M = 64;
+  uint8_t* As = sm;
+  uint8_t* Bs = sm + (size_t)M * K * 2;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (warp == 0) tc::tmem_alloc(&tbase, 256);
+  if (threadIdx.x == 0) tc::mbar_init(&bar, 1);
+  const int rgsK = (K / 8) * 128;
+  for (int e = threadIdx.x; e < M * K; e += blockDim.x) *(uint16_t*)(As + tc::core_offset(e / K, e % K, rgsK)) = A[e];
+  for (int e = threadIdx.x; e < N * K; e += blockDim.x) *(uint16_t*)(Bs + tc::core_offset(e / K, e % K, rgsK)) = B[e];
+  tc::fence_smem_to_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (threadIdx.x == 0) {
+    const uint32_t idesc = tc::idesc_f16(M, N, 1, 0, 0);
+    for (int ks = 0; ks < K / 16; ++ks)
+      tc::mma_f16(tbase, tc::sdesc(tc::smem_u32(As) + ks * 256, 128, rgsK),
+                  tc::sdesc(tc::smem_u32(Bs) + ks * 256, 128, rgsK), idesc, ks > 0);
+    tc::mma_commit(&bar);
+  }
+  const bool ok = tc::mbar_wait(&bar, 0, 1ll << 30);
+  tc::fence_after_sync();
+  if (!ok) {
+    if (threadIdx.x == 0) atomicExch(status, 1);
+  } else {
+    float v[16];
+    tc::tmem_ld16_x2(tbase + ((uint32_t)(32 * warp) << 16) + col, v);
+    tc::tmem_ld_wait();
+    for (int j = 0; j < 16; ++j) raw[(size_t)(warp * 32 + lane) * 16 + j] = v[j];
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tbase, 256);
+}
+
+extern "C" int atlas_mem_selftest_ld16x2(int N, int K, const void* A, const void* B, float* raw_out, int col,
+                                         int* status, void* stream) {
+  using namespace atlas;
+  if (N < 64 || N > 256 || N % 16 || K < 16 || K > 128 || K % 16 || col < 0 || col + 32 > N || !A || !B ||
+      !raw_out || !status)
+    return ATLAS_ERR_INVALID_ARG;
+  const int smem = 200 * 1024;
+  cudaFuncSetAttribute(k_selftest_ld16x2, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  k_selftest_ld16x2<<<1, 128, smem, (cudaStream_t)stream>>>(N, K, (const uint16_t*)A, (const uint16_t*)B, raw_out,
+                                                            col, status);
+  return cudaGetLastError() == cudaSuccess ? ATLAS_OK : ATLAS_ERR_CUDA;
+}
+
 extern "C" int atlas_mem_selftest_mma(int M, int N, int K, int a_mn_major, int b_mn_major, int bf16, const void* A,
                                       const void* B, float* raw_out, int* status, void* stream) {
   using namespace atlas;

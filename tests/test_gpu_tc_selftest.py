@@ -52,3 +52,39 @@ def test_mma_layouts(gpu_lib, M, N, K, a_mn, b_mn, bf16):
             hits[r] = int(d.argmin())
         print("row -> lane", hits)
     assert err < 1e-6, err
+
+
+def test_tmem_ld_16x32bx2_layout(gpu_lib):
+    """Thread t of warp w gets accumulator row 16 w + t % 16, columns
+    col + 16 (t // 16) + j.  D[r][c] = 256 r + c exactly, so every loaded
+    value names its own row and column."""
+    import torch
+    lib = gpu_lib.load()
+    lib.atlas_mem_selftest_ld16x2.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    lib.atlas_mem_selftest_ld16x2.restype = ctypes.c_int
+    N, K, col = 128, 16, 32
+    A = torch.zeros(64, K)
+    A[:, 0] = torch.arange(64, dtype=torch.float32)
+    A[:, 1] = 1.0
+    Bm = torch.zeros(N, K)
+    Bm[:, 0] = 256.0
+    Bm[:, 1] = torch.arange(N, dtype=torch.float32)
+    A, Bm = A.to(torch.bfloat16), Bm.to(torch.bfloat16)
+    raw = torch.full((128, 16), -1.0, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Adev, Bdev = A.cuda(), Bm.cuda()          # keep the device copies alive during the launch
+    rc = lib.atlas_mem_selftest_ld16x2(N, K, Adev.data_ptr(), Bdev.data_ptr(), raw.data_ptr(), col,
+                                       st.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    raw = raw.cpu().numpy().astype(np.int64)
+    got = {(w, t, j): (int(raw[32 * w + t, j]) // 256, int(raw[32 * w + t, j]) % 256)
+           for w in range(4) for t in range(32) for j in range(16)}
+    want = {(w, t, j): (16 * w + t % 16, col + 16 * (t // 16) + j) for w in range(4) for t in range(32) for j in range(16)}
+    if got != want:
+        for t in range(32):
+            print("warp 0 thread", t, [got[(0, t, j)] for j in (0, 1, 2, 15)])
+        print("warp 1 thread 0", [got[(1, 0, j)] for j in (0, 1, 15)])
+    assert got == want
