@@ -129,6 +129,7 @@ static Layout layout(const Geom& g, int units, int T) {
       g.ns_iters ? U * g.C * mat : 0,      // Ubuf
       U * (size_t)(g.c > 1 ? g.c - 1 : 0) * (g.d_k + g.d_v + 1),  // cache temp
       64,                                  // status
+      ns_tc_xch_floats(g, num_sms()),      // Gram exchange of the CTA-pair Newton-Schulz
   };
   const int n = sizeof sizes / sizeof sizes[0];
   size_t o = 0;
@@ -152,6 +153,7 @@ static Work work_from(const Geom& g, void* base, const Layout& L, float** cache_
   w.Ubuf = F(21);
   *cache_tmp = F(22);
   w.status = (int*)F(23);
+  w.xch = F(24);
   return w;
 }
 
@@ -268,10 +270,12 @@ extern "C" int atlas_mem_forward(atlas_mem_handle* h, const atlas_mem_io* io, vo
     h->launched = true;
     return ATLAS_OK;
   }
+  const bool ns_tc = ns_tc_supported(g);   // keeps S transposed for tall matrices
   for (int m = 0; m < g.nmat; ++m) {
     const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
     CUDA_TRY(cudaMemcpyAsync(w.Wst[0][m], io->W0[m], bytes, cudaMemcpyDeviceToDevice, st));
-    CUDA_TRY(cudaMemcpyAsync(w.Sst[0][m], io->S0[m], bytes, cudaMemcpyDeviceToDevice, st));
+    if (ns_tc) CUDA_TRY(ns_tc_state_in(g, m, io->S0[m], w.Sst[0][m], st));
+    else CUDA_TRY(cudaMemcpyAsync(w.Sst[0][m], io->S0[m], bytes, cudaMemcpyDeviceToDevice, st));
   }
   GenericIO gio{io->q, io->k, io->v, io->P, io->win_len ? io->win_k : nullptr, io->win_len ? io->win_v : nullptr,
                 io->theta, io->eta, io->alpha, io->gamma, io->win_len ? io->win_gamma : nullptr, io->y};
@@ -291,7 +295,8 @@ extern "C" int atlas_mem_forward(atlas_mem_handle* h, const atlas_mem_io* io, vo
   for (int m = 0; m < g.nmat; ++m) {
     const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
     CUDA_TRY(cudaMemcpyAsync(io->W_out[m], w.Wst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
-    CUDA_TRY(cudaMemcpyAsync(io->S_out[m], w.Sst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
+    if (ns_tc) CUDA_TRY(ns_tc_state_out(g, m, w.Sst[buf][m], io->S_out[m], st));
+    else CUDA_TRY(cudaMemcpyAsync(io->S_out[m], w.Sst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
   }
   if (g.c > 1 && (io->win_k_out || io->win_v_out || io->win_gamma_out))
     CUDA_TRY(generic_cache_out(g, gio, cache_tmp, io->win_k_out, io->win_v_out, io->win_gamma_out, st, &nl));
@@ -450,10 +455,12 @@ extern "C" int atlas_mem_forward_noalloc(atlas_mem_handle* h, const atlas_mem_io
   // the scratch keeps the previous call's contents: the status word must start at 0
   CUDA_TRY(cudaMemsetAsync(w.status, 0, sizeof(int), st));
   h->status = w.status;
+  const bool ns_tc = ns_tc_supported(g);   // keeps S transposed for tall matrices
   for (int m = 0; m < g.nmat; ++m) {
     const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
     CUDA_TRY(cudaMemcpyAsync(w.Wst[0][m], io->W0[m], bytes, cudaMemcpyDeviceToDevice, st));
-    CUDA_TRY(cudaMemcpyAsync(w.Sst[0][m], io->S0[m], bytes, cudaMemcpyDeviceToDevice, st));
+    if (ns_tc) CUDA_TRY(ns_tc_state_in(g, m, io->S0[m], w.Sst[0][m], st));
+    else CUDA_TRY(cudaMemcpyAsync(w.Sst[0][m], io->S0[m], bytes, cudaMemcpyDeviceToDevice, st));
   }
   GenericIO gio{io->q, io->k, io->v, io->P, io->win_len ? io->win_k : nullptr, io->win_len ? io->win_v : nullptr,
                 io->theta, io->eta, io->alpha, io->gamma, io->win_len ? io->win_gamma : nullptr, io->y};
@@ -473,7 +480,8 @@ extern "C" int atlas_mem_forward_noalloc(atlas_mem_handle* h, const atlas_mem_io
   for (int m = 0; m < g.nmat; ++m) {
     const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
     CUDA_TRY(cudaMemcpyAsync(io->W_out[m], w.Wst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
-    CUDA_TRY(cudaMemcpyAsync(io->S_out[m], w.Sst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
+    if (ns_tc) CUDA_TRY(ns_tc_state_out(g, m, w.Sst[buf][m], io->S_out[m], st));
+    else CUDA_TRY(cudaMemcpyAsync(io->S_out[m], w.Sst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
   }
   if (g.c > 1 && (io->win_k_out || io->win_v_out || io->win_gamma_out))
     CUDA_TRY(generic_cache_out(g, gio, cache_tmp, io->win_k_out, io->win_v_out, io->win_gamma_out, st, &nl));

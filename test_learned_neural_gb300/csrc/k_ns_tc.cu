@@ -16,6 +16,10 @@
 // split bf16 (x = hi + lo, hi*hi' + hi*lo' + lo*hi', about 2^-16 relative)
 // with fp32 accumulation in TMEM, and S_t, the norm and B' stay fp32.
 //
+// On this path the momentum state S of a matrix with rows > cols is kept
+// transposed (the X orientation) for the whole call; ns_tc_state_in/out
+// transpose it at the boundary.
+//
 // Shared-memory operands use the no-swizzle core-matrix layout of tc.cuh.
 // X lives in one layout that is read as a K-major operand by X X^T and as an
 // MN-major operand by B' X.
@@ -212,18 +216,11 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
       // diag(cs) Rx is the MN-major B operand: k = window row i, n = long index b
       store_split16(rx_hi, rx_lo, tc::core_offset(i, b0, rgsN), v);
     }
-    // (b) Sbar in the X orientation, fp32 staging
-    if (!tall) {
-      for (int e = threadIdx.x; e < R * n / 4; e += NT) {
-        const int a = e / (n / 4), b = (e % (n / 4)) * 4;
-        const float4 s4 = *reinterpret_cast<const float4*>(Sb + (size_t)a * n + b);
-        *reinterpret_cast<float4*>(stg + a * stg_ld + b) = s4;
-      }
-    } else {
-      for (int e = threadIdx.x; e < R * n; e += NT) {
-        const int b = e / R, a = e % R;   // Sbar stored [b][a]
-        stg[a * stg_ld + b] = Sb[e];
-      }
+    // (b) Sbar (kept in the X orientation on this path), fp32 staging
+    for (int e = threadIdx.x; e < R * n / 4; e += NT) {
+      const int a = e / (n / 4), b = (e % (n / 4)) * 4;
+      const float4 s4 = *reinterpret_cast<const float4*>(Sb + (size_t)a * n + b);
+      *reinterpret_cast<float4*>(stg + a * stg_ld + b) = s4;
     }
     sync_for_mma();
     // (c) D = Lx^T diag(cs) Rx   (M = 64, N = n, K = Kp)
@@ -255,11 +252,11 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
 #pragma unroll
     for (int k2 = 0; k2 < NT / 32; ++k2) tot += red[k2];
     const float scale = 1.f / (sqrtf(tot) + kNsEps);
-    if (t == ch.e - 1) {   // chunk-end momentum, original orientation
+    if (t == ch.e - 1) {   // chunk-end momentum (X orientation)
       float* So = w.Sst[buf ^ 1][m] + (size_t)u * nel;
-      for (int e = threadIdx.x; e < R * n; e += NT) {
-        if (!tall) { const int a = e / n, b = e % n; So[e] = stg[a * stg_ld + b]; }
-        else { const int b = e / R, a = e % R; So[e] = stg[a * stg_ld + b]; }
+      for (int e = threadIdx.x; e < R * n / 4; e += NT) {
+        const int a = e / (n / 4), b = (e % (n / 4)) * 4;
+        *reinterpret_cast<float4*>(So + (size_t)a * n + b) = *reinterpret_cast<const float4*>(stg + a * stg_ld + b);
       }
     }
     // X_0 = S * scale -> split bf16 (opr region is free: the factor MMA is done)
@@ -340,25 +337,359 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
   if (warp == 0) tc::tmem_dealloc(tbase, 512);
 }
 
-bool ns_tc_supported(const Geom& g) {
-  if (g.ns_iters <= 0) return false;
-  int n0 = -1;
+// ============================================================ short side 128
+// Matrices with a short side of 128 and a long side of 512 (the 128 -> 512
+// -> 128 MLP memory).  X in split bf16 (256 KB) does not fit one SM, so a
+// cluster of two CTAs shares each task: CTA p holds columns [256 p, 256 p +
+// 256) of X.  X X^T = sum of the two halves' Gram matrices: each CTA writes
+// its partial (fp32) to a double-buffered L2 scratch, one cluster barrier,
+// and each adds the partner's.  A^2 and B' are formed redundantly by both;
+// X <- B' X splits by columns with no exchange.
+namespace {
+
+constexpr int R2 = 128, NH = 256, NT2 = 256;
+constexpr int OPR2 = 131072;                    // factors (120 KB) / X hi+lo (128 KB)
+constexpr int AB2 = 65536;                      // A / B' hi+lo
+constexpr int SMEM2 = OPR2 + AB2;
+constexpr int XCH_FLOATS = 2 * 2 * R2 * R2;     // per cluster: 2 CTAs x 2 buffers
+
+__device__ __forceinline__ uint32_t cluster_rank2() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync2() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_cluster_f(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t mapa2(uint32_t saddr, uint32_t cta) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(cta));
+  return r;
+}
+
+struct PairCtx {
+  uint64_t* bar;
+  uint32_t phase;
+  bool ok;
+};
+
+// Bounded wait that never leaves the loop structure: after a timeout the
+// CTA stops issuing and waiting, but keeps meeting its partner at every
+// cluster barrier so neither can hang the other.
+__device__ __forceinline__ void pair_commit_wait(PairCtx& c) {
+  if (threadIdx.x == 0 && c.ok) tc::mma_commit(c.bar);
+  bool good = true;
+  if (c.ok) good = tc::mbar_wait(c.bar, c.phase, kWaitCycles);
+  c.phase ^= 1;
+  if (__syncthreads_or(!good)) c.ok = false;
+  tc::fence_after_sync();
+}
+
+}  // namespace
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
+    k_ns_tc128(Geom g, Chunk ch, Work w, int buf, size_t slot_stride, int Kp) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tbase;
+  __shared__ float red[NT2 / 32];
+  __shared__ float ss_cta;
+  const uint32_t p = cluster_rank2();
+  const int cl = blockIdx.x / 2, ncl = gridDim.x / 2;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int sp = warp & 3, half = warp >> 2;
+  const int row = 32 * sp + lane;                   // M = 128: lane i of sub-partition sp holds row 32 sp + i
+  const uint32_t lane_base = (uint32_t)(32 * sp) << 16;
+  const int n = 2 * NH;                             // long side of X
+
+  if (warp == 0) tc::tmem_alloc(&tbase, 512);
+  if (threadIdx.x == 0) tc::mbar_init(&bar, 1);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tA = tbase, tA2 = tbase + 128, tX = tbase + 256;
+  PairCtx cx{&bar, 0u, true};
+  int xpar = 0;
+
+  const int lxb = R2 * Kp * 2, rxb = Kp * NH * 2;
+  uint8_t* lx_hi = sm;
+  uint8_t* lx_lo = sm + lxb;
+  uint8_t* rx_hi = sm + 2 * lxb;
+  uint8_t* rx_lo = sm + 2 * lxb + rxb;
+  uint8_t* x_hi = sm;
+  uint8_t* x_lo = sm + R2 * NH * 2;
+  uint8_t* a_hi = sm + OPR2;
+  uint8_t* a_lo = sm + OPR2 + R2 * R2 * 2;
+  const int rgsKp = (Kp / 8) * 128, rgsN = (NH / 8) * 128, rgsR = (R2 / 8) * 128;
+  float* xch = w.xch + (size_t)cl * XCH_FLOATS;
+
+  const int Ct = ch.e - ch.s;
+  const int ntasks = g.units * g.nmat * Ct;
+  for (int task = cl; task < ntasks; task += ncl) {
+    const int r = task % Ct;
+    const int m = (task / Ct) % g.nmat;
+    const int u = task / (Ct * g.nmat);
+    const int t = ch.s + r;
+    const int rows = g.rows[m], cols = g.cols[m];
+    const bool tall = rows > cols;
+    const float* Lf;
+    const float* Rf;
+    int lstride, rstride;
+    if (g.depth == 2 && m == 1) {
+      Lf = w.DY + (size_t)u * g.Kw * g.d_v; lstride = g.d_v;
+      Rf = w.Aact + (size_t)u * g.Kw * g.hidden; rstride = g.hidden;
+    } else if (g.depth == 2) {
+      Lf = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * g.F; lstride = g.F;
+      Rf = w.DZ + (size_t)u * g.Kw * g.hidden; rstride = g.hidden;
+    } else {
+      const float* xf = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * g.F;
+      const float* dy = w.DY + (size_t)u * g.Kw * g.d_v;
+      if (tall) { Lf = dy; lstride = g.d_v; Rf = xf; rstride = g.F; }
+      else { Lf = xf; lstride = g.F; Rf = dy; rstride = g.d_v; }
+    }
+    const float* cs = w.Cs + ((size_t)u * g.C + r) * g.Kw;
+    const float At = w.Ap[(size_t)u * g.C + r];
+    const size_t nel = (size_t)rows * cols;
+    const float* Sb = w.Sst[buf][m] + (size_t)u * nel;   // X orientation [128][512]
+
+    // (a) factors: Lx^T (K-major [128][Kp]) and this CTA's columns of diag(cs) Rx
+    for (int e = threadIdx.x; e < Kp * (R2 / 8); e += NT2) {
+      const int i = e / (R2 / 8), a0 = (e % (R2 / 8)) * 8;
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = i < ch.nw ? Lf[(size_t)i * lstride + a0 + q] : 0.f;
+      uint16_t h[8], l[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) tc::split_bf16(v[q], h[q], l[q]);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t off = tc::core_offset(a0 + q, i, rgsKp);
+        *reinterpret_cast<uint16_t*>(lx_hi + off) = h[q];
+        *reinterpret_cast<uint16_t*>(lx_lo + off) = l[q];
+      }
+    }
+    for (int e = threadIdx.x; e < Kp * (NH / 8); e += NT2) {
+      const int i = e / (NH / 8), b0 = (e % (NH / 8)) * 8;
+      float v[8];
+      if (i < ch.nw) {
+        const float c = cs[i];
+        const float* src = Rf + (size_t)i * rstride + p * NH + b0;
+        const float4 r0 = *reinterpret_cast<const float4*>(src);
+        const float4 r1 = *reinterpret_cast<const float4*>(src + 4);
+        v[0] = c * r0.x; v[1] = c * r0.y; v[2] = c * r0.z; v[3] = c * r0.w;
+        v[4] = c * r1.x; v[5] = c * r1.y; v[6] = c * r1.z; v[7] = c * r1.w;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = 0.f;
+      }
+      store_split16(rx_hi, rx_lo, tc::core_offset(i, b0, rgsN), v);
+    }
+    sync_for_mma();
+    // (b) D = Lx^T diag(cs) Rx[:, half]   (M = 128, N = 256, K = Kp)
+    if (threadIdx.x == 0 && cx.ok) mma_x3(tX, lx_hi, lx_lo, rgsKp, rx_hi, rx_lo, rgsN, 1, R2, NH, Kp);
+    pair_commit_wait(cx);
+    // (c) S = A_t Sbar - D: sum of squares over both halves, chunk-end S
+    float ss = 0.f;
+    const bool last_tok = (t == ch.e - 1);
+    float* So = w.Sst[buf ^ 1][m] + (size_t)u * nel;
+    for (int c32 = 32 * half; c32 < NH; c32 += 64) {
+      float d0[16], d1[16];
+      tc::tmem_ld16(tX + lane_base + c32, d0);
+      tc::tmem_ld16(tX + lane_base + c32 + 16, d1);
+      tc::tmem_ld_wait();
+      const float* sb = Sb + (size_t)row * n + p * NH + c32;
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        const float4 s4 = *reinterpret_cast<const float4*>(sb + 4 * q4);
+        const float* d = q4 < 4 ? d0 + 4 * q4 : d1 + 4 * (q4 - 4);
+        float4 o;
+        o.x = At * s4.x - d[0]; o.y = At * s4.y - d[1]; o.z = At * s4.z - d[2]; o.w = At * s4.w - d[3];
+        ss += o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w;
+        if (last_tok) *reinterpret_cast<float4*>(So + (size_t)row * n + p * NH + c32 + 4 * q4) = o;
+      }
+    }
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float tot = 0.f;
+      for (int k2 = 0; k2 < NT2 / 32; ++k2) tot += red[k2];
+      ss_cta = tot;
+    }
+    cluster_sync2();
+    const float tot = ss_cta + ld_cluster_f(mapa2(tc::smem_u32(&ss_cta), p ^ 1u));
+    const float scale = 1.f / (sqrtf(tot) + kNsEps);
+    // (d) X_0 = S * scale -> split bf16 into this CTA's half of X
+    for (int c32 = 32 * half; c32 < NH; c32 += 64) {
+      float d[32];
+      tc::tmem_ld16(tX + lane_base + c32, d);
+      tc::tmem_ld16(tX + lane_base + c32 + 16, d + 16);
+      tc::tmem_ld_wait();
+      const float* sb = Sb + (size_t)row * n + p * NH + c32;
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        const float4 s0 = *reinterpret_cast<const float4*>(sb + 8 * q8);
+        const float4 s1 = *reinterpret_cast<const float4*>(sb + 8 * q8 + 4);
+        const float* dd = d + 8 * q8;
+        const float v[8] = {(At * s0.x - dd[0]) * scale, (At * s0.y - dd[1]) * scale, (At * s0.z - dd[2]) * scale,
+                            (At * s0.w - dd[3]) * scale, (At * s1.x - dd[4]) * scale, (At * s1.y - dd[5]) * scale,
+                            (At * s1.z - dd[6]) * scale, (At * s1.w - dd[7]) * scale};
+        store_split16(x_hi, x_lo, tc::core_offset(row, c32 + 8 * q8, rgsN), v);
+      }
+    }
+    cluster_sync2();   // both CTAs read ss_cta above before the next task rewrites it
+    sync_for_mma();
+
+    float* slot = w.Ubuf + ((size_t)u * g.C + r) * slot_stride;
+    for (int mm = 0; mm < m; ++mm) slot += (size_t)g.rows[mm] * g.cols[mm];
+    for (int it = 0; it < g.ns_iters; ++it) {
+      // partial A = X_p X_p^T  (M = 128, N = 128, K = 256)
+      if (threadIdx.x == 0 && cx.ok) mma_x3(tA, x_hi, x_lo, rgsN, x_hi, x_lo, rgsN, 0, R2, R2, NH);
+      pair_commit_wait(cx);
+      float af[64];   // this thread's row, columns [64 half, 64 half + 64) of A
+      tc::tmem_ld16(tA + lane_base + 64 * half, af);
+      tc::tmem_ld16(tA + lane_base + 64 * half + 16, af + 16);
+      tc::tmem_ld16(tA + lane_base + 64 * half + 32, af + 32);
+      tc::tmem_ld16(tA + lane_base + 64 * half + 48, af + 48);
+      tc::tmem_ld_wait();
+      float* mine = xch + (size_t)(p * 2 + xpar) * R2 * R2 + (size_t)row * R2 + 64 * half;
+      const float* theirs = xch + (size_t)((p ^ 1) * 2 + xpar) * R2 * R2 + (size_t)row * R2 + 64 * half;
+#pragma unroll
+      for (int q4 = 0; q4 < 16; ++q4)
+        *reinterpret_cast<float4*>(mine + 4 * q4) = make_float4(af[4 * q4], af[4 * q4 + 1], af[4 * q4 + 2], af[4 * q4 + 3]);
+      cluster_sync2();
+#pragma unroll
+      for (int q4 = 0; q4 < 16; ++q4) {
+        const float4 o = __ldcg(reinterpret_cast<const float4*>(theirs + 4 * q4));
+        af[4 * q4] += o.x; af[4 * q4 + 1] += o.y; af[4 * q4 + 2] += o.z; af[4 * q4 + 3] += o.w;
+      }
+      xpar ^= 1;
+#pragma unroll
+      for (int q8 = 0; q8 < 8; ++q8) store_split16(a_hi, a_lo, tc::core_offset(row, 64 * half + 8 * q8, rgsR), af + 8 * q8);
+      sync_for_mma();
+      // A^2 (symmetric A: rows serve as the K-major B operand)
+      if (threadIdx.x == 0 && cx.ok) mma_x3(tA2, a_hi, a_lo, rgsR, a_hi, a_lo, rgsR, 0, R2, R2, R2);
+      pair_commit_wait(cx);
+      for (int q = 0; q < 64; q += 16) {
+        float a2[16];
+        tc::tmem_ld16(tA2 + lane_base + 64 * half + q, a2);
+        tc::tmem_ld_wait();
+        float bp[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          bp[j] = kNsB * af[q + j] + kNsC * a2[j] + (row == 64 * half + q + j ? kNsA : 0.f);
+        store_split16(a_hi, a_lo, tc::core_offset(row, 64 * half + q, rgsR), bp);
+        store_split16(a_hi, a_lo, tc::core_offset(row, 64 * half + q + 8, rgsR), bp + 8);
+      }
+      sync_for_mma();
+      // X_p <- B' X_p  (M = 128, N = 256, K = 128; X read as MN-major)
+      if (threadIdx.x == 0 && cx.ok) mma_x3(tX, a_hi, a_lo, rgsR, x_hi, x_lo, rgsN, 1, R2, NH, R2);
+      pair_commit_wait(cx);
+      const bool last = (it == g.ns_iters - 1);
+      for (int c32 = 32 * half; c32 < NH; c32 += 64) {
+        float v[32];
+        tc::tmem_ld16(tX + lane_base + c32, v);
+        tc::tmem_ld16(tX + lane_base + c32 + 16, v + 16);
+        tc::tmem_ld_wait();
+        if (last) {
+          float4* o = reinterpret_cast<float4*>(slot + (size_t)row * n + p * NH + c32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) store_split16(x_hi, x_lo, tc::core_offset(row, c32 + 8 * q8, rgsN), v + 8 * q8);
+        }
+      }
+      sync_for_mma();
+    }
+  }
+  if (!cx.ok && threadIdx.x == 0) atomicExch(w.status, ATLAS_ERR_TIMEOUT);
+  tc::fence_before_sync();
+  __syncthreads();
+  cluster_sync2();
+  if (warp == 0) tc::tmem_dealloc(tbase, 512);
+}
+
+// transpose every unit's rows x cols matrix into cols x rows
+__global__ void k_transpose_units(const float* __restrict__ in, float* __restrict__ out, int rows, int cols) {
+  __shared__ float tile[32][33];
+  const int u = blockIdx.z;
+  const float* src = in + (size_t)u * rows * cols;
+  float* dst = out + (size_t)u * rows * cols;
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[i][threadIdx.x] = src[(size_t)r * cols + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int c = c0 + i, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) dst[(size_t)c * rows + r] = tile[threadIdx.x][i];
+  }
+}
+
+// 0: not covered; 1: short side 64 (one CTA per task); 2: 128 x 512 (CTA pairs)
+int ns_tc_kind(const Geom& g) {
+  if (g.ns_iters <= 0) return 0;
+  const int Kp = (g.Kw + 15) / 16 * 16;
+  if (Kp > 128) return 0;
+  int kind = -1, n0 = -1;
   for (int m = 0; m < g.nmat; ++m) {
     const int s = g.rows[m] < g.cols[m] ? g.rows[m] : g.cols[m];
     const int l = g.rows[m] < g.cols[m] ? g.cols[m] : g.rows[m];
-    if (s != R || l % 16 || l > 256) return false;
-    if (n0 >= 0 && l != n0) return false;
+    int k = 0;
+    if (s == R && l % 16 == 0 && l <= 256) k = 1;
+    if (s == R2 && l == 2 * NH && Kp <= 96) k = 2;
+    if (!k || (kind >= 0 && k != kind) || (n0 >= 0 && l != n0)) return 0;
+    kind = k;
     n0 = l;
   }
-  const int Kp = (g.Kw + 15) / 16 * 16;
-  if (Kp > 128) return false;
-  return ns_smem_layout(n0, Kp).total <= 200 * 1024;
+  if (kind == 1 && ns_smem_layout(n0, Kp).total > 200 * 1024) return 0;
+  return kind;
+}
+
+bool ns_tc_supported(const Geom& g) { return ns_tc_kind(g) != 0; }
+
+size_t ns_tc_xch_floats(const Geom& g, int num_sms) {
+  return ns_tc_kind(g) == 2 ? (size_t)(num_sms / 2) * XCH_FLOATS : 0;
+}
+
+// momentum state of the tensor-core path: transposed (X orientation) for
+// matrices with rows > cols
+cudaError_t ns_tc_state_in(const Geom& g, int m, const float* src, float* dst, cudaStream_t st) {
+  const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
+  if (g.rows[m] <= g.cols[m]) return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st);
+  dim3 grid((g.cols[m] + 31) / 32, (g.rows[m] + 31) / 32, g.units);
+  k_transpose_units<<<grid, dim3(32, 8), 0, st>>>(src, dst, g.rows[m], g.cols[m]);
+  return cudaGetLastError();
+}
+
+cudaError_t ns_tc_state_out(const Geom& g, int m, const float* src, float* dst, cudaStream_t st) {
+  const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
+  if (g.rows[m] <= g.cols[m]) return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st);
+  dim3 grid((g.rows[m] + 31) / 32, (g.cols[m] + 31) / 32, g.units);
+  k_transpose_units<<<grid, dim3(32, 8), 0, st>>>(src, dst, g.cols[m], g.rows[m]);
+  return cudaGetLastError();
 }
 
 cudaError_t ns_tc_launch(const Geom& g, const Chunk& ch, const Work& w, int buf, size_t slot_stride, int num_sms,
                          cudaStream_t st) {
   const int n = g.rows[0] < g.cols[0] ? g.cols[0] : g.rows[0];
   const int Kp = (g.Kw + 15) / 16 * 16;
+  if (ns_tc_kind(g) == 2) {
+    cudaError_t e = cudaFuncSetAttribute(k_ns_tc128, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2);
+    if (e != cudaSuccess) return e;
+    const int ntasks = g.units * g.nmat * (ch.e - ch.s);
+    int ncl = num_sms / 2;
+    if (ncl > ntasks) ncl = ntasks;
+    k_ns_tc128<<<2 * ncl, NT2, SMEM2, st>>>(g, ch, w, buf, slot_stride, Kp);
+    return cudaGetLastError();
+  }
   const int smem = ns_smem_layout(n, Kp).total;
   cudaFuncSetAttribute(k_ns_tc64, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   const int ntasks = g.units * g.nmat * (ch.e - ch.s);
