@@ -561,6 +561,10 @@ size_t generic_smem_ns(const Geom& g, int m) {
   return (size_t)(2 * rX * rX + 2 * 16 * 64) * sizeof(float);
 }
 
+bool ns_fused_scan_supported(const Geom& g);
+cudaError_t ns_fused_scan(const Geom& g, const Chunk& ch, const Work& w, int buf, size_t slot_stride,
+                          const float* alpha, float* aq, float* y, cudaStream_t st);
+
 cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const GenericIO& io, int buf,
                           cudaStream_t st, int* nl) {
   *nl += g.ns_iters == 0 ? 3 + g.nmat : 3 + 2 * g.nmat;
@@ -591,6 +595,10 @@ cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const G
     k_ns_simt<<<dim3(ch.e - ch.s, g.units), 256, sn, st>>>(g, ch, w, buf, m, slot_stride, off);
     off += (size_t)g.rows[m] * g.cols[m];
   }
+  if (ns_fused_scan_supported(g)) {
+    *nl -= 1;   // two fused launches replace nmat scans + one read-out
+    return ns_fused_scan(g, ch, w, buf, slot_stride, io.alpha, w.Zpre, io.y, st);
+  }
   off = 0;
   for (int m = 0; m < g.nmat; ++m) {
     const size_t n = (size_t)g.rows[m] * g.cols[m];
@@ -610,6 +618,148 @@ cudaError_t generic_cache_out(const Geom& g, const GenericIO& io, float* tmp, vo
   k_cache_gather<<<dim3(g.c - 1, g.units), 128, 0, st>>>(g, io.k, io.v, io.gamma, io.win_k, io.win_v, io.win_gamma,
                                                          tmp);
   k_cache_scatter<<<dim3(g.c - 1, g.units), 128, 0, st>>>(g, tmp, k_out, v_out, g_out);
+  return cudaGetLastError();
+}
+
+}  // namespace atlas
+
+namespace atlas {
+
+// --------------------------------------------- fused decay scan + read-out
+// Newton-Schulz path, depth 2 with W1 (F x h, F <= h) and W2 (h x d, h > d),
+// both stored per token in Ubuf in the X orientation (W1 as is, W2
+// transposed).  W_t = (1 - alpha_t) W_{t-1} + U_t is scanned in registers;
+// every U_t is read once and no W_t is written back, only W_e.
+//
+// Pass 1: z_t = r_t W1_t, aq_t = SiLU(z_t).  CTA = (unit, 32 columns of W1);
+// thread = (column j = lane, row group g = warp): rows [g * rpg, (g+1) * rpg)
+// in registers; partial dot products meet in shared memory.
+template <int RPG>
+__global__ void __launch_bounds__(256) k_ns_scan_w1(Geom g, Chunk ch, Work w, int buf, size_t slot_stride,
+                                                    const float* alpha, float* aq) {
+  __shared__ float part[8][33];
+  __shared__ float rq[64][RPG * 8 + 1];
+  const int u = blockIdx.y, jb = blockIdx.x * 32;
+  const int lane = threadIdx.x % 32, grp = threadIdx.x / 32;
+  const int F = g.F, h = g.hidden, j = jb + lane, i0 = grp * RPG;
+  const int Ct = ch.e - ch.s;
+  // queries of the chunk
+  for (int e = threadIdx.x; e < Ct * F; e += 256) rq[e / F][e % F] = w.R[((size_t)u * g.T + ch.s + e / F) * F + e % F];
+  float W[RPG];
+  const float* Wb = w.Wst[buf][0] + (size_t)u * F * h;
+#pragma unroll
+  for (int q = 0; q < RPG; ++q) W[q] = Wb[(size_t)(i0 + q) * h + j];
+  __syncthreads();
+  const float* slot0 = w.Ubuf + (size_t)u * g.C * slot_stride;
+  float nxt[RPG];
+#pragma unroll
+  for (int q = 0; q < RPG; ++q) nxt[q] = slot0[(size_t)(i0 + q) * h + j];
+  for (int r = 0; r < Ct; ++r) {
+    float cur[RPG];
+#pragma unroll
+    for (int q = 0; q < RPG; ++q) cur[q] = nxt[q];
+    if (r + 1 < Ct) {   // next token's U in flight while this one is used
+      const float* sl = slot0 + (size_t)(r + 1) * slot_stride;
+#pragma unroll
+      for (int q = 0; q < RPG; ++q) nxt[q] = sl[(size_t)(i0 + q) * h + j];
+    }
+    const float be = 1.f - alpha[(size_t)u * g.T + ch.s + r];
+    float z = 0.f;
+#pragma unroll
+    for (int q = 0; q < RPG; ++q) {
+      W[q] = be * W[q] + cur[q];
+      z += rq[r][i0 + q] * W[q];
+    }
+    part[grp][lane] = z;
+    __syncthreads();
+    if (grp == 0) {
+      float s = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) s += part[k][lane];
+      aq[((size_t)u * g.C + r) * h + j] = siluf_(s);
+    }
+    __syncthreads();
+  }
+  float* Wo = w.Wst[buf ^ 1][0] + (size_t)u * F * h;
+#pragma unroll
+  for (int q = 0; q < RPG; ++q) Wo[(size_t)(i0 + q) * h + j] = W[q];
+}
+
+// Pass 2: y_t = r_t + aq_t W2_t.  One warp per row k of W2^T (d x h): lane
+// holds columns [lane * CPL, (lane + 1) * CPL); a shuffle sum over the warp
+// gives y_t[k].
+template <int CPL>
+__global__ void __launch_bounds__(256) k_ns_scan_w2(Geom g, Chunk ch, Work w, int buf, size_t slot_stride,
+                                                    const float* alpha, const float* aq, float* y) {
+  extern __shared__ float aqs[];   // [Ct][h]
+  const int u = blockIdx.y;
+  const int lane = threadIdx.x % 32, k = blockIdx.x * 8 + threadIdx.x / 32;
+  const int F = g.F, h = g.hidden, d = g.d_v, j0 = lane * CPL;
+  const int Ct = ch.e - ch.s;
+  for (int e = threadIdx.x; e < Ct * h; e += 256) aqs[e] = aq[(size_t)u * g.C * h + e];
+  float W[CPL];
+  const float* Wb = w.Wst[buf][1] + (size_t)u * h * d;   // original orientation [h][d]
+#pragma unroll
+  for (int q = 0; q < CPL; ++q) W[q] = Wb[(size_t)(j0 + q) * d + k];
+  __syncthreads();
+  const float* slot0 = w.Ubuf + (size_t)u * g.C * slot_stride + (size_t)F * h + (size_t)k * h + j0;
+  float nxt[CPL];
+#pragma unroll
+  for (int q = 0; q < CPL; q += 4) *reinterpret_cast<float4*>(nxt + q) = *reinterpret_cast<const float4*>(slot0 + q);
+  for (int r = 0; r < Ct; ++r) {
+    float cur[CPL];
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) cur[q] = nxt[q];
+    if (r + 1 < Ct) {
+      const float* sl = slot0 + (size_t)(r + 1) * slot_stride;
+#pragma unroll
+      for (int q = 0; q < CPL; q += 4) *reinterpret_cast<float4*>(nxt + q) = *reinterpret_cast<const float4*>(sl + q);
+    }
+    const float be = 1.f - alpha[(size_t)u * g.T + ch.s + r];
+    float acc = 0.f;
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) {
+      W[q] = be * W[q] + cur[q];
+      acc += aqs[r * h + j0 + q] * W[q];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+      const size_t yi = ((size_t)u * g.T + ch.s + r) * d + k;
+      y[yi] = w.R[((size_t)u * g.T + ch.s + r) * F + k] + acc;
+    }
+  }
+  float* Wo = w.Wst[buf ^ 1][1] + (size_t)u * h * d;
+#pragma unroll
+  for (int q = 0; q < CPL; ++q) Wo[(size_t)(j0 + q) * d + k] = W[q];
+}
+
+bool ns_fused_scan_supported(const Geom& g) {
+  if (g.depth != 2 || g.ns_iters <= 0) return false;
+  const int F = g.F, h = g.hidden, d = g.d_v;
+  if (!(F <= h && h > d)) return false;              // W1 not tall, W2 tall
+  if (h % 32 || d % 8 || F % 8) return false;
+  if (!((F / 8 == 8) || (F / 8 == 16))) return false;   // row groups of 8 or 16
+  if (!((h / 32 == 8) || (h / 32 == 16))) return false; // 8 or 16 columns per lane
+  if (g.C > 64) return false;
+  return true;
+}
+
+cudaError_t ns_fused_scan(const Geom& g, const Chunk& ch, const Work& w, int buf, size_t slot_stride,
+                          const float* alpha, float* aq, float* y, cudaStream_t st) {
+  const int F = g.F, h = g.hidden, d = g.d_v;
+  dim3 g1(h / 32, g.units);
+  if (F / 8 == 8) k_ns_scan_w1<8><<<g1, 256, 0, st>>>(g, ch, w, buf, slot_stride, alpha, aq);
+  else k_ns_scan_w1<16><<<g1, 256, 0, st>>>(g, ch, w, buf, slot_stride, alpha, aq);
+  const size_t sm2 = (size_t)(ch.e - ch.s) * h * sizeof(float);
+  dim3 g2(d / 8, g.units);
+  if (h / 32 == 8) {
+    cudaFuncSetAttribute(k_ns_scan_w2<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);
+    k_ns_scan_w2<8><<<g2, 256, sm2, st>>>(g, ch, w, buf, slot_stride, alpha, aq, y);
+  } else {
+    cudaFuncSetAttribute(k_ns_scan_w2<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);
+    k_ns_scan_w2<16><<<g2, 256, sm2, st>>>(g, ch, w, buf, slot_stride, alpha, aq, y);
+  }
   return cudaGetLastError();
 }
 
