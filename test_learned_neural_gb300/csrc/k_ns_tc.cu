@@ -179,26 +179,15 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
     const size_t nel = (size_t)rows * cols;
     const float* Sb = w.Sst[buf][m] + (size_t)u * nel;
 
-    // (a) factors -> split-bf16 operands (zero rows beyond the window)
-    for (int e = threadIdx.x; e < Kp * (R / 8); e += NT) {
-      const int i = e / (R / 8), a0 = (e % (R / 8)) * 8;
+    // (a) factors -> split-bf16 operands (zero rows beyond the window).
+    // Lx^T is the K-major A operand: thread = (row a, 8 window rows), one
+    // 16-byte chunk of the core layout per array.
+    for (int e = threadIdx.x; e < R * (Kp / 8); e += NT) {
+      const int a = e % R, i0 = (e / R) * 8;
       float v[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) v[q] = 0.f;
-      if (i < ch.nw) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = Lf[(size_t)i * lstride + a0 + q];
-      }
-      // Lx^T is the K-major A operand: row = short index a, k = window row i
-      uint16_t h[8], l[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) tc::split_bf16(v[q], h[q], l[q]);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint32_t off = tc::core_offset(a0 + q, i, rgsKp);
-        *reinterpret_cast<uint16_t*>(lx_hi + off) = h[q];
-        *reinterpret_cast<uint16_t*>(lx_lo + off) = l[q];
-      }
+      for (int q = 0; q < 8; ++q) v[q] = (i0 + q < ch.nw) ? Lf[(size_t)(i0 + q) * lstride + a] : 0.f;
+      store_split16(lx_hi, lx_lo, tc::core_offset(a, i0, rgsKp), v);
     }
     for (int e = threadIdx.x; e < Kp * (n / 8); e += NT) {
       const int i = e / (n / 8), b0 = (e % (n / 8)) * 8;
@@ -342,16 +331,15 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
 // -> 128 MLP memory).  X in split bf16 (256 KB) does not fit one SM, so a
 // cluster of two CTAs shares each task: CTA p holds columns [256 p, 256 p +
 // 256) of X.  X X^T = sum of the two halves' Gram matrices: each CTA writes
-// its partial (fp32) to a double-buffered L2 scratch, one cluster barrier,
-// and each adds the partner's.  A^2 and B' are formed redundantly by both;
-// X <- B' X splits by columns with no exchange.
+// its partial (fp32) into the partner's A/B' buffer over DSMEM between two
+// cluster barriers, and each adds the partner's.  A^2 and B' are formed
+// redundantly by both; X <- B' X splits by columns with no exchange.
 namespace {
 
 constexpr int R2 = 128, NH = 256, NT2 = 256;
 constexpr int OPR2 = 131072;                    // factors (120 KB) / X hi+lo (128 KB)
 constexpr int AB2 = 65536;                      // A / B' hi+lo
 constexpr int SMEM2 = OPR2 + AB2;
-constexpr int XCH_FLOATS = 2 * 2 * R2 * R2;     // per cluster: 2 CTAs x 2 buffers
 
 __device__ __forceinline__ uint32_t cluster_rank2() {
   uint32_t r;
@@ -414,7 +402,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
   tc::fence_after_sync();
   const uint32_t tA = tbase, tA2 = tbase + 128, tX = tbase + 256;
   PairCtx cx{&bar, 0u, true};
-  int xpar = 0;
 
   const int lxb = R2 * Kp * 2, rxb = Kp * NH * 2;
   uint8_t* lx_hi = sm;
@@ -426,7 +413,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
   uint8_t* a_hi = sm + OPR2;
   uint8_t* a_lo = sm + OPR2 + R2 * R2 * 2;
   const int rgsKp = (Kp / 8) * 128, rgsN = (NH / 8) * 128, rgsR = (R2 / 8) * 128;
-  float* xch = w.xch + (size_t)cl * XCH_FLOATS;
 
   const int Ct = ch.e - ch.s;
   const int ntasks = g.units * g.nmat * Ct;
@@ -457,21 +443,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
     const size_t nel = (size_t)rows * cols;
     const float* Sb = w.Sst[buf][m] + (size_t)u * nel;   // X orientation [128][512]
 
-    // (a) factors: Lx^T (K-major [128][Kp]) and this CTA's columns of diag(cs) Rx
-    for (int e = threadIdx.x; e < Kp * (R2 / 8); e += NT2) {
-      const int i = e / (R2 / 8), a0 = (e % (R2 / 8)) * 8;
+    // (a) factors: Lx^T (K-major [128][Kp]; thread = (row a, 8 window rows))
+    // and this CTA's columns of diag(cs) Rx
+    for (int e = threadIdx.x; e < R2 * (Kp / 8); e += NT2) {
+      const int a = e % R2, i0 = (e / R2) * 8;
       float v[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) v[q] = i < ch.nw ? Lf[(size_t)i * lstride + a0 + q] : 0.f;
-      uint16_t h[8], l[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) tc::split_bf16(v[q], h[q], l[q]);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint32_t off = tc::core_offset(a0 + q, i, rgsKp);
-        *reinterpret_cast<uint16_t*>(lx_hi + off) = h[q];
-        *reinterpret_cast<uint16_t*>(lx_lo + off) = l[q];
-      }
+      for (int q = 0; q < 8; ++q) v[q] = (i0 + q < ch.nw) ? Lf[(size_t)(i0 + q) * lstride + a] : 0.f;
+      store_split16(lx_hi, lx_lo, tc::core_offset(a, i0, rgsKp), v);
     }
     for (int e = threadIdx.x; e < Kp * (NH / 8); e += NT2) {
       const int i = e / (NH / 8), b0 = (e % (NH / 8)) * 8;
@@ -493,26 +472,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
     // (b) D = Lx^T diag(cs) Rx[:, half]   (M = 128, N = 256, K = Kp)
     if (threadIdx.x == 0 && cx.ok) mma_x3(tX, lx_hi, lx_lo, rgsKp, rx_hi, rx_lo, rgsN, 1, R2, NH, Kp);
     pair_commit_wait(cx);
-    // (c) S = A_t Sbar - D: sum of squares over both halves, chunk-end S
+    // (c) S = A_t Sbar - D, written back over D in TMEM; sum of squares over
+    // both halves; chunk-end S
     float ss = 0.f;
     const bool last_tok = (t == ch.e - 1);
     float* So = w.Sst[buf ^ 1][m] + (size_t)u * nel;
     for (int c32 = 32 * half; c32 < NH; c32 += 64) {
-      float d0[16], d1[16];
-      tc::tmem_ld16(tX + lane_base + c32, d0);
-      tc::tmem_ld16(tX + lane_base + c32 + 16, d1);
-      tc::tmem_ld_wait();
+      float d[32];
+      tc::tmem_ld16(tX + lane_base + c32, d);
+      tc::tmem_ld16(tX + lane_base + c32 + 16, d + 16);
       const float* sb = Sb + (size_t)row * n + p * NH + c32;
+      float4 s4[8];
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) s4[q4] = *reinterpret_cast<const float4*>(sb + 4 * q4);
+      tc::tmem_ld_wait();
 #pragma unroll
       for (int q4 = 0; q4 < 8; ++q4) {
-        const float4 s4 = *reinterpret_cast<const float4*>(sb + 4 * q4);
-        const float* d = q4 < 4 ? d0 + 4 * q4 : d1 + 4 * (q4 - 4);
-        float4 o;
-        o.x = At * s4.x - d[0]; o.y = At * s4.y - d[1]; o.z = At * s4.z - d[2]; o.w = At * s4.w - d[3];
-        ss += o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w;
-        if (last_tok) *reinterpret_cast<float4*>(So + (size_t)row * n + p * NH + c32 + 4 * q4) = o;
+        float* o = d + 4 * q4;
+        o[0] = At * s4[q4].x - o[0]; o[1] = At * s4[q4].y - o[1];
+        o[2] = At * s4[q4].z - o[2]; o[3] = At * s4[q4].w - o[3];
+        ss += o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
+        if (last_tok) *reinterpret_cast<float4*>(So + (size_t)row * n + p * NH + c32 + 4 * q4) =
+            make_float4(o[0], o[1], o[2], o[3]);
       }
+      tc::tmem_st16(tX + lane_base + c32, d);
+      tc::tmem_st16(tX + lane_base + c32 + 16, d + 16);
     }
+    tc::tmem_st_wait();
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (lane == 0) red[warp] = ss;
     __syncthreads();
@@ -530,17 +516,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
       tc::tmem_ld16(tX + lane_base + c32, d);
       tc::tmem_ld16(tX + lane_base + c32 + 16, d + 16);
       tc::tmem_ld_wait();
-      const float* sb = Sb + (size_t)row * n + p * NH + c32;
 #pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
-        const float4 s0 = *reinterpret_cast<const float4*>(sb + 8 * q8);
-        const float4 s1 = *reinterpret_cast<const float4*>(sb + 8 * q8 + 4);
-        const float* dd = d + 8 * q8;
-        const float v[8] = {(At * s0.x - dd[0]) * scale, (At * s0.y - dd[1]) * scale, (At * s0.z - dd[2]) * scale,
-                            (At * s0.w - dd[3]) * scale, (At * s1.x - dd[4]) * scale, (At * s1.y - dd[5]) * scale,
-                            (At * s1.z - dd[6]) * scale, (At * s1.w - dd[7]) * scale};
-        store_split16(x_hi, x_lo, tc::core_offset(row, c32 + 8 * q8, rgsN), v);
-      }
+      for (int q = 0; q < 32; ++q) d[q] *= scale;
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) store_split16(x_hi, x_lo, tc::core_offset(row, c32 + 8 * q8, rgsN), d + 8 * q8);
     }
     cluster_sync2();   // both CTAs read ss_cta above before the next task rewrites it
     sync_for_mma();
@@ -557,18 +536,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
       tc::tmem_ld16(tA + lane_base + 64 * half + 32, af + 32);
       tc::tmem_ld16(tA + lane_base + 64 * half + 48, af + 48);
       tc::tmem_ld_wait();
-      float* mine = xch + (size_t)(p * 2 + xpar) * R2 * R2 + (size_t)row * R2 + 64 * half;
-      const float* theirs = xch + (size_t)((p ^ 1) * 2 + xpar) * R2 * R2 + (size_t)row * R2 + 64 * half;
-#pragma unroll
-      for (int q4 = 0; q4 < 16; ++q4)
-        *reinterpret_cast<float4*>(mine + 4 * q4) = make_float4(af[4 * q4], af[4 * q4 + 1], af[4 * q4 + 2], af[4 * q4 + 3]);
+      // exchange through the partner's A/B' buffer (free now: both CTAs are
+      // past their B'X product), as fp32 [row][col]
       cluster_sync2();
+      {
+        const uint32_t dst = mapa2(tc::smem_u32(sm + OPR2) + (uint32_t)((row * R2 + 64 * half) * 4), p ^ 1u);
 #pragma unroll
-      for (int q4 = 0; q4 < 16; ++q4) {
-        const float4 o = __ldcg(reinterpret_cast<const float4*>(theirs + 4 * q4));
-        af[4 * q4] += o.x; af[4 * q4 + 1] += o.y; af[4 * q4 + 2] += o.z; af[4 * q4 + 3] += o.w;
+        for (int q4 = 0; q4 < 16; ++q4)
+          asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16 * q4), "f"(af[4 * q4]),
+                       "f"(af[4 * q4 + 1]), "f"(af[4 * q4 + 2]), "f"(af[4 * q4 + 3])
+                       : "memory");
       }
-      xpar ^= 1;
+      cluster_sync2();
+      {
+        const float* theirs = reinterpret_cast<const float*>(sm + OPR2) + row * R2 + 64 * half;
+#pragma unroll
+        for (int q4 = 0; q4 < 16; ++q4) {
+          const float4 o = *reinterpret_cast<const float4*>(theirs + 4 * q4);
+          af[4 * q4] += o.x; af[4 * q4 + 1] += o.y; af[4 * q4 + 2] += o.z; af[4 * q4 + 3] += o.w;
+        }
+      }
+      __syncthreads();   // every partial read before the buffer takes A hi/lo
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) store_split16(a_hi, a_lo, tc::core_offset(row, 64 * half + 8 * q8, rgsR), af + 8 * q8);
       sync_for_mma();
@@ -656,7 +644,9 @@ int ns_tc_kind(const Geom& g) {
 bool ns_tc_supported(const Geom& g) { return ns_tc_kind(g) != 0; }
 
 size_t ns_tc_xch_floats(const Geom& g, int num_sms) {
-  return ns_tc_kind(g) == 2 ? (size_t)(num_sms / 2) * XCH_FLOATS : 0;
+  (void)g;
+  (void)num_sms;
+  return 0;   // the CTA pairs exchange over DSMEM: no global scratch
 }
 
 // momentum state of the tensor-core path: transposed (X orientation) for
