@@ -220,6 +220,29 @@ def run_reference(args):
     return 0
 
 
+# ------------------------------------------------------------- multi-rank
+def replica_workload(w, rank: int):
+    """Every rank runs its own batch of the same shape (weak scaling): the
+    (batch, head) units are independent, so no data crosses ranks."""
+    return w.scaled(seed=w.seed + 1000 * rank) if rank else w
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Slowest rank's value (the timed region ends when the last rank ends)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, steps: int, slowest_seconds: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world * steps / slowest_seconds
+
+
 # ------------------------------------------------------------------- ours
 def run_ours(args):
     import torch
@@ -235,8 +258,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
-    w0 = WORKLOADS[args.workload]
-    w = w0.scaled(seed=w0.seed + 1000 * rank) if rank else w0
+    w = replica_workload(WORKLOADS[args.workload], rank)
     inp = make_inputs(w)
     t = tensors_from_numpy(inp, device=dev)
     mem = Memory(w)
@@ -277,13 +299,8 @@ def run_ours(args):
     clk = clocks.stop()
     mem.status()
     step_ms = [a.elapsed_time(b) for a, b in evs]
-    total_s = sum(step_ms) / 1e3
-    if world > 1:
-        tt = torch.tensor([total_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_s = float(tt.item())
-    tokens = w.tokens * args.steps * world
-    value = tokens / total_s
+    total_s = max_over_ranks(sum(step_ms) / 1e3, dev)
+    value = job_throughput(w.tokens, world, args.steps, total_s)
 
     # end to end through the host-buffer entry point (pinned host memory)
     e2e = None
@@ -302,12 +319,8 @@ def run_ours(args):
         t0 = time.perf_counter()
         for _ in range(reps):
             mem.forward(th, out=oh, host=True)
-        e2e_s = (time.perf_counter() - t0) / reps
-        if world > 1:
-            tt = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_s = float(tt.item())
-        e2e = {"value": w.tokens * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+        e2e_s = max_over_ranks((time.perf_counter() - t0) / reps, dev)
+        e2e = {"value": job_throughput(w.tokens, world, 1, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h)}
 
     if rank != 0:

@@ -24,10 +24,10 @@
 //
 // Cs, Cw, A_t, B_t, D_t are the momentum/decay coefficients of the chunk
 // (scans over eta and 1 - alpha, see k_generic.cu).  Every product is one
-// tcgen05.mma chain (M = 64, fp16 operands, fp32 accumulation in TMEM); the
+// tcgen05.mma chain (M = 64, bf16 operands, fp32 accumulation in TMEM); the
 // operands live in shared memory in the core-matrix layout of tc.cuh, each
 // written once and read K-major or MN-major as the product needs.
-#include <cuda_fp16.h>
+#include <cuda_bf16.h>
 
 #include "atlas_common.cuh"
 #include "tc.cuh"
@@ -36,7 +36,7 @@ namespace atlas {
 namespace {
 
 constexpr int D = 64, HQ = 64, CS = 4, TOK = 64, NT = 256;
-constexpr int TILE = 64 * 64 * 2;       // fp16 64x64 operand tile
+constexpr int TILE = 64 * 64 * 2;       // bf16 64x64 operand tile
 constexpr int RGS = 1024;               // row-group stride of a 64-column tile
 constexpr int RGS2 = 2048;              // of a 128-column tile
 constexpr int F32T = 64 * 64 * 4;       // fp32 64x64 tile (swizzled rows)
@@ -49,7 +49,7 @@ constexpr int OX = OS2 + TILE, OA = OX + TILE, ODY = OA + TILE, ODZ = ODY + TILE
 constexpr int UNI = ODZ + TILE;                                   // phase-local operands
 constexpr int OR_ = UNI, OM1 = UNI + TILE, OAQ = UNI + 2 * TILE, OM2 = UNI + 3 * TILE;
 constexpr int ODZS = UNI, ODYS = UNI + 2 * TILE;                  // [cs.dz | cw.dz], [cs.dy | cw.dy]
-constexpr int OSP = UNI + 4 * TILE;                               // fp16 SiLU'(Z)
+constexpr int OSP = UNI + 4 * TILE;                               // bf16 SiLU'(Z)
 constexpr int CWM = OSP + TILE;                                   // fp32 Cw[t][i]
 constexpr int RED = CWM + F32T;                                   // 2 fp32 tiles shared over the cluster
 constexpr int VEC = RED + 2 * F32T;                               // gate vectors
@@ -86,27 +86,30 @@ __device__ __forceinline__ float4 ld_cluster4(uint32_t addr) {
   return v;
 }
 
+// Operands are bf16: the memory's state decays over long sequences (to
+// ~1e-8 on a 4096-token Titans run) and needs fp32's exponent range; fp16
+// would flush it to zero.
 __device__ __forceinline__ void st_h8(uint8_t* tile, int rgs, int row, int col, const float* v) {
-  __half2 h[4];
+  __nv_bfloat162 h[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
   *reinterpret_cast<uint4*>(tile + tc::core_offset(row, col, rgs)) = *reinterpret_cast<uint4*>(h);
 }
 __device__ __forceinline__ void ld_h8(const uint8_t* tile, int rgs, int row, int col, float* v) {
   const uint4 u = *reinterpret_cast<const uint4*>(tile + tc::core_offset(row, col, rgs));
-  const __half2* h = reinterpret_cast<const __half2*>(&u);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 f = __half22float2(h[i]);
+    const float2 f = __bfloat1622float2(h[i]);
     v[2 * i] = f.x;
     v[2 * i + 1] = f.y;
   }
 }
 
-// 64 x N (x K) product, fp16 operands, issued by one thread.
+// 64 x N (x K) product, bf16 operands, issued by one thread.
 __device__ __forceinline__ void mma64(uint32_t d, const uint8_t* a, int a_mn, int a_rgs, const uint8_t* b, int b_mn,
                                       int b_rgs, int N, int K, bool accumulate) {
-  const uint32_t idesc = tc::idesc_f16(64, N, 0, a_mn, b_mn);
+  const uint32_t idesc = tc::idesc_f16(64, N, 1, a_mn, b_mn);
   for (int ks = 0; ks < K / 16; ++ks) {
     const uint64_t ad = a_mn ? tc::sdesc(tc::smem_u32(a) + ks * 2 * a_rgs, a_rgs, 128)
                              : tc::sdesc(tc::smem_u32(a) + ks * 256, 128, a_rgs);
