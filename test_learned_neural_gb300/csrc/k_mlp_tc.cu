@@ -89,6 +89,15 @@ __device__ __forceinline__ float4 ld_cluster4(uint32_t addr) {
 // Operands are bf16: the memory's state decays over long sequences (to
 // ~1e-8 on a 4096-token Titans run) and needs fp32's exponent range; fp16
 // would flush it to zero.
+__device__ __forceinline__ void st_cluster4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_u2(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
 __device__ __forceinline__ void st_h8(uint8_t* tile, int rgs, int row, int col, const float* v) {
   __nv_bfloat162 h[4];
 #pragma unroll
@@ -106,16 +115,19 @@ __device__ __forceinline__ void ld_h8(const uint8_t* tile, int rgs, int row, int
   }
 }
 
-// 64 x N (x K) product, bf16 operands, issued by one thread.
+// 64 x N (x K) product, bf16 operands, issued by one thread.  Each K step
+// moves the operand start address by a fixed byte count, so the descriptors
+// are built once and stepped by adding (bytes >> 4) to their address field.
 __device__ __forceinline__ void mma64(uint32_t d, const uint8_t* a, int a_mn, int a_rgs, const uint8_t* b, int b_mn,
                                       int b_rgs, int N, int K, bool accumulate) {
   const uint32_t idesc = tc::idesc_f16(64, N, 1, a_mn, b_mn);
+  uint64_t ad = a_mn ? tc::sdesc(tc::smem_u32(a), a_rgs, 128) : tc::sdesc(tc::smem_u32(a), 128, a_rgs);
+  uint64_t bd = b_mn ? tc::sdesc(tc::smem_u32(b), b_rgs, 128) : tc::sdesc(tc::smem_u32(b), 128, b_rgs);
+  const uint64_t astep = (uint64_t)((a_mn ? 2 * a_rgs : 256) >> 4), bstep = (uint64_t)((b_mn ? 2 * b_rgs : 256) >> 4);
   for (int ks = 0; ks < K / 16; ++ks) {
-    const uint64_t ad = a_mn ? tc::sdesc(tc::smem_u32(a) + ks * 2 * a_rgs, a_rgs, 128)
-                             : tc::sdesc(tc::smem_u32(a) + ks * 256, 128, a_rgs);
-    const uint64_t bd = b_mn ? tc::sdesc(tc::smem_u32(b) + ks * 2 * b_rgs, b_rgs, 128)
-                             : tc::sdesc(tc::smem_u32(b) + ks * 256, 128, b_rgs);
     tc::mma_f16(d, ad, bd, idesc, (ks > 0 || accumulate) ? 1u : 0u);
+    ad += astep;
+    bd += bstep;
   }
 }
 
@@ -286,40 +298,56 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
         vec[V_GA + tid] = pf.ga;
       }
     }
-    const Prefetch cur = pf;   // this chunk's k, v stay in registers for dy
     prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, s + TOK);
-    __syncthreads();
-    if (tid < 64) {  // column i = tid of Cs / Cw (window of token t is {t})
-      const int i = tid;
-      float cs = 0.f, cw = 0.f;
-#pragma unroll
-      for (int t = 0; t < TOK; ++t) {
-        cs = vec[V_ET + t] * cs + (t == i ? vec[V_TH + t] : 0.f);
-        cw = vec[V_BE + t] * cw + cs;
-        cwm[swz(t, i)] = cw;
-      }
-      vec[V_CS + i] = cs;
-      vec[V_CW + i] = cw;
-    } else if (tid == 64) {
-      float Ap = 1.f, Bp = 1.f, Dp = 0.f;
-#pragma unroll
-      for (int t = 0; t < TOK; ++t) {
-        Ap *= vec[V_ET + t];
-        Bp *= vec[V_BE + t];
-        Dp = vec[V_BE + t] * Dp + Ap;
-        vec[V_AP + t] = Ap;
-        vec[V_BP + t] = Bp;
-        vec[V_DP + t] = Dp;
-      }
-    }
     sync_smem_for_mma();
-    // ---------------------------------------------------------------- 1: Z, G1
+    // ---------------------------------------------------------------- 1: Z, G1, R W1, R S1
     if (tid == 0 && cx.ok) {
       mma64(tb + C_Z, sm + OX, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
       mma64(tb + C_G1, sm + OR_, 0, RGS, sm + OX, 0, RGS, 64, 64, false);
       mma64(tb + C_P1, sm + OR_, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
       mma64(tb + C_P2, sm + OR_, 0, RGS, sm + OS1, 1, RGS, 64, 64, false);
     }
+    if (tid < 64) {  // column i = tid of Cs / Cw (window of token t is {t})
+      const int i = tid;
+      float cs = 0.f, cw = 0.f;
+      for (int t0 = 0; t0 < TOK; t0 += 8) {
+        float et[8], th[8], be[8];   // loads ahead of the stores (same shared array)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          et[q] = vec[V_ET + t0 + q];
+          th[q] = vec[V_TH + t0 + q];
+          be[q] = vec[V_BE + t0 + q];
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          cs = et[q] * cs + (t0 + q == i ? th[q] : 0.f);
+          cw = be[q] * cw + cs;
+          cwm[swz(t0 + q, i)] = cw;
+        }
+      }
+      vec[V_CS + i] = cs;
+      vec[V_CW + i] = cw;
+    } else if (tid == 64) {
+      float Ap = 1.f, Bp = 1.f, Dp = 0.f;
+      for (int t0 = 0; t0 < TOK; t0 += 8) {
+        float et[8], be[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          et[q] = vec[V_ET + t0 + q];
+          be[q] = vec[V_BE + t0 + q];
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          Ap *= et[q];
+          Bp *= be[q];
+          Dp = be[q] * Dp + Ap;
+          vec[V_AP + t0 + q] = Ap;
+          vec[V_BP + t0 + q] = Bp;
+          vec[V_DP + t0 + q] = Dp;
+        }
+      }
+    }
+    __syncthreads();
     commit_wait(cx);
     {
       float z[16], g[16];
@@ -345,43 +373,48 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     // ---------------------------------------------------------------- 2: Yp = A W2q
     if (tid == 0 && cx.ok) mma64(tb + C_YP, sm + OA, 0, RGS, sm + OW2, 1, RGS, 64, 64, false);
     commit_wait(cx);
-    // cluster-shared buffers: RED holds this slice's Yp, RED + F32T its Yq.
-    // Yp(n+1) is written after the second cluster barrier of chunk n, when
-    // every peer has read Yp(n); Yq(n+1) after the first barrier of chunk
-    // n+1, when every peer has read Yq(n).
-    float* redb = reinterpret_cast<float*>(sm + RED);
+    // Cross-slice sums are reduce-scatters over DSMEM: CTA p owns rows
+    // [16p, 16p + 16).  Every CTA pushes the row quarter of its partial to the
+    // owner's slot [sender][row % 16][col] (fire-and-forget remote stores),
+    // the owner sums its four slots locally.  RED holds the Yp slots, RED +
+    // F32T the Yq slots; a slot is rewritten only after the owner has passed
+    // the barrier that follows its reads.
     {
       float yp[16];
       tc::tmem_ld16_x2(tb + lb + C_YP, yp);
       tc::tmem_ld_wait();
+      const uint32_t dst = mapa(red_local + (uint32_t)(((qr * 16 + (row & 15)) * 64 + cb) * 4), (uint32_t)(row >> 4));
 #pragma unroll
-      for (int i = 0; i < 16; i += 4)
-        *reinterpret_cast<float4*>(redb + swz(row, cb + i)) = make_float4(yp[i], yp[i + 1], yp[i + 2], yp[i + 3]);
+      for (int i = 0; i < 16; i += 4) st_cluster4(dst + 4 * i, make_float4(yp[i], yp[i + 1], yp[i + 2], yp[i + 3]));
     }
     cluster_sync();
-    // dy = 2 gamma (X + sum_q Yp_q - V): every CTA forms all of it
+    // dy = 2 gamma (X + sum Yp - V) for my 16 rows, broadcast as bf16 into
+    // every CTA's dy operand tile
     {
-      const int r = tid % 64, g = tid / 64;
-      const float g2 = 2.f * vec[V_GA + r];
-      for (int j = 0; j < 2; ++j) {
-        const int cc = (g + 4 * j) * 8;
-        float acc[8], xk[8], vv[8], dy[8];
+      const float* red = reinterpret_cast<const float*>(sm + RED);
+      const int rl = tid >> 4, cc = (tid & 15) * 4, r = 16 * (int)qr + rl;
+      const size_t gb = ((size_t)u * T + s + r) * D + cc;
+      float xk[4], vv[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll
-        for (int p = 0; p < CS; ++p)
-#pragma unroll
-          for (int h4 = 0; h4 < 2; ++h4) {
-            const float4 t4 = ld_cluster4(mapa(red_local + (uint32_t)(swz(r, cc + 4 * h4) * 4), p));
-            acc[4 * h4] += t4.x; acc[4 * h4 + 1] += t4.y; acc[4 * h4 + 2] += t4.z; acc[4 * h4 + 3] += t4.w;
-          }
-        unpack8(cur.k[j], dt, xk);
-        unpack8(cur.v[j], dt, vv);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) dy[i] = g2 * (xk[i] + acc[i] - vv[i]);
-        st_h8(sm + ODY, RGS, r, cc, dy);
+      for (int i = 0; i < 4; ++i) {
+        xk[i] = ld_in(k, gb + i, dt);
+        vv[i] = ld_in(v, gb + i, dt);
       }
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int p = 0; p < CS; ++p) {
+        const float4 t4 = *reinterpret_cast<const float4*>(red + (p * 16 + rl) * 64 + cc);
+        acc.x += t4.x; acc.y += t4.y; acc.z += t4.z; acc.w += t4.w;
+      }
+      const float g2 = 2.f * vec[V_GA + r];
+      const __nv_bfloat162 h0 = __floats2bfloat162_rn(g2 * (xk[0] + acc.x - vv[0]), g2 * (xk[1] + acc.y - vv[1]));
+      const __nv_bfloat162 h1 = __floats2bfloat162_rn(g2 * (xk[2] + acc.z - vv[2]), g2 * (xk[3] + acc.w - vv[3]));
+      const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&h0), a1 = *reinterpret_cast<const uint32_t*>(&h1);
+      const uint32_t off = tc::smem_u32(sm + ODY) + tc::core_offset(r, cc, RGS);
+#pragma unroll
+      for (int p = 0; p < CS; ++p) st_cluster_u2(mapa(off, (uint32_t)p), a0, a1);
     }
+    cluster_sync();
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 3: dz' = dy W2q^T
     if (tid == 0 && cx.ok) mma64(tb + C_Z, sm + ODY, 0, RGS, sm + OW2, 0, RGS, 64, 64, false);
@@ -440,7 +473,6 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     // ---------------------------------------------------------------- 6: Q3 = M2 dy, Yq
     if (tid == 0 && cx.ok) mma64(tb + C_Q3, sm + OM2, 0, RGS, sm + ODY, 1, RGS, 64, 64, false);
     commit_wait(cx);
-    float* redy = reinterpret_cast<float*>(sm + RED + F32T);
     {
       const float Bt = vec[V_BP + row], Dt = vec[V_DP + row];
       float q1[16], q2[16], q3[16];
@@ -448,6 +480,8 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       tc::tmem_ld16_x2(tb + lb + C_Q2, q2);
       tc::tmem_ld16_x2(tb + lb + C_Q3, q3);
       tc::tmem_ld_wait();
+      const uint32_t dst =
+          mapa(red_local + (uint32_t)(F32T + ((qr * 16 + (row & 15)) * 64 + cb) * 4), (uint32_t)(row >> 4));
 #pragma unroll
       for (int i = 0; i < 16; i += 4) {
         float4 o;
@@ -455,7 +489,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
         o.y = Bt * q1[i + 1] + Dt * q2[i + 1] + q3[i + 1];
         o.z = Bt * q1[i + 2] + Dt * q2[i + 2] + q3[i + 2];
         o.w = Bt * q1[i + 3] + Dt * q2[i + 3] + q3[i + 3];
-        *reinterpret_cast<float4*>(redy + swz(row, cb + i)) = o;
+        st_cluster4(dst + 4 * i, o);
       }
     }
     // state-update operands (the read-out operands are dead): diag(cs|cw) dz, dy
@@ -475,13 +509,14 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       st_h8(sm + ODYS, RGS2, r, 64 + cc, t1);
     }
     cluster_sync();
-    // y rows [16q, 16q + 16): R + sum of the four slices' Yq
-    for (int e = tid; e < 16 * 16; e += NT) {
-      const int r = 16 * (int)qr + e / 16, cc = (e % 16) * 4;
+    // y rows [16q, 16q + 16): R + the four slices' Yq from my local slots
+    {
+      const float* red = reinterpret_cast<const float*>(sm + RED + F32T);
+      const int rl = tid >> 4, cc = (tid & 15) * 4, r = 16 * (int)qr + rl;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
       for (int p = 0; p < CS; ++p) {
-        const uint32_t addr = mapa(red_local + (uint32_t)(F32T + swz(r, cc) * 4), p);
-        const float4 t4 = ld_cluster4(addr);
+        const float4 t4 = *reinterpret_cast<const float4*>(red + (p * 16 + rl) * 64 + cc);
         acc.x += t4.x; acc.y += t4.y; acc.z += t4.z; acc.w += t4.w;
       }
       const size_t gb = ((size_t)u * T + s + r) * D + cc;

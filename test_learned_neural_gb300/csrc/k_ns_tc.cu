@@ -74,16 +74,20 @@ __device__ inline void store_split16(uint8_t* hi, uint8_t* lo, uint32_t off, con
 // row-group stride bK) or MN-major [K][N] (b_mn = 1, row-group stride bK).
 __device__ inline void mma_x3(uint32_t d, const uint8_t* a_hi, const uint8_t* a_lo, int aK, const uint8_t* b_hi,
                               const uint8_t* b_lo, int bK, int b_mn, int M, int N, int K) {
+  // descriptors built once per product, stepped by (bytes >> 4) per K step
   const uint32_t idesc = tc::idesc_f16(M, N, 1, 0, b_mn);
   const uint8_t* As[3] = {a_hi, a_hi, a_lo};
   const uint8_t* Bs[3] = {b_hi, b_lo, b_hi};
-  for (int p = 0; p < 3; ++p)
+  const uint64_t bstep = (uint64_t)((b_mn ? 2 * bK : 256) >> 4);
+  for (int p = 0; p < 3; ++p) {
+    uint64_t ad = tc::sdesc(tc::smem_u32(As[p]), 128, aK);
+    uint64_t bd = b_mn ? tc::sdesc(tc::smem_u32(Bs[p]), bK, 128) : tc::sdesc(tc::smem_u32(Bs[p]), 128, bK);
     for (int ks = 0; ks < K / 16; ++ks) {
-      const uint64_t ad = tc::sdesc(tc::smem_u32(As[p]) + ks * 256, 128, aK);
-      const uint64_t bd = b_mn ? tc::sdesc(tc::smem_u32(Bs[p]) + ks * 2 * bK, bK, 128)
-                               : tc::sdesc(tc::smem_u32(Bs[p]) + ks * 256, 128, bK);
       tc::mma_f16(d, ad, bd, idesc, (p > 0 || ks > 0) ? 1u : 0u);
+      ad += 256 >> 4;
+      bd += bstep;
     }
+  }
 }
 
 // Every thread waits for the MMA group; the outcome is made uniform across
