@@ -67,7 +67,8 @@ struct Work {
   float* Bp;      // [units][C]  prod (1 - alpha) (s..t)
   float* Dp;      // [units][C]  coefficient of S_bar in W_t
   float* Ubuf;    // NS path: [units][C][sum_m rows*cols] U_t then W_t (X orientation)
-  float* xch;     // NS path, CTA pairs: Gram-matrix exchange scratch
+  float* xch;     // (unused: the CTA pairs exchange over DSMEM)
+  float* gpart;   // depth 2: per hidden block partial forward outputs [units][h/64][Kw][d_v]
   int* status;    // device status word
 };
 
@@ -87,6 +88,7 @@ cudaError_t generic_cache_out(const Geom& g, const GenericIO& io, float* tmp, vo
 size_t generic_smem_grad(const Geom& g);
 size_t generic_smem_readout(const Geom& g);
 size_t generic_smem_ns(const Geom& g, int m);
+size_t grad_part_floats(const Geom& g);
 int num_sms();
 
 // fused tensor-core MLP memory without Newton-Schulz (k_mlp_tc.cu)

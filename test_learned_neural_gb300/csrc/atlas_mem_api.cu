@@ -130,6 +130,7 @@ static Layout layout(const Geom& g, int units, int T) {
       U * (size_t)(g.c > 1 ? g.c - 1 : 0) * (g.d_k + g.d_v + 1),  // cache temp
       64,                                  // status
       ns_tc_xch_floats(g, num_sms()),      // Gram exchange of the CTA-pair Newton-Schulz
+      g.depth == 2 ? U * ((size_t)(g.hidden + 63) / 64) * Kw * g.d_v : 0,  // tiled-gradient partial outputs
   };
   const int n = sizeof sizes / sizeof sizes[0];
   size_t o = 0;
@@ -154,6 +155,7 @@ static Work work_from(const Geom& g, void* base, const Layout& L, float** cache_
   *cache_tmp = F(22);
   w.status = (int*)F(23);
   w.xch = F(24);
+  w.gpart = F(25);
   return w;
 }
 

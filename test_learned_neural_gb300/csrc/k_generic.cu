@@ -538,8 +538,19 @@ int num_sms() {
   return cached[dev];
 }
 
+size_t features_proj_smem(const Geom& g);
+bool features_proj_supported(const Geom& g);
+cudaError_t features_proj_launch(const Geom& g, const void* src, const void* cache, int rows, int from_cache,
+                                 const void* P, float* out, cudaStream_t st);
+
 cudaError_t generic_prepare(const Geom& g, const Work& w, const GenericIO& io, cudaStream_t st, int* nl) {
   *nl += 3;
+  if (features_proj_supported(g)) {
+    CUDA_CHECK_RET(features_proj_launch(g, io.k, io.win_k, g.L, 1, io.P, w.X, st));
+    CUDA_CHECK_RET(features_proj_launch(g, io.q, nullptr, g.T, 0, io.P, w.R, st));
+    k_values<<<dim3(g.L, g.units), 128, 0, st>>>(g, io.v, io.win_v, io.gamma, io.win_gamma, w.V, w.G);
+    return cudaGetLastError();
+  }
   const size_t sm_feat = (size_t)(g.d_k + (g.proj_dim ? g.poly : 0)) * sizeof(float);
   if (sm_feat > 48 * 1024) cudaFuncSetAttribute(k_features, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_feat);
   k_features<<<dim3(g.L, g.units), 128, sm_feat, st>>>(g, io.k, io.win_k, g.L, 1, io.P, w.X);
@@ -561,6 +572,7 @@ size_t generic_smem_ns(const Geom& g, int m) {
   return (size_t)(2 * rX * rX + 2 * 16 * 64) * sizeof(float);
 }
 
+cudaError_t grad_tiled(const Geom& g, const Chunk& ch, const Work& w, int buf, cudaStream_t st, int* nl);
 bool ns_fused_scan_supported(const Geom& g);
 cudaError_t ns_fused_scan(const Geom& g, const Chunk& ch, const Work& w, int buf, size_t slot_stride,
                           const float* alpha, float* aq, float* y, cudaStream_t st);
@@ -568,9 +580,14 @@ cudaError_t ns_fused_scan(const Geom& g, const Chunk& ch, const Work& w, int buf
 cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const GenericIO& io, int buf,
                           cudaStream_t st, int* nl) {
   *nl += g.ns_iters == 0 ? 3 + g.nmat : 3 + 2 * g.nmat;
-  const size_t sg = generic_smem_grad(g), sr = generic_smem_readout(g);
-  cudaFuncSetAttribute(k_grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg);
-  k_grad<<<dim3(ch.nw, g.units), 256, sg, st>>>(g, ch, w, buf);
+  const size_t sr = generic_smem_readout(g);
+  if (g.depth == 1 || ch.nw <= 128) {
+    CUDA_CHECK_RET(grad_tiled(g, ch, w, buf, st, nl));
+  } else {
+    const size_t sg = generic_smem_grad(g);
+    cudaFuncSetAttribute(k_grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg);
+    k_grad<<<dim3(ch.nw, g.units), 256, sg, st>>>(g, ch, w, buf);
+  }
   const int coef_threads = ((ch.nw + 31) / 32) * 32;
   k_coef<<<g.units, coef_threads, 0, st>>>(g, ch, io.theta, io.eta, io.alpha, w);
   if (g.ns_iters == 0) {
@@ -760,6 +777,232 @@ cudaError_t ns_fused_scan(const Geom& g, const Chunk& ch, const Work& w, int buf
     cudaFuncSetAttribute(k_ns_scan_w2<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);
     k_ns_scan_w2<16><<<g2, 256, sm2, st>>>(g, ch, w, buf, slot_stride, alpha, aq, y);
   }
+  return cudaGetLastError();
+}
+
+}  // namespace atlas
+
+namespace atlas {
+
+// --------------------------------------------- tiled gradient factors
+// The window rows' forward, error and backward at the chunk-start weights
+// as 64 x 64 register-tiled fp32 GEMMs (tile_gemm), one CTA per (unit,
+// 64-wide output block).  Same outputs as k_grad.
+
+// depth 1: dy = 2 gamma (X W - V)
+__global__ void __launch_bounds__(256) k_grad1_tiled(Geom g, Chunk ch, Work w, int buf) {
+  __shared__ float As[16 * 64], Bs[16 * 64];
+  const int u = blockIdx.z, i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
+  const float* Xw = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * g.F;
+  const float* Vw = w.V + ((size_t)u * g.L + ch.lo + g.n_prev) * g.d_v;
+  const float* Gw = w.G + (size_t)u * g.L + ch.lo + g.n_prev;
+  const float* W = w.Wst[buf][0] + (size_t)u * g.F * g.d_v;
+  float acc[4][4];
+  tile_gemm(TileOp{Xw, g.F, 1}, TileOp{W, 1, g.d_v}, ch.nw, g.d_v, g.F, i0, j0, acc, As, Bs);
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  for (int a = 0; a < 4; ++a) {
+    const int i = i0 + ty * 4 + a;
+    if (i >= ch.nw) continue;
+    for (int b = 0; b < 4; ++b) {
+      const int j = j0 + tx * 4 + b;
+      if (j < g.d_v) w.DY[((size_t)u * g.Kw + i) * g.d_v + j] = 2.f * Gw[i] * (acc[a][b] - Vw[(size_t)i * g.d_v + j]);
+    }
+  }
+}
+
+// depth 2, part 1: Z = X W1[:, jb] -> z, a = SiLU(z); partial Yhat = a W2[jb, :]
+__global__ void __launch_bounds__(256) k_grad2_fwd(Geom g, Chunk ch, Work w, int buf, float* part) {
+  __shared__ float As[16 * 64], Bs[16 * 64];
+  __shared__ float Ablk[128 * 65];
+  const int u = blockIdx.y, jb = blockIdx.x * 64, h = g.hidden;
+  const float* Xw = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * g.F;
+  const float* W1 = w.Wst[buf][0] + (size_t)u * g.F * h;
+  const float* W2 = w.Wst[buf][1] + (size_t)u * h * g.d_v;
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  for (int i0 = 0; i0 < ch.nw; i0 += 64) {
+    float acc[4][4];
+    tile_gemm(TileOp{Xw, g.F, 1}, TileOp{W1 + jb, 1, h}, ch.nw, h - jb < 64 ? h - jb : 64, g.F, i0, 0, acc, As, Bs);
+    for (int a = 0; a < 4; ++a) {
+      const int i = i0 + ty * 4 + a;
+      for (int b = 0; b < 4; ++b) {
+        const int j = tx * 4 + b;
+        const float z = acc[a][b];
+        const float av = siluf_(z);
+        if (i < ch.nw && jb + j < h) {
+          const size_t o = ((size_t)u * g.Kw + i) * h + jb + j;
+          w.Zpre[o] = z;
+          w.Aact[o] = av;
+        }
+        Ablk[i * 65 + j] = (i < ch.nw && jb + j < h) ? av : 0.f;
+      }
+    }
+  }
+  __syncthreads();
+  const int nb = (h + 63) / 64;
+  for (int i0 = 0; i0 < ch.nw; i0 += 64)
+    for (int j0 = 0; j0 < g.d_v; j0 += 64) {
+      float acc[4][4];
+      tile_gemm(TileOp{Ablk, 65, 1}, TileOp{W2 + (size_t)jb * g.d_v, 1, g.d_v}, ch.nw, g.d_v, h - jb < 64 ? h - jb : 64,
+                i0, j0, acc, As, Bs);
+      for (int a = 0; a < 4; ++a) {
+        const int i = i0 + ty * 4 + a;
+        if (i >= ch.nw) continue;
+        for (int b = 0; b < 4; ++b) {
+          const int j = j0 + tx * 4 + b;
+          if (j < g.d_v) part[(((size_t)u * nb + blockIdx.x) * g.Kw + i) * g.d_v + j] = acc[a][b];
+        }
+      }
+    }
+}
+
+// depth 2, part 2: dy = 2 gamma (X + sum of partials - V)
+__global__ void k_grad2_dy(Geom g, Chunk ch, Work w, const float* part) {
+  const int u = blockIdx.y;
+  const int nb = (g.hidden + 63) / 64;
+  const size_t n = (size_t)ch.nw * g.d_v;
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
+    const int i = (int)(e / g.d_v), j = (int)(e % g.d_v);
+    const size_t row = (size_t)u * g.L + ch.lo + g.n_prev + i;
+    float yh = w.X[row * g.F + j];   // residual (F == d_v)
+    for (int b = 0; b < nb; ++b) yh += part[(((size_t)u * nb + b) * g.Kw + i) * g.d_v + j];
+    w.DY[((size_t)u * g.Kw + i) * g.d_v + j] = 2.f * w.G[row] * (yh - w.V[row * g.d_v + j]);
+  }
+}
+
+// depth 2, part 3: dz[:, jb] = (dy W2[jb, :]^T) * SiLU'(z)
+__global__ void __launch_bounds__(256) k_grad2_dz(Geom g, Chunk ch, Work w, int buf) {
+  __shared__ float As[16 * 64], Bs[16 * 64];
+  const int u = blockIdx.z, i0 = blockIdx.y * 64, jb = blockIdx.x * 64, h = g.hidden;
+  const float* DYw = w.DY + (size_t)u * g.Kw * g.d_v;
+  const float* W2 = w.Wst[buf][1] + (size_t)u * h * g.d_v;
+  float acc[4][4];
+  tile_gemm(TileOp{DYw, g.d_v, 1}, TileOp{W2 + (size_t)jb * g.d_v, g.d_v, 1}, ch.nw, h - jb < 64 ? h - jb : 64, g.d_v,
+            i0, 0, acc, As, Bs);
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  for (int a = 0; a < 4; ++a) {
+    const int i = i0 + ty * 4 + a;
+    if (i >= ch.nw) continue;
+    for (int b = 0; b < 4; ++b) {
+      const int j = jb + tx * 4 + b;
+      if (j < h) {
+        const size_t o = ((size_t)u * g.Kw + i) * h + j;
+        w.DZ[o] = acc[a][b] * dsiluf_(w.Zpre[o]);
+      }
+    }
+  }
+}
+
+size_t grad_part_floats(const Geom& g) {
+  return g.depth == 2 ? (size_t)g.units * ((g.hidden + 63) / 64) * g.Kw * g.d_v : 0;
+}
+
+cudaError_t grad_tiled(const Geom& g, const Chunk& ch, const Work& w, int buf, cudaStream_t st, int* nl) {
+  const int rt = (ch.nw + 63) / 64;
+  if (g.depth == 1) {
+    k_grad1_tiled<<<dim3((g.d_v + 63) / 64, rt, g.units), 256, 0, st>>>(g, ch, w, buf);
+    return cudaGetLastError();
+  }
+  if (ch.nw > 128) return cudaErrorInvalidValue;   // Ablk holds 128 window rows
+  const int nb = (g.hidden + 63) / 64;
+  k_grad2_fwd<<<dim3(nb, g.units), 256, 0, st>>>(g, ch, w, buf, w.gpart);
+  k_grad2_dy<<<dim3(4, g.units), 256, 0, st>>>(g, ch, w, w.gpart);
+  k_grad2_dz<<<dim3(nb, rt, g.units), 256, 0, st>>>(g, ch, w, buf);
+  *nl += 2;
+  return cudaGetLastError();
+}
+
+}  // namespace atlas
+
+namespace atlas {
+
+// ------------------------------------------- projected polynomial features
+// out = phi(x) P for 64 token rows per CTA as a register-tiled fp32 GEMM;
+// phi is generated tile by tile from the raw rows held in shared memory
+// (pair indices of the degree-2 monomials tabulated once per CTA).
+__global__ void __launch_bounds__(256) k_features_proj(Geom g, const void* src, const void* cache, int rows_per_unit,
+                                                      int from_cache, const void* P, float* out) {
+  extern __shared__ float smf[];
+  float* xs = smf;                              // [64][d_k + 1]
+  float* As = xs + 64 * (g.d_k + 1);            // [16][64] phi tile (k-major)
+  float* Bs = As + 16 * 64;                     // [16][64] P tile
+  unsigned short* pij = reinterpret_cast<unsigned short*>(Bs + 16 * 64);   // [poly] (i << 8) | j
+  const int u = blockIdx.y, r0 = blockIdx.x * 64, d = g.d_k, ld = d + 1;
+  for (int e = threadIdx.x; e < 64 * d; e += blockDim.x) {
+    const int rr = e / d, k = e % d, row = r0 + rr;
+    float val = 0.f;
+    if (row < rows_per_unit) {
+      if (from_cache && row < g.n_prev) {
+        const size_t slot = (size_t)(g.c - 1 - g.n_prev + row);
+        val = load_in(cache, ((size_t)u * (g.c - 1) + slot) * d + k, g.qkv_dtype);
+      } else {
+        const int t = row - (from_cache ? g.n_prev : 0);
+        val = load_in(src, ((size_t)u * g.T + t) * d + k, g.qkv_dtype);
+      }
+    }
+    xs[rr * ld + k] = val;
+  }
+  for (int f = threadIdx.x; f < g.poly; f += blockDim.x) {
+    int i = 0, jj = 0;
+    if (f > d) {
+      int q = f - 1 - d;
+      while (q >= d - i) { q -= d - i; ++i; }
+      jj = i + q;
+    }
+    pij[f] = (unsigned short)((i << 8) | jj);
+  }
+  __syncthreads();
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  float acc[4][4] = {};
+  for (int f0 = 0; f0 < g.poly; f0 += 16) {
+    for (int l = threadIdx.x; l < 16 * 64; l += blockDim.x) {
+      const int kk = l / 64, ii = l % 64, f = f0 + kk;
+      float ph = 0.f;
+      if (f < g.poly) {
+        if (f == 0) ph = 1.f;
+        else if (f <= d) ph = xs[ii * ld + f - 1];
+        else { const unsigned short pr = pij[f]; ph = 0.5f * xs[ii * ld + (pr >> 8)] * xs[ii * ld + (pr & 255)]; }
+      }
+      As[kk * 64 + ii] = ph;
+      Bs[kk * 64 + ii] = (f < g.poly && ii < g.proj_dim) ? load_in(P, (size_t)f * g.proj_dim + ii, g.qkv_dtype) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) av[a] = As[kk * 64 + ty * 4 + a];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) bv[b] = Bs[kk * 64 + tx * 4 + b];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] += av[a] * bv[b];
+    }
+    __syncthreads();
+  }
+  for (int a = 0; a < 4; ++a) {
+    const int row = r0 + ty * 4 + a;
+    if (row >= rows_per_unit) continue;
+    for (int b = 0; b < 4; ++b) {
+      const int j = tx * 4 + b;
+      if (j < g.proj_dim) out[((size_t)u * rows_per_unit + row) * g.F + j] = acc[a][b];
+    }
+  }
+}
+
+size_t features_proj_smem(const Geom& g) {
+  return (size_t)(64 * (g.d_k + 1) + 2 * 16 * 64) * sizeof(float) + (size_t)g.poly * sizeof(unsigned short) + 16;
+}
+
+bool features_proj_supported(const Geom& g) {
+  return g.proj_dim > 0 && g.proj_dim <= 64 && g.p == 2 && g.d_k <= 255 && features_proj_smem(g) <= 200 * 1024;
+}
+
+cudaError_t features_proj_launch(const Geom& g, const void* src, const void* cache, int rows, int from_cache,
+                                 const void* P, float* out, cudaStream_t st) {
+  const size_t sm = features_proj_smem(g);
+  cudaFuncSetAttribute(k_features_proj, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  k_features_proj<<<dim3((rows + 63) / 64, g.units), 256, sm, st>>>(g, src, cache, rows, from_cache, P, out);
   return cudaGetLastError();
 }
 
