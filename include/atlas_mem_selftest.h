@@ -27,7 +27,9 @@ int atlas_mem_selftest_mma(int M, int N, int K, int a_mn_major, int b_mn_major, 
  * 64 <= N <= 256, 16 <= K <= 128, multiples of 16) and has every warp w of 4
  * load columns [col, col + 32) of its 32-lane sub-partition with that shape.
  * raw_out: device fp32 [128][16]: row w * 32 + t = the 16 registers of
- * thread t of warp w.  status: device int, 1 if the bounded wait gave up. */
+ * thread t of warp w.  Before the MMA, lanes 16-31 of every sub-partition
+ * are marked over the accumulator's columns; status: device int, 1 if the
+ * bounded wait gave up, 2 if the MMA changed a mark. */
 int atlas_mem_selftest_ld16x2(int N, int K, const void* A, const void* B, float* raw_out, int col, int* status,
                               void* stream);
 

@@ -8,22 +8,25 @@
 // One cluster of 4 CTAs per (batch, head) unit; CTA q owns the hidden slice
 // [64q, 64q + 64): W1[:, slice] (d x 64), W2[slice, :] (64 x d) and the same
 // slices of S.  The kernel is persistent over the unit's chunks, so the fp32
-// state never leaves shared memory.  Per chunk, with row-vector tokens
-// (X keys, R queries, V values; Kw = C window rows since c = 1):
+// state never leaves the SM: it lives in TMEM lanes 16-31 of each 32-lane
+// sub-partition, which the M = 64 accumulators (lanes 0-15) leave untouched.
+// Per chunk, with row-vector tokens (X keys, R queries, V values; Kw = C
+// window rows since c = 1):
 //
 //   Z  = X W1q                      A = SiLU(Z)
 //   Yp = A W2q      -> summed over the 4 slices (DSMEM) -> dy = 2 gamma (X + sum - V)
 //   dz = (dy W2q^T) * SiLU'(Z)
 //   G1 = R X^T,  M1 = -Cw (.) G1
-//   Zq = B_t (R W1q) + D_t (R S1q) + M1 dz          Aq = SiLU(Zq)
+//   Zq = (B R) W1q + (D R) S1q + M1 dz              Aq = SiLU(Zq)
 //   G2 = Aq A^T, M2 = -Cw (.) G2
-//   Yq = B_t (Aq W2q) + D_t (Aq S2q) + M2 dy  -> summed over slices (DSMEM)
+//   Yq = (B Aq) W2q + (D Aq) S2q + M2 dy  -> summed over slices (DSMEM)
 //   y  = R + sum_q Yq
 //   S1q <- A_e S1q - X^T diag(cs_e) dz,  W1q <- B_e W1q + D_e S1q - X^T diag(cw_e) dz
 //   S2q <- A_e S2q - A^T diag(cs_e) dy,  W2q <- B_e W2q + D_e S2q - A^T diag(cw_e) dy
 //
 // Cs, Cw, A_t, B_t, D_t are the momentum/decay coefficients of the chunk
-// (scans over eta and 1 - alpha, see k_generic.cu).  Every product is one
+// (scans over eta and 1 - alpha, see k_generic.cu); (B R) scales row t of R
+// by B_t.  Every product is one
 // tcgen05.mma chain (M = 64, bf16 operands, fp32 accumulation in TMEM); the
 // operands live in shared memory in the core-matrix layout of tc.cuh, each
 // written once and read K-major or MN-major as the product needs.
@@ -42,16 +45,15 @@ constexpr int RGS2 = 2048;              // of a 128-column tile
 constexpr int F32T = 64 * 64 * 4;       // fp32 64x64 tile (swizzled rows)
 constexpr long long kWait = 1ll << 31;
 
-// shared-memory map (bytes)
-constexpr int W1F = 0, S1F = W1F + F32T, W2F = S1F + F32T, S2F = W2F + F32T;
-constexpr int OW1 = S2F + F32T, OS1 = OW1 + TILE, OW2 = OS1 + TILE, OS2 = OW2 + TILE;
-constexpr int OX = OS2 + TILE, OA = OX + TILE, ODY = OA + TILE, ODZ = ODY + TILE;
-constexpr int UNI = ODZ + TILE;                                   // phase-local operands
-constexpr int OR_ = UNI, OM1 = UNI + TILE, OAQ = UNI + 2 * TILE, OM2 = UNI + 3 * TILE;
-constexpr int ODZS = UNI, ODYS = UNI + 2 * TILE;                  // [cs.dz | cw.dz], [cs.dy | cw.dy]
-constexpr int OSP = UNI + 4 * TILE;                               // bf16 SiLU'(Z)
-constexpr int CWM = OSP + TILE;                                   // fp32 Cw[t][i]
-constexpr int RED = CWM + F32T;                                   // 2 fp32 tiles shared over the cluster
+// shared-memory map (bytes): bf16 operand tiles in the core-matrix layout
+constexpr int OW1 = 0, OS1 = OW1 + TILE, OW2 = OS1 + TILE, OS2 = OW2 + TILE;   // state operands
+constexpr int OX = OS2 + TILE, OR_ = OX + TILE, OA = OR_ + TILE, ODY = OA + TILE, ODZ = ODY + TILE;
+constexpr int OSP = ODZ + TILE;                                   // SiLU'(Z)
+constexpr int ORB = OSP + TILE, ORD = ORB + TILE;                 // B_t r_t, D_t r_t
+constexpr int OM1 = ORD + TILE, OAQ = OM1 + TILE, OAQB = OAQ + TILE, OAQD = OAQB + TILE, OM2 = OAQD + TILE;
+constexpr int ODZS = OM2 + TILE, ODYS = ODZS + 2 * TILE;          // [cs.dz | cw.dz], [cs.dy | cw.dy]
+constexpr int CWM = ODYS + 2 * TILE;                              // fp32 Cw[t][i]
+constexpr int RED = CWM + F32T;                                   // Yp slots, Yq slots (cluster-shared)
 constexpr int VEC = RED + 2 * F32T;                               // gate vectors
 constexpr int SMEM_BYTES = VEC + 12 * 64 * 4;
 
@@ -59,9 +61,11 @@ constexpr int SMEM_BYTES = VEC + 12 * 64 * 4;
 constexpr int V_TH = 0, V_ET = 64, V_BE = 128, V_GA = 192, V_AP = 256, V_BP = 320, V_DP = 384, V_CS = 448,
               V_CW = 512;
 
-// TMEM columns
-constexpr uint32_t C_Z = 0, C_YP = 64, C_G1 = 128, C_P1 = 192, C_P2 = 256, C_P3 = 320, C_Q1 = 384, C_Q2 = 448;
-constexpr uint32_t C_G2 = 64, C_Q3 = 128, C_ST1 = 192, C_ST2 = 320;
+// TMEM columns of the accumulators (lanes 0-15 of each sub-partition)
+constexpr uint32_t C_Z = 0, C_YP = 64, C_G1 = 128, C_ZQ = 192, C_ST1 = 256, C_ST2 = 384;
+constexpr uint32_t C_G2 = 64, C_YQ = 128;   // reuse after Yp, G1 are consumed
+// TMEM columns of the fp32 state (lanes 16-31 of each sub-partition)
+constexpr uint32_t S_W1 = 0, S_S1 = 64, S_W2 = 128, S_S2 = 192;
 
 __device__ __forceinline__ int swz(int r, int c) { return r * 64 + (c ^ ((r & 7) << 2)); }
 
@@ -77,13 +81,6 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t cta) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(cta));
   return r;
-}
-__device__ __forceinline__ float4 ld_cluster4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr));
-  return v;
 }
 
 // Operands are bf16: the memory's state decays over long sequences (to
@@ -224,10 +221,6 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   __shared__ uint64_t bar;
   __shared__ uint32_t tbase;
   float* vec = reinterpret_cast<float*>(sm + VEC);
-  float* w1f = reinterpret_cast<float*>(sm + W1F);
-  float* s1f = reinterpret_cast<float*>(sm + S1F);
-  float* w2f = reinterpret_cast<float*>(sm + W2F);
-  float* s2f = reinterpret_cast<float*>(sm + S2F);
   float* cwm = reinterpret_cast<float*>(sm + CWM);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -235,50 +228,71 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   // M = 64 accumulators keep rows 16 sp .. 16 sp + 15 in lanes 0-15 of
   // sub-partition sp; the 16x32bx2 load gives thread `lane` row
   // 16 sp + lane % 16 and 16 columns starting at cb (all 32 lanes busy).
+  // The state uses the same rows in lanes 16-31.
   const int row = 16 * sp + (lane & 15);
   const int cb = 32 * half + 16 * (lane >> 4);
   const uint32_t lb = ((uint32_t)(32 * sp) << 16) + 32 * half;
+  const uint32_t ls = ((uint32_t)(32 * sp + 16) << 16) + 32 * half;
   const uint32_t qr = cluster_rank();
   const int u = blockIdx.x / CS;
-  const int H = 4 * HQ;                       // hidden width
+  const int H = 4 * HQ;
 
   if (warp == 0) tc::tmem_alloc(&tbase, 512);
   if (tid == 0) tc::mbar_init(&bar, 1);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tb = tbase;
 
   // ---- state slices in: W1[:, 64q:64q+64] (d x 64), W2[64q:64q+64, :] (64 x d)
-  for (int e = tid; e < 64 * 64; e += NT) {
-    const int r = e / 64, c = e % 64;
-    const size_t i1 = ((size_t)u * D + r) * H + 64 * qr + c;
-    const size_t i2 = ((size_t)u * H + 64 * qr + r) * D + c;
-    w1f[swz(r, c)] = W0a[i1];
-    s1f[swz(r, c)] = S0a[i1];
-    w2f[swz(r, c)] = W0b[i2];
-    s2f[swz(r, c)] = S0b[i2];
-  }
-  __syncthreads();
-  for (int e = tid; e < 64 * 8; e += NT) {
-    const int r = e % 64, cc = (e / 64) * 8;
-    float a[8], b[8], c[8], d[8];
+  {
+    const size_t i1 = ((size_t)u * D + row) * H + 64 * qr + cb;
+    const size_t i2 = ((size_t)u * H + 64 * qr + row) * D + cb;
+    const float* src[4] = {W0a + i1, S0a + i1, W0b + i2, S0b + i2};
+    const uint32_t col[4] = {S_W1, S_S1, S_W2, S_S2};
+    const int op[4] = {OW1, OS1, OW2, OS2};
+    for (int m = 0; m < 4; ++m) {
+      float x[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      a[i] = w1f[swz(r, cc + i)];
-      b[i] = s1f[swz(r, cc + i)];
-      c[i] = w2f[swz(r, cc + i)];
-      d[i] = s2f[swz(r, cc + i)];
+      for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4*>(x + i) = *reinterpret_cast<const float4*>(src[m] + i);
+      tc::tmem_st16_x2(tb + ls + col[m], x);
+      st_h8(sm + op[m], RGS, row, cb, x);
+      st_h8(sm + op[m], RGS, row, cb + 8, x + 8);
     }
-    st_h8(sm + OW1, RGS, r, cc, a);
-    st_h8(sm + OS1, RGS, r, cc, b);
-    st_h8(sm + OW2, RGS, r, cc, c);
-    st_h8(sm + OS2, RGS, r, cc, d);
+    tc::tmem_st_wait();
   }
+  tc::fence_smem_to_async();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   Ctx cx{&bar, 0u, true};
-  const uint32_t tb = tbase;
   Prefetch pf;
   prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, 0);
   const uint32_t red_local = tc::smem_u32(sm + RED);
+
+  // one state half-update: S <- A_e S - corr_S, W <- B_e W + D_e S - corr_W
+  auto state_update = [&](uint32_t c_corr, uint32_t s_w, uint32_t s_s, int ow, int os) {
+    const float Ae = vec[V_AP + 63], Be = vec[V_BP + 63], De = vec[V_DP + 63];
+    float scr[16], wcr[16], so[16], wo[16];
+    tc::tmem_ld16_x2(tb + lb + c_corr, scr);
+    tc::tmem_ld16_x2(tb + lb + c_corr + 64, wcr);
+    tc::tmem_ld16_x2(tb + ls + s_s, so);
+    tc::tmem_ld16_x2(tb + ls + s_w, wo);
+    tc::tmem_ld_wait();
+    float sn[16], wn[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      sn[i] = Ae * so[i] - scr[i];
+      wn[i] = Be * wo[i] + De * so[i] - wcr[i];
+    }
+    tc::tmem_st16_x2(tb + ls + s_s, sn);
+    tc::tmem_st16_x2(tb + ls + s_w, wn);
+    st_h8(sm + ow, RGS, row, cb, wn);
+    st_h8(sm + ow, RGS, row, cb + 8, wn + 8);
+    st_h8(sm + os, RGS, row, cb, sn);
+    st_h8(sm + os, RGS, row, cb + 8, sn + 8);
+    tc::tmem_st_wait();
+  };
 
   for (int s = 0; s < T; s += TOK) {
     // ---------------------------------------------------------------- L
@@ -300,29 +314,28 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     }
     prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, s + TOK);
     sync_smem_for_mma();
-    // ---------------------------------------------------------------- 1: Z, G1, R W1, R S1
+    // ---------------------------------------------------------------- 1: Z, G1
     if (tid == 0 && cx.ok) {
       mma64(tb + C_Z, sm + OX, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
       mma64(tb + C_G1, sm + OR_, 0, RGS, sm + OX, 0, RGS, 64, 64, false);
-      mma64(tb + C_P1, sm + OR_, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
-      mma64(tb + C_P2, sm + OR_, 0, RGS, sm + OS1, 1, RGS, 64, 64, false);
     }
+    // gate scans (overlap the first products)
     if (tid < 64) {  // column i = tid of Cs / Cw (window of token t is {t})
       const int i = tid;
       float cs = 0.f, cw = 0.f;
       for (int t0 = 0; t0 < TOK; t0 += 8) {
         float et[8], th[8], be[8];   // loads ahead of the stores (same shared array)
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          et[q] = vec[V_ET + t0 + q];
-          th[q] = vec[V_TH + t0 + q];
-          be[q] = vec[V_BE + t0 + q];
+        for (int qq = 0; qq < 8; ++qq) {
+          et[qq] = vec[V_ET + t0 + qq];
+          th[qq] = vec[V_TH + t0 + qq];
+          be[qq] = vec[V_BE + t0 + qq];
         }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          cs = et[q] * cs + (t0 + q == i ? th[q] : 0.f);
-          cw = be[q] * cw + cs;
-          cwm[swz(t0 + q, i)] = cw;
+        for (int qq = 0; qq < 8; ++qq) {
+          cs = et[qq] * cs + (t0 + qq == i ? th[qq] : 0.f);
+          cw = be[qq] * cw + cs;
+          cwm[swz(t0 + qq, i)] = cw;
         }
       }
       vec[V_CS + i] = cs;
@@ -332,22 +345,41 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       for (int t0 = 0; t0 < TOK; t0 += 8) {
         float et[8], be[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          et[q] = vec[V_ET + t0 + q];
-          be[q] = vec[V_BE + t0 + q];
+        for (int qq = 0; qq < 8; ++qq) {
+          et[qq] = vec[V_ET + t0 + qq];
+          be[qq] = vec[V_BE + t0 + qq];
         }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          Ap *= et[q];
-          Bp *= be[q];
-          Dp = be[q] * Dp + Ap;
-          vec[V_AP + t0 + q] = Ap;
-          vec[V_BP + t0 + q] = Bp;
-          vec[V_DP + t0 + q] = Dp;
+        for (int qq = 0; qq < 8; ++qq) {
+          Ap *= et[qq];
+          Bp *= be[qq];
+          Dp = be[qq] * Dp + Ap;
+          vec[V_AP + t0 + qq] = Ap;
+          vec[V_BP + t0 + qq] = Bp;
+          vec[V_DP + t0 + qq] = Dp;
         }
       }
     }
     __syncthreads();
+    // (B R), (D R): the read-out's state terms, issued with the first group
+    {
+      const int r = tid % 64, g = tid / 64;
+      const float Bt = vec[V_BP + r], Dt = vec[V_DP + r];
+      for (int j = 0; j < 2; ++j) {
+        const int cc = (g + 4 * j) * 8;
+        float x[8], b8[8], d8[8];
+        ld_h8(sm + OR_, RGS, r, cc, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { b8[i] = Bt * x[i]; d8[i] = Dt * x[i]; }
+        st_h8(sm + ORB, RGS, r, cc, b8);
+        st_h8(sm + ORD, RGS, r, cc, d8);
+      }
+    }
+    sync_smem_for_mma();
+    if (tid == 0 && cx.ok) {
+      mma64(tb + C_ZQ, sm + ORB, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
+      mma64(tb + C_ZQ, sm + ORD, 0, RGS, sm + OS1, 1, RGS, 64, 64, true);
+    }
     commit_wait(cx);
     {
       float z[16], g[16];
@@ -360,7 +392,11 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
         const float sg = __frcp_rn(1.f + __expf(-z[i]));
         a[i] = z[i] * sg;
         spv[i] = sg * (1.f + z[i] * (1.f - sg));
-        m1[i] = -cwm[swz(row, cb + i)] * g[i];
+      }
+#pragma unroll
+      for (int i = 0; i < 16; i += 4) {
+        const float4 c4 = *reinterpret_cast<const float4*>(cwm + swz(row, cb + i));
+        m1[i] = -c4.x * g[i]; m1[i + 1] = -c4.y * g[i + 1]; m1[i + 2] = -c4.z * g[i + 2]; m1[i + 3] = -c4.w * g[i + 3];
       }
       st_h8(sm + OA, RGS, row, cb, a);
       st_h8(sm + OA, RGS, row, cb + 8, a + 8);
@@ -418,6 +454,20 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 3: dz' = dy W2q^T
     if (tid == 0 && cx.ok) mma64(tb + C_Z, sm + ODY, 0, RGS, sm + OW2, 0, RGS, 64, 64, false);
+    // state operand diag(cs | cw) dy from the broadcast dy tile (overlaps the product)
+    {
+      const int r = tid % 64, g = tid / 64;
+      const float csr = vec[V_CS + r], cwr = vec[V_CW + r];
+      for (int j = 0; j < 2; ++j) {
+        const int cc = (g + 4 * j) * 8;
+        float dy[8], t0[8], t1[8];
+        ld_h8(sm + ODY, RGS, r, cc, dy);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { t0[i] = csr * dy[i]; t1[i] = cwr * dy[i]; }
+        st_h8(sm + ODYS, RGS2, r, cc, t0);
+        st_h8(sm + ODYS, RGS2, r, 64 + cc, t1);
+      }
+    }
     commit_wait(cx);
     {
       float t[16], spv[16];
@@ -425,39 +475,56 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       ld_h8(sm + OSP, RGS, row, cb, spv);
       ld_h8(sm + OSP, RGS, row, cb + 8, spv + 8);
       tc::tmem_ld_wait();
+      const float csr = vec[V_CS + row], cwr = vec[V_CW + row];
+      float t0[16], t1[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) t[i] *= spv[i];
+      for (int i = 0; i < 16; ++i) {
+        t[i] *= spv[i];
+        t0[i] = csr * t[i];
+        t1[i] = cwr * t[i];
+      }
       st_h8(sm + ODZ, RGS, row, cb, t);
       st_h8(sm + ODZ, RGS, row, cb + 8, t + 8);
+      st_h8(sm + ODZS, RGS2, row, cb, t0);
+      st_h8(sm + ODZS, RGS2, row, cb + 8, t0 + 8);
+      st_h8(sm + ODZS, RGS2, row, 64 + cb, t1);
+      st_h8(sm + ODZS, RGS2, row, 64 + cb + 8, t1 + 8);
     }
     sync_smem_for_mma();
-    // ---------------------------------------------------------------- 4: Zq parts
+    // ---------------------------------------------------------------- 4: Zq += M1 dz; state corrections
     if (tid == 0 && cx.ok) {
-      mma64(tb + C_P3, sm + OM1, 0, RGS, sm + ODZ, 1, RGS, 64, 64, false);
+      mma64(tb + C_ZQ, sm + OM1, 0, RGS, sm + ODZ, 1, RGS, 64, 64, true);
+      mma64(tb + C_ST1, sm + OX, 1, RGS, sm + ODZS, 1, RGS2, 128, 64, false);   // X^T [cs dz | cw dz]
+      mma64(tb + C_ST2, sm + OA, 1, RGS, sm + ODYS, 1, RGS2, 128, 64, false);   // A^T [cs dy | cw dy]
     }
     commit_wait(cx);
     {
       const float Bt = vec[V_BP + row], Dt = vec[V_DP + row];
-      float p1[16], p2[16], p3[16];
-      tc::tmem_ld16_x2(tb + lb + C_P1, p1);
-      tc::tmem_ld16_x2(tb + lb + C_P2, p2);
-      tc::tmem_ld16_x2(tb + lb + C_P3, p3);
+      float zq[16];
+      tc::tmem_ld16_x2(tb + lb + C_ZQ, zq);
       tc::tmem_ld_wait();
-      float aq[16];
+      float aq[16], ab[16], ad[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float zq = Bt * p1[i] + Dt * p2[i] + p3[i];
-        aq[i] = zq * __frcp_rn(1.f + __expf(-zq));
+        aq[i] = zq[i] * __frcp_rn(1.f + __expf(-zq[i]));
+        ab[i] = Bt * aq[i];
+        ad[i] = Dt * aq[i];
       }
       st_h8(sm + OAQ, RGS, row, cb, aq);
       st_h8(sm + OAQ, RGS, row, cb + 8, aq + 8);
+      st_h8(sm + OAQB, RGS, row, cb, ab);
+      st_h8(sm + OAQB, RGS, row, cb + 8, ab + 8);
+      st_h8(sm + OAQD, RGS, row, cb, ad);
+      st_h8(sm + OAQD, RGS, row, cb + 8, ad + 8);
     }
+    // W1, S1 are no longer read by this chunk's products
+    state_update(C_ST1, S_W1, S_S1, OW1, OS1);
     sync_smem_for_mma();
-    // ---------------------------------------------------------------- 5: G2, Aq W2q, Aq S2q
+    // ---------------------------------------------------------------- 5: G2, Yq state terms
     if (tid == 0 && cx.ok) {
       mma64(tb + C_G2, sm + OAQ, 0, RGS, sm + OA, 0, RGS, 64, 64, false);
-      mma64(tb + C_Q1, sm + OAQ, 0, RGS, sm + OW2, 1, RGS, 64, 64, false);
-      mma64(tb + C_Q2, sm + OAQ, 0, RGS, sm + OS2, 1, RGS, 64, 64, false);
+      mma64(tb + C_YQ, sm + OAQB, 0, RGS, sm + OW2, 1, RGS, 64, 64, false);
+      mma64(tb + C_YQ, sm + OAQD, 0, RGS, sm + OS2, 1, RGS, 64, 64, true);
     }
     commit_wait(cx);
     {
@@ -465,48 +532,27 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       tc::tmem_ld16_x2(tb + lb + C_G2, g);
       tc::tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 16; ++i) m2[i] = -cwm[swz(row, cb + i)] * g[i];
+      for (int i = 0; i < 16; i += 4) {
+        const float4 c4 = *reinterpret_cast<const float4*>(cwm + swz(row, cb + i));
+        m2[i] = -c4.x * g[i]; m2[i + 1] = -c4.y * g[i + 1]; m2[i + 2] = -c4.z * g[i + 2]; m2[i + 3] = -c4.w * g[i + 3];
+      }
       st_h8(sm + OM2, RGS, row, cb, m2);
       st_h8(sm + OM2, RGS, row, cb + 8, m2 + 8);
     }
     sync_smem_for_mma();
-    // ---------------------------------------------------------------- 6: Q3 = M2 dy, Yq
-    if (tid == 0 && cx.ok) mma64(tb + C_Q3, sm + OM2, 0, RGS, sm + ODY, 1, RGS, 64, 64, false);
+    // ---------------------------------------------------------------- 6: Yq += M2 dy
+    if (tid == 0 && cx.ok) mma64(tb + C_YQ, sm + OM2, 0, RGS, sm + ODY, 1, RGS, 64, 64, true);
+    // W2, S2 are no longer read by this chunk's products (overlaps the last one)
+    state_update(C_ST2, S_W2, S_S2, OW2, OS2);
     commit_wait(cx);
     {
-      const float Bt = vec[V_BP + row], Dt = vec[V_DP + row];
-      float q1[16], q2[16], q3[16];
-      tc::tmem_ld16_x2(tb + lb + C_Q1, q1);
-      tc::tmem_ld16_x2(tb + lb + C_Q2, q2);
-      tc::tmem_ld16_x2(tb + lb + C_Q3, q3);
+      float yq[16];
+      tc::tmem_ld16_x2(tb + lb + C_YQ, yq);
       tc::tmem_ld_wait();
       const uint32_t dst =
           mapa(red_local + (uint32_t)(F32T + ((qr * 16 + (row & 15)) * 64 + cb) * 4), (uint32_t)(row >> 4));
 #pragma unroll
-      for (int i = 0; i < 16; i += 4) {
-        float4 o;
-        o.x = Bt * q1[i] + Dt * q2[i] + q3[i];
-        o.y = Bt * q1[i + 1] + Dt * q2[i + 1] + q3[i + 1];
-        o.z = Bt * q1[i + 2] + Dt * q2[i + 2] + q3[i + 2];
-        o.w = Bt * q1[i + 3] + Dt * q2[i + 3] + q3[i + 3];
-        st_cluster4(dst + 4 * i, o);
-      }
-    }
-    // state-update operands (the read-out operands are dead): diag(cs|cw) dz, dy
-    for (int e = tid; e < 64 * 8; e += NT) {
-      const int r = e % 64, cc = (e / 64) * 8;
-      const float csr = vec[V_CS + r], cwr = vec[V_CW + r];
-      float dz[8], dy[8], t0[8], t1[8];
-      ld_h8(sm + ODZ, RGS, r, cc, dz);
-      ld_h8(sm + ODY, RGS, r, cc, dy);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) { t0[i] = csr * dz[i]; t1[i] = cwr * dz[i]; }
-      st_h8(sm + ODZS, RGS2, r, cc, t0);
-      st_h8(sm + ODZS, RGS2, r, 64 + cc, t1);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) { t0[i] = csr * dy[i]; t1[i] = cwr * dy[i]; }
-      st_h8(sm + ODYS, RGS2, r, cc, t0);
-      st_h8(sm + ODYS, RGS2, r, 64 + cc, t1);
+      for (int i = 0; i < 16; i += 4) st_cluster4(dst + 4 * i, make_float4(yq[i], yq[i + 1], yq[i + 2], yq[i + 3]));
     }
     cluster_sync();
     // y rows [16q, 16q + 16): R + the four slices' Yq from my local slots
@@ -528,58 +574,21 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       *reinterpret_cast<float4*>(y + gb) = o;
     }
     sync_smem_for_mma();
-    // ---------------------------------------------------------------- 7: state corrections
-    if (tid == 0 && cx.ok) {
-      mma64(tb + C_ST1, sm + OX, 1, RGS, sm + ODZS, 1, RGS2, 128, 64, false);   // X^T [cs dz | cw dz]
-      mma64(tb + C_ST2, sm + OA, 1, RGS, sm + ODYS, 1, RGS2, 128, 64, false);   // A^T [cs dy | cw dy]
-    }
-    commit_wait(cx);
-    {
-      const float Ae = vec[V_AP + 63], Be = vec[V_BP + 63], De = vec[V_DP + 63];
-      for (int mtx = 0; mtx < 2; ++mtx) {
-        float* wf = mtx ? w2f : w1f;
-        float* sf = mtx ? s2f : s1f;
-        uint8_t* ow = sm + (mtx ? OW2 : OW1);
-        uint8_t* os = sm + (mtx ? OS2 : OS1);
-        const uint32_t cb_t = mtx ? C_ST2 : C_ST1;
-        {
-          float scr[16], wcr[16];
-          tc::tmem_ld16_x2(tb + lb + cb_t, scr);
-          tc::tmem_ld16_x2(tb + lb + cb_t + 64, wcr);
-          tc::tmem_ld_wait();
-          float wn[16], sn[16];
-#pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            const float4 so = *reinterpret_cast<const float4*>(sf + swz(row, cb + i));
-            const float4 wo = *reinterpret_cast<const float4*>(wf + swz(row, cb + i));
-            const float sov[4] = {so.x, so.y, so.z, so.w}, wov[4] = {wo.x, wo.y, wo.z, wo.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              sn[i + j] = Ae * sov[j] - scr[i + j];
-              wn[i + j] = Be * wov[j] + De * sov[j] - wcr[i + j];
-            }
-            *reinterpret_cast<float4*>(sf + swz(row, cb + i)) = make_float4(sn[i], sn[i + 1], sn[i + 2], sn[i + 3]);
-            *reinterpret_cast<float4*>(wf + swz(row, cb + i)) = make_float4(wn[i], wn[i + 1], wn[i + 2], wn[i + 3]);
-          }
-          st_h8(ow, RGS, row, cb, wn);
-          st_h8(ow, RGS, row, cb + 8, wn + 8);
-          st_h8(os, RGS, row, cb, sn);
-          st_h8(os, RGS, row, cb + 8, sn + 8);
-        }
-      }
-    }
-    sync_smem_for_mma();
   }
 
   // ---- state slices out
-  for (int e = tid; e < 64 * 64; e += NT) {
-    const int r = e / 64, c = e % 64;
-    const size_t i1 = ((size_t)u * D + r) * H + 64 * qr + c;
-    const size_t i2 = ((size_t)u * H + 64 * qr + r) * D + c;
-    Woa[i1] = w1f[swz(r, c)];
-    Soa[i1] = s1f[swz(r, c)];
-    Wob[i2] = w2f[swz(r, c)];
-    Sob[i2] = s2f[swz(r, c)];
+  {
+    const size_t i1 = ((size_t)u * D + row) * H + 64 * qr + cb;
+    const size_t i2 = ((size_t)u * H + 64 * qr + row) * D + cb;
+    float* dst[4] = {Woa + i1, Soa + i1, Wob + i2, Sob + i2};
+    const uint32_t col[4] = {S_W1, S_S1, S_W2, S_S2};
+    for (int m = 0; m < 4; ++m) {
+      float x[16];
+      tc::tmem_ld16_x2(tb + ls + col[m], x);
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4*>(dst[m] + i) = *reinterpret_cast<const float4*>(x + i);
+    }
   }
   if (!cx.ok && tid == 0) atomicExch(status, ATLAS_ERR_TIMEOUT);
   tc::fence_before_sync();

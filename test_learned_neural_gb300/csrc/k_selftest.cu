@@ -78,6 +78,13 @@ __global__ void __launch_bounds__(128) k_selftest_ld16x2(int N, int K, const uin
   const int rgsK = (K / 8) * 128;
   for (int e = threadIdx.x; e < M * K; e += blockDim.x) *(uint16_t*)(As + tc::core_offset(e / K, e % K, rgsK)) = A[e];
   for (int e = threadIdx.x; e < N * K; e += blockDim.x) *(uint16_t*)(Bs + tc::core_offset(e / K, e % K, rgsK)) = B[e];
+  // mark lanes 16-31 of every sub-partition over the accumulator's columns
+  {
+    float mark[16];
+    for (int j = 0; j < 16; ++j) mark[j] = 1000.f + warp * 100 + j;
+    for (int c = 0; c < N; c += 32) tc::tmem_st16_x2(tbase + ((uint32_t)(32 * warp + 16) << 16) + c, mark);
+    tc::tmem_st_wait();
+  }
   tc::fence_smem_to_async();
   tc::fence_before_sync();
   __syncthreads();
@@ -94,10 +101,14 @@ __global__ void __launch_bounds__(128) k_selftest_ld16x2(int N, int K, const uin
   if (!ok) {
     if (threadIdx.x == 0) atomicExch(status, 1);
   } else {
-    float v[16];
+    float v[16], m[16];
     tc::tmem_ld16_x2(tbase + ((uint32_t)(32 * warp) << 16) + col, v);
+    tc::tmem_ld16_x2(tbase + ((uint32_t)(32 * warp + 16) << 16) + col, m);
     tc::tmem_ld_wait();
     for (int j = 0; j < 16; ++j) raw[(size_t)(warp * 32 + lane) * 16 + j] = v[j];
+    // lanes 16-31 must still hold their marks after the M = 64 MMA
+    for (int j = 0; j < 16; ++j)
+      if (m[j] != 1000.f + warp * 100 + j) atomicExch(status, 2);
   }
   tc::fence_before_sync();
   __syncthreads();

@@ -57,7 +57,8 @@ def test_mma_layouts(gpu_lib, M, N, K, a_mn, b_mn, bf16):
 def test_tmem_ld_16x32bx2_layout(gpu_lib):
     """Thread t of warp w gets accumulator row 16 w + t % 16, columns
     col + 16 (t // 16) + j.  D[r][c] = 256 r + c exactly, so every loaded
-    value names its own row and column."""
+    value names its own row and column.  Lanes 16-31 of each sub-partition,
+    marked before the M = 64 MMA, must come back unchanged."""
     import torch
     lib = gpu_lib.load()
     lib.atlas_mem_selftest_ld16x2.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
@@ -78,7 +79,8 @@ def test_tmem_ld_16x32bx2_layout(gpu_lib):
                                        st.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert rc == 0
     torch.cuda.synchronize()
-    assert st.item() == 0
+    assert st.item() != 1, "bounded wait gave up"
+    assert st.item() == 0, "an M = 64 MMA changed TMEM lanes 16-31"
     raw = raw.cpu().numpy().astype(np.int64)
     got = {(w, t, j): (int(raw[32 * w + t, j]) // 256, int(raw[32 * w + t, j]) % 256)
            for w in range(4) for t in range(32) for j in range(16)}
