@@ -38,20 +38,22 @@ constexpr long long kWaitCycles = 1ll << 31;
 
 struct NsSmem {
   // byte offsets inside dynamic shared memory
-  int opr;        // factor operands, later X hi/lo
-  int stg;        // fp32 staging of S (R x (n + 4)), later A / B' hi/lo
+  int rx;         // window factor on the long side, split bf16, unscaled (kept across a (unit, matrix)'s tokens)
+  int lx;         // window factor on the short side, scaled by the token's coefficients
+  int x;          // X hi, X lo (X lo directly after X hi: read together as one 128-row operand)
+  int a;          // A, then B' (hi, lo; likewise adjacent)
+  int qt;         // fp32 transpose buffer [64][65]
   int total;
 };
 
 __host__ __device__ inline NsSmem ns_smem_layout(int n, int Kp) {
   NsSmem s;
-  const int lx = R * Kp * 2, rx = Kp * n * 2, xx = R * n * 2;
-  int opr_bytes = 2 * lx + 2 * rx;
-  if (opr_bytes < 2 * xx) opr_bytes = 2 * xx;
-  const int stg_bytes = R * (n + 4) * 4;
-  s.opr = 0;
-  s.stg = (opr_bytes + 1023) & ~1023;
-  s.total = s.stg + ((stg_bytes + 1023) & ~1023);
+  s.rx = 0;
+  s.lx = s.rx + 2 * Kp * n * 2;
+  s.x = s.lx + 2 * R * Kp * 2;
+  s.a = s.x + 2 * R * n * 2;
+  s.qt = s.a + 2 * R * R * 2;
+  s.total = s.qt + R * (R + 1) * 4;
   return s;
 }
 
@@ -90,6 +92,19 @@ __device__ inline void mma_x3(uint32_t d, const uint8_t* a_hi, const uint8_t* a_
   }
 }
 
+// [P | Q] = Y_hi [Y_hi ; Y_lo]^T for a 64-row split-bf16 Y (K-major, Y_lo
+// stored 8 row groups after Y_hi): one N = 128 chain instead of two N = 64.
+__device__ inline void mma_hilo(uint32_t d, const uint8_t* y_hi, int rgs, int M, int K) {
+  const uint32_t idesc = tc::idesc_f16(M, 2 * M, 1, 0, 0);
+  uint64_t ad = tc::sdesc(tc::smem_u32(y_hi), 128, rgs);
+  uint64_t bd = tc::sdesc(tc::smem_u32(y_hi), 128, rgs);
+  for (int ks = 0; ks < K / 16; ++ks) {
+    tc::mma_f16(d, ad, bd, idesc, ks > 0 ? 1u : 0u);
+    ad += 256 >> 4;
+    bd += 256 >> 4;
+  }
+}
+
 // Every thread waits for the MMA group; the outcome is made uniform across
 // the CTA (a timed-out wait anywhere aborts everyone).
 __device__ inline bool wait_all(uint64_t* bar, uint32_t& phase) {
@@ -109,8 +124,17 @@ __device__ inline void sync_for_mma() {
 
 }  // namespace
 
-// Persistent over tasks.  n = long side of X (multiple of 16, <= 256);
-// Kp = window rows padded to a multiple of 16.
+// Persistent over tasks; CTA b takes a contiguous run of tasks ordered
+// (unit, matrix, token), so the long-side window factor is split into
+// bf16 hi/lo once per (unit, matrix) run and only the small short-side
+// factor is rebuilt (scaled by the token's coefficients) per token.
+// n = long side of X (multiple of 16, <= 256); Kp = window rows padded to a
+// multiple of 16.
+//
+// X X^T and A^2 use the symmetry of the split: with Y = Y_hi + Y_lo,
+// Y Y^T ~ P + Q + Q^T where [P | Q] = Y_hi [Y_hi ; Y_lo]^T is one N = 128
+// product (Y_lo is stored right after Y_hi, so the pair is one 128-row
+// operand); Q^T comes from a shared-memory transpose.
 __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int buf, size_t slot_stride, int n,
                                                     int Kp) {
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -118,8 +142,6 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
   __shared__ uint32_t tbase;
   __shared__ float red[NT / 32];
   const NsSmem L = ns_smem_layout(n, Kp);
-  uint8_t* opr = sm + L.opr;
-  float* stg = reinterpret_cast<float*>(sm + L.stg);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // M = 64 accumulators: rows 16 sp .. 16 sp + 15 sit in lanes 0-15 of
   // sub-partition sp.  With the 16x32bx2 load a warp reads 16 rows x 32
@@ -130,32 +152,34 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
   const int row = 16 * sp + (lane & 15);
   const int csub = 16 * (lane >> 4);
   const uint32_t lane_base = (uint32_t)(32 * sp) << 16;
-  const int stg_ld = n + 4;
 
   if (warp == 0) tc::tmem_alloc(&tbase, 512);
   if (threadIdx.x == 0) tc::mbar_init(&bar, 1);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tA = tbase, tA2 = tbase + 64, tX = tbase + 128;
+  const uint32_t tA = tbase, tA2 = tbase + 128, tX = tbase + 256;
   uint32_t phase = 0;
   bool ok = true;
 
-  // operand buffers inside opr / stg
-  const int lxb = R * Kp * 2, rxb = Kp * n * 2, xb = R * n * 2, ab = R * R * 2;
-  uint8_t* lx_hi = opr;
-  uint8_t* lx_lo = opr + lxb;
-  uint8_t* rx_hi = opr + 2 * lxb;
-  uint8_t* rx_lo = opr + 2 * lxb + rxb;
-  uint8_t* x_hi = opr;
-  uint8_t* x_lo = opr + xb;
-  uint8_t* a_hi = sm + L.stg;
-  uint8_t* a_lo = sm + L.stg + ab;
+  uint8_t* rx_hi = sm + L.rx;
+  uint8_t* rx_lo = sm + L.rx + Kp * n * 2;
+  uint8_t* lx_hi = sm + L.lx;
+  uint8_t* lx_lo = sm + L.lx + R * Kp * 2;
+  uint8_t* x_hi = sm + L.x;
+  uint8_t* x_lo = sm + L.x + R * n * 2;
+  uint8_t* a_hi = sm + L.a;
+  uint8_t* a_lo = sm + L.a + R * R * 2;
+  float* qt = reinterpret_cast<float*>(sm + L.qt);
   const int rgsKp = (Kp / 8) * 128, rgsN = (n / 8) * 128, rgsR = (R / 8) * 128;
+  const int c = 32 * half + csub;           // this thread's 16 columns of a 64-wide accumulator
 
   const int Ct = ch.e - ch.s;
   const int ntasks = g.units * g.nmat * Ct;
-  for (int task = blockIdx.x; task < ntasks; task += gridDim.x) {
+  const int t_begin = (int)((long long)ntasks * blockIdx.x / gridDim.x);
+  const int t_end = (int)((long long)ntasks * (blockIdx.x + 1) / gridDim.x);
+  int loaded = -1;                          // (unit, matrix) whose long-side factor is resident
+  for (int task = t_begin; task < t_end; ++task) {
     const int r = task % Ct;
     const int m = (task / Ct) % g.nmat;
     const int u = task / (Ct * g.nmat);
@@ -181,61 +205,63 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
     const float* cs = w.Cs + ((size_t)u * g.C + r) * g.Kw;
     const float At = w.Ap[(size_t)u * g.C + r];
     const size_t nel = (size_t)rows * cols;
-    const float* Sb = w.Sst[buf][m] + (size_t)u * nel;
+    const float* Sb = w.Sst[buf][m] + (size_t)u * nel;   // X orientation [R][n]
 
-    // (a) factors -> split-bf16 operands (zero rows beyond the window).
-    // Lx^T is the K-major A operand: thread = (row a, 8 window rows), one
-    // 16-byte chunk of the core layout per array.
+    // (a) long-side factor once per (unit, matrix): MN-major B operand [Kp][n]
+    if (loaded != u * g.nmat + m) {
+      loaded = u * g.nmat + m;
+      for (int e = threadIdx.x; e < Kp * (n / 8); e += NT) {
+        const int i = e / (n / 8), b0 = (e % (n / 8)) * 8;
+        float v[8];
+        if (i < ch.nw) {
+          const float4 r0 = *reinterpret_cast<const float4*>(Rf + (size_t)i * rstride + b0);
+          const float4 r1 = *reinterpret_cast<const float4*>(Rf + (size_t)i * rstride + b0 + 4);
+          v[0] = r0.x; v[1] = r0.y; v[2] = r0.z; v[3] = r0.w; v[4] = r1.x; v[5] = r1.y; v[6] = r1.z; v[7] = r1.w;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[q] = 0.f;
+        }
+        store_split16(rx_hi, rx_lo, tc::core_offset(i, b0, rgsN), v);
+      }
+    }
+    // short-side factor scaled by this token's coefficients: K-major A operand [R][Kp]
     for (int e = threadIdx.x; e < R * (Kp / 8); e += NT) {
       const int a = e % R, i0 = (e / R) * 8;
       float v[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) v[q] = (i0 + q < ch.nw) ? Lf[(size_t)(i0 + q) * lstride + a] : 0.f;
+      for (int q = 0; q < 8; ++q) v[q] = (i0 + q < ch.nw) ? cs[i0 + q] * Lf[(size_t)(i0 + q) * lstride + a] : 0.f;
       store_split16(lx_hi, lx_lo, tc::core_offset(a, i0, rgsKp), v);
     }
-    for (int e = threadIdx.x; e < Kp * (n / 8); e += NT) {
-      const int i = e / (n / 8), b0 = (e % (n / 8)) * 8;
-      float v[8];
-      if (i < ch.nw) {
-        const float c = cs[i];
-        const float4 r0 = *reinterpret_cast<const float4*>(Rf + (size_t)i * rstride + b0);
-        const float4 r1 = *reinterpret_cast<const float4*>(Rf + (size_t)i * rstride + b0 + 4);
-        v[0] = c * r0.x; v[1] = c * r0.y; v[2] = c * r0.z; v[3] = c * r0.w;
-        v[4] = c * r1.x; v[5] = c * r1.y; v[6] = c * r1.z; v[7] = c * r1.w;
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = 0.f;
-      }
-      // diag(cs) Rx is the MN-major B operand: k = window row i, n = long index b
-      store_split16(rx_hi, rx_lo, tc::core_offset(i, b0, rgsN), v);
-    }
-    // (b) Sbar (kept in the X orientation on this path), fp32 staging
-    for (int e = threadIdx.x; e < R * n / 4; e += NT) {
-      const int a = e / (n / 4), b = (e % (n / 4)) * 4;
-      const float4 s4 = *reinterpret_cast<const float4*>(Sb + (size_t)a * n + b);
-      *reinterpret_cast<float4*>(stg + a * stg_ld + b) = s4;
-    }
     sync_for_mma();
-    // (c) D = Lx^T diag(cs) Rx   (M = 64, N = n, K = Kp)
+    // (b) D = (Lx diag cs)^T Rx   (M = 64, N = n, K = Kp)
     if (threadIdx.x == 0) {
       mma_x3(tX, lx_hi, lx_lo, rgsKp, rx_hi, rx_lo, rgsN, 1, R, n, Kp);
       tc::mma_commit(&bar);
     }
     if (!(ok = wait_all(&bar, phase))) break;
-    // (d) S = A_t Sbar - D, in place in the staging; sum of squares
+    // (c) S = A_t Sbar - D, kept in TMEM over D; sum of squares; chunk-end S
     float ss = 0.f;
+    const bool last_tok = (t == ch.e - 1);
+    float* So = w.Sst[buf ^ 1][m] + (size_t)u * nel;
     for (int c32 = 32 * half; c32 < n; c32 += 64) {
       float d[16];
       tc::tmem_ld16_x2(tX + lane_base + c32, d);
-      tc::tmem_ld_wait();
-      float* srow = stg + row * stg_ld + c32 + csub;
+      const float* sb = Sb + (size_t)row * n + c32 + csub;
+      float4 s4[4];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float s = At * srow[q] - d[q];
-        srow[q] = s;
-        ss += s * s;
+      for (int q4 = 0; q4 < 4; ++q4) s4[q4] = *reinterpret_cast<const float4*>(sb + 4 * q4);
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float* o = d + 4 * q4;
+        o[0] = At * s4[q4].x - o[0]; o[1] = At * s4[q4].y - o[1];
+        o[2] = At * s4[q4].z - o[2]; o[3] = At * s4[q4].w - o[3];
+        ss += o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
+        if (last_tok) *reinterpret_cast<float4*>(So + (size_t)row * n + c32 + csub + 4 * q4) = make_float4(o[0], o[1], o[2], o[3]);
       }
+      tc::tmem_st16_x2(tX + lane_base + c32, d);
     }
+    tc::tmem_st_wait();
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (lane == 0) red[warp] = ss;
     tc::fence_before_sync();
@@ -245,56 +271,61 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
 #pragma unroll
     for (int k2 = 0; k2 < NT / 32; ++k2) tot += red[k2];
     const float scale = 1.f / (sqrtf(tot) + kNsEps);
-    if (t == ch.e - 1) {   // chunk-end momentum (X orientation)
-      float* So = w.Sst[buf ^ 1][m] + (size_t)u * nel;
-      for (int e = threadIdx.x; e < R * n / 4; e += NT) {
-        const int a = e / (n / 4), b = (e % (n / 4)) * 4;
-        *reinterpret_cast<float4*>(So + (size_t)a * n + b) = *reinterpret_cast<const float4*>(stg + a * stg_ld + b);
-      }
-    }
-    // X_0 = S * scale -> split bf16 (opr region is free: the factor MMA is done)
-    for (int c32 = 32 * half; c32 < n; c32 += 64)
-      for (int h8 = 0; h8 < 16; h8 += 8) {
-        float v[8];
-        const int c = c32 + csub + h8;
+    // (d) X_0 = S * scale -> split bf16
+    for (int c32 = 32 * half; c32 < n; c32 += 64) {
+      float d[16];
+      tc::tmem_ld16_x2(tX + lane_base + c32, d);
+      tc::tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = stg[row * stg_ld + c + q] * scale;
-        store_split16(x_hi, x_lo, tc::core_offset(row, c, rgsN), v);
-      }
+      for (int q = 0; q < 16; ++q) d[q] *= scale;
+      store_split16(x_hi, x_lo, tc::core_offset(row, c32 + csub, rgsN), d);
+      store_split16(x_hi, x_lo, tc::core_offset(row, c32 + csub + 8, rgsN), d + 8);
+    }
     sync_for_mma();
 
     float* slot = w.Ubuf + ((size_t)u * g.C + r) * slot_stride;
     for (int mm = 0; mm < m; ++mm) slot += (size_t)g.rows[mm] * g.cols[mm];
     for (int it = 0; it < g.ns_iters && ok; ++it) {
-      // A = X X^T  (M = 64, N = 64, K = n; both operands K-major)
+      // [P | Q] = X_hi [X_hi ; X_lo]^T   (M = 64, N = 128, K = n)
       if (threadIdx.x == 0) {
-        mma_x3(tA, x_hi, x_lo, rgsN, x_hi, x_lo, rgsN, 0, R, R, n);
+        mma_hilo(tA, x_hi, rgsN, R, n);
         tc::mma_commit(&bar);
       }
       if (!(ok = wait_all(&bar, phase))) break;
+      float av[16];
       {
-        float v[16];
-        const int c = 32 * half + csub;
-        tc::tmem_ld16_x2(tA + lane_base + 32 * half, v);
-        tc::tmem_ld_wait();
-        store_split16(a_hi, a_lo, tc::core_offset(row, c, rgsR), v);
-        store_split16(a_hi, a_lo, tc::core_offset(row, c + 8, rgsR), v + 8);
-      }
-      sync_for_mma();
-      // A^2 (A symmetric: its rows serve as the K-major B operand)
-      if (threadIdx.x == 0) {
-        mma_x3(tA2, a_hi, a_lo, rgsR, a_hi, a_lo, rgsR, 0, R, R, R);
-        tc::mma_commit(&bar);
-      }
-      if (!(ok = wait_all(&bar, phase))) break;
-      {
-        float va[16], v2[16], bp[16];
-        const int c = 32 * half + csub;
-        tc::tmem_ld16_x2(tA + lane_base + 32 * half, va);
-        tc::tmem_ld16_x2(tA2 + lane_base + 32 * half, v2);
+        float p[16], qv[16];
+        tc::tmem_ld16_x2(tA + lane_base + 32 * half, p);
+        tc::tmem_ld16_x2(tA + lane_base + 64 + 32 * half, qv);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 16; ++q) bp[q] = kNsB * va[q] + kNsC * v2[q] + (row == c + q ? kNsA : 0.f);
+        for (int q = 0; q < 16; ++q) qt[row * (R + 1) + c + q] = qv[q];
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 16; ++q) av[q] = p[q] + qv[q] + qt[(c + q) * (R + 1) + row];
+        store_split16(a_hi, a_lo, tc::core_offset(row, c, rgsR), av);
+        store_split16(a_hi, a_lo, tc::core_offset(row, c + 8, rgsR), av + 8);
+      }
+      sync_for_mma();
+      // [P2 | Q2] = A_hi [A_hi ; A_lo]^T  (A symmetric: its rows are the K-major B operand)
+      if (threadIdx.x == 0) {
+        mma_hilo(tA2, a_hi, rgsR, R, R);
+        tc::mma_commit(&bar);
+      }
+      if (!(ok = wait_all(&bar, phase))) break;
+      {
+        float p[16], qv[16], bp[16];
+        tc::tmem_ld16_x2(tA2 + lane_base + 32 * half, p);
+        tc::tmem_ld16_x2(tA2 + lane_base + 64 + 32 * half, qv);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 16; ++q) qt[row * (R + 1) + c + q] = qv[q];
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const float a2 = p[q] + qv[q] + qt[(c + q) * (R + 1) + row];
+          bp[q] = kNsB * av[q] + kNsC * a2 + (row == c + q ? kNsA : 0.f);
+        }
         store_split16(a_hi, a_lo, tc::core_offset(row, c, rgsR), bp);
         store_split16(a_hi, a_lo, tc::core_offset(row, c + 8, rgsR), bp + 8);
       }
@@ -308,16 +339,16 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
       const bool last = (it == g.ns_iters - 1);
       for (int c32 = 32 * half; c32 < n; c32 += 64) {
         float v[16];
-        const int c = c32 + csub;
+        const int cc = c32 + csub;
         tc::tmem_ld16_x2(tX + lane_base + c32, v);
         tc::tmem_ld_wait();
         if (last) {
-          float4* o = reinterpret_cast<float4*>(slot + (size_t)row * n + c);
+          float4* o = reinterpret_cast<float4*>(slot + (size_t)row * n + cc);
 #pragma unroll
           for (int q = 0; q < 4; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         } else {
-          store_split16(x_hi, x_lo, tc::core_offset(row, c, rgsN), v);
-          store_split16(x_hi, x_lo, tc::core_offset(row, c + 8, rgsN), v + 8);
+          store_split16(x_hi, x_lo, tc::core_offset(row, cc, rgsN), v);
+          store_split16(x_hi, x_lo, tc::core_offset(row, cc + 8, rgsN), v + 8);
         }
       }
       sync_for_mma();
@@ -687,7 +718,7 @@ cudaError_t ns_tc_launch(const Geom& g, const Chunk& ch, const Work& w, int buf,
   const int smem = ns_smem_layout(n, Kp).total;
   cudaFuncSetAttribute(k_ns_tc64, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   const int ntasks = g.units * g.nmat * (ch.e - ch.s);
-  const int grid = ntasks < num_sms ? ntasks : num_sms;
+  const int grid = ntasks < num_sms ? ntasks : num_sms;   // each CTA takes a contiguous run of tasks
   k_ns_tc64<<<grid, NT, smem, st>>>(g, ch, w, buf, slot_stride, n, Kp);
   return cudaGetLastError();
 }
