@@ -68,7 +68,9 @@ struct Work {
   float* Dp;      // [units][C]  coefficient of S_bar in W_t
   float* Ubuf;    // NS path: [units][C][sum_m rows*cols] U_t then W_t (X orientation)
   float* xch;     // (unused: the CTA pairs exchange over DSMEM)
-  float* gpart;   // depth 2: per hidden block partial forward outputs [units][h/64][Kw][d_v]
+  float* gpart;   // depth 2: per hidden block partial forward outputs [units][h/64][Kw][d_v];
+                  // depth 1: cs_e dy and cw_e dy [units][2][Kw][d_v], then per
+                  // (unit, 64-feature slice) partial products R W, R S, R X^T, X W
   int* status;    // device status word
 };
 
@@ -89,6 +91,7 @@ size_t generic_smem_grad(const Geom& g);
 size_t generic_smem_readout(const Geom& g);
 size_t generic_smem_ns(const Geom& g, int m);
 size_t grad_part_floats(const Geom& g);
+size_t dual1_split_floats(const Geom& g, size_t units);
 int num_sms();
 
 // fused tensor-core MLP memory without Newton-Schulz (k_mlp_tc.cu)

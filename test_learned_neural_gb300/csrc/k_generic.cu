@@ -573,12 +573,20 @@ size_t generic_smem_ns(const Geom& g, int m) {
 }
 
 cudaError_t grad_tiled(const Geom& g, const Chunk& ch, const Work& w, int buf, cudaStream_t st, int* nl);
+bool dual1_split_supported(const Geom& g);
+cudaError_t dual1_split(const Geom& g, const Chunk& ch, const Work& w, int buf, float* y, cudaStream_t st);
 bool ns_fused_scan_supported(const Geom& g);
 cudaError_t ns_fused_scan(const Geom& g, const Chunk& ch, const Work& w, int buf, size_t slot_stride,
                           const float* alpha, float* aq, float* y, cudaStream_t st);
 
 cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const GenericIO& io, int buf,
                           cudaStream_t st, int* nl) {
+  if (dual1_split_supported(g)) {
+    const int coef_threads = ((ch.nw + 31) / 32) * 32;
+    k_coef<<<g.units, coef_threads, 0, st>>>(g, ch, io.theta, io.eta, io.alpha, w);
+    *nl += 4;   // coefficients, partial products, read-out, state
+    return dual1_split(g, ch, w, buf, io.y, st);
+  }
   *nl += g.ns_iters == 0 ? 3 + g.nmat : 3 + 2 * g.nmat;
   const size_t sr = generic_smem_readout(g);
   if (g.depth == 1 || ch.nw <= 128) {
@@ -1003,6 +1011,205 @@ cudaError_t features_proj_launch(const Geom& g, const void* src, const void* cac
   const size_t sm = features_proj_smem(g);
   cudaFuncSetAttribute(k_features_proj, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   k_features_proj<<<dim3((rows + 63) / 64, g.units), 256, sm, st>>>(g, src, cache, rows, from_cache, P, out);
+  return cudaGetLastError();
+}
+
+}  // namespace atlas
+
+namespace atlas {
+
+// ------------------------------------------ split dual form, depth 1
+// Every product of a depth-1 chunk contracts over the feature axis F (561
+// for degree-2 features of 32-dim keys) except the small window term, so
+// the chunk is cut along F: one CTA per (64 features, unit) forms
+//   PW = R W, PS = R S, PX = R X^T, PG = X W    (all restricted to its slice)
+// from shared-memory copies of its slices, a second kernel sums the slices
+// and forms dy_i = 2 gamma_i (x_i W - v_i), M = Cw (.) R X^T and
+//   y_t = B_t (R W)_t + D_t (R S)_t - (M dY)_t,
+// and a third forms the chunk-end state
+//   S' = A_e S - X^T diag(cs_e) dY,  W' = B_e W + D_e S - X^T diag(cw_e) dY.
+
+// floats per (unit, slice) of partial products
+__host__ __device__ inline size_t dual1_part_floats(const Geom& g) {
+  return 2 * (size_t)g.C * g.d_v + (size_t)g.C * g.Kw + (size_t)g.Kw * g.d_v;
+}
+
+// acc[a][b] = sum_{k < 64} A(ty*4+a, k) B(k, tx*4+b) over shared-memory
+// operands A(i, k) = A[i * ai + k * ak], B(k, j) = B[k * bk + j]
+__device__ __forceinline__ void smem_gemm64(const float* A, int ai, int ak, const float* B, int bk, float acc[4][4]) {
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 8
+  for (int k = 0; k < 64; ++k) {
+    float av[4], bv[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) av[a] = A[(ty * 4 + a) * ai + k * ak];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) bv[b] = B[k * bk + tx * 4 + b];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] += av[a] * bv[b];
+  }
+}
+
+// store rows [r0, r0 + 64) x cols [0, 64) of acc into out (row stride ld),
+// rows < nr and cols < nc only
+__device__ __forceinline__ void store_tile(float* out, int ld, int r0, int nr, int nc, const float acc[4][4]) {
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int r = r0 + ty * 4 + a;
+    if (r >= nr) continue;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int c = tx * 4 + b;
+      if (c < nc) out[(size_t)r * ld + c] = acc[a][b];
+    }
+  }
+}
+
+constexpr size_t kDual1PartSmem = (64 * 65 + 64 * 129 + 2 * 64 * 64) * sizeof(float);
+
+__global__ void __launch_bounds__(256) k_dual1_partials(Geom g, Chunk ch, Work w, int buf, float* part) {
+  extern __shared__ float sm[];
+  float* Rs = sm;               // [t][f], row stride 65
+  float* Xt = Rs + 64 * 65;     // [f][i], row stride 129 (window rows transposed)
+  float* Ws = Xt + 64 * 129;    // [f][j]
+  float* Ss = Ws + 64 * 64;     // [f][j]
+  const int kb = blockIdx.x, u = blockIdx.y, f0 = kb * 64;
+  const int Ct = ch.e - ch.s, nw = ch.nw, dv = g.d_v;
+  const int nf = min(64, g.F - f0);
+  const float* Rw = w.R + ((size_t)u * g.T + ch.s) * g.F + f0;
+  const float* Xw = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * g.F + f0;
+  const float* W = w.Wst[buf][0] + ((size_t)u * g.F + f0) * dv;
+  const float* S = w.Sst[buf][0] + ((size_t)u * g.F + f0) * dv;
+  for (int l = threadIdx.x; l < 64 * 64; l += blockDim.x) {
+    const int r = l / 64, c = l % 64;
+    Rs[r * 65 + c] = (r < Ct && c < nf) ? Rw[(size_t)r * g.F + c] : 0.f;
+    Ws[l] = (r < nf && c < dv) ? W[(size_t)r * dv + c] : 0.f;
+    Ss[l] = (r < nf && c < dv) ? S[(size_t)r * dv + c] : 0.f;
+  }
+  for (int l = threadIdx.x; l < 128 * 64; l += blockDim.x) {
+    const int i = l / 64, f = l % 64;
+    Xt[f * 129 + i] = (i < nw && f < nf) ? Xw[(size_t)i * g.F + f] : 0.f;
+  }
+  __syncthreads();
+  float* pb = part + ((size_t)u * gridDim.x + kb) * dual1_part_floats(g);
+  float* PW = pb;
+  float* PS = PW + (size_t)g.C * dv;
+  float* PX = PS + (size_t)g.C * dv;
+  float* PG = PX + (size_t)g.C * g.Kw;
+  float acc[4][4];
+  smem_gemm64(Rs, 65, 1, Ws, 64, acc);
+  store_tile(PW, dv, 0, Ct, dv, acc);
+  smem_gemm64(Rs, 65, 1, Ss, 64, acc);
+  store_tile(PS, dv, 0, Ct, dv, acc);
+  for (int i0 = 0; i0 < nw; i0 += 64) {
+    smem_gemm64(Rs, 65, 1, Xt + i0, 129, acc);
+    store_tile(PX + i0, g.Kw, 0, Ct, nw - i0, acc);
+    smem_gemm64(Xt + i0, 1, 129, Ws, 64, acc);
+    store_tile(PG, dv, i0, nw, dv, acc);
+  }
+}
+
+__global__ void __launch_bounds__(256) k_dual1_combine(Geom g, Chunk ch, Work w, const float* part, float* dys,
+                                                        float* y) {
+  __shared__ float M[16][129];   // Cw (.) R X^T for 16 tokens
+  __shared__ float Dy[128][17];  // dy for 16 columns
+  const int jb = blockIdx.x * 16, tb = blockIdx.y * 16, u = blockIdx.z;
+  const int Ct = ch.e - ch.s, nw = ch.nw, dv = g.d_v;
+  const int ks = (g.F + 63) / 64;
+  const size_t per = dual1_part_floats(g);
+  const float* pu = part + (size_t)u * ks * per;
+  const size_t oS = (size_t)g.C * dv, oX = 2 * oS, oG = oX + (size_t)g.C * g.Kw;
+  const size_t row0 = (size_t)u * g.L + ch.lo + g.n_prev;
+  const int re = ch.e - 1 - ch.s;
+  const float* cs = w.Cs + ((size_t)u * g.C + re) * g.Kw;
+  const float* cw = w.Cw + ((size_t)u * g.C + re) * g.Kw;
+  for (int l = threadIdx.x; l < nw * 16; l += blockDim.x) {
+    const int i = l / 16, jj = l % 16, j = jb + jj;
+    float d = 0.f;
+    if (j < dv) {
+      float s = 0.f;
+      for (int kb = 0; kb < ks; ++kb) s += pu[kb * per + oG + (size_t)i * dv + j];
+      d = 2.f * w.G[row0 + i] * (s - w.V[(row0 + i) * dv + j]);
+      if (blockIdx.y == 0) {
+        dys[((size_t)u * 2 + 0) * g.Kw * dv + (size_t)i * dv + j] = cs[i] * d;
+        dys[((size_t)u * 2 + 1) * g.Kw * dv + (size_t)i * dv + j] = cw[i] * d;
+      }
+    }
+    Dy[i][jj] = d;
+  }
+  for (int l = threadIdx.x; l < 16 * nw; l += blockDim.x) {
+    const int tt = l / nw, i = l % nw, t = tb + tt;
+    float m = 0.f;
+    if (t < Ct) {
+      float s = 0.f;
+      for (int kb = 0; kb < ks; ++kb) s += pu[kb * per + oX + (size_t)t * g.Kw + i];
+      m = w.Cw[((size_t)u * g.C + t) * g.Kw + i] * s;
+    }
+    M[tt][i] = m;
+  }
+  __syncthreads();
+  const int tt = threadIdx.x / 16, jj = threadIdx.x % 16, t = tb + tt, j = jb + jj;
+  if (t >= Ct || j >= dv) return;
+  float pw = 0.f, ps = 0.f;
+  for (int kb = 0; kb < ks; ++kb) {
+    pw += pu[kb * per + (size_t)t * dv + j];
+    ps += pu[kb * per + oS + (size_t)t * dv + j];
+  }
+  float c = 0.f;
+  for (int i = 0; i < nw; ++i) c += M[tt][i] * Dy[i][jj];
+  const float Bt = w.Bp[(size_t)u * g.C + t], Dt = w.Dp[(size_t)u * g.C + t];
+  y[((size_t)u * g.T + ch.s + t) * dv + j] = Bt * pw + Dt * ps - c;
+}
+
+__global__ void __launch_bounds__(256) k_dual1_state(Geom g, Chunk ch, Work w, int buf, const float* dys) {
+  __shared__ float As[16 * 64], Bs[16 * 64];
+  const int u = blockIdx.z, i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
+  const float* Xw = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * g.F;
+  const float* Ds = dys + (size_t)u * 2 * g.Kw * g.d_v;
+  float cs_acc[4][4], cw_acc[4][4];
+  tile_gemm(TileOp{Xw, 1, g.F}, TileOp{Ds, 1, g.d_v}, g.F, g.d_v, ch.nw, i0, j0, cs_acc, As, Bs);
+  tile_gemm(TileOp{Xw, 1, g.F}, TileOp{Ds + (size_t)g.Kw * g.d_v, 1, g.d_v}, g.F, g.d_v, ch.nw, i0, j0, cw_acc, As, Bs);
+  const int r = ch.e - 1 - ch.s;
+  const float Ae = w.Ap[(size_t)u * g.C + r], Be = w.Bp[(size_t)u * g.C + r], De = w.Dp[(size_t)u * g.C + r];
+  const size_t base = (size_t)u * g.F * g.d_v;
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  for (int a = 0; a < 4; ++a) {
+    const int i = i0 + ty * 4 + a;
+    if (i >= g.F) continue;
+    for (int b = 0; b < 4; ++b) {
+      const int j = j0 + tx * 4 + b;
+      if (j >= g.d_v) continue;
+      const size_t o = base + (size_t)i * g.d_v + j;
+      const float Sb = w.Sst[buf][0][o], Wb = w.Wst[buf][0][o];
+      w.Sst[buf ^ 1][0][o] = Ae * Sb - cs_acc[a][b];
+      w.Wst[buf ^ 1][0][o] = Be * Wb + De * Sb - cw_acc[a][b];
+    }
+  }
+}
+
+bool dual1_split_supported(const Geom& g) {
+  return g.depth == 1 && g.ns_iters == 0 && g.Kw <= 128 && g.C <= 64 && g.d_v <= 64;
+}
+
+size_t dual1_split_floats(const Geom& g, size_t units) {
+  return units * (2 * (size_t)g.Kw * g.d_v + (size_t)((g.F + 63) / 64) * dual1_part_floats(g));
+}
+
+cudaError_t dual1_split(const Geom& g, const Chunk& ch, const Work& w, int buf, float* y, cudaStream_t st) {
+  const int ks = (g.F + 63) / 64, Ct = ch.e - ch.s;
+  float* dys = w.gpart;
+  float* part = w.gpart + (size_t)g.units * 2 * g.Kw * g.d_v;
+  cudaFuncSetAttribute(k_dual1_partials, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDual1PartSmem);
+  k_dual1_partials<<<dim3(ks, g.units), 256, kDual1PartSmem, st>>>(g, ch, w, buf, part);
+  k_dual1_combine<<<dim3((g.d_v + 15) / 16, (Ct + 15) / 16, g.units), 256, 0, st>>>(g, ch, w, part, dys, y);
+  k_dual1_state<<<dim3((g.d_v + 63) / 64, (g.F + 63) / 64, g.units), 256, 0, st>>>(g, ch, w, buf, dys);
   return cudaGetLastError();
 }
 
