@@ -574,19 +574,15 @@ size_t generic_smem_ns(const Geom& g, int m) {
 
 cudaError_t grad_tiled(const Geom& g, const Chunk& ch, const Work& w, int buf, cudaStream_t st, int* nl);
 bool dual1_split_supported(const Geom& g);
-cudaError_t dual1_split(const Geom& g, const Chunk& ch, const Work& w, int buf, float* y, cudaStream_t st);
+cudaError_t dual1_split(const Geom& g, const Chunk& ch, const Work& w, const GenericIO& io, int buf,
+                        cudaStream_t st, int* nl);
 bool ns_fused_scan_supported(const Geom& g);
 cudaError_t ns_fused_scan(const Geom& g, const Chunk& ch, const Work& w, int buf, size_t slot_stride,
                           const float* alpha, float* aq, float* y, cudaStream_t st);
 
 cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const GenericIO& io, int buf,
                           cudaStream_t st, int* nl) {
-  if (dual1_split_supported(g)) {
-    const int coef_threads = ((ch.nw + 31) / 32) * 32;
-    k_coef<<<g.units, coef_threads, 0, st>>>(g, ch, io.theta, io.eta, io.alpha, w);
-    *nl += 4;   // coefficients, partial products, read-out, state
-    return dual1_split(g, ch, w, buf, io.y, st);
-  }
+  if (dual1_split_supported(g)) return dual1_split(g, ch, w, io, buf, st, nl);
   *nl += g.ns_iters == 0 ? 3 + g.nmat : 3 + 2 * g.nmat;
   const size_t sr = generic_smem_readout(g);
   if (g.depth == 1 || ch.nw <= 128) {
@@ -1021,29 +1017,33 @@ namespace atlas {
 // ------------------------------------------ split dual form, depth 1
 // Every product of a depth-1 chunk contracts over the feature axis F (561
 // for degree-2 features of 32-dim keys) except the small window term, so
-// the chunk is cut along F: one CTA per (64 features, unit) forms
-//   PW = R W, PS = R S, PX = R X^T, PG = X W    (all restricted to its slice)
-// from shared-memory copies of its slices, a second kernel sums the slices
-// and forms dy_i = 2 gamma_i (x_i W - v_i), M = Cw (.) R X^T and
-//   y_t = B_t (R W)_t + D_t (R S)_t - (M dY)_t,
-// and a third forms the chunk-end state
-//   S' = A_e S - X^T diag(cs_e) dY,  W' = B_e W + D_e S - X^T diag(cw_e) dY.
+// the chunk is cut along F.  For each (64-feature slice, unit):
+//   PW = R W, PS = R S, PX = R X^T, PG = X W    (restricted to the slice)
+// A combine kernel sums the slices, runs the chunk's coefficient scans and
+// forms dy_i = 2 gamma_i (x_i W - v_i), M = Cw (.) R X^T and
+//   y_t = B_t (R W)_t + D_t (R S)_t - (M dY)_t.
+// A step kernel, again one CTA per (slice, unit), updates the slice's rows
+// of the state,
+//   S' = A_e S - X^T diag(cs_e) dY,  W' = B_e W + D_e S - X^T diag(cw_e) dY,
+// and, keeping them in shared memory, forms the next chunk's partial
+// products.  Two launches per chunk.
 
 // floats per (unit, slice) of partial products
 __host__ __device__ inline size_t dual1_part_floats(const Geom& g) {
   return 2 * (size_t)g.C * g.d_v + (size_t)g.C * g.Kw + (size_t)g.Kw * g.d_v;
 }
 
-// acc[a][b] = sum_{k < 64} A(ty*4+a, k) B(k, tx*4+b) over shared-memory
+// acc[a][b] = sum_{k < K} A(ty*4+a, k) B(k, tx*4+b) over shared-memory
 // operands A(i, k) = A[i * ai + k * ak], B(k, j) = B[k * bk + j]
-__device__ __forceinline__ void smem_gemm64(const float* A, int ai, int ak, const float* B, int bk, float acc[4][4]) {
+__device__ __forceinline__ void smem_gemm(const float* A, int ai, int ak, const float* B, int bk, int K,
+                                          float acc[4][4]) {
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
 #pragma unroll
   for (int a = 0; a < 4; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
-#pragma unroll 8
-  for (int k = 0; k < 64; ++k) {
+#pragma unroll 4
+  for (int k = 0; k < K; ++k) {
     float av[4], bv[4];
 #pragma unroll
     for (int a = 0; a < 4; ++a) av[a] = A[(ty * 4 + a) * ai + k * ak];
@@ -1072,74 +1072,181 @@ __device__ __forceinline__ void store_tile(float* out, int ld, int r0, int nr, i
   }
 }
 
-constexpr size_t kDual1PartSmem = (64 * 65 + 64 * 129 + 2 * 64 * 64) * sizeof(float);
+// Asynchronous 4-byte global -> shared copies: every load of a stage is in
+// flight at once instead of one round trip per loop iteration.  An invalid
+// element copies 0 bytes from a valid address and zero-fills.
+__device__ __forceinline__ void cp_async4(float* dst, const float* src, bool valid, const float* fallback) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d), "l"(valid ? src : fallback),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-__global__ void __launch_bounds__(256) k_dual1_partials(Geom g, Chunk ch, Work w, int buf, float* part) {
-  extern __shared__ float sm[];
-  float* Rs = sm;               // [t][f], row stride 65
-  float* Xt = Rs + 64 * 65;     // [f][i], row stride 129 (window rows transposed)
-  float* Ws = Xt + 64 * 129;    // [f][j]
-  float* Ss = Ws + 64 * 64;     // [f][j]
-  const int kb = blockIdx.x, u = blockIdx.y, f0 = kb * 64;
-  const int Ct = ch.e - ch.s, nw = ch.nw, dv = g.d_v;
-  const int nf = min(64, g.F - f0);
+// shared-memory slices: R [t][f] (row stride 65), X transposed [f][i]
+// (row stride 129), W and S [f][j] (row stride 64)
+constexpr int kRsF = 64 * 65, kXtF = 64 * 129, kWsF = 64 * 64;
+constexpr size_t kDual1PartSmem = (size_t)(kRsF + kXtF + 2 * kWsF) * sizeof(float);
+constexpr size_t kDual1StepSmem = kDual1PartSmem + (size_t)(kXtF + 2 * 128 * 64) * sizeof(float);
+
+// issue copies of the R rows of chunk ch and its window rows of X,
+// features [f0, f0 + 64)
+__device__ void dual1_load_rx(const Geom& g, const Chunk& ch, const Work& w, int u, int f0, float* Rs, float* Xt) {
+  const int Ct = ch.e - ch.s, nf = min(64, g.F - f0);
   const float* Rw = w.R + ((size_t)u * g.T + ch.s) * g.F + f0;
   const float* Xw = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * g.F + f0;
-  const float* W = w.Wst[buf][0] + ((size_t)u * g.F + f0) * dv;
-  const float* S = w.Sst[buf][0] + ((size_t)u * g.F + f0) * dv;
   for (int l = threadIdx.x; l < 64 * 64; l += blockDim.x) {
     const int r = l / 64, c = l % 64;
-    Rs[r * 65 + c] = (r < Ct && c < nf) ? Rw[(size_t)r * g.F + c] : 0.f;
-    Ws[l] = (r < nf && c < dv) ? W[(size_t)r * dv + c] : 0.f;
-    Ss[l] = (r < nf && c < dv) ? S[(size_t)r * dv + c] : 0.f;
+    cp_async4(&Rs[r * 65 + c], Rw + (size_t)r * g.F + c, r < Ct && c < nf, w.R);
   }
   for (int l = threadIdx.x; l < 128 * 64; l += blockDim.x) {
     const int i = l / 64, f = l % 64;
-    Xt[f * 129 + i] = (i < nw && f < nf) ? Xw[(size_t)i * g.F + f] : 0.f;
+    cp_async4(&Xt[f * 129 + i], Xw + (size_t)i * g.F + f, i < ch.nw && f < nf, w.X);
   }
-  __syncthreads();
-  float* pb = part + ((size_t)u * gridDim.x + kb) * dual1_part_floats(g);
+}
+
+// issue copies of rows [f0, f0 + 64) of the state matrices
+__device__ void dual1_load_ws(const Geom& g, const Work& w, int buf, int u, int f0, float* Ws, float* Ss) {
+  const int nf = min(64, g.F - f0), dv = g.d_v;
+  const size_t so = ((size_t)u * g.F + f0) * dv;
+  for (int l = threadIdx.x; l < 64 * 64; l += blockDim.x) {
+    const int r = l / 64, c = l % 64;
+    const bool ok = r < nf && c < dv;
+    cp_async4(&Ws[l], w.Wst[buf][0] + so + (size_t)r * dv + c, ok, w.Wst[buf][0]);
+    cp_async4(&Ss[l], w.Sst[buf][0] + so + (size_t)r * dv + c, ok, w.Sst[buf][0]);
+  }
+}
+
+__device__ void dual1_partials_smem(const Geom& g, const Chunk& ch, const float* Rs, const float* Xt,
+                                    const float* Ws, const float* Ss, float* pb) {
+  const int Ct = ch.e - ch.s, nw = ch.nw, dv = g.d_v;
   float* PW = pb;
   float* PS = PW + (size_t)g.C * dv;
   float* PX = PS + (size_t)g.C * dv;
   float* PG = PX + (size_t)g.C * g.Kw;
   float acc[4][4];
-  smem_gemm64(Rs, 65, 1, Ws, 64, acc);
+  smem_gemm(Rs, 65, 1, Ws, 64, 64, acc);
   store_tile(PW, dv, 0, Ct, dv, acc);
-  smem_gemm64(Rs, 65, 1, Ss, 64, acc);
+  smem_gemm(Rs, 65, 1, Ss, 64, 64, acc);
   store_tile(PS, dv, 0, Ct, dv, acc);
   for (int i0 = 0; i0 < nw; i0 += 64) {
-    smem_gemm64(Rs, 65, 1, Xt + i0, 129, acc);
+    smem_gemm(Rs, 65, 1, Xt + i0, 129, 64, acc);
     store_tile(PX + i0, g.Kw, 0, Ct, nw - i0, acc);
-    smem_gemm64(Xt + i0, 1, 129, Ws, 64, acc);
+    smem_gemm(Xt + i0, 1, 129, Ws, 64, 64, acc);
     store_tile(PG, dv, i0, nw, dv, acc);
   }
 }
 
-__global__ void __launch_bounds__(256) k_dual1_combine(Geom g, Chunk ch, Work w, const float* part, float* dys,
-                                                        float* y) {
-  __shared__ float M[16][129];   // Cw (.) R X^T for 16 tokens
+// partial products of the first chunk, from the state in global memory
+__global__ void __launch_bounds__(256) k_dual1_partials(Geom g, Chunk ch, Work w, int buf, float* part) {
+  extern __shared__ float sm[];
+  float* Rs = sm;
+  float* Xt = Rs + kRsF;
+  float* Ws = Xt + kXtF;
+  float* Ss = Ws + kWsF;
+  const int kb = blockIdx.x, u = blockIdx.y, f0 = kb * 64;
+  dual1_load_ws(g, w, buf, u, f0, Ws, Ss);
+  dual1_load_rx(g, ch, w, u, f0, Rs, Xt);
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  dual1_partials_smem(g, ch, Rs, Xt, Ws, Ss, part + ((size_t)u * gridDim.x + kb) * dual1_part_floats(g));
+}
+
+// floats of the combine kernel's staging buffer
+__host__ __device__ inline size_t dual1_combine_floats(const Geom& g) {
+  const size_t ks = (g.F + 63) / 64;
+  return ks * (32 * (size_t)g.Kw + 512) + 17 * (size_t)g.Kw;
+}
+
+// coefficient scans, slice sums, dy and the chunk's read-out; one CTA per
+// (16 columns, 16 tokens, unit)
+__global__ void __launch_bounds__(256) k_dual1_combine(Geom g, Chunk ch, Work w, const float* theta,
+                                                        const float* eta, const float* alpha, const float* part,
+                                                        float* dys, float* y) {
+  extern __shared__ float sm[];
+  __shared__ float M[16][129];   // Cw, then Cw (.) R X^T, for 16 tokens
   __shared__ float Dy[128][17];  // dy for 16 columns
+  __shared__ float th[64], et[64], be[64], Bt[64], Dt[64], cse[128], cwe[128];
   const int jb = blockIdx.x * 16, tb = blockIdx.y * 16, u = blockIdx.z;
-  const int Ct = ch.e - ch.s, nw = ch.nw, dv = g.d_v;
+  const int Ct = ch.e - ch.s, nw = ch.nw, dv = g.d_v, Kw = g.Kw;
   const int ks = (g.F + 63) / 64;
   const size_t per = dual1_part_floats(g);
   const float* pu = part + (size_t)u * ks * per;
-  const size_t oS = (size_t)g.C * dv, oX = 2 * oS, oG = oX + (size_t)g.C * g.Kw;
+  const size_t oS = (size_t)g.C * dv, oX = 2 * oS, oG = oX + (size_t)g.C * Kw;
   const size_t row0 = (size_t)u * g.L + ch.lo + g.n_prev;
-  const int re = ch.e - 1 - ch.s;
-  const float* cs = w.Cs + ((size_t)u * g.C + re) * g.Kw;
-  const float* cw = w.Cw + ((size_t)u * g.C + re) * g.Kw;
+  // staging: sG[kb][i][16], sX[kb][16][Kw], sP[kb][2][16][16], sV[i][16], sGam[i]
+  float* sG = sm;
+  float* sX = sG + (size_t)ks * Kw * 16;
+  float* sP = sX + (size_t)ks * 16 * Kw;
+  float* sV = sP + (size_t)ks * 512;
+  float* sGam = sV + (size_t)Kw * 16;
+  for (int l = threadIdx.x; l < ks * nw * 16; l += blockDim.x) {
+    const int kb = l / (nw * 16), r = l % (nw * 16), i = r / 16, jj = r % 16;
+    cp_async4(&sG[((size_t)kb * Kw + i) * 16 + jj], pu + kb * per + oG + (size_t)i * dv + jb + jj, jb + jj < dv, part);
+  }
+  for (int l = threadIdx.x; l < ks * 16 * nw; l += blockDim.x) {
+    const int kb = l / (16 * nw), r = l % (16 * nw), tt = r / nw, i = r % nw;
+    cp_async4(&sX[((size_t)kb * 16 + tt) * Kw + i], pu + kb * per + oX + (size_t)(tb + tt) * Kw + i, tb + tt < Ct,
+              part);
+  }
+  for (int l = threadIdx.x; l < ks * 512; l += blockDim.x) {
+    const int kb = l / 512, h = (l / 256) % 2, tt = (l / 16) % 16, jj = l % 16;
+    cp_async4(&sP[l], pu + kb * per + (h ? oS : 0) + (size_t)(tb + tt) * dv + jb + jj,
+              tb + tt < Ct && jb + jj < dv, part);
+  }
+  for (int l = threadIdx.x; l < nw * 16; l += blockDim.x) {
+    const int i = l / 16, jj = l % 16;
+    cp_async4(&sV[l], w.V + (row0 + i) * dv + jb + jj, jb + jj < dv, w.V);
+  }
+  for (int i = threadIdx.x; i < nw; i += blockDim.x) cp_async4(&sGam[i], w.G + row0 + i, true, w.G);
+  for (int r = threadIdx.x; r < Ct; r += blockDim.x) {
+    cp_async4(&th[r], theta + (size_t)u * g.T + ch.s + r, true, theta);
+    cp_async4(&et[r], eta + (size_t)u * g.T + ch.s + r, true, eta);
+    cp_async4(&be[r], alpha + (size_t)u * g.T + ch.s + r, true, alpha);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  for (int r = threadIdx.x; r < Ct; r += blockDim.x) be[r] = 1.f - be[r];
+  __syncthreads();
+  // window row i: Cs_t = eta_t Cs_{t-1} + theta_t [t in window of i],
+  // Cw_t = (1 - alpha_t) Cw_{t-1} + Cs_t
+  if (threadIdx.x < nw) {
+    const int i = threadIdx.x, ti = ch.lo + i;
+    float cs = 0.f, cw = 0.f;
+    for (int r = 0; r < Ct; ++r) {
+      const int t = ch.s + r;
+      const bool in_win = ti <= t && t <= ti + g.c - 1;
+      cs = et[r] * cs + (in_win ? th[r] : 0.f);
+      cw = be[r] * cw + cs;
+      if (r >= tb && r < tb + 16) M[r - tb][i] = cw;
+    }
+    cse[i] = cs;
+    cwe[i] = cw;
+  } else if (threadIdx.x == blockDim.x - 1) {
+    float Ap = 1.f, Bp = 1.f, Dp = 0.f;
+    for (int r = 0; r < Ct; ++r) {
+      Ap *= et[r];
+      Bp *= be[r];
+      Dp = be[r] * Dp + Ap;
+      Bt[r] = Bp;
+      Dt[r] = Dp;
+    }
+  }
+  __syncthreads();
   for (int l = threadIdx.x; l < nw * 16; l += blockDim.x) {
     const int i = l / 16, jj = l % 16, j = jb + jj;
     float d = 0.f;
     if (j < dv) {
       float s = 0.f;
-      for (int kb = 0; kb < ks; ++kb) s += pu[kb * per + oG + (size_t)i * dv + j];
-      d = 2.f * w.G[row0 + i] * (s - w.V[(row0 + i) * dv + j]);
+      for (int kb = 0; kb < ks; ++kb) s += sG[((size_t)kb * Kw + i) * 16 + jj];
+      d = 2.f * sGam[i] * (s - sV[l]);
       if (blockIdx.y == 0) {
-        dys[((size_t)u * 2 + 0) * g.Kw * dv + (size_t)i * dv + j] = cs[i] * d;
-        dys[((size_t)u * 2 + 1) * g.Kw * dv + (size_t)i * dv + j] = cw[i] * d;
+        dys[((size_t)u * 2 + 0) * Kw * dv + (size_t)i * dv + j] = cse[i] * d;
+        dys[((size_t)u * 2 + 1) * Kw * dv + (size_t)i * dv + j] = cwe[i] * d;
       }
     }
     Dy[i][jj] = d;
@@ -1149,8 +1256,8 @@ __global__ void __launch_bounds__(256) k_dual1_combine(Geom g, Chunk ch, Work w,
     float m = 0.f;
     if (t < Ct) {
       float s = 0.f;
-      for (int kb = 0; kb < ks; ++kb) s += pu[kb * per + oX + (size_t)t * g.Kw + i];
-      m = w.Cw[((size_t)u * g.C + t) * g.Kw + i] * s;
+      for (int kb = 0; kb < ks; ++kb) s += sX[((size_t)kb * 16 + tt) * Kw + i];
+      m = M[tt][i] * s;
     }
     M[tt][i] = m;
   }
@@ -1159,57 +1266,121 @@ __global__ void __launch_bounds__(256) k_dual1_combine(Geom g, Chunk ch, Work w,
   if (t >= Ct || j >= dv) return;
   float pw = 0.f, ps = 0.f;
   for (int kb = 0; kb < ks; ++kb) {
-    pw += pu[kb * per + (size_t)t * dv + j];
-    ps += pu[kb * per + oS + (size_t)t * dv + j];
+    pw += sP[kb * 512 + threadIdx.x];
+    ps += sP[kb * 512 + 256 + threadIdx.x];
   }
   float c = 0.f;
   for (int i = 0; i < nw; ++i) c += M[tt][i] * Dy[i][jj];
-  const float Bt = w.Bp[(size_t)u * g.C + t], Dt = w.Dp[(size_t)u * g.C + t];
-  y[((size_t)u * g.T + ch.s + t) * dv + j] = Bt * pw + Dt * ps - c;
+  y[((size_t)u * g.T + ch.s + t) * dv + j] = Bt[t] * pw + Dt[t] * ps - c;
 }
 
-__global__ void __launch_bounds__(256) k_dual1_state(Geom g, Chunk ch, Work w, int buf, const float* dys) {
-  __shared__ float As[16 * 64], Bs[16 * 64];
-  const int u = blockIdx.z, i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
-  const float* Xw = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * g.F;
-  const float* Ds = dys + (size_t)u * 2 * g.Kw * g.d_v;
-  float cs_acc[4][4], cw_acc[4][4];
-  tile_gemm(TileOp{Xw, 1, g.F}, TileOp{Ds, 1, g.d_v}, g.F, g.d_v, ch.nw, i0, j0, cs_acc, As, Bs);
-  tile_gemm(TileOp{Xw, 1, g.F}, TileOp{Ds + (size_t)g.Kw * g.d_v, 1, g.d_v}, g.F, g.d_v, ch.nw, i0, j0, cw_acc, As, Bs);
-  const int r = ch.e - 1 - ch.s;
-  const float Ae = w.Ap[(size_t)u * g.C + r], Be = w.Bp[(size_t)u * g.C + r], De = w.Dp[(size_t)u * g.C + r];
-  const size_t base = (size_t)u * g.F * g.d_v;
+// chunk-end state of one 64-feature slice, then (if there is a next chunk)
+// that slice's partial products of the next chunk from the new state
+__global__ void __launch_bounds__(256) k_dual1_step(Geom g, Chunk ch, Chunk nx, int has_next, Work w, int buf,
+                                                     const float* eta, const float* alpha, const float* dys,
+                                                     float* part) {
+  extern __shared__ float sm[];
+  float* Rs = sm;          // next chunk's R
+  float* Xt = Rs + kRsF;   // this chunk's X, transposed
+  float* Ws = Xt + kXtF;
+  float* Ss = Ws + kWsF;
+  float* Xn = Ss + kWsF;   // next chunk's X, transposed
+  float* Dc = Xn + kXtF;   // [2][128][64]: cs_e dy, cw_e dy
+  __shared__ float sc[3];
+  const int kb = blockIdx.x, u = blockIdx.y, f0 = kb * 64, dv = g.d_v, nw = ch.nw;
+  const int nf = min(64, g.F - f0);
+  const size_t so = ((size_t)u * g.F + f0) * dv;
+  dual1_load_ws(g, w, buf, u, f0, Ws, Ss);
+  const float* Xw = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * g.F + f0;
+  for (int l = threadIdx.x; l < 128 * 64; l += blockDim.x) {
+    const int i = l / 64, f = l % 64;
+    cp_async4(&Xt[f * 129 + i], Xw + (size_t)i * g.F + f, i < nw && f < nf, w.X);
+    for (int h = 0; h < 2; ++h)
+      cp_async4(&Dc[h * 128 * 64 + l], dys + (((size_t)u * 2 + h) * g.Kw + i) * dv + f, i < nw && f < dv, dys);
+  }
+  cp_async_commit();
+  if (has_next) dual1_load_rx(g, nx, w, u, f0, Rs, Xn);
+  cp_async_commit();
+  if (threadIdx.x == 0) {
+    float Ap = 1.f, Bp = 1.f, Dp = 0.f;
+    for (int t = ch.s; t < ch.e; ++t) {
+      const float e = eta[(size_t)u * g.T + t], b = 1.f - alpha[(size_t)u * g.T + t];
+      Ap *= e;
+      Bp *= b;
+      Dp = b * Dp + Ap;
+    }
+    sc[0] = Ap;
+    sc[1] = Bp;
+    sc[2] = Dp;
+  }
+  cp_async_wait<1>();
+  __syncthreads();
+  float as_[4][4], aw[4][4];
+  smem_gemm(Xt, 129, 1, Dc, 64, nw, as_);
+  smem_gemm(Xt, 129, 1, Dc + 128 * 64, 64, nw, aw);
+  const float Ae = sc[0], Be = sc[1], De = sc[2];
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+#pragma unroll
   for (int a = 0; a < 4; ++a) {
-    const int i = i0 + ty * 4 + a;
-    if (i >= g.F) continue;
+    const int f = ty * 4 + a;
+    if (f >= nf) continue;
+#pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const int j = j0 + tx * 4 + b;
-      if (j >= g.d_v) continue;
-      const size_t o = base + (size_t)i * g.d_v + j;
-      const float Sb = w.Sst[buf][0][o], Wb = w.Wst[buf][0][o];
-      w.Sst[buf ^ 1][0][o] = Ae * Sb - cs_acc[a][b];
-      w.Wst[buf ^ 1][0][o] = Be * Wb + De * Sb - cw_acc[a][b];
+      const int j = tx * 4 + b;
+      if (j >= dv) continue;
+      const float Sb = Ss[f * 64 + j], Wb = Ws[f * 64 + j];
+      const float Sn = Ae * Sb - as_[a][b], Wn = Be * Wb + De * Sb - aw[a][b];
+      w.Sst[buf ^ 1][0][so + (size_t)f * dv + j] = Sn;
+      w.Wst[buf ^ 1][0][so + (size_t)f * dv + j] = Wn;
+      Ss[f * 64 + j] = Sn;
+      Ws[f * 64 + j] = Wn;
     }
   }
+  cp_async_wait<0>();
+  if (!has_next) return;
+  __syncthreads();
+  dual1_partials_smem(g, nx, Rs, Xn, Ws, Ss, part + ((size_t)u * gridDim.x + kb) * dual1_part_floats(g));
 }
 
 bool dual1_split_supported(const Geom& g) {
-  return g.depth == 1 && g.ns_iters == 0 && g.Kw <= 128 && g.C <= 64 && g.d_v <= 64;
+  return g.depth == 1 && g.ns_iters == 0 && g.Kw <= 128 && g.C <= 64 && g.d_v <= 64 &&
+         dual1_combine_floats(g) * sizeof(float) <= 160 * 1024;
 }
 
 size_t dual1_split_floats(const Geom& g, size_t units) {
   return units * (2 * (size_t)g.Kw * g.d_v + (size_t)((g.F + 63) / 64) * dual1_part_floats(g));
 }
 
-cudaError_t dual1_split(const Geom& g, const Chunk& ch, const Work& w, int buf, float* y, cudaStream_t st) {
+static Chunk chunk_at(const Geom& g, int s) {
+  Chunk c;
+  c.s = s;
+  c.e = s + g.C;
+  c.lo = s - g.c + 1;
+  if (c.lo < -g.n_prev) c.lo = -g.n_prev;
+  c.nw = c.e - c.lo;
+  return c;
+}
+
+cudaError_t dual1_split(const Geom& g, const Chunk& ch, const Work& w, const GenericIO& io, int buf,
+                        cudaStream_t st, int* nl) {
   const int ks = (g.F + 63) / 64, Ct = ch.e - ch.s;
   float* dys = w.gpart;
   float* part = w.gpart + (size_t)g.units * 2 * g.Kw * g.d_v;
-  cudaFuncSetAttribute(k_dual1_partials, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDual1PartSmem);
-  k_dual1_partials<<<dim3(ks, g.units), 256, kDual1PartSmem, st>>>(g, ch, w, buf, part);
-  k_dual1_combine<<<dim3((g.d_v + 15) / 16, (Ct + 15) / 16, g.units), 256, 0, st>>>(g, ch, w, part, dys, y);
-  k_dual1_state<<<dim3((g.d_v + 63) / 64, (g.F + 63) / 64, g.units), 256, 0, st>>>(g, ch, w, buf, dys);
+  if (ch.s == 0) {
+    cudaFuncSetAttribute(k_dual1_partials, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDual1PartSmem);
+    k_dual1_partials<<<dim3(ks, g.units), 256, kDual1PartSmem, st>>>(g, ch, w, buf, part);
+    *nl += 1;
+  }
+  const size_t sc = dual1_combine_floats(g) * sizeof(float);
+  cudaFuncSetAttribute(k_dual1_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
+  k_dual1_combine<<<dim3((g.d_v + 15) / 16, (Ct + 15) / 16, g.units), 256, sc, st>>>(g, ch, w, io.theta, io.eta,
+                                                                                      io.alpha, part, dys, io.y);
+  const int has_next = ch.e < g.T;
+  const Chunk nx = chunk_at(g, has_next ? ch.e : ch.s);
+  cudaFuncSetAttribute(k_dual1_step, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDual1StepSmem);
+  k_dual1_step<<<dim3(ks, g.units), 256, kDual1StepSmem, st>>>(g, ch, nx, has_next, w, buf, io.eta, io.alpha, dys,
+                                                               part);
+  *nl += 2;
   return cudaGetLastError();
 }
 
