@@ -70,7 +70,8 @@ struct Work {
   float* xch;     // (unused: the CTA pairs exchange over DSMEM)
   float* gpart;   // depth 2: per hidden block partial forward outputs [units][h/64][Kw][d_v];
                   // depth 1: cs_e dy and cw_e dy [units][2][Kw][d_v], then per
-                  // (unit, 64-feature slice) partial products R W, R S, R X^T, X W
+                  // (unit, 64-feature slice) partial products R W, R S, R X^T, X W,
+                  // then per (unit, chunk) gate-scan coefficients
   int* status;    // device status word
 };
 
@@ -91,7 +92,7 @@ size_t generic_smem_grad(const Geom& g);
 size_t generic_smem_readout(const Geom& g);
 size_t generic_smem_ns(const Geom& g, int m);
 size_t grad_part_floats(const Geom& g);
-size_t dual1_split_floats(const Geom& g, size_t units);
+size_t dual1_split_floats(const Geom& g, size_t units, int T);
 int num_sms();
 
 // fused tensor-core MLP memory without Newton-Schulz (k_mlp_tc.cu)

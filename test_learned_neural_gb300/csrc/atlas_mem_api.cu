@@ -131,7 +131,7 @@ static Layout layout(const Geom& g, int units, int T) {
       64,                                  // status
       ns_tc_xch_floats(g, num_sms()),      // Gram exchange of the CTA-pair Newton-Schulz
       g.depth == 2 ? U * ((size_t)(g.hidden + 63) / 64) * Kw * g.d_v  // tiled-gradient partial outputs
-                   : dual1_split_floats(g, U),                       // depth 1: scaled dy + feature-slice partials
+                   : dual1_split_floats(g, U, T),                       // depth 1: scaled dy + feature-slice partials
   };
   const int n = sizeof sizes / sizeof sizes[0];
   size_t o = 0;

@@ -1034,32 +1034,33 @@ __host__ __device__ inline size_t dual1_part_floats(const Geom& g) {
 }
 
 // acc[a][b] = sum_{k < K} A(ty*4+a, k) B(k, tx*4+b) over shared-memory
-// operands A(i, k) = A[i * ai + k * ak], B(k, j) = B[k * bk + j]
-__device__ __forceinline__ void smem_gemm(const float* A, int ai, int ak, const float* B, int bk, int K,
-                                          float acc[4][4]) {
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+// operands stored k-major: A(i, k) = At[k * lda + i], B(k, j) = B[k * ldb + j]
+// (lda, ldb and both bases multiples of 4 floats: one 16-byte load per
+// operand and k)
+__device__ __forceinline__ void smem_gemm(const float* At, int lda, const float* B, int ldb, int K,
+                                          float acc[4][4], int tid) {
+  const int tx = tid % 16, ty = tid / 16;
 #pragma unroll
   for (int a = 0; a < 4; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
 #pragma unroll 4
   for (int k = 0; k < K; ++k) {
-    float av[4], bv[4];
-#pragma unroll
-    for (int a = 0; a < 4; ++a) av[a] = A[(ty * 4 + a) * ai + k * ak];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) bv[b] = B[k * bk + tx * 4 + b];
+    const float4 av = *reinterpret_cast<const float4*>(At + k * lda + ty * 4);
+    const float4 bv = *reinterpret_cast<const float4*>(B + k * ldb + tx * 4);
+    const float ar[4] = {av.x, av.y, av.z, av.w}, br[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
-      for (int b = 0; b < 4; ++b) acc[a][b] += av[a] * bv[b];
+      for (int b = 0; b < 4; ++b) acc[a][b] += ar[a] * br[b];
   }
 }
 
 // store rows [r0, r0 + 64) x cols [0, 64) of acc into out (row stride ld),
 // rows < nr and cols < nc only
-__device__ __forceinline__ void store_tile(float* out, int ld, int r0, int nr, int nc, const float acc[4][4]) {
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+__device__ __forceinline__ void store_tile(float* out, int ld, int r0, int nr, int nc, const float acc[4][4],
+                                           int tid) {
+  const int tx = tid % 16, ty = tid / 16;
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
     const int r = r0 + ty * 4 + a;
@@ -1085,25 +1086,26 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// shared-memory slices: R [t][f] (row stride 65), X transposed [f][i]
-// (row stride 129), W and S [f][j] (row stride 64)
-constexpr int kRsF = 64 * 65, kXtF = 64 * 129, kWsF = 64 * 64;
-constexpr size_t kDual1PartSmem = (size_t)(kRsF + kXtF + 2 * kWsF) * sizeof(float);
-constexpr size_t kDual1StepSmem = kDual1PartSmem + (size_t)(kXtF + 2 * 128 * 64) * sizeof(float);
+// shared-memory slices, all k-major for smem_gemm: R transposed [f][t]
+// (row stride 68), X transposed [f][i] (row stride 132), X [i][f] (row
+// stride 68), W and S [f][j] (row stride 64)
+constexpr int kRtF = 64 * 68, kXtF = 64 * 132, kXrF = 128 * 68, kWsF = 64 * 64;
+constexpr size_t kDual1PartSmem = (size_t)(kRtF + kXtF + 2 * kWsF) * sizeof(float);
+constexpr size_t kDual1StepSmem = kDual1PartSmem + (size_t)(kXrF + 2 * 128 * 64) * sizeof(float);
 
 // issue copies of the R rows of chunk ch and its window rows of X,
-// features [f0, f0 + 64)
-__device__ void dual1_load_rx(const Geom& g, const Chunk& ch, const Work& w, int u, int f0, float* Rs, float* Xt) {
+// features [f0, f0 + 64), both transposed
+__device__ void dual1_load_rx(const Geom& g, const Chunk& ch, const Work& w, int u, int f0, float* Rt, float* Xt) {
   const int Ct = ch.e - ch.s, nf = min(64, g.F - f0);
   const float* Rw = w.R + ((size_t)u * g.T + ch.s) * g.F + f0;
   const float* Xw = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * g.F + f0;
   for (int l = threadIdx.x; l < 64 * 64; l += blockDim.x) {
     const int r = l / 64, c = l % 64;
-    cp_async4(&Rs[r * 65 + c], Rw + (size_t)r * g.F + c, r < Ct && c < nf, w.R);
+    cp_async4(&Rt[c * 68 + r], Rw + (size_t)r * g.F + c, r < Ct && c < nf, w.R);
   }
   for (int l = threadIdx.x; l < 128 * 64; l += blockDim.x) {
     const int i = l / 64, f = l % 64;
-    cp_async4(&Xt[f * 129 + i], Xw + (size_t)i * g.F + f, i < ch.nw && f < nf, w.X);
+    cp_async4(&Xt[f * 132 + i], Xw + (size_t)i * g.F + f, i < ch.nw && f < nf, w.X);
   }
 }
 
@@ -1119,7 +1121,7 @@ __device__ void dual1_load_ws(const Geom& g, const Work& w, int buf, int u, int 
   }
 }
 
-__device__ void dual1_partials_smem(const Geom& g, const Chunk& ch, const float* Rs, const float* Xt,
+__device__ void dual1_partials_smem(const Geom& g, const Chunk& ch, const float* Rt, const float* Xt,
                                     const float* Ws, const float* Ss, float* pb) {
   const int Ct = ch.e - ch.s, nw = ch.nw, dv = g.d_v;
   float* PW = pb;
@@ -1127,94 +1129,75 @@ __device__ void dual1_partials_smem(const Geom& g, const Chunk& ch, const float*
   float* PX = PS + (size_t)g.C * dv;
   float* PG = PX + (size_t)g.C * g.Kw;
   float acc[4][4];
-  smem_gemm(Rs, 65, 1, Ws, 64, 64, acc);
-  store_tile(PW, dv, 0, Ct, dv, acc);
-  smem_gemm(Rs, 65, 1, Ss, 64, 64, acc);
-  store_tile(PS, dv, 0, Ct, dv, acc);
+  smem_gemm(Rt, 68, Ws, 64, 64, acc, threadIdx.x);
+  store_tile(PW, dv, 0, Ct, dv, acc, threadIdx.x);
+  smem_gemm(Rt, 68, Ss, 64, 64, acc, threadIdx.x);
+  store_tile(PS, dv, 0, Ct, dv, acc, threadIdx.x);
   for (int i0 = 0; i0 < nw; i0 += 64) {
-    smem_gemm(Rs, 65, 1, Xt + i0, 129, 64, acc);
-    store_tile(PX + i0, g.Kw, 0, Ct, nw - i0, acc);
-    smem_gemm(Xt + i0, 1, 129, Ws, 64, 64, acc);
-    store_tile(PG, dv, i0, nw, dv, acc);
+    smem_gemm(Rt, 68, Xt + i0, 132, 64, acc, threadIdx.x);
+    store_tile(PX + i0, g.Kw, 0, Ct, nw - i0, acc, threadIdx.x);
+    smem_gemm(Xt + i0, 132, Ws, 64, 64, acc, threadIdx.x);
+    store_tile(PG, dv, i0, nw, dv, acc, threadIdx.x);
   }
 }
 
 // partial products of the first chunk, from the state in global memory
 __global__ void __launch_bounds__(256) k_dual1_partials(Geom g, Chunk ch, Work w, int buf, float* part) {
-  extern __shared__ float sm[];
-  float* Rs = sm;
-  float* Xt = Rs + kRsF;
+  extern __shared__ __align__(16) float sm[];
+  float* Rt = sm;
+  float* Xt = Rt + kRtF;
   float* Ws = Xt + kXtF;
   float* Ss = Ws + kWsF;
   const int kb = blockIdx.x, u = blockIdx.y, f0 = kb * 64;
   dual1_load_ws(g, w, buf, u, f0, Ws, Ss);
-  dual1_load_rx(g, ch, w, u, f0, Rs, Xt);
+  dual1_load_rx(g, ch, w, u, f0, Rt, Xt);
   cp_async_commit();
   cp_async_wait<0>();
   __syncthreads();
-  dual1_partials_smem(g, ch, Rs, Xt, Ws, Ss, part + ((size_t)u * gridDim.x + kb) * dual1_part_floats(g));
+  dual1_partials_smem(g, ch, Rt, Xt, Ws, Ss, part + ((size_t)u * gridDim.x + kb) * dual1_part_floats(g));
 }
 
-// floats of the combine kernel's staging buffer
-__host__ __device__ inline size_t dual1_combine_floats(const Geom& g) {
-  const size_t ks = (g.F + 63) / 64;
-  return ks * (32 * (size_t)g.Kw + 512) + 17 * (size_t)g.Kw;
+__host__ __device__ inline Chunk dual1_chunk_at(const Geom& g, int s) {
+  Chunk c;
+  c.s = s;
+  c.e = s + g.C;
+  c.lo = s - g.c + 1;
+  if (c.lo < -g.n_prev) c.lo = -g.n_prev;
+  c.nw = c.e - c.lo;
+  return c;
 }
 
-// coefficient scans, slice sums, dy and the chunk's read-out; one CTA per
-// (16 columns, 16 tokens, unit)
-__global__ void __launch_bounds__(256) k_dual1_combine(Geom g, Chunk ch, Work w, const float* theta,
-                                                        const float* eta, const float* alpha, const float* part,
-                                                        float* dys, float* y) {
-  extern __shared__ float sm[];
-  __shared__ float M[16][129];   // Cw, then Cw (.) R X^T, for 16 tokens
-  __shared__ float Dy[128][17];  // dy for 16 columns
-  __shared__ float th[64], et[64], be[64], Bt[64], Dt[64], cse[128], cwe[128];
-  const int jb = blockIdx.x * 16, tb = blockIdx.y * 16, u = blockIdx.z;
-  const int Ct = ch.e - ch.s, nw = ch.nw, dv = g.d_v, Kw = g.Kw;
-  const int ks = (g.F + 63) / 64;
-  const size_t per = dual1_part_floats(g);
-  const float* pu = part + (size_t)u * ks * per;
-  const size_t oS = (size_t)g.C * dv, oX = 2 * oS, oG = oX + (size_t)g.C * Kw;
-  const size_t row0 = (size_t)u * g.L + ch.lo + g.n_prev;
-  // staging: sG[kb][i][16], sX[kb][16][Kw], sP[kb][2][16][16], sV[i][16], sGam[i]
-  float* sG = sm;
-  float* sX = sG + (size_t)ks * Kw * 16;
-  float* sP = sX + (size_t)ks * 16 * Kw;
-  float* sV = sP + (size_t)ks * 512;
-  float* sGam = sV + (size_t)Kw * 16;
-  for (int l = threadIdx.x; l < ks * nw * 16; l += blockDim.x) {
-    const int kb = l / (nw * 16), r = l % (nw * 16), i = r / 16, jj = r % 16;
-    cp_async4(&sG[((size_t)kb * Kw + i) * 16 + jj], pu + kb * per + oG + (size_t)i * dv + jb + jj, jb + jj < dv, part);
-  }
-  for (int l = threadIdx.x; l < ks * 16 * nw; l += blockDim.x) {
-    const int kb = l / (16 * nw), r = l % (16 * nw), tt = r / nw, i = r % nw;
-    cp_async4(&sX[((size_t)kb * 16 + tt) * Kw + i], pu + kb * per + oX + (size_t)(tb + tt) * Kw + i, tb + tt < Ct,
-              part);
-  }
-  for (int l = threadIdx.x; l < ks * 512; l += blockDim.x) {
-    const int kb = l / 512, h = (l / 256) % 2, tt = (l / 16) % 16, jj = l % 16;
-    cp_async4(&sP[l], pu + kb * per + (h ? oS : 0) + (size_t)(tb + tt) * dv + jb + jj,
-              tb + tt < Ct && jb + jj < dv, part);
-  }
-  for (int l = threadIdx.x; l < nw * 16; l += blockDim.x) {
-    const int i = l / 16, jj = l % 16;
-    cp_async4(&sV[l], w.V + (row0 + i) * dv + jb + jj, jb + jj < dv, w.V);
-  }
-  for (int i = threadIdx.x; i < nw; i += blockDim.x) cp_async4(&sGam[i], w.G + row0 + i, true, w.G);
+// per (unit, chunk) coefficient block: Cw [C][Kw], cs_e [Kw], cw_e [Kw],
+// B_t [C], D_t [C], (A_e, B_e, D_e, pad)
+__host__ __device__ inline size_t dual1_coef_floats(const Geom& g) {
+  return (size_t)g.C * g.Kw + 2 * (size_t)g.Kw + 2 * (size_t)g.C + 4;
+}
+
+// The gate scans depend on theta, eta, alpha only, so every chunk's are
+// formed up front, one CTA per (chunk, unit):
+//   Cs_t[i] = eta_t Cs_{t-1}[i] + theta_t [t in window of row i],
+//   Cw_t[i] = (1 - alpha_t) Cw_{t-1}[i] + Cs_t[i],
+//   A_t = prod eta, B_t = prod (1 - alpha), D_t = (1 - alpha_t) D_{t-1} + A_t.
+__global__ void __launch_bounds__(160) k_dual1_coef_all(Geom g, const float* theta, const float* eta,
+                                                         const float* alpha, float* coef) {
+  __shared__ float th[64], et[64], be[64];
+  const int n = blockIdx.x, u = blockIdx.y;
+  const Chunk ch = dual1_chunk_at(g, n * g.C);
+  const int Ct = g.C;
   for (int r = threadIdx.x; r < Ct; r += blockDim.x) {
-    cp_async4(&th[r], theta + (size_t)u * g.T + ch.s + r, true, theta);
-    cp_async4(&et[r], eta + (size_t)u * g.T + ch.s + r, true, eta);
-    cp_async4(&be[r], alpha + (size_t)u * g.T + ch.s + r, true, alpha);
+    th[r] = theta[(size_t)u * g.T + ch.s + r];
+    et[r] = eta[(size_t)u * g.T + ch.s + r];
+    be[r] = 1.f - alpha[(size_t)u * g.T + ch.s + r];
   }
-  cp_async_commit();
-  cp_async_wait<0>();
   __syncthreads();
-  for (int r = threadIdx.x; r < Ct; r += blockDim.x) be[r] = 1.f - be[r];
-  __syncthreads();
-  // window row i: Cs_t = eta_t Cs_{t-1} + theta_t [t in window of i],
-  // Cw_t = (1 - alpha_t) Cw_{t-1} + Cs_t
-  if (threadIdx.x < nw) {
+  float* cb = coef + ((size_t)u * gridDim.x + n) * dual1_coef_floats(g);
+  float* Cw = cb;
+  float* cse = Cw + (size_t)g.C * g.Kw;
+  float* cwe = cse + g.Kw;
+  float* Bt = cwe + g.Kw;
+  float* Dt = Bt + g.C;
+  float* ABD = Dt + g.C;
+  if (threadIdx.x < ch.nw) {
     const int i = threadIdx.x, ti = ch.lo + i;
     float cs = 0.f, cw = 0.f;
     for (int r = 0; r < Ct; ++r) {
@@ -1222,7 +1205,7 @@ __global__ void __launch_bounds__(256) k_dual1_combine(Geom g, Chunk ch, Work w,
       const bool in_win = ti <= t && t <= ti + g.c - 1;
       cs = et[r] * cs + (in_win ? th[r] : 0.f);
       cw = be[r] * cw + cs;
-      if (r >= tb && r < tb + 16) M[r - tb][i] = cw;
+      Cw[(size_t)r * g.Kw + i] = cw;
     }
     cse[i] = cs;
     cwe[i] = cw;
@@ -1235,91 +1218,137 @@ __global__ void __launch_bounds__(256) k_dual1_combine(Geom g, Chunk ch, Work w,
       Bt[r] = Bp;
       Dt[r] = Dp;
     }
+    ABD[0] = Ap;
+    ABD[1] = Bp;
+    ABD[2] = Dp;
   }
-  __syncthreads();
+}
+
+// Sum of the slices' partial products, one thread per element of a unit's
+// block, with the elementwise steps that need only that element:
+//   PW, PS copied;  M[t][i] = Cw_t[i] (R X^T)[t][i];
+//   dy[i][j] = 2 gamma_i ((X W)[i][j] - v_i[j]) and its cs_e / cw_e scalings.
+__global__ void __launch_bounds__(256) k_dual1_reduce(Geom g, Chunk ch, int n, Work w, const float* part,
+                                                       const float* coef, float* red, float* dys) {
+  const int u = blockIdx.y;
+  const size_t per = dual1_part_floats(g);
+  const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= per) return;
+  const int ks = (g.F + 63) / 64, dv = g.d_v, Kw = g.Kw;
+  const size_t oX = 2 * (size_t)g.C * dv, oG = oX + (size_t)g.C * Kw;
+  // rows past the chunk's window were never written: skip them
+  if (e >= oX && e < oG && (int)((e - oX) % Kw) >= ch.nw) return;
+  if (e >= oG && (int)((e - oG) / dv) >= ch.nw) return;
+  const float* p = part + (size_t)u * ks * per + e;
+  float s = 0.f;
+#pragma unroll 16
+  for (int kb = 0; kb < ks; ++kb) s += p[kb * per];
+  float* ru = red + (size_t)u * per;
+  if (e < oX) {
+    ru[e] = s;
+  } else if (e < oG) {
+    const float* Cw = coef + ((size_t)u * (g.T / g.C) + n) * dual1_coef_floats(g);
+    ru[e] = Cw[e - oX] * s;
+  } else {
+    const float* cb = coef + ((size_t)u * (g.T / g.C) + n) * dual1_coef_floats(g);
+    const float* cse = cb + (size_t)g.C * Kw;
+    const float* cwe = cse + Kw;
+    const int i = (int)((e - oG) / dv), j = (int)((e - oG) % dv);
+    const size_t row = (size_t)u * g.L + ch.lo + g.n_prev + i;
+    const float d = 2.f * w.G[row] * (s - w.V[row * dv + j]);
+    ru[e] = d;
+    dys[((size_t)u * 2 + 0) * Kw * dv + (size_t)i * dv + j] = cse[i] * d;
+    dys[((size_t)u * 2 + 1) * Kw * dv + (size_t)i * dv + j] = cwe[i] * d;
+  }
+}
+
+// y_t = B_t (R W)_t + D_t (R S)_t - (M dY)_t; one CTA per (16 columns,
+// 16 tokens, unit)
+__global__ void __launch_bounds__(256) k_dual1_readout(Geom g, Chunk ch, int n, const float* red,
+                                                        const float* coef, float* y) {
+  __shared__ float M[16][129];
+  __shared__ float Dy[128][17];
+  const int jb = blockIdx.x * 16, tb = blockIdx.y * 16, u = blockIdx.z;
+  const int Ct = ch.e - ch.s, nw = ch.nw, dv = g.d_v, Kw = g.Kw;
+  const size_t per = dual1_part_floats(g);
+  const float* ru = red + (size_t)u * per;
+  const size_t oS = (size_t)g.C * dv, oX = 2 * oS, oG = oX + (size_t)g.C * Kw;
   for (int l = threadIdx.x; l < nw * 16; l += blockDim.x) {
-    const int i = l / 16, jj = l % 16, j = jb + jj;
-    float d = 0.f;
-    if (j < dv) {
-      float s = 0.f;
-      for (int kb = 0; kb < ks; ++kb) s += sG[((size_t)kb * Kw + i) * 16 + jj];
-      d = 2.f * sGam[i] * (s - sV[l]);
-      if (blockIdx.y == 0) {
-        dys[((size_t)u * 2 + 0) * Kw * dv + (size_t)i * dv + j] = cse[i] * d;
-        dys[((size_t)u * 2 + 1) * Kw * dv + (size_t)i * dv + j] = cwe[i] * d;
-      }
-    }
-    Dy[i][jj] = d;
+    const int i = l >> 4, jj = l & 15;
+    Dy[i][jj] = jb + jj < dv ? ru[oG + (size_t)i * dv + jb + jj] : 0.f;
   }
-  for (int l = threadIdx.x; l < 16 * nw; l += blockDim.x) {
-    const int tt = l / nw, i = l % nw, t = tb + tt;
-    float m = 0.f;
-    if (t < Ct) {
-      float s = 0.f;
-      for (int kb = 0; kb < ks; ++kb) s += sX[((size_t)kb * 16 + tt) * Kw + i];
-      m = M[tt][i] * s;
-    }
-    M[tt][i] = m;
+  {
+    const int i = threadIdx.x & 127;
+    if (i < nw)
+      for (int tt = threadIdx.x >> 7; tt < 16; tt += 2)
+        M[tt][i] = tb + tt < Ct ? ru[oX + (size_t)(tb + tt) * Kw + i] : 0.f;
   }
   __syncthreads();
   const int tt = threadIdx.x / 16, jj = threadIdx.x % 16, t = tb + tt, j = jb + jj;
   if (t >= Ct || j >= dv) return;
-  float pw = 0.f, ps = 0.f;
-  for (int kb = 0; kb < ks; ++kb) {
-    pw += sP[kb * 512 + threadIdx.x];
-    ps += sP[kb * 512 + 256 + threadIdx.x];
-  }
+  const float* cb = coef + ((size_t)u * (g.T / g.C) + n) * dual1_coef_floats(g);
+  const float* Bt = cb + (size_t)g.C * Kw + 2 * (size_t)Kw;
+  const float* Dt = Bt + g.C;
   float c = 0.f;
   for (int i = 0; i < nw; ++i) c += M[tt][i] * Dy[i][jj];
-  y[((size_t)u * g.T + ch.s + t) * dv + j] = Bt[t] * pw + Dt[t] * ps - c;
+  y[((size_t)u * g.T + ch.s + t) * dv + j] =
+      Bt[t] * ru[(size_t)t * dv + j] + Dt[t] * ru[oS + (size_t)t * dv + j] - c;
 }
 
 // chunk-end state of one 64-feature slice, then (if there is a next chunk)
-// that slice's partial products of the next chunk from the new state
-__global__ void __launch_bounds__(256) k_dual1_step(Geom g, Chunk ch, Chunk nx, int has_next, Work w, int buf,
-                                                     const float* eta, const float* alpha, const float* dys,
-                                                     float* part) {
-  extern __shared__ float sm[];
-  float* Rs = sm;          // next chunk's R
-  float* Xt = Rs + kRsF;   // this chunk's X, transposed
+// that slice's partial products of the next chunk from the new state.
+// 512 threads: the two 256-thread halves take different products.
+__global__ void __launch_bounds__(512) k_dual1_step(Geom g, Chunk ch, Chunk nx, int has_next, int n, Work w,
+                                                     int buf, const float* coef, const float* dys, float* part) {
+  extern __shared__ __align__(16) float sm[];
+  float* Rt = sm;          // next chunk's R, transposed
+  float* Xt = Rt + kRtF;   // next chunk's X, transposed
   float* Ws = Xt + kXtF;
   float* Ss = Ws + kWsF;
-  float* Xn = Ss + kWsF;   // next chunk's X, transposed
-  float* Dc = Xn + kXtF;   // [2][128][64]: cs_e dy, cw_e dy
-  __shared__ float sc[3];
+  float* Xr = Ss + kWsF;   // this chunk's X [i][f]
+  float* Dc = Xr + kXrF;   // [2][128][64]: cs_e dy, cw_e dy
   const int kb = blockIdx.x, u = blockIdx.y, f0 = kb * 64, dv = g.d_v, nw = ch.nw;
   const int nf = min(64, g.F - f0);
+  const int half = threadIdx.x >> 8, tid = threadIdx.x & 255;
   const size_t so = ((size_t)u * g.F + f0) * dv;
   dual1_load_ws(g, w, buf, u, f0, Ws, Ss);
   const float* Xw = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * g.F + f0;
   for (int l = threadIdx.x; l < 128 * 64; l += blockDim.x) {
     const int i = l / 64, f = l % 64;
-    cp_async4(&Xt[f * 129 + i], Xw + (size_t)i * g.F + f, i < nw && f < nf, w.X);
+    cp_async4(&Xr[i * 68 + f], Xw + (size_t)i * g.F + f, i < nw && f < nf, w.X);
     for (int h = 0; h < 2; ++h)
       cp_async4(&Dc[h * 128 * 64 + l], dys + (((size_t)u * 2 + h) * g.Kw + i) * dv + f, i < nw && f < dv, dys);
   }
   cp_async_commit();
-  if (has_next) dual1_load_rx(g, nx, w, u, f0, Rs, Xn);
+  if (has_next) dual1_load_rx(g, nx, w, u, f0, Rt, Xt);
   cp_async_commit();
-  if (threadIdx.x == 0) {
-    float Ap = 1.f, Bp = 1.f, Dp = 0.f;
-    for (int t = ch.s; t < ch.e; ++t) {
-      const float e = eta[(size_t)u * g.T + t], b = 1.f - alpha[(size_t)u * g.T + t];
-      Ap *= e;
-      Bp *= b;
-      Dp = b * Dp + Ap;
-    }
-    sc[0] = Ap;
-    sc[1] = Bp;
-    sc[2] = Dp;
-  }
+  const float* ABD = coef + ((size_t)u * (g.T / g.C) + n) * dual1_coef_floats(g) + (size_t)g.C * g.Kw +
+                     2 * (size_t)g.Kw + 2 * (size_t)g.C;
+  const float Ae = ABD[0], Be = ABD[1], De = ABD[2];
   cp_async_wait<1>();
   __syncthreads();
-  float as_[4][4], aw[4][4];
-  smem_gemm(Xt, 129, 1, Dc, 64, nw, as_);
-  smem_gemm(Xt, 129, 1, Dc + 128 * 64, 64, nw, aw);
-  const float Ae = sc[0], Be = sc[1], De = sc[2];
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  float acc[4][4];
+  // half 0: X^T (cs_e dy) -> S;  half 1: X^T (cw_e dy) -> W
+  smem_gemm(Xr, 68, Dc + half * 128 * 64, 64, nw, acc, tid);
+  const int tx = tid % 16, ty = tid / 16;
+  float sn[4][4];
+  if (half == 0) {
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) sn[a][b] = Ae * Ss[(ty * 4 + a) * 64 + tx * 4 + b] - acc[a][b];
+  } else {
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int o = (ty * 4 + a) * 64 + tx * 4 + b;
+        sn[a][b] = Be * Ws[o] + De * Ss[o] - acc[a][b];
+      }
+  }
+  __syncthreads();   // every read of the old S is done
+  float* dst = half == 0 ? w.Sst[buf ^ 1][0] : w.Wst[buf ^ 1][0];
+  float* sdst = half == 0 ? Ss : Ws;
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
     const int f = ty * 4 + a;
@@ -1328,59 +1357,66 @@ __global__ void __launch_bounds__(256) k_dual1_step(Geom g, Chunk ch, Chunk nx, 
     for (int b = 0; b < 4; ++b) {
       const int j = tx * 4 + b;
       if (j >= dv) continue;
-      const float Sb = Ss[f * 64 + j], Wb = Ws[f * 64 + j];
-      const float Sn = Ae * Sb - as_[a][b], Wn = Be * Wb + De * Sb - aw[a][b];
-      w.Sst[buf ^ 1][0][so + (size_t)f * dv + j] = Sn;
-      w.Wst[buf ^ 1][0][so + (size_t)f * dv + j] = Wn;
-      Ss[f * 64 + j] = Sn;
-      Ws[f * 64 + j] = Wn;
+      dst[so + (size_t)f * dv + j] = sn[a][b];
+      sdst[f * 64 + j] = sn[a][b];
     }
   }
   cp_async_wait<0>();
   if (!has_next) return;
   __syncthreads();
-  dual1_partials_smem(g, nx, Rs, Xn, Ws, Ss, part + ((size_t)u * gridDim.x + kb) * dual1_part_floats(g));
+  const int Ct = nx.e - nx.s, nwn = nx.nw;
+  float* pb = part + ((size_t)u * gridDim.x + kb) * dual1_part_floats(g);
+  float* PW = pb;
+  float* PS = PW + (size_t)g.C * dv;
+  float* PX = PS + (size_t)g.C * dv;
+  float* PG = PX + (size_t)g.C * g.Kw;
+  if (half == 0) {
+    smem_gemm(Rt, 68, Ws, 64, 64, acc, tid);
+    store_tile(PW, dv, 0, Ct, dv, acc, tid);
+    for (int i0 = 0; i0 < nwn; i0 += 64) {
+      smem_gemm(Rt, 68, Xt + i0, 132, 64, acc, tid);
+      store_tile(PX + i0, g.Kw, 0, Ct, nwn - i0, acc, tid);
+    }
+  } else {
+    smem_gemm(Rt, 68, Ss, 64, 64, acc, tid);
+    store_tile(PS, dv, 0, Ct, dv, acc, tid);
+    for (int i0 = 0; i0 < nwn; i0 += 64) {
+      smem_gemm(Xt + i0, 132, Ws, 64, 64, acc, tid);
+      store_tile(PG, dv, i0, nwn, dv, acc, tid);
+    }
+  }
 }
 
 bool dual1_split_supported(const Geom& g) {
-  return g.depth == 1 && g.ns_iters == 0 && g.Kw <= 128 && g.C <= 64 && g.d_v <= 64 &&
-         dual1_combine_floats(g) * sizeof(float) <= 160 * 1024;
+  return g.depth == 1 && g.ns_iters == 0 && g.Kw <= 128 && g.C <= 64 && g.d_v <= 64;
 }
 
-size_t dual1_split_floats(const Geom& g, size_t units) {
-  return units * (2 * (size_t)g.Kw * g.d_v + (size_t)((g.F + 63) / 64) * dual1_part_floats(g));
-}
-
-static Chunk chunk_at(const Geom& g, int s) {
-  Chunk c;
-  c.s = s;
-  c.e = s + g.C;
-  c.lo = s - g.c + 1;
-  if (c.lo < -g.n_prev) c.lo = -g.n_prev;
-  c.nw = c.e - c.lo;
-  return c;
+size_t dual1_split_floats(const Geom& g, size_t units, int T) {
+  return units * (2 * (size_t)g.Kw * g.d_v + (size_t)((g.F + 63) / 64 + 1) * dual1_part_floats(g) +
+                  (size_t)(T / g.C) * dual1_coef_floats(g));
 }
 
 cudaError_t dual1_split(const Geom& g, const Chunk& ch, const Work& w, const GenericIO& io, int buf,
                         cudaStream_t st, int* nl) {
-  const int ks = (g.F + 63) / 64, Ct = ch.e - ch.s;
+  const int ks = (g.F + 63) / 64, Ct = ch.e - ch.s, n = ch.s / g.C;
+  const size_t per = dual1_part_floats(g);
   float* dys = w.gpart;
-  float* part = w.gpart + (size_t)g.units * 2 * g.Kw * g.d_v;
+  float* part = dys + (size_t)g.units * 2 * g.Kw * g.d_v;
+  float* red = part + (size_t)g.units * ks * per;
+  float* coef = red + (size_t)g.units * per;
   if (ch.s == 0) {
+    k_dual1_coef_all<<<dim3(g.T / g.C, g.units), 160, 0, st>>>(g, io.theta, io.eta, io.alpha, coef);
     cudaFuncSetAttribute(k_dual1_partials, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDual1PartSmem);
     k_dual1_partials<<<dim3(ks, g.units), 256, kDual1PartSmem, st>>>(g, ch, w, buf, part);
-    *nl += 1;
+    *nl += 2;
   }
-  const size_t sc = dual1_combine_floats(g) * sizeof(float);
-  cudaFuncSetAttribute(k_dual1_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
-  k_dual1_combine<<<dim3((g.d_v + 15) / 16, (Ct + 15) / 16, g.units), 256, sc, st>>>(g, ch, w, io.theta, io.eta,
-                                                                                      io.alpha, part, dys, io.y);
+  k_dual1_reduce<<<dim3((unsigned)((per + 255) / 256), g.units), 256, 0, st>>>(g, ch, n, w, part, coef, red, dys);
+  k_dual1_readout<<<dim3((g.d_v + 15) / 16, (Ct + 15) / 16, g.units), 256, 0, st>>>(g, ch, n, red, coef, io.y);
   const int has_next = ch.e < g.T;
-  const Chunk nx = chunk_at(g, has_next ? ch.e : ch.s);
+  const Chunk nx = dual1_chunk_at(g, has_next ? ch.e : ch.s);
   cudaFuncSetAttribute(k_dual1_step, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDual1StepSmem);
-  k_dual1_step<<<dim3(ks, g.units), 256, kDual1StepSmem, st>>>(g, ch, nx, has_next, w, buf, io.eta, io.alpha, dys,
-                                                               part);
-  *nl += 2;
+  k_dual1_step<<<dim3(ks, g.units), 512, kDual1StepSmem, st>>>(g, ch, nx, has_next, n, w, buf, coef, dys, part);
+  *nl += 3;
   return cudaGetLastError();
 }
 
