@@ -135,22 +135,40 @@ __device__ __forceinline__ void sync_smem_for_mma() {
   tc::fence_after_sync();
 }
 
-__device__ __forceinline__ float ld_in(const void* p, size_t i, int dt) {
-  return dt == ATLAS_BF16 ? __uint_as_float(((uint32_t)((const uint16_t*)p)[i]) << 16) : ((const float*)p)[i];
-}
-
 // Raw inputs of one chunk held in registers: thread tid covers row
-// r = tid % 64 of the k, q, v tiles, column groups g and g + 4 (g = tid / 64),
-// 8 bf16 (or 8 fp32 as two float4) values each; threads 0-63 hold token
-// tid's gates.  Loaded one chunk ahead so global latency hides behind work.
+// r = tid % 64 of the k and q tiles, column groups g and g + 4 (g = tid / 64),
+// 8 bf16 (or 8 fp32 as two float4) values each; for the cross-slice sums it
+// also holds k, v, q of row 16 (cluster rank) + tid / 16, columns
+// 4 (tid % 16) .. + 3; threads 0-63 hold token tid's gates.  Loaded one
+// chunk ahead so global latency hides behind work.
 struct Prefetch {
-  uint4 k[2][2], q[2][2], v[2][2];   // [group][0: values 0-3 | 1: values 4-7] (fp32) or [group][0] (bf16)
+  uint4 k[2][2], q[2][2];   // [group][0: values 0-3 | 1: values 4-7] (fp32) or [group][0] (bf16)
+  uint4 kd, vd, qd;         // 4 values: fp32, or bf16 in .x, .y
   float th, et, al, ga;
 };
 
+__device__ __forceinline__ uint4 ld_in4(const void* p, size_t i, int dt) {
+  if (dt == ATLAS_BF16) {
+    const uint2 a = __ldg(reinterpret_cast<const uint2*>((const uint16_t*)p + i));
+    return make_uint4(a.x, a.y, 0u, 0u);
+  }
+  return __ldg(reinterpret_cast<const uint4*>((const float*)p + i));
+}
+
+__device__ __forceinline__ void unpack4(uint4 w, int dt, float* o) {
+  if (dt == ATLAS_BF16) {
+    o[0] = __uint_as_float(w.x << 16);
+    o[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    o[2] = __uint_as_float(w.y << 16);
+    o[3] = __uint_as_float(w.y & 0xFFFF0000u);
+  } else {
+    o[0] = __uint_as_float(w.x); o[1] = __uint_as_float(w.y); o[2] = __uint_as_float(w.z); o[3] = __uint_as_float(w.w);
+  }
+}
+
 __device__ __forceinline__ void prefetch_chunk(Prefetch& p, int dt, const void* q, const void* k, const void* v,
                                                const float* theta, const float* eta, const float* alpha,
-                                               const float* gamma, int u, int T, int s) {
+                                               const float* gamma, int u, int T, int s, uint32_t qr) {
   const int tid = threadIdx.x, r = tid % 64, g = tid / 64;
   if (s >= T) return;
   for (int j = 0; j < 2; ++j) {
@@ -158,16 +176,17 @@ __device__ __forceinline__ void prefetch_chunk(Prefetch& p, int dt, const void* 
     if (dt == ATLAS_BF16) {
       p.k[j][0] = __ldg(reinterpret_cast<const uint4*>((const uint16_t*)k + base));
       p.q[j][0] = __ldg(reinterpret_cast<const uint4*>((const uint16_t*)q + base));
-      p.v[j][0] = __ldg(reinterpret_cast<const uint4*>((const uint16_t*)v + base));
     } else {
       p.k[j][0] = __ldg(reinterpret_cast<const uint4*>((const float*)k + base));
       p.k[j][1] = __ldg(reinterpret_cast<const uint4*>((const float*)k + base + 4));
       p.q[j][0] = __ldg(reinterpret_cast<const uint4*>((const float*)q + base));
       p.q[j][1] = __ldg(reinterpret_cast<const uint4*>((const float*)q + base + 4));
-      p.v[j][0] = __ldg(reinterpret_cast<const uint4*>((const float*)v + base));
-      p.v[j][1] = __ldg(reinterpret_cast<const uint4*>((const float*)v + base + 4));
     }
   }
+  const size_t gd = ((size_t)u * T + s + 16 * qr + (tid >> 4)) * 64 + (tid & 15) * 4;
+  p.kd = ld_in4(k, gd, dt);
+  p.vd = ld_in4(v, gd, dt);
+  p.qd = ld_in4(q, gd, dt);
   if (tid < 64) {
     const size_t gi = (size_t)u * T + s + tid;
     p.th = __ldg(theta + gi);
@@ -175,6 +194,13 @@ __device__ __forceinline__ void prefetch_chunk(Prefetch& p, int dt, const void* 
     p.al = __ldg(alpha + gi);
     p.ga = gamma ? __ldg(gamma + gi) : 1.f;
   }
+}
+
+// logistic sigmoid through the hardware tanh: s(z) = (1 + tanh(z / 2)) / 2
+__device__ __forceinline__ float sigmoid_fast(float z) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * z));
+  return fmaf(0.5f, t, 0.5f);
 }
 
 __device__ __forceinline__ void unpack8(const uint4* w, int dt, float* o) {
@@ -190,6 +216,21 @@ __device__ __forceinline__ void unpack8(const uint4* w, int dt, float* o) {
     o[0] = __uint_as_float(x.x); o[1] = __uint_as_float(x.y); o[2] = __uint_as_float(x.z); o[3] = __uint_as_float(x.w);
     o[4] = __uint_as_float(y.x); o[5] = __uint_as_float(y.y); o[6] = __uint_as_float(y.z); o[7] = __uint_as_float(y.w);
   }
+}
+
+// y rows [16q, 16q + 16) of the chunk at token s: r_t + the four slices'
+// Yq from this CTA's slots (thread: row tid / 16, columns 4 (tid % 16) .. + 3)
+__device__ __forceinline__ void y_rows(float* y, const float* slots, const float* qv, int u, int T, int s,
+                                       uint32_t qr) {
+  const int tid = threadIdx.x, rl = tid >> 4, cc = (tid & 15) * 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int p = 0; p < CS; ++p) {
+    const float4 t4 = *reinterpret_cast<const float4*>(slots + (p * 16 + rl) * 64 + cc);
+    acc.x += t4.x; acc.y += t4.y; acc.z += t4.z; acc.w += t4.w;
+  }
+  const size_t gb = ((size_t)u * T + s + 16 * (int)qr + rl) * D + cc;
+  *reinterpret_cast<float4*>(y + gb) = make_float4(qv[0] + acc.x, qv[1] + acc.y, qv[2] + acc.z, qv[3] + acc.w);
 }
 
 struct Ctx {
@@ -267,7 +308,8 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   tc::fence_after_sync();
   Ctx cx{&bar, 0u, true};
   Prefetch pf;
-  prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, 0);
+  prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, 0, qr);
+  float qprev[4] = {0.f, 0.f, 0.f, 0.f};   // q of the previous chunk's rows, for its deferred y
   const uint32_t red_local = tc::smem_u32(sm + RED);
 
   // one state half-update: S <- A_e S - corr_S, W <- B_e W + D_e S - corr_W
@@ -312,7 +354,11 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
         vec[V_GA + tid] = pf.ga;
       }
     }
-    prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, s + TOK);
+    float xkd[4], vvd[4], qcur[4];
+    unpack4(pf.kd, dt, xkd);
+    unpack4(pf.vd, dt, vvd);
+    unpack4(pf.qd, dt, qcur);
+    prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, s + TOK, qr);
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 1: Z, G1
     if (tid == 0 && cx.ok) {
@@ -389,7 +435,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       float a[16], spv[16], m1[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float sg = __frcp_rn(1.f + __expf(-z[i]));
+        const float sg = sigmoid_fast(z[i]);
         a[i] = z[i] * sg;
         spv[i] = sg * (1.f + z[i] * (1.f - sg));
       }
@@ -425,17 +471,11 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     }
     cluster_sync();
     // dy = 2 gamma (X + sum Yp - V) for my 16 rows, broadcast as bf16 into
-    // every CTA's dy operand tile
+    // every CTA's dy operand tile; the same barrier also completed the
+    // previous chunk's Yq slots, so its y rows are summed here too
     {
       const float* red = reinterpret_cast<const float*>(sm + RED);
       const int rl = tid >> 4, cc = (tid & 15) * 4, r = 16 * (int)qr + rl;
-      const size_t gb = ((size_t)u * T + s + r) * D + cc;
-      float xk[4], vv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        xk[i] = ld_in(k, gb + i, dt);
-        vv[i] = ld_in(v, gb + i, dt);
-      }
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int p = 0; p < CS; ++p) {
@@ -443,12 +483,13 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
         acc.x += t4.x; acc.y += t4.y; acc.z += t4.z; acc.w += t4.w;
       }
       const float g2 = 2.f * vec[V_GA + r];
-      const __nv_bfloat162 h0 = __floats2bfloat162_rn(g2 * (xk[0] + acc.x - vv[0]), g2 * (xk[1] + acc.y - vv[1]));
-      const __nv_bfloat162 h1 = __floats2bfloat162_rn(g2 * (xk[2] + acc.z - vv[2]), g2 * (xk[3] + acc.w - vv[3]));
+      const __nv_bfloat162 h0 = __floats2bfloat162_rn(g2 * (xkd[0] + acc.x - vvd[0]), g2 * (xkd[1] + acc.y - vvd[1]));
+      const __nv_bfloat162 h1 = __floats2bfloat162_rn(g2 * (xkd[2] + acc.z - vvd[2]), g2 * (xkd[3] + acc.w - vvd[3]));
       const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&h0), a1 = *reinterpret_cast<const uint32_t*>(&h1);
       const uint32_t off = tc::smem_u32(sm + ODY) + tc::core_offset(r, cc, RGS);
 #pragma unroll
       for (int p = 0; p < CS; ++p) st_cluster_u2(mapa(off, (uint32_t)p), a0, a1);
+      if (s > 0) y_rows(y, reinterpret_cast<const float*>(sm + RED + F32T), qprev, u, T, s - TOK, qr);
     }
     cluster_sync();
     sync_smem_for_mma();
@@ -506,7 +547,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       float aq[16], ab[16], ad[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        aq[i] = zq[i] * __frcp_rn(1.f + __expf(-zq[i]));
+        aq[i] = zq[i] * sigmoid_fast(zq[i]);
         ab[i] = Bt * aq[i];
         ad[i] = Dt * aq[i];
       }
@@ -554,27 +595,13 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
 #pragma unroll
       for (int i = 0; i < 16; i += 4) st_cluster4(dst + 4 * i, make_float4(yq[i], yq[i + 1], yq[i + 2], yq[i + 3]));
     }
-    cluster_sync();
-    // y rows [16q, 16q + 16): R + the four slices' Yq from my local slots
-    {
-      const float* red = reinterpret_cast<const float*>(sm + RED + F32T);
-      const int rl = tid >> 4, cc = (tid & 15) * 4, r = 16 * (int)qr + rl;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int p = 0; p < CS; ++p) {
-        const float4 t4 = *reinterpret_cast<const float4*>(red + (p * 16 + rl) * 64 + cc);
-        acc.x += t4.x; acc.y += t4.y; acc.z += t4.z; acc.w += t4.w;
-      }
-      const size_t gb = ((size_t)u * T + s + r) * D + cc;
-      float4 o;
-      o.x = ld_in(q, gb, dt) + acc.x;
-      o.y = ld_in(q, gb + 1, dt) + acc.y;
-      o.z = ld_in(q, gb + 2, dt) + acc.z;
-      o.w = ld_in(q, gb + 3, dt) + acc.w;
-      *reinterpret_cast<float4*>(y + gb) = o;
-    }
-    sync_smem_for_mma();
+    for (int i = 0; i < 4; ++i) qprev[i] = qcur[i];
+    __syncthreads();
   }
+  // the last chunk's y
+  cluster_sync();
+  y_rows(y, reinterpret_cast<const float*>(sm + RED + F32T), qprev, u, T, T - TOK, qr);
 
   // ---- state slices out
   {
