@@ -44,18 +44,25 @@ constexpr int RGS = 1024;               // row-group stride of a 64-column tile
 constexpr int RGS2 = 2048;              // of a 128-column tile
 constexpr int F32T = 64 * 64 * 4;       // fp32 64x64 tile (swizzled rows)
 constexpr long long kWait = 1ll << 31;
+constexpr uint32_t kSliceBytes = (CS - 1) * 16 * 64 * 4;   // fp32 row quarters from the 3 peers
+constexpr uint32_t kDyBytes = (CS - 1) * 16 * 64 * 2;      // bf16 dy rows from the 3 peers
 
-// shared-memory map (bytes): bf16 operand tiles in the core-matrix layout
+// shared-memory map (bytes): bf16 operand tiles in the core-matrix layout.
+// X, Cw and the gate vectors have two buffers by chunk parity: the next
+// chunk's are filled while the current chunk waits on its cluster barriers.
 constexpr int OW1 = 0, OS1 = OW1 + TILE, OW2 = OS1 + TILE, OS2 = OW2 + TILE;   // state operands
-constexpr int OX = OS2 + TILE, OR_ = OX + TILE, OA = OR_ + TILE, ODY = OA + TILE, ODZ = ODY + TILE;
+constexpr int OX0 = OS2 + TILE, OX1 = OX0 + TILE;                 // X by chunk parity
+constexpr int OR_ = OX1 + TILE, OA = OR_ + TILE, ODY = OA + TILE, ODZ = ODY + TILE;
 constexpr int OSP = ODZ + TILE;                                   // SiLU'(Z)
-constexpr int ORB = OSP + TILE, ORD = ORB + TILE;                 // B_t r_t, D_t r_t
-constexpr int OM1 = ORD + TILE, OAQ = OM1 + TILE, OAQB = OAQ + TILE, OAQD = OAQB + TILE, OM2 = OAQD + TILE;
-constexpr int ODZS = OM2 + TILE, ODYS = ODZS + 2 * TILE;          // [cs.dz | cw.dz], [cs.dy | cw.dy]
-constexpr int CWM = ODYS + 2 * TILE;                              // fp32 Cw[t][i]
-constexpr int RED = CWM + F32T;                                   // Yp slots, Yq slots (cluster-shared)
-constexpr int VEC = RED + 2 * F32T;                               // gate vectors
-constexpr int SMEM_BYTES = VEC + 12 * 64 * 4;
+constexpr int ORB = OSP + TILE, ORD = ORB + TILE;                 // B_t r_t, D_t r_t; later B_t aq_t, D_t aq_t
+constexpr int OM = ORD + TILE, OAQ = OM + TILE;                   // M1, later M2; SiLU(Zq)
+constexpr int ODZS = OAQ + TILE, ODYS = ODZS + 2 * TILE;          // [cs.dz | cw.dz], [cs.dy | cw.dy]
+constexpr int CWM = ODYS + 2 * TILE;                              // fp32 Cw[t][i], by chunk parity
+constexpr int RED = CWM + 2 * F32T;                               // Yp slots, Yq slots (cluster-shared)
+constexpr int VEC = RED + 2 * F32T;                               // gate vectors, by chunk parity
+constexpr int VECN = 12 * 64;                                     // floats per gate-vector buffer
+constexpr int SMEM_BYTES = VEC + 2 * VECN * 4;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory map exceeds a CTA's limit");
 
 // vectors inside VEC
 constexpr int V_TH = 0, V_ET = 64, V_BE = 128, V_GA = 192, V_AP = 256, V_BP = 320, V_DP = 384, V_CS = 448,
@@ -77,6 +84,23 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Bulk copy of `bytes` from this CTA's shared memory to a peer's (cluster
+// address), completing `bytes` of the transaction count of the peer's
+// mbarrier (cluster address); 16-byte aligned, multiple of 16 bytes.
+__device__ __forceinline__ void bulk_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(src), "r"(bytes), "r"(mbar)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the issuing thread's bulk copies have finished reading their sources
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// one arrival on *bar that also expects `bytes` more of transactions
+__device__ __forceinline__ void mbar_arm_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t cta) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(cta));
@@ -86,15 +110,6 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t cta) {
 // Operands are bf16: the memory's state decays over long sequences (to
 // ~1e-8 on a 4096-token Titans run) and needs fp32's exponent range; fp16
 // would flush it to zero.
-__device__ __forceinline__ void st_cluster4(uint32_t addr, float4 v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
-               "f"(v.w)
-               : "memory");
-}
-__device__ __forceinline__ void st_cluster_u2(uint32_t addr, uint32_t a, uint32_t b) {
-  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
-}
-
 __device__ __forceinline__ void st_h8(uint8_t* tile, int rgs, int row, int col, const float* v) {
   __nv_bfloat162 h[4];
 #pragma unroll
@@ -260,6 +275,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
                   int* status) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ uint64_t bar;
+  __shared__ uint64_t xbar[3];   // arrivals of the peers' Yp slices, dy rows, Yq slices
   __shared__ uint32_t tbase;
   float* vec = reinterpret_cast<float*>(sm + VEC);
   float* cwm = reinterpret_cast<float*>(sm + CWM);
@@ -279,10 +295,17 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   const int H = 4 * HQ;
 
   if (warp == 0) tc::tmem_alloc(&tbase, 512);
-  if (tid == 0) tc::mbar_init(&bar, 1);
+  if (tid == 0) {
+    tc::mbar_init(&bar, 1);
+    for (int i = 0; i < 3; ++i) {
+      tc::mbar_init(&xbar[i], 1);
+      mbar_arm_tx(&xbar[i], i == 1 ? kDyBytes : kSliceBytes);   // phase 0 of each
+    }
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  cluster_sync();   // every CTA's exchange barriers are initialised and armed
   const uint32_t tb = tbase;
 
   // ---- state slices in: W1[:, 64q:64q+64] (d x 64), W2[64q:64q+64, :] (64 x d)
@@ -310,11 +333,132 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   Prefetch pf;
   prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, 0, qr);
   float qprev[4] = {0.f, 0.f, 0.f, 0.f};   // q of the previous chunk's rows, for its deferred y
+  float xkd[4], vvd[4], qcur[4];            // this chunk's k, v, q rows of the cross-slice sums
+  float xkn[4], vvn[4], qnx[4];             // the next chunk's
   const uint32_t red_local = tc::smem_u32(sm + RED);
+  // an M = 64 accumulator's row quarters: the owner's own quarter into its
+  // slot, the others into the staging blocks (ODZS, 4 KB per owner)
+  auto stage_slices = [&](uint32_t col, int slot_off) {
+    float v16[16];
+    tc::tmem_ld16_x2(tb + lb + col, v16);
+    tc::tmem_ld_wait();
+    const int owner = row >> 4;
+    float* dst = owner == (int)qr ? reinterpret_cast<float*>(sm + RED + slot_off) + (qr * 16 + (row & 15)) * 64 + cb
+                                  : reinterpret_cast<float*>(sm + ODZS) + (owner * 16 + (row & 15)) * 64 + cb;
+#pragma unroll
+    for (int i = 0; i < 16; i += 4)
+      *reinterpret_cast<float4*>(dst + i) = make_float4(v16[i], v16[i + 1], v16[i + 2], v16[i + 3]);
+    tc::fence_smem_to_async();   // staging is the bulk copies' source
+    __syncthreads();
+  };
+  // thread 0: the three staged quarters to their owners' slots [qr]
+  auto send_slices = [&](int slot_off, int xb) {
+    for (uint32_t p = 1; p < CS; ++p) {
+      const uint32_t dst = (qr + p) % CS;
+      const uint32_t src = tc::smem_u32(sm + ODZS) + dst * 4096;
+      bulk_to_peer(mapa(red_local + slot_off + qr * 4096, dst), src, 4096, mapa(tc::smem_u32(&xbar[xb]), dst));
+    }
+    bulk_commit();
+  };
+  // thread 0 waits for phase `parity` of exchange barrier xb (bounded); the
+  // CTA barrier then makes the arrived data visible to every thread
+  auto xwait = [&](int xb, uint32_t parity) {
+    bool good = true;
+    if (tid == 0 && cx.ok) good = tc::mbar_wait(&xbar[xb], parity, kWait);
+    if (__syncthreads_or(!good)) cx.ok = false;
+  };
+  auto vecb = [&](int b) { return vec + b * VECN; };
+  auto cwmb = [&](int b) { return cwm + b * (F32T / 4); };
+
+  // raw inputs of the chunk at token sn (held in pf) into buffer bn and
+  // registers; then prefetch the chunk after it
+  auto load_chunk = [&](int sn, int bn) {
+    float* vb = vecb(bn);
+    const int r = tid % 64, g = tid / 64;
+    for (int j = 0; j < 2; ++j) {
+      float xk[8], xq[8];
+      unpack8(pf.k[j], dt, xk);
+      unpack8(pf.q[j], dt, xq);
+      st_h8(sm + (bn ? OX1 : OX0), RGS, r, (g + 4 * j) * 8, xk);
+      st_h8(sm + OR_, RGS, r, (g + 4 * j) * 8, xq);
+    }
+    if (tid < 64) {
+      vb[V_TH + tid] = pf.th;
+      vb[V_ET + tid] = pf.et;
+      vb[V_BE + tid] = 1.f - pf.al;
+      vb[V_GA + tid] = pf.ga;
+    }
+    unpack4(pf.kd, dt, xkn);
+    unpack4(pf.vd, dt, vvn);
+    unpack4(pf.qd, dt, qnx);
+    prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, sn + TOK, qr);
+  };
+
+  // gate scans of buffer bn (window of token t is {t})
+  auto scan_chunk = [&](int bn) {
+    float* vb = vecb(bn);
+    float* cwp = cwmb(bn);
+    if (tid < 64) {  // column i = tid of Cs / Cw
+      const int i = tid;
+      float cs = 0.f, cw = 0.f;
+      for (int t0 = 0; t0 < TOK; t0 += 8) {
+        float et[8], th[8], be[8];   // loads ahead of the stores (same shared array)
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq) {
+          et[qq] = vb[V_ET + t0 + qq];
+          th[qq] = vb[V_TH + t0 + qq];
+          be[qq] = vb[V_BE + t0 + qq];
+        }
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq) {
+          cs = et[qq] * cs + (t0 + qq == i ? th[qq] : 0.f);
+          cw = be[qq] * cw + cs;
+          cwp[swz(t0 + qq, i)] = cw;
+        }
+      }
+      vb[V_CS + i] = cs;
+      vb[V_CW + i] = cw;
+    } else if (tid == 64) {
+      float Ap = 1.f, Bp = 1.f, Dp = 0.f;
+      for (int t0 = 0; t0 < TOK; t0 += 8) {
+        float et[8], be[8];
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq) {
+          et[qq] = vb[V_ET + t0 + qq];
+          be[qq] = vb[V_BE + t0 + qq];
+        }
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq) {
+          Ap *= et[qq];
+          Bp *= be[qq];
+          Dp = be[qq] * Dp + Ap;
+          vb[V_AP + t0 + qq] = Ap;
+          vb[V_BP + t0 + qq] = Bp;
+          vb[V_DP + t0 + qq] = Dp;
+        }
+      }
+    }
+  };
+
+  // (B R), (D R): the read-out's state terms of buffer bn's chunk
+  auto brdr = [&](int bn) {
+    const float* vb = vecb(bn);
+    const int r = tid % 64, g = tid / 64;
+    const float Bt = vb[V_BP + r], Dt = vb[V_DP + r];
+    for (int j = 0; j < 2; ++j) {
+      const int cc = (g + 4 * j) * 8;
+      float x[8], b8[8], d8[8];
+      ld_h8(sm + OR_, RGS, r, cc, x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { b8[i] = Bt * x[i]; d8[i] = Dt * x[i]; }
+      st_h8(sm + ORB, RGS, r, cc, b8);
+      st_h8(sm + ORD, RGS, r, cc, d8);
+    }
+  };
 
   // one state half-update: S <- A_e S - corr_S, W <- B_e W + D_e S - corr_W
-  auto state_update = [&](uint32_t c_corr, uint32_t s_w, uint32_t s_s, int ow, int os) {
-    const float Ae = vec[V_AP + 63], Be = vec[V_BP + 63], De = vec[V_DP + 63];
+  auto state_update = [&](const float* vb, uint32_t c_corr, uint32_t s_w, uint32_t s_s, int ow, int os) {
+    const float Ae = vb[V_AP + 63], Be = vb[V_BP + 63], De = vb[V_DP + 63];
     float scr[16], wcr[16], so[16], wo[16];
     tc::tmem_ld16_x2(tb + lb + c_corr, scr);
     tc::tmem_ld16_x2(tb + lb + c_corr + 64, wcr);
@@ -336,93 +480,29 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     tc::tmem_st_wait();
   };
 
-  for (int s = 0; s < T; s += TOK) {
-    // ---------------------------------------------------------------- L
-    {
-      const int r = tid % 64, g = tid / 64;
-      for (int j = 0; j < 2; ++j) {
-        float xk[8], xq[8];
-        unpack8(pf.k[j], dt, xk);
-        unpack8(pf.q[j], dt, xq);
-        st_h8(sm + OX, RGS, r, (g + 4 * j) * 8, xk);
-        st_h8(sm + OR_, RGS, r, (g + 4 * j) * 8, xq);
-      }
-      if (tid < 64) {
-        vec[V_TH + tid] = pf.th;
-        vec[V_ET + tid] = pf.et;
-        vec[V_BE + tid] = 1.f - pf.al;
-        vec[V_GA + tid] = pf.ga;
-      }
-    }
-    float xkd[4], vvd[4], qcur[4];
-    unpack4(pf.kd, dt, xkd);
-    unpack4(pf.vd, dt, vvd);
-    unpack4(pf.qd, dt, qcur);
-    prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, s + TOK, qr);
-    sync_smem_for_mma();
-    // ---------------------------------------------------------------- 1: Z, G1
+  // ---- first chunk's inputs, gate scans, (B R), (D R) and Z = X W1q
+  load_chunk(0, 0);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) { xkd[i] = xkn[i]; vvd[i] = vvn[i]; qcur[i] = qnx[i]; }
+  __syncthreads();
+  scan_chunk(0);
+  __syncthreads();
+  brdr(0);
+  sync_smem_for_mma();
+  if (tid == 0 && cx.ok) mma64(tb + C_Z, sm + OX0, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
+
+  // Software pipeline: a chunk starts with its X, R, gates, gate scans,
+  // (B R), (D R) in shared memory and Z = X W1q issued; the next chunk's
+  // are prepared inside this chunk's cluster-barrier waits and tail.
+  for (int s = 0, n = 0; s < T; s += TOK, ++n) {
+    const int b = n & 1;
+    const bool has_next = s + TOK < T;
+    const float* vb = vecb(b);
+    const float* cwc = cwmb(b);
+    const uint8_t* oxc = sm + (b ? OX1 : OX0);
+    // ---------------------------------------------------------------- 1: G1, Zq state terms
     if (tid == 0 && cx.ok) {
-      mma64(tb + C_Z, sm + OX, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
-      mma64(tb + C_G1, sm + OR_, 0, RGS, sm + OX, 0, RGS, 64, 64, false);
-    }
-    // gate scans (overlap the first products)
-    if (tid < 64) {  // column i = tid of Cs / Cw (window of token t is {t})
-      const int i = tid;
-      float cs = 0.f, cw = 0.f;
-      for (int t0 = 0; t0 < TOK; t0 += 8) {
-        float et[8], th[8], be[8];   // loads ahead of the stores (same shared array)
-#pragma unroll
-        for (int qq = 0; qq < 8; ++qq) {
-          et[qq] = vec[V_ET + t0 + qq];
-          th[qq] = vec[V_TH + t0 + qq];
-          be[qq] = vec[V_BE + t0 + qq];
-        }
-#pragma unroll
-        for (int qq = 0; qq < 8; ++qq) {
-          cs = et[qq] * cs + (t0 + qq == i ? th[qq] : 0.f);
-          cw = be[qq] * cw + cs;
-          cwm[swz(t0 + qq, i)] = cw;
-        }
-      }
-      vec[V_CS + i] = cs;
-      vec[V_CW + i] = cw;
-    } else if (tid == 64) {
-      float Ap = 1.f, Bp = 1.f, Dp = 0.f;
-      for (int t0 = 0; t0 < TOK; t0 += 8) {
-        float et[8], be[8];
-#pragma unroll
-        for (int qq = 0; qq < 8; ++qq) {
-          et[qq] = vec[V_ET + t0 + qq];
-          be[qq] = vec[V_BE + t0 + qq];
-        }
-#pragma unroll
-        for (int qq = 0; qq < 8; ++qq) {
-          Ap *= et[qq];
-          Bp *= be[qq];
-          Dp = be[qq] * Dp + Ap;
-          vec[V_AP + t0 + qq] = Ap;
-          vec[V_BP + t0 + qq] = Bp;
-          vec[V_DP + t0 + qq] = Dp;
-        }
-      }
-    }
-    __syncthreads();
-    // (B R), (D R): the read-out's state terms, issued with the first group
-    {
-      const int r = tid % 64, g = tid / 64;
-      const float Bt = vec[V_BP + r], Dt = vec[V_DP + r];
-      for (int j = 0; j < 2; ++j) {
-        const int cc = (g + 4 * j) * 8;
-        float x[8], b8[8], d8[8];
-        ld_h8(sm + OR_, RGS, r, cc, x);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) { b8[i] = Bt * x[i]; d8[i] = Dt * x[i]; }
-        st_h8(sm + ORB, RGS, r, cc, b8);
-        st_h8(sm + ORD, RGS, r, cc, d8);
-      }
-    }
-    sync_smem_for_mma();
-    if (tid == 0 && cx.ok) {
+      mma64(tb + C_G1, sm + OR_, 0, RGS, oxc, 0, RGS, 64, 64, false);
       mma64(tb + C_ZQ, sm + ORB, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
       mma64(tb + C_ZQ, sm + ORD, 0, RGS, sm + OS1, 1, RGS, 64, 64, true);
     }
@@ -441,38 +521,41 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       }
 #pragma unroll
       for (int i = 0; i < 16; i += 4) {
-        const float4 c4 = *reinterpret_cast<const float4*>(cwm + swz(row, cb + i));
+        const float4 c4 = *reinterpret_cast<const float4*>(cwc + swz(row, cb + i));
         m1[i] = -c4.x * g[i]; m1[i + 1] = -c4.y * g[i + 1]; m1[i + 2] = -c4.z * g[i + 2]; m1[i + 3] = -c4.w * g[i + 3];
       }
       st_h8(sm + OA, RGS, row, cb, a);
       st_h8(sm + OA, RGS, row, cb + 8, a + 8);
       st_h8(sm + OSP, RGS, row, cb, spv);
       st_h8(sm + OSP, RGS, row, cb + 8, spv + 8);
-      st_h8(sm + OM1, RGS, row, cb, m1);
-      st_h8(sm + OM1, RGS, row, cb + 8, m1 + 8);
+      st_h8(sm + OM, RGS, row, cb, m1);
+      st_h8(sm + OM, RGS, row, cb + 8, m1 + 8);
     }
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 2: Yp = A W2q
     if (tid == 0 && cx.ok) mma64(tb + C_YP, sm + OA, 0, RGS, sm + OW2, 1, RGS, 64, 64, false);
     commit_wait(cx);
     // Cross-slice sums are reduce-scatters over DSMEM: CTA p owns rows
-    // [16p, 16p + 16).  Every CTA pushes the row quarter of its partial to the
-    // owner's slot [sender][row % 16][col] (fire-and-forget remote stores),
-    // the owner sums its four slots locally.  RED holds the Yp slots, RED +
-    // F32T the Yq slots; a slot is rewritten only after the owner has passed
-    // the barrier that follows its reads.
-    {
-      float yp[16];
-      tc::tmem_ld16_x2(tb + lb + C_YP, yp);
-      tc::tmem_ld_wait();
-      const uint32_t dst = mapa(red_local + (uint32_t)(((qr * 16 + (row & 15)) * 64 + cb) * 4), (uint32_t)(row >> 4));
-#pragma unroll
-      for (int i = 0; i < 16; i += 4) st_cluster4(dst + 4 * i, make_float4(yp[i], yp[i + 1], yp[i + 2], yp[i + 3]));
-    }
-    cluster_sync();
-    // dy = 2 gamma (X + sum Yp - V) for my 16 rows, broadcast as bf16 into
-    // every CTA's dy operand tile; the same barrier also completed the
-    // previous chunk's Yq slots, so its y rows are summed here too
+    // [16p, 16p + 16).  Every CTA stages the row quarters of its partial
+    // (fp32, 4 KB each; ODZS is free until the dz step), bulk-copies each to
+    // its owner's slot [sender] with a transaction on the owner's xbar, and
+    // writes its own quarter straight into its slot.  RED holds the Yp
+    // slots, RED + F32T the Yq slots.  A slot is rewritten only after its
+    // owner has read it: the owner reads before sending the next dy rows,
+    // which every sender needs before its next slice is formed.
+    if (tid == 0) bulk_wait_read();   // the previous Yq copies have left ODZS
+    __syncthreads();
+    stage_slices(C_YP, 0);
+    if (tid == 0 && cx.ok) send_slices(0, 0);
+    // while the peers' slices travel: the next chunk's inputs (R and its
+    // buffers are free: this chunk's G1, (B R), (D R) products are done)
+    if (has_next) load_chunk(s + TOK, b ^ 1);
+    xwait(0, n & 1);
+    if (tid == 0 && cx.ok && has_next) mbar_arm_tx(&xbar[0], kSliceBytes);
+    // dy = 2 gamma (X + sum Yp - V) for my 16 rows into my dy operand tile,
+    // then bulk-copied (2 KB: rows 16q .. 16q + 15 are two row groups) into
+    // every peer's; the previous chunk's Yq slots are summed here too
+    if (s > 0) xwait(2, (n - 1) & 1);
     {
       const float* red = reinterpret_cast<const float*>(sm + RED);
       const int rl = tid >> 4, cc = (tid & 15) * 4, r = 16 * (int)qr + rl;
@@ -482,23 +565,40 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
         const float4 t4 = *reinterpret_cast<const float4*>(red + (p * 16 + rl) * 64 + cc);
         acc.x += t4.x; acc.y += t4.y; acc.z += t4.z; acc.w += t4.w;
       }
-      const float g2 = 2.f * vec[V_GA + r];
+      const float g2 = 2.f * vb[V_GA + r];
       const __nv_bfloat162 h0 = __floats2bfloat162_rn(g2 * (xkd[0] + acc.x - vvd[0]), g2 * (xkd[1] + acc.y - vvd[1]));
       const __nv_bfloat162 h1 = __floats2bfloat162_rn(g2 * (xkd[2] + acc.z - vvd[2]), g2 * (xkd[3] + acc.w - vvd[3]));
-      const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&h0), a1 = *reinterpret_cast<const uint32_t*>(&h1);
-      const uint32_t off = tc::smem_u32(sm + ODY) + tc::core_offset(r, cc, RGS);
-#pragma unroll
-      for (int p = 0; p < CS; ++p) st_cluster_u2(mapa(off, (uint32_t)p), a0, a1);
+      uint2 pk;
+      pk.x = *reinterpret_cast<const uint32_t*>(&h0);
+      pk.y = *reinterpret_cast<const uint32_t*>(&h1);
+      *reinterpret_cast<uint2*>(sm + ODY + tc::core_offset(r, cc, RGS)) = pk;
       if (s > 0) y_rows(y, reinterpret_cast<const float*>(sm + RED + F32T), qprev, u, T, s - TOK, qr);
     }
-    cluster_sync();
+    tc::fence_smem_to_async();   // the dy rows are the bulk copies' source
+    __syncthreads();
+    if (tid == 0) {
+      // Yq slots read (the y rows above): the next Yq slices may come
+      if (s > 0 && cx.ok) mbar_arm_tx(&xbar[2], kSliceBytes);
+      if (cx.ok) {
+        const uint32_t src = tc::smem_u32(sm + ODY + 2 * (int)qr * RGS);
+        for (uint32_t p = 1; p < CS; ++p) {
+          const uint32_t dst = (qr + p) % CS;
+          bulk_to_peer(mapa(src, dst), src, 2 * RGS, mapa(tc::smem_u32(&xbar[1]), dst));
+        }
+        bulk_commit();
+      }
+    }
+    // while the peers' dy rows travel: the next chunk's gate scans
+    if (has_next) scan_chunk(b ^ 1);
+    xwait(1, n & 1);
+    if (tid == 0 && cx.ok && has_next) mbar_arm_tx(&xbar[1], kDyBytes);
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 3: dz' = dy W2q^T
     if (tid == 0 && cx.ok) mma64(tb + C_Z, sm + ODY, 0, RGS, sm + OW2, 0, RGS, 64, 64, false);
     // state operand diag(cs | cw) dy from the broadcast dy tile (overlaps the product)
     {
       const int r = tid % 64, g = tid / 64;
-      const float csr = vec[V_CS + r], cwr = vec[V_CW + r];
+      const float csr = vb[V_CS + r], cwr = vb[V_CW + r];
       for (int j = 0; j < 2; ++j) {
         const int cc = (g + 4 * j) * 8;
         float dy[8], t0[8], t1[8];
@@ -509,6 +609,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
         st_h8(sm + ODYS, RGS2, r, 64 + cc, t1);
       }
     }
+    if (tid == 0) bulk_wait_read();   // the Yp copies have left ODZS (rewritten next)
     commit_wait(cx);
     {
       float t[16], spv[16];
@@ -516,7 +617,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       ld_h8(sm + OSP, RGS, row, cb, spv);
       ld_h8(sm + OSP, RGS, row, cb + 8, spv + 8);
       tc::tmem_ld_wait();
-      const float csr = vec[V_CS + row], cwr = vec[V_CW + row];
+      const float csr = vb[V_CS + row], cwr = vb[V_CW + row];
       float t0[16], t1[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -534,13 +635,13 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 4: Zq += M1 dz; state corrections
     if (tid == 0 && cx.ok) {
-      mma64(tb + C_ZQ, sm + OM1, 0, RGS, sm + ODZ, 1, RGS, 64, 64, true);
-      mma64(tb + C_ST1, sm + OX, 1, RGS, sm + ODZS, 1, RGS2, 128, 64, false);   // X^T [cs dz | cw dz]
+      mma64(tb + C_ZQ, sm + OM, 0, RGS, sm + ODZ, 1, RGS, 64, 64, true);
+      mma64(tb + C_ST1, oxc, 1, RGS, sm + ODZS, 1, RGS2, 128, 64, false);    // X^T [cs dz | cw dz]
       mma64(tb + C_ST2, sm + OA, 1, RGS, sm + ODYS, 1, RGS2, 128, 64, false);   // A^T [cs dy | cw dy]
     }
     commit_wait(cx);
     {
-      const float Bt = vec[V_BP + row], Dt = vec[V_DP + row];
+      const float Bt = vb[V_BP + row], Dt = vb[V_DP + row];
       float zq[16];
       tc::tmem_ld16_x2(tb + lb + C_ZQ, zq);
       tc::tmem_ld_wait();
@@ -553,19 +654,21 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       }
       st_h8(sm + OAQ, RGS, row, cb, aq);
       st_h8(sm + OAQ, RGS, row, cb + 8, aq + 8);
-      st_h8(sm + OAQB, RGS, row, cb, ab);
-      st_h8(sm + OAQB, RGS, row, cb + 8, ab + 8);
-      st_h8(sm + OAQD, RGS, row, cb, ad);
-      st_h8(sm + OAQD, RGS, row, cb + 8, ad + 8);
+      st_h8(sm + ORB, RGS, row, cb, ab);
+      st_h8(sm + ORB, RGS, row, cb + 8, ab + 8);
+      st_h8(sm + ORD, RGS, row, cb, ad);
+      st_h8(sm + ORD, RGS, row, cb + 8, ad + 8);
     }
     // W1, S1 are no longer read by this chunk's products
-    state_update(C_ST1, S_W1, S_S1, OW1, OS1);
+    state_update(vb, C_ST1, S_W1, S_S1, OW1, OS1);
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 5: G2, Yq state terms
+    // and the next chunk's Z = X' W1q (W1 is final for this chunk)
     if (tid == 0 && cx.ok) {
       mma64(tb + C_G2, sm + OAQ, 0, RGS, sm + OA, 0, RGS, 64, 64, false);
-      mma64(tb + C_YQ, sm + OAQB, 0, RGS, sm + OW2, 1, RGS, 64, 64, false);
-      mma64(tb + C_YQ, sm + OAQD, 0, RGS, sm + OS2, 1, RGS, 64, 64, true);
+      mma64(tb + C_YQ, sm + ORB, 0, RGS, sm + OW2, 1, RGS, 64, 64, false);
+      mma64(tb + C_YQ, sm + ORD, 0, RGS, sm + OS2, 1, RGS, 64, 64, true);
+      if (has_next) mma64(tb + C_Z, sm + (b ? OX0 : OX1), 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
     }
     commit_wait(cx);
     {
@@ -574,33 +677,35 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       tc::tmem_ld_wait();
 #pragma unroll
       for (int i = 0; i < 16; i += 4) {
-        const float4 c4 = *reinterpret_cast<const float4*>(cwm + swz(row, cb + i));
+        const float4 c4 = *reinterpret_cast<const float4*>(cwc + swz(row, cb + i));
         m2[i] = -c4.x * g[i]; m2[i + 1] = -c4.y * g[i + 1]; m2[i + 2] = -c4.z * g[i + 2]; m2[i + 3] = -c4.w * g[i + 3];
       }
-      st_h8(sm + OM2, RGS, row, cb, m2);
-      st_h8(sm + OM2, RGS, row, cb + 8, m2 + 8);
+      st_h8(sm + OM, RGS, row, cb, m2);
+      st_h8(sm + OM, RGS, row, cb + 8, m2 + 8);
     }
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 6: Yq += M2 dy
-    if (tid == 0 && cx.ok) mma64(tb + C_YQ, sm + OM2, 0, RGS, sm + ODY, 1, RGS, 64, 64, true);
+    if (tid == 0 && cx.ok) mma64(tb + C_YQ, sm + OM, 0, RGS, sm + ODY, 1, RGS, 64, 64, true);
     // W2, S2 are no longer read by this chunk's products (overlaps the last one)
-    state_update(C_ST2, S_W2, S_S2, OW2, OS2);
+    state_update(vb, C_ST2, S_W2, S_S2, OW2, OS2);
+    // the next chunk's (B R), (D R): this chunk's B aq, D aq products are done
+    if (has_next) brdr(b ^ 1);
     commit_wait(cx);
-    {
-      float yq[16];
-      tc::tmem_ld16_x2(tb + lb + C_YQ, yq);
-      tc::tmem_ld_wait();
-      const uint32_t dst =
-          mapa(red_local + (uint32_t)(F32T + ((qr * 16 + (row & 15)) * 64 + cb) * 4), (uint32_t)(row >> 4));
+    stage_slices(C_YQ, F32T);
+    if (tid == 0 && cx.ok) send_slices(F32T, 2);
 #pragma unroll
-      for (int i = 0; i < 16; i += 4) st_cluster4(dst + 4 * i, make_float4(yq[i], yq[i + 1], yq[i + 2], yq[i + 3]));
+    for (int i = 0; i < 4; ++i) {
+      qprev[i] = qcur[i];
+      xkd[i] = xkn[i];
+      vvd[i] = vvn[i];
+      qcur[i] = qnx[i];
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) qprev[i] = qcur[i];
-    __syncthreads();
+    sync_smem_for_mma();
   }
   // the last chunk's y
-  cluster_sync();
+  xwait(2, ((T / TOK) - 1) & 1);
+  if (tid == 0) bulk_wait_all();   // every copy this CTA issued has landed
+  __syncthreads();
   y_rows(y, reinterpret_cast<const float*>(sm + RED + F32T), qprev, u, T, T - TOK, qr);
 
   // ---- state slices out
