@@ -365,16 +365,20 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
 // Matrices with a short side of 128 and a long side of 512 (the 128 -> 512
 // -> 128 MLP memory).  X in split bf16 (256 KB) does not fit one SM, so a
 // cluster of two CTAs shares each task: CTA p holds columns [256 p, 256 p +
-// 256) of X.  X X^T = sum of the two halves' Gram matrices: each CTA writes
-// its partial (fp32) into the partner's A/B' buffer over DSMEM between two
-// cluster barriers, and each adds the partner's.  A^2 and B' are formed
+// 256) of X.  X X^T = sum of the two halves' Gram matrices.  Each partial is
+// symmetric, so a CTA sends the partner only rows 0-63 (32 KB fp32) and the
+// lower-right 64 x 64 block (16 KB): two bulk DSMEM copies that complete on
+// the partner's mbarrier.  The receiver reads block (1, 0) of the partner's
+// partial as the transpose of block (0, 1).  A^2 and B' are formed
 // redundantly by both; X <- B' X splits by columns with no exchange.
 namespace {
 
 constexpr int R2 = 128, NH = 256, NT2 = 256;
 constexpr int OPR2 = 131072;                    // factors (120 KB) / X hi+lo (128 KB)
-constexpr int AB2 = 65536;                      // A / B' hi+lo
-constexpr int SMEM2 = OPR2 + AB2;
+constexpr int AB2 = 65536;                      // A / B' hi+lo; receives the partner's partial
+constexpr int STG2 = OPR2 + AB2;                // 32 KB staging of this CTA's rows 0-63
+constexpr int SMEM2 = STG2 + 32768;
+constexpr uint32_t kPartBytes = 64 * R2 * 4 + 64 * 64 * 4;   // rows 0-63 + block (1, 1)
 
 __device__ __forceinline__ uint32_t cluster_rank2() {
   uint32_t r;
@@ -393,6 +397,29 @@ __device__ __forceinline__ uint32_t mapa2(uint32_t saddr, uint32_t cta) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(cta));
   return r;
+}
+// bulk copy of local shared memory into the partner's, completing on the
+// partner's mbarrier (cluster addresses for dst and mbar)
+__device__ __forceinline__ void bulk_to_partner(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(src), "r"(bytes), "r"(mbar)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read2() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all2() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arm_tx2(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+// fp32 row-major exchange blocks with the 16-byte chunks of row r XOR-ed by
+// r % 8: a warp touching one chunk of 32 consecutive rows hits every bank
+// (unswizzled, rows 512 or 256 bytes apart all start in the same bank)
+__device__ __forceinline__ int xswz128(int r, int c) { return r * 128 + ((((c >> 2) ^ (r & 7)) << 2) | (c & 3)); }
+__device__ __forceinline__ int xswz64(int r, int c) { return r * 64 + ((((c >> 2) ^ (r & 7)) << 2) | (c & 3)); }
+// one arrival on the partner's mbarrier (cluster address)
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 struct PairCtx {
@@ -430,13 +457,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
   const uint32_t lane_base = (uint32_t)(32 * sp) << 16;
   const int n = 2 * NH;                             // long side of X
 
+  __shared__ uint64_t xdata, xfree;   // partner's partial arrived / partner ready to receive
   if (warp == 0) tc::tmem_alloc(&tbase, 512);
-  if (threadIdx.x == 0) tc::mbar_init(&bar, 1);
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::mbar_init(&xdata, 1);
+    tc::mbar_init(&xfree, 1);
+    mbar_arm_tx2(&xdata, kPartBytes);   // exchange 0
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  cluster_sync2();   // both CTAs' exchange barriers are initialised
   const uint32_t tA = tbase, tA2 = tbase + 128, tX = tbase + 256;
   PairCtx cx{&bar, 0u, true};
+  uint32_t xe = 0;   // exchanges so far (phase parity of xdata and xfree)
+  float* stg = reinterpret_cast<float*>(sm + STG2);                 // [64][128] fp32
+  float* recv = reinterpret_cast<float*>(sm + OPR2);                // partner's rows 0-63, then block (1, 1)
+  float* stg11 = reinterpret_cast<float*>(sm + OPR2 + kPartBytes);  // this CTA's block (1, 1) [64][64]
 
   const int lxb = R2 * Kp * 2, rxb = Kp * NH * 2;
   uint8_t* lx_hi = sm;
@@ -571,27 +609,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
       tc::tmem_ld16(tA + lane_base + 64 * half + 32, af + 32);
       tc::tmem_ld16(tA + lane_base + 64 * half + 48, af + 48);
       tc::tmem_ld_wait();
-      // exchange through the partner's A/B' buffer (free now: both CTAs are
-      // past their B'X product), as fp32 [row][col]
-      cluster_sync2();
-      {
-        const uint32_t dst = mapa2(tc::smem_u32(sm + OPR2) + (uint32_t)((row * R2 + 64 * half) * 4), p ^ 1u);
+      // exchange: this CTA's A/B' buffer is free (its B'X product is done);
+      // tell the partner, and wait until the partner's is free too
+      bool good = true;
+      if (threadIdx.x == 0 && cx.ok) {
+        mbar_arrive_remote(mapa2(tc::smem_u32(&xfree), p ^ 1u));
+        good = tc::mbar_wait(&xfree, xe & 1, kWaitCycles);
+      }
+      // stage rows 0-63 and block (1, 1) of this CTA's partial
+      if (row < 64) {
 #pragma unroll
         for (int q4 = 0; q4 < 16; ++q4)
-          asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16 * q4), "f"(af[4 * q4]),
-                       "f"(af[4 * q4 + 1]), "f"(af[4 * q4 + 2]), "f"(af[4 * q4 + 3])
-                       : "memory");
-      }
-      cluster_sync2();
-      {
-        const float* theirs = reinterpret_cast<const float*>(sm + OPR2) + row * R2 + 64 * half;
+          *reinterpret_cast<float4*>(stg + xswz128(row, 64 * half + 4 * q4)) =
+              make_float4(af[4 * q4], af[4 * q4 + 1], af[4 * q4 + 2], af[4 * q4 + 3]);
+      } else if (half == 1) {
 #pragma unroll
-        for (int q4 = 0; q4 < 16; ++q4) {
-          const float4 o = *reinterpret_cast<const float4*>(theirs + 4 * q4);
-          af[4 * q4] += o.x; af[4 * q4 + 1] += o.y; af[4 * q4 + 2] += o.z; af[4 * q4 + 3] += o.w;
+        for (int q4 = 0; q4 < 16; ++q4)
+          *reinterpret_cast<float4*>(stg11 + xswz64(row - 64, 4 * q4)) =
+              make_float4(af[4 * q4], af[4 * q4 + 1], af[4 * q4 + 2], af[4 * q4 + 3]);
+      }
+      tc::fence_smem_to_async();   // staging is the bulk copies' source
+      if (__syncthreads_or(!good)) cx.ok = false;
+      good = true;
+      if (threadIdx.x == 0 && cx.ok) {
+        const uint32_t xb = mapa2(tc::smem_u32(&xdata), p ^ 1u);
+        const uint32_t rv = tc::smem_u32(recv);
+        bulk_to_partner(mapa2(rv, p ^ 1u), tc::smem_u32(stg), 64 * R2 * 4, xb);
+        bulk_to_partner(mapa2(rv + 64 * R2 * 4, p ^ 1u), tc::smem_u32(stg11), 64 * 64 * 4, xb);
+        good = tc::mbar_wait(&xdata, xe & 1, kWaitCycles);
+        if (good) mbar_arm_tx2(&xdata, kPartBytes);   // the next exchange
+        bulk_wait_read2();   // staging read: the buffer below may be rewritten
+      }
+      ++xe;
+      if (__syncthreads_or(!good)) cx.ok = false;
+      {
+        // partner's entries of my row, columns [64 half, 64 half + 64)
+        if (row < 64) {
+#pragma unroll
+          for (int q4 = 0; q4 < 16; ++q4) {
+            const float4 o = *reinterpret_cast<const float4*>(recv + xswz128(row, 64 * half + 4 * q4));
+            af[4 * q4] += o.x; af[4 * q4 + 1] += o.y; af[4 * q4 + 2] += o.z; af[4 * q4 + 3] += o.w;
+          }
+        } else if (half == 1) {
+          const float* th = recv + 64 * R2;
+#pragma unroll
+          for (int q4 = 0; q4 < 16; ++q4) {
+            const float4 o = *reinterpret_cast<const float4*>(th + xswz64(row - 64, 4 * q4));
+            af[4 * q4] += o.x; af[4 * q4 + 1] += o.y; af[4 * q4 + 2] += o.z; af[4 * q4 + 3] += o.w;
+          }
+        } else {
+          // block (1, 0): the partner's P[row][c] = P[c][row], c < 64
+#pragma unroll
+          for (int c = 0; c < 64; ++c) af[c] += recv[xswz128(c, row)];
         }
       }
-      __syncthreads();   // every partial read before the buffer takes A hi/lo
+      __syncthreads();   // every received entry read before the buffer takes A hi/lo
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) store_split16(a_hi, a_lo, tc::core_offset(row, 64 * half + 8 * q8, rgsR), af + 8 * q8);
       sync_for_mma();
@@ -631,6 +703,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
       sync_for_mma();
     }
   }
+  if (threadIdx.x == 0) bulk_wait_all2();
   if (!cx.ok && threadIdx.x == 0) atomicExch(w.status, ATLAS_ERR_TIMEOUT);
   tc::fence_before_sync();
   __syncthreads();
