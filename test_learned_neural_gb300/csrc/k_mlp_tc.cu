@@ -75,6 +75,9 @@ constexpr uint32_t C_G2 = 64, C_YQ = 128;   // reuse after Yp, G1 are consumed
 constexpr uint32_t S_W1 = 0, S_S1 = 64, S_W2 = 128, S_S2 = 192;
 
 __device__ __forceinline__ int swz(int r, int c) { return r * 64 + (c ^ ((r & 7) << 2)); }
+// slot rows of 64 fp32 (16 rows per sender) use the same chunk swizzle:
+// 16 threads writing one column chunk of 16 rows spread over all banks
+__device__ __forceinline__ int slot_idx(int sender, int r16, int c) { return sender * 1024 + swz(r16, c); }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -241,7 +244,7 @@ __device__ __forceinline__ void y_rows(float* y, const float* slots, const float
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int p = 0; p < CS; ++p) {
-    const float4 t4 = *reinterpret_cast<const float4*>(slots + (p * 16 + rl) * 64 + cc);
+    const float4 t4 = *reinterpret_cast<const float4*>(slots + slot_idx(p, rl, cc));
     acc.x += t4.x; acc.y += t4.y; acc.z += t4.z; acc.w += t4.w;
   }
   const size_t gb = ((size_t)u * T + s + 16 * (int)qr + rl) * D + cc;
@@ -343,11 +346,13 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     tc::tmem_ld16_x2(tb + lb + col, v16);
     tc::tmem_ld_wait();
     const int owner = row >> 4;
-    float* dst = owner == (int)qr ? reinterpret_cast<float*>(sm + RED + slot_off) + (qr * 16 + (row & 15)) * 64 + cb
-                                  : reinterpret_cast<float*>(sm + ODZS) + (owner * 16 + (row & 15)) * 64 + cb;
+    // my own quarter: my slot [qr] (= [owner]); the others: staging block [owner]
+    float* base = owner == (int)qr ? reinterpret_cast<float*>(sm + RED + slot_off)
+                                   : reinterpret_cast<float*>(sm + ODZS);
 #pragma unroll
     for (int i = 0; i < 16; i += 4)
-      *reinterpret_cast<float4*>(dst + i) = make_float4(v16[i], v16[i + 1], v16[i + 2], v16[i + 3]);
+      *reinterpret_cast<float4*>(base + slot_idx(owner, row & 15, cb + i)) =
+          make_float4(v16[i], v16[i + 1], v16[i + 2], v16[i + 3]);
     tc::fence_smem_to_async();   // staging is the bulk copies' source
     __syncthreads();
   };
@@ -562,7 +567,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int p = 0; p < CS; ++p) {
-        const float4 t4 = *reinterpret_cast<const float4*>(red + (p * 16 + rl) * 64 + cc);
+        const float4 t4 = *reinterpret_cast<const float4*>(red + slot_idx(p, rl, cc));
         acc.x += t4.x; acc.y += t4.y; acc.z += t4.z; acc.w += t4.w;
       }
       const float g2 = 2.f * vb[V_GA + r];
