@@ -43,6 +43,7 @@ struct NsSmem {
   int x;          // X hi, X lo (X lo directly after X hi: read together as one 128-row operand)
   int a;          // A, then B' (hi, lo; likewise adjacent)
   int qt;         // fp32 transpose buffer [64][65]
+  int lf;         // window factor on the short side, fp32 [Kp][64], unscaled (kept like rx)
   int total;
 };
 
@@ -53,7 +54,8 @@ __host__ __device__ inline NsSmem ns_smem_layout(int n, int Kp) {
   s.x = s.lx + 2 * R * Kp * 2;
   s.a = s.x + 2 * R * n * 2;
   s.qt = s.a + 2 * R * R * 2;
-  s.total = s.qt + R * (R + 1) * 4;
+  s.lf = s.qt + R * (R + 1) * 4;
+  s.total = s.lf + Kp * R * 4;
   return s;
 }
 
@@ -171,6 +173,11 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
   uint8_t* a_hi = sm + L.a;
   uint8_t* a_lo = sm + L.a + R * R * 2;
   float* qt = reinterpret_cast<float*>(sm + L.qt);
+  float* lfs = reinterpret_cast<float*>(sm + L.lf);
+  // the chunk-start momentum S-bar of the current (unit, matrix), fp32, in
+  // TMEM lanes 16-31 (the M = 64 accumulators use lanes 0-15), same row and
+  // column layout as tX
+  const uint32_t lane_sbar = (uint32_t)(32 * sp + 16) << 16;
   const int rgsKp = (Kp / 8) * 128, rgsN = (n / 8) * 128, rgsR = (R / 8) * 128;
   const int c = 32 * half + csub;           // this thread's 16 columns of a 64-wide accumulator
 
@@ -207,9 +214,22 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
     const size_t nel = (size_t)rows * cols;
     const float* Sb = w.Sst[buf][m] + (size_t)u * nel;   // X orientation [R][n]
 
-    // (a) long-side factor once per (unit, matrix): MN-major B operand [Kp][n]
+    // (a) per (unit, matrix): long-side factor (MN-major B operand [Kp][n],
+    // split bf16), short-side factor (fp32) and S-bar (TMEM)
     if (loaded != u * g.nmat + m) {
       loaded = u * g.nmat + m;
+      for (int e = threadIdx.x; e < Kp * R; e += NT) {
+        const int i = e / R, a = e % R;
+        lfs[e] = i < ch.nw ? Lf[(size_t)i * lstride + a] : 0.f;
+      }
+      for (int c32 = 32 * half; c32 < n; c32 += 64) {
+        const float* sb = Sb + (size_t)row * n + c32 + csub;
+        float v[16];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) *reinterpret_cast<float4*>(v + 4 * q4) = *reinterpret_cast<const float4*>(sb + 4 * q4);
+        tc::tmem_st16_x2(tA + lane_sbar + c32, v);
+      }
+      tc::tmem_st_wait();
       for (int e = threadIdx.x; e < Kp * (n / 8); e += NT) {
         const int i = e / (n / 8), b0 = (e % (n / 8)) * 8;
         float v[8];
@@ -223,13 +243,14 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
         }
         store_split16(rx_hi, rx_lo, tc::core_offset(i, b0, rgsN), v);
       }
+      __syncthreads();   // the fp32 short-side factor is read by other threads below
     }
     // short-side factor scaled by this token's coefficients: K-major A operand [R][Kp]
     for (int e = threadIdx.x; e < R * (Kp / 8); e += NT) {
       const int a = e % R, i0 = (e / R) * 8;
       float v[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) v[q] = (i0 + q < ch.nw) ? cs[i0 + q] * Lf[(size_t)(i0 + q) * lstride + a] : 0.f;
+      for (int q = 0; q < 8; ++q) v[q] = (i0 + q < ch.nw) ? cs[i0 + q] * lfs[(i0 + q) * R + a] : 0.f;
       store_split16(lx_hi, lx_lo, tc::core_offset(a, i0, rgsKp), v);
     }
     sync_for_mma();
@@ -244,18 +265,16 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
     const bool last_tok = (t == ch.e - 1);
     float* So = w.Sst[buf ^ 1][m] + (size_t)u * nel;
     for (int c32 = 32 * half; c32 < n; c32 += 64) {
-      float d[16];
+      float d[16], sv[16];
       tc::tmem_ld16_x2(tX + lane_base + c32, d);
-      const float* sb = Sb + (size_t)row * n + c32 + csub;
-      float4 s4[4];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) s4[q4] = *reinterpret_cast<const float4*>(sb + 4 * q4);
+      tc::tmem_ld16_x2(tA + lane_sbar + c32, sv);
       tc::tmem_ld_wait();
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         float* o = d + 4 * q4;
-        o[0] = At * s4[q4].x - o[0]; o[1] = At * s4[q4].y - o[1];
-        o[2] = At * s4[q4].z - o[2]; o[3] = At * s4[q4].w - o[3];
+        const float* sbv = sv + 4 * q4;
+        o[0] = At * sbv[0] - o[0]; o[1] = At * sbv[1] - o[1];
+        o[2] = At * sbv[2] - o[2]; o[3] = At * sbv[3] - o[3];
         ss += o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
         if (last_tok) *reinterpret_cast<float4*>(So + (size_t)row * n + c32 + csub + 4 * q4) = make_float4(o[0], o[1], o[2], o[3]);
       }
@@ -745,7 +764,7 @@ int ns_tc_kind(const Geom& g) {
     kind = k;
     n0 = l;
   }
-  if (kind == 1 && ns_smem_layout(n0, Kp).total > 200 * 1024) return 0;
+  if (kind == 1 && ns_smem_layout(n0, Kp).total > 226 * 1024) return 0;
   return kind;
 }
 
