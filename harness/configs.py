@@ -35,6 +35,7 @@ class Workload:
     use_gamma: bool = False       # per-token Omega weights drawn, else all ones
     alpha_mu: float = -4.0        # mean of the normal under the decay sigmoid
     w0_init: str = "zero"         # "zero" or "xavier" (per head, shared over B)
+    readout: str = "post"         # "post": y_t from the memory after token t's update; "pre": before it
 
     @property
     def units(self) -> int:

@@ -143,6 +143,12 @@ def forward_unit(cfg, k, q, v, theta, eta, alpha, gamma, W0, S0, P=None,
     Returns y [T, d_v], W_T, S_T (lists) and the outgoing cache
     (the last min(c-1, cached + T) raw keys, values and weights)."""
     depth, C, c = cfg.depth, cfg.C, cfg.c
+    # Read-out: "post" (default) reads token t with the memory after its own
+    # update, as the atlas-torch implementation does (atlas-torch README,
+    # "Known deviations from the paper's MAC"); "pre" reads it with the
+    # memory before the update, h_t = M*_{t-1}(q_t) (titans-pytorch-mlx
+    # README, MAC, Eq. 21).  The state itself is the same in both modes.
+    pre = getattr(cfg, "readout", "post") == "pre"
     k = np.asarray(k, np.float64)
     q = np.asarray(q, np.float64)
     v = np.asarray(v, np.float64)
@@ -179,8 +185,11 @@ def forward_unit(cfg, k, q, v, theta, eta, alpha, gamma, W0, S0, P=None,
             g_t = [wg[first:last].sum(axis=0) for wg in weighted]
             S = [eta[t] * Sm - theta[t] * gm for Sm, gm in zip(S, g_t)]
             U = [newton_schulz(Sm, cfg.ns_iters) for Sm in S] if cfg.ns_iters else S
+            if pre:   # read-out with the memory before token t's update
+                y[t] = memory_apply(W, R[t:t + 1], depth)[0]
             W = [(1.0 - alpha[t]) * Wm + Um for Wm, Um in zip(W, U)]
-            y[t] = memory_apply(W, R[t:t + 1], depth)[0]
+            if not pre:
+                y[t] = memory_apply(W, R[t:t + 1], depth)[0]
     keep = min(c - 1, n_prev + T)
     cache = (K_all[len(K_all) - keep:], V_all[len(V_all) - keep:], G_all[len(G_all) - keep:])
     return y, W, S, cache

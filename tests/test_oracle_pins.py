@@ -26,6 +26,7 @@ class Cfg:
     c: int = 1
     p: int = 1
     ns_iters: int = 0
+    readout: str = "post"
 
 
 def _rand_case(rng, depth, d_k, d_v, hidden, T, p=1, proj=0, gamma=True, scale_w=0.3):
@@ -358,3 +359,42 @@ def test_bruteforce_with_window_cache():
     yb, Wb, Sb = bf.forward(2, 4, 3, 1, 0, case["k"], case["q"], case["v"], case["theta"], case["eta"],
                             case["alpha"], case["gamma"], case["W0"], case["S0"], prev=cache)
     np.testing.assert_allclose(y, yb, rtol=1e-11, atol=1e-12)
+
+
+# ---- pre-update read-out (titans-pytorch-mlx README, MAC, Eq. 21:
+# h_t = M*_{t-1}(q_t)); the default reads the post-update state
+# (atlas-torch README, "Known deviations from the paper's MAC")
+
+PRE_CASES = [
+    (1, 4, 1, 1, 0, 0, 3, 2, 0, 9),       # linear delta rule, several chunks
+    (2, 3, 2, 1, 0, 0, 3, 3, 4, 8),       # MLP, Omega window 2
+    (2, 4, 3, 1, 0, 5, 4, 4, 6, 10),      # Omega + Muon
+    (1, 3, 5, 2, 0, 0, 2, 2, 0, 9),       # polynomial features, window longer than a chunk
+]
+
+
+@pytest.mark.parametrize("case_def", PRE_CASES)
+def test_pre_update_readout_matches_bruteforce(case_def):
+    depth, C, c, p, proj, ns, d_k, d_v, hidden, T = case_def
+    rng = np.random.default_rng(sum(case_def) * 7919 + 1)
+    case = _rand_case(rng, depth, d_k, d_v, hidden, T, p=p, proj=proj)
+    y, W, S, _ = _run_oracle(Cfg(depth=depth, C=C, c=c, p=p, ns_iters=ns, readout="pre"), case)
+    yb, Wb, Sb = bf.forward(depth, C, c, p, ns, case["k"], case["q"], case["v"], case["theta"], case["eta"],
+                            case["alpha"], case["gamma"], case["W0"], case["S0"], case["P"], pre=True)
+    np.testing.assert_allclose(y, yb, rtol=1e-10, atol=1e-11)
+    for a, b in zip(W + S, Wb + Sb):
+        np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-11)
+
+
+def test_pre_update_readout_changes_only_the_readout():
+    """The two read-out modes write back the same state; the pre-update
+    read-out of the first token is the initial memory applied to q_0, and
+    the two modes' outputs differ elsewhere (the shift is real)."""
+    rng = np.random.default_rng(4242)
+    case = _rand_case(rng, 2, 3, 3, 5, T=8)
+    y_post, W_post, S_post, _ = _run_oracle(Cfg(depth=2, C=4, c=2), case)
+    y_pre, W_pre, S_pre, _ = _run_oracle(Cfg(depth=2, C=4, c=2, readout="pre"), case)
+    for a, b in zip(W_post + S_post, W_pre + S_pre):
+        np.testing.assert_array_equal(a, b)
+    np.testing.assert_allclose(y_pre[0], bf.apply_mem(case["W0"], case["q"][0], 2), rtol=1e-13, atol=1e-14)
+    assert np.abs(y_pre[1:] - y_post[1:]).max() > 1e-6
