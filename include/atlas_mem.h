@@ -50,6 +50,10 @@ extern "C" {
 #define ATLAS_F32 0
 #define ATLAS_BF16 1
 
+/* read-out modes (atlas_mem_config.readout) */
+#define ATLAS_READOUT_POST 0
+#define ATLAS_READOUT_PRE 1
+
 typedef struct {
     int depth;      /* 1 (matrix memory) or 2 (residual SiLU MLP) */
     int d_k;        /* key/query width before the feature map */
@@ -61,6 +65,11 @@ typedef struct {
     int proj_dim;   /* 0: no projection; else features are x P, P [poly_dim, proj_dim] */
     int ns_iters;   /* Newton-Schulz steps applied to the momentum, 0 = off */
     int qkv_dtype;  /* ATLAS_F32 or ATLAS_BF16 (q, k, v, P, window cache) */
+    int readout;    /* ATLAS_READOUT_POST: y_t = M_t(q_t), the memory after token t's
+                     * update (atlas-torch README, "Known deviations from the
+                     * paper's MAC"); ATLAS_READOUT_PRE: y_t = M_{t-1}(q_t), the
+                     * memory before it (titans-pytorch-mlx README, MAC, Eq. 21).
+                     * The state written back is the same either way. */
 } atlas_mem_config;
 
 typedef struct atlas_mem_handle atlas_mem_handle;

@@ -25,6 +25,7 @@ struct Geom {
   int L;          // key rows per unit = n_prev + T
   int Kw;         // max window rows of one chunk = C + c - 1
   int rows[2], cols[2], nmat;
+  int readout;    // ATLAS_READOUT_POST / ATLAS_READOUT_PRE
 };
 
 // Per-chunk indices: the chunk covers tokens [s, e) of the call; its Omega

@@ -61,12 +61,15 @@ static int derive_geom(const atlas_mem_config& c, Geom* g, char* why, size_t why
   if (c.proj_dim < 0) BAD("proj_dim must be >= 0");
   if (c.ns_iters < 0) BAD("ns_iters must be >= 0");
   if (c.qkv_dtype != ATLAS_F32 && c.qkv_dtype != ATLAS_BF16) BAD("qkv_dtype must be ATLAS_F32 or ATLAS_BF16");
+  if (c.readout != ATLAS_READOUT_POST && c.readout != ATLAS_READOUT_PRE)
+    BAD("readout must be ATLAS_READOUT_POST or ATLAS_READOUT_PRE");
   long long poly = c.p == 1 ? c.d_k : 1 + c.d_k + choose2(c.d_k + 1);
   long long F = c.proj_dim ? c.proj_dim : poly;
   if (c.depth == 2 && F != c.d_v) BAD("depth 2 (residual memory) needs feature width %lld == d_v %d", F, c.d_v);
   g->depth = c.depth; g->d_k = c.d_k; g->d_v = c.d_v; g->hidden = c.depth == 2 ? c.hidden : 0;
   g->C = c.C; g->c = c.c; g->p = c.p; g->proj_dim = c.proj_dim; g->ns_iters = c.ns_iters;
   g->qkv_dtype = c.qkv_dtype;
+  g->readout = c.readout;
   g->Kw = c.C + c.c - 1;
   if (c.depth == 1) {
     g->nmat = 1; g->rows[0] = (int)F; g->cols[0] = c.d_v;

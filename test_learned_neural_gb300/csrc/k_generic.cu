@@ -184,9 +184,12 @@ __global__ void k_dual_readout(Geom g, Chunk ch, Work w, int buf, float* y) {
   float* cw = gm + g.Kw;           // nw
   const float* rq = w.R + ((size_t)u * g.T + t) * g.F;
   for (int f = threadIdx.x; f < g.F; f += blockDim.x) rs[f] = rq[f];
-  for (int i = threadIdx.x; i < ch.nw; i += blockDim.x) cw[i] = w.Cw[((size_t)u * g.C + r) * g.Kw + i];
+  // read-out coefficients: token r's own, or in pre-update mode token
+  // r - 1's (the chunk-start state for r = 0: Cw = 0, B = 1, D = 0)
+  const int rr = g.readout == ATLAS_READOUT_PRE ? r - 1 : r;
+  for (int i = threadIdx.x; i < ch.nw; i += blockDim.x) cw[i] = rr < 0 ? 0.f : w.Cw[((size_t)u * g.C + rr) * g.Kw + i];
   __syncthreads();
-  const float Bt = w.Bp[(size_t)u * g.C + r], Dt = w.Dp[(size_t)u * g.C + r];
+  const float Bt = rr < 0 ? 1.f : w.Bp[(size_t)u * g.C + rr], Dt = rr < 0 ? 0.f : w.Dp[(size_t)u * g.C + rr];
   const float* Xw = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * g.F;
   for (int i = threadIdx.x; i < ch.nw; i += blockDim.x) {
     float acc = 0.f;
@@ -409,8 +412,9 @@ __global__ void __launch_bounds__(256) k_ns_simt(Geom g, Chunk ch, Work w, int b
   }
 }
 
-// Decay scan over the chunk, in place: slot t holds U_t on entry and W_t on
-// exit (W_{s-1} = Wbar).  One thread per matrix element (X orientation).
+// Decay scan over the chunk, in place: slot t holds U_t on entry and the
+// weights token t reads out on exit: W_t, or W_{t-1} in pre-update mode
+// (W_{s-1} = Wbar).  One thread per matrix element (X orientation).
 __global__ void k_ns_wscan(Geom g, Chunk ch, Work w, int buf, int m, size_t slot_stride, size_t slot_off,
                            const float* alpha) {
   const int u = blockIdx.y;
@@ -422,10 +426,12 @@ __global__ void k_ns_wscan(Geom g, Chunk ch, Work w, int buf, int m, size_t slot
   const int a = (int)(e / cols), b = (int)(e % cols);
   const size_t xe = tall ? (size_t)b * rows + a : e;
   float W = w.Wst[buf][m][(size_t)u * n + e];
+  const bool pre = g.readout == ATLAS_READOUT_PRE;
   for (int t = ch.s; t < ch.e; ++t) {
     float* slot = w.Ubuf + ((size_t)u * g.C + (t - ch.s)) * slot_stride + slot_off;
+    const float W_prev = W;
     W = (1.f - alpha[(size_t)u * g.T + t]) * W + slot[xe];
-    slot[xe] = W;
+    slot[xe] = pre ? W_prev : W;   // the weights token t reads out
   }
   w.Wst[buf ^ 1][m][(size_t)u * n + e] = W;
 }
@@ -664,6 +670,7 @@ __global__ void __launch_bounds__(256) k_ns_scan_w1(Geom g, Chunk ch, Work w, in
   const int lane = threadIdx.x % 32, grp = threadIdx.x / 32;
   const int F = g.F, h = g.hidden, j = jb + lane, i0 = grp * RPG;
   const int Ct = ch.e - ch.s;
+  const bool pre = g.readout == ATLAS_READOUT_PRE;   // read out before token r's update
   // queries of the chunk
   for (int e = threadIdx.x; e < Ct * F; e += 256) rq[e / F][e % F] = w.R[((size_t)u * g.T + ch.s + e / F) * F + e % F];
   float W[RPG];
@@ -688,8 +695,9 @@ __global__ void __launch_bounds__(256) k_ns_scan_w1(Geom g, Chunk ch, Work w, in
     float z = 0.f;
 #pragma unroll
     for (int q = 0; q < RPG; ++q) {
+      if (pre) z += rq[r][i0 + q] * W[q];
       W[q] = be * W[q] + cur[q];
-      z += rq[r][i0 + q] * W[q];
+      if (!pre) z += rq[r][i0 + q] * W[q];
     }
     part[grp][lane] = z;
     __syncthreads();
@@ -717,6 +725,7 @@ __global__ void __launch_bounds__(256) k_ns_scan_w2(Geom g, Chunk ch, Work w, in
   const int lane = threadIdx.x % 32, k = blockIdx.x * 8 + threadIdx.x / 32;
   const int F = g.F, h = g.hidden, d = g.d_v, j0 = lane * CPL;
   const int Ct = ch.e - ch.s;
+  const bool pre = g.readout == ATLAS_READOUT_PRE;   // read out before token r's update
   for (int e = threadIdx.x; e < Ct * h; e += 256) aqs[e] = aq[(size_t)u * g.C * h + e];
   float W[CPL];
   const float* Wb = w.Wst[buf][1] + (size_t)u * h * d;   // original orientation [h][d]
@@ -740,8 +749,9 @@ __global__ void __launch_bounds__(256) k_ns_scan_w2(Geom g, Chunk ch, Work w, in
     float acc = 0.f;
 #pragma unroll
     for (int q = 0; q < CPL; ++q) {
+      if (pre) acc += aqs[r * h + j0 + q] * W[q];
       W[q] = be * W[q] + cur[q];
-      acc += aqs[r * h + j0 + q] * W[q];
+      if (!pre) acc += aqs[r * h + j0 + q] * W[q];
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
@@ -1168,7 +1178,9 @@ __host__ __device__ inline Chunk dual1_chunk_at(const Geom& g, int s) {
 }
 
 // per (unit, chunk) coefficient block: Cw [C][Kw], cs_e [Kw], cw_e [Kw],
-// B_t [C], D_t [C], (A_e, B_e, D_e, pad)
+// B_t [C], D_t [C], (A_e, B_e, D_e, pad).  Cw, B_t, D_t are the read-out's
+// (shifted by one token in pre-update mode); cs_e, cw_e, A_e, B_e, D_e the
+// chunk-end state's.
 __host__ __device__ inline size_t dual1_coef_floats(const Geom& g) {
   return (size_t)g.C * g.Kw + 2 * (size_t)g.Kw + 2 * (size_t)g.C + 4;
 }
@@ -1182,6 +1194,9 @@ __global__ void __launch_bounds__(160) k_dual1_coef_all(Geom g, const float* the
                                                          const float* alpha, float* coef) {
   __shared__ float th[64], et[64], be[64];
   const int n = blockIdx.x, u = blockIdx.y;
+  // pre-update read-out: token r reads the state after token r - 1 (the
+  // chunk-start state for r = 0: Cw = 0, B = 1, D = 0)
+  const bool pre = g.readout == ATLAS_READOUT_PRE;
   const Chunk ch = dual1_chunk_at(g, n * g.C);
   const int Ct = g.C;
   for (int r = threadIdx.x; r < Ct; r += blockDim.x) {
@@ -1203,20 +1218,22 @@ __global__ void __launch_bounds__(160) k_dual1_coef_all(Geom g, const float* the
     for (int r = 0; r < Ct; ++r) {
       const int t = ch.s + r;
       const bool in_win = ti <= t && t <= ti + g.c - 1;
+      const float cw_prev = cw;
       cs = et[r] * cs + (in_win ? th[r] : 0.f);
       cw = be[r] * cw + cs;
-      Cw[(size_t)r * g.Kw + i] = cw;
+      Cw[(size_t)r * g.Kw + i] = pre ? cw_prev : cw;   // read-out weights of token r
     }
     cse[i] = cs;
     cwe[i] = cw;
   } else if (threadIdx.x == blockDim.x - 1) {
     float Ap = 1.f, Bp = 1.f, Dp = 0.f;
     for (int r = 0; r < Ct; ++r) {
+      const float Bprev = Bp, Dprev = Dp;
       Ap *= et[r];
       Bp *= be[r];
       Dp = be[r] * Dp + Ap;
-      Bt[r] = Bp;
-      Dt[r] = Dp;
+      Bt[r] = pre ? Bprev : Bp;
+      Dt[r] = pre ? Dprev : Dp;
     }
     ABD[0] = Ap;
     ABD[1] = Bp;

@@ -67,6 +67,9 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory map exceeds a CTA's limit
 // vectors inside VEC
 constexpr int V_TH = 0, V_ET = 64, V_BE = 128, V_GA = 192, V_AP = 256, V_BP = 320, V_DP = 384, V_CS = 448,
               V_CW = 512;
+// B_t, D_t of the read-out: the post-update state's (= V_BP, V_DP) or, in
+// pre-update mode, the previous token's (1, 0 for the chunk's first token)
+constexpr int V_BR = 576, V_DR = 640;
 
 // TMEM columns of the accumulators (lanes 0-15 of each sub-partition)
 constexpr uint32_t C_Z = 0, C_YP = 64, C_G1 = 128, C_ZQ = 192, C_ST1 = 256, C_ST2 = 384;
@@ -275,7 +278,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
                   const float* __restrict__ theta, const float* __restrict__ eta, const float* __restrict__ alpha,
                   const float* __restrict__ gamma, const float* W0a, const float* W0b, const float* S0a,
                   const float* S0b, float* __restrict__ y, float* Woa, float* Wob, float* Soa, float* Sob,
-                  int* status) {
+                  int* status, int pre) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ uint64_t bar;
   __shared__ uint64_t xbar[3];   // arrivals of the peers' Yp slices, dy rows, Yq slices
@@ -416,9 +419,10 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
         }
 #pragma unroll
         for (int qq = 0; qq < 8; ++qq) {
+          const float cw_prev = cw;
           cs = et[qq] * cs + (t0 + qq == i ? th[qq] : 0.f);
           cw = be[qq] * cw + cs;
-          cwp[swz(t0 + qq, i)] = cw;
+          cwp[swz(t0 + qq, i)] = pre ? cw_prev : cw;   // read-out weights of token t0 + qq
         }
       }
       vb[V_CS + i] = cs;
@@ -434,12 +438,15 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
         }
 #pragma unroll
         for (int qq = 0; qq < 8; ++qq) {
+          const float Bprev = Bp, Dprev = Dp;
           Ap *= et[qq];
           Bp *= be[qq];
           Dp = be[qq] * Dp + Ap;
           vb[V_AP + t0 + qq] = Ap;
           vb[V_BP + t0 + qq] = Bp;
           vb[V_DP + t0 + qq] = Dp;
+          vb[V_BR + t0 + qq] = pre ? Bprev : Bp;
+          vb[V_DR + t0 + qq] = pre ? Dprev : Dp;
         }
       }
     }
@@ -449,7 +456,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   auto brdr = [&](int bn) {
     const float* vb = vecb(bn);
     const int r = tid % 64, g = tid / 64;
-    const float Bt = vb[V_BP + r], Dt = vb[V_DP + r];
+    const float Bt = vb[V_BR + r], Dt = vb[V_DR + r];
     for (int j = 0; j < 2; ++j) {
       const int cc = (g + 4 * j) * 8;
       float x[8], b8[8], d8[8];
@@ -646,7 +653,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     }
     commit_wait(cx);
     {
-      const float Bt = vb[V_BP + row], Dt = vb[V_DP + row];
+      const float Bt = vb[V_BR + row], Dt = vb[V_DR + row];
       float zq[16];
       tc::tmem_ld16_x2(tb + lb + C_ZQ, zq);
       tc::tmem_ld_wait();
@@ -747,7 +754,7 @@ cudaError_t mlp_tc_launch(const Geom& g, const void* q, const void* k, const voi
   if (e != cudaSuccess) return e;
   k_mlp_dual_tc<<<g.units * CS, NT, SMEM_BYTES, st>>>(g.T, g.qkv_dtype, q, k, v, theta, eta, alpha, gamma, W0[0],
                                                       W0[1], S0[0], S0[1], y, W_out[0], W_out[1], S_out[0],
-                                                      S_out[1], status);
+                                                      S_out[1], status, g.readout == ATLAS_READOUT_PRE ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -33,6 +33,23 @@ def test_small_parity(gpu_lib, name):
             assert v <= 5 * tol, (k, v)
 
 
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_parity_pre_update_readout(gpu_lib, name):
+    """Read-out with the memory before each token's update (titans-pytorch-mlx
+    README, MAC, Eq. 21) on every path: fused MLP kernel, depth-1 split path,
+    tensor-core Newton-Schulz with its decay scans."""
+    w = (WORKLOADS[name].scaled(**SMALL[name]) if SMALL[name] else WORKLOADS[name]).scaled(readout="pre")
+    errs = compare(w)
+    tol = TOL[w.qkv_dtype]
+    print(name, "pre", {k: f"{v:.2e}" for k, v in errs.items()})
+    assert errs["y"] <= tol
+    for k, v in errs.items():
+        if k.startswith("W"):
+            assert v <= tol, (k, v)
+        if k.startswith("S"):
+            assert v <= 5 * tol, (k, v)
+
+
 @pytest.mark.parametrize("name", ["titans_mlp", "atlas_poly_c16", "atlas_long"])
 def test_split_continuation_matches_whole(gpu_lib, name):
     """Two calls with carried W, S and window cache equal one call."""
