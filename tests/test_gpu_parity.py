@@ -109,3 +109,35 @@ def test_alpha_one_wipes_state_on_gpu(gpu_lib):
     for m in range(2):
         U = oracle.newton_schulz(flat_units(S[m])[0], w.ns_iters)
         assert maxrel(flat_units(g["W"][m])[0], U) < 2e-3
+
+
+@pytest.mark.parametrize("readout", ["post", "pre"])
+def test_streaming_one_token_calls(gpu_lib, readout):
+    """Streaming decode: with one-token chunks (C = 1) a sequence fed one
+    token per call, carrying W, S and the Omega window cache between calls,
+    equals one call over the whole sequence and the oracle."""
+    import torch
+    from test_learned_neural_gb300.runner import Memory, tensors_from_numpy
+    w = WORKLOADS["atlas_poly_c4"].scaled(B=1, H=2, T=12, C=1, readout=readout)
+    inp = make_inputs(w)
+    whole = run_gpu(w, inp)
+    r = oracle.forward(w, inp)
+    assert maxrel(flat_units(whole["y"]), r["y"]) <= TOL[w.qkv_dtype]
+    mem = Memory(w)
+    t = tensors_from_numpy(inp)
+    seq = ("q", "k", "v", "theta", "eta", "alpha", "gamma")
+    W, S, win, ys = t["W0"], t["S0"], None, []
+    for i in range(w.T):
+        step = {k: (v[:, :, i:i + 1].contiguous() if k in seq and v is not None else v) for k, v in t.items()}
+        step["W0"], step["S0"] = W, S
+        o = mem.forward(step, win=win)
+        ys.append(o["y"].cpu().numpy())
+        W, S = o["W"], o["S"]
+        win = (min(w.c - 1, i + 1), o["win_k"], o["win_v"], o["win_gamma"])
+    torch.cuda.synchronize()
+    mem.status()
+    y = np.concatenate(ys, axis=2)
+    assert maxrel(y, whole["y"]) < 1e-5
+    for m in range(len(W)):
+        assert maxrel(W[m].cpu().numpy(), whole["W"][m]) < 1e-5
+    mem.close()
