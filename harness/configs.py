@@ -36,6 +36,7 @@ class Workload:
     alpha_mu: float = -4.0        # mean of the normal under the decay sigmoid
     w0_init: str = "zero"         # "zero" or "xavier" (per head, shared over B)
     readout: str = "post"         # "post": y_t from the memory after token t's update; "pre": before it
+    ns_target: str = "momentum"   # Newton-Schulz on the momentum, or "surprise": on each token's windowed gradient
 
     @property
     def units(self) -> int:

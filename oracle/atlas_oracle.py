@@ -149,6 +149,14 @@ def forward_unit(cfg, k, q, v, theta, eta, alpha, gamma, W0, S0, P=None,
     # memory before the update, h_t = M*_{t-1}(q_t) (titans-pytorch-mlx
     # README, MAC, Eq. 21).  The state itself is the same in both modes.
     pre = getattr(cfg, "readout", "post") == "pre"
+    # Where Newton-Schulz sits (with ns_iters > 0): "momentum" (default)
+    # orthogonalises the applied momentum, U_t = NS(S_t) (ATLAS summary,
+    # Section 5); "surprise" orthogonalises each token's windowed gradient
+    # with the momentum and step size outside it, S_t = eta_t S_{t-1} -
+    # theta_t NS(g_t), W_t = (1 - alpha_t) W_{t-1} + S_t (atlas-torch README:
+    # "orthogonalization of the surprise updates", per-token store path with
+    # "eta outside Newton-Schulz").
+    surprise_ns = bool(cfg.ns_iters) and getattr(cfg, "ns_target", "momentum") == "surprise"
     k = np.asarray(k, np.float64)
     q = np.asarray(q, np.float64)
     v = np.asarray(v, np.float64)
@@ -183,8 +191,13 @@ def forward_unit(cfg, k, q, v, theta, eta, alpha, gamma, W0, S0, P=None,
             first = max(t - c + 1, lo) - lo
             last = t - lo + 1
             g_t = [wg[first:last].sum(axis=0) for wg in weighted]
-            S = [eta[t] * Sm - theta[t] * gm for Sm, gm in zip(S, g_t)]
-            U = [newton_schulz(Sm, cfg.ns_iters) for Sm in S] if cfg.ns_iters else S
+            if surprise_ns:
+                # Newton-Schulz on the windowed surprise, eta and theta outside
+                S = [eta[t] * Sm - theta[t] * newton_schulz(gm, cfg.ns_iters) for Sm, gm in zip(S, g_t)]
+                U = S
+            else:
+                S = [eta[t] * Sm - theta[t] * gm for Sm, gm in zip(S, g_t)]
+                U = [newton_schulz(Sm, cfg.ns_iters) for Sm in S] if cfg.ns_iters else S
             if pre:   # read-out with the memory before token t's update
                 y[t] = memory_apply(W, R[t:t + 1], depth)[0]
             W = [(1.0 - alpha[t]) * Wm + Um for Wm, Um in zip(W, U)]

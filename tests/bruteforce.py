@@ -71,10 +71,11 @@ def apply_mem(W, x, depth):
 
 
 def forward(depth, C, c, p, ns_iters, k, q, v, theta, eta, alpha, gamma, W0, S0,
-            P=None, prev=None, pre=False):
+            P=None, prev=None, pre=False, surprise_ns=False):
     """prev = (keys, values, gammas) of tokens preceding the call, oldest first.
     pre = True reads token t out of the memory before its update (the paper's
-    MAC retrieval, h_t = M*_{t-1}(q_t)); else after it."""
+    MAC retrieval, h_t = M*_{t-1}(q_t)); else after it.  surprise_ns = True
+    orthogonalises each token's windowed gradient instead of the momentum."""
     T = len(k)
     gamma = np.ones(T) if gamma is None else gamma
     pk, pv, pg = ([], [], []) if prev is None else prev
@@ -100,8 +101,12 @@ def forward(depth, C, c, p, ns_iters, k, q, v, theta, eta, alpha, gamma, W0, S0,
                 continue
             gi = autograd_grad(W_bar, feat(keys[i + n_prev]), np.asarray(vals[i + n_prev]), depth)
             g = [a + gams[i + n_prev] * b for a, b in zip(g, gi)]
-        S = [eta[t] * Sm - theta[t] * gm for Sm, gm in zip(S, g)]
-        U = [ns_closed_form(Sm, ns_iters) for Sm in S] if ns_iters else S
+        if surprise_ns and ns_iters:
+            S = [eta[t] * Sm - theta[t] * ns_closed_form(gm, ns_iters) for Sm, gm in zip(S, g)]
+            U = S
+        else:
+            S = [eta[t] * Sm - theta[t] * gm for Sm, gm in zip(S, g)]
+            U = [ns_closed_form(Sm, ns_iters) for Sm in S] if ns_iters else S
         W_before = W
         W = [(1.0 - alpha[t]) * Wm + Um for Wm, Um in zip(W, U)]
         y.append(apply_mem(W_before if pre else W, feat(q[t]), depth))

@@ -27,6 +27,7 @@ class Cfg:
     p: int = 1
     ns_iters: int = 0
     readout: str = "post"
+    ns_target: str = "momentum"
 
 
 def _rand_case(rng, depth, d_k, d_v, hidden, T, p=1, proj=0, gamma=True, scale_w=0.3):
@@ -398,3 +399,51 @@ def test_pre_update_readout_changes_only_the_readout():
         np.testing.assert_array_equal(a, b)
     np.testing.assert_allclose(y_pre[0], bf.apply_mem(case["W0"], case["q"][0], 2), rtol=1e-13, atol=1e-14)
     assert np.abs(y_pre[1:] - y_post[1:]).max() > 1e-6
+
+
+# ---- Newton-Schulz on the windowed surprise (atlas-torch README, "Atlas
+# Extensions": orthogonalisation of the surprise updates; per-token store
+# path with eta outside Newton-Schulz)
+
+SURPRISE_CASES = [
+    (1, 4, 3, 1, 0, 5, 3, 2, 0, 9),       # linear memory, Omega window 3
+    (2, 3, 2, 1, 0, 5, 3, 3, 4, 8),       # MLP, window 2
+    (2, 4, 1, 1, 0, 3, 4, 4, 6, 8),       # MLP, c = 1 (rank-one surprise)
+    (1, 3, 5, 2, 0, 5, 2, 2, 0, 9),       # polynomial features, window longer than a chunk
+]
+
+
+@pytest.mark.parametrize("case_def", SURPRISE_CASES)
+def test_surprise_ns_matches_bruteforce(case_def):
+    depth, C, c, p, proj, ns, d_k, d_v, hidden, T = case_def
+    rng = np.random.default_rng(sum(case_def) * 104729 + 3)
+    case = _rand_case(rng, depth, d_k, d_v, hidden, T, p=p, proj=proj)
+    y, W, S, _ = _run_oracle(Cfg(depth=depth, C=C, c=c, p=p, ns_iters=ns, ns_target="surprise"), case)
+    yb, Wb, Sb = bf.forward(depth, C, c, p, ns, case["k"], case["q"], case["v"], case["theta"], case["eta"],
+                            case["alpha"], case["gamma"], case["W0"], case["S0"], case["P"], surprise_ns=True)
+    np.testing.assert_allclose(y, yb, rtol=1e-9, atol=1e-11)
+    for a, b in zip(W + S, Wb + Sb):
+        np.testing.assert_allclose(a, b, rtol=1e-9, atol=1e-11)
+
+
+def test_surprise_ns_rank_one_closed_form():
+    """c = 1, linear memory, one token: the surprise 2 x^T (x W - v) is rank
+    one, so NS maps it to f5(s) x_hat e_hat^T with s = |g| / (|g| + eps) and
+    f5 the quintic applied five times (Muon's polynomial); the momentum and
+    step size stay outside: S = eta S0 - theta f5(s) x_hat e_hat^T."""
+    rng = np.random.default_rng(77)
+    x = rng.standard_normal(3); q = rng.standard_normal(3); v = rng.standard_normal(2)
+    W0 = 0.3 * rng.standard_normal((3, 2)); S0 = 0.1 * rng.standard_normal((3, 2))
+    th, et, al = 0.07, 0.6, 0.05
+    e = x @ W0 - v
+    g = 2.0 * np.outer(x, e)
+    s = np.linalg.norm(g) / (np.linalg.norm(g) + 1e-7)
+    for _ in range(5):
+        s = 3.4445 * s - 4.7750 * s ** 3 + 2.0315 * s ** 5
+    S_exp = et * S0 - th * s * np.outer(x / np.linalg.norm(x), e / np.linalg.norm(e))
+    W_exp = (1 - al) * W0 + S_exp
+    y, W, S, _ = oracle.forward_unit(Cfg(depth=1, C=1, c=1, ns_iters=5, ns_target="surprise"), x[None], q[None],
+                                     v[None], [th], [et], [al], None, [W0], [S0])
+    np.testing.assert_allclose(S[0], S_exp, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(W[0], W_exp, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(y[0], q @ W_exp, rtol=1e-12, atol=1e-14)
