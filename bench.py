@@ -45,7 +45,19 @@ def flops_per_chunk(w) -> float:
     feat = 0.0
     if w.proj_dim:
         feat = 2.0 * w.poly_dim * w.proj_dim * (C + C)     # keys and queries of the chunk
-    if w.ns_iters == 0:
+    surprise = w.ns_iters > 0 and getattr(w, "ns_target", "momentum") == "surprise"
+    if w.ns_iters == 0 or surprise:
+        extra = 0.0
+        if surprise:
+            # c x c Newton-Schulz cores per token and matrix, Gram bands of
+            # the window factors, banded coefficient mixes in the read-out
+            # and the chunk-end state (the rest is the plain dual form)
+            mats = [(F, dv)] if w.depth == 1 else [(F, h), (h, dv)]
+            band = 2 * w.c - 1
+            for (r, c) in mats:
+                extra += 2.0 * Kw * band * (r + c)                          # Gram bands
+                extra += C * w.ns_iters * 5 * 2.0 * w.c ** 3                # cores
+                extra += C * 2.0 * Kw * band + 2 * 2.0 * Kw * band * c      # read-out mix, M_e R
         if w.depth == 1:
             fwd = 2.0 * Kw * F * dv
             read = 2.0 * C * 2 * F * dv + 2.0 * C * Kw * F + 2.0 * C * Kw * dv
@@ -55,7 +67,7 @@ def flops_per_chunk(w) -> float:
             read = (2.0 * C * 2 * F * h + 2.0 * C * Kw * F + 2.0 * C * Kw * h
                     + 2.0 * C * 2 * h * dv + 2.0 * C * Kw * h + 2.0 * C * Kw * dv)
             state = 2 * 2 * 2.0 * F * h * Kw
-        return feat + fwd + read + state
+        return feat + fwd + read + state + extra
     # Newton-Schulz: per token and matrix, S_t from the window factors, k
     # quintic steps on the short side, decay scan and read-out.
     mats = [(F, dv)] if w.depth == 1 else [(F, h), (h, dv)]

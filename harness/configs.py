@@ -91,6 +91,12 @@ WORKLOADS = {
         "atlas_muon", depth=2, d_k=128, d_v=128, hidden=512, C=64, c=8, p=1,
         proj_dim=0, ns_iters=5, qkv_dtype="bf16", B=2, H=16, T=16384, seed=3,
         w0_init="xavier"),
+    # ATLAS with Newton-Schulz on the windowed surprise (eta, theta outside
+    # NS) instead of the momentum; otherwise the Muon workload.
+    "atlas_muon_surprise": Workload(
+        "atlas_muon_surprise", depth=2, d_k=128, d_v=128, hidden=512, C=64, c=8, p=1,
+        proj_dim=0, ns_iters=5, qkv_dtype="bf16", B=2, H=16, T=16384, seed=3,
+        w0_init="xavier", ns_target="surprise"),
     # Long context: degree-2 features of 64-dim keys (2145) projected to 64.
     "atlas_long": Workload(
         "atlas_long", depth=2, d_k=64, d_v=64, hidden=256, C=64, c=8, p=2,

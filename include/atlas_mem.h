@@ -54,6 +54,10 @@ extern "C" {
 #define ATLAS_READOUT_POST 0
 #define ATLAS_READOUT_PRE 1
 
+/* where Newton-Schulz applies (atlas_mem_config.ns_target) */
+#define ATLAS_NS_MOMENTUM 0
+#define ATLAS_NS_SURPRISE 1
+
 typedef struct {
     int depth;      /* 1 (matrix memory) or 2 (residual SiLU MLP) */
     int d_k;        /* key/query width before the feature map */
@@ -70,6 +74,14 @@ typedef struct {
                      * paper's MAC"); ATLAS_READOUT_PRE: y_t = M_{t-1}(q_t), the
                      * memory before it (titans-pytorch-mlx README, MAC, Eq. 21).
                      * The state written back is the same either way. */
+    int ns_target;  /* with ns_iters > 0: ATLAS_NS_MOMENTUM orthogonalises the
+                     * applied momentum, U_t = NS(S_t) (ATLAS summary, Section
+                     * 5); ATLAS_NS_SURPRISE orthogonalises each token's windowed
+                     * gradient with eta and theta outside, S_t = eta_t S_{t-1}
+                     * - theta_t NS(g_t), W_t = (1 - alpha_t) W_{t-1} + S_t
+                     * (atlas-torch README, "Atlas Extensions": Muon / Newton-
+                     * Schulz on the surprise; "eta outside Newton-Schulz").
+                     * The surprise has rank <= c, so it needs c <= 32. */
 } atlas_mem_config;
 
 typedef struct atlas_mem_handle atlas_mem_handle;

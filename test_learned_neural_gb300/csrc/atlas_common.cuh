@@ -26,6 +26,7 @@ struct Geom {
   int Kw;         // max window rows of one chunk = C + c - 1
   int rows[2], cols[2], nmat;
   int readout;    // ATLAS_READOUT_POST / ATLAS_READOUT_PRE
+  int ns_target;  // ATLAS_NS_MOMENTUM / ATLAS_NS_SURPRISE
 };
 
 // Per-chunk indices: the chunk covers tokens [s, e) of the call; its Omega
@@ -73,6 +74,8 @@ struct Work {
                   // depth 1: cs_e dy and cw_e dy [units][2][Kw][d_v], then per
                   // (unit, 64-feature slice) partial products R W, R S, R X^T, X W,
                   // then per (unit, chunk) gate-scan coefficients
+  float* surp;    // Newton-Schulz on the surprise: Gram matrices, c x c cores,
+                  // banded coefficient matrices (k_surprise.cu)
   int* status;    // device status word
 };
 
@@ -94,6 +97,11 @@ size_t generic_smem_readout(const Geom& g);
 size_t generic_smem_ns(const Geom& g, int m);
 size_t grad_part_floats(const Geom& g);
 size_t dual1_split_floats(const Geom& g, size_t units, int T);
+
+// Newton-Schulz on the windowed surprise (k_surprise.cu)
+size_t surprise_floats(const Geom& g, size_t units);
+cudaError_t surprise_chunk(const Geom& g, const Chunk& ch, const Work& w, const float* theta, const float* eta,
+                           const float* alpha, float* y, int buf, cudaStream_t st, int* nl);
 int num_sms();
 
 // fused tensor-core MLP memory without Newton-Schulz (k_mlp_tc.cu)

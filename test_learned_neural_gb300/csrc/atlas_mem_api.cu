@@ -63,6 +63,10 @@ static int derive_geom(const atlas_mem_config& c, Geom* g, char* why, size_t why
   if (c.qkv_dtype != ATLAS_F32 && c.qkv_dtype != ATLAS_BF16) BAD("qkv_dtype must be ATLAS_F32 or ATLAS_BF16");
   if (c.readout != ATLAS_READOUT_POST && c.readout != ATLAS_READOUT_PRE)
     BAD("readout must be ATLAS_READOUT_POST or ATLAS_READOUT_PRE");
+  if (c.ns_target != ATLAS_NS_MOMENTUM && c.ns_target != ATLAS_NS_SURPRISE)
+    BAD("ns_target must be ATLAS_NS_MOMENTUM or ATLAS_NS_SURPRISE");
+  if (c.ns_target == ATLAS_NS_SURPRISE && c.ns_iters > 0 && c.c > 32)
+    BAD("Newton-Schulz on the surprise needs c <= 32 (its c x c core)");
   long long poly = c.p == 1 ? c.d_k : 1 + c.d_k + choose2(c.d_k + 1);
   long long F = c.proj_dim ? c.proj_dim : poly;
   if (c.depth == 2 && F != c.d_v) BAD("depth 2 (residual memory) needs feature width %lld == d_v %d", F, c.d_v);
@@ -70,6 +74,7 @@ static int derive_geom(const atlas_mem_config& c, Geom* g, char* why, size_t why
   g->C = c.C; g->c = c.c; g->p = c.p; g->proj_dim = c.proj_dim; g->ns_iters = c.ns_iters;
   g->qkv_dtype = c.qkv_dtype;
   g->readout = c.readout;
+  g->ns_target = c.ns_target;
   g->Kw = c.C + c.c - 1;
   if (c.depth == 1) {
     g->nmat = 1; g->rows[0] = (int)F; g->cols[0] = c.d_v;
@@ -85,7 +90,7 @@ static int derive_geom(const atlas_mem_config& c, Geom* g, char* why, size_t why
   if (generic_smem_grad(*g) > kSmemLimit || generic_smem_readout(*g) > kSmemLimit)
     BAD("memory widths too large for the on-chip working set");
   if ((size_t)(c.d_k + (c.proj_dim ? poly : 0)) * 4 > kSmemLimit) BAD("feature map too wide");
-  if (c.ns_iters > 0)
+  if (c.ns_iters > 0 && c.ns_target == ATLAS_NS_MOMENTUM)
     for (int m = 0; m < g->nmat; ++m) {
       int rX = g->rows[m] < g->cols[m] ? g->rows[m] : g->cols[m];
       if (rX > 128) BAD("Newton-Schulz on matrices whose short side exceeds 128 is not supported");
@@ -129,12 +134,13 @@ static Layout layout(const Geom& g, int units, int T) {
       U * g.C * Kw,                        // Cs
       U * g.C * Kw,                        // Cw
       U * g.C, U * g.C, U * g.C,           // Ap Bp Dp
-      g.ns_iters ? U * g.C * mat : 0,      // Ubuf
+      g.ns_iters && g.ns_target == ATLAS_NS_MOMENTUM ? U * g.C * mat : 0,   // Ubuf
       U * (size_t)(g.c > 1 ? g.c - 1 : 0) * (g.d_k + g.d_v + 1),  // cache temp
       64,                                  // status
       ns_tc_xch_floats(g, num_sms()),      // Gram exchange of the CTA-pair Newton-Schulz
       g.depth == 2 ? U * ((size_t)(g.hidden + 63) / 64) * Kw * g.d_v  // tiled-gradient partial outputs
                    : dual1_split_floats(g, U, T),                       // depth 1: scaled dy + feature-slice partials
+      g.ns_iters && g.ns_target == ATLAS_NS_SURPRISE ? surprise_floats(g, U) : 0,   // surprise NS scratch
   };
   const int n = sizeof sizes / sizeof sizes[0];
   size_t o = 0;
@@ -160,6 +166,7 @@ static Work work_from(const Geom& g, void* base, const Layout& L, float** cache_
   w.status = (int*)F(23);
   w.xch = F(24);
   w.gpart = F(25);
+  w.surp = F(26);
   return w;
 }
 

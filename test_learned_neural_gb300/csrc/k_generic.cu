@@ -586,9 +586,27 @@ bool ns_fused_scan_supported(const Geom& g);
 cudaError_t ns_fused_scan(const Geom& g, const Chunk& ch, const Work& w, int buf, size_t slot_stride,
                           const float* alpha, float* aq, float* y, cudaStream_t st);
 
+// window-row gradient factors at the chunk-start weights: tiled kernels
+// where they fit, one block per window row otherwise
+static cudaError_t grad_tiled_or_rows(const Geom& g, const Chunk& ch, const Work& w, int buf, cudaStream_t st,
+                                      int* nl) {
+  if (g.depth == 1 || ch.nw <= 128) return grad_tiled(g, ch, w, buf, st, nl);
+  const size_t sg = generic_smem_grad(g);
+  cudaFuncSetAttribute(k_grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg);
+  k_grad<<<dim3(ch.nw, g.units), 256, sg, st>>>(g, ch, w, buf);
+  return cudaGetLastError();
+}
+
 cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const GenericIO& io, int buf,
                           cudaStream_t st, int* nl) {
   if (dual1_split_supported(g)) return dual1_split(g, ch, w, io, buf, st, nl);
+  if (g.ns_iters > 0 && g.ns_target == ATLAS_NS_SURPRISE) {
+    CUDA_CHECK_RET(grad_tiled_or_rows(g, ch, w, buf, st, nl));
+    const int coef_threads = ((ch.nw + 31) / 32) * 32;
+    k_coef<<<g.units, coef_threads, 0, st>>>(g, ch, io.theta, io.eta, io.alpha, w);
+    *nl += 2;
+    return surprise_chunk(g, ch, w, io.theta, io.eta, io.alpha, io.y, buf, st, nl);
+  }
   *nl += g.ns_iters == 0 ? 3 + g.nmat : 3 + 2 * g.nmat;
   const size_t sr = generic_smem_readout(g);
   if (g.depth == 1 || ch.nw <= 128) {

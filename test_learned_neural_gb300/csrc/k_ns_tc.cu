@@ -750,7 +750,7 @@ __global__ void k_transpose_units(const float* __restrict__ in, float* __restric
 
 // 0: not covered; 1: short side 64 (one CTA per task); 2: 128 x 512 (CTA pairs)
 int ns_tc_kind(const Geom& g) {
-  if (g.ns_iters <= 0) return 0;
+  if (g.ns_iters <= 0 || g.ns_target != ATLAS_NS_MOMENTUM) return 0;
   const int Kp = (g.Kw + 15) / 16 * 16;
   if (Kp > 128) return 0;
   int kind = -1, n0 = -1;

@@ -30,7 +30,8 @@ class Memory:
         self.qkv_torch = torch.float32 if cfg.qkv_dtype in ("f32", ATLAS_F32) else torch.bfloat16
         self.h = atlas_mem_create(make_config(cfg.depth, cfg.d_k, cfg.d_v, cfg.hidden if cfg.depth == 2 else 0,
                                               cfg.C, cfg.c, cfg.p, cfg.proj_dim, cfg.ns_iters, cfg.qkv_dtype,
-                                              getattr(cfg, "readout", "post")))
+                                              getattr(cfg, "readout", "post"),
+                                              getattr(cfg, "ns_target", "momentum")))
 
     def close(self):
         if self.h is not None:

@@ -52,6 +52,8 @@ def _cfg(**kw):
     (dict(p=3), tln.ATLAS_ERR_INVALID_ARG),
     (dict(qkv_dtype=7), tln.ATLAS_ERR_INVALID_ARG),
     (dict(readout=5), tln.ATLAS_ERR_INVALID_ARG),
+    (dict(ns_target=3), tln.ATLAS_ERR_INVALID_ARG),
+    (dict(ns_target=1, ns_iters=5, c=40), tln.ATLAS_ERR_INVALID_ARG),
     (dict(C=1000, c=100), tln.ATLAS_ERR_UNSUPPORTED),     # window rows > 1024
     (dict(d_k=256, d_v=256, hidden=512, ns_iters=5), tln.ATLAS_ERR_UNSUPPORTED),  # NS short side > 128
 ])

@@ -141,3 +141,30 @@ def test_streaming_one_token_calls(gpu_lib, readout):
     for m in range(len(W)):
         assert maxrel(W[m].cpu().numpy(), whole["W"][m]) < 1e-5
     mem.close()
+
+
+SURPRISE = {
+    "linear_f32": dict(ns_iters=5, c=3),                       # fp32, Omega window 3
+    "atlas_poly_c4": dict(B=1, H=2, T=256, ns_iters=5),        # depth 1, degree-2 features
+    "titans_mlp": dict(B=1, H=2, T=256, ns_iters=5),           # c = 1: rank-one surprise
+    "atlas_muon_surprise": dict(B=1, H=1, T=128),              # 128 -> 512 -> 128, c = 8
+    "atlas_long": dict(B=1, H=2, T=192),                       # projected features, c = 8
+}
+
+
+@pytest.mark.parametrize("name", list(SURPRISE))
+@pytest.mark.parametrize("readout", ["post", "pre"])
+def test_small_parity_surprise_ns(gpu_lib, name, readout):
+    """Newton-Schulz on each token's windowed surprise (atlas-torch README,
+    "Atlas Extensions"), run on the GPU as a c x c core iteration with banded
+    dual-form coefficients, against the oracle's dense NS of g_t."""
+    w = WORKLOADS[name].scaled(ns_target="surprise", readout=readout, **SURPRISE[name])
+    errs = compare(w)
+    tol = TOL[w.qkv_dtype]
+    print(name, "surprise", readout, {k: f"{v:.2e}" for k, v in errs.items()})
+    assert errs["y"] <= tol
+    for k, v in errs.items():
+        if k.startswith("W"):
+            assert v <= tol, (k, v)
+        if k.startswith("S"):
+            assert v <= 5 * tol, (k, v)
