@@ -26,6 +26,7 @@
 // K~_t being K_t placed on token t's window rows.  The read-out of token t
 // goes through (r_t L^T) Mw_t R; the chunk-end state through L^T (Ms_e R).
 #include "atlas_common.cuh"
+#include "simt_tile.cuh"
 
 namespace atlas {
 namespace {
@@ -212,93 +213,118 @@ __global__ void __launch_bounds__(256) k_surp_scan(Geom g, Chunk ch, Work w, con
   base[S.mwe + ((size_t)m * g.Kw + i) * band + d] = Mw;
 }
 
-// out_j = sum_i v_i M[i][j] over the band (M rows of 2c - 1 entries)
-__device__ void band_mix(const Geom& g, int nw, const float* v, const float* M, float* out) {
-  const int band = 2 * g.c - 1, c = g.c;
-  for (int j = threadIdx.x; j < nw; j += blockDim.x) {
-    float acc = 0.f;
-    const int i0 = j - c + 1 > 0 ? j - c + 1 : 0, i1 = j + c - 1 < nw - 1 ? j + c - 1 : nw - 1;
-    for (int i = i0; i <= i1; ++i) acc += v[i] * M[(size_t)i * band + (j - i + c - 1)];
-    out[j] = acc;
-  }
-}
+constexpr int TG = 8;   // tokens per read-out block: W, S columns are loaded once for all of them
 
-// read-out of token r: y = B_t r W + D_t r S - ((r L^T) Mw) R  (through the
-// MLP at depth 2); one block per (token, unit)
+// read-out of tokens [r0, r0 + TG): y = B_t r W + D_t r S - ((r L^T) Mw_t) R
+// (through the MLP at depth 2); one block per (token group, unit)
 __global__ void __launch_bounds__(256) k_surp_readout(Geom g, Chunk ch, Work w, int buf, float* y) {
   extern __shared__ float sm[];
-  const int u = blockIdx.y, r = blockIdx.x, t = ch.s + r;
+  __shared__ float Bt[TG], Dt[TG];
+  const int u = blockIdx.y, r0 = blockIdx.x * TG;
+  const int Ct = ch.e - ch.s, nt = Ct - r0 < TG ? Ct - r0 : TG, nw = ch.nw;
   const SurpLayout S = surp_layout(g);
-  const int band = 2 * g.c - 1;
-  float* rs = sm;              // F
-  float* gm = rs + g.F;        // Kw
-  float* gm2 = gm + g.Kw;      // Kw
-  float* aq = gm2 + g.Kw;      // hidden (depth 2)
-  const float* rq = w.R + ((size_t)u * g.T + t) * g.F;
-  for (int f = threadIdx.x; f < g.F; f += blockDim.x) rs[f] = rq[f];
-  __syncthreads();
-  const int rr = g.readout == ATLAS_READOUT_PRE ? r - 1 : r;
-  const float Bt = rr < 0 ? 1.f : w.Bp[(size_t)u * g.C + rr], Dt = rr < 0 ? 0.f : w.Dp[(size_t)u * g.C + rr];
-  const float* Xw = lfac(g, ch, w, u, 0);
-  for (int i = threadIdx.x; i < ch.nw; i += blockDim.x) {
-    float acc = 0.f;
-    for (int f = 0; f < g.F; ++f) acc += rs[f] * Xw[(size_t)i * g.F + f];
-    gm[i] = acc;
+  const int band = 2 * g.c - 1, F = g.F, Kw = g.Kw;
+  float* rs = sm;              // [TG][F]
+  float* gm = rs + TG * F;     // [TG][Kw]
+  float* gm2 = gm + TG * Kw;   // [TG][Kw]
+  float* aq = gm2 + TG * Kw;   // [TG][hidden] (depth 2)
+  for (int e = threadIdx.x; e < TG * F; e += blockDim.x) {
+    const int tt = e / F, f = e % F;
+    rs[e] = tt < nt ? w.R[((size_t)u * g.T + ch.s + r0 + tt) * F + f] : 0.f;
+  }
+  if (threadIdx.x < TG) {
+    const int rr = (g.readout == ATLAS_READOUT_PRE ? -1 : 0) + r0 + (int)threadIdx.x;
+    const bool ok = rr >= 0 && r0 + (int)threadIdx.x < Ct;
+    Bt[threadIdx.x] = ok ? w.Bp[(size_t)u * g.C + rr] : (rr < 0 ? 1.f : 0.f);
+    Dt[threadIdx.x] = ok ? w.Dp[(size_t)u * g.C + rr] : 0.f;
   }
   __syncthreads();
   const float* mwb = w.surp + (size_t)u * S.per_unit + S.mwb;
-  band_mix(g, ch.nw, gm, mwb + (size_t)r * g.Kw * band, gm2);
-  __syncthreads();
-  float* yo = y + ((size_t)u * g.T + t) * g.d_v;
-  if (g.depth == 1) {
-    const float* W = w.Wst[buf][0] + (size_t)u * g.F * g.d_v;
-    const float* Sb = w.Sst[buf][0] + (size_t)u * g.F * g.d_v;
-    const float* DY = rfac(g, w, u, 0);
-    for (int k = threadIdx.x; k < g.d_v; k += blockDim.x) {
-      float a = 0.f, b = 0.f, c2 = 0.f;
-      for (int f = 0; f < g.F; ++f) {
-        a += rs[f] * W[(size_t)f * g.d_v + k];
-        b += rs[f] * Sb[(size_t)f * g.d_v + k];
+  // gm[tt][i] = r . L_i, then gm2[tt][j] = sum_i gm[tt][i] Mw_t[i][j] (band)
+  auto mix = [&](const float* Lw, int width, const float* vec, int vstride, const float* Mw) {
+    // one warp per window row: coalesced loads of L_i, all TG tokens at once
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    for (int i = warp; i < nw; i += blockDim.x / 32) {
+      float acc[TG];
+#pragma unroll
+      for (int tt = 0; tt < TG; ++tt) acc[tt] = 0.f;
+#pragma unroll 4
+      for (int f = lane; f < width; f += 32) {
+        const float lv = Lw[(size_t)i * width + f];
+#pragma unroll
+        for (int tt = 0; tt < TG; ++tt) acc[tt] += vec[tt * vstride + f] * lv;
       }
-      for (int j = 0; j < ch.nw; ++j) c2 += gm2[j] * DY[(size_t)j * g.d_v + k];
-      yo[k] = Bt * a + Dt * b - c2;
+#pragma unroll
+      for (int tt = 0; tt < TG; ++tt) {
+        float v = acc[tt];
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) gm[tt * Kw + i] = v;
+      }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < TG * nw; e += blockDim.x) {
+      const int tt = e / nw, j = e % nw;
+      float acc = 0.f;
+      if (tt < nt) {
+        const float* M = Mw + (size_t)(r0 + tt) * Kw * band;
+        const int i0 = j - g.c + 1 > 0 ? j - g.c + 1 : 0, i1 = j + g.c - 1 < nw - 1 ? j + g.c - 1 : nw - 1;
+        for (int i = i0; i <= i1; ++i) acc += gm[tt * Kw + i] * M[(size_t)i * band + (j - i + g.c - 1)];
+      }
+      gm2[tt * Kw + j] = acc;
+    }
+    __syncthreads();
+  };
+  // out[tt][k] = B_t (v W)[k] + D_t (v S)[k] - (gm2 R)[k] for k < cols
+  auto terms = [&](const float* vec, int vstride, int K, const float* Wm, const float* Sm, const float* Rf, int cols,
+                   int k, float* res) {
+    float a[TG], b[TG], c2[TG];
+#pragma unroll
+    for (int tt = 0; tt < TG; ++tt) a[tt] = b[tt] = c2[tt] = 0.f;
+#pragma unroll 4
+    for (int f = 0; f < K; ++f) {
+      const float wv = Wm[(size_t)f * cols + k], sv = Sm[(size_t)f * cols + k];
+#pragma unroll
+      for (int tt = 0; tt < TG; ++tt) {
+        a[tt] += vec[tt * vstride + f] * wv;
+        b[tt] += vec[tt * vstride + f] * sv;
+      }
+    }
+#pragma unroll 4
+    for (int j = 0; j < nw; ++j) {
+      const float rv = Rf[(size_t)j * cols + k];
+#pragma unroll
+      for (int tt = 0; tt < TG; ++tt) c2[tt] += gm2[tt * Kw + j] * rv;
+    }
+#pragma unroll
+    for (int tt = 0; tt < TG; ++tt) res[tt] = Bt[tt] * a[tt] + Dt[tt] * b[tt] - c2[tt];
+  };
+  mix(lfac(g, ch, w, u, 0), F, rs, F, mwb);
+  if (g.depth == 1) {
+    const float* W = w.Wst[buf][0] + (size_t)u * F * g.d_v;
+    const float* Sb = w.Sst[buf][0] + (size_t)u * F * g.d_v;
+    for (int k = threadIdx.x; k < g.d_v; k += blockDim.x) {
+      float res[TG];
+      terms(rs, F, F, W, Sb, rfac(g, w, u, 0), g.d_v, k, res);
+      for (int tt = 0; tt < nt; ++tt) y[((size_t)u * g.T + ch.s + r0 + tt) * g.d_v + k] = res[tt];
     }
     return;
   }
   const int h = g.hidden;
-  const float* W1 = w.Wst[buf][0] + (size_t)u * g.F * h;
-  const float* S1 = w.Sst[buf][0] + (size_t)u * g.F * h;
-  const float* DZ = rfac(g, w, u, 0);
   for (int k = threadIdx.x; k < h; k += blockDim.x) {
-    float a = 0.f, b = 0.f, c2 = 0.f;
-    for (int f = 0; f < g.F; ++f) {
-      a += rs[f] * W1[(size_t)f * h + k];
-      b += rs[f] * S1[(size_t)f * h + k];
-    }
-    for (int j = 0; j < ch.nw; ++j) c2 += gm2[j] * DZ[(size_t)j * h + k];
-    aq[k] = siluf_(Bt * a + Dt * b - c2);
+    float res[TG];
+    terms(rs, F, F, w.Wst[buf][0] + (size_t)u * F * h, w.Sst[buf][0] + (size_t)u * F * h, rfac(g, w, u, 0), h, k,
+          res);
+#pragma unroll
+    for (int tt = 0; tt < TG; ++tt) aq[tt * h + k] = siluf_(res[tt]);
   }
   __syncthreads();
-  const float* Aw = lfac(g, ch, w, u, 1);
-  for (int i = threadIdx.x; i < ch.nw; i += blockDim.x) {
-    float acc = 0.f;
-    for (int k = 0; k < h; ++k) acc += aq[k] * Aw[(size_t)i * h + k];
-    gm[i] = acc;
-  }
-  __syncthreads();
-  band_mix(g, ch.nw, gm, mwb + ((size_t)g.C + r) * g.Kw * band, gm2);
-  __syncthreads();
-  const float* W2 = w.Wst[buf][1] + (size_t)u * h * g.d_v;
-  const float* S2 = w.Sst[buf][1] + (size_t)u * h * g.d_v;
-  const float* DY = rfac(g, w, u, 1);
+  mix(lfac(g, ch, w, u, 1), h, aq, h, mwb + (size_t)g.C * Kw * band);
   for (int k = threadIdx.x; k < g.d_v; k += blockDim.x) {
-    float a = 0.f, b = 0.f, c2 = 0.f;
-    for (int j2 = 0; j2 < h; ++j2) {
-      a += aq[j2] * W2[(size_t)j2 * g.d_v + k];
-      b += aq[j2] * S2[(size_t)j2 * g.d_v + k];
-    }
-    for (int j = 0; j < ch.nw; ++j) c2 += gm2[j] * DY[(size_t)j * g.d_v + k];
-    yo[k] = rs[k] + Bt * a + Dt * b - c2;
+    float res[TG];
+    terms(aq, h, h, w.Wst[buf][1] + (size_t)u * h * g.d_v, w.Sst[buf][1] + (size_t)u * h * g.d_v,
+          rfac(g, w, u, 1), g.d_v, k, res);
+    for (int tt = 0; tt < nt; ++tt)
+      y[((size_t)u * g.T + ch.s + r0 + tt) * g.d_v + k] = rs[tt * F + k] + res[tt];
   }
 }
 
@@ -319,31 +345,35 @@ __global__ void __launch_bounds__(256) k_surp_rprime(Geom g, Chunk ch, Work w) {
   }
 }
 
-// chunk-end state: S = A_e Sbar - L^T (Ms_e R), W = B_e Wbar + D_e Sbar - L^T (Mw_e R)
-__global__ void k_surp_state(Geom g, Chunk ch, Work w, int m, int buf) {
-  const int u = blockIdx.y;
-  const int rows = g.rows[m], cols = g.cols[m];
-  const size_t n = (size_t)rows * cols;
-  const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= n) return;
-  const int a = (int)(e / cols), b = (int)(e % cols);
+// chunk-end state: S = A_e Sbar - L^T (Ms_e R), W = B_e Wbar + D_e Sbar - L^T (Mw_e R);
+// one 64 x 64 tile of matrix m per block
+__global__ void __launch_bounds__(256) k_surp_state(Geom g, Chunk ch, Work w, int m, int buf) {
+  __shared__ float As[16 * 64], Bs[16 * 64];
+  const int u = blockIdx.z, a0 = blockIdx.y * 64, b0 = blockIdx.x * 64;
+  const int rows = g.rows[m], cols = g.cols[m], mc = max_cols(g);
   const SurpLayout S = surp_layout(g);
-  const int mc = max_cols(g);
   const float* L = lfac(g, ch, w, u, m);
   const float* rps = w.surp + (size_t)u * S.per_unit + S.rp + ((size_t)m * 2 + 0) * g.Kw * mc;
   const float* rpw = rps + (size_t)g.Kw * mc;
-  float accs = 0.f, accw = 0.f;
-  for (int i = 0; i < ch.nw; ++i) {
-    const float l = L[(size_t)i * rows + a];
-    accs += l * rps[(size_t)i * mc + b];
-    accw += l * rpw[(size_t)i * mc + b];
-  }
+  float accs[4][4], accw[4][4];
+  tile_gemm(TileOp{L, 1, rows}, TileOp{rps, 1, mc}, rows, cols, ch.nw, a0, b0, accs, As, Bs);
+  tile_gemm(TileOp{L, 1, rows}, TileOp{rpw, 1, mc}, rows, cols, ch.nw, a0, b0, accw, As, Bs);
   const int re = ch.e - 1 - ch.s;
   const float Ae = w.Ap[(size_t)u * g.C + re], Be = w.Bp[(size_t)u * g.C + re], De = w.Dp[(size_t)u * g.C + re];
-  const size_t o = (size_t)u * n + e;
-  const float Sb = w.Sst[buf][m][o], Wb = w.Wst[buf][m][o];
-  w.Sst[buf ^ 1][m][o] = Ae * Sb - accs;
-  w.Wst[buf ^ 1][m][o] = Be * Wb + De * Sb - accw;
+  const size_t n = (size_t)rows * cols;
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  for (int p = 0; p < 4; ++p) {
+    const int a = a0 + ty * 4 + p;
+    if (a >= rows) continue;
+    for (int q = 0; q < 4; ++q) {
+      const int b = b0 + tx * 4 + q;
+      if (b >= cols) continue;
+      const size_t o = (size_t)u * n + (size_t)a * cols + b;
+      const float Sb = w.Sst[buf][m][o], Wb = w.Wst[buf][m][o];
+      w.Sst[buf ^ 1][m][o] = Ae * Sb - accs[p][q];
+      w.Wst[buf ^ 1][m][o] = Be * Wb + De * Sb - accw[p][q];
+    }
+  }
 }
 
 }  // namespace
@@ -356,14 +386,12 @@ cudaError_t surprise_chunk(const Geom& g, const Chunk& ch, const Work& w, const 
   k_surp_gram<<<dim3(ch.nw, g.nmat * 2, g.units), 256, 0, st>>>(g, ch, w);
   k_surp_ns<<<dim3(Ct, g.nmat, g.units), 256, 0, st>>>(g, ch, w);
   k_surp_scan<<<dim3((g.Kw * band + 255) / 256, g.nmat, g.units), 256, 0, st>>>(g, ch, w, theta, eta, alpha);
-  const size_t sr = (size_t)(g.F + 2 * g.Kw + (g.depth == 2 ? g.hidden : 0)) * sizeof(float);
+  const size_t sr = (size_t)TG * (g.F + 2 * g.Kw + (g.depth == 2 ? g.hidden : 0)) * sizeof(float);
   cudaFuncSetAttribute(k_surp_readout, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sr);
-  k_surp_readout<<<dim3(Ct, g.units), 256, sr, st>>>(g, ch, w, buf, y);
+  k_surp_readout<<<dim3((Ct + TG - 1) / TG, g.units), 256, sr, st>>>(g, ch, w, buf, y);
   k_surp_rprime<<<dim3(ch.nw, g.nmat * 2, g.units), 256, 0, st>>>(g, ch, w);
-  for (int m = 0; m < g.nmat; ++m) {
-    const size_t n = (size_t)g.rows[m] * g.cols[m];
-    k_surp_state<<<dim3((unsigned)((n + 255) / 256), g.units), 256, 0, st>>>(g, ch, w, m, buf);
-  }
+  for (int m = 0; m < g.nmat; ++m)
+    k_surp_state<<<dim3((g.cols[m] + 63) / 64, (g.rows[m] + 63) / 64, g.units), 256, 0, st>>>(g, ch, w, m, buf);
   *nl += 5 + g.nmat;
   return cudaGetLastError();
 }
