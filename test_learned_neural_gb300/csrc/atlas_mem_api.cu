@@ -25,6 +25,17 @@ struct atlas_mem_handle {
   bool launched = false;
   int launches = 0;       // kernel launches of the last forward
   std::string err;
+  // Repeated identical calls of the multi-launch path replay a CUDA graph:
+  // the second call with the same arguments (and workspace) captures the
+  // launch sequence on a private stream, later ones launch the graph.
+  cudaStream_t cap = nullptr;
+  cudaGraphExec_t gexec = nullptr;
+  atlas_mem_io gkey{};    // arguments the graph was captured with
+  void* gws = nullptr;
+  int glaunches = 0;
+  atlas_mem_io last_io{}; // arguments of the previous multi-launch call
+  void* last_ws = nullptr;
+  bool have_last = false;
 };
 
 // message of the last atlas_mem_create failure on this thread (no handle yet)
@@ -194,6 +205,8 @@ extern "C" int atlas_mem_create(const atlas_mem_config* cfg, atlas_mem_handle** 
 
 extern "C" void atlas_mem_destroy(atlas_mem_handle* h) {
   if (!h) return;
+  if (h->gexec) cudaGraphExecDestroy(h->gexec);
+  if (h->cap) cudaStreamDestroy(h->cap);
   if (h->ws) cudaFree(h->ws);
   if (h->stage) cudaFree(h->stage);
   delete h;
@@ -258,6 +271,48 @@ static int ensure_workspace(atlas_mem_handle* h, size_t bytes) {
   return ATLAS_OK;
 }
 
+// the multi-launch path: state in, per-chunk kernels, state and cache out
+static int run_generic(atlas_mem_handle* h, const Geom& g, const Work& w, const atlas_mem_io* io, float* cache_tmp,
+                       cudaStream_t st, int* nl_out) {
+  int nl = 0;
+  const bool ns_tc = ns_tc_supported(g);   // keeps S transposed for tall matrices
+  for (int m = 0; m < g.nmat; ++m) {
+    const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
+    CUDA_TRY(cudaMemcpyAsync(w.Wst[0][m], io->W0[m], bytes, cudaMemcpyDeviceToDevice, st));
+    if (ns_tc) CUDA_TRY(ns_tc_state_in(g, m, io->S0[m], w.Sst[0][m], st));
+    else CUDA_TRY(cudaMemcpyAsync(w.Sst[0][m], io->S0[m], bytes, cudaMemcpyDeviceToDevice, st));
+  }
+  GenericIO gio{io->q, io->k, io->v, io->P, io->win_len ? io->win_k : nullptr, io->win_len ? io->win_v : nullptr,
+                io->theta, io->eta, io->alpha, io->gamma, io->win_len ? io->win_gamma : nullptr, io->y};
+  CUDA_TRY(generic_prepare(g, w, gio, st, &nl));
+  int buf = 0;
+  for (int s = 0; s < g.T; s += g.C) {
+    Chunk ch;
+    ch.s = s;
+    ch.e = s + g.C;
+    ch.lo = s - g.c + 1;
+    if (ch.lo < -g.n_prev) ch.lo = -g.n_prev;
+    ch.nw = ch.e - ch.lo;
+    CUDA_TRY(generic_chunk(g, ch, w, gio, buf, st, &nl));
+    buf ^= 1;
+  }
+  for (int m = 0; m < g.nmat; ++m) {
+    const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
+    CUDA_TRY(cudaMemcpyAsync(io->W_out[m], w.Wst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
+    if (ns_tc) CUDA_TRY(ns_tc_state_out(g, m, w.Sst[buf][m], io->S_out[m], st));
+    else CUDA_TRY(cudaMemcpyAsync(io->S_out[m], w.Sst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
+  }
+  if (g.c > 1 && (io->win_k_out || io->win_v_out || io->win_gamma_out))
+    CUDA_TRY(generic_cache_out(g, gio, cache_tmp, io->win_k_out, io->win_v_out, io->win_gamma_out, st, &nl));
+  *nl_out = nl;
+  return ATLAS_OK;
+}
+
+static bool graphs_enabled() {
+  const char* e = getenv("ATLAS_NO_GRAPH");
+  return !(e && e[0] == '1');
+}
+
 extern "C" int atlas_mem_forward(atlas_mem_handle* h, const atlas_mem_io* io, void* stream) {
   if (!h) return ATLAS_ERR_INVALID_ARG;
   int rc = check_io(h, io);
@@ -283,36 +338,49 @@ extern "C" int atlas_mem_forward(atlas_mem_handle* h, const atlas_mem_io* io, vo
     h->launched = true;
     return ATLAS_OK;
   }
-  const bool ns_tc = ns_tc_supported(g);   // keeps S transposed for tall matrices
-  for (int m = 0; m < g.nmat; ++m) {
-    const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
-    CUDA_TRY(cudaMemcpyAsync(w.Wst[0][m], io->W0[m], bytes, cudaMemcpyDeviceToDevice, st));
-    if (ns_tc) CUDA_TRY(ns_tc_state_in(g, m, io->S0[m], w.Sst[0][m], st));
-    else CUDA_TRY(cudaMemcpyAsync(w.Sst[0][m], io->S0[m], bytes, cudaMemcpyDeviceToDevice, st));
-  }
-  GenericIO gio{io->q, io->k, io->v, io->P, io->win_len ? io->win_k : nullptr, io->win_len ? io->win_v : nullptr,
-                io->theta, io->eta, io->alpha, io->gamma, io->win_len ? io->win_gamma : nullptr, io->y};
   int nl = 0;
-  CUDA_TRY(generic_prepare(g, w, gio, st, &nl));
-  int buf = 0;
-  for (int s = 0; s < g.T; s += g.C) {
-    Chunk ch;
-    ch.s = s;
-    ch.e = s + g.C;
-    ch.lo = s - g.c + 1;
-    if (ch.lo < -g.n_prev) ch.lo = -g.n_prev;
-    ch.nw = ch.e - ch.lo;
-    CUDA_TRY(generic_chunk(g, ch, w, gio, buf, st, &nl));
-    buf ^= 1;
+  if (graphs_enabled()) {
+    const bool same_as_graph = h->gexec && h->gws == h->ws && memcmp(&h->gkey, io, sizeof *io) == 0;
+    if (same_as_graph) {
+      CUDA_TRY(cudaGraphLaunch(h->gexec, st));
+      h->launches = h->glaunches;
+      h->last_stream = st;
+      h->launched = true;
+      return ATLAS_OK;
+    }
+    const bool repeat = h->have_last && h->last_ws == h->ws && memcmp(&h->last_io, io, sizeof *io) == 0;
+    h->last_io = *io;
+    h->last_ws = h->ws;
+    h->have_last = true;
+    if (repeat) {
+      if (!h->cap) CUDA_TRY(cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking));
+      CUDA_TRY(cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeThreadLocal));
+      const int rc2 = run_generic(h, g, w, io, cache_tmp, h->cap, &nl);
+      cudaGraph_t graph = nullptr;
+      const cudaError_t ec = cudaStreamEndCapture(h->cap, &graph);
+      if (rc2) {
+        if (graph) cudaGraphDestroy(graph);
+        return rc2;
+      }
+      if (ec != cudaSuccess) return fail(h, ATLAS_ERR_CUDA, "cudaStreamEndCapture: %s", cudaGetErrorString(ec));
+      cudaGraphExec_t ex = nullptr;
+      const cudaError_t ei = cudaGraphInstantiate(&ex, graph, 0);
+      cudaGraphDestroy(graph);
+      if (ei != cudaSuccess) return fail(h, ATLAS_ERR_CUDA, "cudaGraphInstantiate: %s", cudaGetErrorString(ei));
+      if (h->gexec) cudaGraphExecDestroy(h->gexec);
+      h->gexec = ex;
+      h->gkey = *io;
+      h->gws = h->ws;
+      h->glaunches = nl;
+      CUDA_TRY(cudaGraphLaunch(h->gexec, st));
+      h->launches = nl;
+      h->last_stream = st;
+      h->launched = true;
+      return ATLAS_OK;
+    }
   }
-  for (int m = 0; m < g.nmat; ++m) {
-    const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
-    CUDA_TRY(cudaMemcpyAsync(io->W_out[m], w.Wst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
-    if (ns_tc) CUDA_TRY(ns_tc_state_out(g, m, w.Sst[buf][m], io->S_out[m], st));
-    else CUDA_TRY(cudaMemcpyAsync(io->S_out[m], w.Sst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
-  }
-  if (g.c > 1 && (io->win_k_out || io->win_v_out || io->win_gamma_out))
-    CUDA_TRY(generic_cache_out(g, gio, cache_tmp, io->win_k_out, io->win_v_out, io->win_gamma_out, st, &nl));
+  rc = run_generic(h, g, w, io, cache_tmp, st, &nl);
+  if (rc) return rc;
   h->launches = nl;
   h->last_stream = st;
   h->launched = true;

@@ -168,3 +168,37 @@ def test_small_parity_surprise_ns(gpu_lib, name, readout):
             assert v <= tol, (k, v)
         if k.startswith("S"):
             assert v <= 5 * tol, (k, v)
+
+
+@pytest.mark.parametrize("name", ["atlas_poly_c4", "atlas_long", "atlas_muon_surprise"])
+def test_repeated_calls_replay_identically(gpu_lib, name):
+    """Identical repeated calls replay a captured CUDA graph of the launch
+    sequence: its results equal a direct run's bit for bit, and new data in
+    the same buffers is read."""
+    import torch
+    from test_learned_neural_gb300.runner import Memory, tensors_from_numpy
+    w = WORKLOADS[name].scaled(B=1, H=2, T=128)
+    inp = make_inputs(w)
+    mem = Memory(w)
+    t = tensors_from_numpy(inp)
+    out = mem.alloc_outputs(w.B, w.H, w.T, "cuda")
+    results = []
+    for _ in range(4):                       # direct, capture, replay, replay
+        mem.forward(t, out=out)
+        torch.cuda.synchronize()
+        results.append(out["y"].clone())
+    mem.status()
+    for r in results[1:]:
+        assert torch.equal(r, results[0])
+    with torch.no_grad():
+        t["q"].mul_(0.5)                     # new data, same buffer: replayed
+    mem.forward(t, out=out)
+    torch.cuda.synchronize()
+    fresh = Memory(w)
+    ref = fresh.forward(t)
+    torch.cuda.synchronize()
+    assert torch.equal(out["y"], ref["y"])
+    for m in range(len(ref["W"])):
+        assert torch.equal(out["W"][m], ref["W"][m])
+    mem.close()
+    fresh.close()
