@@ -29,6 +29,11 @@ struct atlas_mem_handle {
   // the second call with the same arguments (and workspace) captures the
   // launch sequence on a private stream, later ones launch the graph.
   cudaStream_t cap = nullptr;
+  // host-buffer calls on the fused path: unit groups on their own streams,
+  // so the copies of one group overlap the kernel of another
+  static const int kGroups = 4;
+  cudaStream_t pst[kGroups] = {};
+  cudaEvent_t pev[kGroups + 1] = {};
   cudaGraphExec_t gexec = nullptr;
   atlas_mem_io gkey{};    // arguments the graph was captured with
   void* gws = nullptr;
@@ -207,6 +212,10 @@ extern "C" void atlas_mem_destroy(atlas_mem_handle* h) {
   if (!h) return;
   if (h->gexec) cudaGraphExecDestroy(h->gexec);
   if (h->cap) cudaStreamDestroy(h->cap);
+  for (int i = 0; i < atlas_mem_handle::kGroups; ++i)
+    if (h->pst[i]) cudaStreamDestroy(h->pst[i]);
+  for (int i = 0; i <= atlas_mem_handle::kGroups; ++i)
+    if (h->pev[i]) cudaEventDestroy(h->pev[i]);
   if (h->ws) cudaFree(h->ws);
   if (h->stage) cudaFree(h->stage);
   delete h;
@@ -400,6 +409,69 @@ extern "C" int atlas_mem_status(atlas_mem_handle* h) {
   return ATLAS_OK;
 }
 
+struct Item {
+  const void* src;   // host source of an input, else nullptr
+  void* dst_host;    // host destination of an output, else nullptr
+  size_t bytes;
+};
+
+// Host-buffer forward on the fused path, pipelined over unit groups: group i
+// copies its slices in, runs the fused kernel on its units and copies its
+// outputs back, all on stream pst[i]; the copies of one group overlap the
+// kernels of the others.  items / dptr follow the order of
+// atlas_mem_forward_host (inputs q k v theta eta alpha gamma P W0[2] S0[2]
+// window[3], then outputs y W_out[2] S_out[2] window[3]).
+static int forward_host_pipelined(atlas_mem_handle* h, const atlas_mem_io* io, const Geom& g, const Item* items,
+                                  void* const* dptr, int n, cudaStream_t st) {
+  const int NG = atlas_mem_handle::kGroups;
+  const size_t U = (size_t)g.units, ug = U / NG;
+  const Layout L = layout(g, g.units, g.T);
+  int rc = ensure_workspace(h, L.total);
+  if (rc) return rc;
+  float* cache_tmp = nullptr;
+  Work w = work_from(g, h->ws, L, &cache_tmp);
+  h->status = w.status;
+  for (int i = 0; i < NG; ++i)
+    if (!h->pst[i]) CUDA_TRY(cudaStreamCreateWithFlags(&h->pst[i], cudaStreamNonBlocking));
+  for (int i = 0; i <= NG; ++i)
+    if (!h->pev[i]) CUDA_TRY(cudaEventCreateWithFlags(&h->pev[i], cudaEventDisableTiming));
+  CUDA_TRY(cudaEventRecord(h->pev[NG], st));
+  Geom gg = g;
+  gg.units = (int)ug;
+  for (int gi = 0; gi < NG; ++gi) {
+    cudaStream_t s = h->pst[gi];
+    CUDA_TRY(cudaStreamWaitEvent(s, h->pev[NG], 0));
+    // slice of array i for this group: bytes per unit = total / U
+    auto dev = [&](int i) -> char* {
+      return dptr[i] ? (char*)dptr[i] + gi * ug * (items[i].bytes / U) : nullptr;
+    };
+    for (int i = 0; i < n; ++i)
+      if (items[i].src && items[i].bytes) {
+        const size_t b = ug * (items[i].bytes / U);
+        CUDA_TRY(cudaMemcpyAsync(dev(i), (const char*)items[i].src + gi * b, b, cudaMemcpyHostToDevice, s));
+      }
+    const float* W0g[2] = {(const float*)dev(8), (const float*)dev(9)};
+    const float* S0g[2] = {(const float*)dev(10), (const float*)dev(11)};
+    float* Wog[2] = {(float*)dev(16), (float*)dev(17)};
+    float* Sog[2] = {(float*)dev(18), (float*)dev(19)};
+    CUDA_TRY(mlp_tc_launch(gg, dev(0), dev(1), dev(2), (const float*)dev(3), (const float*)dev(4),
+                           (const float*)dev(5), (const float*)dev(6), W0g, S0g, (float*)dev(15), Wog, Sog, w.status,
+                           s));
+    for (int i = 15; i < n; ++i)
+      if (items[i].dst_host && items[i].bytes) {
+        const size_t b = ug * (items[i].bytes / U);
+        CUDA_TRY(cudaMemcpyAsync((char*)items[i].dst_host + gi * b, dev(i), b, cudaMemcpyDeviceToHost, s));
+      }
+    CUDA_TRY(cudaEventRecord(h->pev[gi], s));
+    CUDA_TRY(cudaStreamWaitEvent(st, h->pev[gi], 0));
+  }
+  h->launches = NG;
+  h->last_stream = st;
+  h->launched = true;
+  CUDA_TRY(cudaStreamSynchronize(st));
+  return atlas_mem_status(h);
+}
+
 extern "C" int atlas_mem_forward_host(atlas_mem_handle* h, const atlas_mem_io* io, void* stream) {
   if (!h) return ATLAS_ERR_INVALID_ARG;
   int rc = check_io(h, io);
@@ -409,8 +481,7 @@ extern "C" int atlas_mem_forward_host(atlas_mem_handle* h, const atlas_mem_io* i
   const size_t U = (size_t)io->B * io->H, T = io->T;
   const size_t es = g.qkv_dtype == ATLAS_BF16 ? 2 : 4;
   const size_t ncache = (size_t)(g.c > 1 ? g.c - 1 : 0);
-  // staged arrays: {host pointer, bytes, is_output}
-  struct Item { const void* src; void* dst_host; size_t bytes; };
+  // staged arrays: host source (input) or destination (output), bytes
   Item items[24];
   int n = 0;
   auto in = [&](const void* p, size_t bytes) { items[n++] = Item{p, nullptr, p ? bytes : 0}; };
@@ -455,11 +526,19 @@ extern "C" int atlas_mem_forward_host(atlas_mem_handle* h, const atlas_mem_io* i
   }
   char* base = (char*)h->stage;
   void* dptr[24];
-  for (int i = 0; i < n; ++i) {
-    dptr[i] = items[i].bytes ? base + off[i] : nullptr;
+  for (int i = 0; i < n; ++i) dptr[i] = items[i].bytes ? base + off[i] : nullptr;
+  // fused path: pipeline over unit groups (every array but P is unit-major)
+  Geom gu = g;
+  gu.units = (int)U;
+  gu.T = (int)T;
+  gu.n_prev = io->win_len;
+  gu.L = gu.n_prev + gu.T;
+  const int NG = atlas_mem_handle::kGroups;
+  if (mlp_tc_supported(gu) && io->P == nullptr && U % NG == 0 && getenv("ATLAS_NO_PIPELINE") == nullptr)
+    return forward_host_pipelined(h, io, gu, items, dptr, n, st);
+  for (int i = 0; i < n; ++i)
     if (items[i].src && items[i].bytes)
       CUDA_TRY(cudaMemcpyAsync(dptr[i], items[i].src, items[i].bytes, cudaMemcpyHostToDevice, st));
-  }
   atlas_mem_io d = *io;
   int i = 0;
   d.q = dptr[i++]; d.k = dptr[i++]; d.v = dptr[i++];

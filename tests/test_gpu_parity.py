@@ -79,8 +79,11 @@ def test_split_continuation_matches_whole(gpu_lib, name):
     mem.close()
 
 
-def test_host_buffers_match_device_buffers(gpu_lib):
-    w = WORKLOADS["titans_mlp"].scaled(B=1, H=2, T=128)
+@pytest.mark.parametrize("H", [2, 4])
+def test_host_buffers_match_device_buffers(gpu_lib, H):
+    """Host-buffer entry point = device entry point, bit for bit; with 4
+    units the fused path's host call runs pipelined over unit groups."""
+    w = WORKLOADS["titans_mlp"].scaled(B=1, H=H, T=128)
     inp = make_inputs(w)
     d = run_gpu(w, inp)
     h = run_gpu(w, inp, host=True)
