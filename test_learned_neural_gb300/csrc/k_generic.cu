@@ -647,50 +647,61 @@ namespace atlas {
 template <int RPG>
 __global__ void __launch_bounds__(256) k_ns_scan_w1(Geom g, Chunk ch, Work w, int buf, size_t slot_stride,
                                                     const float* alpha, float* aq) {
-  __shared__ float part[8][33];
-  __shared__ float rq[64][RPG * 8 + 1];
+  // W1 decay scan fused with the hidden read-out.  Thread (grp, lane) keeps
+  // rows [grp RPG, grp RPG + RPG) of column jb + lane of W1.  The U_t of
+  // PD tokens are loaded together; each token's partial dot products go to
+  // shared memory and are summed over the 8 row groups once at the end, so
+  // the token loop has no barrier.
+  constexpr int PD = 4;
+  extern __shared__ float scan_sm[];
   const int u = blockIdx.y, jb = blockIdx.x * 32;
   const int lane = threadIdx.x % 32, grp = threadIdx.x / 32;
   const int F = g.F, h = g.hidden, j = jb + lane, i0 = grp * RPG;
   const int Ct = ch.e - ch.s;
   const bool pre = g.readout == ATLAS_READOUT_PRE;   // read out before token r's update
-  // queries of the chunk
-  for (int e = threadIdx.x; e < Ct * F; e += 256) rq[e / F][e % F] = w.R[((size_t)u * g.T + ch.s + e / F) * F + e % F];
+  float* rq = scan_sm;                   // [C][F + 1] queries of the chunk
+  float* part = rq + g.C * (F + 1);      // [C][8][33] per-group partial sums
+  float* bes = part + g.C * 8 * 33;      // [C] 1 - alpha
+  for (int e = threadIdx.x; e < Ct * F; e += 256)
+    rq[(e / F) * (F + 1) + e % F] = w.R[((size_t)u * g.T + ch.s + e / F) * F + e % F];
+  for (int r = threadIdx.x; r < Ct; r += 256) bes[r] = 1.f - alpha[(size_t)u * g.T + ch.s + r];
   float W[RPG];
   const float* Wb = w.Wst[buf][0] + (size_t)u * F * h;
 #pragma unroll
   for (int q = 0; q < RPG; ++q) W[q] = Wb[(size_t)(i0 + q) * h + j];
   __syncthreads();
-  const float* slot0 = w.Ubuf + (size_t)u * g.C * slot_stride;
-  float nxt[RPG];
+  const float* slot0 = w.Ubuf + (size_t)u * g.C * slot_stride + (size_t)i0 * h + j;
+  for (int r0 = 0; r0 < Ct; r0 += PD) {
+    float cur[PD][RPG];
 #pragma unroll
-  for (int q = 0; q < RPG; ++q) nxt[q] = slot0[(size_t)(i0 + q) * h + j];
-  for (int r = 0; r < Ct; ++r) {
-    float cur[RPG];
+    for (int p = 0; p < PD; ++p) {
+      const float* sl = slot0 + (size_t)(r0 + p) * slot_stride;
 #pragma unroll
-    for (int q = 0; q < RPG; ++q) cur[q] = nxt[q];
-    if (r + 1 < Ct) {   // next token's U in flight while this one is used
-      const float* sl = slot0 + (size_t)(r + 1) * slot_stride;
-#pragma unroll
-      for (int q = 0; q < RPG; ++q) nxt[q] = sl[(size_t)(i0 + q) * h + j];
+      for (int q = 0; q < RPG; ++q) cur[p][q] = r0 + p < Ct ? sl[(size_t)q * h] : 0.f;
     }
-    const float be = 1.f - alpha[(size_t)u * g.T + ch.s + r];
+#pragma unroll
+    for (int p = 0; p < PD; ++p) {
+      const int r = r0 + p;
+      if (r >= Ct) break;
+      const float be = bes[r];
+      const float* rr = rq + r * (F + 1) + i0;
+      float z = 0.f;
+#pragma unroll
+      for (int q = 0; q < RPG; ++q) {
+        if (pre) z += rr[q] * W[q];
+        W[q] = be * W[q] + cur[p][q];
+        if (!pre) z += rr[q] * W[q];
+      }
+      part[(r * 8 + grp) * 33 + lane] = z;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < Ct * 32; e += 256) {
+    const int r = e >> 5, l = e & 31;
     float z = 0.f;
 #pragma unroll
-    for (int q = 0; q < RPG; ++q) {
-      if (pre) z += rq[r][i0 + q] * W[q];
-      W[q] = be * W[q] + cur[q];
-      if (!pre) z += rq[r][i0 + q] * W[q];
-    }
-    part[grp][lane] = z;
-    __syncthreads();
-    if (grp == 0) {
-      float s = 0.f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) s += part[k][lane];
-      aq[((size_t)u * g.C + r) * h + j] = siluf_(s);
-    }
-    __syncthreads();
+    for (int k = 0; k < 8; ++k) z += part[(r * 8 + k) * 33 + l];
+    aq[((size_t)u * g.C + r) * h + jb + l] = siluf_(z);
   }
   float* Wo = w.Wst[buf ^ 1][0] + (size_t)u * F * h;
 #pragma unroll
@@ -703,45 +714,65 @@ __global__ void __launch_bounds__(256) k_ns_scan_w1(Geom g, Chunk ch, Work w, in
 template <int CPL>
 __global__ void __launch_bounds__(256) k_ns_scan_w2(Geom g, Chunk ch, Work w, int buf, size_t slot_stride,
                                                     const float* alpha, const float* aq, float* y) {
-  extern __shared__ float aqs[];   // [Ct][h]
+  // W2 decay scan fused with the output read-out.  Warp = output column k,
+  // lane = CPL hidden entries; the U_t of PD tokens are loaded together and
+  // their PD warp reductions interleave.
+  constexpr int PD = 4;
+  extern __shared__ float aqs[];   // [Ct][h], then [Ct] 1 - alpha
   const int u = blockIdx.y;
   const int lane = threadIdx.x % 32, k = blockIdx.x * 8 + threadIdx.x / 32;
   const int F = g.F, h = g.hidden, d = g.d_v, j0 = lane * CPL;
   const int Ct = ch.e - ch.s;
   const bool pre = g.readout == ATLAS_READOUT_PRE;   // read out before token r's update
+  float* bes = aqs + Ct * h;
   for (int e = threadIdx.x; e < Ct * h; e += 256) aqs[e] = aq[(size_t)u * g.C * h + e];
+  for (int r = threadIdx.x; r < Ct; r += 256) bes[r] = 1.f - alpha[(size_t)u * g.T + ch.s + r];
   float W[CPL];
   const float* Wb = w.Wst[buf][1] + (size_t)u * h * d;   // original orientation [h][d]
 #pragma unroll
   for (int q = 0; q < CPL; ++q) W[q] = Wb[(size_t)(j0 + q) * d + k];
   __syncthreads();
   const float* slot0 = w.Ubuf + (size_t)u * g.C * slot_stride + (size_t)F * h + (size_t)k * h + j0;
-  float nxt[CPL];
+  for (int r0 = 0; r0 < Ct; r0 += PD) {
+    float cur[PD][CPL];
 #pragma unroll
-  for (int q = 0; q < CPL; q += 4) *reinterpret_cast<float4*>(nxt + q) = *reinterpret_cast<const float4*>(slot0 + q);
-  for (int r = 0; r < Ct; ++r) {
-    float cur[CPL];
+    for (int p = 0; p < PD; ++p) {
+      const float* sl = slot0 + (size_t)(r0 + p) * slot_stride;
 #pragma unroll
-    for (int q = 0; q < CPL; ++q) cur[q] = nxt[q];
-    if (r + 1 < Ct) {
-      const float* sl = slot0 + (size_t)(r + 1) * slot_stride;
-#pragma unroll
-      for (int q = 0; q < CPL; q += 4) *reinterpret_cast<float4*>(nxt + q) = *reinterpret_cast<const float4*>(sl + q);
+      for (int q = 0; q < CPL; q += 4) {
+        const float4 v4 = r0 + p < Ct ? *reinterpret_cast<const float4*>(sl + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+        cur[p][q] = v4.x; cur[p][q + 1] = v4.y; cur[p][q + 2] = v4.z; cur[p][q + 3] = v4.w;
+      }
     }
-    const float be = 1.f - alpha[(size_t)u * g.T + ch.s + r];
-    float acc = 0.f;
+    float acc[PD];
 #pragma unroll
-    for (int q = 0; q < CPL; ++q) {
-      if (pre) acc += aqs[r * h + j0 + q] * W[q];
-      W[q] = be * W[q] + cur[q];
-      if (!pre) acc += aqs[r * h + j0 + q] * W[q];
+    for (int p = 0; p < PD; ++p) {
+      const int r = r0 + p < Ct ? r0 + p : Ct - 1;
+      const float be = bes[r];
+      float a = 0.f;
+#pragma unroll
+      for (int q = 0; q < CPL; ++q) {
+        if (r0 + p < Ct) {
+          if (pre) a += aqs[r * h + j0 + q] * W[q];
+          W[q] = be * W[q] + cur[p][q];
+          if (!pre) a += aqs[r * h + j0 + q] * W[q];
+        }
+      }
+      acc[p] = a;
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) {
-      const size_t yi = ((size_t)u * g.T + ch.s + r) * d + k;
-      y[yi] = w.R[((size_t)u * g.T + ch.s + r) * F + k] + acc;
-    }
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int p = 0; p < PD; ++p) acc[p] += __shfl_xor_sync(0xffffffffu, acc[p], o);
+    if (lane == 0)
+#pragma unroll
+      for (int p = 0; p < PD; ++p) {
+        const int r = r0 + p;
+        if (r < Ct) {
+          const size_t yi = ((size_t)u * g.T + ch.s + r) * d + k;
+          y[yi] = w.R[((size_t)u * g.T + ch.s + r) * F + k] + acc[p];
+        }
+      }
   }
   float* Wo = w.Wst[buf ^ 1][1] + (size_t)u * h * d;
 #pragma unroll
@@ -763,9 +794,15 @@ cudaError_t ns_fused_scan(const Geom& g, const Chunk& ch, const Work& w, int buf
                           const float* alpha, float* aq, float* y, cudaStream_t st) {
   const int F = g.F, h = g.hidden, d = g.d_v;
   dim3 g1(h / 32, g.units);
-  if (F / 8 == 8) k_ns_scan_w1<8><<<g1, 256, 0, st>>>(g, ch, w, buf, slot_stride, alpha, aq);
-  else k_ns_scan_w1<16><<<g1, 256, 0, st>>>(g, ch, w, buf, slot_stride, alpha, aq);
-  const size_t sm2 = (size_t)(ch.e - ch.s) * h * sizeof(float);
+  const size_t sm1 = ((size_t)g.C * (F + 1) + (size_t)g.C * 8 * 33 + g.C) * sizeof(float);
+  if (F / 8 == 8) {
+    cudaFuncSetAttribute(k_ns_scan_w1<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1);
+    k_ns_scan_w1<8><<<g1, 256, sm1, st>>>(g, ch, w, buf, slot_stride, alpha, aq);
+  } else {
+    cudaFuncSetAttribute(k_ns_scan_w1<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1);
+    k_ns_scan_w1<16><<<g1, 256, sm1, st>>>(g, ch, w, buf, slot_stride, alpha, aq);
+  }
+  const size_t sm2 = ((size_t)(ch.e - ch.s) * h + (ch.e - ch.s)) * sizeof(float);
   dim3 g2(d / 8, g.units);
   if (h / 32 == 8) {
     cudaFuncSetAttribute(k_ns_scan_w2<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);
