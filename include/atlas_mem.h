@@ -63,7 +63,8 @@ typedef struct {
     int d_k;        /* key/query width before the feature map */
     int d_v;        /* value width; depth 2 needs F == d_v (residual) */
     int hidden;     /* MLP hidden width (depth 2), else ignored */
-    int C;          /* tokens per chunk; gradients use the chunk-start weights */
+    int C;          /* tokens per chunk (C + c - 1 <= 1024, else UNSUPPORTED);
+                     * gradients use the chunk-start weights */
     int c;          /* Omega window: the last c tokens, including t (c >= 1) */
     int p;          /* polynomial degree of the feature map: 1 or 2 */
     int proj_dim;   /* 0: no projection; else features are x P, P [poly_dim, proj_dim] */

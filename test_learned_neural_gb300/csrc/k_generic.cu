@@ -148,15 +148,23 @@ __global__ void k_grad(Geom g, Chunk ch, Work w, int buf) {
 // One block per unit, one thread per window row (plus thread 0 for the
 // per-token products).  Sequential over the tokens of the chunk.
 __global__ void k_coef(Geom g, Chunk ch, const float* theta, const float* eta, const float* alpha, Work w) {
+  // the chunk's gates in shared memory first: the scans below then run
+  // without a global-memory round trip per token
+  extern __shared__ float gates[];   // [3][C]: theta, eta, 1 - alpha
   const int u = blockIdx.x;
   const int i = threadIdx.x;
+  const int Ct = ch.e - ch.s;
+  for (int r = threadIdx.x; r < Ct; r += blockDim.x) {
+    gates[r] = theta[(size_t)u * g.T + ch.s + r];
+    gates[g.C + r] = eta[(size_t)u * g.T + ch.s + r];
+    gates[2 * g.C + r] = 1.f - alpha[(size_t)u * g.T + ch.s + r];
+  }
+  __syncthreads();
   const int ti = ch.lo + i;  // token index of window row i (may be < 0: cached)
   float cs = 0.f, cw = 0.f, Ap = 1.f, Bp = 1.f, Dp = 0.f;
-  for (int t = ch.s; t < ch.e; ++t) {
-    const float th = theta[(size_t)u * g.T + t];
-    const float et = eta[(size_t)u * g.T + t];
-    const float be = 1.f - alpha[(size_t)u * g.T + t];
-    const int r = t - ch.s;
+  for (int r = 0; r < Ct; ++r) {
+    const int t = ch.s + r;
+    const float th = gates[r], et = gates[g.C + r], be = gates[2 * g.C + r];
     if (i < ch.nw) {
       const bool in_win = ti <= t && t <= ti + g.c - 1;
       cs = et * cs + (in_win ? th : 0.f);
@@ -568,7 +576,7 @@ cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const G
   if (g.ns_iters > 0 && g.ns_target == ATLAS_NS_SURPRISE) {
     CUDA_CHECK_RET(grad_tiled_or_rows(g, ch, w, buf, st, nl));
     const int coef_threads = ((ch.nw + 31) / 32) * 32;
-    k_coef<<<g.units, coef_threads, 0, st>>>(g, ch, io.theta, io.eta, io.alpha, w);
+    k_coef<<<g.units, coef_threads, 3 * g.C * sizeof(float), st>>>(g, ch, io.theta, io.eta, io.alpha, w);
     *nl += 2;
     return surprise_chunk(g, ch, w, io.theta, io.eta, io.alpha, io.y, buf, st, nl);
   }
@@ -582,7 +590,7 @@ cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const G
     k_grad<<<dim3(ch.nw, g.units), 256, sg, st>>>(g, ch, w, buf);
   }
   const int coef_threads = ((ch.nw + 31) / 32) * 32;
-  k_coef<<<g.units, coef_threads, 0, st>>>(g, ch, io.theta, io.eta, io.alpha, w);
+  k_coef<<<g.units, coef_threads, 3 * g.C * sizeof(float), st>>>(g, ch, io.theta, io.eta, io.alpha, w);
   if (g.ns_iters == 0) {
     cudaFuncSetAttribute(k_dual_readout, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sr);
     k_dual_readout<<<dim3(ch.e - ch.s, g.units), 256, sr, st>>>(g, ch, w, buf, io.y);

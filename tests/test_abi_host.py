@@ -52,6 +52,7 @@ def _cfg(**kw):
     (dict(p=3), tln.ATLAS_ERR_INVALID_ARG),
     (dict(qkv_dtype=7), tln.ATLAS_ERR_INVALID_ARG),
     (dict(readout=5), tln.ATLAS_ERR_INVALID_ARG),
+    (dict(C=2048), tln.ATLAS_ERR_UNSUPPORTED),            # window rows > 1024
     (dict(ns_target=3), tln.ATLAS_ERR_INVALID_ARG),
     (dict(ns_target=1, ns_iters=5, c=40), tln.ATLAS_ERR_INVALID_ARG),
     (dict(C=1000, c=100), tln.ATLAS_ERR_UNSUPPORTED),     # window rows > 1024
