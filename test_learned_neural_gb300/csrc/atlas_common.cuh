@@ -92,7 +92,6 @@ cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const G
                           cudaStream_t st, int* nl);
 cudaError_t generic_cache_out(const Geom& g, const GenericIO& io, float* tmp, void* k_out, void* v_out,
                               float* g_out, cudaStream_t st, int* nl);
-size_t generic_smem_grad(const Geom& g);
 size_t generic_smem_readout(const Geom& g);
 size_t generic_smem_ns(const Geom& g, int m);
 size_t grad_part_floats(const Geom& g);

@@ -103,7 +103,7 @@ static int derive_geom(const atlas_mem_config& c, Geom* g, char* why, size_t why
   if (g->Kw > 1024) BAD("C + c - 1 = %d > 1024 window rows per chunk is not supported", g->Kw);
   g->poly = (int)poly;
   g->F = (int)F;
-  if (generic_smem_grad(*g) > kSmemLimit || generic_smem_readout(*g) > kSmemLimit)
+  if (generic_smem_readout(*g) > kSmemLimit)
     BAD("memory widths too large for the on-chip working set");
   if ((size_t)(c.d_k + (c.proj_dim ? poly : 0)) * 4 > kSmemLimit) BAD("feature map too wide");
   if (c.ns_iters > 0 && c.ns_target == ATLAS_NS_MOMENTUM)

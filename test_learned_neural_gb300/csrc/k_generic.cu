@@ -92,57 +92,6 @@ __global__ void k_values(Geom g, const void* v, const void* win_v, const float* 
   }
 }
 
-// --------------------------------------------------------------------- grad
-// One block per (window row, unit).  Gradient factors at Wbar.
-__global__ void k_grad(Geom g, Chunk ch, Work w, int buf) {
-  extern __shared__ float sm[];
-  const int u = blockIdx.y, i = blockIdx.x;
-  const size_t key_row = (size_t)(ch.lo + g.n_prev + i);
-  const float* x = w.X + ((size_t)u * g.L + key_row) * g.F;
-  const float* v = w.V + ((size_t)u * g.L + key_row) * g.d_v;
-  const float gam = w.G[(size_t)u * g.L + key_row];
-  float* xs = sm;                 // F
-  float* dys = sm + g.F;          // d_v
-  for (int f = threadIdx.x; f < g.F; f += blockDim.x) xs[f] = x[f];
-  __syncthreads();
-  const size_t rowKw = (size_t)u * g.Kw + i;
-  if (g.depth == 1) {
-    const float* W = w.Wst[buf][0] + (size_t)u * g.F * g.d_v;
-    for (int k = threadIdx.x; k < g.d_v; k += blockDim.x) {
-      float acc = 0.f;
-      for (int f = 0; f < g.F; ++f) acc += xs[f] * W[(size_t)f * g.d_v + k];
-      w.DY[rowKw * g.d_v + k] = 2.f * gam * (acc - v[k]);
-    }
-    return;
-  }
-  const int h = g.hidden;
-  float* zs = dys + g.d_v;        // h
-  float* as = zs + h;             // h
-  const float* W1 = w.Wst[buf][0] + (size_t)u * g.F * h;
-  const float* W2 = w.Wst[buf][1] + (size_t)u * h * g.d_v;
-  for (int j = threadIdx.x; j < h; j += blockDim.x) {
-    float acc = 0.f;
-    for (int f = 0; f < g.F; ++f) acc += xs[f] * W1[(size_t)f * h + j];
-    zs[j] = acc;
-    as[j] = siluf_(acc);
-    w.Zpre[rowKw * h + j] = acc;
-    w.Aact[rowKw * h + j] = as[j];
-  }
-  __syncthreads();
-  for (int k = threadIdx.x; k < g.d_v; k += blockDim.x) {
-    float acc = xs[k];  // residual (F == d_v)
-    for (int j = 0; j < h; ++j) acc += as[j] * W2[(size_t)j * g.d_v + k];
-    float dy = 2.f * gam * (acc - v[k]);
-    dys[k] = dy;
-    w.DY[rowKw * g.d_v + k] = dy;
-  }
-  __syncthreads();
-  for (int j = threadIdx.x; j < h; j += blockDim.x) {
-    float acc = 0.f;
-    for (int k = 0; k < g.d_v; ++k) acc += dys[k] * W2[(size_t)j * g.d_v + k];
-    w.DZ[rowKw * h + j] = acc * dsiluf_(zs[j]);
-  }
-}
 
 // --------------------------------------------------------------------- coef
 // One block per unit, one thread per window row (plus thread 0 for the
@@ -540,9 +489,6 @@ cudaError_t generic_prepare(const Geom& g, const Work& w, const GenericIO& io, c
 
 // Shared-memory bytes each generic kernel needs (checked against the device
 // limit on the host before launching).
-size_t generic_smem_grad(const Geom& g) {
-  return (size_t)(g.F + g.d_v + (g.depth == 2 ? 2 * g.hidden : 0)) * sizeof(float);
-}
 size_t generic_smem_readout(const Geom& g) {
   return (size_t)(g.F + 2 * g.Kw + (g.depth == 2 ? g.hidden : 0)) * sizeof(float);
 }
@@ -559,22 +505,12 @@ bool ns_fused_scan_supported(const Geom& g);
 cudaError_t ns_fused_scan(const Geom& g, const Chunk& ch, const Work& w, int buf, size_t slot_stride,
                           const float* alpha, float* aq, float* y, cudaStream_t st);
 
-// window-row gradient factors at the chunk-start weights: tiled kernels
-// where they fit, one block per window row otherwise
-static cudaError_t grad_tiled_or_rows(const Geom& g, const Chunk& ch, const Work& w, int buf, cudaStream_t st,
-                                      int* nl) {
-  if (g.depth == 1 || ch.nw <= 128) return grad_tiled(g, ch, w, buf, st, nl);
-  const size_t sg = generic_smem_grad(g);
-  cudaFuncSetAttribute(k_grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg);
-  k_grad<<<dim3(ch.nw, g.units), 256, sg, st>>>(g, ch, w, buf);
-  return cudaGetLastError();
-}
 
 cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const GenericIO& io, int buf,
                           cudaStream_t st, int* nl) {
   if (dual1_split_supported(g)) return dual1_split(g, ch, w, io, buf, st, nl);
   if (g.ns_iters > 0 && g.ns_target == ATLAS_NS_SURPRISE) {
-    CUDA_CHECK_RET(grad_tiled_or_rows(g, ch, w, buf, st, nl));
+    CUDA_CHECK_RET(grad_tiled(g, ch, w, buf, st, nl));
     const int coef_threads = ((ch.nw + 31) / 32) * 32;
     k_coef<<<g.units, coef_threads, 3 * g.C * sizeof(float), st>>>(g, ch, io.theta, io.eta, io.alpha, w);
     *nl += 2;
@@ -582,13 +518,7 @@ cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const G
   }
   *nl += g.ns_iters == 0 ? 3 + g.nmat : 3 + 2 * g.nmat;
   const size_t sr = generic_smem_readout(g);
-  if (g.depth == 1 || ch.nw <= 128) {
-    CUDA_CHECK_RET(grad_tiled(g, ch, w, buf, st, nl));
-  } else {
-    const size_t sg = generic_smem_grad(g);
-    cudaFuncSetAttribute(k_grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg);
-    k_grad<<<dim3(ch.nw, g.units), 256, sg, st>>>(g, ch, w, buf);
-  }
+  CUDA_CHECK_RET(grad_tiled(g, ch, w, buf, st, nl));
   const int coef_threads = ((ch.nw + 31) / 32) * 32;
   k_coef<<<g.units, coef_threads, 3 * g.C * sizeof(float), st>>>(g, ch, io.theta, io.eta, io.alpha, w);
   if (g.ns_iters == 0) {
@@ -829,7 +759,7 @@ namespace atlas {
 // --------------------------------------------- tiled gradient factors
 // The window rows' forward, error and backward at the chunk-start weights
 // as 64 x 64 register-tiled fp32 GEMMs (tile_gemm), one CTA per (unit,
-// 64-wide output block).  Same outputs as k_grad.
+// 64-wide output block).
 
 // depth 1: dy = 2 gamma (X W - V)
 __global__ void __launch_bounds__(256) k_grad1_tiled(Geom g, Chunk ch, Work w, int buf) {
@@ -854,47 +784,49 @@ __global__ void __launch_bounds__(256) k_grad1_tiled(Geom g, Chunk ch, Work w, i
 
 // depth 2, part 1: Z = X W1[:, jb] -> z, a = SiLU(z); partial Yhat = a W2[jb, :]
 __global__ void __launch_bounds__(256) k_grad2_fwd(Geom g, Chunk ch, Work w, int buf, float* part) {
+  // one CTA per (64 hidden units, 64 window rows, unit): Z and A of its
+  // tile, then its hidden block's partial forward output A W2
   __shared__ float As[16 * 64], Bs[16 * 64];
-  __shared__ float Ablk[128 * 65];
-  const int u = blockIdx.y, jb = blockIdx.x * 64, h = g.hidden;
+  __shared__ float Ablk[64 * 65];
+  const int u = blockIdx.z, i0 = blockIdx.y * 64, jb = blockIdx.x * 64, h = g.hidden;
   const float* Xw = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * g.F;
   const float* W1 = w.Wst[buf][0] + (size_t)u * g.F * h;
   const float* W2 = w.Wst[buf][1] + (size_t)u * h * g.d_v;
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  for (int i0 = 0; i0 < ch.nw; i0 += 64) {
+  const int hb = h - jb < 64 ? h - jb : 64;
+  {
     float acc[4][4];
-    tile_gemm(TileOp{Xw, g.F, 1}, TileOp{W1 + jb, 1, h}, ch.nw, h - jb < 64 ? h - jb : 64, g.F, i0, 0, acc, As, Bs);
+    tile_gemm(TileOp{Xw, g.F, 1}, TileOp{W1 + jb, 1, h}, ch.nw, hb, g.F, i0, 0, acc, As, Bs);
     for (int a = 0; a < 4; ++a) {
-      const int i = i0 + ty * 4 + a;
+      const int il = ty * 4 + a, i = i0 + il;
       for (int b = 0; b < 4; ++b) {
         const int j = tx * 4 + b;
         const float z = acc[a][b];
         const float av = siluf_(z);
-        if (i < ch.nw && jb + j < h) {
+        if (i < ch.nw && j < hb) {
           const size_t o = ((size_t)u * g.Kw + i) * h + jb + j;
           w.Zpre[o] = z;
           w.Aact[o] = av;
         }
-        Ablk[i * 65 + j] = (i < ch.nw && jb + j < h) ? av : 0.f;
+        Ablk[il * 65 + j] = (i < ch.nw && j < hb) ? av : 0.f;
       }
     }
   }
   __syncthreads();
   const int nb = (h + 63) / 64;
-  for (int i0 = 0; i0 < ch.nw; i0 += 64)
-    for (int j0 = 0; j0 < g.d_v; j0 += 64) {
-      float acc[4][4];
-      tile_gemm(TileOp{Ablk, 65, 1}, TileOp{W2 + (size_t)jb * g.d_v, 1, g.d_v}, ch.nw, g.d_v, h - jb < 64 ? h - jb : 64,
-                i0, j0, acc, As, Bs);
-      for (int a = 0; a < 4; ++a) {
-        const int i = i0 + ty * 4 + a;
-        if (i >= ch.nw) continue;
-        for (int b = 0; b < 4; ++b) {
-          const int j = j0 + tx * 4 + b;
-          if (j < g.d_v) part[(((size_t)u * nb + blockIdx.x) * g.Kw + i) * g.d_v + j] = acc[a][b];
-        }
+  for (int j0 = 0; j0 < g.d_v; j0 += 64) {
+    float acc[4][4];
+    tile_gemm(TileOp{Ablk, 65, 1}, TileOp{W2 + (size_t)jb * g.d_v, 1, g.d_v}, ch.nw - i0, g.d_v, hb, 0, j0, acc, As,
+              Bs);
+    for (int a = 0; a < 4; ++a) {
+      const int i = i0 + ty * 4 + a;
+      if (i >= ch.nw) continue;
+      for (int b = 0; b < 4; ++b) {
+        const int j = j0 + tx * 4 + b;
+        if (j < g.d_v) part[(((size_t)u * nb + blockIdx.x) * g.Kw + i) * g.d_v + j] = acc[a][b];
       }
     }
+  }
 }
 
 // depth 2, part 2: dy = 2 gamma (X + sum of partials - V)
@@ -944,9 +876,8 @@ cudaError_t grad_tiled(const Geom& g, const Chunk& ch, const Work& w, int buf, c
     k_grad1_tiled<<<dim3((g.d_v + 63) / 64, rt, g.units), 256, 0, st>>>(g, ch, w, buf);
     return cudaGetLastError();
   }
-  if (ch.nw > 128) return cudaErrorInvalidValue;   // Ablk holds 128 window rows
   const int nb = (g.hidden + 63) / 64;
-  k_grad2_fwd<<<dim3(nb, g.units), 256, 0, st>>>(g, ch, w, buf, w.gpart);
+  k_grad2_fwd<<<dim3(nb, rt, g.units), 256, 0, st>>>(g, ch, w, buf, w.gpart);
   k_grad2_dy<<<dim3(4, g.units), 256, 0, st>>>(g, ch, w, w.gpart);
   k_grad2_dz<<<dim3(nb, rt, g.units), 256, 0, st>>>(g, ch, w, buf);
   *nl += 2;
