@@ -58,6 +58,7 @@ constexpr int ORB = OSP + TILE, ORD = ORB + TILE;                 // B_t r_t, D_
 constexpr int OM = ORD + TILE, OAQ = OM + TILE;                   // M1, later M2; SiLU(Zq)
 constexpr int ODZS = OAQ + TILE, ODYS = ODZS + 2 * TILE;          // [cs.dz | cw.dz], [cs.dy | cw.dy]
 constexpr int CWM = ODYS + 2 * TILE;                              // fp32 Cw[t][i], by chunk parity
+constexpr int OBRN = ODZS, ODRN = ODZS + TILE;                    // next chunk's B_t r_t, D_t r_t (in ODZS)
 constexpr int RED = CWM + 2 * F32T;                               // Yp slots, Yq slots (cluster-shared)
 constexpr int VEC = RED + 2 * F32T;                               // gate vectors, by chunk parity
 constexpr int VECN = 12 * 64;                                     // floats per gate-vector buffer
@@ -72,7 +73,10 @@ constexpr int V_TH = 0, V_ET = 64, V_BE = 128, V_GA = 192, V_AP = 256, V_BP = 32
 constexpr int V_BR = 576, V_DR = 640;
 
 // TMEM columns of the accumulators (lanes 0-15 of each sub-partition)
-constexpr uint32_t C_Z = 0, C_YP = 64, C_G1 = 128, C_ZQ = 192, C_ST1 = 256, C_ST2 = 384;
+constexpr uint32_t C_Z = 0, C_YP = 64, C_ZQ = 192, C_ST1 = 256, C_ST2 = 384;
+// G1 of the next chunk is formed after this chunk's W1 state update, in the
+// columns of the consumed W1 corrections
+constexpr uint32_t C_G1 = C_ST1;
 constexpr uint32_t C_G2 = 64, C_YQ = 128;   // reuse after Yp, G1 are consumed
 // TMEM columns of the fp32 state (lanes 16-31 of each sub-partition)
 constexpr uint32_t S_W1 = 0, S_S1 = 64, S_W2 = 128, S_S2 = 192;
@@ -452,7 +456,9 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     }
   };
 
-  // (B R), (D R): the read-out's state terms of buffer bn's chunk
+  // (B R), (D R): the read-out's state terms of buffer bn's chunk, into the
+  // two 64-column tiles at ODZS (free from the corrections product of the
+  // current chunk until the Yq staging at its end)
   auto brdr = [&](int bn) {
     const float* vb = vecb(bn);
     const int r = tid % 64, g = tid / 64;
@@ -463,8 +469,8 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       ld_h8(sm + OR_, RGS, r, cc, x);
 #pragma unroll
       for (int i = 0; i < 8; ++i) { b8[i] = Bt * x[i]; d8[i] = Dt * x[i]; }
-      st_h8(sm + ORB, RGS, r, cc, b8);
-      st_h8(sm + ORD, RGS, r, cc, d8);
+      st_h8(sm + OBRN, RGS, r, cc, b8);
+      st_h8(sm + ODRN, RGS, r, cc, d8);
     }
   };
 
@@ -501,7 +507,13 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   __syncthreads();
   brdr(0);
   sync_smem_for_mma();
-  if (tid == 0 && cx.ok) mma64(tb + C_Z, sm + OX0, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
+  if (tid == 0 && cx.ok) {
+    mma64(tb + C_Z, sm + OX0, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
+    mma64(tb + C_G1, sm + OR_, 0, RGS, sm + OX0, 0, RGS, 64, 64, false);
+    mma64(tb + C_ZQ, sm + OBRN, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
+    mma64(tb + C_ZQ, sm + ODRN, 0, RGS, sm + OS1, 1, RGS, 64, 64, true);
+  }
+  commit_wait(cx);
 
   // Software pipeline: a chunk starts with its X, R, gates, gate scans,
   // (B R), (D R) in shared memory and Z = X W1q issued; the next chunk's
@@ -513,12 +525,8 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     const float* cwc = cwmb(b);
     const uint8_t* oxc = sm + (b ? OX1 : OX0);
     // ---------------------------------------------------------------- 1: G1, Zq state terms
-    if (tid == 0 && cx.ok) {
-      mma64(tb + C_G1, sm + OR_, 0, RGS, oxc, 0, RGS, 64, 64, false);
-      mma64(tb + C_ZQ, sm + ORB, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
-      mma64(tb + C_ZQ, sm + ORD, 0, RGS, sm + OS1, 1, RGS, 64, 64, true);
-    }
-    commit_wait(cx);
+    // Z, G1 and Zq's state terms were formed with the previous chunk's tail
+    // (or before the loop) and waited for there
     {
       float z[16], g[16];
       tc::tmem_ld16_x2(tb + lb + C_Z, z);
@@ -673,6 +681,8 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     }
     // W1, S1 are no longer read by this chunk's products
     state_update(vb, C_ST1, S_W1, S_S1, OW1, OS1);
+    // the corrections product has read ODZS: the next chunk's (B R), (D R)
+    if (has_next) brdr(b ^ 1);
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 5: G2, Yq state terms
     // and the next chunk's Z = X' W1q (W1 is final for this chunk)
@@ -680,7 +690,14 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       mma64(tb + C_G2, sm + OAQ, 0, RGS, sm + OA, 0, RGS, 64, 64, false);
       mma64(tb + C_YQ, sm + ORB, 0, RGS, sm + OW2, 1, RGS, 64, 64, false);
       mma64(tb + C_YQ, sm + ORD, 0, RGS, sm + OS2, 1, RGS, 64, 64, true);
-      if (has_next) mma64(tb + C_Z, sm + (b ? OX0 : OX1), 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
+      if (has_next) {
+        // the next chunk's first products: W1, S1 are final for this chunk
+        const uint8_t* oxn = sm + (b ? OX0 : OX1);
+        mma64(tb + C_Z, oxn, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
+        mma64(tb + C_G1, sm + OR_, 0, RGS, oxn, 0, RGS, 64, 64, false);
+        mma64(tb + C_ZQ, sm + OBRN, 0, RGS, sm + OW1, 1, RGS, 64, 64, false);
+        mma64(tb + C_ZQ, sm + ODRN, 0, RGS, sm + OS1, 1, RGS, 64, 64, true);
+      }
     }
     commit_wait(cx);
     {
@@ -700,8 +717,6 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     if (tid == 0 && cx.ok) mma64(tb + C_YQ, sm + OM, 0, RGS, sm + ODY, 1, RGS, 64, 64, true);
     // W2, S2 are no longer read by this chunk's products (overlaps the last one)
     state_update(vb, C_ST2, S_W2, S_S2, OW2, OS2);
-    // the next chunk's (B R), (D R): this chunk's B aq, D aq products are done
-    if (has_next) brdr(b ^ 1);
     commit_wait(cx);
     stage_slices(C_YQ, F32T);
     if (tid == 0 && cx.ok) send_slices(F32T, 2);
