@@ -69,7 +69,6 @@ struct Work {
   float* Bp;      // [units][C]  prod (1 - alpha) (s..t)
   float* Dp;      // [units][C]  coefficient of S_bar in W_t
   float* Ubuf;    // NS path: [units][C][sum_m rows*cols] U_t then W_t (X orientation)
-  float* xch;     // (unused: the CTA pairs exchange over DSMEM)
   float* gpart;   // depth 2: per hidden block partial forward outputs [units][h/64][Kw][d_v];
                   // depth 1: cs_e dy and cw_e dy [units][2][Kw][d_v], then per
                   // (unit, 64-feature slice) partial products R W, R S, R X^T, X W,
@@ -112,7 +111,6 @@ cudaError_t mlp_tc_launch(const Geom& g, const void* q, const void* k, const voi
 
 // tensor-core Newton-Schulz (k_ns_tc.cu)
 bool ns_tc_supported(const Geom& g);
-size_t ns_tc_xch_floats(const Geom& g, int num_sms);
 cudaError_t ns_tc_state_in(const Geom& g, int m, const float* src, float* dst, cudaStream_t st);
 cudaError_t ns_tc_state_out(const Geom& g, int m, const float* src, float* dst, cudaStream_t st);
 cudaError_t ns_tc_launch(const Geom& g, const Chunk& ch, const Work& w, int buf, size_t slot_stride, int num_sms,

@@ -153,7 +153,6 @@ static Layout layout(const Geom& g, int units, int T) {
       g.ns_iters && g.ns_target == ATLAS_NS_MOMENTUM ? U * g.C * mat : 0,   // Ubuf
       U * (size_t)(g.c > 1 ? g.c - 1 : 0) * (g.d_k + g.d_v + 1),  // cache temp
       64,                                  // status
-      ns_tc_xch_floats(g, num_sms()),      // Gram exchange of the CTA-pair Newton-Schulz
       g.depth == 2 ? U * ((size_t)(g.hidden + 63) / 64) * Kw * g.d_v  // tiled-gradient partial outputs
                    : dual1_split_floats(g, U, T),                       // depth 1: scaled dy + feature-slice partials
       g.ns_iters && g.ns_target == ATLAS_NS_SURPRISE ? surprise_floats(g, U) : 0,   // surprise NS scratch
@@ -180,9 +179,8 @@ static Work work_from(const Geom& g, void* base, const Layout& L, float** cache_
   w.Ubuf = F(21);
   *cache_tmp = F(22);
   w.status = (int*)F(23);
-  w.xch = F(24);
-  w.gpart = F(25);
-  w.surp = F(26);
+  w.gpart = F(24);
+  w.surp = F(25);
   return w;
 }
 

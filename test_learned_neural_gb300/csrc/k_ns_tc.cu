@@ -770,12 +770,6 @@ int ns_tc_kind(const Geom& g) {
 
 bool ns_tc_supported(const Geom& g) { return ns_tc_kind(g) != 0; }
 
-size_t ns_tc_xch_floats(const Geom& g, int num_sms) {
-  (void)g;
-  (void)num_sms;
-  return 0;   // the CTA pairs exchange over DSMEM: no global scratch
-}
-
 // momentum state of the tensor-core path: transposed (X orientation) for
 // matrices with rows > cols
 cudaError_t ns_tc_state_in(const Geom& g, int m, const float* src, float* dst, cudaStream_t st) {

@@ -42,7 +42,8 @@ def _sample_units(w):
     return sorted({0, w.units - 1})
 
 
-@pytest.mark.parametrize("name", ["titans_mlp", "atlas_muon", "atlas_long", "atlas_poly_c4", "atlas_poly_c16"])
+@pytest.mark.parametrize("name", ["titans_mlp", "atlas_muon", "atlas_long", "atlas_poly_c4", "atlas_poly_c16",
+                                  "atlas_muon_surprise"])
 def test_full_size_prefix(gpu_lib, name):
     from test_learned_neural_gb300.runner import tensors_from_numpy
     w = WORKLOADS[name]
