@@ -107,7 +107,7 @@ bool mlp_tc_supported(const Geom& g);
 cudaError_t mlp_tc_launch(const Geom& g, const void* q, const void* k, const void* v, const float* theta,
                           const float* eta, const float* alpha, const float* gamma, const float* const* W0,
                           const float* const* S0, float* y, float* const* W_out, float* const* S_out, int* status,
-                          cudaStream_t st);
+                          cudaStream_t st, int Tst = 0);   // Tst: token stride between units (0: g.T)
 
 // tensor-core Newton-Schulz (k_ns_tc.cu)
 bool ns_tc_supported(const Geom& g);

@@ -33,7 +33,7 @@ struct atlas_mem_handle {
   // so the copies of one group overlap the kernel of another
   static const int kGroups = 4;
   cudaStream_t pst[kGroups] = {};
-  cudaEvent_t pev[kGroups + 1] = {};
+  cudaEvent_t pev[2 * kGroups + 2] = {};
   cudaGraphExec_t gexec = nullptr;
   atlas_mem_io gkey{};    // arguments the graph was captured with
   void* gws = nullptr;
@@ -212,7 +212,7 @@ extern "C" void atlas_mem_destroy(atlas_mem_handle* h) {
   if (h->cap) cudaStreamDestroy(h->cap);
   for (int i = 0; i < atlas_mem_handle::kGroups; ++i)
     if (h->pst[i]) cudaStreamDestroy(h->pst[i]);
-  for (int i = 0; i <= atlas_mem_handle::kGroups; ++i)
+  for (int i = 0; i < 2 * atlas_mem_handle::kGroups + 2; ++i)
     if (h->pev[i]) cudaEventDestroy(h->pev[i]);
   if (h->ws) cudaFree(h->ws);
   if (h->stage) cudaFree(h->stage);
@@ -413,59 +413,91 @@ struct Item {
   size_t bytes;
 };
 
-// Host-buffer forward on the fused path, pipelined over unit groups: group i
-// copies its slices in, runs the fused kernel on its units and copies its
-// outputs back, all on stream pst[i]; the copies of one group overlap the
-// kernels of the others.  items / dptr follow the order of
-// atlas_mem_forward_host (inputs q k v theta eta alpha gamma P W0[2] S0[2]
-// window[3], then outputs y W_out[2] S_out[2] window[3]).
+// Host-buffer forward on the fused path, pipelined over time segments: the
+// sequence is cut into NS segments of whole chunks; segment i's inputs are
+// copied in on one stream while segment i-1 runs, the kernel runs segment i
+// from the state segment i-1 left (fp32, so the result equals one launch
+// bit for bit), and its y is copied out on a third stream while segment
+// i+1 runs.  items / dptr follow the order of atlas_mem_forward_host
+// (inputs q k v theta eta alpha gamma P W0[2] S0[2] window[3], then outputs
+// y W_out[2] S_out[2] window[3]).
 static int forward_host_pipelined(atlas_mem_handle* h, const atlas_mem_io* io, const Geom& g, const Item* items,
                                   void* const* dptr, int n, cudaStream_t st) {
-  const int NG = atlas_mem_handle::kGroups;
-  const size_t U = (size_t)g.units, ug = U / NG;
+  const int NS = atlas_mem_handle::kGroups;
+  const size_t U = (size_t)g.units, T = (size_t)g.T, Ts = T / NS;
   const Layout L = layout(g, g.units, g.T);
   int rc = ensure_workspace(h, L.total);
   if (rc) return rc;
   float* cache_tmp = nullptr;
   Work w = work_from(g, h->ws, L, &cache_tmp);
   h->status = w.status;
-  for (int i = 0; i < NG; ++i)
+  for (int i = 0; i < 2; ++i)
     if (!h->pst[i]) CUDA_TRY(cudaStreamCreateWithFlags(&h->pst[i], cudaStreamNonBlocking));
-  for (int i = 0; i <= NG; ++i)
+  for (int i = 0; i < 2 * NS + 2; ++i)
     if (!h->pev[i]) CUDA_TRY(cudaEventCreateWithFlags(&h->pev[i], cudaEventDisableTiming));
-  CUDA_TRY(cudaEventRecord(h->pev[NG], st));
-  Geom gg = g;
-  gg.units = (int)ug;
-  for (int gi = 0; gi < NG; ++gi) {
-    cudaStream_t s = h->pst[gi];
-    CUDA_TRY(cudaStreamWaitEvent(s, h->pev[NG], 0));
-    // slice of array i for this group: bytes per unit = total / U
-    auto dev = [&](int i) -> char* {
-      return dptr[i] ? (char*)dptr[i] + gi * ug * (items[i].bytes / U) : nullptr;
-    };
-    for (int i = 0; i < n; ++i)
-      if (items[i].src && items[i].bytes) {
-        const size_t b = ug * (items[i].bytes / U);
-        CUDA_TRY(cudaMemcpyAsync(dev(i), (const char*)items[i].src + gi * b, b, cudaMemcpyHostToDevice, s));
-      }
-    const float* W0g[2] = {(const float*)dev(8), (const float*)dev(9)};
-    const float* S0g[2] = {(const float*)dev(10), (const float*)dev(11)};
-    float* Wog[2] = {(float*)dev(16), (float*)dev(17)};
-    float* Sog[2] = {(float*)dev(18), (float*)dev(19)};
-    CUDA_TRY(mlp_tc_launch(gg, dev(0), dev(1), dev(2), (const float*)dev(3), (const float*)dev(4),
-                           (const float*)dev(5), (const float*)dev(6), W0g, S0g, (float*)dev(15), Wog, Sog, w.status,
-                           s));
-    for (int i = 15; i < n; ++i)
-      if (items[i].dst_host && items[i].bytes) {
-        const size_t b = ug * (items[i].bytes / U);
-        CUDA_TRY(cudaMemcpyAsync((char*)items[i].dst_host + gi * b, dev(i), b, cudaMemcpyDeviceToHost, s));
-      }
-    CUDA_TRY(cudaEventRecord(h->pev[gi], s));
-    CUDA_TRY(cudaStreamWaitEvent(st, h->pev[gi], 0));
+  cudaStream_t cin = h->pst[0], cout = h->pst[1];
+  cudaEvent_t* in_done = h->pev;          // [NS]
+  cudaEvent_t* k_done = h->pev + NS;      // [NS]
+  cudaEvent_t start = h->pev[2 * NS], out_done = h->pev[2 * NS + 1];
+  CUDA_TRY(cudaEventRecord(start, st));
+  CUDA_TRY(cudaStreamWaitEvent(cin, start, 0));
+  CUDA_TRY(cudaStreamWaitEvent(cout, start, 0));
+  // one time segment of a [U][T][width] array: U rows of Ts * width bytes
+  auto seg_copy = [&](int i, void* dst, const void* src, size_t bytes_per_unit, cudaMemcpyKind kind,
+                      cudaStream_t s) -> cudaError_t {
+    const size_t pitch = bytes_per_unit, wb = bytes_per_unit / NS, off = (size_t)i * wb;
+    return cudaMemcpy2DAsync((char*)dst + off, pitch, (const char*)src + off, pitch, wb, U, kind, s);
+  };
+  // state in (whole), then each segment's per-token inputs
+  for (int m = 8; m < 12; ++m)
+    if (items[m].src && items[m].bytes)
+      CUDA_TRY(cudaMemcpyAsync(dptr[m], items[m].src, items[m].bytes, cudaMemcpyHostToDevice, cin));
+  const int per_token[] = {0, 1, 2, 3, 4, 5, 6};
+  for (int i = 0; i < NS; ++i) {
+    for (int a : per_token)
+      if (items[a].src && items[a].bytes)
+        CUDA_TRY(seg_copy(i, dptr[a], items[a].src, items[a].bytes / U, cudaMemcpyHostToDevice, cin));
+    CUDA_TRY(cudaEventRecord(in_done[i], cin));
   }
-  h->launches = NG;
+  Geom gs = g;
+  gs.T = (int)Ts;
+  // the state ping-pongs between the staging of W0/S0 and of W_out/S_out
+  float* st_a[4] = {(float*)dptr[8], (float*)dptr[9], (float*)dptr[10], (float*)dptr[11]};
+  float* st_b[4] = {(float*)dptr[16], (float*)dptr[17], (float*)dptr[18], (float*)dptr[19]};
+  const size_t es = g.qkv_dtype == ATLAS_BF16 ? 2 : 4;
+  for (int i = 0; i < NS; ++i) {
+    CUDA_TRY(cudaStreamWaitEvent(st, in_done[i], 0));
+    float** sin = (i % 2 == 0) ? st_a : st_b;
+    float** sout = (i % 2 == 0) ? st_b : st_a;
+    const size_t t0 = (size_t)i * Ts;
+    const char* q = (const char*)dptr[0] + t0 * g.d_k * es;
+    const char* k = (const char*)dptr[1] + t0 * g.d_k * es;
+    const char* v = (const char*)dptr[2] + t0 * g.d_v * es;
+    const float* th = (const float*)dptr[3] + t0;
+    const float* et = (const float*)dptr[4] + t0;
+    const float* al = (const float*)dptr[5] + t0;
+    const float* ga = dptr[6] ? (const float*)dptr[6] + t0 : nullptr;
+    const float* W0[2] = {sin[0], sin[1]};
+    const float* S0[2] = {sin[2], sin[3]};
+    float* Wo[2] = {sout[0], sout[1]};
+    float* So[2] = {sout[2], sout[3]};
+    CUDA_TRY(mlp_tc_launch(gs, q, k, v, th, et, al, ga, W0, S0, (float*)dptr[15] + t0 * g.d_v, Wo, So, w.status, st,
+                           (int)T));
+    CUDA_TRY(cudaEventRecord(k_done[i], st));
+    CUDA_TRY(cudaStreamWaitEvent(cout, k_done[i], 0));
+    CUDA_TRY(seg_copy(i, items[15].dst_host, dptr[15], items[15].bytes / U, cudaMemcpyDeviceToHost, cout));
+  }
+  // final state: in st_b after an odd number of segments, else st_a
+  float** fin = (NS % 2 == 1) ? st_b : st_a;
+  for (int m = 0; m < 4; ++m)
+    if (items[16 + m].dst_host && items[16 + m].bytes)
+      CUDA_TRY(cudaMemcpyAsync(items[16 + m].dst_host, fin[m], items[16 + m].bytes, cudaMemcpyDeviceToHost, cout));
+  CUDA_TRY(cudaEventRecord(out_done, cout));
+  CUDA_TRY(cudaStreamWaitEvent(st, out_done, 0));
+  h->launches = NS;
   h->last_stream = st;
   h->launched = true;
+  (void)n;
   CUDA_TRY(cudaStreamSynchronize(st));
   return atlas_mem_status(h);
 }
@@ -532,7 +564,8 @@ extern "C" int atlas_mem_forward_host(atlas_mem_handle* h, const atlas_mem_io* i
   gu.n_prev = io->win_len;
   gu.L = gu.n_prev + gu.T;
   const int NG = atlas_mem_handle::kGroups;
-  if (mlp_tc_supported(gu) && io->P == nullptr && U % NG == 0 && getenv("ATLAS_NO_PIPELINE") == nullptr)
+  if (mlp_tc_supported(gu) && io->P == nullptr && T % ((size_t)NG * g.C) == 0 &&
+      getenv("ATLAS_NO_PIPELINE") == nullptr)
     return forward_host_pipelined(h, io, gu, items, dptr, n, st);
   for (int i = 0; i < n; ++i)
     if (items[i].src && items[i].bytes)

@@ -193,11 +193,11 @@ __device__ __forceinline__ void unpack4(uint4 w, int dt, float* o) {
 
 __device__ __forceinline__ void prefetch_chunk(Prefetch& p, int dt, const void* q, const void* k, const void* v,
                                                const float* theta, const float* eta, const float* alpha,
-                                               const float* gamma, int u, int T, int s, uint32_t qr) {
+                                               const float* gamma, int u, int T, int Tst, int s, uint32_t qr) {
   const int tid = threadIdx.x, r = tid % 64, g = tid / 64;
   if (s >= T) return;
   for (int j = 0; j < 2; ++j) {
-    const size_t base = ((size_t)u * T + s + r) * 64 + (g + 4 * j) * 8;
+    const size_t base = ((size_t)u * Tst + s + r) * 64 + (g + 4 * j) * 8;
     if (dt == ATLAS_BF16) {
       p.k[j][0] = __ldg(reinterpret_cast<const uint4*>((const uint16_t*)k + base));
       p.q[j][0] = __ldg(reinterpret_cast<const uint4*>((const uint16_t*)q + base));
@@ -208,12 +208,12 @@ __device__ __forceinline__ void prefetch_chunk(Prefetch& p, int dt, const void* 
       p.q[j][1] = __ldg(reinterpret_cast<const uint4*>((const float*)q + base + 4));
     }
   }
-  const size_t gd = ((size_t)u * T + s + 16 * qr + (tid >> 4)) * 64 + (tid & 15) * 4;
+  const size_t gd = ((size_t)u * Tst + s + 16 * qr + (tid >> 4)) * 64 + (tid & 15) * 4;
   p.kd = ld_in4(k, gd, dt);
   p.vd = ld_in4(v, gd, dt);
   p.qd = ld_in4(q, gd, dt);
   if (tid < 64) {
-    const size_t gi = (size_t)u * T + s + tid;
+    const size_t gi = (size_t)u * Tst + s + tid;
     p.th = __ldg(theta + gi);
     p.et = __ldg(eta + gi);
     p.al = __ldg(alpha + gi);
@@ -245,7 +245,7 @@ __device__ __forceinline__ void unpack8(const uint4* w, int dt, float* o) {
 
 // y rows [16q, 16q + 16) of the chunk at token s: r_t + the four slices'
 // Yq from this CTA's slots (thread: row tid / 16, columns 4 (tid % 16) .. + 3)
-__device__ __forceinline__ void y_rows(float* y, const float* slots, const float* qv, int u, int T, int s,
+__device__ __forceinline__ void y_rows(float* y, const float* slots, const float* qv, int u, int Tst, int s,
                                        uint32_t qr) {
   const int tid = threadIdx.x, rl = tid >> 4, cc = (tid & 15) * 4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -254,7 +254,7 @@ __device__ __forceinline__ void y_rows(float* y, const float* slots, const float
     const float4 t4 = *reinterpret_cast<const float4*>(slots + slot_idx(p, rl, cc));
     acc.x += t4.x; acc.y += t4.y; acc.z += t4.z; acc.w += t4.w;
   }
-  const size_t gb = ((size_t)u * T + s + 16 * (int)qr + rl) * D + cc;
+  const size_t gb = ((size_t)u * Tst + s + 16 * (int)qr + rl) * D + cc;
   *reinterpret_cast<float4*>(y + gb) = make_float4(qv[0] + acc.x, qv[1] + acc.y, qv[2] + acc.z, qv[3] + acc.w);
 }
 
@@ -278,7 +278,7 @@ __device__ __forceinline__ void commit_wait(Ctx& c) {
 }  // namespace
 
 __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
-    k_mlp_dual_tc(int T, int dt, const void* __restrict__ q, const void* __restrict__ k, const void* __restrict__ v,
+    k_mlp_dual_tc(int T, int Tst, int dt, const void* __restrict__ q, const void* __restrict__ k, const void* __restrict__ v,
                   const float* __restrict__ theta, const float* __restrict__ eta, const float* __restrict__ alpha,
                   const float* __restrict__ gamma, const float* W0a, const float* W0b, const float* S0a,
                   const float* S0b, float* __restrict__ y, float* Woa, float* Wob, float* Soa, float* Sob,
@@ -341,7 +341,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   tc::fence_after_sync();
   Ctx cx{&bar, 0u, true};
   Prefetch pf;
-  prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, 0, qr);
+  prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, Tst, 0, qr);
   float qprev[4] = {0.f, 0.f, 0.f, 0.f};   // q of the previous chunk's rows, for its deferred y
   float xkd[4], vvd[4], qcur[4];            // this chunk's k, v, q rows of the cross-slice sums
   float xkn[4], vvn[4], qnx[4];             // the next chunk's
@@ -403,7 +403,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     unpack4(pf.kd, dt, xkn);
     unpack4(pf.vd, dt, vvn);
     unpack4(pf.qd, dt, qnx);
-    prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, sn + TOK, qr);
+    prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, Tst, sn + TOK, qr);
   };
 
   // gate scans of buffer bn (window of token t is {t})
@@ -592,7 +592,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       pk.x = *reinterpret_cast<const uint32_t*>(&h0);
       pk.y = *reinterpret_cast<const uint32_t*>(&h1);
       *reinterpret_cast<uint2*>(sm + ODY + tc::core_offset(r, cc, RGS)) = pk;
-      if (s > 0) y_rows(y, reinterpret_cast<const float*>(sm + RED + F32T), qprev, u, T, s - TOK, qr);
+      if (s > 0) y_rows(y, reinterpret_cast<const float*>(sm + RED + F32T), qprev, u, Tst, s - TOK, qr);
     }
     tc::fence_smem_to_async();   // the dy rows are the bulk copies' source
     __syncthreads();
@@ -733,7 +733,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   xwait(2, ((T / TOK) - 1) & 1);
   if (tid == 0) bulk_wait_all();   // every copy this CTA issued has landed
   __syncthreads();
-  y_rows(y, reinterpret_cast<const float*>(sm + RED + F32T), qprev, u, T, T - TOK, qr);
+  y_rows(y, reinterpret_cast<const float*>(sm + RED + F32T), qprev, u, Tst, T - TOK, qr);
 
   // ---- state slices out
   {
@@ -764,10 +764,11 @@ bool mlp_tc_supported(const Geom& g) {
 cudaError_t mlp_tc_launch(const Geom& g, const void* q, const void* k, const void* v, const float* theta,
                           const float* eta, const float* alpha, const float* gamma, const float* const* W0,
                           const float* const* S0, float* y, float* const* W_out, float* const* S_out, int* status,
-                          cudaStream_t st) {
+                          cudaStream_t st, int Tst) {
   cudaError_t e = cudaFuncSetAttribute(k_mlp_dual_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  k_mlp_dual_tc<<<g.units * CS, NT, SMEM_BYTES, st>>>(g.T, g.qkv_dtype, q, k, v, theta, eta, alpha, gamma, W0[0],
+  k_mlp_dual_tc<<<g.units * CS, NT, SMEM_BYTES, st>>>(g.T, Tst > 0 ? Tst : g.T, g.qkv_dtype, q, k, v, theta, eta,
+                                                      alpha, gamma, W0[0],
                                                       W0[1], S0[0], S0[1], y, W_out[0], W_out[1], S_out[0],
                                                       S_out[1], status, g.readout == ATLAS_READOUT_PRE ? 1 : 0);
   return cudaGetLastError();

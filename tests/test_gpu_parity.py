@@ -79,11 +79,12 @@ def test_split_continuation_matches_whole(gpu_lib, name):
     mem.close()
 
 
-@pytest.mark.parametrize("H", [2, 4])
-def test_host_buffers_match_device_buffers(gpu_lib, H):
-    """Host-buffer entry point = device entry point, bit for bit; with 4
-    units the fused path's host call runs pipelined over unit groups."""
-    w = WORKLOADS["titans_mlp"].scaled(B=1, H=H, T=128)
+@pytest.mark.parametrize("H,T", [(2, 128), (4, 256), (3, 512)])
+def test_host_buffers_match_device_buffers(gpu_lib, H, T):
+    """Host-buffer entry point = device entry point, bit for bit.  With T a
+    multiple of four chunks the fused path's host call runs pipelined over
+    four time segments (one launch each, the state handed on in fp32)."""
+    w = WORKLOADS["titans_mlp"].scaled(B=1, H=H, T=T)
     inp = make_inputs(w)
     d = run_gpu(w, inp)
     h = run_gpu(w, inp, host=True)
