@@ -35,6 +35,12 @@ order the pages define:
              Eq. 13).
 * read-out   y_t = M_{W_t}(r_t) from the post-update state of token t
              (atlas-torch README, "Known deviations from the paper's MAC").
+
+The chunk-wise update rule (``update = "chunkwise"``) is the titans-pytorch
+store path that the atlas-torch README sets beside the per-token one ("Bug
+Fixes": the per_token_updates flag): one gradient per chunk, summed over its
+tokens at W_bar, the chunk's momentum and decay gates pooled, one momentum /
+decay step per chunk, and a read-out per chunk.
 """
 from __future__ import annotations
 
@@ -157,6 +163,20 @@ def forward_unit(cfg, k, q, v, theta, eta, alpha, gamma, W0, S0, P=None,
     # "orthogonalization of the surprise updates", per-token store path with
     # "eta outside Newton-Schulz").
     surprise_ns = bool(cfg.ns_iters) and getattr(cfg, "ns_target", "momentum") == "surprise"
+    # Update rule: "per_token" (default, everything above) or "chunkwise", the
+    # titans-pytorch chunk-wise store path (atlas-torch README, "Bug Fixes":
+    # per_token_updates): per chunk, G = sum_i theta_i gamma_i grad l_i(W_bar)
+    # over its tokens, the gates eta and alpha pooled to their mean over the
+    # chunk, S <- eta_bar S - G, U = NS_k(S) (eta inside Newton-Schulz) or S,
+    # W <- (1 - alpha_bar) W + U.  The memory exists only at chunk ends: token
+    # t reads the one after the last chunk that ends at or before t ("post":
+    # the chunk's last token reads its own chunk's update, the others the
+    # chunk-start memory) or, "pre", the chunk-start memory.  There is no
+    # Omega window on this path (c = 1) and Newton-Schulz, if any, is on the
+    # momentum.  With C = 1 it is the per-token rule with c = 1.
+    chunkwise = getattr(cfg, "update", "per_token") == "chunkwise"
+    if chunkwise and (c != 1 or surprise_ns):
+        raise ValueError("the chunk-wise update has no Omega window (c = 1) and no Newton-Schulz on the surprise")
     k = np.asarray(k, np.float64)
     q = np.asarray(q, np.float64)
     v = np.asarray(v, np.float64)
@@ -187,6 +207,17 @@ def forward_unit(cfg, k, q, v, theta, eta, alpha, gamma, W0, S0, P=None,
         rows = slice(lo + n_prev, e + n_prev)
         grads = token_gradients(W_bar, X_all[rows], V_all[rows], depth)
         weighted = [g * G_all[rows][:, None, None] for g in grads]
+        if chunkwise:
+            # c = 1: the window rows are exactly the chunk's tokens s .. e-1
+            G = [(wg * theta[s:e, None, None]).sum(axis=0) for wg in weighted]
+            eta_bar, alpha_bar = eta[s:e].mean(), alpha[s:e].mean()
+            S = [eta_bar * Sm - Gm for Sm, Gm in zip(S, G)]
+            U = [newton_schulz(Sm, cfg.ns_iters) for Sm in S] if cfg.ns_iters else S
+            W = [(1.0 - alpha_bar) * Wm + Um for Wm, Um in zip(W_bar, U)]
+            y[s:e] = memory_apply(W_bar, R[s:e], depth)
+            if not pre:
+                y[e - 1] = memory_apply(W, R[e - 1:e], depth)[0]
+            continue
         for t in range(s, e):
             first = max(t - c + 1, lo) - lo
             last = t - lo + 1

@@ -71,11 +71,12 @@ def apply_mem(W, x, depth):
 
 
 def forward(depth, C, c, p, ns_iters, k, q, v, theta, eta, alpha, gamma, W0, S0,
-            P=None, prev=None, pre=False, surprise_ns=False):
+            P=None, prev=None, pre=False, surprise_ns=False, chunkwise=False):
     """prev = (keys, values, gammas) of tokens preceding the call, oldest first.
     pre = True reads token t out of the memory before its update (the paper's
     MAC retrieval, h_t = M*_{t-1}(q_t)); else after it.  surprise_ns = True
-    orthogonalises each token's windowed gradient instead of the momentum."""
+    orthogonalises each token's windowed gradient instead of the momentum.
+    chunkwise = True runs the chunk-wise store path instead (no window)."""
     T = len(k)
     gamma = np.ones(T) if gamma is None else gamma
     pk, pv, pg = ([], [], []) if prev is None else prev
@@ -90,6 +91,8 @@ def forward(depth, C, c, p, ns_iters, k, q, v, theta, eta, alpha, gamma, W0, S0,
 
     W = [np.array(m, np.float64) for m in W0]
     S = [np.array(m, np.float64) for m in S0]
+    if chunkwise:
+        return _chunkwise(depth, C, ns_iters, feat, keys, vals, gams, n_prev, q, theta, eta, alpha, W, S, pre)
     W_bar = None
     y = []
     for t in range(T):
@@ -110,4 +113,32 @@ def forward(depth, C, c, p, ns_iters, k, q, v, theta, eta, alpha, gamma, W0, S0,
         W_before = W
         W = [(1.0 - alpha[t]) * Wm + Um for Wm, Um in zip(W, U)]
         y.append(apply_mem(W_before if pre else W, feat(q[t]), depth))
+    return np.array(y), W, S
+
+
+def _chunkwise(depth, C, ns_iters, feat, keys, vals, gams, n_prev, q, theta, eta, alpha, W, S, pre):
+    """Chunk-wise store path, written as loops: per chunk one gradient summed
+    over its tokens at the chunk-start memory (each token's weighted by its
+    theta and gamma), one momentum step with the chunk's average eta, one
+    decay step with its average alpha; a token reads the memory after the
+    last chunk that has ended by it (or, pre, its chunk's start memory)."""
+    T = len(q)
+    y = []
+    for s in range(0, T, C):
+        e = min(s + C, T)
+        W_bar = W
+        G = [np.zeros_like(m) for m in W]
+        eta_sum = alpha_sum = 0.0
+        for i in range(s, e):
+            gi = autograd_grad(W_bar, feat(keys[i + n_prev]), np.asarray(vals[i + n_prev]), depth)
+            G = [a + theta[i] * gams[i + n_prev] * b for a, b in zip(G, gi)]
+            eta_sum += eta[i]
+            alpha_sum += alpha[i]
+        n = e - s
+        S = [(eta_sum / n) * Sm - Gm for Sm, Gm in zip(S, G)]
+        U = [ns_closed_form(Sm, ns_iters) for Sm in S] if ns_iters else S
+        W = [(1.0 - alpha_sum / n) * Wm + Um for Wm, Um in zip(W_bar, U)]
+        for t in range(s, e):
+            reads = W if (t == e - 1 and not pre) else W_bar
+            y.append(apply_mem(reads, feat(q[t]), depth))
     return np.array(y), W, S

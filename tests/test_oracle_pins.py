@@ -28,6 +28,7 @@ class Cfg:
     ns_iters: int = 0
     readout: str = "post"
     ns_target: str = "momentum"
+    update: str = "per_token"
 
 
 def _rand_case(rng, depth, d_k, d_v, hidden, T, p=1, proj=0, gamma=True, scale_w=0.3):
@@ -447,3 +448,120 @@ def test_surprise_ns_rank_one_closed_form():
     np.testing.assert_allclose(S[0], S_exp, rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(W[0], W_exp, rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(y[0], q @ W_exp, rtol=1e-12, atol=1e-14)
+
+
+# ---- chunk-wise store path (atlas-torch README, "Bug Fixes": the
+# per_token_updates flag; the titans-pytorch chunk-wise path: one summed
+# gradient per chunk, pooled gates, a per-chunk scan and read-out)
+
+CHUNKWISE_CASES = [
+    # depth, C, p, proj, ns, d_k, d_v, hidden, T, readout
+    (1, 4, 1, 0, 0, 4, 3, 0, 10, "post"),    # partial last chunk
+    (2, 3, 1, 0, 0, 3, 3, 5, 9, "post"),
+    (2, 4, 1, 0, 0, 4, 4, 6, 8, "pre"),
+    (1, 3, 2, 0, 0, 2, 2, 0, 9, "post"),     # polynomial features
+    (2, 4, 1, 0, 5, 4, 4, 6, 10, "post"),    # Muon on the momentum
+    (2, 3, 2, 4, 3, 3, 4, 5, 9, "pre"),      # polynomial + projection + Muon
+]
+
+
+@pytest.mark.parametrize("case_def", CHUNKWISE_CASES)
+def test_chunkwise_matches_bruteforce(case_def):
+    depth, C, p, proj, ns, d_k, d_v, hidden, T, ro = case_def
+    rng = np.random.default_rng(sum(x for x in case_def if isinstance(x, int)) * 31337 + len(ro))
+    case = _rand_case(rng, depth, d_k, d_v, hidden, T, p=p, proj=proj)
+    y, W, S, _ = _run_oracle(Cfg(depth=depth, C=C, c=1, p=p, ns_iters=ns, readout=ro, update="chunkwise"), case)
+    yb, Wb, Sb = bf.forward(depth, C, 1, p, ns, case["k"], case["q"], case["v"], case["theta"], case["eta"],
+                            case["alpha"], case["gamma"], case["W0"], case["S0"], case["P"], pre=(ro == "pre"),
+                            chunkwise=True)
+    np.testing.assert_allclose(y, yb, rtol=1e-9, atol=1e-11)
+    for a, b in zip(W + S, Wb + Sb):
+        np.testing.assert_allclose(a, b, rtol=1e-9, atol=1e-11)
+
+
+@pytest.mark.parametrize("depth,ns,ro", [(1, 0, "post"), (2, 0, "post"), (2, 0, "pre"), (2, 3, "post"),
+                                         (1, 5, "pre")])
+def test_chunkwise_with_chunks_of_one_is_the_per_token_rule(depth, ns, ro):
+    """With C = 1 a chunk is a token: pooling is the identity, the summed
+    gradient is the token's own, and the chunk-end memory is W_t, so the
+    chunk-wise path must give the per-token rule with c = 1 exactly."""
+    rng = np.random.default_rng(500 + 10 * depth + ns)
+    case = _rand_case(rng, depth, 3, 3, 4, T=7)
+    a = _run_oracle(Cfg(depth=depth, C=1, c=1, ns_iters=ns, readout=ro, update="chunkwise"), case)
+    b = _run_oracle(Cfg(depth=depth, C=1, c=1, ns_iters=ns, readout=ro), case)
+    np.testing.assert_allclose(a[0], b[0], rtol=1e-12, atol=1e-14)
+    for x, z in zip(a[1] + a[2], b[1] + b[2]):
+        np.testing.assert_allclose(x, z, rtol=1e-12, atol=1e-14)
+
+
+def test_chunkwise_closed_form_one_chunk():
+    """Linear memory, one chunk, eta = alpha = 0: S = -sum_t theta_t gamma_t
+    2 x_t^T (x_t W0 - v_t), W = W0 + S; every token but the last reads W0,
+    the last reads W."""
+    rng = np.random.default_rng(606)
+    T = 6
+    case = _rand_case(rng, 1, 4, 3, 0, T=T)
+    case["eta"] = np.zeros(T)
+    case["alpha"] = np.zeros(T)
+    case["S0"] = [0.2 * rng.standard_normal((4, 3))]      # eta = 0 forgets it
+    y, W, S, _ = _run_oracle(Cfg(depth=1, C=T, c=1, update="chunkwise"), case)
+    W0 = case["W0"][0]
+    G = sum(case["theta"][t] * case["gamma"][t] * 2.0 * np.outer(case["k"][t], case["k"][t] @ W0 - case["v"][t])
+            for t in range(T))
+    np.testing.assert_allclose(S[0], -G, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(W[0], W0 - G, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(y[:-1], case["q"][:-1] @ W0, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(y[-1], case["q"][-1] @ (W0 - G), rtol=1e-12, atol=1e-14)
+
+
+def test_chunkwise_gates_enter_only_through_their_chunk_mean():
+    """Replacing eta and alpha by their per-chunk means changes nothing on
+    the chunk-wise path, and does change the per-token rule (the pin has
+    something to catch); permuting the tokens inside every chunk, last token
+    kept, leaves the chunk-end memory and the outputs alike unchanged."""
+    rng = np.random.default_rng(707)
+    T, C = 12, 4
+    case = _rand_case(rng, 2, 3, 3, 5, T=T)
+    pooled = dict(case)
+    for key in ("eta", "alpha"):
+        pooled[key] = np.repeat(case[key].reshape(-1, C).mean(axis=1), C)
+    cw = Cfg(depth=2, C=C, c=1, ns_iters=2, update="chunkwise")
+    a, b = _run_oracle(cw, case), _run_oracle(cw, pooled)
+    np.testing.assert_allclose(a[0], b[0], rtol=1e-12, atol=1e-14)
+    for x, z in zip(a[1] + a[2], b[1] + b[2]):
+        np.testing.assert_allclose(x, z, rtol=1e-12, atol=1e-14)
+    pt = Cfg(depth=2, C=C, c=1, ns_iters=2)
+    assert np.abs(_run_oracle(pt, case)[1][0] - _run_oracle(pt, pooled)[1][0]).max() > 1e-6
+    perm = np.concatenate([s + np.r_[rng.permutation(C - 1), C - 1] for s in range(0, T, C)])
+    shuffled = {k: (v[perm] if isinstance(v, np.ndarray) and v.shape[:1] == (T,) else v) for k, v in case.items()}
+    c_ = _run_oracle(cw, shuffled)
+    np.testing.assert_allclose(c_[0], a[0][perm], rtol=1e-11, atol=1e-13)
+    for x, z in zip(c_[1] + c_[2], a[1] + a[2]):
+        np.testing.assert_allclose(x, z, rtol=1e-11, atol=1e-13)
+
+
+def test_chunkwise_split_continuation():
+    """Carrying the state across calls cut at a chunk edge gives the
+    whole-sequence result on the chunk-wise path too."""
+    rng = np.random.default_rng(808)
+    T, T1, C = 16, 8, 4
+    case = _rand_case(rng, 2, 4, 4, 6, T=T)
+    cfg = Cfg(depth=2, C=C, c=1, ns_iters=3, update="chunkwise")
+    y, W, S, _ = _run_oracle(cfg, case)
+    first = {k: (v[:T1] if isinstance(v, np.ndarray) and v.shape[:1] == (T,) else v) for k, v in case.items()}
+    y1, W1, S1, _ = _run_oracle(cfg, first)
+    second = {k: (v[T1:] if isinstance(v, np.ndarray) and v.shape[:1] == (T,) else v) for k, v in case.items()}
+    second["W0"], second["S0"] = W1, S1
+    y2, W2, S2, _ = _run_oracle(cfg, second)
+    np.testing.assert_allclose(np.concatenate([y1, y2]), y, rtol=1e-12, atol=1e-12)
+    for a, b in zip(W2 + S2, W + S):
+        np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+def test_chunkwise_rejects_a_window_and_surprise_ns():
+    rng = np.random.default_rng(909)
+    case = _rand_case(rng, 1, 3, 3, 0, T=4)
+    with pytest.raises(ValueError):
+        _run_oracle(Cfg(depth=1, C=2, c=2, update="chunkwise"), case)
+    with pytest.raises(ValueError):
+        _run_oracle(Cfg(depth=1, C=2, c=1, ns_iters=3, ns_target="surprise", update="chunkwise"), case)
