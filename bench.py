@@ -46,6 +46,16 @@ def flops_per_chunk(w) -> float:
     if w.proj_dim:
         feat = 2.0 * w.poly_dim * w.proj_dim * (C + C)     # keys and queries of the chunk
     surprise = w.ns_iters > 0 and getattr(w, "ns_target", "momentum") == "surprise"
+    if getattr(w, "update", "per_token") == "chunkwise":
+        # one update per chunk: the forward/backward at W_bar, one summed
+        # gradient product per matrix, Newton-Schulz once per matrix, and
+        # every token's read-out through the memory
+        mats = [(F, dv)] if w.depth == 1 else [(F, h), (h, dv)]
+        fwd = 2.0 * Kw * F * dv if w.depth == 1 else 3 * 2.0 * Kw * F * h
+        state = sum(2.0 * r * c * C for (r, c) in mats)
+        read = C * sum(2.0 * r * c for (r, c) in mats)
+        ns = sum(w.ns_iters * (2.0 * min(r, c) ** 2 * max(r, c) * 2 + 2.0 * min(r, c) ** 3) for (r, c) in mats)
+        return feat + fwd + state + read + ns
     if w.ns_iters == 0 or surprise:
         extra = 0.0
         if surprise:

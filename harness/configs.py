@@ -37,6 +37,8 @@ class Workload:
     w0_init: str = "zero"         # "zero" or "xavier" (per head, shared over B)
     readout: str = "post"         # "post": y_t from the memory after token t's update; "pre": before it
     ns_target: str = "momentum"   # Newton-Schulz on the momentum, or "surprise": on each token's windowed gradient
+    update: str = "per_token"     # or "chunkwise": one summed gradient, pooled gates and one step per chunk
+    theta_scale: float = 0.1      # theta = theta_scale * sigmoid(N(0, 1))
 
     @property
     def units(self) -> int:
@@ -97,6 +99,20 @@ WORKLOADS = {
         "atlas_muon_surprise", depth=2, d_k=128, d_v=128, hidden=512, C=64, c=8, p=1,
         proj_dim=0, ns_iters=5, qkv_dtype="bf16", B=2, H=16, T=16384, seed=3,
         w0_init="xavier", ns_target="surprise"),
+    # The chunk-wise store path of titans-pytorch (one summed gradient per
+    # chunk, pooled eta / alpha, one momentum and decay step per chunk) on
+    # the Titans memory, and with Muon on the Muon geometry (no Omega window
+    # on that path: c = 1).  Without Muon the chunk's step is the sum of C
+    # token steps, so theta is drawn C times smaller: with the per-token
+    # scale this memory diverges within ~1000 tokens, in fp64 as well.
+    "titans_chunkwise": Workload(
+        "titans_chunkwise", depth=2, d_k=64, d_v=64, hidden=256, C=64, c=1, p=1,
+        proj_dim=0, ns_iters=0, qkv_dtype="bf16", B=4, H=8, T=4096, seed=1,
+        w0_init="xavier", update="chunkwise", theta_scale=0.1 / 64),
+    "atlas_muon_chunkwise": Workload(
+        "atlas_muon_chunkwise", depth=2, d_k=128, d_v=128, hidden=512, C=64, c=1, p=1,
+        proj_dim=0, ns_iters=5, qkv_dtype="bf16", B=2, H=16, T=16384, seed=3,
+        w0_init="xavier", update="chunkwise"),
     # Long context: degree-2 features of 64-dim keys (2145) projected to 64.
     "atlas_long": Workload(
         "atlas_long", depth=2, d_k=64, d_v=64, hidden=256, C=64, c=8, p=2,

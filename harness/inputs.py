@@ -8,7 +8,8 @@ where features are projected).
 * k, q ~ N(0, 1), L2-normalised per token, then stored in the input precision
   (float32, or bf16 by round-to-nearest-even).
 * v ~ N(0, 1), same storage.
-* theta = 0.1 * sigmoid(N(0, 1)), eta = sigmoid(N(1, 1)),
+* theta = theta_scale * sigmoid(N(0, 1)) (theta_scale 0.1, or 0.1 / C on the
+  chunk-wise Titans workload, whose chunk sums C gradients), eta = sigmoid(N(1, 1)),
   alpha = sigmoid(N(alpha_mu, 1)), gamma = sigmoid(N(0, 1)); all float32.
 * W0: zeros, or Xavier-normal (std sqrt(2 / (fan_in + fan_out))) drawn once per
   head and shared by every batch row; S0 = 0.  float32.
@@ -68,7 +69,7 @@ def make_inputs(w: Workload) -> dict:
     out["q"] = _store(_l2n(rng.standard_normal((B, H, T, w.d_k))), w.qkv_dtype)
     out["v"] = _store(rng.standard_normal((B, H, T, w.d_v)), w.qkv_dtype)
     f32 = np.float32
-    out["theta"] = (0.1 * _sigmoid(rng.standard_normal((B, H, T)))).astype(f32)
+    out["theta"] = (w.theta_scale * _sigmoid(rng.standard_normal((B, H, T)))).astype(f32)
     out["eta"] = _sigmoid(rng.normal(1.0, 1.0, (B, H, T))).astype(f32)
     out["alpha"] = _sigmoid(rng.normal(w.alpha_mu, 1.0, (B, H, T))).astype(f32)
     out["gamma"] = (_sigmoid(rng.standard_normal((B, H, T))).astype(f32)

@@ -58,6 +58,10 @@ extern "C" {
 #define ATLAS_NS_MOMENTUM 0
 #define ATLAS_NS_SURPRISE 1
 
+/* update rules (atlas_mem_config.update) */
+#define ATLAS_UPDATE_PER_TOKEN 0
+#define ATLAS_UPDATE_CHUNKWISE 1
+
 typedef struct {
     int depth;      /* 1 (matrix memory) or 2 (residual SiLU MLP) */
     int d_k;        /* key/query width before the feature map */
@@ -83,6 +87,18 @@ typedef struct {
                      * (atlas-torch README, "Atlas Extensions": Muon / Newton-
                      * Schulz on the surprise; "eta outside Newton-Schulz").
                      * The surprise has rank <= c, so it needs c <= 32. */
+    int update;     /* ATLAS_UPDATE_PER_TOKEN: the per-token rule above (a
+                     * momentum, decay and read-out step for every token).
+                     * ATLAS_UPDATE_CHUNKWISE: the titans-pytorch chunk-wise
+                     * store path (atlas-torch README, "Bug Fixes": the
+                     * per_token_updates flag): per chunk one gradient
+                     * G = sum_i theta_i gamma_i grad l_i(W_bar) over its
+                     * tokens, eta and alpha pooled to their mean over the
+                     * chunk, S <- eta_bar S - G, W <- (1 - alpha_bar) W +
+                     * NS(S) (or + S); token t reads the memory after the last
+                     * chunk ending at or before t (READOUT_POST) or its
+                     * chunk's start memory (READOUT_PRE).  Needs c == 1 and
+                     * Newton-Schulz, if any, on the momentum. */
 } atlas_mem_config;
 
 typedef struct atlas_mem_handle atlas_mem_handle;

@@ -17,6 +17,7 @@ ATLAS_OK, ATLAS_ERR_INVALID_ARG, ATLAS_ERR_UNSUPPORTED, ATLAS_ERR_CUDA, ATLAS_ER
 ATLAS_F32, ATLAS_BF16 = 0, 1
 ATLAS_READOUT_POST, ATLAS_READOUT_PRE = 0, 1
 ATLAS_NS_MOMENTUM, ATLAS_NS_SURPRISE = 0, 1
+ATLAS_UPDATE_PER_TOKEN, ATLAS_UPDATE_CHUNKWISE = 0, 1
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "OOM", 5: "TIMEOUT"}
 
 # exported symbols, as declared in include/atlas_mem.h
@@ -28,7 +29,7 @@ EXPORTS = ("atlas_mem_create", "atlas_mem_forward", "atlas_mem_forward_host", "a
 class atlas_mem_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("depth", "d_k", "d_v", "hidden", "C", "c", "p", "proj_dim", "ns_iters", "qkv_dtype", "readout",
-                                     "ns_target")]
+                                     "ns_target", "update")]
 
 
 _vp = ctypes.c_void_p
@@ -140,11 +141,12 @@ def atlas_mem_destroy(h):
 
 # ------------------------------------------------------------- marshalling
 def make_config(depth, d_k, d_v, hidden, C, c, p, proj_dim, ns_iters, qkv_dtype,
-                readout="post", ns_target="momentum") -> atlas_mem_config:
+                readout="post", ns_target="momentum", update="per_token") -> atlas_mem_config:
     dt = {"f32": ATLAS_F32, "bf16": ATLAS_BF16}.get(qkv_dtype, qkv_dtype)
     ro = {"post": ATLAS_READOUT_POST, "pre": ATLAS_READOUT_PRE}.get(readout, readout)
     nt = {"momentum": ATLAS_NS_MOMENTUM, "surprise": ATLAS_NS_SURPRISE}.get(ns_target, ns_target)
-    return atlas_mem_config(depth, d_k, d_v, hidden, C, c, p, proj_dim, ns_iters, dt, ro, nt)
+    up = {"per_token": ATLAS_UPDATE_PER_TOKEN, "chunkwise": ATLAS_UPDATE_CHUNKWISE}.get(update, update)
+    return atlas_mem_config(depth, d_k, d_v, hidden, C, c, p, proj_dim, ns_iters, dt, ro, nt, up)
 
 
 def _ptr(t):

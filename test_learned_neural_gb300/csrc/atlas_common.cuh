@@ -27,6 +27,7 @@ struct Geom {
   int rows[2], cols[2], nmat;
   int readout;    // ATLAS_READOUT_POST / ATLAS_READOUT_PRE
   int ns_target;  // ATLAS_NS_MOMENTUM / ATLAS_NS_SURPRISE
+  int update;     // ATLAS_UPDATE_PER_TOKEN / ATLAS_UPDATE_CHUNKWISE
 };
 
 // Per-chunk indices: the chunk covers tokens [s, e) of the call; its Omega
@@ -34,6 +35,14 @@ struct Geom {
 struct Chunk {
   int s, e, lo, nw;  // nw = e - lo window rows
 };
+
+// First token of a chunk (0-based in the chunk) whose momentum goes through
+// Newton-Schulz: every token under the per-token rule; under the chunk-wise
+// rule the memory changes once per chunk, so only the last token's.  The
+// tokens before it add U = 0 to the decay scans.
+__host__ __device__ __forceinline__ int ns_first_row(const Geom& g, const Chunk& ch) {
+  return g.update == ATLAS_UPDATE_CHUNKWISE ? ch.e - ch.s - 1 : 0;
+}
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
   return __uint_as_float(((uint32_t)b) << 16);
@@ -75,6 +84,8 @@ struct Work {
                   // then per (unit, chunk) gate-scan coefficients
   float* surp;    // Newton-Schulz on the surprise: Gram matrices, c x c cores,
                   // banded coefficient matrices (k_surprise.cu)
+  float* aeff;    // chunk-wise update with Newton-Schulz: [units][T] the decay
+                  // each token applies (0, the chunk's mean alpha at its last token)
   int* status;    // device status word
 };
 

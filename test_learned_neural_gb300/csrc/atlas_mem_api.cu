@@ -83,6 +83,11 @@ static int derive_geom(const atlas_mem_config& c, Geom* g, char* why, size_t why
     BAD("ns_target must be ATLAS_NS_MOMENTUM or ATLAS_NS_SURPRISE");
   if (c.ns_target == ATLAS_NS_SURPRISE && c.ns_iters > 0 && c.c > 32)
     BAD("Newton-Schulz on the surprise needs c <= 32 (its c x c core)");
+  if (c.update != ATLAS_UPDATE_PER_TOKEN && c.update != ATLAS_UPDATE_CHUNKWISE)
+    BAD("update must be ATLAS_UPDATE_PER_TOKEN or ATLAS_UPDATE_CHUNKWISE");
+  if (c.update == ATLAS_UPDATE_CHUNKWISE && c.c != 1) BAD("the chunk-wise update has no Omega window: c must be 1");
+  if (c.update == ATLAS_UPDATE_CHUNKWISE && c.ns_iters > 0 && c.ns_target != ATLAS_NS_MOMENTUM)
+    BAD("the chunk-wise update orthogonalises the momentum only");
   long long poly = c.p == 1 ? c.d_k : 1 + c.d_k + choose2(c.d_k + 1);
   long long F = c.proj_dim ? c.proj_dim : poly;
   if (c.depth == 2 && F != c.d_v) BAD("depth 2 (residual memory) needs feature width %lld == d_v %d", F, c.d_v);
@@ -91,6 +96,7 @@ static int derive_geom(const atlas_mem_config& c, Geom* g, char* why, size_t why
   g->qkv_dtype = c.qkv_dtype;
   g->readout = c.readout;
   g->ns_target = c.ns_target;
+  g->update = c.update;
   g->Kw = c.C + c.c - 1;
   if (c.depth == 1) {
     g->nmat = 1; g->rows[0] = (int)F; g->cols[0] = c.d_v;
@@ -156,6 +162,7 @@ static Layout layout(const Geom& g, int units, int T) {
       g.depth == 2 ? U * ((size_t)(g.hidden + 63) / 64) * Kw * g.d_v  // tiled-gradient partial outputs
                    : dual1_split_floats(g, U, T),                       // depth 1: scaled dy + feature-slice partials
       g.ns_iters && g.ns_target == ATLAS_NS_SURPRISE ? surprise_floats(g, U) : 0,   // surprise NS scratch
+      g.ns_iters && g.update == ATLAS_UPDATE_CHUNKWISE ? U * (size_t)T : 0,          // per-token decay (aeff)
   };
   const int n = sizeof sizes / sizeof sizes[0];
   size_t o = 0;
@@ -181,6 +188,7 @@ static Work work_from(const Geom& g, void* base, const Layout& L, float** cache_
   w.status = (int*)F(23);
   w.gpart = F(24);
   w.surp = F(25);
+  w.aeff = g.ns_iters && g.update == ATLAS_UPDATE_CHUNKWISE ? F(26) : nullptr;
   return w;
 }
 

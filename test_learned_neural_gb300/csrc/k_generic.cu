@@ -132,6 +132,55 @@ __global__ void k_coef(Geom g, Chunk ch, const float* theta, const float* eta, c
   }
 }
 
+// Chunk-wise update rule (titans-pytorch store path, as the atlas-torch
+// README's per_token_updates fix describes it): the same coefficient arrays
+// for a memory that changes once per chunk.  With c = 1 window row i is
+// token s + i.  Before the chunk's last token nothing has changed: S_t is
+// reported as 0 (Newton-Schulz, if any, is skipped there and adds U = 0), W_t
+// = W_bar.  At the last token S_e = eta_bar S_bar - sum_i theta_i g_i and
+// W_e = (1 - alpha_bar) W_bar + eta_bar S_bar - sum_i theta_i g_i, with
+// eta_bar, alpha_bar the chunk's mean gates.  One block per unit.
+__global__ void k_coef_chunkwise(Geom g, Chunk ch, const float* theta, const float* eta, const float* alpha,
+                                 Work w) {
+  __shared__ float red[2][32];
+  const int u = blockIdx.x;
+  const int Ct = ch.e - ch.s;
+  const size_t base = (size_t)u * g.T + ch.s;
+  float se = 0.f, sa = 0.f;
+  for (int r = threadIdx.x; r < Ct; r += blockDim.x) {
+    se += eta[base + r];
+    sa += alpha[base + r];
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    se += __shfl_xor_sync(0xffffffffu, se, o);
+    sa += __shfl_xor_sync(0xffffffffu, sa, o);
+  }
+  if (threadIdx.x % 32 == 0) {
+    red[0][threadIdx.x / 32] = se;
+    red[1][threadIdx.x / 32] = sa;
+  }
+  __syncthreads();
+  se = sa = 0.f;
+  for (int k = 0; k < (int)(blockDim.x / 32); ++k) {
+    se += red[0][k];
+    sa += red[1][k];
+  }
+  const float eb = se / Ct, ab = sa / Ct;
+  for (int e = threadIdx.x; e < Ct * ch.nw; e += blockDim.x) {
+    const int r = e / ch.nw, i = e % ch.nw;
+    const float v = r == Ct - 1 ? theta[base + i] : 0.f;
+    w.Cs[((size_t)u * g.C + r) * g.Kw + i] = v;
+    w.Cw[((size_t)u * g.C + r) * g.Kw + i] = v;
+  }
+  for (int r = threadIdx.x; r < Ct; r += blockDim.x) {
+    const bool last = r == Ct - 1;
+    w.Ap[(size_t)u * g.C + r] = last ? eb : 0.f;
+    w.Bp[(size_t)u * g.C + r] = last ? 1.f - ab : 1.f;
+    w.Dp[(size_t)u * g.C + r] = last ? eb : 0.f;
+    if (w.aeff) w.aeff[base + r] = last ? ab : 0.f;   // the decay the W scans apply
+  }
+}
+
 // ---------------------------------------------------------------- dual form
 // Read-out without Newton-Schulz.  One block per (token of chunk, unit).
 __global__ void k_dual_readout(Geom g, Chunk ch, Work w, int buf, float* y) {
@@ -241,13 +290,14 @@ __global__ void k_dual_state(Geom g, Chunk ch, Work w, int m, int buf) {
 
 // ------------------------------------------------------------ Newton-Schulz
 
-// One block per (token, matrix, unit): form S_t, orthogonalise, store U_t in
-// the token's slot of Ubuf (X orientation: the short side first).
+// One block per (token from ns_first_row on, matrix, unit): form S_t,
+// orthogonalise, store U_t in the token's slot of Ubuf (X orientation: the
+// short side first).
 // Shared memory: Am[rX*rX] + Bm[rX*rX] + 2 tiles of 16x64.
 __global__ void __launch_bounds__(256) k_ns_simt(Geom g, Chunk ch, Work w, int buf, int m, size_t slot_stride,
                                                   size_t slot_off) {
   extern __shared__ float sm[];
-  const int u = blockIdx.y, r = blockIdx.x, t = ch.s + r;
+  const int u = blockIdx.y, r = ns_first_row(g, ch) + blockIdx.x, t = ch.s + r;
   const int rows = g.rows[m], cols = g.cols[m];
   const bool tall = rows > cols;
   const int rX = tall ? cols : rows, cX = tall ? rows : cols;
@@ -349,10 +399,11 @@ __global__ void k_ns_wscan(Geom g, Chunk ch, Work w, int buf, int m, size_t slot
   const size_t xe = tall ? (size_t)b * rows + a : e;
   float W = w.Wst[buf][m][(size_t)u * n + e];
   const bool pre = g.readout == ATLAS_READOUT_PRE;
+  const int rn = ns_first_row(g, ch);   // slots before it hold no U_t: U_t = 0
   for (int t = ch.s; t < ch.e; ++t) {
     float* slot = w.Ubuf + ((size_t)u * g.C + (t - ch.s)) * slot_stride + slot_off;
     const float W_prev = W;
-    W = (1.f - alpha[(size_t)u * g.T + t]) * W + slot[xe];
+    W = (1.f - alpha[(size_t)u * g.T + t]) * W + (t - ch.s >= rn ? slot[xe] : 0.f);
     slot[xe] = pre ? W_prev : W;   // the weights token t reads out
   }
   w.Wst[buf ^ 1][m][(size_t)u * n + e] = W;
@@ -519,8 +570,15 @@ cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const G
   *nl += g.ns_iters == 0 ? 3 + g.nmat : 3 + 2 * g.nmat;
   const size_t sr = generic_smem_readout(g);
   CUDA_CHECK_RET(grad_tiled(g, ch, w, buf, st, nl));
-  const int coef_threads = ((ch.nw + 31) / 32) * 32;
-  k_coef<<<g.units, coef_threads, 3 * g.C * sizeof(float), st>>>(g, ch, io.theta, io.eta, io.alpha, w);
+  const bool chunkwise = g.update == ATLAS_UPDATE_CHUNKWISE;
+  if (chunkwise) {
+    k_coef_chunkwise<<<g.units, 256, 0, st>>>(g, ch, io.theta, io.eta, io.alpha, w);
+  } else {
+    const int coef_threads = ((ch.nw + 31) / 32) * 32;
+    k_coef<<<g.units, coef_threads, 3 * g.C * sizeof(float), st>>>(g, ch, io.theta, io.eta, io.alpha, w);
+  }
+  // the decay the W scans apply per token (chunk-wise: only at the chunk's end)
+  const float* alpha_scan = chunkwise ? w.aeff : io.alpha;
   if (g.ns_iters == 0) {
     cudaFuncSetAttribute(k_dual_readout, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sr);
     k_dual_readout<<<dim3(ch.e - ch.s, g.units), 256, sr, st>>>(g, ch, w, buf, io.y);
@@ -540,17 +598,18 @@ cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const G
   for (int m = 0; m < g.nmat; ++m) {
     const size_t sn = generic_smem_ns(g, m);
     cudaFuncSetAttribute(k_ns_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sn);
-    k_ns_simt<<<dim3(ch.e - ch.s, g.units), 256, sn, st>>>(g, ch, w, buf, m, slot_stride, off);
+    k_ns_simt<<<dim3(ch.e - ch.s - ns_first_row(g, ch), g.units), 256, sn, st>>>(g, ch, w, buf, m, slot_stride,
+                                                                                   off);
     off += (size_t)g.rows[m] * g.cols[m];
   }
   if (ns_fused_scan_supported(g)) {
     *nl -= 1;   // two fused launches replace nmat scans + one read-out
-    return ns_fused_scan(g, ch, w, buf, slot_stride, io.alpha, w.Zpre, io.y, st);
+    return ns_fused_scan(g, ch, w, buf, slot_stride, alpha_scan, w.Zpre, io.y, st);
   }
   off = 0;
   for (int m = 0; m < g.nmat; ++m) {
     const size_t n = (size_t)g.rows[m] * g.cols[m];
-    k_ns_wscan<<<dim3(cdiv(n, 256), g.units), 256, 0, st>>>(g, ch, w, buf, m, slot_stride, off, io.alpha);
+    k_ns_wscan<<<dim3(cdiv(n, 256), g.units), 256, 0, st>>>(g, ch, w, buf, m, slot_stride, off, alpha_scan);
     off += n;
   }
   const size_t srd = (size_t)(g.F + (g.depth == 2 ? g.hidden : 0)) * sizeof(float);
@@ -597,6 +656,7 @@ __global__ void __launch_bounds__(256) k_ns_scan_w1(Geom g, Chunk ch, Work w, in
   const int F = g.F, h = g.hidden, j = jb + lane, i0 = grp * RPG;
   const int Ct = ch.e - ch.s;
   const bool pre = g.readout == ATLAS_READOUT_PRE;   // read out before token r's update
+  const int rn = ns_first_row(g, ch);                 // slots before it hold no U_t: U_t = 0
   float* rq = scan_sm;                   // [C][F + 1] queries of the chunk
   float* part = rq + g.C * (F + 1);      // [C][8][33] per-group partial sums
   float* bes = part + g.C * 8 * 33;      // [C] 1 - alpha
@@ -615,7 +675,7 @@ __global__ void __launch_bounds__(256) k_ns_scan_w1(Geom g, Chunk ch, Work w, in
     for (int p = 0; p < PD; ++p) {
       const float* sl = slot0 + (size_t)(r0 + p) * slot_stride;
 #pragma unroll
-      for (int q = 0; q < RPG; ++q) cur[p][q] = r0 + p < Ct ? sl[(size_t)q * h] : 0.f;
+      for (int q = 0; q < RPG; ++q) cur[p][q] = r0 + p < Ct && r0 + p >= rn ? sl[(size_t)q * h] : 0.f;
     }
 #pragma unroll
     for (int p = 0; p < PD; ++p) {
@@ -662,6 +722,7 @@ __global__ void __launch_bounds__(256) k_ns_scan_w2(Geom g, Chunk ch, Work w, in
   const int F = g.F, h = g.hidden, d = g.d_v, j0 = lane * CPL;
   const int Ct = ch.e - ch.s;
   const bool pre = g.readout == ATLAS_READOUT_PRE;   // read out before token r's update
+  const int rn = ns_first_row(g, ch);                 // slots before it hold no U_t: U_t = 0
   float* bes = aqs + Ct * h;
   for (int e = threadIdx.x; e < Ct * h; e += 256) aqs[e] = aq[(size_t)u * g.C * h + e];
   for (int r = threadIdx.x; r < Ct; r += 256) bes[r] = 1.f - alpha[(size_t)u * g.T + ch.s + r];
@@ -678,7 +739,8 @@ __global__ void __launch_bounds__(256) k_ns_scan_w2(Geom g, Chunk ch, Work w, in
       const float* sl = slot0 + (size_t)(r0 + p) * slot_stride;
 #pragma unroll
       for (int q = 0; q < CPL; q += 4) {
-        const float4 v4 = r0 + p < Ct ? *reinterpret_cast<const float4*>(sl + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 v4 = r0 + p < Ct && r0 + p >= rn ? *reinterpret_cast<const float4*>(sl + q)
+                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
         cur[p][q] = v4.x; cur[p][q + 1] = v4.y; cur[p][q + 2] = v4.z; cur[p][q + 3] = v4.w;
       }
     }
@@ -1364,7 +1426,8 @@ __global__ void __launch_bounds__(512) k_dual1_step(Geom g, Chunk ch, Chunk nx, 
 }
 
 bool dual1_split_supported(const Geom& g) {
-  return g.depth == 1 && g.ns_iters == 0 && g.Kw <= 128 && g.C <= 64 && g.d_v <= 64;
+  return g.depth == 1 && g.ns_iters == 0 && g.update == ATLAS_UPDATE_PER_TOKEN && g.Kw <= 128 && g.C <= 64 &&
+         g.d_v <= 64;
 }
 
 size_t dual1_split_floats(const Geom& g, size_t units, int T) {

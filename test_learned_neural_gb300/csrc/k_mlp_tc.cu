@@ -282,7 +282,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
                   const float* __restrict__ theta, const float* __restrict__ eta, const float* __restrict__ alpha,
                   const float* __restrict__ gamma, const float* W0a, const float* W0b, const float* S0a,
                   const float* S0b, float* __restrict__ y, float* Woa, float* Wob, float* Soa, float* Sob,
-                  int* status, int pre) {
+                  int* status, int pre, int cwise) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ uint64_t bar;
   __shared__ uint64_t xbar[3];   // arrivals of the peers' Yp slices, dy rows, Yq slices
@@ -410,6 +410,36 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   auto scan_chunk = [&](int bn) {
     float* vb = vecb(bn);
     float* cwp = cwmb(bn);
+    if (cwise) {
+      // chunk-wise update rule (titans-pytorch store path): the memory
+      // changes once, at the chunk's last token, by S_e = eta_bar S_bar -
+      // sum_i theta_i g_i, W_e = (1 - alpha_bar) W_bar + S_e with the chunk's
+      // mean gates; every earlier token reads W_bar, the last reads W_e
+      // (post) or W_bar (pre)
+      if (tid < 64) {
+        const int i = tid;
+        const float th = vb[V_TH + i];
+        for (int t = 0; t < TOK; ++t) cwp[swz(t, i)] = (t == TOK - 1 && !pre) ? th : 0.f;
+        vb[V_CS + i] = th;
+        vb[V_CW + i] = th;
+      } else if (tid == 64) {
+        float se = 0.f, sb = 0.f;
+        for (int t = 0; t < TOK; ++t) {
+          se += vb[V_ET + t];
+          sb += vb[V_BE + t];
+        }
+        const float eb = se / TOK, bb = sb / TOK;   // mean eta, mean (1 - alpha)
+        for (int t = 0; t < TOK; ++t) {
+          const bool last = t == TOK - 1;
+          vb[V_AP + t] = last ? eb : 0.f;
+          vb[V_BP + t] = last ? bb : 1.f;
+          vb[V_DP + t] = last ? eb : 0.f;
+          vb[V_BR + t] = last && !pre ? bb : 1.f;
+          vb[V_DR + t] = last && !pre ? eb : 0.f;
+        }
+      }
+      return;
+    }
     if (tid < 64) {  // column i = tid of Cs / Cw
       const int i = tid;
       float cs = 0.f, cw = 0.f;
@@ -770,7 +800,8 @@ cudaError_t mlp_tc_launch(const Geom& g, const void* q, const void* k, const voi
   k_mlp_dual_tc<<<g.units * CS, NT, SMEM_BYTES, st>>>(g.T, Tst > 0 ? Tst : g.T, g.qkv_dtype, q, k, v, theta, eta,
                                                       alpha, gamma, W0[0],
                                                       W0[1], S0[0], S0[1], y, W_out[0], W_out[1], S_out[0],
-                                                      S_out[1], status, g.readout == ATLAS_READOUT_PRE ? 1 : 0);
+                                                      S_out[1], status, g.readout == ATLAS_READOUT_PRE ? 1 : 0,
+                                                      g.update == ATLAS_UPDATE_CHUNKWISE ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -181,15 +181,15 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
   const int rgsKp = (Kp / 8) * 128, rgsN = (n / 8) * 128, rgsR = (R / 8) * 128;
   const int c = 32 * half + csub;           // this thread's 16 columns of a 64-wide accumulator
 
-  const int Ct = ch.e - ch.s;
-  const int ntasks = g.units * g.nmat * Ct;
+  const int rn = ns_first_row(g, ch), Cn = ch.e - ch.s - rn;   // tokens [rn, Ct) of the chunk
+  const int ntasks = g.units * g.nmat * Cn;
   const int t_begin = (int)((long long)ntasks * blockIdx.x / gridDim.x);
   const int t_end = (int)((long long)ntasks * (blockIdx.x + 1) / gridDim.x);
   int loaded = -1;                          // (unit, matrix) whose long-side factor is resident
   for (int task = t_begin; task < t_end; ++task) {
-    const int r = task % Ct;
-    const int m = (task / Ct) % g.nmat;
-    const int u = task / (Ct * g.nmat);
+    const int r = rn + task % Cn;
+    const int m = (task / Cn) % g.nmat;
+    const int u = task / (Cn * g.nmat);
     const int t = ch.s + r;
     const int rows = g.rows[m], cols = g.cols[m];
     const bool tall = rows > cols;
@@ -506,12 +506,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
   uint8_t* a_lo = sm + OPR2 + R2 * R2 * 2;
   const int rgsKp = (Kp / 8) * 128, rgsN = (NH / 8) * 128, rgsR = (R2 / 8) * 128;
 
-  const int Ct = ch.e - ch.s;
-  const int ntasks = g.units * g.nmat * Ct;
+  const int rn = ns_first_row(g, ch), Cn = ch.e - ch.s - rn;   // tokens [rn, Ct) of the chunk
+  const int ntasks = g.units * g.nmat * Cn;
   for (int task = cl; task < ntasks; task += ncl) {
-    const int r = task % Ct;
-    const int m = (task / Ct) % g.nmat;
-    const int u = task / (Ct * g.nmat);
+    const int r = rn + task % Cn;
+    const int m = (task / Cn) % g.nmat;
+    const int u = task / (Cn * g.nmat);
     const int t = ch.s + r;
     const int rows = g.rows[m], cols = g.cols[m];
     const bool tall = rows > cols;
@@ -795,7 +795,7 @@ cudaError_t ns_tc_launch(const Geom& g, const Chunk& ch, const Work& w, int buf,
   if (ns_tc_kind(g) == 2) {
     cudaError_t e = cudaFuncSetAttribute(k_ns_tc128, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2);
     if (e != cudaSuccess) return e;
-    const int ntasks = g.units * g.nmat * (ch.e - ch.s);
+    const int ntasks = g.units * g.nmat * (ch.e - ch.s - ns_first_row(g, ch));
     int ncl = num_sms / 2;
     if (ncl > ntasks) ncl = ntasks;
     k_ns_tc128<<<2 * ncl, NT2, SMEM2, st>>>(g, ch, w, buf, slot_stride, Kp);
@@ -803,7 +803,7 @@ cudaError_t ns_tc_launch(const Geom& g, const Chunk& ch, const Work& w, int buf,
   }
   const int smem = ns_smem_layout(n, Kp).total;
   cudaFuncSetAttribute(k_ns_tc64, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  const int ntasks = g.units * g.nmat * (ch.e - ch.s);
+  const int ntasks = g.units * g.nmat * (ch.e - ch.s - ns_first_row(g, ch));
   const int grid = ntasks < num_sms ? ntasks : num_sms;   // each CTA takes a contiguous run of tasks
   k_ns_tc64<<<grid, NT, smem, st>>>(g, ch, w, buf, slot_stride, n, Kp);
   return cudaGetLastError();

@@ -31,7 +31,8 @@ class Memory:
         self.h = atlas_mem_create(make_config(cfg.depth, cfg.d_k, cfg.d_v, cfg.hidden if cfg.depth == 2 else 0,
                                               cfg.C, cfg.c, cfg.p, cfg.proj_dim, cfg.ns_iters, cfg.qkv_dtype,
                                               getattr(cfg, "readout", "post"),
-                                              getattr(cfg, "ns_target", "momentum")))
+                                              getattr(cfg, "ns_target", "momentum"),
+                                              getattr(cfg, "update", "per_token")))
 
     def close(self):
         if self.h is not None:

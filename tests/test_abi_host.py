@@ -56,6 +56,9 @@ def _cfg(**kw):
     (dict(ns_target=3), tln.ATLAS_ERR_INVALID_ARG),
     (dict(ns_target=1, ns_iters=5, c=40), tln.ATLAS_ERR_INVALID_ARG),
     (dict(C=1000, c=100), tln.ATLAS_ERR_UNSUPPORTED),     # window rows > 1024
+    (dict(update=2), tln.ATLAS_ERR_INVALID_ARG),
+    (dict(update="chunkwise", c=2), tln.ATLAS_ERR_INVALID_ARG),           # no Omega window on that path
+    (dict(update="chunkwise", ns_iters=5, ns_target="surprise"), tln.ATLAS_ERR_INVALID_ARG),
     (dict(d_k=256, d_v=256, hidden=512, ns_iters=5), tln.ATLAS_ERR_UNSUPPORTED),  # NS short side > 128
 ])
 def test_create_rejects(lib, kw, code):
@@ -69,7 +72,7 @@ def test_create_accepts_every_named_workload(lib):
     from harness import WORKLOADS
     for w in WORKLOADS.values():
         h = tln.atlas_mem_create(tln.make_config(w.depth, w.d_k, w.d_v, w.hidden, w.C, w.c, w.p, w.proj_dim,
-                                                 w.ns_iters, w.qkv_dtype))
+                                                 w.ns_iters, w.qkv_dtype, w.readout, w.ns_target, w.update))
         assert tln.atlas_mem_workspace_bytes(h, w.B, w.H, w.T) > 0
         tln.atlas_mem_destroy(h)
 

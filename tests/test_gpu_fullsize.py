@@ -43,7 +43,7 @@ def _sample_units(w):
 
 
 @pytest.mark.parametrize("name", ["titans_mlp", "atlas_muon", "atlas_long", "atlas_poly_c4", "atlas_poly_c16",
-                                  "atlas_muon_surprise"])
+                                  "atlas_muon_surprise", "titans_chunkwise", "atlas_muon_chunkwise"])
 def test_full_size_prefix(gpu_lib, name):
     from test_learned_neural_gb300.runner import tensors_from_numpy
     w = WORKLOADS[name]
@@ -63,7 +63,8 @@ def _to64(t, dtype):
     return bf16_from_bits(a).astype(np.float64) if dtype == "bf16" else a.astype(np.float64)
 
 
-@pytest.mark.parametrize("name", ["titans_mlp", "atlas_muon", "atlas_long"])
+@pytest.mark.parametrize("name", ["titans_mlp", "atlas_muon", "atlas_long", "titans_chunkwise",
+                                  "atlas_muon_chunkwise"])
 def test_full_size_last_chunk(gpu_lib, name):
     from test_learned_neural_gb300.runner import tensors_from_numpy
     w = WORKLOADS[name]

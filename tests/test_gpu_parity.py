@@ -206,3 +206,32 @@ def test_repeated_calls_replay_identically(gpu_lib, name):
         assert torch.equal(out["W"][m], ref["W"][m])
     mem.close()
     fresh.close()
+
+
+CHUNKWISE = [
+    ("linear_f32", dict()),                                 # depth 1, fp32, 16 chunks
+    ("linear_f32", dict(ns_iters=5)),                       # depth 1 with Muon (SIMT Newton-Schulz)
+    ("titans_chunkwise", dict(B=1, H=2, T=256)),            # MLP 64 -> 256 -> 64
+    ("atlas_poly_c4", dict(B=1, H=2, T=256, c=1)),          # degree-2 features (561 wide)
+    ("atlas_muon_chunkwise", dict(B=1, H=1, T=128)),        # Muon on 128 x 512 (CTA-pair kernel)
+    ("atlas_long", dict(B=1, H=2, T=192, c=1)),             # projected features, Muon short side 64
+]
+
+
+@pytest.mark.parametrize("case", CHUNKWISE, ids=lambda c: c[0] + ("_ns" if c[1].get("ns_iters") else ""))
+@pytest.mark.parametrize("readout", ["post", "pre"])
+def test_small_parity_chunkwise(gpu_lib, case, readout):
+    """The titans-pytorch chunk-wise store path (atlas-torch README, "Bug
+    Fixes": per_token_updates): one summed gradient, pooled gates and one
+    momentum / decay step per chunk, Newton-Schulz once per chunk."""
+    name, kw = case
+    w = WORKLOADS[name].scaled(update="chunkwise", readout=readout, **kw)
+    errs = compare(w)
+    tol = TOL[w.qkv_dtype]
+    print(name, "chunkwise", readout, {k: f"{v:.2e}" for k, v in errs.items()})
+    assert errs["y"] <= tol
+    for k, v in errs.items():
+        if k.startswith("W"):
+            assert v <= tol, (k, v)
+        if k.startswith("S"):
+            assert v <= 5 * tol, (k, v)
