@@ -123,3 +123,62 @@ WORKLOADS = {
 
 def get_workload(name: str) -> Workload:
     return WORKLOADS[name]
+
+
+@dataclasses.dataclass(frozen=True)
+class Prologue:
+    """The stage in front of the memory: x [B, T, D] -> q, k, v [B, H, T, d]
+    and the gates [B, H, T] through one projection, a causal depthwise
+    convolution of ``conv`` taps on the q/k/v channels, q/k L2 normalisation
+    and one sigmoid head per gate and head."""
+    name: str
+    D: int              # model width
+    H: int
+    d_k: int
+    d_v: int
+    conv: int           # taps of the short causal convolution (4 on the pages)
+    with_gamma: bool    # a fourth gate head gives the Omega weights gamma
+    theta_max: float    # theta = theta_max * sigmoid(.)
+    qkv_dtype: str      # type of x, W_in and the q, k, v outputs
+    B: int
+    T: int
+    seed: int
+    alpha_bias: float = -4.0   # bias of the decay head (the memory inputs' alpha mean)
+
+    @property
+    def G(self) -> int:
+        return 4 if self.with_gamma else 3
+
+    @property
+    def Nc(self) -> int:
+        """Convolved channels: the q, k and v heads."""
+        return self.H * (2 * self.d_k + self.d_v)
+
+    @property
+    def N(self) -> int:
+        """Projection width: the q/k/v channels, then G logit columns per head."""
+        return self.Nc + self.G * self.H
+
+    @property
+    def tokens(self) -> int:
+        return self.B * self.T
+
+    def scaled(self, **kw) -> "Prologue":
+        return dataclasses.replace(self, **kw)
+
+
+PROLOGUES = {
+    # In front of the Titans memory (8 heads of 64 on a 512-wide model).
+    "titans_prologue": Prologue(
+        "titans_prologue", D=512, H=8, d_k=64, d_v=64, conv=4, with_gamma=False, theta_max=0.1,
+        qkv_dtype="bf16", B=4, T=4096, seed=11),
+    # The atlas-torch configuration example: 768 wide, 16 heads of 48,
+    # with the Omega weights' gate head.
+    "atlas_prologue": Prologue(
+        "atlas_prologue", D=768, H=16, d_k=48, d_v=48, conv=4, with_gamma=True, theta_max=0.1,
+        qkv_dtype="bf16", B=2, T=8192, seed=12),
+    # fp32 throughout, odd widths.
+    "small_prologue_f32": Prologue(
+        "small_prologue_f32", D=40, H=3, d_k=8, d_v=12, conv=4, with_gamma=True, theta_max=0.1,
+        qkv_dtype="f32", B=2, T=100, seed=13),
+}

@@ -110,3 +110,24 @@ def unit_slice(inp: dict, w: Workload, units) -> dict:
                     for m in inp[key]]
     sel["P"] = inp["P"]
     return sel
+
+
+def make_prologue_inputs(p, cache=False) -> dict:
+    """Seeded inputs of the stage in front of the memory.
+
+    One ``default_rng(seed)``, drawing in order: x ~ N(0, 1) [B, T, D];
+    W_in ~ N(0, 1 / D) [D, N]; conv taps ~ N(0, 1 / conv) [Nc, conv]; gate
+    biases (theta 0, eta 1, alpha ``alpha_bias``, gamma 0, the centres of the
+    memory inputs' gate draws) plus N(0, 0.1) per head [G, H]; with
+    ``cache``, a carried convolution cache ~ N(0, 1) [B, conv - 1, Nc].
+    x and W_in are stored in ``qkv_dtype``; the rest is float32."""
+    rng = np.random.default_rng(p.seed)
+    f32 = np.float32
+    out = {}
+    out["x"] = _store(rng.standard_normal((p.B, p.T, p.D)), p.qkv_dtype)
+    out["W_in"] = _store(rng.normal(0.0, np.sqrt(1.0 / p.D), (p.D, p.N)), p.qkv_dtype)
+    out["conv_w"] = rng.normal(0.0, np.sqrt(1.0 / p.conv), (p.Nc, p.conv)).astype(f32)
+    centres = np.array([0.0, 1.0, p.alpha_bias, 0.0][:p.G])
+    out["gate_b"] = (centres[:, None] + rng.normal(0.0, 0.1, (p.G, p.H))).astype(f32)
+    out["cache"] = (rng.standard_normal((p.B, p.conv - 1, p.Nc)).astype(f32) if cache else None)
+    return out

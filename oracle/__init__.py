@@ -16,3 +16,4 @@ from .atlas_oracle import (  # noqa: F401
     token_gradients,
     unit_inputs,
 )
+from .prologue import prologue_row  # noqa: F401,E402

@@ -142,3 +142,43 @@ def _chunkwise(depth, C, ns_iters, feat, keys, vals, gams, n_prev, q, theta, eta
             reads = W if (t == e - 1 and not pre) else W_bar
             y.append(apply_mem(reads, feat(q[t]), depth))
     return np.array(y), W, S
+
+
+def prologue(H, d_k, d_v, K, with_gamma, theta_max, x, W_in, conv_w, gate_b, cache=None):
+    """The stage in front of the memory as scalar loops: every projected
+    channel is a dot product over the model width, the convolution walks its
+    taps backwards in time, norms are square roots of explicit sums, and the
+    sigmoid is math.exp.  Returns per head lists of q, k, v rows and gate
+    values, and the outgoing cache rows."""
+    T, D = len(x), len(x[0])
+    N = len(W_in[0])
+    Nc = H * (2 * d_k + d_v)
+    G = 4 if with_gamma else 3
+    u = [[sum(float(x[t][i]) * float(W_in[i][n]) for i in range(D)) for n in range(N)] for t in range(T)]
+    past = [[0.0] * Nc for _ in range(K - 1)] if cache is None else [[float(a) for a in row] for row in cache]
+    rows = past + [r[:Nc] for r in u]
+
+    def conv(t, c):
+        return sum(float(conv_w[c][K - 1 - j]) * rows[K - 1 + t - j][c] for j in range(K))
+
+    out = {"q": [], "k": [], "v": []}
+    for h in range(H):
+        for name, base, d, norm in (("q", h * d_k, d_k, True), ("k", H * d_k + h * d_k, d_k, True),
+                                    ("v", 2 * H * d_k + h * d_v, d_v, False)):
+            seq = []
+            for t in range(T):
+                vec = [conv(t, base + i) for i in range(d)]
+                if norm:
+                    n2 = math.sqrt(sum(a * a for a in vec))
+                    vec = [a / max(n2, 1e-12) for a in vec]
+                seq.append(vec)
+            out[name].append(seq)
+    for g, name in enumerate(("theta", "eta", "alpha", "gamma")):
+        if g >= G:
+            out[name] = None
+            continue
+        out[name] = [[(theta_max if name == "theta" else 1.0)
+                      / (1.0 + math.exp(-(u[t][Nc + g * H + h] + float(gate_b[g][h])))) for t in range(T)]
+                     for h in range(H)]
+    out["cache"] = rows[len(rows) - (K - 1):]
+    return out
