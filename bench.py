@@ -31,7 +31,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from harness import WORKLOADS, make_inputs  # noqa: E402
+from harness import PROLOGUES, WORKLOADS, make_inputs, make_prologue_inputs  # noqa: E402
 
 METRIC = "memory-layer tokens/s (B*H*T/s) on 1 GB300"
 
@@ -394,18 +394,120 @@ def run_ours(args):
     return 0
 
 
+# ------------------------------------------- stage in front of the memory
+PROLOGUE_METRIC = "stage tokens/s (B*T/s, x -> q, k, v, gates) on 1 GB300"
+
+
+def prologue_bytes_per_step(p) -> float:
+    """Algorithmic bytes of one call: x and W_in read, taps and biases read,
+    q, k, v and the gates written (the fp32 projection in between is the
+    implementation's, not the method's)."""
+    es = 2 if p.qkv_dtype == "bf16" else 4
+    return (p.tokens * p.D * es + p.D * p.N * es + 4 * (p.Nc * p.conv + p.G * p.H)
+            + p.tokens * p.H * (es * (2 * p.d_k + p.d_v) + 4 * p.G))
+
+
+def time_prologue_oracle(p, T=1024):
+    """The oracle on the first T tokens of batch row 0 (one process)."""
+    import oracle
+    inp = make_prologue_inputs(p.scaled(B=1))
+    from harness import bf16_from_bits
+    dec = (lambda a: bf16_from_bits(a).astype(np.float64)) if p.qkv_dtype == "bf16" else (lambda a: a.astype(np.float64))
+    x, W = dec(inp["x"])[0, :T], dec(inp["W_in"])
+    t0 = time.perf_counter()
+    oracle.prologue_row(p, x, W, inp["conv_w"], inp["gate_b"])
+    dt = time.perf_counter() - t0
+    return T / dt, 1, f"batch row 0 x first {T} tokens of {p.name} (fp64 numpy, one process)"
+
+
+def run_prologue(args):
+    import torch
+    from test_learned_neural_gb300.runner import Prologue, prologue_tensors_from_numpy
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    p = PROLOGUES[args.workload]
+    if args.impl == "reference":
+        tps, cores, desc = time_prologue_oracle(p)
+        print(json.dumps({"impl": "reference", "metric": PROLOGUE_METRIC, "value": tps, "unit": "tokens/s",
+                          "n_gpus": args.gpus, "steps": 1, "warmup": 0, "ms_per_step": 1e3 * p.tokens / tps,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic (seeded, harness recipe)", "config": {"workload": p.name},
+                          "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                           "sample": desc},
+                          "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return 0
+    torch.cuda.set_device(0)
+    inp = make_prologue_inputs(p)
+    pro = Prologue(p)
+    t = prologue_tensors_from_numpy(inp)
+    out = pro.alloc_outputs(p.B, p.T, "cuda")
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(max(args.warmup, 0)):
+        pro.forward(t, out=out)
+    torch.cuda.synchronize()
+    clocks = ClockSampler()
+    clocks.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        pro.forward(t, out=out)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_s = sum(step_ms) / 1e3
+    peaks, src = measured_peaks()
+    byt = prologue_bytes_per_step(p)
+    achieved = byt / (statistics.mean(step_ms) / 1e3) / 1e9
+    peak = peaks.get("hbm_gbs", 6800.0)
+    line = {
+        "metric": PROLOGUE_METRIC, "value": p.tokens * args.steps / total_s, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": p.qkv_dtype,
+        "data": "synthetic (seeded, harness recipe), inputs resident in HBM",
+        "config": {"workload": p.name, "B": p.B, "T": p.T, "D": p.D, "H": p.H, "d_k": p.d_k, "d_v": p.d_v,
+                   "conv": p.conv, "l2": "flushed between timed steps (256 MB write)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "peak_source": f"hbm_gbs ({src})",
+                     "kernel": "whole stage (cuBLAS projection + k_prologue, 2 launches per step)",
+                     "algorithmic_bytes_per_step": byt,
+                     "algorithmic_flops_per_step": 2.0 * p.tokens * p.D * p.N},
+        "gpu_launches": 1 * args.steps,
+        "e2e": None,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_cpu_baseline:
+        tps, cores, desc = time_prologue_oracle(p)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+    pro.close()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="titans_mlp", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="titans_mlp", choices=sorted(WORKLOADS) + sorted(PROLOGUES))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.workload in PROLOGUES:
+        return run_prologue(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -20,10 +20,12 @@ ATLAS_NS_MOMENTUM, ATLAS_NS_SURPRISE = 0, 1
 ATLAS_UPDATE_PER_TOKEN, ATLAS_UPDATE_CHUNKWISE = 0, 1
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "OOM", 5: "TIMEOUT"}
 
-# exported symbols, as declared in include/atlas_mem.h
+# exported symbols, as declared in include/atlas_mem.h and include/atlas_prologue.h
 EXPORTS = ("atlas_mem_create", "atlas_mem_forward", "atlas_mem_forward_host", "atlas_mem_forward_noalloc",
            "atlas_mem_status",
-           "atlas_mem_workspace_bytes", "atlas_mem_last_launches", "atlas_mem_last_error", "atlas_mem_destroy")
+           "atlas_mem_workspace_bytes", "atlas_mem_last_launches", "atlas_mem_last_error", "atlas_mem_destroy",
+           "atlas_prologue_create", "atlas_prologue_forward", "atlas_prologue_workspace_bytes",
+           "atlas_prologue_last_error", "atlas_prologue_destroy")
 
 
 class atlas_mem_config(ctypes.Structure):
@@ -48,6 +50,18 @@ class atlas_mem_io(ctypes.Structure):
         ("W_out", _vp * 2), ("S_out", _vp * 2),
         ("win_k_out", _vp), ("win_v_out", _vp), ("win_gamma_out", _vp),
     ]
+
+
+class atlas_prologue_config(ctypes.Structure):
+    _fields_ = [("D", ctypes.c_int), ("H", ctypes.c_int), ("d_k", ctypes.c_int), ("d_v", ctypes.c_int),
+                ("conv", ctypes.c_int), ("with_gamma", ctypes.c_int), ("theta_max", ctypes.c_float),
+                ("qkv_dtype", ctypes.c_int)]
+
+
+class atlas_prologue_io(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int)] + [
+        (n, _vp) for n in ("x", "W_in", "conv_w", "gate_b", "cache", "q", "k", "v", "theta", "eta", "alpha",
+                           "gamma", "cache_out")]
 
 
 class AtlasError(RuntimeError):
@@ -83,6 +97,16 @@ def load(path: str = LIB_PATH):
     lib.atlas_mem_last_error.restype = ctypes.c_char_p
     lib.atlas_mem_destroy.argtypes = [ctypes.c_void_p]
     lib.atlas_mem_destroy.restype = None
+    lib.atlas_prologue_create.argtypes = [ctypes.POINTER(atlas_prologue_config), ctypes.POINTER(ctypes.c_void_p)]
+    lib.atlas_prologue_create.restype = ctypes.c_int
+    lib.atlas_prologue_forward.argtypes = [ctypes.c_void_p, ctypes.POINTER(atlas_prologue_io), ctypes.c_void_p]
+    lib.atlas_prologue_forward.restype = ctypes.c_int
+    lib.atlas_prologue_workspace_bytes.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
+    lib.atlas_prologue_workspace_bytes.restype = ctypes.c_size_t
+    lib.atlas_prologue_last_error.argtypes = [ctypes.c_void_p]
+    lib.atlas_prologue_last_error.restype = ctypes.c_char_p
+    lib.atlas_prologue_destroy.argtypes = [ctypes.c_void_p]
+    lib.atlas_prologue_destroy.restype = None
     _lib = lib
     return lib
 
@@ -133,6 +157,39 @@ def atlas_mem_last_launches(h) -> int:
 
 def atlas_mem_last_error(h) -> str:
     return load().atlas_mem_last_error(h).decode()
+
+
+def atlas_prologue_create(cfg: atlas_prologue_config):
+    lib = load()
+    h = ctypes.c_void_p()
+    rc = lib.atlas_prologue_create(ctypes.byref(cfg), ctypes.byref(h))
+    if rc:
+        raise AtlasError(rc, lib.atlas_prologue_last_error(None).decode())
+    return h
+
+
+def atlas_prologue_forward(h, io: atlas_prologue_io, stream: int = 0):
+    lib = load()
+    rc = lib.atlas_prologue_forward(h, ctypes.byref(io), ctypes.c_void_p(stream))
+    if rc:
+        raise AtlasError(rc, lib.atlas_prologue_last_error(h).decode())
+
+
+def atlas_prologue_workspace_bytes(h, B, T) -> int:
+    return load().atlas_prologue_workspace_bytes(h, B, T)
+
+
+def atlas_prologue_last_error(h) -> str:
+    return load().atlas_prologue_last_error(h).decode()
+
+
+def atlas_prologue_destroy(h):
+    load().atlas_prologue_destroy(h)
+
+
+def make_prologue_config(D, H, d_k, d_v, conv, with_gamma, theta_max, qkv_dtype) -> atlas_prologue_config:
+    dt = {"f32": ATLAS_F32, "bf16": ATLAS_BF16}.get(qkv_dtype, qkv_dtype)
+    return atlas_prologue_config(D, H, d_k, d_v, conv, int(with_gamma), theta_max, dt)
 
 
 def atlas_mem_destroy(h):

@@ -1,0 +1,306 @@
+// The stage in front of the memory: projection (one cuBLAS GEMM into the
+// workspace), then one kernel for the causal depthwise convolution, the q/k
+// normalisation, the gate heads, the layout change to [B][H][T][d] and the
+// outgoing convolution cache.
+#include <cublas_v2.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <string>
+
+#include "../../include/atlas_prologue.h"
+
+namespace {
+
+constexpr int kTok = 64;        // tokens per CTA
+constexpr int kThreads = 256;
+constexpr int kMaxTaps = 8;
+constexpr int kMaxHeadCh = 512; // 2 d_k + d_v
+
+struct PGeom {
+  int D, H, dk, dv, K, G, Ch, Nc, N, dtype;
+  float theta_max;
+  int Np;     // row stride of the fp32 projection: N rounded up to 4 floats (16 bytes)
+};
+
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
+}
+
+size_t pro_smem_bytes(const PGeom& p) {
+  // U rows with the K-1 halo, then the taps [K][Ch]
+  return ((size_t)(kTok + p.K - 1) * p.Ch + (size_t)p.K * p.Ch) * sizeof(float);
+}
+
+// global channel of the head's local channel c (q: [0, dk), k: [dk, 2dk), v: [2dk, Ch))
+__device__ __forceinline__ int head_channel(const PGeom& p, int h, int c) {
+  if (c < p.dk) return h * p.dk + c;
+  if (c < 2 * p.dk) return p.H * p.dk + h * p.dk + (c - p.dk);
+  return 2 * p.H * p.dk + h * p.dv + (c - 2 * p.dk);
+}
+
+__device__ __forceinline__ void store_out(void* base, size_t i, float v, int dtype) {
+  if (dtype == ATLAS_BF16)
+    reinterpret_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
+  else
+    reinterpret_cast<float*>(base)[i] = v;
+}
+
+// One CTA per (64-token tile, head, batch row).  The head's projected rows
+// (with the K-1 halo) come into shared memory by cp.async, 16-byte copies
+// where every segment is a multiple of 4 floats (vec), all in flight before
+// one wait.  Then lane l of every warp owns the head's channels l, l + 32,
+// ...; a warp takes whole token rows, so the q and k norms are one warp
+// reduction and no row leaves registers between the convolution and the
+// store.
+template <int kSlots>   // channels per lane: ceil(Ch / 32) rounded up to an instantiated count
+__global__ void __launch_bounds__(kThreads) k_prologue(PGeom p, int T, const float* __restrict__ U,
+                                                       const float* __restrict__ conv_w,
+                                                       const float* __restrict__ gate_b,
+                                                       const float* __restrict__ cache, void* q, void* k, void* v,
+                                                       float* theta, float* eta, float* alpha, float* gamma,
+                                                       float* cache_out, int vec) {
+  extern __shared__ float sm[];
+  const int t0 = blockIdx.x * kTok, h = blockIdx.y, b = blockIdx.z;
+  const int K = p.K, Ch = p.Ch, rows = kTok + K - 1;
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  constexpr int NW = kThreads / 32;
+  float* Us = sm;                          // [rows][Ch]: token t0 - (K-1) + r
+  float* taps = Us + (size_t)rows * Ch;    // [K][Ch]
+  const size_t urow = (size_t)b * T;       // first U row of this batch row
+  int gcs[kSlots];                         // global channel of each owned channel
+#pragma unroll
+  for (int i = 0; i < kSlots; ++i) gcs[i] = lane + 32 * i < Ch ? head_channel(p, h, lane + 32 * i) : 0;
+  for (int j = warp; j < K; j += NW)
+#pragma unroll
+    for (int i = 0; i < kSlots; ++i)
+      if (lane + 32 * i < Ch) taps[j * Ch + lane + 32 * i] = conv_w[(size_t)gcs[i] * K + j];
+  {
+    const int wv = vec ? 4 : 1, nv = Ch / wv;
+    for (int e = threadIdx.x; e < rows * nv; e += kThreads) {
+      const int r = e / nv, c = (e - r * nv) * wv, t = t0 - (K - 1) + r;
+      float* dst = Us + r * Ch + c;
+      const float* src = nullptr;
+      if (t >= 0 && t < T)
+        src = U + (urow + t) * p.Np + head_channel(p, h, c);
+      else if (t < 0 && cache)
+        src = cache + ((size_t)b * (K - 1) + (K - 1) + t) * p.Nc + head_channel(p, h, c);
+      if (src) {
+        if (vec)
+          cp_async16(dst, src);
+        else
+          cp_async4(dst, src);
+      } else {
+        for (int q4 = 0; q4 < wv; ++q4) dst[q4] = 0.f;
+      }
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+  }
+  __syncthreads();
+  const size_t uh = (size_t)b * p.H + h;   // (batch, head) index of the outputs
+  for (int r = warp; r < kTok; r += NW) {
+    const int t = t0 + r;
+    if (t >= T) break;
+    float val[kSlots];
+    float sq = 0.f, sk = 0.f;
+#pragma unroll
+    for (int i = 0; i < kSlots; ++i) {
+      const int c = lane + 32 * i;
+      float acc = 0.f;
+      if (c < Ch) {
+        for (int j = 0; j < K; ++j) acc += taps[(K - 1 - j) * Ch + c] * Us[(r + K - 1 - j) * Ch + c];
+        if (c < p.dk) sq += acc * acc;
+        else if (c < 2 * p.dk) sk += acc * acc;
+      }
+      val[i] = acc;
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      sk += __shfl_xor_sync(0xffffffffu, sk, o);
+    }
+    const float iq = 1.f / fmaxf(sqrtf(sq), 1e-12f), ik = 1.f / fmaxf(sqrtf(sk), 1e-12f);
+#pragma unroll
+    for (int i = 0; i < kSlots; ++i) {
+      const int c = lane + 32 * i;
+      if (c >= Ch) continue;
+      if (c < p.dk)
+        store_out(q, (uh * T + t) * p.dk + c, val[i] * iq, p.dtype);
+      else if (c < 2 * p.dk)
+        store_out(k, (uh * T + t) * p.dk + (c - p.dk), val[i] * ik, p.dtype);
+      else
+        store_out(v, (uh * T + t) * p.dv + (c - 2 * p.dk), val[i], p.dtype);
+    }
+  }
+  for (int e = threadIdx.x; e < p.G * kTok; e += kThreads) {
+    const int g = e / kTok, r = e % kTok, t = t0 + r;
+    if (t >= T) continue;
+    const float l = U[(urow + t) * p.Np + p.Nc + (size_t)g * p.H + h] + gate_b[g * p.H + h];
+    const float s = 1.f / (1.f + expf(-l));
+    float* dst = g == 0 ? theta : g == 1 ? eta : g == 2 ? alpha : gamma;
+    dst[uh * T + t] = g == 0 ? p.theta_max * s : s;
+  }
+  // the last K-1 projected rows (from the earlier cache where T < K-1), by
+  // the CTA that holds token T-1
+  if (cache_out && t0 <= T - 1 && T - 1 < t0 + kTok) {
+    for (int i = warp; i < K - 1; i += NW) {
+      const int t = T - (K - 1) + i;
+      const float* src = nullptr;
+      if (t >= 0)
+        src = U + (urow + t) * p.Np;
+      else if (cache)
+        src = cache + ((size_t)b * (K - 1) + (K - 1) + t) * p.Nc;
+      float* dst = cache_out + ((size_t)b * (K - 1) + i) * p.Nc;
+#pragma unroll
+      for (int s2 = 0; s2 < kSlots; ++s2)
+        if (lane + 32 * s2 < Ch) dst[gcs[s2]] = src ? src[gcs[s2]] : 0.f;
+    }
+  }
+}
+
+}  // namespace
+
+struct atlas_prologue_handle {
+  atlas_prologue_config cfg;
+  PGeom p;
+  cublasHandle_t blas = nullptr;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  std::string err;
+};
+
+static thread_local std::string g_pro_create_err;
+
+static int pfail(atlas_prologue_handle* h, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (h) h->err = buf;
+  return code;
+}
+
+extern "C" int atlas_prologue_create(const atlas_prologue_config* cfg, atlas_prologue_handle** out) {
+  if (!out || !cfg) {
+    g_pro_create_err = "cfg and out must be non-NULL";
+    if (out) *out = nullptr;
+    return ATLAS_ERR_INVALID_ARG;
+  }
+  *out = nullptr;
+  const atlas_prologue_config& c = *cfg;
+  auto bad = [&](int code, const char* why) {
+    g_pro_create_err = why;
+    return code;
+  };
+  if (c.D < 1 || c.H < 1 || c.d_k < 1 || c.d_v < 1) return bad(ATLAS_ERR_INVALID_ARG, "D, H, d_k, d_v must be >= 1");
+  if (c.conv < 1) return bad(ATLAS_ERR_INVALID_ARG, "conv (taps) must be >= 1");
+  if (c.with_gamma != 0 && c.with_gamma != 1) return bad(ATLAS_ERR_INVALID_ARG, "with_gamma must be 0 or 1");
+  if (!(c.theta_max > 0.f) || !isfinite(c.theta_max)) return bad(ATLAS_ERR_INVALID_ARG, "theta_max must be > 0");
+  if (c.qkv_dtype != ATLAS_F32 && c.qkv_dtype != ATLAS_BF16)
+    return bad(ATLAS_ERR_INVALID_ARG, "qkv_dtype must be ATLAS_F32 or ATLAS_BF16");
+  if (c.conv > kMaxTaps) return bad(ATLAS_ERR_UNSUPPORTED, "more than 8 convolution taps are not supported");
+  if (2LL * c.d_k + c.d_v > kMaxHeadCh) return bad(ATLAS_ERR_UNSUPPORTED, "2 d_k + d_v > 512 per head is not supported");
+  const long long Nc = (long long)c.H * (2 * c.d_k + c.d_v), N = Nc + (3LL + c.with_gamma) * c.H;
+  if (N > (1LL << 24) || c.D > (1 << 24)) return bad(ATLAS_ERR_UNSUPPORTED, "projection wider than 2^24 is not supported");
+  auto* h = new atlas_prologue_handle();
+  h->cfg = c;
+  h->p = PGeom{c.D, c.H, c.d_k, c.d_v, c.conv, 3 + c.with_gamma, 2 * c.d_k + c.d_v, (int)Nc, (int)N, c.qkv_dtype,
+               c.theta_max, (int)((N + 3) / 4 * 4)};
+  *out = h;
+  return ATLAS_OK;
+}
+
+extern "C" size_t atlas_prologue_workspace_bytes(const atlas_prologue_handle* h, int B, int T) {
+  if (!h || B < 1 || T < 1) return 0;
+  return (size_t)B * T * h->p.Np * sizeof(float);
+}
+
+extern "C" const char* atlas_prologue_last_error(const atlas_prologue_handle* h) {
+  return h ? h->err.c_str() : g_pro_create_err.c_str();
+}
+
+extern "C" void atlas_prologue_destroy(atlas_prologue_handle* h) {
+  if (!h) return;
+  if (h->blas) cublasDestroy(h->blas);
+  if (h->ws) cudaFree(h->ws);
+  delete h;
+}
+
+extern "C" int atlas_prologue_forward(atlas_prologue_handle* h, const atlas_prologue_io* io, void* stream) {
+  if (!h) return ATLAS_ERR_INVALID_ARG;
+  if (!io) return pfail(h, ATLAS_ERR_INVALID_ARG, "io must be non-NULL");
+  const PGeom& p = h->p;
+  if (io->B < 1 || io->T < 1) return pfail(h, ATLAS_ERR_INVALID_ARG, "B and T must be >= 1");
+  if (io->B > 65535) return pfail(h, ATLAS_ERR_UNSUPPORTED, "B > 65535 is not supported");
+  if (!io->x || !io->W_in || !io->conv_w || !io->gate_b || !io->q || !io->k || !io->v || !io->theta || !io->eta ||
+      !io->alpha)
+    return pfail(h, ATLAS_ERR_INVALID_ARG, "x, W_in, conv_w, gate_b, q, k, v, theta, eta, alpha must be non-NULL");
+  if ((p.G == 4) != (io->gamma != nullptr))
+    return pfail(h, ATLAS_ERR_INVALID_ARG, "gamma must be given exactly when with_gamma is set");
+  if (io->cache_out && io->cache_out == io->cache)
+    return pfail(h, ATLAS_ERR_INVALID_ARG, "cache_out must not alias cache");
+  const long long M = (long long)io->B * io->T;
+  if (M > (1LL << 31) / 2 || M * p.N > (1LL << 40))
+    return pfail(h, ATLAS_ERR_UNSUPPORTED, "B * T too large for one projection");
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t need = atlas_prologue_workspace_bytes(h, io->B, io->T);
+  if (h->ws_bytes < need) {
+    if (h->ws) {
+      cudaError_t e = cudaStreamSynchronize(st);
+      if (e != cudaSuccess) return pfail(h, ATLAS_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+      cudaFree(h->ws);
+      h->ws = nullptr;
+      h->ws_bytes = 0;
+    }
+    cudaError_t e = cudaMalloc(&h->ws, need);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      h->ws = nullptr;
+      return pfail(h, ATLAS_ERR_OOM, "cudaMalloc(%zu) failed: %s", need, cudaGetErrorString(e));
+    }
+    h->ws_bytes = need;
+  }
+  if (!h->blas) {
+    cublasStatus_t s = cublasCreate(&h->blas);
+    if (s != CUBLAS_STATUS_SUCCESS) {
+      h->blas = nullptr;
+      return pfail(h, ATLAS_ERR_CUDA, "cublasCreate failed (status %d)", (int)s);
+    }
+  }
+  cublasStatus_t s = cublasSetStream(h->blas, st);
+  if (s != CUBLAS_STATUS_SUCCESS) return pfail(h, ATLAS_ERR_CUDA, "cublasSetStream failed (status %d)", (int)s);
+  // U [M][N] row-major = x [M][D] W_in [D][N]; in cuBLAS's column-major
+  // terms U^T (N x M) = W_in^T (N x D) x^T (D x M), fp32 accumulation
+  const float one = 1.f, zero = 0.f;
+  const cudaDataType_t in_t = p.dtype == ATLAS_BF16 ? CUDA_R_16BF : CUDA_R_32F;
+  s = cublasGemmEx(h->blas, CUBLAS_OP_N, CUBLAS_OP_N, p.N, (int)M, p.D, &one, io->W_in, in_t, p.N, io->x, in_t, p.D,
+                   &zero, h->ws, CUDA_R_32F, p.Np, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+  if (s != CUBLAS_STATUS_SUCCESS) return pfail(h, ATLAS_ERR_CUDA, "cublasGemmEx failed (status %d)", (int)s);
+  const size_t smem = pro_smem_bytes(p);
+  const int slots = (p.Ch + 31) / 32;
+  auto kern = slots <= 2 ? k_prologue<2> : slots <= 4 ? k_prologue<4> : slots <= 6 ? k_prologue<6>
+            : slots <= 8 ? k_prologue<8> : slots <= 12 ? k_prologue<12> : k_prologue<16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return pfail(h, ATLAS_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  dim3 grid((io->T + kTok - 1) / kTok, p.H, io->B);
+  // 16-byte copies need every head segment, the projection's row stride and
+  // the caller's cache rows on 16-byte boundaries
+  const float* cache = p.K > 1 ? io->cache : nullptr;
+  const int vec = p.dk % 4 == 0 && p.dv % 4 == 0 && ((uintptr_t)cache % 16) == 0;
+  kern<<<grid, kThreads, smem, st>>>(p, io->T, (const float*)h->ws, io->conv_w, io->gate_b, cache, io->q, io->k,
+                                     io->v, io->theta, io->eta, io->alpha, io->gamma,
+                                     p.K > 1 ? io->cache_out : nullptr, vec);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return pfail(h, ATLAS_ERR_CUDA, "k_prologue launch: %s", cudaGetErrorString(e));
+  return ATLAS_OK;
+}

@@ -11,7 +11,9 @@ import numpy as np
 import torch
 
 from . import (ATLAS_BF16, ATLAS_F32, atlas_mem_create, atlas_mem_destroy, atlas_mem_forward,
-               atlas_mem_forward_host, atlas_mem_status, current_stream, make_config, make_io, AtlasError)
+               atlas_mem_forward_host, atlas_mem_status, atlas_prologue_create, atlas_prologue_destroy,
+               atlas_prologue_forward, atlas_prologue_io, current_stream, make_config, make_io,
+               make_prologue_config, AtlasError)
 
 
 def matrix_shapes(cfg):
@@ -106,3 +108,63 @@ def tensors_from_numpy(inp: dict, device="cuda", pin=False):
     out["W0"] = [conv(m) for m in inp["W0"]]
     out["S0"] = [conv(m) for m in inp["S0"]]
     return out
+
+
+class Prologue:
+    """A configured stage in front of the memory (one library handle):
+    x [B, T, D] -> q, k, v [B, H, T, d] and the gates [B, H, T]."""
+
+    def __init__(self, cfg):
+        self.cfg = cfg
+        self.qkv_torch = torch.float32 if cfg.qkv_dtype in ("f32", ATLAS_F32) else torch.bfloat16
+        self.h = atlas_prologue_create(make_prologue_config(cfg.D, cfg.H, cfg.d_k, cfg.d_v, cfg.conv,
+                                                            cfg.with_gamma, cfg.theta_max, cfg.qkv_dtype))
+
+    def close(self):
+        if self.h is not None:
+            atlas_prologue_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def alloc_outputs(self, B, T, device):
+        c, f32 = self.cfg, torch.float32
+        out = dict(q=torch.empty((B, c.H, T, c.d_k), dtype=self.qkv_torch, device=device),
+                   k=torch.empty((B, c.H, T, c.d_k), dtype=self.qkv_torch, device=device),
+                   v=torch.empty((B, c.H, T, c.d_v), dtype=self.qkv_torch, device=device))
+        for g in ("theta", "eta", "alpha") + (("gamma",) if c.with_gamma else ()):
+            out[g] = torch.empty((B, c.H, T), dtype=f32, device=device)
+        if c.conv > 1:
+            out["cache"] = torch.empty((B, c.conv - 1, c.Nc), dtype=f32, device=device)
+        return out
+
+    def forward(self, t, out=None, stream=None):
+        """t: dict of device tensors x, W_in, conv_w, gate_b and optional cache."""
+        B, T = t["x"].shape[:2]
+        if out is None:
+            out = self.alloc_outputs(B, T, t["x"].device)
+
+        def ptr(a):
+            return None if a is None else a.data_ptr()
+
+        io = atlas_prologue_io(B, T, ptr(t["x"]), ptr(t["W_in"]), ptr(t["conv_w"]), ptr(t["gate_b"]),
+                               ptr(t.get("cache")), ptr(out["q"]), ptr(out["k"]), ptr(out["v"]), ptr(out["theta"]),
+                               ptr(out["eta"]), ptr(out["alpha"]), ptr(out.get("gamma")), ptr(out.get("cache")))
+        atlas_prologue_forward(self.h, io, current_stream() if stream is None else stream)
+        return out
+
+
+def prologue_tensors_from_numpy(inp: dict, device="cuda"):
+    """Seeded prologue inputs (bf16 as uint16 bit patterns) -> torch."""
+    def conv(a):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(a).to(device)
+    return {k: conv(inp.get(k)) for k in ("x", "W_in", "conv_w", "gate_b", "cache")}

@@ -98,3 +98,52 @@ def test_null_handle(lib):
     assert lib.atlas_mem_forward(None, None, None) == tln.ATLAS_ERR_INVALID_ARG
     assert lib.atlas_mem_status(None) == tln.ATLAS_ERR_INVALID_ARG
     lib.atlas_mem_destroy(None)
+
+
+def _pcfg(**kw):
+    base = dict(D=32, H=2, d_k=8, d_v=8, conv=4, with_gamma=1, theta_max=0.1, qkv_dtype="bf16")
+    base.update(kw)
+    return tln.make_prologue_config(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=0), tln.ATLAS_ERR_INVALID_ARG),
+    (dict(H=0), tln.ATLAS_ERR_INVALID_ARG),
+    (dict(conv=0), tln.ATLAS_ERR_INVALID_ARG),
+    (dict(with_gamma=2), tln.ATLAS_ERR_INVALID_ARG),
+    (dict(theta_max=0.0), tln.ATLAS_ERR_INVALID_ARG),
+    (dict(theta_max=float("inf")), tln.ATLAS_ERR_INVALID_ARG),
+    (dict(qkv_dtype=7), tln.ATLAS_ERR_INVALID_ARG),
+    (dict(conv=9), tln.ATLAS_ERR_UNSUPPORTED),
+    (dict(d_k=200, d_v=200), tln.ATLAS_ERR_UNSUPPORTED),  # 2 d_k + d_v > 512 per head
+])
+def test_prologue_create_rejects(lib, kw, code):
+    with pytest.raises(tln.AtlasError) as ei:
+        tln.atlas_prologue_create(_pcfg(**kw))
+    assert ei.value.code == code
+    assert tln.atlas_prologue_last_error(None)
+
+
+def test_prologue_forward_validates_before_any_cuda_call(lib):
+    import ctypes
+    h = tln.atlas_prologue_create(_pcfg())
+    try:
+        assert lib.atlas_prologue_forward(h, None, None) == tln.ATLAS_ERR_INVALID_ARG
+        io = tln.atlas_prologue_io()
+        io.B, io.T = 1, 0
+        assert lib.atlas_prologue_forward(h, ctypes.byref(io), None) == tln.ATLAS_ERR_INVALID_ARG
+        io.T = 16                              # null tensors
+        assert lib.atlas_prologue_forward(h, ctypes.byref(io), None) == tln.ATLAS_ERR_INVALID_ARG
+        assert "non-NULL" in tln.atlas_prologue_last_error(h)
+        for name in ("x", "W_in", "conv_w", "gate_b", "q", "k", "v", "theta", "eta", "alpha"):
+            setattr(io, name, 16)              # never dereferenced: validation fails first
+        assert lib.atlas_prologue_forward(h, ctypes.byref(io), None) == tln.ATLAS_ERR_INVALID_ARG
+        assert "gamma" in tln.atlas_prologue_last_error(h)
+        io.gamma = 16
+        io.cache = io.cache_out = 32
+        assert lib.atlas_prologue_forward(h, ctypes.byref(io), None) == tln.ATLAS_ERR_INVALID_ARG
+        assert "alias" in tln.atlas_prologue_last_error(h)
+        assert tln.atlas_prologue_workspace_bytes(h, 2, 16) == 2 * 16 * (2 * (2 * 8 + 8) + 4 * 2) * 4
+    finally:
+        tln.atlas_prologue_destroy(h)
+    lib.atlas_prologue_destroy(None)
