@@ -60,10 +60,12 @@ __device__ __forceinline__ void store_out(void* base, size_t i, float v, int dty
 // (with the K-1 halo) come into shared memory by cp.async, 16-byte copies
 // where every segment is a multiple of 4 floats (vec), all in flight before
 // one wait.  Then lane l of every warp owns the head's channels l, l + 32,
-// ...; a warp takes whole token rows, so the q and k norms are one warp
-// reduction and no row leaves registers between the convolution and the
-// store.
-template <int kSlots>   // channels per lane: ceil(Ch / 32) rounded up to an instantiated count
+// ...; warp w takes the 8 consecutive token rows [8w, 8w + 8) in groups of
+// RG, sliding a register window of RG + K - 1 rows down each channel, so the
+// q and k norms are warp reductions and no row leaves registers between the
+// convolution and the store.  KT = K at compile time (the pages' 4), or 0
+// for any K <= 8.
+template <int kSlots, int KT>
 __global__ void __launch_bounds__(kThreads) k_prologue(PGeom p, int T, const float* __restrict__ U,
                                                        const float* __restrict__ conv_w,
                                                        const float* __restrict__ gate_b,
@@ -72,11 +74,11 @@ __global__ void __launch_bounds__(kThreads) k_prologue(PGeom p, int T, const flo
                                                        float* cache_out, int vec) {
   extern __shared__ float sm[];
   const int t0 = blockIdx.x * kTok, h = blockIdx.y, b = blockIdx.z;
-  const int K = p.K, Ch = p.Ch, rows = kTok + K - 1;
+  const int K = KT > 0 ? KT : p.K, Ch = p.Ch, rows = kTok + K - 1;
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
   constexpr int NW = kThreads / 32;
   float* Us = sm;                          // [rows][Ch]: token t0 - (K-1) + r
-  float* taps = Us + (size_t)rows * Ch;    // [K][Ch]
+  float* taps = Us + (size_t)rows * Ch;    // [K][Ch]: tap s weighs token t - (K-1) + s
   const size_t urow = (size_t)b * T;       // first U row of this batch row
   int gcs[kSlots];                         // global channel of each owned channel
 #pragma unroll
@@ -87,58 +89,85 @@ __global__ void __launch_bounds__(kThreads) k_prologue(PGeom p, int T, const flo
       if (lane + 32 * i < Ch) taps[j * Ch + lane + 32 * i] = conv_w[(size_t)gcs[i] * K + j];
   {
     const int wv = vec ? 4 : 1, nv = Ch / wv;
-    for (int e = threadIdx.x; e < rows * nv; e += kThreads) {
-      const int r = e / nv, c = (e - r * nv) * wv, t = t0 - (K - 1) + r;
-      float* dst = Us + r * Ch + c;
-      const float* src = nullptr;
+    for (int r = warp; r < rows; r += NW) {
+      const int t = t0 - (K - 1) + r;
+      const float* srow = nullptr;
       if (t >= 0 && t < T)
-        src = U + (urow + t) * p.Np + head_channel(p, h, c);
+        srow = U + (urow + t) * p.Np;
       else if (t < 0 && cache)
-        src = cache + ((size_t)b * (K - 1) + (K - 1) + t) * p.Nc + head_channel(p, h, c);
-      if (src) {
-        if (vec)
-          cp_async16(dst, src);
-        else
-          cp_async4(dst, src);
-      } else {
-        for (int q4 = 0; q4 < wv; ++q4) dst[q4] = 0.f;
+        srow = cache + ((size_t)b * (K - 1) + (K - 1) + t) * p.Nc;
+      for (int cc = lane; cc < nv; cc += 32) {
+        const int c = cc * wv;
+        float* dst = Us + r * Ch + c;
+        if (srow) {
+          if (vec)
+            cp_async16(dst, srow + head_channel(p, h, c));
+          else
+            cp_async4(dst, srow + head_channel(p, h, c));
+        } else {
+          for (int q4 = 0; q4 < wv; ++q4) dst[q4] = 0.f;
+        }
       }
     }
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
   }
   __syncthreads();
   const size_t uh = (size_t)b * p.H + h;   // (batch, head) index of the outputs
-  for (int r = warp; r < kTok; r += NW) {
-    const int t = t0 + r;
-    if (t >= T) break;
-    float val[kSlots];
-    float sq = 0.f, sk = 0.f;
+  constexpr int RPW = kTok / NW;           // rows per warp
+  constexpr int RG = kSlots <= 8 ? 4 : 2;  // rows per register group
+  for (int g0 = warp * RPW; g0 < warp * RPW + RPW; g0 += RG) {
+    if (t0 + g0 >= T) break;
+    float val[RG][kSlots];
 #pragma unroll
     for (int i = 0; i < kSlots; ++i) {
       const int c = lane + 32 * i;
-      float acc = 0.f;
       if (c < Ch) {
-        for (int j = 0; j < K; ++j) acc += taps[(K - 1 - j) * Ch + c] * Us[(r + K - 1 - j) * Ch + c];
-        if (c < p.dk) sq += acc * acc;
-        else if (c < 2 * p.dk) sk += acc * acc;
-      }
-      val[i] = acc;
-    }
-    for (int o = 16; o > 0; o >>= 1) {
-      sq += __shfl_xor_sync(0xffffffffu, sq, o);
-      sk += __shfl_xor_sync(0xffffffffu, sk, o);
-    }
-    const float iq = 1.f / fmaxf(sqrtf(sq), 1e-12f), ik = 1.f / fmaxf(sqrtf(sk), 1e-12f);
+        float tp[kMaxTaps], win[RG + kMaxTaps - 1];
 #pragma unroll
-    for (int i = 0; i < kSlots; ++i) {
-      const int c = lane + 32 * i;
-      if (c >= Ch) continue;
-      if (c < p.dk)
-        store_out(q, (uh * T + t) * p.dk + c, val[i] * iq, p.dtype);
-      else if (c < 2 * p.dk)
-        store_out(k, (uh * T + t) * p.dk + (c - p.dk), val[i] * ik, p.dtype);
-      else
-        store_out(v, (uh * T + t) * p.dv + (c - 2 * p.dk), val[i], p.dtype);
+        for (int s2 = 0; s2 < kMaxTaps; ++s2) tp[s2] = s2 < K ? taps[s2 * Ch + c] : 0.f;
+#pragma unroll
+        for (int m = 0; m < RG + kMaxTaps - 1; ++m) win[m] = m < RG + K - 1 ? Us[(g0 + m) * Ch + c] : 0.f;
+#pragma unroll
+        for (int rr = 0; rr < RG; ++rr) {
+          float acc = 0.f;
+#pragma unroll
+          for (int s2 = 0; s2 < kMaxTaps; ++s2)
+            if (s2 < K) acc += tp[s2] * win[rr + s2];
+          val[rr][i] = acc;
+        }
+      } else {
+#pragma unroll
+        for (int rr = 0; rr < RG; ++rr) val[rr][i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < RG; ++rr) {
+      const int t = t0 + g0 + rr;   // warp-uniform
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int i = 0; i < kSlots; ++i) {
+        const int c = lane + 32 * i;
+        if (c < p.dk) sq += val[rr][i] * val[rr][i];
+        else if (c < 2 * p.dk) sk += val[rr][i] * val[rr][i];
+      }
+      for (int o = 16; o > 0; o >>= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        sk += __shfl_xor_sync(0xffffffffu, sk, o);
+      }
+      if (t >= T) continue;
+      const float iq = 1.f / fmaxf(sqrtf(sq), 1e-12f), ik = 1.f / fmaxf(sqrtf(sk), 1e-12f);
+      const size_t rk = (uh * T + t) * p.dk, rv = (uh * T + t) * p.dv;
+#pragma unroll
+      for (int i = 0; i < kSlots; ++i) {
+        const int c = lane + 32 * i;
+        if (c >= Ch) continue;
+        if (c < p.dk)
+          store_out(q, rk + c, val[rr][i] * iq, p.dtype);
+        else if (c < 2 * p.dk)
+          store_out(k, rk + (c - p.dk), val[rr][i] * ik, p.dtype);
+        else
+          store_out(v, rv + (c - 2 * p.dk), val[rr][i], p.dtype);
+      }
     }
   }
   for (int e = threadIdx.x; e < p.G * kTok; e += kThreads) {
@@ -288,8 +317,13 @@ extern "C" int atlas_prologue_forward(atlas_prologue_handle* h, const atlas_prol
   if (s != CUBLAS_STATUS_SUCCESS) return pfail(h, ATLAS_ERR_CUDA, "cublasGemmEx failed (status %d)", (int)s);
   const size_t smem = pro_smem_bytes(p);
   const int slots = (p.Ch + 31) / 32;
-  auto kern = slots <= 2 ? k_prologue<2> : slots <= 4 ? k_prologue<4> : slots <= 6 ? k_prologue<6>
-            : slots <= 8 ? k_prologue<8> : slots <= 12 ? k_prologue<12> : k_prologue<16>;
+  auto pick = [&](auto four, auto any) { return p.K == 4 ? four : any; };
+  auto kern = slots <= 2   ? pick(k_prologue<2, 4>, k_prologue<2, 0>)
+              : slots <= 4 ? pick(k_prologue<4, 4>, k_prologue<4, 0>)
+              : slots <= 6 ? pick(k_prologue<6, 4>, k_prologue<6, 0>)
+              : slots <= 8 ? pick(k_prologue<8, 4>, k_prologue<8, 0>)
+              : slots <= 12 ? pick(k_prologue<12, 4>, k_prologue<12, 0>)
+                            : pick(k_prologue<16, 4>, k_prologue<16, 0>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return pfail(h, ATLAS_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   dim3 grid((io->T + kTok - 1) / kTok, p.H, io->B);
