@@ -56,17 +56,43 @@ __device__ __forceinline__ void store_out(void* base, size_t i, float v, int dty
     reinterpret_cast<float*>(base)[i] = v;
 }
 
+// P consecutive floats from shared memory (P = 1 or 2; 2: 8-byte aligned)
+template <int P>
+__device__ __forceinline__ void lds(float* out, const float* src) {
+  if constexpr (P == 2) {
+    const float2 f = *reinterpret_cast<const float2*>(src);
+    out[0] = f.x;
+    out[1] = f.y;
+  } else {
+    out[0] = *src;
+  }
+}
+
+// P consecutive outputs at element i (P = 2: i even, base aligned to 2 elements)
+template <int P>
+__device__ __forceinline__ void store_vec(void* base, size_t i, const float* v, int dtype) {
+  if constexpr (P == 2) {
+    if (dtype == ATLAS_BF16)
+      *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(base) + i) = __floats2bfloat162_rn(v[0], v[1]);
+    else
+      *reinterpret_cast<float2*>(reinterpret_cast<float*>(base) + i) = make_float2(v[0], v[1]);
+  } else {
+    store_out(base, i, v[0], dtype);
+  }
+}
+
 // One CTA per (64-token tile, head, batch row).  The head's projected rows
 // (with the K-1 halo) come into shared memory by cp.async, 16-byte copies
 // where every segment is a multiple of 4 floats (vec), all in flight before
-// one wait.  Then lane l of every warp owns the head's channels l, l + 32,
-// ...; warp w takes the 8 consecutive token rows [8w, 8w + 8) in groups of
-// RG, sliding a register window of RG + K - 1 rows down each channel, so the
-// q and k norms are warp reductions and no row leaves registers between the
-// convolution and the store.  KT = K at compile time (the pages' 4), or 0
-// for any K <= 8.
-template <int kSlots, int KT>
-__global__ void __launch_bounds__(kThreads) k_prologue(PGeom p, int T, const float* __restrict__ U,
+// one wait.  Then lane l of every warp owns the head's channels P l + 32 P i
+// (+0 .. P-1; P = 2 where the head widths are even: paired loads and
+// stores); warp w takes the 8 consecutive token rows [8w, 8w + 8) in groups
+// of RG, sliding a register window of RG + K - 1 rows down each channel, so
+// the q and k norms are warp reductions and no row leaves registers between
+// the convolution and the store.  KT = K at compile time (the pages' 4), or
+// 0 for any K <= 8.
+template <int kSlots, int KT, int P>
+__global__ void __launch_bounds__(kThreads, kSlots * P <= 6 ? 4 : 1) k_prologue(PGeom p, int T, const float* __restrict__ U,
                                                        const float* __restrict__ conv_w,
                                                        const float* __restrict__ gate_b,
                                                        const float* __restrict__ cache, void* q, void* k, void* v,
@@ -80,13 +106,20 @@ __global__ void __launch_bounds__(kThreads) k_prologue(PGeom p, int T, const flo
   float* Us = sm;                          // [rows][Ch]: token t0 - (K-1) + r
   float* taps = Us + (size_t)rows * Ch;    // [K][Ch]: tap s weighs token t - (K-1) + s
   const size_t urow = (size_t)b * T;       // first U row of this batch row
-  int gcs[kSlots];                         // global channel of each owned channel
+  int gcs[kSlots];                         // global channel of each owned slot's first channel
 #pragma unroll
-  for (int i = 0; i < kSlots; ++i) gcs[i] = lane + 32 * i < Ch ? head_channel(p, h, lane + 32 * i) : 0;
+  for (int i = 0; i < kSlots; ++i) {
+    const int c = P * lane + 32 * P * i;
+    gcs[i] = c < Ch ? head_channel(p, h, c) : 0;
+  }
   for (int j = warp; j < K; j += NW)
 #pragma unroll
-    for (int i = 0; i < kSlots; ++i)
-      if (lane + 32 * i < Ch) taps[j * Ch + lane + 32 * i] = conv_w[(size_t)gcs[i] * K + j];
+    for (int i = 0; i < kSlots; ++i) {
+      const int c = P * lane + 32 * P * i;
+      if (c < Ch)
+#pragma unroll
+        for (int e = 0; e < P; ++e) taps[j * Ch + c + e] = conv_w[(size_t)(gcs[i] + e) * K + j];
+    }
   {
     const int wv = vec ? 4 : 1, nv = Ch / wv;
     for (int r = warp; r < rows; r += NW) {
@@ -114,30 +147,48 @@ __global__ void __launch_bounds__(kThreads) k_prologue(PGeom p, int T, const flo
   __syncthreads();
   const size_t uh = (size_t)b * p.H + h;   // (batch, head) index of the outputs
   constexpr int RPW = kTok / NW;           // rows per warp
-  constexpr int RG = kSlots <= 8 ? 4 : 2;  // rows per register group
+  constexpr int RG = kSlots * P <= 8 ? 4 : 2;   // rows per register group
   for (int g0 = warp * RPW; g0 < warp * RPW + RPW; g0 += RG) {
     if (t0 + g0 >= T) break;
-    float val[RG][kSlots];
+    float val[RG][kSlots][P];
 #pragma unroll
     for (int i = 0; i < kSlots; ++i) {
-      const int c = lane + 32 * i;
+      const int c = P * lane + 32 * P * i;
       if (c < Ch) {
-        float tp[kMaxTaps], win[RG + kMaxTaps - 1];
+        float tp[kMaxTaps][P], win[RG + kMaxTaps - 1][P];
 #pragma unroll
-        for (int s2 = 0; s2 < kMaxTaps; ++s2) tp[s2] = s2 < K ? taps[s2 * Ch + c] : 0.f;
+        for (int s2 = 0; s2 < kMaxTaps; ++s2) {
+          if (s2 < K) {
+            lds<P>(tp[s2], taps + s2 * Ch + c);
+          } else {
 #pragma unroll
-        for (int m = 0; m < RG + kMaxTaps - 1; ++m) win[m] = m < RG + K - 1 ? Us[(g0 + m) * Ch + c] : 0.f;
-#pragma unroll
-        for (int rr = 0; rr < RG; ++rr) {
-          float acc = 0.f;
-#pragma unroll
-          for (int s2 = 0; s2 < kMaxTaps; ++s2)
-            if (s2 < K) acc += tp[s2] * win[rr + s2];
-          val[rr][i] = acc;
+            for (int e = 0; e < P; ++e) tp[s2][e] = 0.f;
+          }
         }
+#pragma unroll
+        for (int m = 0; m < RG + kMaxTaps - 1; ++m) {
+          if (m < RG + K - 1) {
+            lds<P>(win[m], Us + (g0 + m) * Ch + c);
+          } else {
+#pragma unroll
+            for (int e = 0; e < P; ++e) win[m][e] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int rr = 0; rr < RG; ++rr)
+#pragma unroll
+          for (int e = 0; e < P; ++e) {
+            float acc = 0.f;
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxTaps; ++s2)
+              if (s2 < K) acc += tp[s2][e] * win[rr + s2][e];
+            val[rr][i][e] = acc;
+          }
       } else {
 #pragma unroll
-        for (int rr = 0; rr < RG; ++rr) val[rr][i] = 0.f;
+        for (int rr = 0; rr < RG; ++rr)
+#pragma unroll
+          for (int e = 0; e < P; ++e) val[rr][i][e] = 0.f;
       }
     }
 #pragma unroll
@@ -146,9 +197,12 @@ __global__ void __launch_bounds__(kThreads) k_prologue(PGeom p, int T, const flo
       float sq = 0.f, sk = 0.f;
 #pragma unroll
       for (int i = 0; i < kSlots; ++i) {
-        const int c = lane + 32 * i;
-        if (c < p.dk) sq += val[rr][i] * val[rr][i];
-        else if (c < 2 * p.dk) sk += val[rr][i] * val[rr][i];
+        const int c = P * lane + 32 * P * i;   // a slot never straddles q, k, v (even widths when P = 2)
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < P; ++e) ss += val[rr][i][e] * val[rr][i][e];
+        if (c < p.dk) sq += ss;
+        else if (c < 2 * p.dk) sk += ss;
       }
       for (int o = 16; o > 0; o >>= 1) {
         sq += __shfl_xor_sync(0xffffffffu, sq, o);
@@ -159,14 +213,20 @@ __global__ void __launch_bounds__(kThreads) k_prologue(PGeom p, int T, const flo
       const size_t rk = (uh * T + t) * p.dk, rv = (uh * T + t) * p.dv;
 #pragma unroll
       for (int i = 0; i < kSlots; ++i) {
-        const int c = lane + 32 * i;
+        const int c = P * lane + 32 * P * i;
         if (c >= Ch) continue;
-        if (c < p.dk)
-          store_out(q, rk + c, val[rr][i] * iq, p.dtype);
-        else if (c < 2 * p.dk)
-          store_out(k, rk + (c - p.dk), val[rr][i] * ik, p.dtype);
-        else
-          store_out(v, rv + (c - 2 * p.dk), val[rr][i], p.dtype);
+        float o[P];
+        if (c < p.dk) {
+#pragma unroll
+          for (int e = 0; e < P; ++e) o[e] = val[rr][i][e] * iq;
+          store_vec<P>(q, rk + c, o, p.dtype);
+        } else if (c < 2 * p.dk) {
+#pragma unroll
+          for (int e = 0; e < P; ++e) o[e] = val[rr][i][e] * ik;
+          store_vec<P>(k, rk + (c - p.dk), o, p.dtype);
+        } else {
+          store_vec<P>(v, rv + (c - 2 * p.dk), val[rr][i], p.dtype);
+        }
       }
     }
   }
@@ -191,7 +251,9 @@ __global__ void __launch_bounds__(kThreads) k_prologue(PGeom p, int T, const flo
       float* dst = cache_out + ((size_t)b * (K - 1) + i) * p.Nc;
 #pragma unroll
       for (int s2 = 0; s2 < kSlots; ++s2)
-        if (lane + 32 * s2 < Ch) dst[gcs[s2]] = src ? src[gcs[s2]] : 0.f;
+        if (P * lane + 32 * P * s2 < Ch)
+#pragma unroll
+          for (int e = 0; e < P; ++e) dst[gcs[s2] + e] = src ? src[gcs[s2] + e] : 0.f;
     }
   }
 }
@@ -316,14 +378,24 @@ extern "C" int atlas_prologue_forward(atlas_prologue_handle* h, const atlas_prol
                    &zero, h->ws, CUDA_R_32F, p.Np, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
   if (s != CUBLAS_STATUS_SUCCESS) return pfail(h, ATLAS_ERR_CUDA, "cublasGemmEx failed (status %d)", (int)s);
   const size_t smem = pro_smem_bytes(p);
-  const int slots = (p.Ch + 31) / 32;
-  auto pick = [&](auto four, auto any) { return p.K == 4 ? four : any; };
-  auto kern = slots <= 2   ? pick(k_prologue<2, 4>, k_prologue<2, 0>)
-              : slots <= 4 ? pick(k_prologue<4, 4>, k_prologue<4, 0>)
-              : slots <= 6 ? pick(k_prologue<6, 4>, k_prologue<6, 0>)
-              : slots <= 8 ? pick(k_prologue<8, 4>, k_prologue<8, 0>)
-              : slots <= 12 ? pick(k_prologue<12, 4>, k_prologue<12, 0>)
-                            : pick(k_prologue<16, 4>, k_prologue<16, 0>);
+  // channel pairs where both head widths are even and q, k, v are aligned
+  // for paired stores
+  const size_t es = p.dtype == ATLAS_BF16 ? 2 : 4;
+  const bool pairs = p.dk % 2 == 0 && p.dv % 2 == 0 && (uintptr_t)io->q % (2 * es) == 0 &&
+                     (uintptr_t)io->k % (2 * es) == 0 && (uintptr_t)io->v % (2 * es) == 0;
+  decltype(&k_prologue<2, 4, 2>) kern;
+  if (pairs) {
+    const int slots = (p.Ch + 63) / 64;
+    auto pick = [&](auto four, auto any) { return p.K == 4 ? four : any; };
+    kern = slots <= 2   ? pick(k_prologue<2, 4, 2>, k_prologue<2, 0, 2>)
+           : slots <= 3 ? pick(k_prologue<3, 4, 2>, k_prologue<3, 0, 2>)
+           : slots <= 4 ? pick(k_prologue<4, 4, 2>, k_prologue<4, 0, 2>)
+                        : pick(k_prologue<8, 4, 2>, k_prologue<8, 0, 2>);
+  } else {
+    const int slots = (p.Ch + 31) / 32;
+    kern = slots <= 2 ? k_prologue<2, 0, 1> : slots <= 4 ? k_prologue<4, 0, 1>
+         : slots <= 8 ? k_prologue<8, 0, 1> : k_prologue<16, 0, 1>;
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return pfail(h, ATLAS_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   dim3 grid((io->T + kTok - 1) / kTok, p.H, io->B);

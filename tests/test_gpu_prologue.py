@@ -75,11 +75,13 @@ def _check(p, g, ref, rows, sl=slice(None), cache=True):
 
 
 SMALL = [
-    ("titans_prologue", dict(B=1, T=100)),        # 8 heads of 64; 100 = 3 tiles of 32 + a ragged 4
+    ("titans_prologue", dict(B=1, T=100)),        # 8 heads of 64; 100 = a 64-token tile + a ragged 36
     ("atlas_prologue", dict(B=2, T=70)),          # 16 heads of 48, gamma head
-    ("small_prologue_f32", dict()),               # fp32, odd widths
+    ("small_prologue_f32", dict()),               # fp32, widths 8 and 12, 40-wide model
     ("small_prologue_f32", dict(conv=1)),         # no convolution
     ("small_prologue_f32", dict(conv=8, T=5)),    # more taps than tokens
+    ("small_prologue_f32", dict(d_k=7, d_v=5)),   # odd widths: single channels, 4-byte copies
+    ("atlas_prologue", dict(B=1, T=40, D=50, H=3, d_k=9, d_v=6)),   # bf16, odd q/k width
 ]
 
 
