@@ -91,6 +91,20 @@ def flops_per_chunk(w) -> float:
     return feat + fwd + C * per_tok
 
 
+def path_dtype(w) -> str:
+    """Arithmetic type of the path a workload runs on: the fused MLP kernel
+    multiplies bf16 operands (fp32 accumulation and state); the tensor-core
+    Newton-Schulz path multiplies split bf16 pairs (three products, about
+    fp32 accuracy); everything else is fp32."""
+    fused = (w.depth == 2 and w.ns_iters == 0 and w.c == 1 and w.p == 1 and w.proj_dim == 0 and w.d_k == 64
+             and w.d_v == 64 and w.hidden == 256 and w.C == 64)
+    if fused:
+        return "bf16"
+    if w.ns_iters and getattr(w, "ns_target", "momentum") == "momentum" and w.depth == 2:
+        return "bf16x3"
+    return "f32"
+
+
 def bytes_per_step(w) -> float:
     es = 2 if w.qkv_dtype == "bf16" else 4
     per_tok = es * (2 * w.d_k + w.d_v) + 4 * 3 + (4 if w.use_gamma else 0) + 4 * w.d_v
@@ -370,7 +384,7 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "scaling": "weak", "vs_baseline": None, "dtype": path_dtype(w),
         "data": "synthetic (seeded, harness recipe), inputs resident in HBM",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "depth": w.depth, "d": w.d_v,
                    "hidden": w.hidden, "C": w.C, "c": w.c, "p": w.p, "ns_iters": w.ns_iters,
