@@ -632,6 +632,24 @@ cudaError_t generic_cache_out(const Geom& g, const GenericIO& io, float* tmp, vo
 
 namespace atlas {
 
+// Asynchronous 4-byte global -> shared copies: every load of a stage is in
+// flight at once instead of one round trip per loop iteration.  An invalid
+// element copies 0 bytes from a valid address and zero-fills.
+__device__ __forceinline__ void cp_async4(float* dst, const float* src, bool valid, const float* fallback) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d), "l"(valid ? src : fallback),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// 16-byte copy (both addresses 16-byte aligned)
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+
 // --------------------------------------------- fused decay scan + read-out
 // Newton-Schulz path, depth 2 with W1 (F x h, F <= h) and W2 (h x d, h > d),
 // both stored per token in Ubuf in the X orientation (W1 as is, W2
@@ -660,13 +678,16 @@ __global__ void __launch_bounds__(256) k_ns_scan_w1(Geom g, Chunk ch, Work w, in
   float* rq = scan_sm;                   // [C][F + 1] queries of the chunk
   float* part = rq + g.C * (F + 1);      // [C][8][33] per-group partial sums
   float* bes = part + g.C * 8 * 33;      // [C] 1 - alpha
+  // the chunk's queries by cp.async (all in flight at once), then the gates
   for (int e = threadIdx.x; e < Ct * F; e += 256)
-    rq[(e / F) * (F + 1) + e % F] = w.R[((size_t)u * g.T + ch.s + e / F) * F + e % F];
+    cp_async4(&rq[(e / F) * (F + 1) + e % F], &w.R[((size_t)u * g.T + ch.s + e / F) * F + e % F], true, w.R);
+  cp_async_commit();
   for (int r = threadIdx.x; r < Ct; r += 256) bes[r] = 1.f - alpha[(size_t)u * g.T + ch.s + r];
   float W[RPG];
   const float* Wb = w.Wst[buf][0] + (size_t)u * F * h;
 #pragma unroll
   for (int q = 0; q < RPG; ++q) W[q] = Wb[(size_t)(i0 + q) * h + j];
+  cp_async_wait<0>();
   __syncthreads();
   const float* slot0 = w.Ubuf + (size_t)u * g.C * slot_stride + (size_t)i0 * h + j;
   for (int r0 = 0; r0 < Ct; r0 += PD) {
@@ -724,12 +745,19 @@ __global__ void __launch_bounds__(256) k_ns_scan_w2(Geom g, Chunk ch, Work w, in
   const bool pre = g.readout == ATLAS_READOUT_PRE;   // read out before token r's update
   const int rn = ns_first_row(g, ch);                 // slots before it hold no U_t: U_t = 0
   float* bes = aqs + Ct * h;
-  for (int e = threadIdx.x; e < Ct * h; e += 256) aqs[e] = aq[(size_t)u * g.C * h + e];
+  {
+    // the chunk's hidden read-outs by 16-byte cp.async (h % 32 == 0, 16-byte
+    // aligned rows), all in flight at once
+    const float* src = aq + (size_t)u * g.C * h;
+    for (int e = 4 * threadIdx.x; e < Ct * h; e += 4 * 256) cp_async16(aqs + e, src + e);
+    cp_async_commit();
+  }
   for (int r = threadIdx.x; r < Ct; r += 256) bes[r] = 1.f - alpha[(size_t)u * g.T + ch.s + r];
   float W[CPL];
   const float* Wb = w.Wst[buf][1] + (size_t)u * h * d;   // original orientation [h][d]
 #pragma unroll
   for (int q = 0; q < CPL; ++q) W[q] = Wb[(size_t)(j0 + q) * d + k];
+  cp_async_wait<0>();
   __syncthreads();
   const float* slot0 = w.Ubuf + (size_t)u * g.C * slot_stride + (size_t)F * h + (size_t)k * h + j0;
   for (int r0 = 0; r0 < Ct; r0 += PD) {
@@ -1104,18 +1132,6 @@ __device__ __forceinline__ void store_tile(float* out, int ld, int r0, int nr, i
   }
 }
 
-// Asynchronous 4-byte global -> shared copies: every load of a stage is in
-// flight at once instead of one round trip per loop iteration.  An invalid
-// element copies 0 bytes from a valid address and zero-fills.
-__device__ __forceinline__ void cp_async4(float* dst, const float* src, bool valid, const float* fallback) {
-  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d), "l"(valid ? src : fallback),
-               "r"(valid ? 4 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // shared-memory slices, all k-major for smem_gemm: R transposed [f][t]
 // (row stride 68), X transposed [f][i] (row stride 132), X [i][f] (row
