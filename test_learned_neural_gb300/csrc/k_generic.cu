@@ -728,8 +728,9 @@ __global__ void __launch_bounds__(256) k_ns_scan_w1(Geom g, Chunk ch, Work w, in
 }
 
 // Pass 2: y_t = r_t + aq_t W2_t.  One warp per row k of W2^T (d x h): lane
-// holds columns [lane * CPL, (lane + 1) * CPL); a shuffle sum over the warp
-// gives y_t[k].
+// holds columns lane, lane + 32, ... (CPL of them: the warp's shared-memory
+// reads of aq_t are conflict-free and its U_t reads coalesced); a shuffle sum
+// over the warp gives y_t[k].
 template <int CPL>
 __global__ void __launch_bounds__(256) k_ns_scan_w2(Geom g, Chunk ch, Work w, int buf, size_t slot_stride,
                                                     const float* alpha, const float* aq, float* y) {
@@ -740,7 +741,7 @@ __global__ void __launch_bounds__(256) k_ns_scan_w2(Geom g, Chunk ch, Work w, in
   extern __shared__ float aqs[];   // [Ct][h], then [Ct] 1 - alpha
   const int u = blockIdx.y;
   const int lane = threadIdx.x % 32, k = blockIdx.x * 8 + threadIdx.x / 32;
-  const int F = g.F, h = g.hidden, d = g.d_v, j0 = lane * CPL;
+  const int F = g.F, h = g.hidden, d = g.d_v;   // lane holds hidden columns lane + 32 q
   const int Ct = ch.e - ch.s;
   const bool pre = g.readout == ATLAS_READOUT_PRE;   // read out before token r's update
   const int rn = ns_first_row(g, ch);                 // slots before it hold no U_t: U_t = 0
@@ -756,21 +757,17 @@ __global__ void __launch_bounds__(256) k_ns_scan_w2(Geom g, Chunk ch, Work w, in
   float W[CPL];
   const float* Wb = w.Wst[buf][1] + (size_t)u * h * d;   // original orientation [h][d]
 #pragma unroll
-  for (int q = 0; q < CPL; ++q) W[q] = Wb[(size_t)(j0 + q) * d + k];
+  for (int q = 0; q < CPL; ++q) W[q] = Wb[(size_t)(lane + 32 * q) * d + k];
   cp_async_wait<0>();
   __syncthreads();
-  const float* slot0 = w.Ubuf + (size_t)u * g.C * slot_stride + (size_t)F * h + (size_t)k * h + j0;
+  const float* slot0 = w.Ubuf + (size_t)u * g.C * slot_stride + (size_t)F * h + (size_t)k * h + lane;
   for (int r0 = 0; r0 < Ct; r0 += PD) {
     float cur[PD][CPL];
 #pragma unroll
     for (int p = 0; p < PD; ++p) {
       const float* sl = slot0 + (size_t)(r0 + p) * slot_stride;
 #pragma unroll
-      for (int q = 0; q < CPL; q += 4) {
-        const float4 v4 = r0 + p < Ct && r0 + p >= rn ? *reinterpret_cast<const float4*>(sl + q)
-                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-        cur[p][q] = v4.x; cur[p][q + 1] = v4.y; cur[p][q + 2] = v4.z; cur[p][q + 3] = v4.w;
-      }
+      for (int q = 0; q < CPL; ++q) cur[p][q] = r0 + p < Ct && r0 + p >= rn ? sl[32 * q] : 0.f;
     }
     float acc[PD];
 #pragma unroll
@@ -781,9 +778,9 @@ __global__ void __launch_bounds__(256) k_ns_scan_w2(Geom g, Chunk ch, Work w, in
 #pragma unroll
       for (int q = 0; q < CPL; ++q) {
         if (r0 + p < Ct) {
-          if (pre) a += aqs[r * h + j0 + q] * W[q];
+          if (pre) a += aqs[r * h + lane + 32 * q] * W[q];
           W[q] = be * W[q] + cur[p][q];
-          if (!pre) a += aqs[r * h + j0 + q] * W[q];
+          if (!pre) a += aqs[r * h + lane + 32 * q] * W[q];
         }
       }
       acc[p] = a;
@@ -804,7 +801,7 @@ __global__ void __launch_bounds__(256) k_ns_scan_w2(Geom g, Chunk ch, Work w, in
   }
   float* Wo = w.Wst[buf ^ 1][1] + (size_t)u * h * d;
 #pragma unroll
-  for (int q = 0; q < CPL; ++q) Wo[(size_t)(j0 + q) * d + k] = W[q];
+  for (int q = 0; q < CPL; ++q) Wo[(size_t)(lane + 32 * q) * d + k] = W[q];
 }
 
 bool ns_fused_scan_supported(const Geom& g) {
