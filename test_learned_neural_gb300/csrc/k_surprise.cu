@@ -280,7 +280,9 @@ __global__ void __launch_bounds__(256) k_surp_readout(Geom g, Chunk ch, Work w, 
     float a[TG], b[TG], c2[TG];
 #pragma unroll
     for (int tt = 0; tt < TG; ++tt) a[tt] = b[tt] = c2[tt] = 0.f;
-#pragma unroll 4
+    // unrolled 16 deep so that many W, S loads are in flight per thread (the
+    // loop is bound by their latency, not by the FMAs)
+#pragma unroll 16
     for (int f = 0; f < K; ++f) {
       const float wv = Wm[(size_t)f * cols + k], sv = Sm[(size_t)f * cols + k];
 #pragma unroll
@@ -289,7 +291,7 @@ __global__ void __launch_bounds__(256) k_surp_readout(Geom g, Chunk ch, Work w, 
         b[tt] += vec[tt * vstride + f] * sv;
       }
     }
-#pragma unroll 4
+#pragma unroll 16
     for (int j = 0; j < nw; ++j) {
       const float rv = Rf[(size_t)j * cols + k];
 #pragma unroll
