@@ -187,6 +187,21 @@ def test_hand_worked_scalar_memory(name, C, c, use_gamma):
     np.testing.assert_allclose(S[0].ravel(), cases[name]["S"], rtol=0, atol=1e-14)
 
 
+@pytest.mark.parametrize("name,readout,use_gamma", [("CW2", "post", False), ("CW2pre", "pre", False),
+                                                    ("CW2g", "post", True)])
+def test_hand_worked_scalar_memory_chunkwise(name, readout, use_gamma):
+    """The chunk-wise rule on the same three tokens, worked by hand (C = 2,
+    so the last token is a partial chunk of its own)."""
+    rows, cases = _golden_scalar()
+    k, v, q, theta, eta, alpha, gamma = rows.T
+    y, W, S, _ = oracle.forward_unit(Cfg(depth=1, C=2, c=1, readout=readout, update="chunkwise"), k[:, None],
+                                     q[:, None], v[:, None], theta, eta, alpha, gamma if use_gamma else None,
+                                     [np.array([[0.5]])], [np.zeros((1, 1))])
+    np.testing.assert_allclose(y[:, 0], cases[name]["y"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(W[0].ravel(), cases[name]["W"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(S[0].ravel(), cases[name]["S"], rtol=0, atol=1e-14)
+
+
 @pytest.mark.parametrize("depth", [1, 2])
 def test_C1_is_the_sequential_titans_rule(depth):
     """C = 1: every token sees the weights left by the token before, i.e. the

@@ -2,6 +2,7 @@
 short causal convolution, q/k normalisation, gate heads) against facts that
 do not come from the oracle itself."""
 import dataclasses
+import os
 
 import numpy as np
 import pytest
@@ -133,3 +134,35 @@ def test_split_with_carried_cache(T1):
     for key in ("q", "k", "v", "theta", "eta", "alpha", "gamma"):
         np.testing.assert_allclose(np.concatenate([o1[key], o2[key]], axis=1), whole[key], rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(o2["cache"], whole["cache"], rtol=1e-14)
+
+
+def test_hand_worked_golden():
+    """A 1-wide model worked by hand (tests/golden/prologue_scalar.txt):
+    column order, tap orientation, normalisation, gate biases, theta_max and
+    the outgoing cache."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "prologue_scalar.txt")
+    taps, outs = [], {}
+    for ln in open(path):
+        if ln.startswith("#") or not ln.strip():
+            continue
+        head, vals = ln.split(":")
+        nums = [float(t) for t in vals.split()]
+        if head == "win":
+            W_in = np.array([nums])
+        elif head.startswith("tap"):
+            taps.append(nums)
+        elif head == "bias":
+            gate_b = np.array(nums)[:, None]
+        elif head == "x":
+            x = np.array(nums)[:, None]
+        else:
+            outs[head.split()[1]] = np.array(nums)
+    cfg = PCfg(H=1, d_k=2, d_v=1, conv=2, with_gamma=False)
+    o = prologue_row(cfg, x, W_in, np.array(taps), gate_b)
+    np.testing.assert_allclose(o["q"].ravel(), outs["q"], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(o["k"].ravel(), outs["k"], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(o["v"].ravel(), outs["v"], rtol=0, atol=1e-15)
+    for g in ("theta", "eta", "alpha"):
+        np.testing.assert_allclose(o[g].ravel(), outs[g], rtol=1e-15, atol=0)
+    assert o["gamma"] is None
+    np.testing.assert_allclose(o["cache"].ravel(), outs["cache"], rtol=0, atol=0)
