@@ -427,6 +427,7 @@ def time_prologue_oracle(p, T=1024):
     inp = make_prologue_inputs(p.scaled(B=1))
     from harness import bf16_from_bits
     dec = (lambda a: bf16_from_bits(a).astype(np.float64)) if p.qkv_dtype == "bf16" else (lambda a: a.astype(np.float64))
+    T = min(T, p.T)
     x, W = dec(inp["x"])[0, :T], dec(inp["W_in"])
     t0 = time.perf_counter()
     oracle.prologue_row(p, x, W, inp["conv_w"], inp["gate_b"])
