@@ -33,6 +33,15 @@ int atlas_mem_selftest_mma(int M, int N, int K, int a_mn_major, int b_mn_major, 
 int atlas_mem_selftest_ld16x2(int N, int K, const void* A, const void* B, float* raw_out, int col, int* status,
                               void* stream);
 
+/* Failure detection without a fault: one CTA waits, with the library's
+ * bounded mbarrier wait limited to max_cycles (1 .. 2^31 SM clock cycles),
+ * on a barrier that nothing arrives at.  The wait gives up, the kernel stores
+ * ATLAS_ERR_TIMEOUT (5) into *status (device int) and the cycles it waited
+ * into *waited_cycles (device), and returns; the context stays usable.
+ * Asynchronous on `stream`; returns ATLAS_OK, ATLAS_ERR_INVALID_ARG or
+ * ATLAS_ERR_CUDA. */
+int atlas_mem_selftest_wait_timeout(long long max_cycles, int* status, long long* waited_cycles, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

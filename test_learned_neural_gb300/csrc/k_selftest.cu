@@ -115,6 +115,29 @@ __global__ void __launch_bounds__(128) k_selftest_ld16x2(int N, int K, const uin
   if (warp == 0) tc::tmem_dealloc(tbase, 256);
 }
 
+// A bounded mbarrier wait that runs out: the barrier expects one arrival
+// and nothing arrives, so thread 0's wait (the library's own bounded wait,
+// limited to max_cycles) gives up, records ATLAS_ERR_TIMEOUT in the status
+// word and returns; no trap, no fault, the context stays usable.
+__global__ void __launch_bounds__(32) k_selftest_timeout(long long max_cycles, int* status, long long* waited) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) tc::mbar_init(&bar, 1);
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  const long long t0 = clock64();
+  const bool ok = tc::mbar_wait(&bar, 0, max_cycles);
+  *waited = clock64() - t0;
+  if (!ok) atomicExch(status, ATLAS_ERR_TIMEOUT);
+}
+
+extern "C" int atlas_mem_selftest_wait_timeout(long long max_cycles, int* status, long long* waited_cycles,
+                                               void* stream) {
+  using namespace atlas;
+  if (max_cycles < 1 || max_cycles > (1ll << 31) || !status || !waited_cycles) return ATLAS_ERR_INVALID_ARG;
+  k_selftest_timeout<<<1, 32, 0, (cudaStream_t)stream>>>(max_cycles, status, waited_cycles);
+  return cudaGetLastError() == cudaSuccess ? ATLAS_OK : ATLAS_ERR_CUDA;
+}
+
 extern "C" int atlas_mem_selftest_ld16x2(int N, int K, const void* A, const void* B, float* raw_out, int col,
                                          int* status, void* stream) {
   using namespace atlas;

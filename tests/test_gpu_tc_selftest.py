@@ -90,3 +90,33 @@ def test_tmem_ld_16x32bx2_layout(gpu_lib):
             print("warp 0 thread", t, [got[(0, t, j)] for j in (0, 1, 2, 15)])
         print("warp 1 thread 0", [got[(1, 0, j)] for j in (0, 1, 15)])
     assert got == want
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable(gpu_lib):
+    """Failure detection without a GPU fault: a kernel waits on an mbarrier
+    that nothing arrives at, with the library's bounded wait limited to about
+    a millisecond.  It gives up, reports ATLAS_ERR_TIMEOUT in its status
+    word and returns; a memory-layer forward afterwards still matches the
+    oracle."""
+    import torch
+
+    import test_learned_neural_gb300 as tln
+    from harness import WORKLOADS
+    from tests.gpu_common import TOL, compare
+    lib = gpu_lib.load()
+    lib.atlas_mem_selftest_wait_timeout.argtypes = [ctypes.c_longlong, ctypes.c_void_p, ctypes.c_void_p,
+                                                    ctypes.c_void_p]
+    lib.atlas_mem_selftest_wait_timeout.restype = ctypes.c_int
+    assert lib.atlas_mem_selftest_wait_timeout(0, None, None, None) == tln.ATLAS_ERR_INVALID_ARG
+    budget = 2_000_000                                   # SM cycles, about 1 ms
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    waited = torch.zeros(1, dtype=torch.int64, device="cuda")
+    rc = lib.atlas_mem_selftest_wait_timeout(budget, st.data_ptr(), waited.data_ptr(),
+                                             torch.cuda.current_stream().cuda_stream)
+    assert rc == tln.ATLAS_OK
+    torch.cuda.synchronize()
+    assert int(st.item()) == tln.ATLAS_ERR_TIMEOUT
+    assert budget <= int(waited.item()) < 100 * budget
+    w = WORKLOADS["titans_mlp"].scaled(B=1, H=2, T=128)
+    errs = compare(w)
+    assert errs["y"] <= TOL["bf16"] and errs["W0"] <= TOL["bf16"]
