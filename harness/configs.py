@@ -113,6 +113,15 @@ WORKLOADS = {
         "atlas_muon_chunkwise", depth=2, d_k=128, d_v=128, hidden=512, C=64, c=1, p=1,
         proj_dim=0, ns_iters=5, qkv_dtype="bf16", B=2, H=16, T=16384, seed=3,
         w0_init="xavier", update="chunkwise"),
+    # The Titans memory with slow forgetting and a smaller step (alpha mean
+    # -8, theta = 0.02 sigmoid).  With the default gates the memory decays
+    # to ~1e-8 by T = 4096, so late read-outs equal the queries; here W
+    # stays ~0.2 over the whole sequence, so every read-out tests the
+    # memory.  (alpha mean -8 with theta 0.1 diverges, in fp64 as well.)
+    "titans_mlp_slow": Workload(
+        "titans_mlp_slow", depth=2, d_k=64, d_v=64, hidden=256, C=64, c=1, p=1,
+        proj_dim=0, ns_iters=0, qkv_dtype="bf16", B=4, H=8, T=4096, seed=5,
+        w0_init="xavier", alpha_mu=-8.0, theta_scale=0.02),
     # Long context: degree-2 features of 64-dim keys (2145) projected to 64.
     "atlas_long": Workload(
         "atlas_long", depth=2, d_k=64, d_v=64, hidden=256, C=64, c=8, p=2,
