@@ -5,8 +5,10 @@
 
 A step is one forward of the whole memory layer (every chunk of every unit)
 over one batch of synthetic inputs that already sit in HBM.  The default
-workload is the Titans MLP memory (B=4, H=8, T=4096, d=64, hidden 256, C=64).
-One JSON line goes to stdout on rank 0.
+workload is the largest single-GPU one by work, ATLAS with Muon (MLP
+128 -> 512 -> 128, B=2, H=16, T=16384, C=64, Omega window 8, five
+Newton-Schulz iterations per token and weight matrix); ``--workload NAME``
+times any other.  One JSON line goes to stdout on rank 0.
 
 Under torchrun (N > 1) every rank runs its own batch of the same shape on its
 own GPU (the (batch, head) units are independent: no collective on the data
@@ -34,6 +36,11 @@ sys.path.insert(0, ROOT)
 from harness import PROLOGUES, WORKLOADS, make_inputs, make_prologue_inputs  # noqa: E402
 
 METRIC = "memory-layer tokens/s (B*H*T/s) on 1 GB300"
+DEFAULT_WORKLOAD = "atlas_muon"
+
+# fp32 FMA peak of the whole GPU for paths bound by plain ALU issue: 152 SMs
+# x 128 fp32 lanes x 2 FLOP per FMA x the 2070 MHz maximum SM clock
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 
 
 # --------------------------------------------------------------- accounting
@@ -89,6 +96,51 @@ def flops_per_chunk(w) -> float:
         per_tok += w.ns_iters * (2.0 * m * m * n * 2 + 2.0 * m ** 3)  # NS
         per_tok += 2.0 * m * n * 2                                    # scan + read-out
     return feat + fwd + C * per_tok
+
+
+def algorithmic_flops_per_token(w) -> float:
+    """Algorithmic FLOPs per token by the hot-path scope table's accounting:
+    the work the method must do in the dual form, with no per-token state
+    in HBM.
+
+    * Newton-Schulz on the momentum (per token): the quintic steps only,
+      sum over matrices of k (2 m^2 n * 2 + 2 m^3) on the short side m,
+      plus phi P (2 * monomials * proj per key and per query) when the
+      features are projected;
+    * depth 2 without it: forward and backward at W_bar (3 * 2 F h), the
+      chunk-end state products (W and S, both matrices) and the dual-form
+      read-out through W_bar and S_bar (both matrices);
+    * depth 1 without it: phi(k) W_bar, the S and W updates, phi(q) W_bar
+      and S_bar, and the intra-chunk Gram phi(q) X^T over the window rows.
+
+    The chunk-wise rule and Newton-Schulz on the surprise keep the per-chunk
+    counts of flops_per_chunk."""
+    surprise = w.ns_iters > 0 and getattr(w, "ns_target", "momentum") == "surprise"
+    if getattr(w, "update", "per_token") == "chunkwise" or surprise:
+        return flops_per_chunk(w) / w.C
+    F, dv, h = w.feat_dim, w.d_v, w.hidden
+    mats = [(F, dv)] if w.depth == 1 else [(F, h), (h, dv)]
+    feat = 2.0 * 2.0 * w.poly_dim * w.proj_dim if w.proj_dim else 0.0
+    if w.ns_iters:
+        ns = sum(w.ns_iters * (2.0 * min(r, c) ** 2 * max(r, c) * 2 + 2.0 * min(r, c) ** 3) for r, c in mats)
+        return ns + feat
+    if w.depth == 2:
+        fwd = 3 * 2.0 * F * h
+        state = 2 * sum(2.0 * r * c for r, c in mats)
+        read = 2 * sum(2.0 * r * c for r, c in mats)
+        return fwd + state + read + feat
+    Kw = w.C + w.c - 1
+    return 2.0 * F * dv + 2 * 2.0 * F * dv + 2 * 2.0 * F * dv + 2.0 * F * Kw + feat
+
+
+def roofline_bound(w, flops, nbytes, peaks) -> str:
+    """'alu' on the fp32 SIMT paths; else 'tensor' when the step's
+    arithmetic intensity is above the ridge of the measured bf16 tensor
+    peak over the measured HBM bandwidth, 'hbm' below it."""
+    if path_dtype(w) == "f32":
+        return "alu"
+    ridge = peaks.get("bf16_tflops_sustained", 1700.0) * 1e12 / (peaks.get("hbm_gbs", 6800.0) * 1e9)
+    return "tensor" if flops / max(nbytes, 1.0) >= ridge else "hbm"
 
 
 def path_dtype(w) -> str:
@@ -201,20 +253,34 @@ def _oracle_job(args):
     return time.perf_counter() - t0
 
 
-def oracle_sample(w):
-    """Bounded sample of the workload for the CPU oracle: (units, tokens)."""
-    if w.ns_iters:
-        return list(range(min(2, w.units))), 2 * w.C
-    return list(range(min(8, w.units))), min(w.T, 4096)
+# fp64 oracle cost per token and unit on one host core, measured (x86 and
+# Arm hosts within a factor of two); sizes the bounded samples below
+ORACLE_S_PER_TOKEN = {"atlas_muon": 0.019, "atlas_muon_surprise": 0.019, "atlas_muon_chunkwise": 0.0005,
+                      "atlas_long": 0.0034}
 
 
-def time_oracle(name, reps=1):
+def oracle_sample(w, budget_s=None):
+    """Bounded sample of the workload for the CPU oracle: (units, tokens)
+    from the start of the sequence.  Without a budget: up to 8 units (one
+    process each) x 2C tokens on the Newton-Schulz workloads, else x 4096;
+    with one, the token count is cut so that one unit's pass takes about
+    budget_s seconds (at least 8 tokens)."""
+    cores = os.cpu_count() or 1
+    units = list(range(min(8, w.units, cores)))
+    T = 2 * w.C if w.ns_iters else min(w.T, 4096)
+    if budget_s is not None:
+        per_tok = ORACLE_S_PER_TOKEN.get(w.name, 0.0006)
+        T = max(8, min(T, int(budget_s / per_tok)))
+    return units, T
+
+
+def time_oracle(name, reps=1, budget_s=None):
     """Time the oracle on its sample, one spawned process per unit (one BLAS
     thread each, all in parallel).  A rep takes as long as its slowest unit.
     Returns (tokens/s, cores used, description, per-rep seconds)."""
     import multiprocessing as mp
     w = WORKLOADS[name]
-    units, T = oracle_sample(w)
+    units, T = oracle_sample(w, budget_s)
     cores = min(len(units), os.cpu_count() or 1)
     env_keep = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
     for k in env_keep:
@@ -245,9 +311,11 @@ def run_reference(args):
     if rank != 0:
         return 0
     w = WORKLOADS[args.workload]
-    # warm-up: time_oracle runs one untimed pass per worker before the timed reps
-    tps, cores, desc, times = time_oracle(args.workload, reps=args.steps)
-    units, T = oracle_sample(w)
+    # warm-up: time_oracle runs one untimed pass per worker before the timed
+    # reps.  Each step's sample is cut so that all K steps take about a
+    # minute of oracle work in total.
+    budget = 60.0 / max(args.steps, 1)
+    tps, cores, desc, times = time_oracle(args.workload, reps=args.steps, budget_s=budget)
     line = {
         "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
@@ -371,10 +439,22 @@ def run_ours(args):
         return 0
 
     peaks, src = measured_peaks()
-    fl = flops_per_chunk(w) * (w.T // w.C) * w.units
+    fl = algorithmic_flops_per_token(w) * w.tokens
+    nbytes = bytes_per_step(w)
     step_s = statistics.mean(step_ms) / 1e3
-    achieved = fl / step_s / 1e12
-    peak = peaks.get("bf16_tflops", 1900.0)
+    bound = roofline_bound(w, fl, nbytes, peaks)
+    # a step of a second or more runs under the power cap: sustained peak
+    sustained = step_s >= 0.1
+    if bound == "alu":
+        achieved, peak, runit = fl / step_s / 1e12, FP32_ALU_TFLOPS, "TFLOP/s"
+        peak_src = "fp32 FMA issue: 152 SMs x 128 lanes x 2 x 2070 MHz (derived)"
+    elif bound == "hbm":
+        achieved, peak, runit = nbytes / step_s / 1e9, peaks.get("hbm_gbs", 6800.0), "GB/s"
+        peak_src = f"hbm_gbs ({src})"
+    else:
+        key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+        achieved, peak, runit = fl / step_s / 1e12, peaks.get(key, 1700.0 if sustained else 1900.0), "TFLOP/s"
+        peak_src = f"{key} ({src})"
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
@@ -389,11 +469,12 @@ def run_ours(args):
         "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "depth": w.depth, "d": w.d_v,
                    "hidden": w.hidden, "C": w.C, "c": w.c, "p": w.p, "ns_iters": w.ns_iters,
                    "l2": "flushed between timed steps (256 MB write)", "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic, "peak_source": f"bf16_tflops ({src})",
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": runit,
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                      "kernel": ("atlas::k_mlp_dual_tc (the step's only launch)" if launches == 1
                                 else f"whole forward ({launches} launches per step)"),
-                     "algorithmic_flops_per_step": fl, "algorithmic_bytes_per_step": bytes_per_step(w)},
+                     "algorithmic_flops_per_token": algorithmic_flops_per_token(w),
+                     "algorithmic_flops_per_step": fl, "algorithmic_bytes_per_step": nbytes},
         "gpu_launches": launches * args.steps,
         "e2e": e2e,
         "clocks": clk,
@@ -493,10 +574,11 @@ def run_prologue(args):
                    "conv": p.conv, "l2": "flushed between timed steps (256 MB write)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None, "peak_source": f"hbm_gbs ({src})",
-                     "kernel": "whole stage (cuBLAS projection + k_prologue, 2 launches per step)",
+                     "kernel": "whole stage (cuBLAS projection + k_prologue: one library and one own launch per step)",
                      "algorithmic_bytes_per_step": byt,
                      "algorithmic_flops_per_step": 2.0 * p.tokens * p.D * p.N},
-        "gpu_launches": 1 * args.steps,
+        "gpu_launches": 1 * args.steps,          # k_prologue; the projection is a cuBLAS launch
+        "library_launches": 1 * args.steps,
         "e2e": None,
         "clocks": clk,
         "wall_s_timed_region": wall,
@@ -509,16 +591,30 @@ def run_prologue(args):
     return 0
 
 
+# measured ms per forward on one GB300, to size the default step count
+APPROX_MS = {"atlas_muon": 1040, "atlas_long": 920, "atlas_muon_surprise": 122, "atlas_muon_chunkwise": 82,
+             "atlas_poly_c4": 5.1, "atlas_poly_c16": 5.2}
+
+
+def default_steps(name: str) -> int:
+    """About 10 s of timed steps, between 10 and 100."""
+    ms = APPROX_MS.get(name, 0.5)
+    return int(max(10, min(100, 10000 // ms)))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about 10 s of timed work: 10 on the default workload)")
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="titans_mlp", choices=sorted(WORKLOADS) + sorted(PROLOGUES))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS) + sorted(PROLOGUES))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args(argv)
+    if args.steps is None:
+        args.steps = default_steps(args.workload)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.workload in PROLOGUES:

@@ -34,6 +34,43 @@ def test_chunkwise_work_is_below_the_per_token_work():
     assert 30 < ratio < 64
 
 
+def test_algorithmic_flops_follow_the_scope_table():
+    """Per-token FLOPs by the hot-path scope table's accounting: config 3
+    (Muon, 128 x 512 matrices, five steps) 2 x 5 x (2 * 128^2 * 512 * 2 +
+    2 * 128^3) = 377 M; config 4 = Newton-Schulz on 64 x 256 plus phi P
+    (2 x 2145 x 64 per key and per query) = 47.8 M; config 1 ~0.35 M;
+    config 2 the table's items phi(k) W_bar 72 k + S/W updates 144 k +
+    phi(q) W_bar/S_bar 144 k + intra-chunk Gram 72-89 k = 432-449 k (the
+    table's rounded total, 0.37-0.40 M, is below its own items); config 0
+    ~10 k."""
+    f = bench.algorithmic_flops_per_token
+    assert f(WORKLOADS["atlas_muon"]) == 2 * 5 * (2 * 128 ** 2 * 512 * 2 + 2 * 128 ** 3) == 377487360
+    assert abs(f(WORKLOADS["atlas_long"]) - 47.8e6) < 0.1e6
+    assert 0.34e6 < f(WORKLOADS["titans_mlp"]) < 0.37e6
+    assert 0.43e6 < f(WORKLOADS["atlas_poly_c4"]) < f(WORKLOADS["atlas_poly_c16"]) < 0.45e6
+    assert 9e3 < f(WORKLOADS["linear_f32"]) < 12e3
+
+
+def test_roofline_bound_from_intensity():
+    peaks = {"bf16_tflops_sustained": 1737.5, "hbm_gbs": 6705.2}
+    w = WORKLOADS["atlas_muon"]
+    fl = bench.algorithmic_flops_per_token(w) * w.tokens
+    assert bench.roofline_bound(w, fl, bench.bytes_per_step(w), peaks) == "tensor"
+    assert bench.roofline_bound(w, 1.0, 1e9, peaks) == "hbm"
+    assert bench.roofline_bound(WORKLOADS["atlas_poly_c4"], 1e12, 1.0, peaks) == "alu"   # fp32 SIMT path
+
+
+def test_reference_sample_is_bounded():
+    """The reference arm's per-step sample shrinks with the step count, so
+    K steps take about a minute of oracle work, never below 8 tokens."""
+    w = WORKLOADS["atlas_muon"]
+    units, T = bench.oracle_sample(w, budget_s=60.0 / 100)
+    assert 8 <= T <= 2 * w.C and T * bench.ORACLE_S_PER_TOKEN["atlas_muon"] <= 0.61
+    units, T10 = bench.oracle_sample(w, budget_s=6.0)
+    assert T10 == 2 * w.C
+    assert bench.default_steps("atlas_muon") == 10 and bench.default_steps("titans_mlp") == 100
+
+
 def test_prologue_bytes_per_step():
     p = PROLOGUES["titans_prologue"]
     # x (bf16) + W_in (bf16) + taps and biases (fp32) in; q, k, v (bf16) and 3 gates (fp32) out
