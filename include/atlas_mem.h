@@ -45,6 +45,10 @@ extern "C" {
 #define ATLAS_ERR_CUDA 3          /* a CUDA runtime call failed (message has the name) */
 #define ATLAS_ERR_OOM 4           /* workspace allocation failed */
 #define ATLAS_ERR_TIMEOUT 5       /* a device-side bounded wait gave up */
+#define ATLAS_ERR_RANGE 6         /* the fused MLP kernel produced a non-finite y or final state:
+                                     an input beyond the range of its fp16 operands (keys, queries
+                                     or values far from unit scale) or a memory that diverged; the
+                                     outputs of that call are not valid */
 
 /* element types of q, k, v, P and the window cache */
 #define ATLAS_F32 0
@@ -167,17 +171,21 @@ int atlas_mem_forward_host(atlas_mem_handle* h, const atlas_mem_io* io, void* st
  * serving loop that forbids allocation after start-up because cudaMalloc may
  * synchronise the device and stall other streams.  This entry point runs the
  * same forward as atlas_mem_forward (same arguments, device pointers, same
- * results) but takes its working memory from a fixed array of
- * ATLAS_NOALLOC_SCRATCH_BYTES that lives in the library's device image, and
- * calls no cudaMalloc, cudaFree or allocating library routine.  The caller
- * still passes every input and output buffer.
+ * kernels, so the same results bit for bit) but takes its working memory from
+ * a fixed array of ATLAS_NOALLOC_SCRATCH_BYTES that lives in the library's
+ * device image, and calls no cudaMalloc, cudaFree or allocating library
+ * routine.  The caller still passes every input and output buffer.
  *
- * - Calls whose working set exceeds the array (atlas_mem_workspace_bytes(h,
- *   B, H, T) > ATLAS_NOALLOC_SCRATCH_BYTES) return ATLAS_ERR_UNSUPPORTED with
- *   a message giving both sizes; nothing is launched.
- * - The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ * - Shapes the fused MLP kernel covers keep their whole state on chip and use
+ *   only the array's status word: any B, H, T.
+ * - Other calls whose working set exceeds the array
+ *   (atlas_mem_workspace_bytes(h, B, H, T) > ATLAS_NOALLOC_SCRATCH_BYTES)
+ *   return ATLAS_ERR_UNSUPPORTED with a message giving both sizes; nothing is
+ *   launched.
+ * - Every call looks up the array's device address (cudaGetSymbolAddress)
+ *   with the calling device current, so the address is never stale after a
+ *   device reset; the first lookup on a device may load the library's device
+ *   code, so make the first call on each device before any stream capture.
  * - Every call, from every handle, shares the one array per device and finds
  *   the previous call's contents there (the status word is cleared on each
  *   call).  Calls whose work overlaps on the GPU race on it: serialise them
@@ -186,7 +194,7 @@ int atlas_mem_forward_host(atlas_mem_handle* h, const atlas_mem_io* io, void* st
 int atlas_mem_forward_noalloc(atlas_mem_handle* h, const atlas_mem_io* io, void* stream);
 
 /* Wait for the last forward on this handle and return its device status
- * (ATLAS_OK or ATLAS_ERR_TIMEOUT).  Clears the status word. */
+ * (ATLAS_OK, ATLAS_ERR_TIMEOUT or ATLAS_ERR_RANGE).  Clears the status word. */
 int atlas_mem_status(atlas_mem_handle* h);
 
 /* Device workspace, in bytes, that a forward of this size uses. */

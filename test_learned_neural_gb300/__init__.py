@@ -13,7 +13,8 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_lib", "libatlas_mem.so")
 
-ATLAS_OK, ATLAS_ERR_INVALID_ARG, ATLAS_ERR_UNSUPPORTED, ATLAS_ERR_CUDA, ATLAS_ERR_OOM, ATLAS_ERR_TIMEOUT = range(6)
+ATLAS_OK, ATLAS_ERR_INVALID_ARG, ATLAS_ERR_UNSUPPORTED, ATLAS_ERR_CUDA, ATLAS_ERR_OOM, ATLAS_ERR_TIMEOUT, \
+    ATLAS_ERR_RANGE = range(7)
 ATLAS_F32, ATLAS_BF16 = 0, 1
 ATLAS_READOUT_POST, ATLAS_READOUT_PRE = 0, 1
 ATLAS_NS_MOMENTUM, ATLAS_NS_SURPRISE = 0, 1

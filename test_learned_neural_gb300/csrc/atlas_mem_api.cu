@@ -5,7 +5,6 @@
 #include <stdlib.h>
 #include <string.h>
 
-#include <mutex>
 #include <string>
 
 #include "atlas_common.cuh"
@@ -410,6 +409,10 @@ extern "C" int atlas_mem_status(atlas_mem_handle* h) {
   CUDA_TRY(cudaMemcpy(&s, h->status, sizeof s, cudaMemcpyDeviceToHost));
   if (s != 0) {
     CUDA_TRY(cudaMemset(h->status, 0, sizeof s));
+    if (s == ATLAS_ERR_RANGE)
+      return fail(h, ATLAS_ERR_RANGE,
+                  "the fused kernel produced a non-finite y or state (an input beyond the range of its fp16 "
+                  "operands, or a diverging memory): this call's outputs are not valid");
     return fail(h, ATLAS_ERR_TIMEOUT, "a device-side wait gave up (status %d)", s);
   }
   return ATLAS_OK;
@@ -608,25 +611,19 @@ extern "C" int atlas_mem_forward_host(atlas_mem_handle* h, const atlas_mem_io* i
 // kernels get the device address from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[ATLAS_NOALLOC_SCRATCH_BYTES];
 
-static std::mutex g_noalloc_mu;
-static void* g_noalloc_ptr[256];  // device address of the scratch, per device ordinal
-
-// Once per device, with that device current: look up the array's device
-// address.  Runs inside the first atlas_mem_forward_noalloc call on a device.
+// The array's device address, looked up on every call with the calling
+// device current (cheap, allocates nothing): an address cached across calls
+// would go stale after a device reset or a new primary context.
 static int noalloc_scratch(atlas_mem_handle* h, void** out) {
-  int dev = 0;
-  CUDA_TRY(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= 256) return fail(h, ATLAS_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p)
-      return fail(h, ATLAS_ERR_CUDA, "cudaGetSymbolAddress(fixed scratch) on device %d: %s", dev,
-                  cudaGetErrorString(e));
-    g_noalloc_ptr[dev] = p;
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || !p) {
+    int dev = -1;
+    cudaGetDevice(&dev);
+    return fail(h, ATLAS_ERR_CUDA, "cudaGetSymbolAddress(fixed scratch) on device %d: %s", dev,
+                cudaGetErrorString(e));
   }
-  *out = g_noalloc_ptr[dev];
+  *out = p;
   return ATLAS_OK;
 }
 
@@ -641,7 +638,10 @@ extern "C" int atlas_mem_forward_noalloc(atlas_mem_handle* h, const atlas_mem_io
   g.n_prev = io->win_len;
   g.L = g.n_prev + g.T;
   const Layout L = layout(g, g.units, g.T);
-  if (L.total > (size_t)ATLAS_NOALLOC_SCRATCH_BYTES)
+  const bool fused = mlp_tc_supported(g);
+  // the fused kernel keeps its state on chip and needs only the status word;
+  // the multi-launch path needs its whole working set in the array
+  if (!fused && L.total > (size_t)ATLAS_NOALLOC_SCRATCH_BYTES)
     return fail(h, ATLAS_ERR_UNSUPPORTED,
                 "this call needs %zu bytes of scratch but atlas_mem_forward_noalloc has a fixed %zu bytes; "
                 "use fewer units or tokens per call, or atlas_mem_forward",
@@ -649,41 +649,25 @@ extern "C" int atlas_mem_forward_noalloc(atlas_mem_handle* h, const atlas_mem_io
   void* base = nullptr;
   rc = noalloc_scratch(h, &base);
   if (rc) return rc;
+  if (fused) {
+    int* status = (int*)base;
+    // the array keeps the previous call's contents: the status word must start at 0
+    CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int), st));
+    h->status = status;
+    CUDA_TRY(mlp_tc_launch(g, io->q, io->k, io->v, io->theta, io->eta, io->alpha, io->gamma, io->W0, io->S0, io->y,
+                           io->W_out, io->S_out, status, st));
+    h->launches = 1;
+    h->last_stream = st;
+    h->launched = true;
+    return ATLAS_OK;
+  }
   float* cache_tmp = nullptr;
   Work w = work_from(g, base, L, &cache_tmp);
-  // the scratch keeps the previous call's contents: the status word must start at 0
   CUDA_TRY(cudaMemsetAsync(w.status, 0, sizeof(int), st));
   h->status = w.status;
-  const bool ns_tc = ns_tc_supported(g);   // keeps S transposed for tall matrices
-  for (int m = 0; m < g.nmat; ++m) {
-    const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
-    CUDA_TRY(cudaMemcpyAsync(w.Wst[0][m], io->W0[m], bytes, cudaMemcpyDeviceToDevice, st));
-    if (ns_tc) CUDA_TRY(ns_tc_state_in(g, m, io->S0[m], w.Sst[0][m], st));
-    else CUDA_TRY(cudaMemcpyAsync(w.Sst[0][m], io->S0[m], bytes, cudaMemcpyDeviceToDevice, st));
-  }
-  GenericIO gio{io->q, io->k, io->v, io->P, io->win_len ? io->win_k : nullptr, io->win_len ? io->win_v : nullptr,
-                io->theta, io->eta, io->alpha, io->gamma, io->win_len ? io->win_gamma : nullptr, io->y};
   int nl = 0;
-  CUDA_TRY(generic_prepare(g, w, gio, st, &nl));
-  int buf = 0;
-  for (int s = 0; s < g.T; s += g.C) {
-    Chunk ch;
-    ch.s = s;
-    ch.e = s + g.C;
-    ch.lo = s - g.c + 1;
-    if (ch.lo < -g.n_prev) ch.lo = -g.n_prev;
-    ch.nw = ch.e - ch.lo;
-    CUDA_TRY(generic_chunk(g, ch, w, gio, buf, st, &nl));
-    buf ^= 1;
-  }
-  for (int m = 0; m < g.nmat; ++m) {
-    const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);
-    CUDA_TRY(cudaMemcpyAsync(io->W_out[m], w.Wst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
-    if (ns_tc) CUDA_TRY(ns_tc_state_out(g, m, w.Sst[buf][m], io->S_out[m], st));
-    else CUDA_TRY(cudaMemcpyAsync(io->S_out[m], w.Sst[buf][m], bytes, cudaMemcpyDeviceToDevice, st));
-  }
-  if (g.c > 1 && (io->win_k_out || io->win_v_out || io->win_gamma_out))
-    CUDA_TRY(generic_cache_out(g, gio, cache_tmp, io->win_k_out, io->win_v_out, io->win_gamma_out, st, &nl));
+  rc = run_generic(h, g, w, io, cache_tmp, st, &nl);
+  if (rc) return rc;
   h->launches = nl;
   h->last_stream = st;
   h->launched = true;

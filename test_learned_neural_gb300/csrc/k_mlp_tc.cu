@@ -27,10 +27,27 @@
 // Cs, Cw, A_t, B_t, D_t are the momentum/decay coefficients of the chunk
 // (scans over eta and 1 - alpha, see k_generic.cu); (B R) scales row t of R
 // by B_t.  Every product is one
-// tcgen05.mma chain (M = 64, bf16 operands, fp32 accumulation in TMEM); the
+// tcgen05.mma chain (M = 64, fp16 operands, fp32 accumulation in TMEM); the
 // operands live in shared memory in the core-matrix layout of tc.cuh, each
 // written once and read K-major or MN-major as the product needs.
-#include <cuda_bf16.h>
+//
+// Operand precision.  The memory's state decays over long sequences (to
+// ~1e-8 on the 4096-token Titans workload), and every chunk's gradient is
+// taken from operands rounded from that fp32 state, so relative rounding
+// errors accumulate over the chunks.  The operands are fp16 (11 significant
+// bits, 8x finer than bf16), each tile multiplied by a power of two that
+// brings its values near 1, so fp16's exponent range never flushes a
+// decayed state:
+//   s1, s2   W1q/S1q and W2q/S2q and the activations derived from them
+//            (A, Aq ~ s1; dz ~ s2), from the CTA-wide maximum of the state
+//            each state update writes.  The scale is a function of that
+//            state alone, so a call that starts from a chunk boundary's
+//            state rounds exactly as one that runs through it;
+//   sx[b]    the chunk's keys and queries (one scale per chunk buffer),
+//            reduced from the prefetched registers a chunk ahead.
+// Epilogues divide the fp32 accumulators by the product of their operands'
+// scales; sums of terms with different scales use separate accumulators.
+#include <cuda_fp16.h>
 
 #include "atlas_common.cuh"
 #include "tc.cuh"
@@ -45,7 +62,11 @@ constexpr int RGS2 = 2048;              // of a 128-column tile
 constexpr int F32T = 64 * 64 * 4;       // fp32 64x64 tile (swizzled rows)
 constexpr long long kWait = 1ll << 31;
 constexpr uint32_t kSliceBytes = (CS - 1) * 16 * 64 * 4;   // fp32 row quarters from the 3 peers
-constexpr uint32_t kDyBytes = (CS - 1) * 16 * 64 * 2;      // bf16 dy rows from the 3 peers
+constexpr uint32_t kDyBytes = (CS - 1) * 16 * 64 * 2;      // fp16 dy rows from the 3 peers
+// fixed powers of two on tiles whose values are O(1) but whose bounds grow
+// with the gates: dy (2 gamma (k + Yp - v)), the state corrections' operands
+// (cs, cw up to C times a step) and M2 (Cw times a Gram of activations)
+constexpr float kDyS = 1.f / 64, kCorrS = 1.f / 16, kM2S = 1.f / 16;
 
 // shared-memory map (bytes): bf16 operand tiles in the core-matrix layout.
 // X, Cw and the gate vectors have two buffers by chunk parity: the next
@@ -117,32 +138,62 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t cta) {
   return r;
 }
 
-// Operands are bf16: the memory's state decays over long sequences (to
-// ~1e-8 on a 4096-token Titans run) and needs fp32's exponent range; fp16
-// would flush it to zero.
-__device__ __forceinline__ void st_h8(uint8_t* tile, int rgs, int row, int col, const float* v) {
-  __nv_bfloat162 h[4];
+// 8 consecutive values of one row, times `scale`, as fp16 into an operand tile
+__device__ __forceinline__ void st_h8(uint8_t* tile, int rgs, int row, int col, const float* v, float scale) {
+  __half2 h[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+  for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(scale * v[2 * i], scale * v[2 * i + 1]);
   *reinterpret_cast<uint4*>(tile + tc::core_offset(row, col, rgs)) = *reinterpret_cast<uint4*>(h);
 }
+// the stored (scaled) values back as fp32
 __device__ __forceinline__ void ld_h8(const uint8_t* tile, int rgs, int row, int col, float* v) {
   const uint4 u = *reinterpret_cast<const uint4*>(tile + tc::core_offset(row, col, rgs));
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+  const __half2* h = reinterpret_cast<const __half2*>(&u);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 f = __bfloat1622float2(h[i]);
+    const float2 f = __half22float2(h[i]);
     v[2 * i] = f.x;
     v[2 * i + 1] = f.y;
   }
 }
 
-// 64 x N (x K) product, bf16 operands, issued by one thread.  Each K step
+// 2^-e for m = f 2^e, f in [0.5, 1): the power of two that brings the
+// largest magnitude m into [0.5, 1) (1 for m = 0 or not finite)
+__device__ __forceinline__ float pow2_scale(float m) {
+  if (!(m > 0.f) || !(m < 3.0e38f)) return 1.f;
+  int e = (int)((__float_as_uint(m) >> 23) & 255u) - 126;   // normal m; subnormals give e = -126
+  // kept within 2^+-60 so that products of three scales stay finite
+  e = e < -60 ? -60 : (e > 60 ? 60 : e);
+  return __uint_as_float((uint32_t)(127 - e) << 23);
+}
+
+// CTA-wide maxima in two halves around a barrier the kernel has anyway:
+// each warp's maximum into slot[warp] (8 floats of shared memory) before
+// it, the CTA's from the slot after it.  No other write to the slot comes
+// before every thread has read it.
+__device__ __forceinline__ void warp_max_to_slot(float v, float* slot) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) slot[threadIdx.x >> 5] = v;
+}
+__device__ __forceinline__ float slot_max(const float* slot) {
+  float m = slot[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) m = fmaxf(m, slot[w]);
+  return m;
+}
+__device__ __forceinline__ float cta_max(float v, float* slot) {
+  warp_max_to_slot(v, slot);
+  __syncthreads();
+  return slot_max(slot);
+}
+
+// 64 x N (x K) product, fp16 operands, issued by one thread.  Each K step
 // moves the operand start address by a fixed byte count, so the descriptors
 // are built once and stepped by adding (bytes >> 4) to their address field.
 __device__ __forceinline__ void mma64(uint32_t d, const uint8_t* a, int a_mn, int a_rgs, const uint8_t* b, int b_mn,
                                       int b_rgs, int N, int K, bool accumulate) {
-  const uint32_t idesc = tc::idesc_f16(64, N, 1, a_mn, b_mn);
+  const uint32_t idesc = tc::idesc_f16(64, N, 0, a_mn, b_mn);
   uint64_t ad = a_mn ? tc::sdesc(tc::smem_u32(a), a_rgs, 128) : tc::sdesc(tc::smem_u32(a), 128, a_rgs);
   uint64_t bd = b_mn ? tc::sdesc(tc::smem_u32(b), b_rgs, 128) : tc::sdesc(tc::smem_u32(b), 128, b_rgs);
   const uint64_t astep = (uint64_t)((a_mn ? 2 * a_rgs : 256) >> 4), bstep = (uint64_t)((b_mn ? 2 * b_rgs : 256) >> 4);
@@ -246,7 +297,7 @@ __device__ __forceinline__ void unpack8(const uint4* w, int dt, float* o) {
 // y rows [16q, 16q + 16) of the chunk at token s: r_t + the four slices'
 // Yq from this CTA's slots (thread: row tid / 16, columns 4 (tid % 16) .. + 3)
 __device__ __forceinline__ void y_rows(float* y, const float* slots, const float* qv, int u, int Tst, int s,
-                                       uint32_t qr) {
+                                       uint32_t qr, bool& ovf) {
   const int tid = threadIdx.x, rl = tid >> 4, cc = (tid & 15) * 4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -255,7 +306,9 @@ __device__ __forceinline__ void y_rows(float* y, const float* slots, const float
     acc.x += t4.x; acc.y += t4.y; acc.z += t4.z; acc.w += t4.w;
   }
   const size_t gb = ((size_t)u * Tst + s + 16 * (int)qr + rl) * D + cc;
-  *reinterpret_cast<float4*>(y + gb) = make_float4(qv[0] + acc.x, qv[1] + acc.y, qv[2] + acc.z, qv[3] + acc.w);
+  const float4 o = make_float4(qv[0] + acc.x, qv[1] + acc.y, qv[2] + acc.z, qv[3] + acc.w);
+  ovf |= !(isfinite(o.x) && isfinite(o.y) && isfinite(o.z) && isfinite(o.w));
+  *reinterpret_cast<float4*>(y + gb) = o;
 }
 
 struct Ctx {
@@ -287,8 +340,13 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   __shared__ uint64_t bar;
   __shared__ uint64_t xbar[3];   // arrivals of the peers' Yp slices, dy rows, Yq slices
   __shared__ uint32_t tbase;
+  __shared__ float redm[3][8];   // CTA-wide maxima: W1/S1, W2/S2, the chunk's keys and queries
   float* vec = reinterpret_cast<float*>(sm + VEC);
   float* cwm = reinterpret_cast<float*>(sm + CWM);
+  // An operand beyond fp16's range becomes inf in its fp32 accumulator, and
+  // every accumulator feeds y or the state: a non-finite y or final state
+  // marks the call (ATLAS_ERR_RANGE) instead of a check at every store.
+  bool ovf = false;
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int sp = warp & 3, half = warp >> 2;
@@ -304,6 +362,10 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   const int u = blockIdx.x / CS;
   const int H = 4 * HQ;
 
+  // operand scales: W1q/S1q and W2q/S2q of the current chunk (s1c, s2c) and
+  // of the tiles its state updates write (s1n, s2n); the keys and queries of
+  // chunk buffer 0 and 1 (sx0, sx1) and of the prefetched chunk (sxp)
+  float s1c = 1.f, s2c = 1.f, s1n = 1.f, s2n = 1.f, sx0 = 1.f, sx1 = 1.f, sxp = 1.f;
   if (warp == 0) tc::tmem_alloc(&tbase, 512);
   if (tid == 0) {
     tc::mbar_init(&bar, 1);
@@ -325,13 +387,22 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     const float* src[4] = {W0a + i1, S0a + i1, W0b + i2, S0b + i2};
     const uint32_t col[4] = {S_W1, S_S1, S_W2, S_S2};
     const int op[4] = {OW1, OS1, OW2, OS2};
-    for (int m = 0; m < 4; ++m) {
-      float x[16];
+    float x[4][16], mx[2] = {0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4*>(x + i) = *reinterpret_cast<const float4*>(src[m] + i);
-      tc::tmem_st16_x2(tb + ls + col[m], x);
-      st_h8(sm + op[m], RGS, row, cb, x);
-      st_h8(sm + op[m], RGS, row, cb + 8, x + 8);
+    for (int m = 0; m < 4; ++m) {
+#pragma unroll
+      for (int i = 0; i < 16; i += 4)
+        *reinterpret_cast<float4*>(x[m] + i) = *reinterpret_cast<const float4*>(src[m] + i);
+      tc::tmem_st16_x2(tb + ls + col[m], x[m]);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) mx[m >> 1] = fmaxf(mx[m >> 1], fabsf(x[m][i]));
+    }
+    s1c = pow2_scale(cta_max(mx[0], redm[0]));
+    s2c = pow2_scale(cta_max(mx[1], redm[1]));
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      st_h8(sm + op[m], RGS, row, cb, x[m], m < 2 ? s1c : s2c);
+      st_h8(sm + op[m], RGS, row, cb + 8, x[m] + 8, m < 2 ? s1c : s2c);
     }
     tc::tmem_st_wait();
   }
@@ -348,10 +419,14 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   const uint32_t red_local = tc::smem_u32(sm + RED);
   // an M = 64 accumulator's row quarters: the owner's own quarter into its
   // slot, the others into the staging blocks (ODZS, 4 KB per owner)
-  auto stage_slices = [&](uint32_t col, int slot_off) {
-    float v16[16];
+  // (the partial is sc * acc[col], plus sc2 * acc[col2] when sc2 != 0)
+  auto stage_slices = [&](uint32_t col, int slot_off, float sc, uint32_t col2, float sc2) {
+    float v16[16], w16[16];
     tc::tmem_ld16_x2(tb + lb + col, v16);
+    if (sc2 != 0.f) tc::tmem_ld16_x2(tb + lb + col2, w16);
     tc::tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v16[i] = sc * v16[i] + (sc2 != 0.f ? sc2 * w16[i] : 0.f);
     const int owner = row >> 4;
     // my own quarter: my slot [qr] (= [owner]); the others: staging block [owner]
     float* base = owner == (int)qr ? reinterpret_cast<float*>(sm + RED + slot_off)
@@ -387,12 +462,18 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   auto load_chunk = [&](int sn, int bn) {
     float* vb = vecb(bn);
     const int r = tid % 64, g = tid / 64;
+    float xk[2][8], xq[2][8];
+#pragma unroll
     for (int j = 0; j < 2; ++j) {
-      float xk[8], xq[8];
-      unpack8(pf.k[j], dt, xk);
-      unpack8(pf.q[j], dt, xq);
-      st_h8(sm + (bn ? OX1 : OX0), RGS, r, (g + 4 * j) * 8, xk);
-      st_h8(sm + OR_, RGS, r, (g + 4 * j) * 8, xq);
+      unpack8(pf.k[j], dt, xk[j]);
+      unpack8(pf.q[j], dt, xq[j]);
+    }
+    const float sc = sxp;   // reduced from these registers beforehand
+    if (bn) sx1 = sc; else sx0 = sc;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      st_h8(sm + (bn ? OX1 : OX0), RGS, r, (g + 4 * j) * 8, xk[j], sc);
+      st_h8(sm + OR_, RGS, r, (g + 4 * j) * 8, xq[j], sc);
     }
     if (tid < 64) {
       vb[V_TH + tid] = pf.th;
@@ -404,6 +485,19 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     unpack4(pf.vd, dt, vvn);
     unpack4(pf.qd, dt, qnx);
     prefetch_chunk(pf, dt, q, k, v, theta, eta, alpha, gamma, u, T, Tst, sn + TOK, qr);
+  };
+
+  // largest magnitude of the prefetched keys and queries held by this thread
+  auto pf_max = [&]() {
+    float xk[8], xq[8], m = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      unpack8(pf.k[j], dt, xk);
+      unpack8(pf.q[j], dt, xq);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fmaxf(fabsf(xk[i]), fabsf(xq[i])));
+    }
+    return m;
   };
 
   // gate scans of buffer bn (window of token t is {t})
@@ -492,20 +586,24 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
   auto brdr = [&](int bn) {
     const float* vb = vecb(bn);
     const int r = tid % 64, g = tid / 64;
-    const float Bt = vb[V_BR + r], Dt = vb[V_DR + r];
+    const float ir = 1.f / (bn ? sx1 : sx0);   // R is stored times the chunk's input scale
+    const float Bt = vb[V_BR + r] * ir, Dt = vb[V_DR + r] * ir;
     for (int j = 0; j < 2; ++j) {
       const int cc = (g + 4 * j) * 8;
       float x[8], b8[8], d8[8];
       ld_h8(sm + OR_, RGS, r, cc, x);
 #pragma unroll
       for (int i = 0; i < 8; ++i) { b8[i] = Bt * x[i]; d8[i] = Dt * x[i]; }
-      st_h8(sm + OBRN, RGS, r, cc, b8);
-      st_h8(sm + ODRN, RGS, r, cc, d8);
+      st_h8(sm + OBRN, RGS, r, cc, b8, 1.f);
+      st_h8(sm + ODRN, RGS, r, cc, d8, 1.f);
     }
   };
 
   // one state half-update: S <- A_e S - corr_S, W <- B_e W + D_e S - corr_W
-  auto state_update = [&](const float* vb, uint32_t c_corr, uint32_t s_w, uint32_t s_s, int ow, int os) {
+  // (ic: 1 / the product of the corrections' operand scales; slot: the
+  // CTA-wide maximum's scratch; s_new: the new state's operand scale)
+  auto state_update = [&](const float* vb, uint32_t c_corr, uint32_t s_w, uint32_t s_s, int ow, int os, float ic,
+                          float* slot, float& s_new) {
     const float Ae = vb[V_AP + 63], Be = vb[V_BP + 63], De = vb[V_DP + 63];
     float scr[16], wcr[16], so[16], wo[16];
     tc::tmem_ld16_x2(tb + lb + c_corr, scr);
@@ -513,26 +611,33 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     tc::tmem_ld16_x2(tb + ls + s_s, so);
     tc::tmem_ld16_x2(tb + ls + s_w, wo);
     tc::tmem_ld_wait();
-    float sn[16], wn[16];
+    float sn[16], wn[16], mx = 0.f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      sn[i] = Ae * so[i] - scr[i];
-      wn[i] = Be * wo[i] + De * so[i] - wcr[i];
+      sn[i] = Ae * so[i] - ic * scr[i];
+      wn[i] = Be * wo[i] + De * so[i] - ic * wcr[i];
+      mx = fmaxf(mx, fmaxf(fabsf(sn[i]), fabsf(wn[i])));
     }
     tc::tmem_st16_x2(tb + ls + s_s, sn);
     tc::tmem_st16_x2(tb + ls + s_w, wn);
-    st_h8(sm + ow, RGS, row, cb, wn);
-    st_h8(sm + ow, RGS, row, cb + 8, wn + 8);
-    st_h8(sm + os, RGS, row, cb, sn);
-    st_h8(sm + os, RGS, row, cb + 8, sn + 8);
+    const float sc = pow2_scale(cta_max(mx, slot));
+    s_new = sc;
+    st_h8(sm + ow, RGS, row, cb, wn, sc);
+    st_h8(sm + ow, RGS, row, cb + 8, wn + 8, sc);
+    st_h8(sm + os, RGS, row, cb, sn, sc);
+    st_h8(sm + os, RGS, row, cb + 8, sn + 8, sc);
     tc::tmem_st_wait();
   };
 
   // ---- first chunk's inputs, gate scans, (B R), (D R) and Z = X W1q
+  sxp = pow2_scale(cta_max(pf_max(), redm[2]));
   load_chunk(0, 0);
+  __syncthreads();   // every thread has read redm[2]
+  warp_max_to_slot(pf_max(), redm[2]);   // chunk 1's, read after the next barrier
 #pragma unroll
   for (int i = 0; i < 4; ++i) { xkd[i] = xkn[i]; vvd[i] = vvn[i]; qcur[i] = qnx[i]; }
   __syncthreads();
+  sxp = pow2_scale(slot_max(redm[2]));
   scan_chunk(0);
   __syncthreads();
   brdr(0);
@@ -562,9 +667,13 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       tc::tmem_ld16_x2(tb + lb + C_Z, z);
       tc::tmem_ld16_x2(tb + lb + C_G1, g);
       tc::tmem_ld_wait();
+      const float sxc = b ? sx1 : sx0;
+      const float iz = 1.f / (sxc * s1c), ig = 1.f / (sxc * sxc);   // Z = (sx X)(s1 W1), G1 = (sx R)(sx X)^T
       float a[16], spv[16], m1[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
+        z[i] *= iz;
+        g[i] *= ig;
         const float sg = sigmoid_fast(z[i]);
         a[i] = z[i] * sg;
         spv[i] = sg * (1.f + z[i] * (1.f - sg));
@@ -574,12 +683,12 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
         const float4 c4 = *reinterpret_cast<const float4*>(cwc + swz(row, cb + i));
         m1[i] = -c4.x * g[i]; m1[i + 1] = -c4.y * g[i + 1]; m1[i + 2] = -c4.z * g[i + 2]; m1[i + 3] = -c4.w * g[i + 3];
       }
-      st_h8(sm + OA, RGS, row, cb, a);
-      st_h8(sm + OA, RGS, row, cb + 8, a + 8);
-      st_h8(sm + OSP, RGS, row, cb, spv);
-      st_h8(sm + OSP, RGS, row, cb + 8, spv + 8);
-      st_h8(sm + OM, RGS, row, cb, m1);
-      st_h8(sm + OM, RGS, row, cb + 8, m1 + 8);
+      st_h8(sm + OA, RGS, row, cb, a, s1c);          // A ~ W1: scale s1
+      st_h8(sm + OA, RGS, row, cb + 8, a + 8, s1c);
+      st_h8(sm + OSP, RGS, row, cb, spv, 1.f);
+      st_h8(sm + OSP, RGS, row, cb + 8, spv + 8, 1.f);
+      st_h8(sm + OM, RGS, row, cb, m1, 1.f);
+      st_h8(sm + OM, RGS, row, cb + 8, m1 + 8, 1.f);
     }
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 2: Yp = A W2q
@@ -595,7 +704,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     // which every sender needs before its next slice is formed.
     if (tid == 0) bulk_wait_read();   // the previous Yq copies have left ODZS
     __syncthreads();
-    stage_slices(C_YP, 0);
+    stage_slices(C_YP, 0, 1.f / (s1c * s2c), 0u, 0.f);   // Yp = (s1 A)(s2 W2)
     if (tid == 0 && cx.ok) send_slices(0, 0);
     // while the peers' slices travel: the next chunk's inputs (R and its
     // buffers are free: this chunk's G1, (B R), (D R) products are done)
@@ -615,14 +724,16 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
         const float4 t4 = *reinterpret_cast<const float4*>(red + slot_idx(p, rl, cc));
         acc.x += t4.x; acc.y += t4.y; acc.z += t4.z; acc.w += t4.w;
       }
-      const float g2 = 2.f * vb[V_GA + r];
-      const __nv_bfloat162 h0 = __floats2bfloat162_rn(g2 * (xkd[0] + acc.x - vvd[0]), g2 * (xkd[1] + acc.y - vvd[1]));
-      const __nv_bfloat162 h1 = __floats2bfloat162_rn(g2 * (xkd[2] + acc.z - vvd[2]), g2 * (xkd[3] + acc.w - vvd[3]));
+      const float g2 = 2.f * vb[V_GA + r] * kDyS;
+      const float d0 = g2 * (xkd[0] + acc.x - vvd[0]), d1 = g2 * (xkd[1] + acc.y - vvd[1]);
+      const float d2 = g2 * (xkd[2] + acc.z - vvd[2]), d3 = g2 * (xkd[3] + acc.w - vvd[3]);
+      const __half2 h0 = __floats2half2_rn(d0, d1);
+      const __half2 h1 = __floats2half2_rn(d2, d3);
       uint2 pk;
       pk.x = *reinterpret_cast<const uint32_t*>(&h0);
       pk.y = *reinterpret_cast<const uint32_t*>(&h1);
       *reinterpret_cast<uint2*>(sm + ODY + tc::core_offset(r, cc, RGS)) = pk;
-      if (s > 0) y_rows(y, reinterpret_cast<const float*>(sm + RED + F32T), qprev, u, Tst, s - TOK, qr);
+      if (s > 0) y_rows(y, reinterpret_cast<const float*>(sm + RED + F32T), qprev, u, Tst, s - TOK, qr, ovf);
     }
     tc::fence_smem_to_async();   // the dy rows are the bulk copies' source
     __syncthreads();
@@ -648,26 +759,30 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     // state operand diag(cs | cw) dy from the broadcast dy tile (overlaps the product)
     {
       const int r = tid % 64, g = tid / 64;
-      const float csr = vb[V_CS + r], cwr = vb[V_CW + r];
+      const float csr = kCorrS * vb[V_CS + r], cwr = kCorrS * vb[V_CW + r];
       for (int j = 0; j < 2; ++j) {
         const int cc = (g + 4 * j) * 8;
         float dy[8], t0[8], t1[8];
         ld_h8(sm + ODY, RGS, r, cc, dy);
 #pragma unroll
         for (int i = 0; i < 8; ++i) { t0[i] = csr * dy[i]; t1[i] = cwr * dy[i]; }
-        st_h8(sm + ODYS, RGS2, r, cc, t0);
-        st_h8(sm + ODYS, RGS2, r, 64 + cc, t1);
+        st_h8(sm + ODYS, RGS2, r, cc, t0, 1.f);
+        st_h8(sm + ODYS, RGS2, r, 64 + cc, t1, 1.f);
       }
     }
     if (tid == 0) bulk_wait_read();   // the Yp copies have left ODZS (rewritten next)
+    // the chunk after next (prefetched at stage 2): its input scale, reduced
+    // at the barrier of the wait below
+    if (has_next) warp_max_to_slot(pf_max(), redm[2]);
     commit_wait(cx);
+    if (has_next) sxp = pow2_scale(slot_max(redm[2]));
     {
       float t[16], spv[16];
       tc::tmem_ld16_x2(tb + lb + C_Z, t);
       ld_h8(sm + OSP, RGS, row, cb, spv);
       ld_h8(sm + OSP, RGS, row, cb + 8, spv + 8);
       tc::tmem_ld_wait();
-      const float csr = vb[V_CS + row], cwr = vb[V_CW + row];
+      const float csr = kCorrS * vb[V_CS + row], cwr = kCorrS * vb[V_CW + row];
       float t0[16], t1[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -675,42 +790,53 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
         t0[i] = csr * t[i];
         t1[i] = cwr * t[i];
       }
-      st_h8(sm + ODZ, RGS, row, cb, t);
-      st_h8(sm + ODZ, RGS, row, cb + 8, t + 8);
-      st_h8(sm + ODZS, RGS2, row, cb, t0);
-      st_h8(sm + ODZS, RGS2, row, cb + 8, t0 + 8);
-      st_h8(sm + ODZS, RGS2, row, 64 + cb, t1);
-      st_h8(sm + ODZS, RGS2, row, 64 + cb + 8, t1 + 8);
+      // t = dz' SiLU'(Z) = kDyS s2 dz (dy's fixed scale, W2's s2)
+      st_h8(sm + ODZ, RGS, row, cb, t, 1.f);
+      st_h8(sm + ODZ, RGS, row, cb + 8, t + 8, 1.f);
+      st_h8(sm + ODZS, RGS2, row, cb, t0, 1.f);   // kCorrS is in csr, cwr
+      st_h8(sm + ODZS, RGS2, row, cb + 8, t0 + 8, 1.f);
+      st_h8(sm + ODZS, RGS2, row, 64 + cb, t1, 1.f);
+      st_h8(sm + ODZS, RGS2, row, 64 + cb + 8, t1 + 8, 1.f);
     }
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 4: Zq += M1 dz; state corrections
     if (tid == 0 && cx.ok) {
-      mma64(tb + C_ZQ, sm + OM, 0, RGS, sm + ODZ, 1, RGS, 64, 64, true);
+      // M1 dz into the Z columns (free: this chunk's Z and dz' are consumed);
+      // its operands carry other scales than Zq's state terms
+      mma64(tb + C_Z, sm + OM, 0, RGS, sm + ODZ, 1, RGS, 64, 64, false);
       mma64(tb + C_ST1, oxc, 1, RGS, sm + ODZS, 1, RGS2, 128, 64, false);    // X^T [cs dz | cw dz]
       mma64(tb + C_ST2, sm + OA, 1, RGS, sm + ODYS, 1, RGS2, 128, 64, false);   // A^T [cs dy | cw dy]
     }
     commit_wait(cx);
     {
       const float Bt = vb[V_BR + row], Dt = vb[V_DR + row];
-      float zq[16];
+      float zq[16], zm[16];
       tc::tmem_ld16_x2(tb + lb + C_ZQ, zq);
+      tc::tmem_ld16_x2(tb + lb + C_Z, zm);
       tc::tmem_ld_wait();
+      // state terms (B R)(s1 W1) + (D R)(s1 S1); M1 (kDyS s2 dz)
+      const float iq = 1.f / s1c, im = 1.f / (kDyS * s2c);
       float aq[16], ab[16], ad[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        aq[i] = zq[i] * sigmoid_fast(zq[i]);
+        zq[i] = iq * zq[i] + im * zm[i];
+        aq[i] = s1c * zq[i] * sigmoid_fast(zq[i]);   // Aq ~ W1: scale s1
         ab[i] = Bt * aq[i];
         ad[i] = Dt * aq[i];
       }
-      st_h8(sm + OAQ, RGS, row, cb, aq);
-      st_h8(sm + OAQ, RGS, row, cb + 8, aq + 8);
-      st_h8(sm + ORB, RGS, row, cb, ab);
-      st_h8(sm + ORB, RGS, row, cb + 8, ab + 8);
-      st_h8(sm + ORD, RGS, row, cb, ad);
-      st_h8(sm + ORD, RGS, row, cb + 8, ad + 8);
+      st_h8(sm + OAQ, RGS, row, cb, aq, 1.f);
+      st_h8(sm + OAQ, RGS, row, cb + 8, aq + 8, 1.f);
+      st_h8(sm + ORB, RGS, row, cb, ab, 1.f);
+      st_h8(sm + ORB, RGS, row, cb + 8, ab + 8, 1.f);
+      st_h8(sm + ORD, RGS, row, cb, ad, 1.f);
+      st_h8(sm + ORD, RGS, row, cb + 8, ad + 8, 1.f);
     }
-    // W1, S1 are no longer read by this chunk's products
-    state_update(vb, C_ST1, S_W1, S_S1, OW1, OS1);
+    // W1, S1 are no longer read by this chunk's products.  Corrections:
+    // (sx X)^T (kCorrS kDyS s2 [cs dz | cw dz])
+    {
+      const float sxc = b ? sx1 : sx0;
+      state_update(vb, C_ST1, S_W1, S_S1, OW1, OS1, 1.f / (sxc * s2c * kCorrS * kDyS), redm[0], s1n);
+    }
     // the corrections product has read ODZS: the next chunk's (B R), (D R)
     if (has_next) brdr(b ^ 1);
     sync_smem_for_mma();
@@ -739,16 +865,20 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
         const float4 c4 = *reinterpret_cast<const float4*>(cwc + swz(row, cb + i));
         m2[i] = -c4.x * g[i]; m2[i + 1] = -c4.y * g[i + 1]; m2[i + 2] = -c4.z * g[i + 2]; m2[i + 3] = -c4.w * g[i + 3];
       }
-      st_h8(sm + OM, RGS, row, cb, m2);
-      st_h8(sm + OM, RGS, row, cb + 8, m2 + 8);
+      // G2 = (s1 Aq)(s1 A)^T: M2 stays in that scale, times kM2S
+      st_h8(sm + OM, RGS, row, cb, m2, kM2S);
+      st_h8(sm + OM, RGS, row, cb + 8, m2 + 8, kM2S);
     }
     sync_smem_for_mma();
     // ---------------------------------------------------------------- 6: Yq += M2 dy
-    if (tid == 0 && cx.ok) mma64(tb + C_YQ, sm + OM, 0, RGS, sm + ODY, 1, RGS, 64, 64, true);
-    // W2, S2 are no longer read by this chunk's products (overlaps the last one)
-    state_update(vb, C_ST2, S_W2, S_S2, OW2, OS2);
+    // M2 dy into the G2 columns (consumed above): other scales than Yq's state terms
+    if (tid == 0 && cx.ok) mma64(tb + C_G2, sm + OM, 0, RGS, sm + ODY, 1, RGS, 64, 64, false);
+    // W2, S2 are no longer read by this chunk's products (overlaps the last
+    // one).  Corrections: (s1 A)^T (kCorrS kDyS [cs dy | cw dy])
+    state_update(vb, C_ST2, S_W2, S_S2, OW2, OS2, 1.f / (s1c * kCorrS * kDyS), redm[1], s2n);
     commit_wait(cx);
-    stage_slices(C_YQ, F32T);
+    // Yq = (s1 B Aq)(s2 W2) + (s1 D Aq)(s2 S2) + (kM2S s1^2 M2)(kDyS dy)
+    stage_slices(C_YQ, F32T, 1.f / (s1c * s2c), C_G2, 1.f / (kM2S * kDyS * s1c * s1c));
     if (tid == 0 && cx.ok) send_slices(F32T, 2);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -757,13 +887,15 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       vvd[i] = vvn[i];
       qcur[i] = qnx[i];
     }
+    s1c = s1n;
+    s2c = s2n;
     sync_smem_for_mma();
   }
   // the last chunk's y
   xwait(2, ((T / TOK) - 1) & 1);
   if (tid == 0) bulk_wait_all();   // every copy this CTA issued has landed
   __syncthreads();
-  y_rows(y, reinterpret_cast<const float*>(sm + RED + F32T), qprev, u, Tst, T - TOK, qr);
+  y_rows(y, reinterpret_cast<const float*>(sm + RED + F32T), qprev, u, Tst, T - TOK, qr, ovf);
 
   // ---- state slices out
   {
@@ -777,9 +909,12 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
       tc::tmem_ld_wait();
 #pragma unroll
       for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4*>(dst[m] + i) = *reinterpret_cast<const float4*>(x + i);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ovf |= !isfinite(x[i]);
     }
   }
   if (!cx.ok && tid == 0) atomicExch(status, ATLAS_ERR_TIMEOUT);
+  if (__syncthreads_or(ovf) && tid == 0) atomicCAS(status, 0, ATLAS_ERR_RANGE);
   tc::fence_before_sync();
   __syncthreads();
   cluster_sync();   // no CTA leaves while a peer may still read its shared memory

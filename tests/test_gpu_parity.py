@@ -235,3 +235,29 @@ def test_small_parity_chunkwise(gpu_lib, case, readout):
             assert v <= tol, (k, v)
         if k.startswith("S"):
             assert v <= 5 * tol, (k, v)
+
+
+def test_fused_kernel_reports_values_beyond_its_operand_range(gpu_lib):
+    """The fused MLP kernel multiplies fp16 operands (scaled per tile by
+    powers of two).  Values far beyond any normalised input (here v = 1e8,
+    so dy leaves fp16's range and the outputs become non-finite) are
+    reported as ATLAS_ERR_RANGE by the status call, without a fault; the
+    next call on the same handle is valid."""
+    import torch
+    from test_learned_neural_gb300.runner import Memory, tensors_from_numpy
+    from harness import bf16_bits
+    w = WORKLOADS["titans_mlp"].scaled(B=1, H=2, T=128)
+    inp = make_inputs(w)
+    big = dict(inp)
+    big["v"] = bf16_bits(np.full(inp["v"].shape, 1.0e8, np.float32))
+    mem = Memory(w)
+    mem.forward(tensors_from_numpy(big))
+    torch.cuda.synchronize()
+    assert gpu_lib.atlas_mem_status(mem.h) == gpu_lib.ATLAS_ERR_RANGE
+    assert "non-finite" in gpu_lib.atlas_mem_last_error(mem.h)
+    out = mem.forward(tensors_from_numpy(inp))
+    torch.cuda.synchronize()
+    assert gpu_lib.atlas_mem_status(mem.h) == gpu_lib.ATLAS_OK
+    ref = oracle.forward(w, inp)
+    assert maxrel(out["y"].cpu().numpy(), ref["y"]) <= TOL["bf16"]
+    mem.close()

@@ -47,11 +47,34 @@ def test_noalloc_matches_forward_on_calls_in_a_row(gpu_lib):
     inps = [make_inputs(w) for w in cases]
     refs = [_call(tln.atlas_mem_forward, w, i) for w, i in zip(cases, inps)]
     # back to back: A, B, then A again over B's leftovers in the fixed array
+    gots = []
     for w, inp, ref in [(cases[0], inps[0], refs[0]), (cases[1], inps[1], refs[1]), (cases[0], inps[0], refs[0])]:
         got = _call(tln.atlas_mem_forward_noalloc, w, inp)
+        gots.append(got)
         tol = TOL[w.qkv_dtype]
         for g, r in zip(got, ref):
             assert maxrel(g, r) <= tol
+    # the same kernels on the same inputs: any difference between the first
+    # and the third call could only come from B's leftovers in the array
+    for a, b in zip(gots[0], gots[2]):
+        assert np.array_equal(a, b)
+    # and the same kernels as atlas_mem_forward: equal bit for bit
+    for g, r in zip(gots[0], refs[0]):
+        assert np.array_equal(g, r)
+    for g, r in zip(gots[1], refs[1]):
+        assert np.array_equal(g, r)
+
+
+@pytest.mark.gpu
+def test_noalloc_runs_the_fused_kernel_at_full_size(gpu_lib):
+    """The fused MLP kernel needs only the array's status word: the full
+    Titans workload, far beyond the array, runs and equals atlas_mem_forward."""
+    w = WORKLOADS["titans_mlp"]
+    inp = make_inputs(w)
+    ref = _call(tln.atlas_mem_forward, w, inp)
+    got = _call(tln.atlas_mem_forward_noalloc, w, inp)
+    for g, r in zip(got, ref):
+        assert np.array_equal(g, r)
 
 
 def test_noalloc_refuses_calls_beyond_its_scratch():
@@ -61,7 +84,7 @@ def test_noalloc_refuses_calls_beyond_its_scratch():
     if not os.path.exists(tln.LIB_PATH):
         tln_build.build()
     lib = tln.load()
-    w = WORKLOADS["titans_mlp"]          # full size: far beyond 16 MiB of scratch
+    w = WORKLOADS["atlas_muon"]          # full size: far beyond 16 MiB of scratch (multi-launch path)
     h = tln.atlas_mem_create(tln.make_config(w.depth, w.d_k, w.d_v, w.hidden, w.C, w.c, w.p, w.proj_dim,
                                              w.ns_iters, w.qkv_dtype))
     try:
