@@ -574,11 +574,10 @@ def run_prologue(args):
                    "conv": p.conv, "l2": "flushed between timed steps (256 MB write)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None, "peak_source": f"hbm_gbs ({src})",
-                     "kernel": "whole stage (cuBLAS projection + k_prologue: one library and one own launch per step)",
+                     "kernel": "whole stage (k_proj_tc projection GEMM + k_prologue: 2 launches per step)",
                      "algorithmic_bytes_per_step": byt,
                      "algorithmic_flops_per_step": 2.0 * p.tokens * p.D * p.N},
-        "gpu_launches": 1 * args.steps,          # k_prologue; the projection is a cuBLAS launch
-        "library_launches": 1 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "e2e": None,
         "clocks": clk,
         "wall_s_timed_region": wall,
@@ -587,6 +586,7 @@ def run_prologue(args):
         tps, cores, desc = time_prologue_oracle(p)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
     print(json.dumps(line), flush=True)
+    pro.status()
     pro.close()
     return 0
 

@@ -25,8 +25,12 @@
  * so the two calls chain on one stream.
  *
  * Execution: asynchronous on the given CUDA stream; the projection is one
- * cuBLAS GEMM (fp32 accumulation) into the handle's workspace, the rest one
- * kernel.  A handle is not re-entrant across concurrent streams.
+ * GEMM of the library's own (fp32 accumulation) into the handle's workspace:
+ * for bf16 inputs tcgen05 tensor-core tiles fed by TMA, exact bf16 products;
+ * for fp32 inputs, or strides and addresses TMA cannot take (D or N not a
+ * multiple of 8, x or W_in not 16-byte aligned), an fp32 SIMT GEMM.  The
+ * rest is one kernel.  A handle is not re-entrant across concurrent
+ * streams.
  *
  * Errors: the status codes of atlas_mem.h; atlas_prologue_last_error gives
  * the message.  Validation failures return before any CUDA call.
@@ -87,6 +91,15 @@ int atlas_prologue_forward(atlas_prologue_handle* h, const atlas_prologue_io* io
 
 /* Device workspace a call of this size needs: the fp32 projection, B T N floats. */
 size_t atlas_prologue_workspace_bytes(const atlas_prologue_handle* h, int B, int T);
+
+/* Wait for the last forward on h and return its device status: ATLAS_OK, or
+ * ATLAS_ERR_TIMEOUT if a bounded wait of the tensor-core projection gave up
+ * (its outputs are then not valid).  Clears the status word. */
+int atlas_prologue_status(atlas_prologue_handle* h);
+
+/* Which projection GEMM the last forward on h ran: 1 = tensor cores (TMA +
+ * tcgen05), 0 = fp32 SIMT, -1 = none yet. */
+int atlas_prologue_last_gemm(const atlas_prologue_handle* h);
 
 /* Message of the last failure on h, or of the last failed create when h is NULL. */
 const char* atlas_prologue_last_error(const atlas_prologue_handle* h);

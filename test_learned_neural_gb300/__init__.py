@@ -26,7 +26,8 @@ EXPORTS = ("atlas_mem_create", "atlas_mem_forward", "atlas_mem_forward_host", "a
            "atlas_mem_status",
            "atlas_mem_workspace_bytes", "atlas_mem_last_launches", "atlas_mem_last_error", "atlas_mem_destroy",
            "atlas_prologue_create", "atlas_prologue_forward", "atlas_prologue_workspace_bytes",
-           "atlas_prologue_last_error", "atlas_prologue_destroy")
+           "atlas_prologue_last_error", "atlas_prologue_destroy", "atlas_prologue_status",
+           "atlas_prologue_last_gemm")
 
 
 class atlas_mem_config(ctypes.Structure):
@@ -108,6 +109,10 @@ def load(path: str = LIB_PATH):
     lib.atlas_prologue_last_error.restype = ctypes.c_char_p
     lib.atlas_prologue_destroy.argtypes = [ctypes.c_void_p]
     lib.atlas_prologue_destroy.restype = None
+    lib.atlas_prologue_status.argtypes = [ctypes.c_void_p]
+    lib.atlas_prologue_status.restype = ctypes.c_int
+    lib.atlas_prologue_last_gemm.argtypes = [ctypes.c_void_p]
+    lib.atlas_prologue_last_gemm.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -182,6 +187,14 @@ def atlas_prologue_workspace_bytes(h, B, T) -> int:
 
 def atlas_prologue_last_error(h) -> str:
     return load().atlas_prologue_last_error(h).decode()
+
+
+def atlas_prologue_status(h) -> int:
+    return load().atlas_prologue_status(h)
+
+
+def atlas_prologue_last_gemm(h) -> int:
+    return load().atlas_prologue_last_gemm(h)
 
 
 def atlas_prologue_destroy(h):

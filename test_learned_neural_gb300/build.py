@@ -54,9 +54,7 @@ def build(verbose: bool = False, extra=()) -> str:
     if failed:
         raise RuntimeError("nvcc failed on: " + ", ".join(os.path.basename(f) for f in failed))
     tmp = LIB + ".tmp"
-    # cuBLAS serves the projection GEMM of the stage in front of the memory
-    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "lib64")
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcublas", "-Xlinker", "-rpath", "-Xlinker", cuda_lib]
+    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
     if r.returncode:
         print(r.stdout, file=sys.stderr)

@@ -1,11 +1,12 @@
-// The stage in front of the memory: projection (one cuBLAS GEMM into the
-// workspace), then one kernel for the causal depthwise convolution, the q/k
-// normalisation, the gate heads, the layout change to [B][H][T][d] and the
-// outgoing convolution cache.
-#include <cublas_v2.h>
+// The stage in front of the memory: projection (one GEMM of our own into the
+// workspace: TMA-fed tcgen05 tiles for bf16 inputs, k_proj_gemm.cu), then
+// one kernel for the causal depthwise convolution, the q/k normalisation,
+// the gate heads, the layout change to [B][H][T][d] and the outgoing
+// convolution cache.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stdint.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -260,12 +261,21 @@ __global__ void __launch_bounds__(kThreads, kSlots * P <= 6 ? 4 : 1) k_prologue(
 
 }  // namespace
 
+namespace atlas {
+size_t proj_gemm_scratch(int N, int K, int bf16);
+cudaError_t proj_gemm(const void* x, const void* W, int M, int N, int Np, int K, int bf16, float* U, void* wt,
+                      int* status, cudaStream_t st, int* kind);
+}
+
 struct atlas_prologue_handle {
   atlas_prologue_config cfg;
   PGeom p;
-  cublasHandle_t blas = nullptr;
-  void* ws = nullptr;
+  void* ws = nullptr;      // the fp32 projection, W_in transposed (tensor-core path), the status word
   size_t ws_bytes = 0;
+  int* status = nullptr;
+  cudaStream_t last_stream = nullptr;
+  bool launched = false;
+  int gemm_kind = -1;      // last projection: 1 tensor cores, 0 SIMT
   std::string err;
 };
 
@@ -311,9 +321,13 @@ extern "C" int atlas_prologue_create(const atlas_prologue_config* cfg, atlas_pro
   return ATLAS_OK;
 }
 
+// bytes of the fp32 projection [B T][Np], rounded to 256
+static size_t proj_bytes(const PGeom& p, int B, int T) { return ((size_t)B * T * p.Np * sizeof(float) + 255) / 256 * 256; }
+
 extern "C" size_t atlas_prologue_workspace_bytes(const atlas_prologue_handle* h, int B, int T) {
   if (!h || B < 1 || T < 1) return 0;
-  return (size_t)B * T * h->p.Np * sizeof(float);
+  // the projection, W_in transposed for the tensor-core GEMM, the status word
+  return proj_bytes(h->p, B, T) + atlas::proj_gemm_scratch(h->p.N, h->p.D, h->p.dtype == ATLAS_BF16) + 256;
 }
 
 extern "C" const char* atlas_prologue_last_error(const atlas_prologue_handle* h) {
@@ -322,7 +336,6 @@ extern "C" const char* atlas_prologue_last_error(const atlas_prologue_handle* h)
 
 extern "C" void atlas_prologue_destroy(atlas_prologue_handle* h) {
   if (!h) return;
-  if (h->blas) cublasDestroy(h->blas);
   if (h->ws) cudaFree(h->ws);
   delete h;
 }
@@ -360,23 +373,18 @@ extern "C" int atlas_prologue_forward(atlas_prologue_handle* h, const atlas_prol
       return pfail(h, ATLAS_ERR_OOM, "cudaMalloc(%zu) failed: %s", need, cudaGetErrorString(e));
     }
     h->ws_bytes = need;
+    h->status = reinterpret_cast<int*>(reinterpret_cast<char*>(h->ws) + (need - 256));
+    e = cudaMemsetAsync(h->status, 0, sizeof(int), st);
+    if (e != cudaSuccess) return pfail(h, ATLAS_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
   }
-  if (!h->blas) {
-    cublasStatus_t s = cublasCreate(&h->blas);
-    if (s != CUBLAS_STATUS_SUCCESS) {
-      h->blas = nullptr;
-      return pfail(h, ATLAS_ERR_CUDA, "cublasCreate failed (status %d)", (int)s);
-    }
+  // U [M][Np] = x [M][D] W_in [D][N], fp32 accumulation
+  {
+    const size_t wt_bytes = atlas::proj_gemm_scratch(p.N, p.D, p.dtype == ATLAS_BF16);
+    void* wt = wt_bytes ? reinterpret_cast<char*>(h->ws) + proj_bytes(p, io->B, io->T) : nullptr;
+    cudaError_t e = atlas::proj_gemm(io->x, io->W_in, (int)M, p.N, p.Np, p.D, p.dtype == ATLAS_BF16, (float*)h->ws,
+                                     wt, h->status, st, &h->gemm_kind);
+    if (e != cudaSuccess) return pfail(h, ATLAS_ERR_CUDA, "projection GEMM launch: %s", cudaGetErrorString(e));
   }
-  cublasStatus_t s = cublasSetStream(h->blas, st);
-  if (s != CUBLAS_STATUS_SUCCESS) return pfail(h, ATLAS_ERR_CUDA, "cublasSetStream failed (status %d)", (int)s);
-  // U [M][N] row-major = x [M][D] W_in [D][N]; in cuBLAS's column-major
-  // terms U^T (N x M) = W_in^T (N x D) x^T (D x M), fp32 accumulation
-  const float one = 1.f, zero = 0.f;
-  const cudaDataType_t in_t = p.dtype == ATLAS_BF16 ? CUDA_R_16BF : CUDA_R_32F;
-  s = cublasGemmEx(h->blas, CUBLAS_OP_N, CUBLAS_OP_N, p.N, (int)M, p.D, &one, io->W_in, in_t, p.N, io->x, in_t, p.D,
-                   &zero, h->ws, CUDA_R_32F, p.Np, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-  if (s != CUBLAS_STATUS_SUCCESS) return pfail(h, ATLAS_ERR_CUDA, "cublasGemmEx failed (status %d)", (int)s);
   const size_t smem = pro_smem_bytes(p);
   // channel pairs where both head widths are even and q, k, v are aligned
   // for paired stores
@@ -408,5 +416,24 @@ extern "C" int atlas_prologue_forward(atlas_prologue_handle* h, const atlas_prol
                                      p.K > 1 ? io->cache_out : nullptr, vec);
   e = cudaGetLastError();
   if (e != cudaSuccess) return pfail(h, ATLAS_ERR_CUDA, "k_prologue launch: %s", cudaGetErrorString(e));
+  h->last_stream = st;
+  h->launched = true;
   return ATLAS_OK;
 }
+
+extern "C" int atlas_prologue_status(atlas_prologue_handle* h) {
+  if (!h) return ATLAS_ERR_INVALID_ARG;
+  if (!h->launched || !h->status) return ATLAS_OK;
+  cudaError_t e = cudaStreamSynchronize(h->last_stream);
+  if (e != cudaSuccess) return pfail(h, ATLAS_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+  int s = 0;
+  e = cudaMemcpy(&s, h->status, sizeof s, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return pfail(h, ATLAS_ERR_CUDA, "cudaMemcpy: %s", cudaGetErrorString(e));
+  if (s != 0) {
+    cudaMemset(h->status, 0, sizeof s);
+    return pfail(h, ATLAS_ERR_TIMEOUT, "a device-side wait of the projection gave up (status %d)", s);
+  }
+  return ATLAS_OK;
+}
+
+extern "C" int atlas_prologue_last_gemm(const atlas_prologue_handle* h) { return h ? h->gemm_kind : -1; }

@@ -12,8 +12,8 @@ import torch
 
 from . import (ATLAS_BF16, ATLAS_F32, atlas_mem_create, atlas_mem_destroy, atlas_mem_forward,
                atlas_mem_forward_host, atlas_mem_status, atlas_prologue_create, atlas_prologue_destroy,
-               atlas_prologue_forward, atlas_prologue_io, current_stream, make_config, make_io,
-               make_prologue_config, AtlasError)
+               atlas_prologue_forward, atlas_prologue_io, atlas_prologue_last_gemm, atlas_prologue_status,
+               current_stream, make_config, make_io, make_prologue_config, AtlasError)
 
 
 def matrix_shapes(cfg):
@@ -156,6 +156,16 @@ class Prologue:
                                ptr(out["eta"]), ptr(out["alpha"]), ptr(out.get("gamma")), ptr(out.get("cache")))
         atlas_prologue_forward(self.h, io, current_stream() if stream is None else stream)
         return out
+
+    def status(self):
+        rc = atlas_prologue_status(self.h)
+        if rc:
+            raise AtlasError(rc, "device status of the stage in front of the memory")
+        return rc
+
+    def last_gemm(self):
+        """1: the projection ran on the tensor cores (TMA + tcgen05), 0: fp32 SIMT."""
+        return atlas_prologue_last_gemm(self.h)
 
 
 def prologue_tensors_from_numpy(inp: dict, device="cuda"):

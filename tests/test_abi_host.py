@@ -143,7 +143,10 @@ def test_prologue_forward_validates_before_any_cuda_call(lib):
         io.cache = io.cache_out = 32
         assert lib.atlas_prologue_forward(h, ctypes.byref(io), None) == tln.ATLAS_ERR_INVALID_ARG
         assert "alias" in tln.atlas_prologue_last_error(h)
-        assert tln.atlas_prologue_workspace_bytes(h, 2, 16) == 2 * 16 * (2 * (2 * 8 + 8) + 4 * 2) * 4
+        # the fp32 projection (rounded to 256 bytes), W_in transposed for the
+        # tensor-core GEMM (bf16 [N][D]: 56 x 32), 256 bytes for the status word
+        N = 2 * (2 * 8 + 8) + 4 * 2
+        assert tln.atlas_prologue_workspace_bytes(h, 2, 16) == -(-2 * 16 * N * 4 // 256) * 256 + N * 32 * 2 + 256
     finally:
         tln.atlas_prologue_destroy(h)
     lib.atlas_prologue_destroy(None)

@@ -53,9 +53,17 @@ def _run(p, inp, T=None):
         t["x"] = t["x"][:, :T].contiguous()
     out = pro.forward(t)
     torch.cuda.synchronize()
+    pro.status()
     res = {k: _host(v) for k, v in out.items()}
+    res["_gemm"] = pro.last_gemm()
     pro.close()
     return res
+
+
+def _tensor_core_projection(p):
+    """The projection runs on the tensor cores (TMA-fed tcgen05 tiles) for
+    bf16 inputs whose row strides TMA can take (D and N multiples of 8)."""
+    return p.qkv_dtype == "bf16" and p.D % 8 == 0 and p.N % 8 == 0
 
 
 def _check(p, g, ref, rows, sl=slice(None), cache=True):
@@ -92,6 +100,7 @@ def test_small_parity(gpu_lib, case, with_cache):
     p = PROLOGUES[name].scaled(**kw)
     inp = make_prologue_inputs(p, cache=with_cache and p.conv > 1)
     g = _run(p, inp)
+    assert g["_gemm"] == (1 if _tensor_core_projection(p) else 0)
     _check(p, g, _oracle_rows(p, inp), list(range(p.B)))
 
 
@@ -127,6 +136,7 @@ def test_full_size_sampled(gpu_lib, name):
     p = PROLOGUES[name]
     inp = make_prologue_inputs(p)
     g = _run(p, inp)
+    assert g["_gemm"] == 1
     rows = sorted({0, p.B - 1})
     _check(p, g, _oracle_rows(p, inp, rows, 0, 96), rows, slice(0, 96), cache=False)
     K = p.conv
