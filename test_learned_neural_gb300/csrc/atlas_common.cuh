@@ -86,6 +86,8 @@ struct Work {
                   // banded coefficient matrices (k_surprise.cu)
   float* aeff;    // chunk-wise update with Newton-Schulz: [units][T] the decay
                   // each token applies (0, the chunk's mean alpha at its last token)
+  void* Pt;       // tensor-core projected features: P transposed, bf16 [proj][monomials
+                  // padded to 64] (k_features_tc.cu)
   int* status;    // device status word
 };
 
@@ -112,6 +114,13 @@ size_t surprise_floats(const Geom& g, size_t units);
 cudaError_t surprise_chunk(const Geom& g, const Chunk& ch, const Work& w, const float* theta, const float* eta,
                            const float* alpha, float* y, int buf, cudaStream_t st, int* nl);
 int num_sms();
+
+// projected polynomial features on the tensor cores (k_features_tc.cu)
+bool features_tc_supported(const Geom& g);
+size_t features_tc_scratch_bytes(const Geom& g);
+cudaError_t features_tc_prepare(const Geom& g, const void* P, void* Pt, cudaStream_t st);
+cudaError_t features_tc_launch(const Geom& g, const void* src, const void* cache, int rows, int from_cache,
+                               const void* Pt, float* out, int* status, cudaStream_t st);
 
 // fused tensor-core MLP memory without Newton-Schulz (k_mlp_tc.cu)
 bool mlp_tc_supported(const Geom& g);

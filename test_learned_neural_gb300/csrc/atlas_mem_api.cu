@@ -162,6 +162,7 @@ static Layout layout(const Geom& g, int units, int T) {
                    : dual1_split_floats(g, U, T),                       // depth 1: scaled dy + feature-slice partials
       g.ns_iters && g.ns_target == ATLAS_NS_SURPRISE ? surprise_floats(g, U) : 0,   // surprise NS scratch
       g.ns_iters && g.update == ATLAS_UPDATE_CHUNKWISE ? U * (size_t)T : 0,          // per-token decay (aeff)
+      (features_tc_scratch_bytes(g) + 3) / 4,                                          // P transposed (bf16)
   };
   const int n = sizeof sizes / sizeof sizes[0];
   size_t o = 0;
@@ -188,6 +189,7 @@ static Work work_from(const Geom& g, void* base, const Layout& L, float** cache_
   w.gpart = F(24);
   w.surp = F(25);
   w.aeff = g.ns_iters && g.update == ATLAS_UPDATE_CHUNKWISE ? F(26) : nullptr;
+  w.Pt = features_tc_scratch_bytes(g) ? (void*)F(27) : nullptr;
   return w;
 }
 

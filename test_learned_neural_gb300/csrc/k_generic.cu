@@ -524,6 +524,15 @@ cudaError_t features_proj_launch(const Geom& g, const void* src, const void* cac
 
 cudaError_t generic_prepare(const Geom& g, const Work& w, const GenericIO& io, cudaStream_t st, int* nl) {
   *nl += 3;
+  if (features_tc_supported(g) && w.Pt) {
+    // tensor cores: P transposed once, then phi(k) P and phi(q) P
+    *nl += 1;
+    CUDA_CHECK_RET(features_tc_prepare(g, io.P, w.Pt, st));
+    CUDA_CHECK_RET(features_tc_launch(g, io.k, io.win_k, g.L, 1, w.Pt, w.X, w.status, st));
+    CUDA_CHECK_RET(features_tc_launch(g, io.q, nullptr, g.T, 0, w.Pt, w.R, w.status, st));
+    k_values<<<dim3(g.L, g.units), 128, 0, st>>>(g, io.v, io.win_v, io.gamma, io.win_gamma, w.V, w.G);
+    return cudaGetLastError();
+  }
   if (features_proj_supported(g)) {
     CUDA_CHECK_RET(features_proj_launch(g, io.k, io.win_k, g.L, 1, io.P, w.X, st));
     CUDA_CHECK_RET(features_proj_launch(g, io.q, nullptr, g.T, 0, io.P, w.R, st));
