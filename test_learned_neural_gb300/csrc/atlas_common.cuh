@@ -115,6 +115,11 @@ cudaError_t surprise_chunk(const Geom& g, const Chunk& ch, const Work& w, const 
                            const float* alpha, float* y, int buf, cudaStream_t st, int* nl);
 int num_sms();
 
+// gradient factors of the depth-2 memory on the tensor cores (k_grad_tc.cu)
+bool grad_tc_supported(const Geom& g);
+cudaError_t grad_tc_fwd_launch(const Geom& g, const Chunk& ch, const Work& w, int buf, float* part, cudaStream_t st);
+cudaError_t grad_tc_dz_launch(const Geom& g, const Chunk& ch, const Work& w, int buf, cudaStream_t st);
+
 // projected polynomial features on the tensor cores (k_features_tc.cu)
 bool features_tc_supported(const Geom& g);
 size_t features_tc_scratch_bytes(const Geom& g);

@@ -968,6 +968,14 @@ size_t grad_part_floats(const Geom& g) {
 
 cudaError_t grad_tiled(const Geom& g, const Chunk& ch, const Work& w, int buf, cudaStream_t st, int* nl) {
   const int rt = (ch.nw + 63) / 64;
+  if (g.depth == 2 && grad_tc_supported(g)) {
+    // tensor cores: z, a and per-block partial outputs; dy; dz
+    CUDA_CHECK_RET(grad_tc_fwd_launch(g, ch, w, buf, w.gpart, st));
+    k_grad2_dy<<<dim3(4, g.units), 256, 0, st>>>(g, ch, w, w.gpart);
+    CUDA_CHECK_RET(cudaGetLastError());
+    *nl += 2;
+    return grad_tc_dz_launch(g, ch, w, buf, st);
+  }
   if (g.depth == 1) {
     k_grad1_tiled<<<dim3((g.d_v + 63) / 64, rt, g.units), 256, 0, st>>>(g, ch, w, buf);
     return cudaGetLastError();

@@ -157,7 +157,8 @@ __global__ void __launch_bounds__(NTHR, 1) k_proj_tc(const __grid_constant__ CUt
     int i = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
       const int a = i & 1;
-      const bool ok = tc::mbar_wait(&acc_full[a], (i >> 1) & 1, kWaitCycles);
+      // warp-uniform: the tcgen05.ld below are .sync.aligned
+      const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&acc_full[a], (i >> 1) & 1, kWaitCycles));
       if (!ok) {
         atomicExch(&failed, 1);
         break;
