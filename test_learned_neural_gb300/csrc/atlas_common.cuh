@@ -139,6 +139,6 @@ bool ns_tc_supported(const Geom& g);
 cudaError_t ns_tc_state_in(const Geom& g, int m, const float* src, float* dst, cudaStream_t st);
 cudaError_t ns_tc_state_out(const Geom& g, int m, const float* src, float* dst, cudaStream_t st);
 cudaError_t ns_tc_launch(const Geom& g, const Chunk& ch, const Work& w, int buf, size_t slot_stride, int num_sms,
-                         cudaStream_t st);
+                         const float* theta, const float* eta, cudaStream_t st);
 
 }  // namespace atlas

@@ -601,7 +601,7 @@ cudaError_t generic_chunk(const Geom& g, const Chunk& ch, const Work& w, const G
   for (int m = 0; m < g.nmat; ++m) slot_stride += (size_t)g.rows[m] * g.cols[m];
   size_t off = 0;
   if (ns_tc_supported(g)) {
-    CUDA_CHECK_RET(ns_tc_launch(g, ch, w, buf, slot_stride, num_sms(), st));
+    CUDA_CHECK_RET(ns_tc_launch(g, ch, w, buf, slot_stride, num_sms(), io.theta, io.eta, st));
     *nl -= g.nmat - 1;   // one tensor-core launch covers every matrix
   } else
   for (int m = 0; m < g.nmat; ++m) {

@@ -94,6 +94,24 @@ __device__ inline void mma_x3(uint32_t d, const uint8_t* a_hi, const uint8_t* a_
   }
 }
 
+// D += A * B^T, as mma_x3 but accumulating onto D's previous contents
+__device__ inline void mma_x3_acc(uint32_t d, const uint8_t* a_hi, const uint8_t* a_lo, int aK, const uint8_t* b_hi,
+                                  const uint8_t* b_lo, int bK, int b_mn, int M, int N, int K) {
+  const uint32_t idesc = tc::idesc_f16(M, N, 1, 0, b_mn);
+  const uint8_t* As[3] = {a_hi, a_hi, a_lo};
+  const uint8_t* Bs[3] = {b_hi, b_lo, b_hi};
+  const uint64_t bstep = (uint64_t)((b_mn ? 2 * bK : 256) >> 4);
+  for (int p = 0; p < 3; ++p) {
+    uint64_t ad = tc::sdesc(tc::smem_u32(As[p]), 128, aK);
+    uint64_t bd = b_mn ? tc::sdesc(tc::smem_u32(Bs[p]), bK, 128) : tc::sdesc(tc::smem_u32(Bs[p]), 128, bK);
+    for (int ks = 0; ks < K / 16; ++ks) {
+      tc::mma_f16(d, ad, bd, idesc, 1u);
+      ad += 256 >> 4;
+      bd += bstep;
+    }
+  }
+}
+
 // [P | Q] = Y_hi [Y_hi ; Y_lo]^T for a 64-row split-bf16 Y (K-major, Y_lo
 // stored 8 row groups after Y_hi): one N = 128 chain instead of two N = 64.
 __device__ inline void mma_hilo(uint32_t d, const uint8_t* y_hi, int rgs, int M, int K) {
@@ -462,7 +480,8 @@ __device__ __forceinline__ void pair_commit_wait(PairCtx& c) {
 }  // namespace
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
-    k_ns_tc128(Geom g, Chunk ch, Work w, int buf, size_t slot_stride, int Kp) {
+    k_ns_tc128(Geom g, Chunk ch, Work w, int buf, size_t slot_stride, int Kp, const float* __restrict__ theta,
+               const float* __restrict__ eta) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ uint64_t bar;
   __shared__ uint32_t tbase;
@@ -488,7 +507,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
   __syncthreads();
   tc::fence_after_sync();
   cluster_sync2();   // both CTAs' exchange barriers are initialised
-  const uint32_t tA = tbase, tA2 = tbase + 128, tX = tbase + 256;
+  // TMEM: the B'X product and, before it, A = X X^T and A^2 in its two
+  // halves (each consumed before the next product writes there); the
+  // running momentum of the current (unit, matrix) in the other 256 columns
+  const uint32_t tX = tbase, tA = tbase, tA2 = tbase + 128, tS = tbase + 256;
   PairCtx cx{&bar, 0u, true};
   uint32_t xe = 0;   // exchanges so far (phase parity of xdata and xfree)
   float* stg = reinterpret_cast<float*>(sm + STG2);                 // [64][128] fp32
@@ -500,15 +522,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
   uint8_t* lx_lo = sm + lxb;
   uint8_t* rx_hi = sm + 2 * lxb;
   uint8_t* rx_lo = sm + 2 * lxb + rxb;
+  // the window update of one token: K = 16 rows (c <= 16)
+  constexpr int KW = 16;
+  const int lwb = R2 * KW * 2, rwb = KW * NH * 2;
+  uint8_t* lw_hi = sm;
+  uint8_t* lw_lo = sm + lwb;
+  uint8_t* rw_hi = sm + 2 * lwb;
+  uint8_t* rw_lo = sm + 2 * lwb + rwb;
   uint8_t* x_hi = sm;
   uint8_t* x_lo = sm + R2 * NH * 2;
   uint8_t* a_hi = sm + OPR2;
   uint8_t* a_lo = sm + OPR2 + R2 * R2 * 2;
-  const int rgsKp = (Kp / 8) * 128, rgsN = (NH / 8) * 128, rgsR = (R2 / 8) * 128;
+  const int rgsKp = (Kp / 8) * 128, rgsN = (NH / 8) * 128, rgsR = (R2 / 8) * 128, rgsKW = (KW / 8) * 128;
 
   const int rn = ns_first_row(g, ch), Cn = ch.e - ch.s - rn;   // tokens [rn, Ct) of the chunk
   const int ntasks = g.units * g.nmat * Cn;
-  for (int task = cl; task < ntasks; task += ncl) {
+  // each CTA pair takes a contiguous run of tasks ordered (unit, matrix,
+  // token), so within a run the momentum steps from one token to the next
+  const int t_begin = (int)((long long)ntasks * cl / ncl), t_end = (int)((long long)ntasks * (cl + 1) / ncl);
+  // momentum held in tS: S_t = lam * Shat for (unit, matrix) cur_um at token cur_r
+  int cur_um = -1, cur_r = -1;
+  float lam = 1.f;
+  for (int task = t_begin; task < t_end; ++task) {
     const int r = rn + task % Cn;
     const int m = (task / Cn) % g.nmat;
     const int u = task / (Cn * g.nmat);
@@ -530,67 +565,136 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
       if (tall) { Lf = dy; lstride = g.d_v; Rf = xf; rstride = g.F; }
       else { Lf = xf; lstride = g.F; Rf = dy; rstride = g.d_v; }
     }
-    const float* cs = w.Cs + ((size_t)u * g.C + r) * g.Kw;
-    const float At = w.Ap[(size_t)u * g.C + r];
     const size_t nel = (size_t)rows * cols;
     const float* Sb = w.Sst[buf][m] + (size_t)u * nel;   // X orientation [128][512]
-
-    // (a) factors: Lx^T (K-major [128][Kp]; thread = (row a, 8 window rows))
-    // and this CTA's columns of diag(cs) Rx
-    for (int e = threadIdx.x; e < R2 * (Kp / 8); e += NT2) {
-      const int a = e % R2, i0 = (e / R2) * 8;
-      float v[8];
+    // the token's momentum steps from the previous one held in TMEM
+    // (titans-pytorch-mlx README, Eq. 14): S_t = eta_t S_{t-1} - theta_t g_t
+    // with g_t the sum of the window rows' gradients (gamma folded in)
+    const bool incr = cur_um == u * g.nmat + m && r == cur_r + 1 && g.update != ATLAS_UPDATE_CHUNKWISE &&
+                      g.c <= KW;
+    if (!incr) {
+      // (a) full: factors Lx^T (K-major [128][Kp]) and this CTA's columns of
+      // diag(cs) Rx, then S_t = A_t Sbar - Lx^T diag(cs) Rx into tS
+      const float* cs = w.Cs + ((size_t)u * g.C + r) * g.Kw;
+      const float At = w.Ap[(size_t)u * g.C + r];
+      for (int e = threadIdx.x; e < R2 * (Kp / 8); e += NT2) {
+        const int a = e % R2, i0 = (e / R2) * 8;
+        float v[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) v[q] = (i0 + q < ch.nw) ? Lf[(size_t)(i0 + q) * lstride + a] : 0.f;
-      store_split16(lx_hi, lx_lo, tc::core_offset(a, i0, rgsKp), v);
-    }
-    for (int e = threadIdx.x; e < Kp * (NH / 8); e += NT2) {
-      const int i = e / (NH / 8), b0 = (e % (NH / 8)) * 8;
-      float v[8];
-      if (i < ch.nw) {
-        const float c = cs[i];
-        const float* src = Rf + (size_t)i * rstride + p * NH + b0;
-        const float4 r0 = *reinterpret_cast<const float4*>(src);
-        const float4 r1 = *reinterpret_cast<const float4*>(src + 4);
-        v[0] = c * r0.x; v[1] = c * r0.y; v[2] = c * r0.z; v[3] = c * r0.w;
-        v[4] = c * r1.x; v[5] = c * r1.y; v[6] = c * r1.z; v[7] = c * r1.w;
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = 0.f;
+        for (int q = 0; q < 8; ++q) v[q] = (i0 + q < ch.nw) ? Lf[(size_t)(i0 + q) * lstride + a] : 0.f;
+        store_split16(lx_hi, lx_lo, tc::core_offset(a, i0, rgsKp), v);
       }
-      store_split16(rx_hi, rx_lo, tc::core_offset(i, b0, rgsN), v);
+      for (int e = threadIdx.x; e < Kp * (NH / 8); e += NT2) {
+        const int i = e / (NH / 8), b0 = (e % (NH / 8)) * 8;
+        float v[8];
+        if (i < ch.nw) {
+          const float c = cs[i];
+          const float* src = Rf + (size_t)i * rstride + p * NH + b0;
+          const float4 r0 = *reinterpret_cast<const float4*>(src);
+          const float4 r1 = *reinterpret_cast<const float4*>(src + 4);
+          v[0] = c * r0.x; v[1] = c * r0.y; v[2] = c * r0.z; v[3] = c * r0.w;
+          v[4] = c * r1.x; v[5] = c * r1.y; v[6] = c * r1.z; v[7] = c * r1.w;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[q] = 0.f;
+        }
+        store_split16(rx_hi, rx_lo, tc::core_offset(i, b0, rgsN), v);
+      }
+      sync_for_mma();
+      if (threadIdx.x == 0 && cx.ok) mma_x3(tX, lx_hi, lx_lo, rgsKp, rx_hi, rx_lo, rgsN, 1, R2, NH, Kp);
+      pair_commit_wait(cx);
+      for (int c32 = 32 * half; c32 < NH; c32 += 64) {
+        float d[32];
+        tc::tmem_ld16(tX + lane_base + c32, d);
+        tc::tmem_ld16(tX + lane_base + c32 + 16, d + 16);
+        const float* sb = Sb + (size_t)row * n + p * NH + c32;
+        float4 s4[8];
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) s4[q4] = *reinterpret_cast<const float4*>(sb + 4 * q4);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          float* o = d + 4 * q4;
+          o[0] = At * s4[q4].x - o[0]; o[1] = At * s4[q4].y - o[1];
+          o[2] = At * s4[q4].z - o[2]; o[3] = At * s4[q4].w - o[3];
+        }
+        tc::tmem_st16(tS + lane_base + c32, d);
+        tc::tmem_st16(tS + lane_base + c32 + 16, d + 16);
+      }
+      tc::tmem_st_wait();
+      lam = 1.f;
+    } else {
+      // (a') incremental: lam_t = lam_{t-1} eta_t; Shat_t = Shat_{t-1} -
+      // (theta_t / lam_t) sum_{i in window(t)} Lf_i^T Rf_i (window rows
+      // w0 .. t - lo of the chunk's factors; K = 16 padded with zeros)
+      const size_t gi = (size_t)u * g.T + t;
+      lam *= __ldg(eta + gi);
+      if (!(lam > 1e-6f)) {
+        // renormalise: Shat <- lam Shat, lam <- 1 (keeps theta / lam finite)
+        for (int c32 = 32 * half; c32 < NH; c32 += 64) {
+          float d[32];
+          tc::tmem_ld16(tS + lane_base + c32, d);
+          tc::tmem_ld16(tS + lane_base + c32 + 16, d + 16);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 32; ++q) d[q] *= lam;
+          tc::tmem_st16(tS + lane_base + c32, d);
+          tc::tmem_st16(tS + lane_base + c32 + 16, d + 16);
+        }
+        tc::tmem_st_wait();
+        lam = 1.f;
+      }
+      const float coef = -__ldg(theta + gi) / lam;
+      const int wt = t - ch.lo;                               // window row of token t
+      const int w0 = (t - g.c + 1 > ch.lo ? t - g.c + 1 : ch.lo) - ch.lo;
+      for (int e = threadIdx.x; e < R2 * (KW / 8); e += NT2) {
+        const int a = e % R2, i0 = (e / R2) * 8;
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int i = w0 + i0 + q;
+          v[q] = (i <= wt) ? coef * Lf[(size_t)i * lstride + a] : 0.f;
+        }
+        store_split16(lw_hi, lw_lo, tc::core_offset(a, i0, rgsKW), v);
+      }
+      for (int e = threadIdx.x; e < KW * (NH / 8); e += NT2) {
+        const int k = e / (NH / 8), b0 = (e % (NH / 8)) * 8, i = w0 + k;
+        float v[8];
+        if (i <= wt) {
+          const float* src = Rf + (size_t)i * rstride + p * NH + b0;
+          const float4 r0 = *reinterpret_cast<const float4*>(src);
+          const float4 r1 = *reinterpret_cast<const float4*>(src + 4);
+          v[0] = r0.x; v[1] = r0.y; v[2] = r0.z; v[3] = r0.w; v[4] = r1.x; v[5] = r1.y; v[6] = r1.z; v[7] = r1.w;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[q] = 0.f;
+        }
+        store_split16(rw_hi, rw_lo, tc::core_offset(k, b0, rgsN), v);
+      }
+      sync_for_mma();
+      if (threadIdx.x == 0 && cx.ok) mma_x3_acc(tS, lw_hi, lw_lo, rgsKW, rw_hi, rw_lo, rgsN, 1, R2, NH, KW);
+      pair_commit_wait(cx);
     }
-    sync_for_mma();
-    // (b) D = Lx^T diag(cs) Rx[:, half]   (M = 128, N = 256, K = Kp)
-    if (threadIdx.x == 0 && cx.ok) mma_x3(tX, lx_hi, lx_lo, rgsKp, rx_hi, rx_lo, rgsN, 1, R2, NH, Kp);
-    pair_commit_wait(cx);
-    // (c) S = A_t Sbar - D, written back over D in TMEM; sum of squares over
-    // both halves; chunk-end S
+    cur_um = u * g.nmat + m;
+    cur_r = r;
+    // (c) ||S_t||_F = lam ||Shat|| over both halves; chunk-end S
     float ss = 0.f;
     const bool last_tok = (t == ch.e - 1);
     float* So = w.Sst[buf ^ 1][m] + (size_t)u * nel;
     for (int c32 = 32 * half; c32 < NH; c32 += 64) {
       float d[32];
-      tc::tmem_ld16(tX + lane_base + c32, d);
-      tc::tmem_ld16(tX + lane_base + c32 + 16, d + 16);
-      const float* sb = Sb + (size_t)row * n + p * NH + c32;
-      float4 s4[8];
-#pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) s4[q4] = *reinterpret_cast<const float4*>(sb + 4 * q4);
+      tc::tmem_ld16(tS + lane_base + c32, d);
+      tc::tmem_ld16(tS + lane_base + c32 + 16, d + 16);
       tc::tmem_ld_wait();
 #pragma unroll
       for (int q4 = 0; q4 < 8; ++q4) {
-        float* o = d + 4 * q4;
-        o[0] = At * s4[q4].x - o[0]; o[1] = At * s4[q4].y - o[1];
-        o[2] = At * s4[q4].z - o[2]; o[3] = At * s4[q4].w - o[3];
+        const float* o = d + 4 * q4;
         ss += o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
-        if (last_tok) *reinterpret_cast<float4*>(So + (size_t)row * n + p * NH + c32 + 4 * q4) =
-            make_float4(o[0], o[1], o[2], o[3]);
+        if (last_tok)
+          *reinterpret_cast<float4*>(So + (size_t)row * n + p * NH + c32 + 4 * q4) =
+              make_float4(lam * o[0], lam * o[1], lam * o[2], lam * o[3]);
       }
-      tc::tmem_st16(tX + lane_base + c32, d);
-      tc::tmem_st16(tX + lane_base + c32 + 16, d + 16);
     }
-    tc::tmem_st_wait();
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (lane == 0) red[warp] = ss;
     __syncthreads();
@@ -601,12 +705,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
     }
     cluster_sync2();
     const float tot = ss_cta + ld_cluster_f(mapa2(tc::smem_u32(&ss_cta), p ^ 1u));
-    const float scale = 1.f / (sqrtf(tot) + kNsEps);
-    // (d) X_0 = S * scale -> split bf16 into this CTA's half of X
+    // X_0 = S_t / (||S_t|| + eps) = Shat * lam / (lam ||Shat|| + eps)
+    const float scale = lam / (lam * sqrtf(tot) + kNsEps);
+    // (d) X_0 -> split bf16 into this CTA's half of X
     for (int c32 = 32 * half; c32 < NH; c32 += 64) {
       float d[32];
-      tc::tmem_ld16(tX + lane_base + c32, d);
-      tc::tmem_ld16(tX + lane_base + c32 + 16, d + 16);
+      tc::tmem_ld16(tS + lane_base + c32, d);
+      tc::tmem_ld16(tS + lane_base + c32 + 16, d + 16);
       tc::tmem_ld_wait();
 #pragma unroll
       for (int q = 0; q < 32; ++q) d[q] *= scale;
@@ -615,7 +720,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
     }
     cluster_sync2();   // both CTAs read ss_cta above before the next task rewrites it
     sync_for_mma();
-
     float* slot = w.Ubuf + ((size_t)u * g.C + r) * slot_stride;
     for (int mm = 0; mm < m; ++mm) slot += (size_t)g.rows[mm] * g.cols[mm];
     for (int it = 0; it < g.ns_iters; ++it) {
@@ -789,7 +893,7 @@ cudaError_t ns_tc_state_out(const Geom& g, int m, const float* src, float* dst, 
 }
 
 cudaError_t ns_tc_launch(const Geom& g, const Chunk& ch, const Work& w, int buf, size_t slot_stride, int num_sms,
-                         cudaStream_t st) {
+                         const float* theta, const float* eta, cudaStream_t st) {
   const int n = g.rows[0] < g.cols[0] ? g.cols[0] : g.rows[0];
   const int Kp = (g.Kw + 15) / 16 * 16;
   if (ns_tc_kind(g) == 2) {
@@ -798,7 +902,7 @@ cudaError_t ns_tc_launch(const Geom& g, const Chunk& ch, const Work& w, int buf,
     const int ntasks = g.units * g.nmat * (ch.e - ch.s - ns_first_row(g, ch));
     int ncl = num_sms / 2;
     if (ncl > ntasks) ncl = ntasks;
-    k_ns_tc128<<<2 * ncl, NT2, SMEM2, st>>>(g, ch, w, buf, slot_stride, Kp);
+    k_ns_tc128<<<2 * ncl, NT2, SMEM2, st>>>(g, ch, w, buf, slot_stride, Kp, theta, eta);
     return cudaGetLastError();
   }
   const int smem = ns_smem_layout(n, Kp).total;
