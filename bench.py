@@ -367,7 +367,10 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
-    w = replica_workload(WORKLOADS[args.workload], rank)
+    w = WORKLOADS[args.workload]
+    if args.geometry:
+        w = w.scaled(**args.geometry)
+    w = replica_workload(w, rank)
     inp = make_inputs(w)
     t = tensors_from_numpy(inp, device=dev)
     mem = Memory(w)
@@ -457,7 +460,7 @@ def run_ours(args):
         peak_src = f"{key} ({src})"
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
+    if os.path.exists(tpath) and not args.geometry:
         rec = json.load(open(tpath)).get(w.name)
         if rec and rec.get("source_digest") == source_digest(TRAFFIC_SOURCES.get(w.name)):
             traffic = rec.get("dram_bytes_per_step")
@@ -468,7 +471,8 @@ def run_ours(args):
         "data": "synthetic (seeded, harness recipe), inputs resident in HBM",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "depth": w.depth, "d": w.d_v,
                    "hidden": w.hidden, "C": w.C, "c": w.c, "p": w.p, "ns_iters": w.ns_iters,
-                   "l2": "flushed between timed steps (256 MB write)", "parallelism": f"replicas x{world}"},
+                   "l2": "flushed between timed steps (256 MB write)", "parallelism": f"replicas x{world}",
+                   **({"geometry": "reduced (--geometry), profiling case"} if args.geometry else {})},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": runit,
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                      "kernel": ("atlas::k_mlp_dual_tc (the step's only launch)" if launches == 1
@@ -612,12 +616,20 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--geometry", default=None, metavar="B,H,T",
+                    help="run the workload's method at a smaller batch x heads x length (for profiler captures; "
+                         "the JSON line's config names the geometry and is not a headline number)")
     args = ap.parse_args(argv)
+    if args.geometry is not None:
+        b, h, t = (int(v) for v in args.geometry.split(","))
+        args.geometry = {"B": b, "H": h, "T": t}
     if args.steps is None:
         args.steps = default_steps(args.workload)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.workload in PROLOGUES:
+        if args.geometry:
+            ap.error("--geometry applies to the memory workloads only")
         return run_prologue(args)
     if args.impl == "reference":
         return run_reference(args)

@@ -36,6 +36,25 @@ struct Chunk {
   int s, e, lo, nw;  // nw = e - lo window rows
 };
 
+// Chunk of the call starting at token s (s a multiple of C).
+__host__ __device__ inline Chunk dual1_chunk_at(const Geom& g, int s) {
+  Chunk c;
+  c.s = s;
+  c.e = s + g.C;
+  c.lo = s - g.c + 1;
+  if (c.lo < -g.n_prev) c.lo = -g.n_prev;
+  c.nw = c.e - c.lo;
+  return c;
+}
+
+// per (unit, chunk) coefficient block: Cw [C][Kw], cs_e [Kw], cw_e [Kw],
+// B_t [C], D_t [C], (A_e, B_e, D_e, pad).  Cw, B_t, D_t are the read-out's
+// (shifted by one token in pre-update mode); cs_e, cw_e, A_e, B_e, D_e the
+// chunk-end state's.
+__host__ __device__ inline size_t dual1_coef_floats(const Geom& g) {
+  return (size_t)g.C * g.Kw + 2 * (size_t)g.Kw + 2 * (size_t)g.C + 4;
+}
+
 // First token of a chunk (0-based in the chunk) whose momentum goes through
 // Newton-Schulz: every token under the per-token rule; under the chunk-wise
 // rule the memory changes once per chunk, so only the last token's.  The
@@ -108,6 +127,17 @@ size_t generic_smem_readout(const Geom& g);
 size_t generic_smem_ns(const Geom& g, int m);
 size_t grad_part_floats(const Geom& g);
 size_t dual1_split_floats(const Geom& g, size_t units, int T);
+// every chunk's gate-scan coefficient block of the depth-1 paths, up front
+cudaError_t dual1_coef_launch(const Geom& g, const GenericIO& io, float* coef, cudaStream_t st);
+// values and Omega weights of every key row into the workspace (V, G)
+cudaError_t values_launch(const Geom& g, const Work& w, const GenericIO& io, cudaStream_t st);
+
+// depth-1 memory on polynomial features on the tensor cores, one persistent
+// launch per call (k_dual1_tc.cu)
+bool dual1_tc_supported(const Geom& g);
+bool dual1_tc_inputs_ok(const GenericIO& io);
+cudaError_t dual1_tc_launch(const Geom& g, const Work& w, const GenericIO& io, const float* coef, int fbuf,
+                            cudaStream_t st);
 
 // Newton-Schulz on the windowed surprise (k_surprise.cu)
 size_t surprise_floats(const Geom& g, size_t units);

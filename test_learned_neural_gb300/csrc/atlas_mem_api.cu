@@ -300,17 +300,22 @@ static int run_generic(atlas_mem_handle* h, const Geom& g, const Work& w, const 
   }
   GenericIO gio{io->q, io->k, io->v, io->P, io->win_len ? io->win_k : nullptr, io->win_len ? io->win_v : nullptr,
                 io->theta, io->eta, io->alpha, io->gamma, io->win_len ? io->win_gamma : nullptr, io->y};
-  CUDA_TRY(generic_prepare(g, w, gio, st, &nl));
   int buf = 0;
-  for (int s = 0; s < g.T; s += g.C) {
-    Chunk ch;
-    ch.s = s;
-    ch.e = s + g.C;
-    ch.lo = s - g.c + 1;
-    if (ch.lo < -g.n_prev) ch.lo = -g.n_prev;
-    ch.nw = ch.e - ch.lo;
-    CUDA_TRY(generic_chunk(g, ch, w, gio, buf, st, &nl));
-    buf ^= 1;
+  if (dual1_tc_supported(g) && dual1_tc_inputs_ok(gio)) {
+    // depth 1 on the tensor cores: values, every chunk's gate coefficients,
+    // then one persistent launch that keeps the state on chip
+    CUDA_TRY(values_launch(g, w, gio, st));
+    CUDA_TRY(dual1_coef_launch(g, gio, w.gpart, st));
+    buf = (g.T / g.C) & 1;
+    CUDA_TRY(dual1_tc_launch(g, w, gio, w.gpart, buf, st));
+    nl += 3;
+  } else {
+    CUDA_TRY(generic_prepare(g, w, gio, st, &nl));
+    for (int s = 0; s < g.T; s += g.C) {
+      const Chunk ch = dual1_chunk_at(g, s);
+      CUDA_TRY(generic_chunk(g, ch, w, gio, buf, st, &nl));
+      buf ^= 1;
+    }
   }
   for (int m = 0; m < g.nmat; ++m) {
     const size_t bytes = (size_t)g.units * g.rows[m] * g.cols[m] * sizeof(float);

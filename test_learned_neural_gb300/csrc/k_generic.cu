@@ -1218,24 +1218,6 @@ __global__ void __launch_bounds__(256) k_dual1_partials(Geom g, Chunk ch, Work w
   dual1_partials_smem(g, ch, Rt, Xt, Ws, Ss, part + ((size_t)u * gridDim.x + kb) * dual1_part_floats(g));
 }
 
-__host__ __device__ inline Chunk dual1_chunk_at(const Geom& g, int s) {
-  Chunk c;
-  c.s = s;
-  c.e = s + g.C;
-  c.lo = s - g.c + 1;
-  if (c.lo < -g.n_prev) c.lo = -g.n_prev;
-  c.nw = c.e - c.lo;
-  return c;
-}
-
-// per (unit, chunk) coefficient block: Cw [C][Kw], cs_e [Kw], cw_e [Kw],
-// B_t [C], D_t [C], (A_e, B_e, D_e, pad).  Cw, B_t, D_t are the read-out's
-// (shifted by one token in pre-update mode); cs_e, cw_e, A_e, B_e, D_e the
-// chunk-end state's.
-__host__ __device__ inline size_t dual1_coef_floats(const Geom& g) {
-  return (size_t)g.C * g.Kw + 2 * (size_t)g.Kw + 2 * (size_t)g.C + 4;
-}
-
 // The gate scans depend on theta, eta, alpha only, so every chunk's are
 // formed up front, one CTA per (chunk, unit):
 //   Cs_t[i] = eta_t Cs_{t-1}[i] + theta_t [t in window of row i],
@@ -1453,6 +1435,16 @@ __global__ void __launch_bounds__(512) k_dual1_step(Geom g, Chunk ch, Chunk nx, 
       store_tile(PG, dv, i0, nwn, dv, acc, tid);
     }
   }
+}
+
+cudaError_t dual1_coef_launch(const Geom& g, const GenericIO& io, float* coef, cudaStream_t st) {
+  k_dual1_coef_all<<<dim3(g.T / g.C, g.units), 160, 0, st>>>(g, io.theta, io.eta, io.alpha, coef);
+  return cudaGetLastError();
+}
+
+cudaError_t values_launch(const Geom& g, const Work& w, const GenericIO& io, cudaStream_t st) {
+  k_values<<<dim3(g.L, g.units), 128, 0, st>>>(g, io.v, io.win_v, io.gamma, io.win_gamma, w.V, w.G);
+  return cudaGetLastError();
 }
 
 bool dual1_split_supported(const Geom& g) {
