@@ -47,13 +47,27 @@ __host__ __device__ inline Chunk dual1_chunk_at(const Geom& g, int s) {
   return c;
 }
 
-// per (unit, chunk) coefficient block: Cw [C][Kw], cs_e [Kw], cw_e [Kw],
-// B_t [C], D_t [C], (A_e, B_e, D_e, pad).  Cw, B_t, D_t are the read-out's
-// (shifted by one token in pre-update mode); cs_e, cw_e, A_e, B_e, D_e the
-// chunk-end state's.
-__host__ __device__ inline size_t dual1_coef_floats(const Geom& g) {
-  return (size_t)g.C * g.Kw + 2 * (size_t)g.Kw + 2 * (size_t)g.C + 4;
+// Layout of one (unit, chunk) coefficient block of the depth-1 paths:
+// Cw [C][kws], cs_e [kws], cw_e [kws], B_t [cp], D_t [cp], (A_e, B_e, D_e,
+// pad), row stride kws >= Kw, cp >= C; entries past the chunk's window rows
+// or tokens are zero.  Cw, B_t, D_t are the read-out's (shifted by one token
+// in pre-update mode); cs_e, cw_e, A_e, B_e, D_e the chunk-end state's.
+struct CoefLayout {
+  int kws, cp;
+  __host__ __device__ size_t floats(int C) const { return (size_t)C * kws + 2 * (size_t)kws + 2 * (size_t)cp + 4; }
+  __host__ __device__ size_t o_cs(int C) const { return (size_t)C * kws; }
+  __host__ __device__ size_t o_cw(int C) const { return o_cs(C) + kws; }
+  __host__ __device__ size_t o_bt(int C) const { return o_cw(C) + kws; }
+  __host__ __device__ size_t o_dt(int C) const { return o_bt(C) + cp; }
+  __host__ __device__ size_t o_abd(int C) const { return o_dt(C) + cp; }
+};
+// the fp32 split path's: unpadded
+__host__ __device__ inline CoefLayout coef_layout_simt(const Geom& g) { return CoefLayout{g.Kw, g.C}; }
+// the tensor-core path's: rows of 16-byte multiples (16-byte copies)
+__host__ __device__ inline CoefLayout coef_layout_tc(const Geom& g) {
+  return CoefLayout{(g.Kw + 15) / 16 * 16, (g.C + 3) / 4 * 4};
 }
+__host__ __device__ inline size_t dual1_coef_floats(const Geom& g) { return coef_layout_simt(g).floats(g.C); }
 
 // First token of a chunk (0-based in the chunk) whose momentum goes through
 // Newton-Schulz: every token under the per-token rule; under the chunk-wise
@@ -128,7 +142,7 @@ size_t generic_smem_ns(const Geom& g, int m);
 size_t grad_part_floats(const Geom& g);
 size_t dual1_split_floats(const Geom& g, size_t units, int T);
 // every chunk's gate-scan coefficient block of the depth-1 paths, up front
-cudaError_t dual1_coef_launch(const Geom& g, const GenericIO& io, float* coef, cudaStream_t st);
+cudaError_t dual1_coef_launch(const Geom& g, const GenericIO& io, float* coef, CoefLayout L, cudaStream_t st);
 // values and Omega weights of every key row into the workspace (V, G)
 cudaError_t values_launch(const Geom& g, const Work& w, const GenericIO& io, cudaStream_t st);
 

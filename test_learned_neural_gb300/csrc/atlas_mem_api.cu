@@ -305,7 +305,7 @@ static int run_generic(atlas_mem_handle* h, const Geom& g, const Work& w, const 
     // depth 1 on the tensor cores: values, every chunk's gate coefficients,
     // then one persistent launch that keeps the state on chip
     CUDA_TRY(values_launch(g, w, gio, st));
-    CUDA_TRY(dual1_coef_launch(g, gio, w.gpart, st));
+    CUDA_TRY(dual1_coef_launch(g, gio, w.gpart, coef_layout_tc(g), st));
     buf = (g.T / g.C) & 1;
     CUDA_TRY(dual1_tc_launch(g, w, gio, w.gpart, buf, st));
     nl += 3;

@@ -1224,7 +1224,7 @@ __global__ void __launch_bounds__(256) k_dual1_partials(Geom g, Chunk ch, Work w
 //   Cw_t[i] = (1 - alpha_t) Cw_{t-1}[i] + Cs_t[i],
 //   A_t = prod eta, B_t = prod (1 - alpha), D_t = (1 - alpha_t) D_{t-1} + A_t.
 __global__ void __launch_bounds__(160) k_dual1_coef_all(Geom g, const float* theta, const float* eta,
-                                                         const float* alpha, float* coef) {
+                                                         const float* alpha, float* coef, CoefLayout L) {
   __shared__ float th[64], et[64], be[64];
   const int n = blockIdx.x, u = blockIdx.y;
   // pre-update read-out: token r reads the state after token r - 1 (the
@@ -1238,13 +1238,13 @@ __global__ void __launch_bounds__(160) k_dual1_coef_all(Geom g, const float* the
     be[r] = 1.f - alpha[(size_t)u * g.T + ch.s + r];
   }
   __syncthreads();
-  float* cb = coef + ((size_t)u * gridDim.x + n) * dual1_coef_floats(g);
+  float* cb = coef + ((size_t)u * gridDim.x + n) * L.floats(g.C);
   float* Cw = cb;
-  float* cse = Cw + (size_t)g.C * g.Kw;
-  float* cwe = cse + g.Kw;
-  float* Bt = cwe + g.Kw;
-  float* Dt = Bt + g.C;
-  float* ABD = Dt + g.C;
+  float* cse = cb + L.o_cs(g.C);
+  float* cwe = cb + L.o_cw(g.C);
+  float* Bt = cb + L.o_bt(g.C);
+  float* Dt = cb + L.o_dt(g.C);
+  float* ABD = cb + L.o_abd(g.C);
   if (threadIdx.x < ch.nw) {
     const int i = threadIdx.x, ti = ch.lo + i;
     float cs = 0.f, cw = 0.f;
@@ -1254,10 +1254,15 @@ __global__ void __launch_bounds__(160) k_dual1_coef_all(Geom g, const float* the
       const float cw_prev = cw;
       cs = et[r] * cs + (in_win ? th[r] : 0.f);
       cw = be[r] * cw + cs;
-      Cw[(size_t)r * g.Kw + i] = pre ? cw_prev : cw;   // read-out weights of token r
+      Cw[(size_t)r * L.kws + i] = pre ? cw_prev : cw;   // read-out weights of token r
     }
     cse[i] = cs;
     cwe[i] = cw;
+  } else if (threadIdx.x < L.kws) {   // padding columns past the window
+    const int i = threadIdx.x;
+    for (int r = 0; r < Ct; ++r) Cw[(size_t)r * L.kws + i] = 0.f;
+    cse[i] = 0.f;
+    cwe[i] = 0.f;
   } else if (threadIdx.x == blockDim.x - 1) {
     float Ap = 1.f, Bp = 1.f, Dp = 0.f;
     for (int r = 0; r < Ct; ++r) {
@@ -1268,9 +1273,14 @@ __global__ void __launch_bounds__(160) k_dual1_coef_all(Geom g, const float* the
       Bt[r] = pre ? Bprev : Bp;
       Dt[r] = pre ? Dprev : Dp;
     }
+    for (int r = Ct; r < L.cp; ++r) {
+      Bt[r] = 0.f;
+      Dt[r] = 0.f;
+    }
     ABD[0] = Ap;
     ABD[1] = Bp;
     ABD[2] = Dp;
+    ABD[3] = 0.f;
   }
 }
 
@@ -1437,8 +1447,8 @@ __global__ void __launch_bounds__(512) k_dual1_step(Geom g, Chunk ch, Chunk nx, 
   }
 }
 
-cudaError_t dual1_coef_launch(const Geom& g, const GenericIO& io, float* coef, cudaStream_t st) {
-  k_dual1_coef_all<<<dim3(g.T / g.C, g.units), 160, 0, st>>>(g, io.theta, io.eta, io.alpha, coef);
+cudaError_t dual1_coef_launch(const Geom& g, const GenericIO& io, float* coef, CoefLayout L, cudaStream_t st) {
+  k_dual1_coef_all<<<dim3(g.T / g.C, g.units), 160, 0, st>>>(g, io.theta, io.eta, io.alpha, coef, L);
   return cudaGetLastError();
 }
 
@@ -1454,7 +1464,7 @@ bool dual1_split_supported(const Geom& g) {
 
 size_t dual1_split_floats(const Geom& g, size_t units, int T) {
   return units * (2 * (size_t)g.Kw * g.d_v + (size_t)((g.F + 63) / 64 + 1) * dual1_part_floats(g) +
-                  (size_t)(T / g.C) * dual1_coef_floats(g));
+                  (size_t)(T / g.C) * coef_layout_tc(g).floats(g.C));   // covers both layouts
 }
 
 cudaError_t dual1_split(const Geom& g, const Chunk& ch, const Work& w, const GenericIO& io, int buf,
@@ -1466,7 +1476,8 @@ cudaError_t dual1_split(const Geom& g, const Chunk& ch, const Work& w, const Gen
   float* red = part + (size_t)g.units * ks * per;
   float* coef = red + (size_t)g.units * per;
   if (ch.s == 0) {
-    k_dual1_coef_all<<<dim3(g.T / g.C, g.units), 160, 0, st>>>(g, io.theta, io.eta, io.alpha, coef);
+    k_dual1_coef_all<<<dim3(g.T / g.C, g.units), 160, 0, st>>>(g, io.theta, io.eta, io.alpha, coef,
+                                                              coef_layout_simt(g));
     cudaFuncSetAttribute(k_dual1_partials, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDual1PartSmem);
     k_dual1_partials<<<dim3(ks, g.units), 256, kDual1PartSmem, st>>>(g, ch, w, buf, part);
     *nl += 2;
