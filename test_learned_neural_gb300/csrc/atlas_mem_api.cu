@@ -302,13 +302,13 @@ static int run_generic(atlas_mem_handle* h, const Geom& g, const Work& w, const 
                 io->theta, io->eta, io->alpha, io->gamma, io->win_len ? io->win_gamma : nullptr, io->y};
   int buf = 0;
   if (dual1_tc_supported(g) && dual1_tc_inputs_ok(gio)) {
-    // depth 1 on the tensor cores: values, every chunk's gate coefficients,
-    // then one persistent launch that keeps the state on chip
-    CUDA_TRY(values_launch(g, w, gio, st));
+    // depth 1 on the tensor cores: every chunk's gate coefficients, then one
+    // persistent launch that keeps the state on chip (it reads the raw keys,
+    // queries, values and Omega weights itself)
     CUDA_TRY(dual1_coef_launch(g, gio, w.gpart, coef_layout_tc(g), st));
     buf = (g.T / g.C) & 1;
     CUDA_TRY(dual1_tc_launch(g, w, gio, w.gpart, buf, st));
-    nl += 3;
+    nl += 2;
   } else {
     CUDA_TRY(generic_prepare(g, w, gio, st, &nl));
     for (int s = 0; s < g.T; s += g.C) {

@@ -23,18 +23,22 @@
 // from the raw bf16 keys and queries; a product of two bf16 values (times
 // 1/2) has at most 16 significant bits, so its hi + lo split is exact.
 //
-// Per chunk, on each CTA:
+// Per chunk, on each CTA (12 warps; warp 0 issues the MMAs):
 //  1. generate the slice's R (C x FS) and window X (Kw x FS) tiles;
-//  2. tensor cores: [R W^ | R S^ | R X^T] (M = 64, N = 128 + Kw) and X W^
-//     (M = 128, N = 64), each as hi hi' + hi lo' + lo hi' (fp32 in TMEM);
+//  2. tensor cores: [R W^ | R S^] (M = 64, N = 128) and X W^ (M = 128,
+//     N = 64), each as hi hi' + hi lo' + lo hi' (fp32 in TMEM); meanwhile
+//     the owned rows of R X^T from the raw rows in closed form, the previous
+//     chunk's read-out, and the bulk copies of the next chunk's rows;
 //  3. the slice's partials go to their owners in the cluster (distributed
-//     shared memory): rows t of B_t RW + D_t RS and of R X^T, rows i of X W^;
+//     shared memory): rows t of B_t RW + D_t RS (owner t / YR), rows i of
+//     X W^ (owner i / XR);
 //  4. owners sum the NC slices in rank order, form dy rows (broadcast to
 //     every CTA) and M = Cw * (R X^T) rows;
 //  5. tensor cores: (cs_e dY)^T X, then (cw_e dY)^T X, for the chunk-end
-//     state, while the owners form y_t = Yp_t - (M dY)_t for their rows;
+//     state;
 //  6. S' = A_e S^ - .., W' = B_e W^ + D_e S^ - .. into the TMEM masters and
-//     the operand copies.
+//     the operand copies;
+// the owned rows' y_t = Yp_t - (M dY)_t follow in the next chunk's step 2.
 // Two cluster barriers per chunk order the exchanges.  Every mbarrier wait
 // is bounded; a wait that gives up sets the status word and the CTA keeps
 // the loop's barrier schedule without issuing further MMAs.
@@ -49,7 +53,7 @@ namespace {
 constexpr int NT = 384;                 // 12 warps: three per TMEM sub-partition
 constexpr int FSM = 96, KWM = 80;       // max features per CTA, max window rows (padded)
 constexpr int YS = 68;                  // row stride (floats) of the 64-wide exchange rows
-constexpr int RECF = 16000;             // floats of the receive buffer (all senders)
+constexpr int RECF = 16640;             // floats of the receive buffer (all senders)
 constexpr int OWN_CW = 880, OWN_ROWS = 16;   // owner prefetch: Cw entries, window rows
 constexpr long long kWait = 1ll << 31;
 
@@ -78,7 +82,7 @@ static_assert(OREC % 16 == 0 && ODYF % 16 == 0 && ORAW % 16 == 0 && OVEC % 16 ==
 // [kws], B_t [cp], D_t [cp], (A_e, B_e, D_e, 0)
 
 // TMEM columns
-constexpr uint32_t T_G1 = 0;     // [RW | RS | RX], M = 64 layout
+constexpr uint32_t T_G1 = 0;     // [RW | RS], M = 64 layout
 constexpr uint32_t T_XW = 224;   // X W^, M = 128 layout
 constexpr uint32_t T_D1 = 0, T_D2 = 96;        // state corrections (M = 64, transposed)
 constexpr uint32_t T_W = 288, T_S = 384;       // fp32 masters W^T, S^T (M = 64, transposed)
@@ -352,6 +356,7 @@ __device__ void rx_rows(const Geom& g, const P1& pp, int rank, const Chunk& ch, 
     float v[4] = {0.f, 0.f, 0.f, 0.f};
     if (t < g.C) {
       float dot[4] = {0.f, 0.f, 0.f, 0.f}, sq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
       for (int a = 0; a < g.d_k; ++a) {
         const float xq = tc::bf2f(xT[a * RT + t]);
         const uint2 kk = *reinterpret_cast<const uint2*>(xT + a * RT + 64 + i0);
@@ -392,6 +397,7 @@ __device__ void readout_rows(const Geom& g, const GenericIO& io, const P1& pp, i
       acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
       m[q] = mine + oRX + (live[q] ? r : 0) * (KWP + 4);
     }
+#pragma unroll 4
     for (int i = h * half; i < (h + 1) * half; ++i) {
       const float4 d = *reinterpret_cast<const float4*>(dyf + i * YS + j0);
 #pragma unroll
@@ -560,16 +566,15 @@ __global__ void __launch_bounds__(NT, 1) k_dual1_tc(Geom g, Work w, GenericIO io
         if (more) prefetch_chunk(g, io, coef, pp, u, n + 1, raw, vec, &bar_ch);
         prefetch_owner(g, io, coef, pp, u, n, (int)rank, ocw, og, ov, &bar_own);
       }
-      // warps 1-3 read out chunk n - 1, warps 5-7 and 9-11 form R X^T of
-      // chunk n; warps 4 (the copies' thread) and 8 leave the MMA warp's
-      // scheduler to it.  One CTA: R X^T goes where the read-out reads M,
-      // after it.
-      const int vt = (warp < 8 ? warp - 5 : warp - 6) * 32 + lane;
+      // warps 1-3 read out chunk n - 1, warps 5-11 form R X^T of chunk n
+      // (warp 4 issues the copies).  One CTA: R X^T goes where the read-out
+      // reads M, after it.
+      const int vt = (warp - 5) * 32 + lane;
       if (NC > 1) {
         if (warp < 4) {
           if (n > 0) readout_rows(g, io, pp, u, (int)rank, dual1_chunk_at(g, (n - 1) * C), mine, dyf, 32, 96);
-        } else if (warp != 4 && warp != 8) {
-          rx_rows(g, pp, (int)rank, ch, xT, rxb, vt, 192);
+        } else if (warp > 4) {
+          rx_rows(g, pp, (int)rank, ch, xT, rxb, vt, NT - 160);
         }
       } else {
         if (n > 0) readout_rows(g, io, pp, u, (int)rank, dual1_chunk_at(g, (n - 1) * C), mine, dyf, 32, NT - 32);
@@ -643,8 +648,8 @@ __global__ void __launch_bounds__(NT, 1) k_dual1_tc(Geom g, Work w, GenericIO io
         mine[oRX + r * (KWP + 4) + i] = cw * rxb[r * (KWP + 4) + i];
       }
       for (int e = tid; e < XR * 16; e += NT) {
-        const int r = e >> 4, j0 = (e & 15) * 4, i = (int)rank * XR + r;
-        if (i >= KWP) break;
+        const int r = e % XR, j0 = (e / XR) * 4, i = (int)rank * XR + r;
+        if (i >= KWP) continue;
         float d[4] = {0.f, 0.f, 0.f, 0.f};
         if (i < ch.nw) {
           float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
