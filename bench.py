@@ -146,13 +146,20 @@ def roofline_bound(w, flops, nbytes, peaks) -> str:
 def path_dtype(w) -> str:
     """Arithmetic type of the path a workload runs on: the fused MLP kernel
     multiplies bf16 operands (fp32 accumulation and state); the tensor-core
-    Newton-Schulz path multiplies split bf16 pairs (three products, about
-    fp32 accuracy); everything else is fp32."""
+    Newton-Schulz path and the tensor-core depth-1 (polynomial-feature)
+    kernel multiply split bf16 pairs (three products, about fp32 accuracy);
+    everything else is fp32."""
     fused = (w.depth == 2 and w.ns_iters == 0 and w.c == 1 and w.p == 1 and w.proj_dim == 0 and w.d_k == 64
              and w.d_v == 64 and w.hidden == 256 and w.C == 64)
     if fused:
         return "bf16"
     if w.ns_iters and getattr(w, "ns_target", "momentum") == "momentum" and w.depth == 2:
+        return "bf16x3"
+    depth1_tc = (w.depth == 1 and w.ns_iters == 0 and w.update == "per_token"
+                 and w.qkv_dtype == "bf16" and w.proj_dim == 0 and w.p in (1, 2) and w.d_k % 8 == 0
+                 and w.d_k <= 32 and w.d_v % 8 == 0 and w.d_v <= 64 and w.C <= 64 and w.C + w.c - 1 <= 80
+                 and w.feat_dim <= 768)
+    if depth1_tc:
         return "bf16x3"
     return "f32"
 
@@ -597,7 +604,7 @@ def run_prologue(args):
 
 # measured ms per forward on one GB300, to size the default step count
 APPROX_MS = {"atlas_muon": 1040, "atlas_long": 920, "atlas_muon_surprise": 122, "atlas_muon_chunkwise": 82,
-             "atlas_poly_c4": 5.1, "atlas_poly_c16": 5.2}
+             "atlas_poly_c4": 1.7, "atlas_poly_c16": 1.7}
 
 
 def default_steps(name: str) -> int:

@@ -19,7 +19,9 @@ def test_path_dtype_names_each_path():
     assert bench.path_dtype(WORKLOADS["titans_chunkwise"]) == "bf16"
     assert bench.path_dtype(WORKLOADS["atlas_muon"]) == "bf16x3"        # split-bf16 Newton-Schulz
     assert bench.path_dtype(WORKLOADS["atlas_long"]) == "bf16x3"
-    for name in ("linear_f32", "atlas_poly_c4", "atlas_poly_c16", "atlas_muon_surprise"):
+    for name in ("atlas_poly_c4", "atlas_poly_c16"):                     # split-bf16 depth-1 kernel
+        assert bench.path_dtype(WORKLOADS[name]) == "bf16x3", name
+    for name in ("linear_f32", "atlas_muon_surprise"):
         assert bench.path_dtype(WORKLOADS[name]) == "f32", name
 
 
@@ -57,7 +59,13 @@ def test_roofline_bound_from_intensity():
     fl = bench.algorithmic_flops_per_token(w) * w.tokens
     assert bench.roofline_bound(w, fl, bench.bytes_per_step(w), peaks) == "tensor"
     assert bench.roofline_bound(w, 1.0, 1e9, peaks) == "hbm"
-    assert bench.roofline_bound(WORKLOADS["atlas_poly_c4"], 1e12, 1.0, peaks) == "alu"   # fp32 SIMT path
+    assert bench.roofline_bound(WORKLOADS["linear_f32"], 1e12, 1.0, peaks) == "alu"   # fp32 SIMT path
+    # the polynomial workloads run the split-bf16 tensor-core kernel
+    wp = WORKLOADS["atlas_poly_c4"]
+    assert bench.path_dtype(wp) == "bf16x3"
+    fl = bench.algorithmic_flops_per_token(wp) * wp.tokens
+    assert bench.roofline_bound(wp, fl, bench.bytes_per_step(wp), peaks) == "tensor"
+    assert bench.path_dtype(wp.scaled(qkv_dtype="f32")) == "f32"
 
 
 def test_reference_sample_is_bounded():
