@@ -155,6 +155,18 @@ cudaError_t dual1_tc_launch(const Geom& g, const Work& w, const GenericIO& io, c
 
 // Newton-Schulz on the windowed surprise (k_surprise.cu)
 size_t surprise_floats(const Geom& g, size_t units);
+// offsets (floats) inside one unit's surprise scratch: the read-out's band of
+// Mw per token [nmat][C][Kw][2c-1] and Ms_e R, Mw_e R [nmat][2][Kw][maxcols]
+struct SurpOff {
+  size_t per_unit, mwb, rp;
+  int maxcols;
+};
+SurpOff surprise_offsets(const Geom& g);
+// the read-out and the chunk-end state of the surprise path on the tensor
+// cores (k_surprise_tc.cu)
+bool surprise_tc_supported(const Geom& g);
+cudaError_t surprise_tc_readout(const Geom& g, const Chunk& ch, const Work& w, int buf, float* y, cudaStream_t st);
+cudaError_t surprise_tc_state(const Geom& g, const Chunk& ch, const Work& w, int buf, cudaStream_t st);
 cudaError_t surprise_chunk(const Geom& g, const Chunk& ch, const Work& w, const float* theta, const float* eta,
                            const float* alpha, float* y, int buf, cudaStream_t st, int* nl);
 int num_sms();

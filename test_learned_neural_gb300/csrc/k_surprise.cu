@@ -382,12 +382,28 @@ __global__ void __launch_bounds__(256) k_surp_state(Geom g, Chunk ch, Work w, in
 
 size_t surprise_floats(const Geom& g, size_t units) { return units * surp_layout(g).per_unit; }
 
+SurpOff surprise_offsets(const Geom& g) {
+  const SurpLayout L = surp_layout(g);
+  return SurpOff{L.per_unit, L.mwb, L.rp, max_cols(g)};
+}
+
 cudaError_t surprise_chunk(const Geom& g, const Chunk& ch, const Work& w, const float* theta, const float* eta,
                            const float* alpha, float* y, int buf, cudaStream_t st, int* nl) {
   const int Ct = ch.e - ch.s, band = 2 * g.c - 1;
   k_surp_gram<<<dim3(ch.nw, g.nmat * 2, g.units), 256, 0, st>>>(g, ch, w);
   k_surp_ns<<<dim3(Ct, g.nmat, g.units), 256, 0, st>>>(g, ch, w);
   k_surp_scan<<<dim3((g.Kw * band + 255) / 256, g.nmat, g.units), 256, 0, st>>>(g, ch, w, theta, eta, alpha);
+  if (surprise_tc_supported(g)) {
+    // tensor cores: read-out in two launches (hidden read-out, output), the
+    // chunk-end state of both matrices in one
+    cudaError_t e = surprise_tc_readout(g, ch, w, buf, y, st);
+    if (e != cudaSuccess) return e;
+    k_surp_rprime<<<dim3(ch.nw, g.nmat * 2, g.units), 256, 0, st>>>(g, ch, w);
+    e = surprise_tc_state(g, ch, w, buf, st);
+    if (e != cudaSuccess) return e;
+    *nl += 7;
+    return cudaGetLastError();
+  }
   const size_t sr = (size_t)TG * (g.F + 2 * g.Kw + (g.depth == 2 ? g.hidden : 0)) * sizeof(float);
   cudaFuncSetAttribute(k_surp_readout, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sr);
   k_surp_readout<<<dim3((Ct + TG - 1) / TG, g.units), 256, sr, st>>>(g, ch, w, buf, y);
