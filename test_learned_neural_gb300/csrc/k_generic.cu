@@ -745,68 +745,84 @@ __global__ void __launch_bounds__(256) k_ns_scan_w2(Geom g, Chunk ch, Work w, in
                                                     const float* alpha, const float* aq, float* y) {
   // W2 decay scan fused with the output read-out.  Warp = output column k,
   // lane = CPL hidden entries; the U_t of PD tokens are loaded together and
-  // their PD warp reductions interleave.
-  constexpr int PD = 4;
-  extern __shared__ float aqs[];   // [Ct][h], then [Ct] 1 - alpha
+  // their PD warp reductions interleave.  The hidden read-outs are staged AW
+  // tokens at a time in two buffers (the next window loads during this one),
+  // which keeps the CTA at 66 KB of shared memory: more CTAs, and more U_t
+  // loads in flight, per SM.
+  constexpr int PD = 4, AW = 16;
+  extern __shared__ float aqs[];   // [2][AW][h], then [Ct] 1 - alpha
   const int u = blockIdx.y;
   const int lane = threadIdx.x % 32, k = blockIdx.x * 8 + threadIdx.x / 32;
   const int F = g.F, h = g.hidden, d = g.d_v;   // lane holds hidden columns lane + 32 q
   const int Ct = ch.e - ch.s;
   const bool pre = g.readout == ATLAS_READOUT_PRE;   // read out before token r's update
   const int rn = ns_first_row(g, ch);                 // slots before it hold no U_t: U_t = 0
-  float* bes = aqs + Ct * h;
-  {
-    // the chunk's hidden read-outs by 16-byte cp.async (h % 32 == 0, 16-byte
-    // aligned rows), all in flight at once
-    const float* src = aq + (size_t)u * g.C * h;
-    for (int e = 4 * threadIdx.x; e < Ct * h; e += 4 * 256) cp_async16(aqs + e, src + e);
+  float* bes = aqs + 2 * AW * h;
+  const float* aq_u = aq + (size_t)u * g.C * h;
+  // window wd's hidden read-outs by 16-byte cp.async (h % 32 == 0, 16-byte
+  // aligned rows), all in flight at once
+  auto stage = [&](int wd) {
+    const int r0w = wd * AW, nr = Ct - r0w < AW ? Ct - r0w : AW;
+    float* dst = aqs + (wd & 1) * AW * h;
+    for (int e = 4 * threadIdx.x; e < nr * h; e += 4 * 256) cp_async16(dst + e, aq_u + (size_t)r0w * h + e);
     cp_async_commit();
-  }
+  };
+  stage(0);
   for (int r = threadIdx.x; r < Ct; r += 256) bes[r] = 1.f - alpha[(size_t)u * g.T + ch.s + r];
   float W[CPL];
   const float* Wb = w.Wst[buf][1] + (size_t)u * h * d;   // original orientation [h][d]
 #pragma unroll
   for (int q = 0; q < CPL; ++q) W[q] = Wb[(size_t)(lane + 32 * q) * d + k];
-  cp_async_wait<0>();
-  __syncthreads();
   const float* slot0 = w.Ubuf + (size_t)u * g.C * slot_stride + (size_t)F * h + (size_t)k * h + lane;
-  for (int r0 = 0; r0 < Ct; r0 += PD) {
-    float cur[PD][CPL];
-#pragma unroll
-    for (int p = 0; p < PD; ++p) {
-      const float* sl = slot0 + (size_t)(r0 + p) * slot_stride;
-#pragma unroll
-      for (int q = 0; q < CPL; ++q) cur[p][q] = r0 + p < Ct && r0 + p >= rn ? sl[32 * q] : 0.f;
+  for (int wd = 0; wd * AW < Ct; ++wd) {
+    if ((wd + 1) * AW < Ct) {
+      stage(wd + 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
-    float acc[PD];
-#pragma unroll
-    for (int p = 0; p < PD; ++p) {
-      const int r = r0 + p < Ct ? r0 + p : Ct - 1;
-      const float be = bes[r];
-      float a = 0.f;
-#pragma unroll
-      for (int q = 0; q < CPL; ++q) {
-        if (r0 + p < Ct) {
-          if (pre) a += aqs[r * h + lane + 32 * q] * W[q];
-          W[q] = be * W[q] + cur[p][q];
-          if (!pre) a += aqs[r * h + lane + 32 * q] * W[q];
-        }
-      }
-      acc[p] = a;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-      for (int p = 0; p < PD; ++p) acc[p] += __shfl_xor_sync(0xffffffffu, acc[p], o);
-    if (lane == 0)
+    __syncthreads();
+    const float* aw = aqs + (wd & 1) * AW * h - (size_t)wd * AW * h;   // indexed by chunk row r
+    const int rend = (wd + 1) * AW < Ct ? (wd + 1) * AW : Ct;
+    for (int r0 = wd * AW; r0 < rend; r0 += PD) {
+      float cur[PD][CPL];
 #pragma unroll
       for (int p = 0; p < PD; ++p) {
-        const int r = r0 + p;
-        if (r < Ct) {
-          const size_t yi = ((size_t)u * g.T + ch.s + r) * d + k;
-          y[yi] = w.R[((size_t)u * g.T + ch.s + r) * F + k] + acc[p];
-        }
+        const float* sl = slot0 + (size_t)(r0 + p) * slot_stride;
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) cur[p][q] = r0 + p < rend && r0 + p >= rn ? sl[32 * q] : 0.f;
       }
+      float acc[PD];
+#pragma unroll
+      for (int p = 0; p < PD; ++p) {
+        const int r = r0 + p < rend ? r0 + p : rend - 1;
+        const float be = bes[r];
+        float a = 0.f;
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+          if (r0 + p < rend) {
+            if (pre) a += aw[r * h + lane + 32 * q] * W[q];
+            W[q] = be * W[q] + cur[p][q];
+            if (!pre) a += aw[r * h + lane + 32 * q] * W[q];
+          }
+        }
+        acc[p] = a;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int p = 0; p < PD; ++p) acc[p] += __shfl_xor_sync(0xffffffffu, acc[p], o);
+      if (lane == 0)
+#pragma unroll
+        for (int p = 0; p < PD; ++p) {
+          const int r = r0 + p;
+          if (r < rend) {
+            const size_t yi = ((size_t)u * g.T + ch.s + r) * d + k;
+            y[yi] = w.R[((size_t)u * g.T + ch.s + r) * F + k] + acc[p];
+          }
+        }
+    }
+    __syncthreads();   // this window's buffer may be restaged
   }
   float* Wo = w.Wst[buf ^ 1][1] + (size_t)u * h * d;
 #pragma unroll
@@ -836,7 +852,7 @@ cudaError_t ns_fused_scan(const Geom& g, const Chunk& ch, const Work& w, int buf
     cudaFuncSetAttribute(k_ns_scan_w1<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1);
     k_ns_scan_w1<16><<<g1, 256, sm1, st>>>(g, ch, w, buf, slot_stride, alpha, aq);
   }
-  const size_t sm2 = ((size_t)(ch.e - ch.s) * h + (ch.e - ch.s)) * sizeof(float);
+  const size_t sm2 = ((size_t)2 * 16 * h + (ch.e - ch.s)) * sizeof(float);   // two windows of 16 tokens
   dim3 g2(d / 8, g.units);
   if (h / 32 == 8) {
     cudaFuncSetAttribute(k_ns_scan_w2<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);
