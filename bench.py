@@ -161,6 +161,11 @@ def path_dtype(w) -> str:
                  and w.feat_dim <= 768)
     if depth1_tc:
         return "bf16x3"
+    surprise_tc = (w.depth == 2 and w.ns_iters > 0 and getattr(w, "ns_target", "momentum") == "surprise"
+                   and w.feat_dim % 16 == 0 and w.feat_dim <= 128 and w.feat_dim == w.d_v and w.hidden % 64 == 0
+                   and w.d_v % 32 == 0 and w.C <= 64 and w.C + w.c - 1 <= 80 and w.c <= 16)
+    if surprise_tc:   # the read-out's and the chunk-end state's products on the tensor cores
+        return "bf16x3"
     return "f32"
 
 

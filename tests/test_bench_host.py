@@ -21,8 +21,8 @@ def test_path_dtype_names_each_path():
     assert bench.path_dtype(WORKLOADS["atlas_long"]) == "bf16x3"
     for name in ("atlas_poly_c4", "atlas_poly_c16"):                     # split-bf16 depth-1 kernel
         assert bench.path_dtype(WORKLOADS[name]) == "bf16x3", name
-    for name in ("linear_f32", "atlas_muon_surprise"):
-        assert bench.path_dtype(WORKLOADS[name]) == "f32", name
+    assert bench.path_dtype(WORKLOADS["atlas_muon_surprise"]) == "bf16x3"   # tensor-core read-out and state
+    assert bench.path_dtype(WORKLOADS["linear_f32"]) == "f32"
 
 
 def test_chunkwise_work_is_below_the_per_token_work():
