@@ -178,7 +178,9 @@ def bytes_per_step(w) -> float:
 
 # sources of the kernel whose DRAM counters profiles/traffic.json records:
 # the record is used only while these files are unchanged
-TRAFFIC_SOURCES = {"titans_mlp": ("k_mlp_tc.cu", "tc.cuh", "atlas_common.cuh")}
+TRAFFIC_SOURCES = {"titans_mlp": ("k_mlp_tc.cu", "tc.cuh", "atlas_common.cuh"),
+                   "atlas_muon": ("k_ns_tc.cu", "tc.cuh", "atlas_common.cuh"),
+                   "atlas_poly_c4": ("k_dual1_tc.cu", "tc.cuh", "atlas_common.cuh")}
 
 
 def source_digest(files=None) -> str:
