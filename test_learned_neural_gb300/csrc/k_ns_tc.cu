@@ -403,19 +403,27 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
 // -> 128 MLP memory).  X in split bf16 (256 KB) does not fit one SM, so a
 // cluster of two CTAs shares each task: CTA p holds columns [256 p, 256 p +
 // 256) of X.  X X^T = sum of the two halves' Gram matrices.  Each partial is
-// symmetric, so a CTA sends the partner only rows 0-63 (32 KB fp32) and the
-// lower-right 64 x 64 block (16 KB): two bulk DSMEM copies that complete on
-// the partner's mbarrier.  The receiver reads block (1, 0) of the partner's
-// partial as the transpose of block (0, 1).  A^2 and B' are formed
-// redundantly by both; X <- B' X splits by columns with no exchange.
+// symmetric, so a CTA sends the partner only its unique entries: block
+// (0, 1) (16 KB fp32) and the two symmetric diagonal blocks' triangles
+// packed into one 64 x 65 block (16.25 KB), one bulk DSMEM copy that
+// completes on the partner's mbarrier (a copy between the two SMs moves
+// about 19 bytes per cycle, so the bytes set the exchange's cost).  The
+// receiver reads block (1, 0) as the transpose of block (0, 1) and the
+// other triangles by symmetry.  A^2 and B' are formed redundantly by both;
+// X <- B' X splits by columns with no exchange.
 namespace {
 
 constexpr int R2 = 128, NH = 256, NT2 = 256;
 constexpr int OPR2 = 131072;                    // factors (120 KB) / X hi+lo (128 KB)
 constexpr int AB2 = 65536;                      // A / B' hi+lo; receives the partner's partial
-constexpr int STG2 = OPR2 + AB2;                // 32 KB staging of this CTA's rows 0-63
-constexpr int SMEM2 = STG2 + 32768;
-constexpr uint32_t kPartBytes = 64 * R2 * 4 + 64 * 64 * 4;   // rows 0-63 + block (1, 1)
+constexpr int STG2 = OPR2 + AB2;                // staging of this CTA's packed partial
+constexpr int kQS = 65;                          // row stride of the packed diagonal blocks
+// block (0, 1) [64][64] (16-byte chunks swizzled by xswz64), then Q
+// [64][65]: row i holds P00[i][0..i] at columns 0..i and P11[i][i..63] at
+// columns i+1..64 (65 = 1 mod 32: a row read and a column read of Q by 32
+// consecutive rows both hit 32 banks)
+constexpr uint32_t kPartBytes = 64 * 64 * 4 + 64 * kQS * 4;
+constexpr int SMEM2 = STG2 + (int)kPartBytes;
 
 __device__ __forceinline__ uint32_t cluster_rank2() {
   uint32_t r;
@@ -449,10 +457,9 @@ __device__ __forceinline__ void mbar_arm_tx2(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(bytes)
                : "memory");
 }
-// fp32 row-major exchange blocks with the 16-byte chunks of row r XOR-ed by
+// fp32 row-major exchange block with the 16-byte chunks of row r XOR-ed by
 // r % 8: a warp touching one chunk of 32 consecutive rows hits every bank
-// (unswizzled, rows 512 or 256 bytes apart all start in the same bank)
-__device__ __forceinline__ int xswz128(int r, int c) { return r * 128 + ((((c >> 2) ^ (r & 7)) << 2) | (c & 3)); }
+// (unswizzled, rows 256 bytes apart all start in the same bank)
 __device__ __forceinline__ int xswz64(int r, int c) { return r * 64 + ((((c >> 2) ^ (r & 7)) << 2) | (c & 3)); }
 // one arrival on the partner's mbarrier (cluster address)
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
@@ -507,15 +514,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
   __syncthreads();
   tc::fence_after_sync();
   cluster_sync2();   // both CTAs' exchange barriers are initialised
+  // One arrival on the partner's xfree per exchange, as soon as this CTA's
+  // A/B' buffer is free for it: after each token's momentum product (its
+  // factors may reach into the buffer) and after every B'X product but a
+  // token's last.
+  const uint32_t xfree_peer = mapa2(tc::smem_u32(&xfree), p ^ 1u);
   // TMEM: the B'X product and, before it, A = X X^T and A^2 in its two
   // halves (each consumed before the next product writes there); the
   // running momentum of the current (unit, matrix) in the other 256 columns
   const uint32_t tX = tbase, tA = tbase, tA2 = tbase + 128, tS = tbase + 256;
   PairCtx cx{&bar, 0u, true};
   uint32_t xe = 0;   // exchanges so far (phase parity of xdata and xfree)
-  float* stg = reinterpret_cast<float*>(sm + STG2);                 // [64][128] fp32
-  float* recv = reinterpret_cast<float*>(sm + OPR2);                // partner's rows 0-63, then block (1, 1)
-  float* stg11 = reinterpret_cast<float*>(sm + OPR2 + kPartBytes);  // this CTA's block (1, 1) [64][64]
+  float* stg = reinterpret_cast<float*>(sm + STG2);    // this CTA's packed partial
+  float* recv = reinterpret_cast<float*>(sm + OPR2);   // the partner's (inside the A/B' buffer)
 
   const int lxb = R2 * Kp * 2, rxb = Kp * NH * 2;
   uint8_t* lx_hi = sm;
@@ -675,6 +686,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
       if (threadIdx.x == 0 && cx.ok) mma_x3_acc(tS, lw_hi, lw_lo, rgsKW, rw_hi, rw_lo, rgsN, 1, R2, NH, KW);
       pair_commit_wait(cx);
     }
+    // the momentum product is done: the partner may send this token's first exchange
+    if (threadIdx.x == 0 && cx.ok) mbar_arrive_remote(xfree_peer);
     cur_um = u * g.nmat + m;
     cur_r = r;
     // (c) ||S_t||_F = lam ||Shat|| over both halves; chunk-end S
@@ -732,58 +745,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
       tc::tmem_ld16(tA + lane_base + 64 * half + 32, af + 32);
       tc::tmem_ld16(tA + lane_base + 64 * half + 48, af + 48);
       tc::tmem_ld_wait();
-      // exchange: this CTA's A/B' buffer is free (its B'X product is done);
-      // tell the partner, and wait until the partner's is free too
+      // stage this CTA's packed partial (row < 64 with half 1 holds block
+      // (0, 1); half 0 the lower triangle of block (0, 0); rows >= 64 with
+      // half 1 the upper triangle of block (1, 1); block (1, 0) is not sent)
+      {
+        float* q = stg + 64 * 64;
+        const int r1 = row & 63;
+        if (row < 64 && half == 1) {
+#pragma unroll
+          for (int q4 = 0; q4 < 16; ++q4)
+            *reinterpret_cast<float4*>(stg + xswz64(row, 4 * q4)) =
+                make_float4(af[4 * q4], af[4 * q4 + 1], af[4 * q4 + 2], af[4 * q4 + 3]);
+        } else if (row < 64) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (j <= r1) q[r1 * kQS + j] = af[j];
+        } else if (half == 1) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (j >= r1) q[r1 * kQS + j + 1] = af[j];
+        }
+      }
+      tc::fence_smem_to_async();   // staging is the bulk copy's source
+      __syncthreads();
+      // one copy once the partner's A/B' buffer is free (it arrives on
+      // xfree when its B'X product is done)
       bool good = true;
       if (threadIdx.x == 0 && cx.ok) {
-        mbar_arrive_remote(mapa2(tc::smem_u32(&xfree), p ^ 1u));
         good = tc::mbar_wait(&xfree, xe & 1, kWaitCycles);
-      }
-      // stage rows 0-63 and block (1, 1) of this CTA's partial
-      if (row < 64) {
-#pragma unroll
-        for (int q4 = 0; q4 < 16; ++q4)
-          *reinterpret_cast<float4*>(stg + xswz128(row, 64 * half + 4 * q4)) =
-              make_float4(af[4 * q4], af[4 * q4 + 1], af[4 * q4 + 2], af[4 * q4 + 3]);
-      } else if (half == 1) {
-#pragma unroll
-        for (int q4 = 0; q4 < 16; ++q4)
-          *reinterpret_cast<float4*>(stg11 + xswz64(row - 64, 4 * q4)) =
-              make_float4(af[4 * q4], af[4 * q4 + 1], af[4 * q4 + 2], af[4 * q4 + 3]);
-      }
-      tc::fence_smem_to_async();   // staging is the bulk copies' source
-      if (__syncthreads_or(!good)) cx.ok = false;
-      good = true;
-      if (threadIdx.x == 0 && cx.ok) {
-        const uint32_t xb = mapa2(tc::smem_u32(&xdata), p ^ 1u);
-        const uint32_t rv = tc::smem_u32(recv);
-        bulk_to_partner(mapa2(rv, p ^ 1u), tc::smem_u32(stg), 64 * R2 * 4, xb);
-        bulk_to_partner(mapa2(rv + 64 * R2 * 4, p ^ 1u), tc::smem_u32(stg11), 64 * 64 * 4, xb);
-        good = tc::mbar_wait(&xdata, xe & 1, kWaitCycles);
-        if (good) mbar_arm_tx2(&xdata, kPartBytes);   // the next exchange
-        bulk_wait_read2();   // staging read: the buffer below may be rewritten
+        if (good) {
+          const uint32_t xb = mapa2(tc::smem_u32(&xdata), p ^ 1u);
+          bulk_to_partner(mapa2(tc::smem_u32(recv), p ^ 1u), tc::smem_u32(stg), kPartBytes, xb);
+          good = tc::mbar_wait(&xdata, xe & 1, kWaitCycles);
+          if (good) mbar_arm_tx2(&xdata, kPartBytes);   // the next exchange
+          bulk_wait_read2();   // staging read: it may be rewritten
+        }
       }
       ++xe;
       if (__syncthreads_or(!good)) cx.ok = false;
       {
         // partner's entries of my row, columns [64 half, 64 half + 64)
-        if (row < 64) {
+        const float* rq = recv + 64 * 64;
+        const int r1 = row & 63;
+        if (row < 64 && half == 1) {
 #pragma unroll
           for (int q4 = 0; q4 < 16; ++q4) {
-            const float4 o = *reinterpret_cast<const float4*>(recv + xswz128(row, 64 * half + 4 * q4));
+            const float4 o = *reinterpret_cast<const float4*>(recv + xswz64(row, 4 * q4));
             af[4 * q4] += o.x; af[4 * q4 + 1] += o.y; af[4 * q4 + 2] += o.z; af[4 * q4 + 3] += o.w;
           }
-        } else if (half == 1) {
-          const float* th = recv + 64 * R2;
+        } else if (row < 64) {
+          // block (0, 0): the stored triangle up to the diagonal, the rest
+          // from the rows below it (P00[r][j] = P00[j][r])
 #pragma unroll
-          for (int q4 = 0; q4 < 16; ++q4) {
-            const float4 o = *reinterpret_cast<const float4*>(th + xswz64(row - 64, 4 * q4));
-            af[4 * q4] += o.x; af[4 * q4 + 1] += o.y; af[4 * q4 + 2] += o.z; af[4 * q4 + 3] += o.w;
-          }
+          for (int j = 0; j < 64; ++j) af[j] += rq[j <= r1 ? r1 * kQS + j : j * kQS + r1];
+        } else if (half == 0) {
+          // block (1, 0): the transpose of block (0, 1)
+#pragma unroll
+          for (int j = 0; j < 64; ++j) af[j] += recv[xswz64(j, r1)];
         } else {
-          // block (1, 0): the partner's P[row][c] = P[c][row], c < 64
+          // block (1, 1): the stored triangle from the diagonal on, the rest
+          // from the rows above it (P11[r][j] = P11[j][r])
 #pragma unroll
-          for (int c = 0; c < 64; ++c) af[c] += recv[xswz128(c, row)];
+          for (int j = 0; j < 64; ++j) af[j] += rq[j >= r1 ? r1 * kQS + j + 1 : j * kQS + r1 + 1];
         }
       }
       __syncthreads();   // every received entry read before the buffer takes A hi/lo
@@ -809,6 +832,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
       if (threadIdx.x == 0 && cx.ok) mma_x3(tX, a_hi, a_lo, rgsR, x_hi, x_lo, rgsN, 1, R2, NH, R2);
       pair_commit_wait(cx);
       const bool last = (it == g.ns_iters - 1);
+      // B' is consumed: the partner may send the next exchange
+      if (!last && threadIdx.x == 0 && cx.ok) mbar_arrive_remote(xfree_peer);
       for (int c32 = 32 * half; c32 < NH; c32 += 64) {
         float v[32];
         tc::tmem_ld16(tX + lane_base + c32, v);
