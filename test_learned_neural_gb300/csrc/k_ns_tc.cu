@@ -424,6 +424,10 @@ constexpr int kQS = 65;                          // row stride of the packed dia
 // consecutive rows both hit 32 banks)
 constexpr uint32_t kPartBytes = 64 * 64 * 4 + 64 * kQS * 4;
 constexpr int SMEM2 = STG2 + (int)kPartBytes;
+// fp32 staging of the U rows: row stride 260 floats (1040 bytes = 16 mod
+// 128, so the same 16-byte chunk of 8 consecutive rows hits 8 bank groups)
+constexpr int kUS = 260;
+static_assert(R2 * kUS * 4 <= STG2, "U staging fits the X and A/B' buffers");
 
 __device__ __forceinline__ uint32_t cluster_rank2() {
   uint32_t r;
@@ -449,6 +453,11 @@ __device__ __forceinline__ void bulk_to_partner(uint32_t dst, uint32_t src, uint
   asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "r"(src), "r"(bytes), "r"(mbar)
                : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// bulk copy of local shared memory to global memory (both 16-byte aligned)
+__device__ __forceinline__ void bulk_to_global(float* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes) : "memory");
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_read2() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
@@ -834,13 +843,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
       const bool last = (it == g.ns_iters - 1);
       // B' is consumed: the partner may send the next exchange
       if (!last && threadIdx.x == 0 && cx.ok) mbar_arrive_remote(xfree_peer);
+      // U rows go out through shared memory, one bulk copy per row (a
+      // thread's own row stored straight to global memory would touch 32
+      // lines per warp store); the staging spans the X and A/B' buffers,
+      // which nothing touches until this CTA's next momentum product
+      float* ust = reinterpret_cast<float*>(sm);
       for (int c32 = 32 * half; c32 < NH; c32 += 64) {
         float v[32];
         tc::tmem_ld16(tX + lane_base + c32, v);
         tc::tmem_ld16(tX + lane_base + c32 + 16, v + 16);
         tc::tmem_ld_wait();
         if (last) {
-          float4* o = reinterpret_cast<float4*>(slot + (size_t)row * n + p * NH + c32);
+          float4* o = reinterpret_cast<float4*>(ust + row * kUS + c32);
 #pragma unroll
           for (int q = 0; q < 8; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         } else {
@@ -848,10 +862,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
           for (int q8 = 0; q8 < 4; ++q8) store_split16(x_hi, x_lo, tc::core_offset(row, c32 + 8 * q8, rgsN), v + 8 * q8);
         }
       }
+      if (last) {
+        tc::fence_smem_to_async();
+        __syncthreads();
+        if (threadIdx.x < R2 && cx.ok) {
+          bulk_to_global(slot + (size_t)threadIdx.x * n + p * NH, tc::smem_u32(ust + threadIdx.x * kUS), NH * 4);
+          bulk_wait_read2();   // the staging is rewritten by the next token
+        }
+      }
       sync_for_mma();
     }
   }
-  if (threadIdx.x == 0) bulk_wait_all2();
+  if (threadIdx.x < R2) bulk_wait_all2();   // the exchange copies and the U rows
   if (!cx.ok && threadIdx.x == 0) atomicExch(w.status, ATLAS_ERR_TIMEOUT);
   tc::fence_before_sync();
   __syncthreads();
