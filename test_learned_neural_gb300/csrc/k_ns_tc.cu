@@ -374,13 +374,17 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
       }
       if (!(ok = wait_all(&bar, phase))) break;
       const bool last = (it == g.ns_iters - 1);
+      // U rows go out through shared memory (row stride n + 4 floats over
+      // the X and A buffers, free once B'X is done), one bulk copy per row
+      float* ust = reinterpret_cast<float*>(sm + L.x);
+      const int us = n + 4;
       for (int c32 = 32 * half; c32 < n; c32 += 64) {
         float v[16];
         const int cc = c32 + csub;
         tc::tmem_ld16_x2(tX + lane_base + c32, v);
         tc::tmem_ld_wait();
         if (last) {
-          float4* o = reinterpret_cast<float4*>(slot + (size_t)row * n + cc);
+          float4* o = reinterpret_cast<float4*>(ust + row * us + cc);
 #pragma unroll
           for (int q = 0; q < 4; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         } else {
@@ -388,10 +392,24 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
           store_split16(x_hi, x_lo, tc::core_offset(row, cc + 8, rgsN), v + 8);
         }
       }
+      if (last) {
+        tc::fence_smem_to_async();
+        __syncthreads();
+        if (threadIdx.x < R) {
+          const float* src = ust + threadIdx.x * us;
+          float* dst = slot + (size_t)threadIdx.x * n;
+          asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(tc::smem_u32(src)),
+                       "r"(n * 4)
+                       : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // the staging is rewritten by the next token
+        }
+      }
       sync_for_mma();
     }
     if (!ok) break;
   }
+  if (threadIdx.x < R) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // the U rows
   if (!ok && threadIdx.x == 0) atomicExch(w.status, ATLAS_ERR_TIMEOUT);
   tc::fence_before_sync();
   __syncthreads();
