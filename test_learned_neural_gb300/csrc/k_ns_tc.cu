@@ -455,11 +455,6 @@ __device__ __forceinline__ uint32_t cluster_rank2() {
 __device__ __forceinline__ void cluster_sync2() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ float ld_cluster_f(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-  return v;
-}
 __device__ __forceinline__ uint32_t mapa2(uint32_t saddr, uint32_t cta) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(cta));
@@ -520,7 +515,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
   __shared__ uint64_t bar;
   __shared__ uint32_t tbase;
   __shared__ float red[NT2 / 32];
-  __shared__ float ss_cta;
   const uint32_t p = cluster_rank2();
   const int cl = blockIdx.x / 2, ncl = gridDim.x / 2;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -717,8 +711,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
     if (threadIdx.x == 0 && cx.ok) mbar_arrive_remote(xfree_peer);
     cur_um = u * g.nmat + m;
     cur_r = r;
-    // (c) ||S_t||_F = lam ||Shat|| over both halves; chunk-end S
-    float ss = 0.f;
+    // (c) Shat itself, unscaled, in split bf16 as this CTA's half of X, and
+    // the chunk-end S = lam Shat.  X_0 = s Shat with s = lam / (lam
+    // ||Shat||_F + eps); ||Shat||^2 is the trace of Shat Shat^T, i.e. of the
+    // first iteration's A before scaling, so s is applied there (A = s^2
+    // Shat Shat^T, X_1 = s B' Shat) and needs no pass or exchange of its own.
     const bool last_tok = (t == ch.e - 1);
     float* So = w.Sst[buf ^ 1][m] + (size_t)u * nel;
     for (int c32 = 32 * half; c32 < NH; c32 += 64) {
@@ -726,40 +723,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
       tc::tmem_ld16(tS + lane_base + c32, d);
       tc::tmem_ld16(tS + lane_base + c32 + 16, d + 16);
       tc::tmem_ld_wait();
+      if (last_tok) {
 #pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) {
-        const float* o = d + 4 * q4;
-        ss += o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
-        if (last_tok)
+        for (int q4 = 0; q4 < 8; ++q4)
           *reinterpret_cast<float4*>(So + (size_t)row * n + p * NH + c32 + 4 * q4) =
-              make_float4(lam * o[0], lam * o[1], lam * o[2], lam * o[3]);
+              make_float4(lam * d[4 * q4], lam * d[4 * q4 + 1], lam * d[4 * q4 + 2], lam * d[4 * q4 + 3]);
       }
-    }
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float tot = 0.f;
-      for (int k2 = 0; k2 < NT2 / 32; ++k2) tot += red[k2];
-      ss_cta = tot;
-    }
-    cluster_sync2();
-    const float tot = ss_cta + ld_cluster_f(mapa2(tc::smem_u32(&ss_cta), p ^ 1u));
-    // X_0 = S_t / (||S_t|| + eps) = Shat * lam / (lam ||Shat|| + eps)
-    const float scale = lam / (lam * sqrtf(tot) + kNsEps);
-    // (d) X_0 -> split bf16 into this CTA's half of X
-    for (int c32 = 32 * half; c32 < NH; c32 += 64) {
-      float d[32];
-      tc::tmem_ld16(tS + lane_base + c32, d);
-      tc::tmem_ld16(tS + lane_base + c32 + 16, d + 16);
-      tc::tmem_ld_wait();
-#pragma unroll
-      for (int q = 0; q < 32; ++q) d[q] *= scale;
 #pragma unroll
       for (int q8 = 0; q8 < 4; ++q8) store_split16(x_hi, x_lo, tc::core_offset(row, c32 + 8 * q8, rgsN), d + 8 * q8);
     }
-    cluster_sync2();   // both CTAs read ss_cta above before the next task rewrites it
     sync_for_mma();
+    float scale = 1.f;   // s, from the first iteration's A
     float* slot = w.Ubuf + ((size_t)u * g.C + r) * slot_stride;
     for (int mm = 0; mm < m; ++mm) slot += (size_t)g.rows[mm] * g.cols[mm];
     for (int it = 0; it < g.ns_iters; ++it) {
@@ -836,7 +810,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
           for (int j = 0; j < 64; ++j) af[j] += rq[j >= r1 ? r1 * kQS + j + 1 : j * kQS + r1 + 1];
         }
       }
+      if (it == 0) {
+        // this thread's diagonal entry of A (if its columns hold one), summed
+        // over the CTA: trace(A) = ||Shat||^2 (both CTAs hold the same
+        // diagonal, so both get the same s)
+        const int jd = row - 64 * half;
+        float dg = 0.f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) dg = (j == jd) ? af[j] : dg;
+        for (int o = 16; o > 0; o >>= 1) dg += __shfl_xor_sync(0xffffffffu, dg, o);
+        if (lane == 0) red[warp] = dg;
+      }
       __syncthreads();   // every received entry read before the buffer takes A hi/lo
+      if (it == 0) {
+        float tot = 0.f;
+        for (int k2 = 0; k2 < NT2 / 32; ++k2) tot += red[k2];
+        scale = lam / (lam * sqrtf(tot) + kNsEps);
+        const float s2 = scale * scale;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) af[j] *= s2;
+      }
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) store_split16(a_hi, a_lo, tc::core_offset(row, 64 * half + 8 * q8, rgsR), af + 8 * q8);
       sync_for_mma();
@@ -871,6 +864,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
         tc::tmem_ld16(tX + lane_base + c32, v);
         tc::tmem_ld16(tX + lane_base + c32 + 16, v + 16);
         tc::tmem_ld_wait();
+        if (it == 0) {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) v[q] *= scale;   // X_1 = s B' Shat
+        }
         if (last) {
           float4* o = reinterpret_cast<float4*>(ust + row * kUS + c32);
 #pragma unroll
