@@ -660,7 +660,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
       // (theta_t / lam_t) sum_{i in window(t)} Lf_i^T Rf_i (window rows
       // w0 .. t - lo of the chunk's factors; K = 16 padded with zeros)
       const size_t gi = (size_t)u * g.T + t;
-      lam *= __ldg(eta + gi);
+      const int wt = t - ch.lo;                               // window row of token t
+      const int w0 = (t - g.c + 1 > ch.lo ? t - g.c + 1 : ch.lo) - ch.lo;
+      // every global read of this step is issued first (one round trip):
+      // eta_t, theta_t, this thread's 8 short-side values (column a, rows
+      // i0 .. i0 + 7 of the window) and 2 x 8 long-side values
+      static_assert(R2 * (KW / 8) == NT2 && KW * (NH / 8) == 2 * NT2, "one / two staging items per thread");
+      const float eta_t = __ldg(eta + gi), theta_t = __ldg(theta + gi);
+      const int la = threadIdx.x % R2, li0 = (threadIdx.x / R2) * 8;
+      float lv[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int i = w0 + li0 + q;
+        lv[q] = (i <= wt) ? Lf[(size_t)i * lstride + la] : 0.f;
+      }
+      float4 rv[4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = threadIdx.x + h * NT2, i = w0 + e / (NH / 8), b0 = (e % (NH / 8)) * 8;
+        if (i <= wt) {
+          const float* src = Rf + (size_t)i * rstride + p * NH + b0;
+          rv[2 * h] = *reinterpret_cast<const float4*>(src);
+          rv[2 * h + 1] = *reinterpret_cast<const float4*>(src + 4);
+        } else {
+          rv[2 * h] = rv[2 * h + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      lam *= eta_t;
       if (!(lam > 1e-6f)) {
         // renormalise: Shat <- lam Shat, lam <- 1 (keeps theta / lam finite)
         for (int c32 = 32 * half; c32 < NH; c32 += 64) {
@@ -676,31 +702,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT2, 1)
         tc::tmem_st_wait();
         lam = 1.f;
       }
-      const float coef = -__ldg(theta + gi) / lam;
-      const int wt = t - ch.lo;                               // window row of token t
-      const int w0 = (t - g.c + 1 > ch.lo ? t - g.c + 1 : ch.lo) - ch.lo;
-      for (int e = threadIdx.x; e < R2 * (KW / 8); e += NT2) {
-        const int a = e % R2, i0 = (e / R2) * 8;
-        float v[8];
+      const float coef = -theta_t / lam;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int i = w0 + i0 + q;
-          v[q] = (i <= wt) ? coef * Lf[(size_t)i * lstride + a] : 0.f;
-        }
-        store_split16(lw_hi, lw_lo, tc::core_offset(a, i0, rgsKW), v);
-      }
-      for (int e = threadIdx.x; e < KW * (NH / 8); e += NT2) {
-        const int k = e / (NH / 8), b0 = (e % (NH / 8)) * 8, i = w0 + k;
-        float v[8];
-        if (i <= wt) {
-          const float* src = Rf + (size_t)i * rstride + p * NH + b0;
-          const float4 r0 = *reinterpret_cast<const float4*>(src);
-          const float4 r1 = *reinterpret_cast<const float4*>(src + 4);
-          v[0] = r0.x; v[1] = r0.y; v[2] = r0.z; v[3] = r0.w; v[4] = r1.x; v[5] = r1.y; v[6] = r1.z; v[7] = r1.w;
-        } else {
+      for (int q = 0; q < 8; ++q) lv[q] *= coef;
+      store_split16(lw_hi, lw_lo, tc::core_offset(la, li0, rgsKW), lv);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) v[q] = 0.f;
-        }
+      for (int h = 0; h < 2; ++h) {
+        const int e = threadIdx.x + h * NT2, k = e / (NH / 8), b0 = (e % (NH / 8)) * 8;
+        const float v[8] = {rv[2 * h].x, rv[2 * h].y, rv[2 * h].z, rv[2 * h].w,
+                            rv[2 * h + 1].x, rv[2 * h + 1].y, rv[2 * h + 1].z, rv[2 * h + 1].w};
         store_split16(rw_hi, rw_lo, tc::core_offset(k, b0, rgsN), v);
       }
       sync_for_mma();
