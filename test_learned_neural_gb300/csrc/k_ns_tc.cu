@@ -278,7 +278,9 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
       tc::mma_commit(&bar);
     }
     if (!(ok = wait_all(&bar, phase))) break;
-    // (c) S = A_t Sbar - D, kept in TMEM over D; sum of squares; chunk-end S
+    // (c) S = A_t Sbar - D, straight into X in split bf16 (unscaled); sum of
+    // squares; chunk-end S.  X_0 = s S with s = 1 / (||S||_F + eps) is
+    // applied inside the first iteration (A = s^2 S S^T, X_1 = s B' S).
     float ss = 0.f;
     const bool last_tok = (t == ch.e - 1);
     float* So = w.Sst[buf ^ 1][m] + (size_t)u * nel;
@@ -296,29 +298,16 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
         ss += o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
         if (last_tok) *reinterpret_cast<float4*>(So + (size_t)row * n + c32 + csub + 4 * q4) = make_float4(o[0], o[1], o[2], o[3]);
       }
-      tc::tmem_st16_x2(tX + lane_base + c32, d);
+      store_split16(x_hi, x_lo, tc::core_offset(row, c32 + csub, rgsN), d);
+      store_split16(x_hi, x_lo, tc::core_offset(row, c32 + csub + 8, rgsN), d + 8);
     }
-    tc::tmem_st_wait();
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (lane == 0) red[warp] = ss;
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
+    sync_for_mma();
     float tot = 0.f;
 #pragma unroll
     for (int k2 = 0; k2 < NT / 32; ++k2) tot += red[k2];
     const float scale = 1.f / (sqrtf(tot) + kNsEps);
-    // (d) X_0 = S * scale -> split bf16
-    for (int c32 = 32 * half; c32 < n; c32 += 64) {
-      float d[16];
-      tc::tmem_ld16_x2(tX + lane_base + c32, d);
-      tc::tmem_ld_wait();
-#pragma unroll
-      for (int q = 0; q < 16; ++q) d[q] *= scale;
-      store_split16(x_hi, x_lo, tc::core_offset(row, c32 + csub, rgsN), d);
-      store_split16(x_hi, x_lo, tc::core_offset(row, c32 + csub + 8, rgsN), d + 8);
-    }
-    sync_for_mma();
 
     float* slot = w.Ubuf + ((size_t)u * g.C + r) * slot_stride;
     for (int mm = 0; mm < m; ++mm) slot += (size_t)g.rows[mm] * g.cols[mm];
@@ -340,6 +329,10 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
         __syncthreads();
 #pragma unroll
         for (int q = 0; q < 16; ++q) av[q] = p[q] + qv[q] + qt[(c + q) * (R + 1) + row];
+        if (it == 0) {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) av[q] *= scale * scale;
+        }
         store_split16(a_hi, a_lo, tc::core_offset(row, c, rgsR), av);
         store_split16(a_hi, a_lo, tc::core_offset(row, c + 8, rgsR), av + 8);
       }
@@ -383,6 +376,10 @@ __global__ void __launch_bounds__(NT, 1) k_ns_tc64(Geom g, Chunk ch, Work w, int
         const int cc = c32 + csub;
         tc::tmem_ld16_x2(tX + lane_base + c32, v);
         tc::tmem_ld_wait();
+        if (it == 0) {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) v[q] *= scale;   // X_1 = s B' S
+        }
         if (last) {
           float4* o = reinterpret_cast<float4*>(ust + row * us + cc);
 #pragma unroll
