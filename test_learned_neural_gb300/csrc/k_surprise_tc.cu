@@ -88,20 +88,41 @@ __device__ __forceinline__ void tmem_rows64_to_smem(uint32_t taddr_col, int kwp,
   }
 }
 
+// n floats from global src to shared dst + mis by asynchronous copies, all
+// in flight at once (16-byte copies where both sides allow it); mis = src's
+// float offset inside its 16-byte chunk, so dst + mis shares src's
+// alignment.  Returns mis once every copy has landed (this thread's).
+__device__ __forceinline__ int stage_async(float* dst, const float* src, int n) {
+  const int mis = (int)((reinterpret_cast<uintptr_t>(src) >> 2) & 3);
+  const int head = mis ? (4 - mis < n ? 4 - mis : n) : 0;   // floats before src's first 16-byte boundary
+  const int nb = (n - head) / 4;                            // 16-byte chunks after them
+  float* d = dst + mis;
+  if (threadIdx.x < head)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc::smem_u32(d + threadIdx.x)), "l"(src + threadIdx.x)
+                 : "memory");
+  for (int b = threadIdx.x; b < nb; b += NT)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(d + head + 4 * b)),
+                 "l"(src + head + 4 * b)
+                 : "memory");
+  for (int e = head + 4 * nb + threadIdx.x; e < n; e += NT)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc::smem_u32(d + e)), "l"(src + e) : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  return mis;
+}
+
 // G2[t][j] = sum_i G[t][i] Mw_t[i][j] over the band |i - j| < c, split into
 // the K-major A tile [t][j] (rgs); rows t >= Ct and columns j >= nw are zero.
 // The tokens' band matrices (contiguous in global memory) are staged in
 // groups of tokens through `stage` (cap floats, at least one token's Kw (2c -
-// 1)) with coalesced loads, so the sums read shared memory.
+// 1) + 3) by asynchronous copies, so the sums read shared memory.
 __device__ __forceinline__ void band_mix(const Geom& g, const Chunk& ch, const float* gf, int kwp, const float* mw,
                                          float* stage, int cap, uint8_t* hi, uint8_t* lo, int rgs) {
   const int Ct = ch.e - ch.s, band = 2 * g.c - 1, nq = kwp / 8, per = g.Kw * band;
-  const int MWG = cap / per < 64 ? cap / per : 64;
+  const int MWG = (cap - 3) / per < 64 ? (cap - 3) / per : 64;
   for (int t0 = 0; t0 < 64; t0 += MWG) {
     const int nt = Ct - t0 < MWG ? (Ct - t0 > 0 ? Ct - t0 : 0) : MWG;
-    const float* src = mw + (size_t)t0 * per;
-#pragma unroll 4
-    for (int e = threadIdx.x; e < nt * per; e += NT) stage[e] = src[e];
+    const int mis = stage_async(stage, mw + (size_t)t0 * per, nt * per);
     __syncthreads();
     for (int e = threadIdx.x; e < MWG * nq; e += NT) {
       const int tt = e % MWG, t = t0 + tt, j0 = (e / MWG) * 8;
@@ -113,7 +134,7 @@ __device__ __forceinline__ void band_mix(const Geom& g, const Chunk& ch, const f
         float acc = 0.f;
         if (tt < nt && j < ch.nw) {
           const int i0 = j - g.c + 1 > 0 ? j - g.c + 1 : 0, i1 = j + g.c - 1 < ch.nw - 1 ? j + g.c - 1 : ch.nw - 1;
-          const float* M = stage + tt * per;
+          const float* M = stage + mis + tt * per;
           for (int i = i0; i <= i1; ++i) acc += gf[t * (kwp + 4) + i] * M[i * band + (j - i + g.c - 1)];
         }
         v[k] = acc;
@@ -134,7 +155,7 @@ constexpr int AZ_R = 0, AZ_X = AZ_R + 2 * 64 * FZ * 2, AZ_WS = AZ_X + 2 * KWM * 
               SMEM_Z = AZ_GF + 64 * (KWM + 4) * 4;
 static_assert(SMEM_Z + 1024 <= 227 * 1024, "k_surp_tc_z shared memory");
 constexpr int CAP_Z = (AZ_WS - AZ_R) / 4;   // band staging in the R and X tiles (floats)
-static_assert(CAP_Z >= KWM * 31, "one token's band matrix (c <= 16) fits the staging");
+static_assert(CAP_Z >= KWM * 31 + 3, "one token's band matrix (c <= 16) fits the staging");
 
 __global__ void __launch_bounds__(NT, 1) k_surp_tc_z(Geom g, Chunk ch, Work w, int buf, SurpOff so, float* aq) {
   extern __shared__ __align__(1024) uint8_t sm[];
