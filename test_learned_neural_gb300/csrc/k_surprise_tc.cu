@@ -71,6 +71,26 @@ __device__ __forceinline__ void stage4(int n, Load load, Store store) {
   }
 }
 
+// Items [0, n1) of one staging loop and [0, n2) of another, PER per thread
+// (n1 + n2 <= PER NT): every global load of both is issued before the
+// shared-memory stores.
+template <int PER, class L1, class S1, class L2, class S2>
+__device__ __forceinline__ void stage2(int n1, int n2, L1 load1, S1 store1, L2 load2, S2 store2) {
+  float v[PER][8];
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int e = threadIdx.x + q * NT;
+    if (e < n1) load1(e, v[q]);
+    else if (e < n1 + n2) load2(e - n1, v[q]);
+  }
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int e = threadIdx.x + q * NT;
+    if (e < n1) store1(e, v[q]);
+    else if (e < n1 + n2) store2(e - n1, v[q]);
+  }
+}
+
 // G (fp32, M = 64 accumulator lanes, TMEM columns [col, col + kwp)) -> rows
 // of gf (stride kwp + 4)
 __device__ __forceinline__ void tmem_rows64_to_smem(uint32_t taddr_col, int kwp, float* gf) {
@@ -186,22 +206,22 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_z(Geom g, Chunk ch, Work w, i
   const float* Wg = w.Wst[buf][0] + (size_t)u * F * h + jb;
   const float* Sg = w.Sst[buf][0] + (size_t)u * F * h + jb;
   const float* DZg = w.DZ + (size_t)u * g.Kw * h + jb;
-  stage4(
-      64 * (F / 8), [&](int e, float* v) { load8(Rg + (size_t)(e % 64) * F + (e / 64) * 8, e % 64 < Ct, v); },
-      [&](int e, float* v) { tcs::put8(r_hi, r_lo, tc::core_offset(e % 64, (e / 64) * 8, rgsF), v); });
-  stage4(
-      kwp * (F / 8), [&](int e, float* v) { load8(Xg + (size_t)(e % kwp) * F + (e / kwp) * 8, e % kwp < nw, v); },
-      [&](int e, float* v) { tcs::put8(x_hi, x_lo, tc::core_offset(e % kwp, (e / kwp) * 8, rgsF), v); });
-  stage4(
-      F * 16,   // columns 0-63: W1, 64-127: S1
-      [&](int e, float* v) {
+  // two staging rounds with every load of a round in flight at once
+  stage2<(64 * 16 + KWM * 16 + NT - 1) / NT>(
+      64 * (F / 8), kwp * (F / 8),
+      [&](int e, float* v) { load8(Rg + (size_t)(e % 64) * F + (e / 64) * 8, e % 64 < Ct, v); },
+      [&](int e, const float* v) { tcs::put8(r_hi, r_lo, tc::core_offset(e % 64, (e / 64) * 8, rgsF), v); },
+      [&](int e, float* v) { load8(Xg + (size_t)(e % kwp) * F + (e / kwp) * 8, e % kwp < nw, v); },
+      [&](int e, const float* v) { tcs::put8(x_hi, x_lo, tc::core_offset(e % kwp, (e / kwp) * 8, rgsF), v); });
+  stage2<(FZ * 16 + KWM * 8 + NT - 1) / NT>(
+      F * 16, kwp * 8,
+      [&](int e, float* v) {   // columns 0-63: W1, 64-127: S1
         const int c0 = (e / F) * 8;
         load8((c0 < 64 ? Wg : Sg) + (size_t)(e % F) * h + (c0 & 63), true, v);
       },
-      [&](int e, float* v) { tcs::put8(ws_hi, ws_lo, tc::core_offset(e % F, (e / F) * 8, rgsW), v); });
-  stage4(
-      kwp * 8, [&](int e, float* v) { load8(DZg + (size_t)(e % kwp) * h + (e / kwp) * 8, e % kwp < nw, v); },
-      [&](int e, float* v) { tcs::put8(dz_hi, dz_lo, tc::core_offset(e % kwp, (e / kwp) * 8, rgsD), v); });
+      [&](int e, const float* v) { tcs::put8(ws_hi, ws_lo, tc::core_offset(e % F, (e / F) * 8, rgsW), v); },
+      [&](int e, float* v) { load8(DZg + (size_t)(e % kwp) * h + (e / kwp) * 8, e % kwp < nw, v); },
+      [&](int e, const float* v) { tcs::put8(dz_hi, dz_lo, tc::core_offset(e % kwp, (e / kwp) * 8, rgsD), v); });
   tcs::sync_for_mma();
   const uint32_t tb = tbase, tD1 = tb, tG = tb + 128, tD3 = tb + 256;
   bool ok = true;
@@ -300,27 +320,54 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_y(Geom g, Chunk ch, Work w, i
   const uint32_t tb = tbase, tD1 = tb, tG = tb + 64, tD3 = tb + 160;
   bool ok = true;
   uint32_t phase = 0;
-  // [aq W2^ | aq S2^] (N = 64) and G' = aq L2^T (N = kwp), K = hidden in chunks of 64
+  // [aq W2^ | aq S2^] (N = 64) and G' = aq L2^T (N = kwp), K = hidden in
+  // chunks of 64.  A chunk's three tiles are items [0, 512) aq rows, [512,
+  // 1024) W2 / S2 rows, [1024, 1024 + 8 kwp) a_i rows, YPER per thread: all
+  // of a chunk's loads are issued at once, the next chunk's while this
+  // chunk's products run.
+  constexpr int YPER = (2 * 64 * 8 + KWM * 8 + NT - 1) / NT;
+  const int ny = 2 * 64 * 8 + kwp * 8;
+  auto y_load = [&](int e, int k0, float* v) {
+    if (e < 512) {
+      load8(AQg + (size_t)(e % 64) * h + k0 + (e / 64) * 8, e % 64 < Ct, v);
+    } else if (e < 1024) {
+      const int f = e - 512, c0 = (f / 64) * 8;   // columns 0-31: W2, 32-63: S2
+      load8((c0 < 32 ? Wg : Sg) + (size_t)(k0 + f % 64) * d + (c0 & 31), true, v);
+    } else {
+      const int f = e - 1024;
+      load8(Ag + (size_t)(f % kwp) * h + k0 + (f / kwp) * 8, f % kwp < nw, v);
+    }
+  };
+  auto y_store = [&](int e, const float* v) {
+    if (e < 512) {
+      tcs::put8(aq_hi, aq_lo, tc::core_offset(e % 64, (e / 64) * 8, rgs64), v);
+    } else if (e < 1024) {
+      const int f = e - 512;
+      tcs::put8(ws_hi, ws_lo, tc::core_offset(f % 64, (f / 64) * 8, rgs64), v);
+    } else {
+      const int f = e - 1024;
+      tcs::put8(aa_hi, aa_lo, tc::core_offset(f % kwp, (f / kwp) * 8, rgs64), v);
+    }
+  };
+  float yv[YPER][8];
+#pragma unroll
+  for (int q = 0; q < YPER; ++q)
+    if (tid + q * NT < ny) y_load(tid + q * NT, 0, yv[q]);
   for (int k0 = 0; k0 < h; k0 += 64) {
-    stage4(
-        64 * 8, [&](int e, float* v) { load8(AQg + (size_t)(e % 64) * h + k0 + (e / 64) * 8, e % 64 < Ct, v); },
-        [&](int e, float* v) { tcs::put8(aq_hi, aq_lo, tc::core_offset(e % 64, (e / 64) * 8, rgs64), v); });
-    stage4(
-        64 * 8,   // columns 0-31: W2, 32-63: S2
-        [&](int e, float* v) {
-          const int c0 = (e / 64) * 8;
-          load8((c0 < 32 ? Wg : Sg) + (size_t)(k0 + e % 64) * d + (c0 & 31), true, v);
-        },
-        [&](int e, float* v) { tcs::put8(ws_hi, ws_lo, tc::core_offset(e % 64, (e / 64) * 8, rgs64), v); });
-    stage4(
-        kwp * 8, [&](int e, float* v) { load8(Ag + (size_t)(e % kwp) * h + k0 + (e / kwp) * 8, e % kwp < nw, v); },
-        [&](int e, float* v) { tcs::put8(aa_hi, aa_lo, tc::core_offset(e % kwp, (e / kwp) * 8, rgs64), v); });
+#pragma unroll
+    for (int q = 0; q < YPER; ++q)
+      if (tid + q * NT < ny) y_store(tid + q * NT, yv[q]);
     tcs::sync_for_mma();
     if (tid == 0 && ok) {
       tcs::mma3(tD1, tcs::kmajor(aq_hi, aq_lo, rgs64), tcs::mnmajor(ws_hi, ws_lo, rgs64),
                 tc::idesc_f16(64, 64, 1, 0, 1), 64, k0 > 0);
       tcs::mma3(tG, tcs::kmajor(aq_hi, aq_lo, rgs64), tcs::kmajor(aa_hi, aa_lo, rgs64),
                 tc::idesc_f16(64, kwp, 1, 0, 0), 64, k0 > 0);
+    }
+    if (k0 + 64 < h) {
+#pragma unroll
+      for (int q = 0; q < YPER; ++q)
+        if (tid + q * NT < ny) y_load(tid + q * NT, k0 + 64, yv[q]);
     }
     ok = tcs::commit_wait(&bar, phase, ok, kWait);   // the chunk's tiles are free again
   }
@@ -397,20 +444,34 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_state(Geom g, Chunk ch, Work 
   // L: the window rows' memory inputs (x_i for W1, a_i for W2), row width = rows
   const float* Lg = (m == 0) ? w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * g.F : w.Aact + (size_t)u * g.Kw * g.hidden;
   const float* Pg = w.surp + (size_t)u * so.per_unit + so.rp + (size_t)m * 2 * g.Kw * so.maxcols;
-  stage4(
-      kwp * 16,
-      [&](int e, float* v) {
+  // both tiles' loads at once: items [0, 16 kwp) L rows, [16 kwp, 48 kwp)
+  // the [Ms_e R | Mw_e R] rows (16 kwp is a multiple of NT: warp-uniform)
+  constexpr int SPER = (KWM * 48 + NT - 1) / NT;
+  const int nl = kwp * 16, ns = kwp * 48;
+  {
+    float sv[SPER][8];
+#pragma unroll
+    for (int q = 0; q < SPER; ++q) {
+      const int e = tid + q * NT;
+      if (e < nl) {
         const int i = e % kwp, a0 = (e / kwp) * 8;
-        load8(Lg + (size_t)i * rows + r0 + a0, i < nw && r0 + a0 < rows, v);
-      },
-      [&](int e, float* v) { tcs::put8(l_hi, l_lo, tc::core_offset(e % kwp, (e / kwp) * 8, rgsL), v); });
-  stage4(
-      kwp * 32,   // columns 0-127: Ms_e R, 128-255: Mw_e R
-      [&](int e, float* v) {
-        const int i = e % kwp, b0 = (e / kwp) * 8, which = b0 >> 7, b = c0 + (b0 & 127);
-        load8(Pg + ((size_t)which * g.Kw + i) * so.maxcols + b, i < nw && b < cols, v);
-      },
-      [&](int e, float* v) { tcs::put8(p_hi, p_lo, tc::core_offset(e % kwp, (e / kwp) * 8, rgsP), v); });
+        load8(Lg + (size_t)i * rows + r0 + a0, i < nw && r0 + a0 < rows, sv[q]);
+      } else if (e < ns) {
+        const int f = e - nl, i = f % kwp, b0 = (f / kwp) * 8, which = b0 >> 7, b = c0 + (b0 & 127);
+        load8(Pg + ((size_t)which * g.Kw + i) * so.maxcols + b, i < nw && b < cols, sv[q]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < SPER; ++q) {
+      const int e = tid + q * NT;
+      if (e < nl) {
+        tcs::put8(l_hi, l_lo, tc::core_offset(e % kwp, (e / kwp) * 8, rgsL), sv[q]);
+      } else if (e < ns) {
+        const int f = e - nl;
+        tcs::put8(p_hi, p_lo, tc::core_offset(f % kwp, (f / kwp) * 8, rgsP), sv[q]);
+      }
+    }
+  }
   tcs::sync_for_mma();
   const uint32_t tb = tbase;
   bool ok = true;
@@ -418,13 +479,29 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_state(Geom g, Chunk ch, Work 
   if (tid == 0)
     tcs::mma3(tb, tcs::mnmajor(l_hi, l_lo, rgsL), tcs::mnmajor(p_hi, p_lo, rgsP), tc::idesc_f16(128, 256, 1, 1, 1),
               kwp, false);
-  ok = tcs::commit_wait(&bar, phase, ok, kWait);
-  // S' = A_e S^ - L^T (Ms_e R), W' = B_e W^ + D_e S^ - L^T (Mw_e R)
+  // S' = A_e S^ - L^T (Ms_e R), W' = B_e W^ + D_e S^ - L^T (Mw_e R): this
+  // thread's rows of S^ and W^ load while the product runs
   const int re = ch.e - 1 - ch.s;
   const float Ae = w.Ap[(size_t)u * g.C + re], Be = w.Bp[(size_t)u * g.C + re], De = w.Dp[(size_t)u * g.C + re];
   const int r = r0 + 32 * q4 + lane;   // M = 128: TMEM lane = tile row
   const size_t base = (size_t)u * rows * cols;
-  for (int cb = 64 * hw; cb < 128; cb += 16) {
+  float4 s4[4][4], w4[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int c = c0 + 64 * hw + 16 * j;
+    if (r < rows && c < cols) {
+      const size_t o = base + (size_t)r * cols + c;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        s4[j][k] = *reinterpret_cast<const float4*>(w.Sst[buf][m] + o + 4 * k);
+        w4[j][k] = *reinterpret_cast<const float4*>(w.Wst[buf][m] + o + 4 * k);
+      }
+    }
+  }
+  ok = tcs::commit_wait(&bar, phase, ok, kWait);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int cb = 64 * hw + 16 * j;
     float ds[16], dw[16];
     tc::tmem_ld16(tb + lane_base + cb, ds);
     tc::tmem_ld16(tb + lane_base + 128 + cb, dw);
@@ -432,19 +509,18 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_state(Geom g, Chunk ch, Work 
     const int c = c0 + cb;
     if (r < rows && c < cols) {
       const size_t o = base + (size_t)r * cols + c;
-      const float* Sb = w.Sst[buf][m] + o;
-      const float* Wb = w.Wst[buf][m] + o;
       float* So = w.Sst[buf ^ 1][m] + o;
       float* Wo = w.Wst[buf ^ 1][m] + o;
 #pragma unroll
-      for (int k = 0; k < 16; k += 4) {
-        const float4 s4 = *reinterpret_cast<const float4*>(Sb + k);
-        const float4 w4 = *reinterpret_cast<const float4*>(Wb + k);
-        *reinterpret_cast<float4*>(So + k) = make_float4(Ae * s4.x - ds[k], Ae * s4.y - ds[k + 1],
-                                                         Ae * s4.z - ds[k + 2], Ae * s4.w - ds[k + 3]);
-        *reinterpret_cast<float4*>(Wo + k) =
-            make_float4(Be * w4.x + De * s4.x - dw[k], Be * w4.y + De * s4.y - dw[k + 1],
-                        Be * w4.z + De * s4.z - dw[k + 2], Be * w4.w + De * s4.w - dw[k + 3]);
+      for (int k = 0; k < 4; ++k) {
+        const float4 sb = s4[j][k], wb = w4[j][k];
+        const float* dsk = ds + 4 * k;
+        const float* dwk = dw + 4 * k;
+        *reinterpret_cast<float4*>(So + 4 * k) =
+            make_float4(Ae * sb.x - dsk[0], Ae * sb.y - dsk[1], Ae * sb.z - dsk[2], Ae * sb.w - dsk[3]);
+        *reinterpret_cast<float4*>(Wo + 4 * k) =
+            make_float4(Be * wb.x + De * sb.x - dwk[0], Be * wb.y + De * sb.y - dwk[1], Be * wb.z + De * sb.z - dwk[2],
+                        Be * wb.w + De * sb.w - dwk[3]);
       }
     }
   }
