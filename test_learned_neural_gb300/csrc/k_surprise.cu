@@ -330,20 +330,42 @@ __global__ void __launch_bounds__(256) k_surp_readout(Geom g, Chunk ch, Work w, 
   }
 }
 
-// Ms_e R and Mw_e R for window row i of matrix m (which = 0: Ms, 1: Mw)
+// Ms_e R and Mw_e R (rows i of the window) of matrix m
 __global__ void __launch_bounds__(256) k_surp_rprime(Geom g, Chunk ch, Work w) {
-  const int i = blockIdx.x, m = blockIdx.y >> 1, which = blockIdx.y & 1, u = blockIdx.z;
+  // One block per (128-column block, matrix, unit): the block's columns of R
+  // (window rows 0 .. nw - 1) and both band matrices are staged in shared
+  // memory once, so each R row is read from global memory once instead of
+  // once per band row that uses it; thread (which, column) then forms its
+  // column for every window row i, in the same order of terms.
+  extern __shared__ float rp_sm[];   // R block [nw][128], then bands [2][nw][2c - 1]
+  const int cb0 = blockIdx.x * 128, m = blockIdx.y, u = blockIdx.z;
+  const int cols = g.cols[m];
+  if (cb0 >= cols) return;
   const SurpLayout S = surp_layout(g);
-  const int band = 2 * g.c - 1, c = g.c, cols = g.cols[m], mc = max_cols(g);
-  const float* base = w.surp + (size_t)u * S.per_unit;
-  const float* M = base + (which ? S.mwe : S.mse) + ((size_t)m * g.Kw + i) * band;
+  const int band = 2 * g.c - 1, c = g.c, nw = ch.nw, mc = max_cols(g);
+  const int ncol = cols - cb0 < 128 ? cols - cb0 : 128;
   const float* R = rfac(g, w, u, m);
-  float* out = w.surp + (size_t)u * S.per_unit + S.rp + (((size_t)m * 2 + which) * g.Kw + i) * mc;
-  const int j0 = i - c + 1 > 0 ? i - c + 1 : 0, j1 = i + c - 1 < ch.nw - 1 ? i + c - 1 : ch.nw - 1;
-  for (int b = threadIdx.x; b < cols; b += blockDim.x) {
+  const float* base = w.surp + (size_t)u * S.per_unit;
+  float* Rs = rp_sm;
+  float* Ms = rp_sm + nw * 128;
+  for (int e = threadIdx.x; e < nw * 128; e += blockDim.x) {
+    const int j = e / 128, b = e % 128;
+    Rs[e] = b < ncol ? R[(size_t)j * cols + cb0 + b] : 0.f;
+  }
+  for (int e = threadIdx.x; e < 2 * nw * band; e += blockDim.x) {
+    const int wh = e / (nw * band), r = e % (nw * band);
+    Ms[e] = base[(wh ? S.mwe : S.mse) + (size_t)m * g.Kw * band + r];
+  }
+  __syncthreads();
+  const int which = threadIdx.x / 128, b = threadIdx.x % 128;
+  if (which > 1 || b >= ncol) return;
+  const float* M = Ms + which * nw * band;
+  float* out = w.surp + (size_t)u * S.per_unit + S.rp + ((size_t)m * 2 + which) * g.Kw * mc + cb0 + b;
+  for (int i = 0; i < nw; ++i) {
+    const int j0 = i - c + 1 > 0 ? i - c + 1 : 0, j1 = i + c - 1 < nw - 1 ? i + c - 1 : nw - 1;
     float acc = 0.f;
-    for (int j = j0; j <= j1; ++j) acc += M[j - i + c - 1] * R[(size_t)j * cols + b];
-    out[b] = acc;
+    for (int j = j0; j <= j1; ++j) acc += M[i * band + (j - i + c - 1)] * Rs[j * 128 + b];
+    out[(size_t)i * mc] = acc;
   }
 }
 
@@ -380,6 +402,14 @@ __global__ void __launch_bounds__(256) k_surp_state(Geom g, Chunk ch, Work w, in
 
 }  // namespace
 
+static cudaError_t rprime_launch(const Geom& g, const Chunk& ch, const Work& w, cudaStream_t st) {
+  const int sm = (ch.nw * 128 + 2 * ch.nw * (2 * g.c - 1)) * (int)sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(k_surp_rprime, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+  if (e != cudaSuccess) return e;
+  k_surp_rprime<<<dim3((max_cols(g) + 127) / 128, g.nmat, g.units), 256, sm, st>>>(g, ch, w);
+  return cudaGetLastError();
+}
+
 size_t surprise_floats(const Geom& g, size_t units) { return units * surp_layout(g).per_unit; }
 
 SurpOff surprise_offsets(const Geom& g) {
@@ -398,7 +428,8 @@ cudaError_t surprise_chunk(const Geom& g, const Chunk& ch, const Work& w, const 
     // chunk-end state of both matrices in one
     cudaError_t e = surprise_tc_readout(g, ch, w, buf, y, st);
     if (e != cudaSuccess) return e;
-    k_surp_rprime<<<dim3(ch.nw, g.nmat * 2, g.units), 256, 0, st>>>(g, ch, w);
+    e = rprime_launch(g, ch, w, st);
+    if (e != cudaSuccess) return e;
     e = surprise_tc_state(g, ch, w, buf, st);
     if (e != cudaSuccess) return e;
     *nl += 7;
@@ -407,7 +438,8 @@ cudaError_t surprise_chunk(const Geom& g, const Chunk& ch, const Work& w, const 
   const size_t sr = (size_t)TG * (g.F + 2 * g.Kw + (g.depth == 2 ? g.hidden : 0)) * sizeof(float);
   cudaFuncSetAttribute(k_surp_readout, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sr);
   k_surp_readout<<<dim3((Ct + TG - 1) / TG, g.units), 256, sr, st>>>(g, ch, w, buf, y);
-  k_surp_rprime<<<dim3(ch.nw, g.nmat * 2, g.units), 256, 0, st>>>(g, ch, w);
+  cudaError_t e = rprime_launch(g, ch, w, st);
+  if (e != cudaSuccess) return e;
   for (int m = 0; m < g.nmat; ++m)
     k_surp_state<<<dim3((g.cols[m] + 63) / 64, (g.rows[m] + 63) / 64, g.units), 256, 0, st>>>(g, ch, w, m, buf);
   *nl += 5 + g.nmat;
