@@ -98,87 +98,93 @@ __global__ void __launch_bounds__(256) k_surp_gram(Geom g, Chunk ch, Work w) {
   }
 }
 
-// c x c Newton-Schulz core of token r of the chunk, matrix m, unit u
+// c x c Newton-Schulz core of token r of the chunk, matrix m, unit u: one
+// warp per (token, matrix), eight per block; the warp's six n x n work
+// matrices (n <= c <= 32, row stride c + 1) sit in its own slice of
+// shared memory and its steps synchronise with __syncwarp only.
 __global__ void __launch_bounds__(256) k_surp_ns(Geom g, Chunk ch, Work w) {
-  __shared__ float Gl[32][33], Gr[32][33], K[32][33], T1[32][33], T2[32][33], H[32][33];
-  __shared__ float red[8];
-  const int r = blockIdx.x, m = blockIdx.y, u = blockIdx.z, t = ch.s + r;
+  extern __shared__ float ns_sm[];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int r = blockIdx.x * 8 + warp, m = blockIdx.y, u = blockIdx.z, t = ch.s + r;
+  if (r >= ch.e - ch.s) return;   // whole warps leave; no block-wide barrier follows
   const SurpLayout S = surp_layout(g);
-  const int band = 2 * g.c - 1, c = g.c;
+  const int band = 2 * g.c - 1, c = g.c, ld = c + 1, sz = c * ld;
+  float* Gl = ns_sm + (size_t)warp * 6 * sz;
+  float* Gr = Gl + sz;
+  float* K = Gr + sz;
+  float* T1 = K + sz;
+  float* T2 = T1 + sz;
+  float* H = T2 + sz;
   int lo_w, hi_w;
   window_rows(g, ch, t, lo_w, hi_w);
   const int n = hi_w - lo_w + 1;   // rows of this token's window (<= c)
   const float* gb = w.surp + (size_t)u * S.per_unit + S.gram + (size_t)m * 2 * g.Kw * band;
   float part = 0.f;
-  for (int e = threadIdx.x; e < n * n; e += blockDim.x) {
+  for (int e = lane; e < n * n; e += 32) {
     const int a = e / n, b = e % n;
     const int d = b - a + c - 1;
     const float gl = gb[(size_t)(lo_w + a) * band + d];
     const float gr = gb[((size_t)g.Kw + lo_w + a) * band + d];
-    Gl[a][b] = gl;
-    Gr[a][b] = gr;
+    Gl[a * ld + b] = gl;
+    Gr[a * ld + b] = gr;
     part += gl * gr;
   }
   for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = part;
-  __syncthreads();
-  float s2 = 0.f;
-  for (int k = 0; k < (int)(blockDim.x / 32); ++k) s2 += red[k];
-  const float nrm = sqrtf(fmaxf(s2, 0.f));
+  const float nrm = sqrtf(fmaxf(part, 0.f));
   // |g|_F = 0: the surprise is zero and so is its orthogonalisation
   const float k0 = nrm > 0.f ? 1.f / (nrm + kNsEps) : 0.f;
-  for (int e = threadIdx.x; e < n * n; e += blockDim.x) {
+  for (int e = lane; e < n * n; e += 32) {
     const int a = e / n, b = e % n;
-    K[a][b] = a == b ? k0 : 0.f;
+    K[a * ld + b] = a == b ? k0 : 0.f;
   }
-  __syncthreads();
+  __syncwarp();
   for (int it = 0; it < g.ns_iters; ++it) {
     // T1 = Gl K, T2 = K^T T1, H = Gr T2, T1 = H H, T2 = a I + b H + c H^2, K = K T2
-    for (int e = threadIdx.x; e < n * n; e += blockDim.x) {
+    for (int e = lane; e < n * n; e += 32) {
       const int a = e / n, b = e % n;
       float acc = 0.f;
-      for (int k = 0; k < n; ++k) acc += Gl[a][k] * K[k][b];
-      T1[a][b] = acc;
+      for (int k = 0; k < n; ++k) acc += Gl[a * ld + k] * K[k * ld + b];
+      T1[a * ld + b] = acc;
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < n * n; e += blockDim.x) {
+    __syncwarp();
+    for (int e = lane; e < n * n; e += 32) {
       const int a = e / n, b = e % n;
       float acc = 0.f;
-      for (int k = 0; k < n; ++k) acc += K[k][a] * T1[k][b];
-      T2[a][b] = acc;
+      for (int k = 0; k < n; ++k) acc += K[k * ld + a] * T1[k * ld + b];
+      T2[a * ld + b] = acc;
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < n * n; e += blockDim.x) {
+    __syncwarp();
+    for (int e = lane; e < n * n; e += 32) {
       const int a = e / n, b = e % n;
       float acc = 0.f;
-      for (int k = 0; k < n; ++k) acc += Gr[a][k] * T2[k][b];
-      H[a][b] = acc;
+      for (int k = 0; k < n; ++k) acc += Gr[a * ld + k] * T2[k * ld + b];
+      H[a * ld + b] = acc;
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < n * n; e += blockDim.x) {
+    __syncwarp();
+    for (int e = lane; e < n * n; e += 32) {
       const int a = e / n, b = e % n;
       float acc = 0.f;
-      for (int k = 0; k < n; ++k) acc += H[a][k] * H[k][b];
-      T2[a][b] = (a == b ? kNsA : 0.f) + kNsB * H[a][b] + kNsC * acc;
+      for (int k = 0; k < n; ++k) acc += H[a * ld + k] * H[k * ld + b];
+      T2[a * ld + b] = (a == b ? kNsA : 0.f) + kNsB * H[a * ld + b] + kNsC * acc;
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < n * n; e += blockDim.x) {
+    __syncwarp();
+    for (int e = lane; e < n * n; e += 32) {
       const int a = e / n, b = e % n;
       float acc = 0.f;
-      for (int k = 0; k < n; ++k) acc += K[a][k] * T2[k][b];
-      T1[a][b] = acc;
+      for (int k = 0; k < n; ++k) acc += K[a * ld + k] * T2[k * ld + b];
+      T1[a * ld + b] = acc;
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < n * n; e += blockDim.x) {
+    __syncwarp();
+    for (int e = lane; e < n * n; e += 32) {
       const int a = e / n, b = e % n;
-      K[a][b] = T1[a][b];
+      K[a * ld + b] = T1[a * ld + b];
     }
-    __syncthreads();
+    __syncwarp();
   }
   float* kt = w.surp + (size_t)u * S.per_unit + S.kt + ((size_t)m * g.C + r) * c * c;
-  for (int e = threadIdx.x; e < c * c; e += blockDim.x) {
+  for (int e = lane; e < c * c; e += 32) {
     const int a = e / c, b = e % c;
-    kt[e] = (a < n && b < n) ? K[a][b] : 0.f;
+    kt[e] = (a < n && b < n) ? K[a * ld + b] : 0.f;
   }
 }
 
@@ -348,14 +354,22 @@ __global__ void __launch_bounds__(256) k_surp_rprime(Geom g, Chunk ch, Work w) {
   const float* base = w.surp + (size_t)u * S.per_unit;
   float* Rs = rp_sm;
   float* Ms = rp_sm + nw * 128;
+  // asynchronous 4-byte copies, all in flight at once (columns past the
+  // matrix are zero-filled: source size 0)
   for (int e = threadIdx.x; e < nw * 128; e += blockDim.x) {
     const int j = e / 128, b = e % 128;
-    Rs[e] = b < ncol ? R[(size_t)j * cols + cb0 + b] : 0.f;
+    const float* src = R + (size_t)j * cols + cb0 + (b < ncol ? b : 0);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(Rs + e)),
+                 "l"(src), "r"(b < ncol ? 4 : 0)
+                 : "memory");
   }
   for (int e = threadIdx.x; e < 2 * nw * band; e += blockDim.x) {
     const int wh = e / (nw * band), r = e % (nw * band);
-    Ms[e] = base[(wh ? S.mwe : S.mse) + (size_t)m * g.Kw * band + r];
+    const float* src = base + (wh ? S.mwe : S.mse) + (size_t)m * g.Kw * band + r;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(Ms + e)), "l"(src)
+                 : "memory");
   }
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
   __syncthreads();
   const int which = threadIdx.x / 128, b = threadIdx.x % 128;
   if (which > 1 || b >= ncol) return;
@@ -421,7 +435,10 @@ cudaError_t surprise_chunk(const Geom& g, const Chunk& ch, const Work& w, const 
                            const float* alpha, float* y, int buf, cudaStream_t st, int* nl) {
   const int Ct = ch.e - ch.s, band = 2 * g.c - 1;
   k_surp_gram<<<dim3(ch.nw, g.nmat * 2, g.units), 256, 0, st>>>(g, ch, w);
-  k_surp_ns<<<dim3(Ct, g.nmat, g.units), 256, 0, st>>>(g, ch, w);
+  const int nsm = 8 * 6 * g.c * (g.c + 1) * (int)sizeof(float);   // eight warps' work matrices
+  cudaError_t es = cudaFuncSetAttribute(k_surp_ns, cudaFuncAttributeMaxDynamicSharedMemorySize, nsm);
+  if (es != cudaSuccess) return es;
+  k_surp_ns<<<dim3((Ct + 7) / 8, g.nmat, g.units), 256, nsm, st>>>(g, ch, w);
   k_surp_scan<<<dim3((g.Kw * band + 255) / 256, g.nmat, g.units), 256, 0, st>>>(g, ch, w, theta, eta, alpha);
   if (surprise_tc_supported(g)) {
     // tensor cores: read-out in two launches (hidden read-out, output), the
