@@ -158,7 +158,7 @@ size_t surprise_floats(const Geom& g, size_t units);
 // offsets (floats) inside one unit's surprise scratch: the read-out's band of
 // Mw per token [nmat][C][Kw][2c-1] and Ms_e R, Mw_e R [nmat][2][Kw][maxcols]
 struct SurpOff {
-  size_t per_unit, mwb, rp;
+  size_t per_unit, mwb, rp, g2;   // floats: per unit, then offsets inside a unit's part
   int maxcols;
 };
 SurpOff surprise_offsets(const Geom& g);

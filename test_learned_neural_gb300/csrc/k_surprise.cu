@@ -41,6 +41,7 @@ struct SurpLayout {
   size_t mse;    // [nmat][Kw][2c-1]     band of Ms at the chunk end
   size_t mwe;    // [nmat][Kw][2c-1]     band of Mw at the chunk end
   size_t rp;     // [nmat][2][Kw][maxcols]  Ms_e R, Mw_e R
+  size_t g2;     // [2][64][kwp] bf16 hi, then lo: the read-outs' (G Mw) tiles (tensor-core path)
   size_t per_unit;
 };
 
@@ -58,6 +59,7 @@ __host__ __device__ inline SurpLayout surp_layout(const Geom& g) {
   L.mse = o;  o += nm * Kw * band;
   L.mwe = o;  o += nm * Kw * band;
   L.rp = o;   o += nm * 2 * Kw * (size_t)max_cols(g);
+  L.g2 = o;   o += 2 * 64 * ((Kw + 15) / 16 * 16);
   L.per_unit = o;
   return L;
 }
@@ -428,7 +430,13 @@ size_t surprise_floats(const Geom& g, size_t units) { return units * surp_layout
 
 SurpOff surprise_offsets(const Geom& g) {
   const SurpLayout L = surp_layout(g);
-  return SurpOff{L.per_unit, L.mwb, L.rp, max_cols(g)};
+  SurpOff so;
+  so.per_unit = L.per_unit;
+  so.mwb = L.mwb;
+  so.rp = L.rp;
+  so.g2 = L.g2;
+  so.maxcols = max_cols(g);
+  return so;
 }
 
 cudaError_t surprise_chunk(const Geom& g, const Chunk& ch, const Work& w, const float* theta, const float* eta,
@@ -449,7 +457,7 @@ cudaError_t surprise_chunk(const Geom& g, const Chunk& ch, const Work& w, const 
     if (e != cudaSuccess) return e;
     e = surprise_tc_state(g, ch, w, buf, st);
     if (e != cudaSuccess) return e;
-    *nl += 7;
+    *nl += 9;
     return cudaGetLastError();
   }
   const size_t sr = (size_t)TG * (g.F + 2 * g.Kw + (g.depth == 2 ? g.hidden : 0)) * sizeof(float);

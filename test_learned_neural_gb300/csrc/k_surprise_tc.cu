@@ -12,12 +12,14 @@
 // Over the chunk's tokens these are products with M = the chunk (64 rows);
 // every product is split bf16 (hi hi' + hi lo' + lo hi', fp32 accumulation
 // in TMEM), the precision of the fp32 path it replaces to about 2^-16.
-//   k_surp_tc_z:     one CTA per (64 hidden columns, unit): [R W1^ | R S1^],
-//                    G = R L1^T, the band mix G Mw1_t (fp32, SIMT), (G Mw1) R1;
-//                    aq to global
+//   k_surp_tc_g2:    one CTA per (16 tokens, unit), once per read-out: G = R
+//                    L1^T (or G' = aq L2^T over K = hidden), the band mix G
+//                    Mw_t (fp32, SIMT), split into the G2 tile the read-out
+//                    reads (the same for all of a unit's column blocks)
+//   k_surp_tc_z:     one CTA per (64 hidden columns, unit): [R W1^ | R S1^]
+//                    and (G Mw1) R1; aq to global
 //   k_surp_tc_y:     one CTA per (32 output columns, unit): [aq W2^ | aq S2^]
-//                    and G' = aq L2^T over K = hidden in chunks of 64, the band
-//                    mix, (G' Mw2) R2; y
+//                    over K = hidden in chunks of 64 and (G' Mw2) R2; y
 //   k_surp_tc_state: one CTA per (128 x 128 tile of a matrix, unit): L^T [Ms_e R
 //                    | Mw_e R] (N = 256) and the decayed chunk-start state
 #include "atlas_common.cuh"
@@ -131,22 +133,24 @@ __device__ __forceinline__ int stage_async(float* dst, const float* src, int n) 
   return mis;
 }
 
-// G2[t][j] = sum_i G[t][i] Mw_t[i][j] over the band |i - j| < c, split into
-// the K-major A tile [t][j] (rgs); rows t >= Ct and columns j >= nw are zero.
+// G2[t][j] = sum_i G[t][i] Mw_t[i][j] over the band |i - j| < c for rows
+// t in [tb, te), split into the K-major A tile [t][j] (rgs); rows t >= Ct
+// and columns j >= nw are zero.
 // The tokens' band matrices (contiguous in global memory) are staged in
 // groups of tokens through `stage` (cap floats, at least one token's Kw (2c -
 // 1) + 3) by asynchronous copies, so the sums read shared memory.
 __device__ __forceinline__ void band_mix(const Geom& g, const Chunk& ch, const float* gf, int kwp, const float* mw,
-                                         float* stage, int cap, uint8_t* hi, uint8_t* lo, int rgs) {
+                                         float* stage, int cap, uint8_t* hi, uint8_t* lo, int rgs, int tb, int te) {
   const int Ct = ch.e - ch.s, band = 2 * g.c - 1, nq = kwp / 8, per = g.Kw * band;
-  const int MWG = (cap - 3) / per < 64 ? (cap - 3) / per : 64;
-  for (int t0 = 0; t0 < 64; t0 += MWG) {
-    const int nt = Ct - t0 < MWG ? (Ct - t0 > 0 ? Ct - t0 : 0) : MWG;
+  const int MWG = (cap - 3) / per < te - tb ? (cap - 3) / per : te - tb;
+  for (int t0 = tb; t0 < te; t0 += MWG) {
+    const int lim = (Ct < te ? Ct : te) - t0;   // rows of this group that have a band matrix
+    const int nt = lim < MWG ? (lim > 0 ? lim : 0) : MWG;
     const int mis = stage_async(stage, mw + (size_t)t0 * per, nt * per);
     __syncthreads();
     for (int e = threadIdx.x; e < MWG * nq; e += NT) {
       const int tt = e % MWG, t = t0 + tt, j0 = (e / MWG) * 8;
-      if (t >= 64) continue;   // the last group may reach past the tile
+      if (t >= te) continue;   // the last group may reach past the rows
       float v[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
@@ -165,17 +169,140 @@ __device__ __forceinline__ void band_mix(const Geom& g, const Chunk& ch, const f
   }
 }
 
-// ------------------------------------------------------------ hidden read-out
-// shared memory (bytes): R [64][F], X [kwp][F] (K-major), [W1 | S1] block
-// [F][128] (MN-major), DZ block [kwp][64] (MN-major), G2 [64][kwp]
-// (K-major), each hi + lo; G fp32 [64][kwp + 4]
+// ------------------------------------------------------------ band products
+// G2 = (A L^T) Mw_t for the rows t of one 16-token group of the chunk: the
+// hidden read-out's (ro = 0: A = the queries R, L = L1 = x_i, K = F) or the
+// output read-out's (ro = 1: A = aq, L = L2 = a_i, K = hidden in chunks of
+// 64).  It does not depend on the read-out's output columns, so it is formed
+// once per unit here and written split (hi, lo) in the read-out kernels'
+// K-major tile layout, which they copy into shared memory as is.
+// shared memory (bytes): A [64][FZ], L [KWM][FZ] (K-major, hi + lo; the
+// output read-out uses their first 64 columns per K chunk), G fp32 [64][KWM
+// + 4], the G2 tile hi + lo, then the band staging
 constexpr int FZ = 128;   // max F
-constexpr int AZ_R = 0, AZ_X = AZ_R + 2 * 64 * FZ * 2, AZ_WS = AZ_X + 2 * KWM * FZ * 2,
-              AZ_DZ = AZ_WS + 2 * FZ * 128 * 2, AZ_G2 = AZ_DZ + 2 * KWM * 64 * 2, AZ_GF = AZ_G2 + 2 * 64 * KWM * 2,
-              SMEM_Z = AZ_GF + 64 * (KWM + 4) * 4;
+constexpr int AG_A = 0, AG_L = AG_A + 2 * 64 * FZ * 2, AG_GF = AG_L + 2 * KWM * FZ * 2,
+              AG_G2 = AG_GF + 64 * (KWM + 4) * 4, AG_MW = AG_G2 + 2 * 64 * KWM * 2, CAP_G = 16384,
+              SMEM_G = AG_MW + CAP_G * 4;
+static_assert(SMEM_G + 1024 <= 227 * 1024, "k_surp_tc_g2 shared memory");
+static_assert(CAP_G >= KWM * 31 + 3, "one token's band matrix (c <= 16) fits the staging");
+
+// the unit's G2 tile of read-out ro in the scratch (hi, then lo)
+__device__ __forceinline__ uint8_t* g2_tile(const Work& w, const SurpOff& so, int u, int ro, int kwp) {
+  return reinterpret_cast<uint8_t*>(w.surp + (size_t)u * so.per_unit + so.g2 + (size_t)ro * 64 * kwp);
+}
+
+__global__ void __launch_bounds__(NT, 1) k_surp_tc_g2(Geom g, Chunk ch, Work w, SurpOff so, int ro, const float* aq) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tbase;
+  const int tid = threadIdx.x, tb = 16 * blockIdx.x, te = tb + 16, u = blockIdx.y;
+  const int F = g.F, h = g.hidden, Ct = ch.e - ch.s, nw = ch.nw, kwp = kwp_of(g);
+  const int rgsF = (F / 8) * 128, rgs64 = 8 * 128, rgsK = (kwp / 8) * 128;
+  uint8_t* a_hi = sm + AG_A;
+  uint8_t* a_lo = a_hi + 64 * FZ * 2;
+  uint8_t* l_hi = sm + AG_L;
+  uint8_t* l_lo = l_hi + KWM * FZ * 2;
+  uint8_t* g2_hi = sm + AG_G2;
+  uint8_t* g2_lo = g2_hi + 64 * KWM * 2;
+  float* gf = reinterpret_cast<float*>(sm + AG_GF);
+  if ((tid >> 5) == 0) tc::tmem_alloc(&tbase, 128);
+  if (tid == 0) tc::mbar_init(&bar, 1);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tG = tbase;
+  bool ok = true;
+  uint32_t phase = 0;
+  if (ro == 0) {
+    const float* Rg = w.R + ((size_t)u * g.T + ch.s) * F;
+    const float* Xg = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * F;
+    stage2<(64 * 16 + KWM * 16 + NT - 1) / NT>(
+        64 * (F / 8), kwp * (F / 8),
+        [&](int e, float* v) { load8(Rg + (size_t)(e % 64) * F + (e / 64) * 8, e % 64 < Ct, v); },
+        [&](int e, const float* v) { tcs::put8(a_hi, a_lo, tc::core_offset(e % 64, (e / 64) * 8, rgsF), v); },
+        [&](int e, float* v) { load8(Xg + (size_t)(e % kwp) * F + (e / kwp) * 8, e % kwp < nw, v); },
+        [&](int e, const float* v) { tcs::put8(l_hi, l_lo, tc::core_offset(e % kwp, (e / kwp) * 8, rgsF), v); });
+    tcs::sync_for_mma();
+    if (tid == 0)
+      tcs::mma3(tG, tcs::kmajor(a_hi, a_lo, rgsF), tcs::kmajor(l_hi, l_lo, rgsF), tc::idesc_f16(64, kwp, 1, 0, 0), F,
+                false);
+    ok = tcs::commit_wait(&bar, phase, ok, kWait);
+  } else {
+    // G' = aq L2^T over K = hidden in chunks of 64; each chunk's loads in
+    // flight together, the next chunk's during this chunk's product
+    const float* AQg = aq + (size_t)u * g.C * h;
+    const float* Ag = w.Aact + (size_t)u * g.Kw * h;
+    constexpr int GPER = (64 * 8 + KWM * 8 + NT - 1) / NT;
+    const int ng = 64 * 8 + kwp * 8;
+    auto g_load = [&](int e, int k0, float* v) {
+      if (e < 512) load8(AQg + (size_t)(e % 64) * h + k0 + (e / 64) * 8, e % 64 < Ct, v);
+      else load8(Ag + (size_t)((e - 512) % kwp) * h + k0 + ((e - 512) / kwp) * 8, (e - 512) % kwp < nw, v);
+    };
+    auto g_store = [&](int e, const float* v) {
+      if (e < 512) tcs::put8(a_hi, a_lo, tc::core_offset(e % 64, (e / 64) * 8, rgs64), v);
+      else tcs::put8(l_hi, l_lo, tc::core_offset((e - 512) % kwp, ((e - 512) / kwp) * 8, rgs64), v);
+    };
+    float gv[GPER][8];
+#pragma unroll
+    for (int q = 0; q < GPER; ++q)
+      if (tid + q * NT < ng) g_load(tid + q * NT, 0, gv[q]);
+    for (int k0 = 0; k0 < h; k0 += 64) {
+#pragma unroll
+      for (int q = 0; q < GPER; ++q)
+        if (tid + q * NT < ng) g_store(tid + q * NT, gv[q]);
+      tcs::sync_for_mma();
+      if (tid == 0 && ok)
+        tcs::mma3(tG, tcs::kmajor(a_hi, a_lo, rgs64), tcs::kmajor(l_hi, l_lo, rgs64), tc::idesc_f16(64, kwp, 1, 0, 0),
+                  64, k0 > 0);
+      if (k0 + 64 < h) {
+#pragma unroll
+        for (int q = 0; q < GPER; ++q)
+          if (tid + q * NT < ng) g_load(tid + q * NT, k0 + 64, gv[q]);
+      }
+      ok = tcs::commit_wait(&bar, phase, ok, kWait);   // the chunk's tiles are free again
+    }
+  }
+  tmem_rows64_to_smem(tG, kwp, gf);
+  __syncthreads();
+  band_mix(g, ch, gf, kwp, w.surp + (size_t)u * so.per_unit + so.mwb + (size_t)ro * g.C * g.Kw * (2 * g.c - 1),
+           reinterpret_cast<float*>(sm + AG_MW), CAP_G, g2_hi, g2_lo, rgsK, tb, te);
+  // this group's two row groups of the hi and lo tiles to the scratch
+  uint8_t* dst = g2_tile(w, so, u, ro, kwp);
+  const int tile = 64 * kwp * 2, nb = 2 * rgsK / 16;
+  for (int e = tid; e < 2 * nb; e += NT) {
+    const int part = e / nb, off = (tb / 8) * rgsK + (e % nb) * 16;
+    *reinterpret_cast<uint4*>(dst + part * tile + off) =
+        *reinterpret_cast<const uint4*>((part ? g2_lo : g2_hi) + off);
+  }
+  if (!ok && tid == 0) atomicExch(w.status, ATLAS_ERR_TIMEOUT);
+  tc::fence_before_sync();
+  __syncthreads();
+  if ((tid >> 5) == 0) tc::tmem_dealloc(tG, 128);
+}
+
+// the unit's G2 tile of read-out ro from the scratch into shared memory (hi,
+// lo), by 16-byte asynchronous copies; waited for by the caller's
+// cp.async.wait_group
+__device__ __forceinline__ void g2_fetch(const Work& w, const SurpOff& so, int u, int ro, int kwp, uint8_t* hi,
+                                         uint8_t* lo) {
+  const uint8_t* src = g2_tile(w, so, u, ro, kwp);
+  const int tile = 64 * kwp * 2, nb = tile / 16;
+  for (int e = threadIdx.x; e < 2 * nb; e += NT) {
+    const int part = e / nb, off = (e % nb) * 16;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32((part ? lo : hi) + off)),
+                 "l"(src + part * tile + off)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// ------------------------------------------------------------ hidden read-out
+// shared memory (bytes): R [64][F] (K-major), [W1 | S1] block [F][128]
+// (MN-major), DZ block [kwp][64] (MN-major), G2 [64][kwp] (K-major), each
+// hi + lo
+constexpr int AZ_R = 0, AZ_WS = AZ_R + 2 * 64 * FZ * 2, AZ_DZ = AZ_WS + 2 * FZ * 128 * 2,
+              AZ_G2 = AZ_DZ + 2 * KWM * 64 * 2, SMEM_Z = AZ_G2 + 2 * 64 * KWM * 2;
 static_assert(SMEM_Z + 1024 <= 227 * 1024, "k_surp_tc_z shared memory");
-constexpr int CAP_Z = (AZ_WS - AZ_R) / 4;   // band staging in the R and X tiles (floats)
-static_assert(CAP_Z >= KWM * 31 + 3, "one token's band matrix (c <= 16) fits the staging");
 
 __global__ void __launch_bounds__(NT, 1) k_surp_tc_z(Geom g, Chunk ch, Work w, int buf, SurpOff so, float* aq) {
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -188,31 +315,22 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_z(Geom g, Chunk ch, Work w, i
   const int rgsF = (F / 8) * 128, rgsW = 16 * 128, rgsD = 8 * 128, rgsK = (kwp / 8) * 128;
   uint8_t* r_hi = sm + AZ_R;
   uint8_t* r_lo = r_hi + 64 * FZ * 2;
-  uint8_t* x_hi = sm + AZ_X;
-  uint8_t* x_lo = x_hi + KWM * FZ * 2;
   uint8_t* ws_hi = sm + AZ_WS;
   uint8_t* ws_lo = ws_hi + FZ * 128 * 2;
   uint8_t* dz_hi = sm + AZ_DZ;
   uint8_t* dz_lo = dz_hi + KWM * 64 * 2;
   uint8_t* g2_hi = sm + AZ_G2;
   uint8_t* g2_lo = g2_hi + 64 * KWM * 2;
-  float* gf = reinterpret_cast<float*>(sm + AZ_GF);
 
-  if (warp == 0) tc::tmem_alloc(&tbase, 512);
+  if (warp == 0) tc::tmem_alloc(&tbase, 256);
   if (tid == 0) tc::mbar_init(&bar, 1);
-  // operands: query features, window inputs x_i, the state blocks, dz_i
+  // operands: query features, the state blocks, dz_i, and the unit's G2 tile
+  g2_fetch(w, so, u, 0, kwp, g2_hi, g2_lo);
   const float* Rg = w.R + ((size_t)u * g.T + ch.s) * F;
-  const float* Xg = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * F;
   const float* Wg = w.Wst[buf][0] + (size_t)u * F * h + jb;
   const float* Sg = w.Sst[buf][0] + (size_t)u * F * h + jb;
   const float* DZg = w.DZ + (size_t)u * g.Kw * h + jb;
   // two staging rounds with every load of a round in flight at once
-  stage2<(64 * 16 + KWM * 16 + NT - 1) / NT>(
-      64 * (F / 8), kwp * (F / 8),
-      [&](int e, float* v) { load8(Rg + (size_t)(e % 64) * F + (e / 64) * 8, e % 64 < Ct, v); },
-      [&](int e, const float* v) { tcs::put8(r_hi, r_lo, tc::core_offset(e % 64, (e / 64) * 8, rgsF), v); },
-      [&](int e, float* v) { load8(Xg + (size_t)(e % kwp) * F + (e / kwp) * 8, e % kwp < nw, v); },
-      [&](int e, const float* v) { tcs::put8(x_hi, x_lo, tc::core_offset(e % kwp, (e / kwp) * 8, rgsF), v); });
   stage2<(FZ * 16 + KWM * 8 + NT - 1) / NT>(
       F * 16, kwp * 8,
       [&](int e, float* v) {   // columns 0-63: W1, 64-127: S1
@@ -222,27 +340,21 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_z(Geom g, Chunk ch, Work w, i
       [&](int e, const float* v) { tcs::put8(ws_hi, ws_lo, tc::core_offset(e % F, (e / F) * 8, rgsW), v); },
       [&](int e, float* v) { load8(DZg + (size_t)(e % kwp) * h + (e / kwp) * 8, e % kwp < nw, v); },
       [&](int e, const float* v) { tcs::put8(dz_hi, dz_lo, tc::core_offset(e % kwp, (e / kwp) * 8, rgsD), v); });
+  stage4(
+      64 * (F / 8), [&](int e, float* v) { load8(Rg + (size_t)(e % 64) * F + (e / 64) * 8, e % 64 < Ct, v); },
+      [&](int e, float* v) { tcs::put8(r_hi, r_lo, tc::core_offset(e % 64, (e / 64) * 8, rgsF), v); });
+  asm volatile("cp.async.wait_group 0;" ::: "memory");   // the G2 tile
   tcs::sync_for_mma();
-  const uint32_t tb = tbase, tD1 = tb, tG = tb + 128, tD3 = tb + 256;
+  const uint32_t tb = tbase, tD1 = tb, tD3 = tb + 128;
   bool ok = true;
   uint32_t phase = 0;
   if (tid == 0) {
-    // [R W1^ | R S1^] (M = 64, N = 128) and G = R L1^T (N = kwp)
+    // [R W1^ | R S1^] (M = 64, N = 128) and (G Mw1) R1 (N = 64)
     tcs::mma3(tD1, tcs::kmajor(r_hi, r_lo, rgsF), tcs::mnmajor(ws_hi, ws_lo, rgsW), tc::idesc_f16(64, 128, 1, 0, 1),
               F, false);
-    tcs::mma3(tG, tcs::kmajor(r_hi, r_lo, rgsF), tcs::kmajor(x_hi, x_lo, rgsF), tc::idesc_f16(64, kwp, 1, 0, 0), F,
-              false);
-  }
-  ok = tcs::commit_wait(&bar, phase, ok, kWait);
-  tmem_rows64_to_smem(tG, kwp, gf);
-  __syncthreads();
-  // the R and X tiles are free: they stage the band matrices
-  band_mix(g, ch, gf, kwp, w.surp + (size_t)u * so.per_unit + so.mwb, reinterpret_cast<float*>(sm + AZ_R), CAP_Z,
-           g2_hi, g2_lo, rgsK);
-  tcs::sync_for_mma();
-  if (tid == 0 && ok)
     tcs::mma3(tD3, tcs::kmajor(g2_hi, g2_lo, rgsK), tcs::mnmajor(dz_hi, dz_lo, rgsD), tc::idesc_f16(64, 64, 1, 0, 1),
               kwp, false);
+  }
   ok = tcs::commit_wait(&bar, phase, ok, kWait);
   // z = B_t (R W1^) + D_t (R S1^) - (G Mw1) R1, aq = SiLU(z)
   {
@@ -269,17 +381,15 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_z(Geom g, Chunk ch, Work w, i
   if (!ok && tid == 0) atomicExch(w.status, ATLAS_ERR_TIMEOUT);
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tb, 512);
+  if (warp == 0) tc::tmem_dealloc(tb, 256);
 }
 
 // ------------------------------------------------------------ output read-out
 // shared memory (bytes): per K chunk of 64 hidden columns aq [64][64]
-// (K-major), [W2 | S2] rows [64][64] (MN-major), L2 = a_i rows [kwp][64]
-// (K-major); then G2' [64][kwp] (K-major), DY block [kwp][32] (MN-major),
-// each hi + lo; G' fp32 [64][kwp + 4]
-constexpr int AY_AQ = 0, AY_WS = AY_AQ + 2 * 64 * 64 * 2, AY_AA = AY_WS + 2 * 64 * 64 * 2,
-              AY_G2 = AY_AA + 2 * KWM * 64 * 2, AY_DY = AY_G2 + 2 * 64 * KWM * 2, AY_GF = AY_DY + 2 * KWM * 32 * 2,
-              AY_MW = AY_GF + 64 * (KWM + 4) * 4, CAP_Y = 16384, SMEM_Y = AY_MW + CAP_Y * 4;
+// (K-major) and [W2 | S2] rows [64][64] (MN-major); then G2' [64][kwp]
+// (K-major) and the DY block [kwp][32] (MN-major); each hi + lo
+constexpr int AY_AQ = 0, AY_WS = AY_AQ + 2 * 64 * 64 * 2, AY_G2 = AY_WS + 2 * 64 * 64 * 2,
+              AY_DY = AY_G2 + 2 * 64 * KWM * 2, SMEM_Y = AY_DY + 2 * KWM * 32 * 2;
 static_assert(SMEM_Y + 1024 <= 227 * 1024, "k_surp_tc_y shared memory");
 
 __global__ void __launch_bounds__(NT, 1) k_surp_tc_y(Geom g, Chunk ch, Work w, int buf, SurpOff so, const float* aq,
@@ -296,18 +406,15 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_y(Geom g, Chunk ch, Work w, i
   uint8_t* aq_lo = aq_hi + 64 * 64 * 2;
   uint8_t* ws_hi = sm + AY_WS;
   uint8_t* ws_lo = ws_hi + 64 * 64 * 2;
-  uint8_t* aa_hi = sm + AY_AA;
-  uint8_t* aa_lo = aa_hi + KWM * 64 * 2;
   uint8_t* g2_hi = sm + AY_G2;
   uint8_t* g2_lo = g2_hi + 64 * KWM * 2;
   uint8_t* dy_hi = sm + AY_DY;
   uint8_t* dy_lo = dy_hi + KWM * 32 * 2;
-  float* gf = reinterpret_cast<float*>(sm + AY_GF);
 
-  if (warp == 0) tc::tmem_alloc(&tbase, 256);
+  if (warp == 0) tc::tmem_alloc(&tbase, 128);
   if (tid == 0) tc::mbar_init(&bar, 1);
+  g2_fetch(w, so, u, 1, kwp, g2_hi, g2_lo);   // the unit's G2' tile, waited for after the K loop
   const float* AQg = aq + (size_t)u * g.C * h;
-  const float* Ag = w.Aact + (size_t)u * g.Kw * h;
   const float* Wg = w.Wst[buf][1] + (size_t)u * h * d + kb;
   const float* Sg = w.Sst[buf][1] + (size_t)u * h * d + kb;
   const float* DYg = w.DY + (size_t)u * g.Kw * d + kb;
@@ -317,36 +424,29 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_y(Geom g, Chunk ch, Work w, i
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tb = tbase, tD1 = tb, tG = tb + 64, tD3 = tb + 160;
+  const uint32_t tb = tbase, tD1 = tb, tD3 = tb + 64;
   bool ok = true;
   uint32_t phase = 0;
-  // [aq W2^ | aq S2^] (N = 64) and G' = aq L2^T (N = kwp), K = hidden in
-  // chunks of 64.  A chunk's three tiles are items [0, 512) aq rows, [512,
-  // 1024) W2 / S2 rows, [1024, 1024 + 8 kwp) a_i rows, YPER per thread: all
-  // of a chunk's loads are issued at once, the next chunk's while this
-  // chunk's products run.
-  constexpr int YPER = (2 * 64 * 8 + KWM * 8 + NT - 1) / NT;
-  const int ny = 2 * 64 * 8 + kwp * 8;
+  // [aq W2^ | aq S2^] (N = 64), K = hidden in chunks of 64.  A chunk's two
+  // tiles are items [0, 512) aq rows and [512, 1024) W2 / S2 rows, YPER per
+  // thread: all of a chunk's loads are issued at once, the next chunk's
+  // while this chunk's product runs.
+  constexpr int YPER = (2 * 64 * 8 + NT - 1) / NT;
+  const int ny = 2 * 64 * 8;
   auto y_load = [&](int e, int k0, float* v) {
     if (e < 512) {
       load8(AQg + (size_t)(e % 64) * h + k0 + (e / 64) * 8, e % 64 < Ct, v);
-    } else if (e < 1024) {
+    } else {
       const int f = e - 512, c0 = (f / 64) * 8;   // columns 0-31: W2, 32-63: S2
       load8((c0 < 32 ? Wg : Sg) + (size_t)(k0 + f % 64) * d + (c0 & 31), true, v);
-    } else {
-      const int f = e - 1024;
-      load8(Ag + (size_t)(f % kwp) * h + k0 + (f / kwp) * 8, f % kwp < nw, v);
     }
   };
   auto y_store = [&](int e, const float* v) {
     if (e < 512) {
       tcs::put8(aq_hi, aq_lo, tc::core_offset(e % 64, (e / 64) * 8, rgs64), v);
-    } else if (e < 1024) {
+    } else {
       const int f = e - 512;
       tcs::put8(ws_hi, ws_lo, tc::core_offset(f % 64, (f / 64) * 8, rgs64), v);
-    } else {
-      const int f = e - 1024;
-      tcs::put8(aa_hi, aa_lo, tc::core_offset(f % kwp, (f / kwp) * 8, rgs64), v);
     }
   };
   float yv[YPER][8];
@@ -358,12 +458,9 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_y(Geom g, Chunk ch, Work w, i
     for (int q = 0; q < YPER; ++q)
       if (tid + q * NT < ny) y_store(tid + q * NT, yv[q]);
     tcs::sync_for_mma();
-    if (tid == 0 && ok) {
+    if (tid == 0 && ok)
       tcs::mma3(tD1, tcs::kmajor(aq_hi, aq_lo, rgs64), tcs::mnmajor(ws_hi, ws_lo, rgs64),
                 tc::idesc_f16(64, 64, 1, 0, 1), 64, k0 > 0);
-      tcs::mma3(tG, tcs::kmajor(aq_hi, aq_lo, rgs64), tcs::kmajor(aa_hi, aa_lo, rgs64),
-                tc::idesc_f16(64, kwp, 1, 0, 0), 64, k0 > 0);
-    }
     if (k0 + 64 < h) {
 #pragma unroll
       for (int q = 0; q < YPER; ++q)
@@ -371,10 +468,7 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_y(Geom g, Chunk ch, Work w, i
     }
     ok = tcs::commit_wait(&bar, phase, ok, kWait);   // the chunk's tiles are free again
   }
-  tmem_rows64_to_smem(tG, kwp, gf);
-  __syncthreads();
-  band_mix(g, ch, gf, kwp, w.surp + (size_t)u * so.per_unit + so.mwb + (size_t)g.C * g.Kw * (2 * g.c - 1),
-           reinterpret_cast<float*>(sm + AY_MW), CAP_Y, g2_hi, g2_lo, rgsK);
+  asm volatile("cp.async.wait_group 0;" ::: "memory");   // the G2' tile
   tcs::sync_for_mma();
   if (tid == 0 && ok)
     tcs::mma3(tD3, tcs::kmajor(g2_hi, g2_lo, rgsK), tcs::mnmajor(dy_hi, dy_lo, rgs32), tc::idesc_f16(64, 32, 1, 0, 1),
@@ -408,7 +502,7 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_y(Geom g, Chunk ch, Work w, i
   if (!ok && tid == 0) atomicExch(w.status, ATLAS_ERR_TIMEOUT);
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tb, 256);
+  if (warp == 0) tc::tmem_dealloc(tb, 128);
 }
 
 // -------------------------------------------------------------- chunk-end state
@@ -540,16 +634,22 @@ bool surprise_tc_supported(const Geom& g) {
   if (g.rows[0] % 16 || g.rows[1] % 16 || g.cols[0] % 16 || g.cols[1] % 16) return false;
   // 16-byte loads of the Ms_e R, Mw_e R rows
   const SurpOff so = surprise_offsets(g);
-  return so.per_unit % 4 == 0 && so.rp % 4 == 0 && so.maxcols % 4 == 0;
+  return so.per_unit % 4 == 0 && so.rp % 4 == 0 && so.g2 % 4 == 0 && so.maxcols % 4 == 0;
 }
 
 cudaError_t surprise_tc_readout(const Geom& g, const Chunk& ch, const Work& w, int buf, float* y, cudaStream_t st) {
   const SurpOff so = surprise_offsets(g);
-  cudaError_t e = cudaFuncSetAttribute(k_surp_tc_z, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_Z);
+  cudaError_t e = cudaFuncSetAttribute(k_surp_tc_g2, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_G);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_surp_tc_z, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_Z);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k_surp_tc_y, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_Y);
   if (e != cudaSuccess) return e;
+  // per unit, the band products of each read-out (four 16-token groups),
+  // then the read-outs over their column blocks
+  k_surp_tc_g2<<<dim3(4, g.units), NT, SMEM_G, st>>>(g, ch, w, so, 0, w.Zpre);
   k_surp_tc_z<<<dim3(g.hidden / 64, g.units), NT, SMEM_Z, st>>>(g, ch, w, buf, so, w.Zpre);
+  k_surp_tc_g2<<<dim3(4, g.units), NT, SMEM_G, st>>>(g, ch, w, so, 1, w.Zpre);
   k_surp_tc_y<<<dim3(g.d_v / 32, g.units), NT, SMEM_Y, st>>>(g, ch, w, buf, so, w.Zpre, y);
   return cudaGetLastError();
 }
