@@ -297,10 +297,10 @@ __device__ __forceinline__ void g2_fetch(const Work& w, const SurpOff& so, int u
 }
 
 // ------------------------------------------------------------ hidden read-out
-// shared memory (bytes): R [64][F] (K-major), [W1 | S1] block [F][128]
-// (MN-major), DZ block [kwp][64] (MN-major), G2 [64][kwp] (K-major), each
-// hi + lo
-constexpr int AZ_R = 0, AZ_WS = AZ_R + 2 * 64 * FZ * 2, AZ_DZ = AZ_WS + 2 * FZ * 128 * 2,
+// shared memory (bytes): R [64][F] (K-major), the W1 block and then the S1
+// block [F][64] (MN-major, one buffer), DZ block [kwp][64] (MN-major), G2
+// [64][kwp] (K-major), each hi + lo: 104 KB, two CTAs per SM
+constexpr int AZ_R = 0, AZ_WS = AZ_R + 2 * 64 * FZ * 2, AZ_DZ = AZ_WS + 2 * FZ * 64 * 2,
               AZ_G2 = AZ_DZ + 2 * KWM * 64 * 2, SMEM_Z = AZ_G2 + 2 * 64 * KWM * 2;
 static_assert(SMEM_Z + 1024 <= 227 * 1024, "k_surp_tc_z shared memory");
 
@@ -312,11 +312,11 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_z(Geom g, Chunk ch, Work w, i
   const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
   const int jb = blockIdx.x * 64, u = blockIdx.y;
   const int F = g.F, h = g.hidden, Ct = ch.e - ch.s, nw = ch.nw, kwp = kwp_of(g);
-  const int rgsF = (F / 8) * 128, rgsW = 16 * 128, rgsD = 8 * 128, rgsK = (kwp / 8) * 128;
+  const int rgsF = (F / 8) * 128, rgsW = 8 * 128, rgsD = 8 * 128, rgsK = (kwp / 8) * 128;
   uint8_t* r_hi = sm + AZ_R;
   uint8_t* r_lo = r_hi + 64 * FZ * 2;
   uint8_t* ws_hi = sm + AZ_WS;
-  uint8_t* ws_lo = ws_hi + FZ * 128 * 2;
+  uint8_t* ws_lo = ws_hi + FZ * 64 * 2;
   uint8_t* dz_hi = sm + AZ_DZ;
   uint8_t* dz_lo = dz_hi + KWM * 64 * 2;
   uint8_t* g2_hi = sm + AZ_G2;
@@ -330,14 +330,13 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_z(Geom g, Chunk ch, Work w, i
   const float* Wg = w.Wst[buf][0] + (size_t)u * F * h + jb;
   const float* Sg = w.Sst[buf][0] + (size_t)u * F * h + jb;
   const float* DZg = w.DZ + (size_t)u * g.Kw * h + jb;
-  // two staging rounds with every load of a round in flight at once
-  stage2<(FZ * 16 + KWM * 8 + NT - 1) / NT>(
-      F * 16, kwp * 8,
-      [&](int e, float* v) {   // columns 0-63: W1, 64-127: S1
-        const int c0 = (e / F) * 8;
-        load8((c0 < 64 ? Wg : Sg) + (size_t)(e % F) * h + (c0 & 63), true, v);
-      },
-      [&](int e, const float* v) { tcs::put8(ws_hi, ws_lo, tc::core_offset(e % F, (e / F) * 8, rgsW), v); },
+  // staging rounds with every load of a round in flight at once: the W1
+  // block with dz, then R; after the first products the S1 block
+  auto ws_store = [&](int e, const float* v) {
+    tcs::put8(ws_hi, ws_lo, tc::core_offset(e % F, (e / F) * 8, rgsW), v);
+  };
+  stage2<(FZ * 8 + KWM * 8 + NT - 1) / NT>(
+      F * 8, kwp * 8, [&](int e, float* v) { load8(Wg + (size_t)(e % F) * h + (e / F) * 8, true, v); }, ws_store,
       [&](int e, float* v) { load8(DZg + (size_t)(e % kwp) * h + (e / kwp) * 8, e % kwp < nw, v); },
       [&](int e, const float* v) { tcs::put8(dz_hi, dz_lo, tc::core_offset(e % kwp, (e / kwp) * 8, rgsD), v); });
   stage4(
@@ -348,13 +347,31 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_z(Geom g, Chunk ch, Work w, i
   const uint32_t tb = tbase, tD1 = tb, tD3 = tb + 128;
   bool ok = true;
   uint32_t phase = 0;
+  // R W1^ into columns 0-63, (G Mw1) R1 (N = 64); then R S1^ into 64-127
   if (tid == 0) {
-    // [R W1^ | R S1^] (M = 64, N = 128) and (G Mw1) R1 (N = 64)
-    tcs::mma3(tD1, tcs::kmajor(r_hi, r_lo, rgsF), tcs::mnmajor(ws_hi, ws_lo, rgsW), tc::idesc_f16(64, 128, 1, 0, 1),
-              F, false);
+    tcs::mma3(tD1, tcs::kmajor(r_hi, r_lo, rgsF), tcs::mnmajor(ws_hi, ws_lo, rgsW), tc::idesc_f16(64, 64, 1, 0, 1), F,
+              false);
     tcs::mma3(tD3, tcs::kmajor(g2_hi, g2_lo, rgsK), tcs::mnmajor(dz_hi, dz_lo, rgsD), tc::idesc_f16(64, 64, 1, 0, 1),
               kwp, false);
   }
+  {
+    float sv[(FZ * 8 + NT - 1) / NT][8];   // the S1 block's loads fly while the products run
+#pragma unroll
+    for (int q = 0; q < (FZ * 8 + NT - 1) / NT; ++q) {
+      const int e = tid + q * NT;
+      if (e < F * 8) load8(Sg + (size_t)(e % F) * h + (e / F) * 8, true, sv[q]);
+    }
+    ok = tcs::commit_wait(&bar, phase, ok, kWait);   // the W1 block is free
+#pragma unroll
+    for (int q = 0; q < (FZ * 8 + NT - 1) / NT; ++q) {
+      const int e = tid + q * NT;
+      if (e < F * 8) ws_store(e, sv[q]);
+    }
+  }
+  tcs::sync_for_mma();
+  if (tid == 0 && ok)
+    tcs::mma3(tD1 + 64, tcs::kmajor(r_hi, r_lo, rgsF), tcs::mnmajor(ws_hi, ws_lo, rgsW), tc::idesc_f16(64, 64, 1, 0, 1),
+              F, false);
   ok = tcs::commit_wait(&bar, phase, ok, kWait);
   // z = B_t (R W1^) + D_t (R S1^) - (G Mw1) R1, aq = SiLU(z)
   {
