@@ -174,6 +174,32 @@ def test_small_parity_surprise_ns(gpu_lib, name, readout):
             assert v <= 5 * tol, (k, v)
 
 
+SURPRISE_TC_RAGGED = [
+    ("C48_c16", dict(B=1, H=1, T=96, C=48, c=16)),          # 48-token chunks (rows 48-63 of the tiles empty), 63 window rows
+    ("C16_c1", dict(B=1, H=2, T=64, C=16, c=1)),            # short chunks, rank-one surprise
+]
+
+
+@pytest.mark.parametrize("case", SURPRISE_TC_RAGGED, ids=[c[0] for c in SURPRISE_TC_RAGGED])
+@pytest.mark.parametrize("readout", ["post", "pre"])
+def test_surprise_tensor_core_path_ragged_chunks(gpu_lib, case, readout):
+    """The tensor-core surprise read-out and state (per-unit band products
+    in 16-token groups, column-block read-outs) on chunks shorter than the
+    64-row tiles and on the widest window they take (atlas-torch README,
+    "Atlas Extensions": Newton-Schulz of the surprise over the Omega window)."""
+    _, kw = case
+    w = WORKLOADS["atlas_muon_surprise"].scaled(readout=readout, **kw)
+    errs = compare(w)
+    tol = TOL[w.qkv_dtype]
+    print(case[0], readout, {k: f"{v:.2e}" for k, v in errs.items()})
+    assert errs["y"] <= tol
+    for k, v in errs.items():
+        if k.startswith("W"):
+            assert v <= tol, (k, v)
+        if k.startswith("S"):
+            assert v <= 5 * tol, (k, v)
+
+
 @pytest.mark.parametrize("name", ["atlas_poly_c4", "atlas_long", "atlas_muon_surprise"])
 def test_repeated_calls_replay_identically(gpu_lib, name):
     """Identical repeated calls replay a captured CUDA graph of the launch
