@@ -660,8 +660,6 @@ __device__ __forceinline__ void cp_async16(float* dst, const float* src) {
 }
 
 // --------------------------------------------- fused decay scan + read-out
-constexpr int kScanStages = 6;   // U_t tiles in flight per W1-scan CTA
-
 // Newton-Schulz path, depth 2 with W1 (F x h, F <= h) and W2 (h x d, h > d),
 // both stored per token in Ubuf in the X orientation (W1 as is, W2
 // transposed).  W_t = (1 - alpha_t) W_{t-1} + U_t is scanned in registers;
@@ -671,14 +669,14 @@ constexpr int kScanStages = 6;   // U_t tiles in flight per W1-scan CTA
 // thread = (column j = lane, row group g = warp): rows [g * rpg, (g+1) * rpg)
 // in registers; partial dot products meet in shared memory.
 template <int RPG>
-__global__ void __launch_bounds__(256, 1) k_ns_scan_w1(Geom g, Chunk ch, Work w, int buf, size_t slot_stride,
-                                                       const float* alpha, float* aq) {
+__global__ void __launch_bounds__(256) k_ns_scan_w1(Geom g, Chunk ch, Work w, int buf, size_t slot_stride,
+                                                    const float* alpha, float* aq) {
   // W1 decay scan fused with the hidden read-out.  Thread (grp, lane) keeps
-  // rows [grp RPG, grp RPG + RPG) of column jb + lane of W1.  The CTA's U_t
-  // tiles (F rows x 32 columns, 16 KB at F = 128) stream through a ring of
-  // kScanStages shared-memory stages by 16-byte cp.async, so the next
-  // tokens' loads are always in flight; each token's partial dot products go
-  // to shared memory and are summed over the 8 row groups once at the end.
+  // rows [grp RPG, grp RPG + RPG) of column jb + lane of W1.  The U_t of
+  // PD tokens are loaded together; each token's partial dot products go to
+  // shared memory and are summed over the 8 row groups once at the end, so
+  // the token loop has no barrier.
+  constexpr int PD = 4;
   extern __shared__ float scan_sm[];
   const int u = blockIdx.y, jb = blockIdx.x * 32;
   const int lane = threadIdx.x % 32, grp = threadIdx.x / 32;
@@ -686,48 +684,45 @@ __global__ void __launch_bounds__(256, 1) k_ns_scan_w1(Geom g, Chunk ch, Work w,
   const int Ct = ch.e - ch.s;
   const bool pre = g.readout == ATLAS_READOUT_PRE;   // read out before token r's update
   const int rn = ns_first_row(g, ch);                 // slots before it hold no U_t: U_t = 0
-  float* ring = scan_sm;                              // [kScanStages][F][32]
-  float* rq = ring + kScanStages * F * 32;            // [C][F + 1] queries of the chunk
-  float* part = rq + g.C * (F + 1);                   // [C][8][33] per-group partial sums
-  float* bes = part + g.C * 8 * 33;                   // [C] 1 - alpha
-  // U_r's tile into stage r % kScanStages (one commit group per token, empty
-  // past the chunk or before rn, so the group count stays uniform)
-  auto issue = [&](int r) {
-    if (r < Ct && r >= rn) {
-      const float* src = w.Ubuf + ((size_t)u * g.C + r) * slot_stride + jb;
-      float* dst = ring + (r % kScanStages) * F * 32;
-      for (int e = threadIdx.x; e < F * 8; e += 256) cp_async16(dst + (e / 8) * 32 + (e % 8) * 4, src + (size_t)(e / 8) * h + (e % 8) * 4);
-    }
-    cp_async_commit();
-  };
-  // the chunk's queries (group 0), then the first stages of the ring
+  float* rq = scan_sm;                   // [C][F + 1] queries of the chunk
+  float* part = rq + g.C * (F + 1);      // [C][8][33] per-group partial sums
+  float* bes = part + g.C * 8 * 33;      // [C] 1 - alpha
+  // the chunk's queries by cp.async (all in flight at once), then the gates
   for (int e = threadIdx.x; e < Ct * F; e += 256)
     cp_async4(&rq[(e / F) * (F + 1) + e % F], &w.R[((size_t)u * g.T + ch.s + e / F) * F + e % F], true, w.R);
   cp_async_commit();
-  for (int r = 0; r < kScanStages - 1; ++r) issue(r);
   for (int r = threadIdx.x; r < Ct; r += 256) bes[r] = 1.f - alpha[(size_t)u * g.T + ch.s + r];
   float W[RPG];
   const float* Wb = w.Wst[buf][0] + (size_t)u * F * h;
 #pragma unroll
   for (int q = 0; q < RPG; ++q) W[q] = Wb[(size_t)(i0 + q) * h + j];
-  for (int r = 0; r < Ct; ++r) {
-    cp_async_wait<kScanStages - 2>();   // token r's tile (and the queries) landed
-    __syncthreads();                    // ... for every thread; stage (r - 1) is free
-    issue(r + kScanStages - 1);
-    const float* cu = ring + (r % kScanStages) * F * 32 + i0 * 32 + lane;
-    const bool has = r >= rn;
-    const float be = bes[r];
-    const float* rr = rq + r * (F + 1) + i0;
-    float z = 0.f;
-#pragma unroll
-    for (int q = 0; q < RPG; ++q) {
-      if (pre) z += rr[q] * W[q];
-      W[q] = be * W[q] + (has ? cu[q * 32] : 0.f);
-      if (!pre) z += rr[q] * W[q];
-    }
-    part[(r * 8 + grp) * 33 + lane] = z;
-  }
   cp_async_wait<0>();
+  __syncthreads();
+  const float* slot0 = w.Ubuf + (size_t)u * g.C * slot_stride + (size_t)i0 * h + j;
+  for (int r0 = 0; r0 < Ct; r0 += PD) {
+    float cur[PD][RPG];
+#pragma unroll
+    for (int p = 0; p < PD; ++p) {
+      const float* sl = slot0 + (size_t)(r0 + p) * slot_stride;
+#pragma unroll
+      for (int q = 0; q < RPG; ++q) cur[p][q] = r0 + p < Ct && r0 + p >= rn ? sl[(size_t)q * h] : 0.f;
+    }
+#pragma unroll
+    for (int p = 0; p < PD; ++p) {
+      const int r = r0 + p;
+      if (r >= Ct) break;
+      const float be = bes[r];
+      const float* rr = rq + r * (F + 1) + i0;
+      float z = 0.f;
+#pragma unroll
+      for (int q = 0; q < RPG; ++q) {
+        if (pre) z += rr[q] * W[q];
+        W[q] = be * W[q] + cur[p][q];
+        if (!pre) z += rr[q] * W[q];
+      }
+      part[(r * 8 + grp) * 33 + lane] = z;
+    }
+  }
   __syncthreads();
   for (int e = threadIdx.x; e < Ct * 32; e += 256) {
     const int r = e >> 5, l = e & 31;
@@ -849,7 +844,7 @@ cudaError_t ns_fused_scan(const Geom& g, const Chunk& ch, const Work& w, int buf
                           const float* alpha, float* aq, float* y, cudaStream_t st) {
   const int F = g.F, h = g.hidden, d = g.d_v;
   dim3 g1(h / 32, g.units);
-  const size_t sm1 = ((size_t)kScanStages * F * 32 + (size_t)g.C * (F + 1) + (size_t)g.C * 8 * 33 + g.C) * sizeof(float);
+  const size_t sm1 = ((size_t)g.C * (F + 1) + (size_t)g.C * 8 * 33 + g.C) * sizeof(float);
   if (F / 8 == 8) {
     cudaFuncSetAttribute(k_ns_scan_w1<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1);
     k_ns_scan_w1<8><<<g1, 256, sm1, st>>>(g, ch, w, buf, slot_stride, alpha, aq);
