@@ -441,6 +441,11 @@ def run_ours(args):
         d2h = oh["y"].numel() * 4 + sum(x.numel() * 4 for x in oh["W"] + oh["S"])
         mem.forward(th, out=oh, host=True)
         reps = max(3, min(args.steps, 10))
+        # clocks during these steps too: they follow the timed region without
+        # a pause, so a GPU that heats up shows it here first
+        clocks_e2e = ClockSampler(f"{bus:02x}:00" if isinstance(bus, int) else None)
+        clocks_e2e.start()
+        time.sleep(0.3)
         if world > 1:
             dist.barrier()
         t0 = time.perf_counter()
@@ -448,7 +453,7 @@ def run_ours(args):
             mem.forward(th, out=oh, host=True)
         e2e_s = max_over_ranks((time.perf_counter() - t0) / reps, dev)
         e2e = {"value": job_throughput(w.tokens, world, 1, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h)}
+               "d2h_bytes_per_step": int(d2h), "clocks": clocks_e2e.stop()}
 
     if rank != 0:
         if world > 1:
