@@ -675,8 +675,8 @@ __global__ void __launch_bounds__(256) k_ns_scan_w1(Geom g, Chunk ch, Work w, in
   // rows [grp RPG, grp RPG + RPG) of column jb + lane of W1.  The U_t of
   // PD tokens are loaded together; each token's partial dot products go to
   // shared memory and are summed over the 8 row groups once at the end, so
-  // the token loop has no barrier.
-  constexpr int PD = 4;
+  // the token loop has no barrier.  PD RPG = 64 values in flight per thread.
+  constexpr int PD = 64 / RPG;
   extern __shared__ float scan_sm[];
   const int u = blockIdx.y, jb = blockIdx.x * 32;
   const int lane = threadIdx.x % 32, grp = threadIdx.x / 32;
@@ -749,7 +749,8 @@ __global__ void __launch_bounds__(256) k_ns_scan_w2(Geom g, Chunk ch, Work w, in
   // tokens at a time in two buffers (the next window loads during this one),
   // which keeps the CTA at 66 KB of shared memory: more CTAs, and more U_t
   // loads in flight, per SM.
-  constexpr int PD = 4, AW = 16;
+  constexpr int PD = 64 / CPL, AW = 16;   // PD CPL = 64 values in flight per thread
+  static_assert(AW % PD == 0, "whole token groups per window");
   extern __shared__ float aqs[];   // [2][AW][h], then [Ct] 1 - alpha
   const int u = blockIdx.y;
   const int lane = threadIdx.x % 32, k = blockIdx.x * 8 + threadIdx.x / 32;
