@@ -12,10 +12,12 @@
 // Over the chunk's tokens these are products with M = the chunk (64 rows);
 // every product is split bf16 (hi hi' + hi lo' + lo hi', fp32 accumulation
 // in TMEM), the precision of the fp32 path it replaces to about 2^-16.
-//   k_surp_tc_g2:    one CTA per (16 tokens, unit), once per read-out: G = R
-//                    L1^T (or G' = aq L2^T over K = hidden), the band mix G
-//                    Mw_t (fp32, SIMT), split into the G2 tile the read-out
-//                    reads (the same for all of a unit's column blocks)
+//   k_surp_tc_g2:    one CTA per (16 tokens, unit), a unit's four in a
+//                    cluster, once per read-out: G = R L1^T (or G' = aq L2^T,
+//                    each CTA a quarter of K = hidden, the partials summed
+//                    over distributed shared memory), the band mix G Mw_t
+//                    (fp32, SIMT), split into the G2 tile the read-out reads
+//                    (the same for all of a unit's column blocks)
 //   k_surp_tc_z:     one CTA per (64 hidden columns, unit): [R W1^ | R S1^]
 //                    and (G Mw1) R1; aq to global
 //   k_surp_tc_y:     one CTA per (32 output columns, unit): [aq W2^ | aq S2^]
@@ -191,7 +193,22 @@ __device__ __forceinline__ uint8_t* g2_tile(const Work& w, const SurpOff& so, in
   return reinterpret_cast<uint8_t*>(w.surp + (size_t)u * so.per_unit + so.g2 + (size_t)ro * 64 * kwp);
 }
 
-__global__ void __launch_bounds__(NT, 1) k_surp_tc_g2(Geom g, Chunk ch, Work w, SurpOff so, int ro, const float* aq) {
+// A unit's four token-group CTAs form a cluster.  For the output read-out
+// each takes a quarter of the K loop over the hidden columns, and the owner
+// of rows [16 q, 16 q + 16) sums the four partial G' rows over distributed
+// shared memory in rank order (the same sum on every run).
+__device__ __forceinline__ void cluster_sync4() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_peer(const float* p, uint32_t rank) {
+  uint32_t a, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(tc::smem_u32(p)), "r"(rank));
+  asm volatile("ld.shared::cluster.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return __uint_as_float(v);
+}
+
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(NT, 1)
+    k_surp_tc_g2(Geom g, Chunk ch, Work w, SurpOff so, int ro, const float* aq) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ uint64_t bar;
   __shared__ uint32_t tbase;
@@ -213,6 +230,7 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_g2(Geom g, Chunk ch, Work w, 
   const uint32_t tG = tbase;
   bool ok = true;
   uint32_t phase = 0;
+  bool have = true;   // this CTA's TMEM holds a product
   if (ro == 0) {
     const float* Rg = w.R + ((size_t)u * g.T + ch.s) * F;
     const float* Xg = w.X + ((size_t)u * g.L + ch.lo + g.n_prev) * F;
@@ -242,28 +260,48 @@ __global__ void __launch_bounds__(NT, 1) k_surp_tc_g2(Geom g, Chunk ch, Work w, 
       if (e < 512) tcs::put8(a_hi, a_lo, tc::core_offset(e % 64, (e / 64) * 8, rgs64), v);
       else tcs::put8(l_hi, l_lo, tc::core_offset((e - 512) % kwp, ((e - 512) / kwp) * 8, rgs64), v);
     };
+    // this CTA's quarter of the 64-column chunks
+    const int nch = h / 64, kb = (int)blockIdx.x * nch / 4 * 64, ke = ((int)blockIdx.x + 1) * nch / 4 * 64;
     float gv[GPER][8];
 #pragma unroll
     for (int q = 0; q < GPER; ++q)
-      if (tid + q * NT < ng) g_load(tid + q * NT, 0, gv[q]);
-    for (int k0 = 0; k0 < h; k0 += 64) {
+      if (kb < ke && tid + q * NT < ng) g_load(tid + q * NT, kb, gv[q]);
+    for (int k0 = kb; k0 < ke; k0 += 64) {
 #pragma unroll
       for (int q = 0; q < GPER; ++q)
         if (tid + q * NT < ng) g_store(tid + q * NT, gv[q]);
       tcs::sync_for_mma();
       if (tid == 0 && ok)
         tcs::mma3(tG, tcs::kmajor(a_hi, a_lo, rgs64), tcs::kmajor(l_hi, l_lo, rgs64), tc::idesc_f16(64, kwp, 1, 0, 0),
-                  64, k0 > 0);
-      if (k0 + 64 < h) {
+                  64, k0 > kb);
+      if (k0 + 64 < ke) {
 #pragma unroll
         for (int q = 0; q < GPER; ++q)
           if (tid + q * NT < ng) g_load(tid + q * NT, k0 + 64, gv[q]);
       }
       ok = tcs::commit_wait(&bar, phase, ok, kWait);   // the chunk's tiles are free again
     }
+    have = kb < ke;
+    if (!have) {
+      // no chunk here: a zero partial
+      for (int e = tid; e < 64 * (kwp + 4); e += NT) gf[e] = 0.f;
+    }
   }
-  tmem_rows64_to_smem(tG, kwp, gf);
+  if (have) tmem_rows64_to_smem(tG, kwp, gf);
   __syncthreads();
+  if (ro == 1) {
+    // G' rows [tb, te) = the four partials summed in rank order, written
+    // over this CTA's own partial rows (no peer reads those)
+    cluster_sync4();   // every partial is in its CTA's shared memory
+    for (int e = tid; e < 16 * kwp; e += NT) {
+      const int t = tb + e / kwp, i = e % kwp;
+      const float* p = gf + t * (kwp + 4) + i;
+      float acc = ld_peer(p, 0);
+      for (int rk = 1; rk < 4; ++rk) acc += ld_peer(p, (uint32_t)rk);
+      gf[t * (kwp + 4) + i] = acc;
+    }
+    cluster_sync4();   // every peer has read this CTA's rows
+  }
   band_mix(g, ch, gf, kwp, w.surp + (size_t)u * so.per_unit + so.mwb + (size_t)ro * g.C * g.Kw * (2 * g.c - 1),
            reinterpret_cast<float*>(sm + AG_MW), CAP_G, g2_hi, g2_lo, rgsK, tb, te);
   // this group's two row groups of the hi and lo tiles to the scratch
